@@ -79,6 +79,7 @@ def inv_temperature(M, seed):
 def prompt_lengths(shape: StepShape, seed, lo=512):
     if shape.B == 1 or not shape.paged:
         return np.full(shape.B, shape.P, dtype=np.int32)
+    lo = min(lo, max(1, shape.P // 2))
     return _rng(seed, S_PROMPT).integers(lo, shape.P + 1, size=shape.B).astype(np.int32)
 
 
