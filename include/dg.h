@@ -1,0 +1,237 @@
+/*
+ * dg.h -- C ABI of libdg, the GB300 (sm_103a) structured-slot-read denoise step.
+ *
+ * The calls follow the prefill / denoise / commit split of the DiffusionGemma
+ * sampler (24-ai.news, "DiffusionGemma integrated into vLLM", section
+ * "Integration into vLLM infrastructure") and the structured-read extension
+ * that seeds the canvas and reads decision slots after one denoise forward
+ * (tau-home.com, "DiffusionGemma like Jev", section "Refusing JSON token
+ * generation").
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - bf16 tensors are passed as `const uint16_t*` (raw bfloat16 bit patterns).
+ *  - Every tensor pointer is a DEVICE pointer unless its comment says "host".
+ *    Tensors are dense and row-major in the layout given; device pointers of
+ *    bf16 matrices read by TMA must be 16-byte aligned and their row length
+ *    (in bytes) a multiple of 16.
+ *  - Ownership: the caller allocates and frees every buffer, including the
+ *    workspace (size from dg_workspace_bytes).  The library never allocates,
+ *    frees or synchronises; every compute call only enqueues work on `stream`
+ *    (a cudaStream_t, NULL = legacy default stream) and returns.
+ *  - Return value: DG_OK, or a negative DG_ERR_* found by synchronous argument
+ *    validation BEFORE anything is launched (nothing was enqueued), or
+ *    DG_ERR_CUDA if a launch failed.  Conditions found on the device (a wait
+ *    that timed out, an out-of-range page or label id met by a kernel) set
+ *    bits in the library's device status word, read with dg_get_status; the
+ *    kernel skips the offending access instead of faulting.
+ */
+#ifndef DG_H_
+#define DG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------- */
+#define DG_OK 0
+#define DG_ERR_ARG (-1)             /* null pointer, non-positive size, misalignment */
+#define DG_ERR_TOO_MANY_LABELS (-2) /* a slot with more than 26 labels (A..Z)        */
+#define DG_ERR_LABEL (-3)           /* duplicate label id, or id outside [0, V)      */
+#define DG_ERR_SHAPE (-4)           /* unsupported or inconsistent dimensions        */
+#define DG_ERR_CUDA (-5)            /* a CUDA runtime call or launch failed          */
+#define DG_ERR_WORKSPACE (-6)       /* workspace null or smaller than required       */
+
+/* bits of the device status word */
+#define DG_DEV_TIMEOUT 1    /* a bounded wait inside a kernel gave up        */
+#define DG_DEV_BAD_PAGE 2   /* a page-table entry outside the page pool      */
+#define DG_DEV_BAD_LABEL 4  /* a label id or label count out of range        */
+#define DG_DEV_BAD_INDEX 8  /* a slot row / token id outside its tensor      */
+
+#define DG_MAX_LABELS 26 /* sotaaz.com, "The server accepts at most 26 alternatives per question" */
+
+/* workspace kinds for dg_workspace_bytes */
+#define DG_WS_ATTN 1
+#define DG_WS_LMHEAD 2
+#define DG_WS_SLOT_READ 3
+#define DG_WS_SELFCOND 4
+
+/* Problem dimensions.  B requests, C canvas tokens each, P_max the longest
+ * prompt (encoder KV) length, Hq/Hkv query/KV heads (GQA, Hq % Hkv == 0),
+ * d_head in {64, 512}, W the +-W canvas window, d_model, V the vocabulary. */
+typedef struct {
+  int B, C, P_max, Hq, Hkv, d_head, W, d_model, V;
+} dg_dims;
+
+/* ---- a1: decoder-mode attention ----------------------------------------
+ * 24-ai.news, "How does diffusion text generation differ?": decoder mode is
+ * bidirectional attention inside a +-W sliding window over the canvas;
+ * thakicloud.com, "What is DiffusionGemma": decoder mode reads the causal
+ * encoder KV of the prompt.  Row i of request b, query head h, attends to all
+ * prompt_len[b] prompt keys and to canvas keys j with |i - j| <= W, one joint
+ * softmax, scale 1/sqrt(d_head); query head h reads KV head h / (Hq/Hkv).
+ *   q      [B, C, Hq, d]  bf16        kc, vc [B, C, Hkv, d] bf16
+ *   contiguous prompt KV (page_table == NULL): kenc, venc [B, P_max, Hkv, d]
+ *   paged prompt KV: kenc, venc are page pools [n_pages, page_size, Hkv, d],
+ *     page_table [B, pages_per_req] int32 (key j of request b lives at
+ *     pool[page_table[b][j / page_size]][j % page_size]); entries outside
+ *     [0, n_pages) set DG_DEV_BAD_PAGE and are read as masked keys.
+ *   prompt_len [B] int32, each in [0, P_max]
+ *   out [B, C, Hq, d] bf16;  lse [B, Hq, C] fp32 (natural log)
+ *   workspace: dg_workspace_bytes(dims, DG_WS_ATTN, 0) bytes. */
+int dg_attn_decode(const dg_dims* dims, const uint16_t* q, const uint16_t* kc,
+                   const uint16_t* vc, const uint16_t* kenc, const uint16_t* venc,
+                   const int32_t* page_table, int pages_per_req, int n_pages,
+                   int page_size, const int32_t* prompt_len, uint16_t* out,
+                   float* lse, void* workspace, size_t workspace_bytes,
+                   void* stream);
+
+/* ---- a2: lm-head -> log-softmax -> entropy -----------------------------
+ * tau-home.com, "Refusing JSON token generation": one denoise forward gives
+ * the logprobs and entropy that the read uses; 24-ai.news, "Token commit
+ * mechanism": per-token confidence for the commit.  For each of the M rows,
+ * z = (h_i . w_v) * inv_t[i] over the whole vocabulary, and
+ *   lse[i] = log sum_v exp z_v, entropy[i] = lse - sum_v p_v z_v (nats),
+ *   maxz[i] = max_v z_v, argmax[i] = lowest v attaining it.
+ * The [M, V] logits are never written to memory.
+ *   h [M, d_model] bf16;  w [V, d_model] bf16;  inv_t [M] fp32 (> 0)
+ *   lse, entropy, maxz [M] fp32;  argmax [M] int32
+ *   workspace: dg_workspace_bytes(dims, DG_WS_LMHEAD, M) bytes. */
+int dg_lmhead_logsoftmax_entropy(const dg_dims* dims, const uint16_t* h, int M,
+                                 const uint16_t* w, const float* inv_t, float* lse,
+                                 float* entropy, float* maxz, int32_t* argmax,
+                                 void* workspace, size_t workspace_bytes,
+                                 void* stream);
+
+/* ---- a0: noise draws for the slot reads --------------------------------
+ * sotaaz.com, "The server accepts at most 26 alternatives per question": the
+ * answer slot is left as noise and re-read with fresh noise draws.  For slot s
+ * and draw r: token n = Philox4x32-10(key = seed, counter = (slot_req[s],
+ * step, r, s)) word 0, top log2(V) bits (V must be a power of two); the row
+ * rows_out[s*R + r] = bf16(h[slot_row[s]] + e[n]) (fp32 add, round to nearest
+ * even), inv_t_out[s*R + r] = inv_t[slot_row[s]].
+ *   h [M, d_model] bf16 (M = rows of h);  e [V, d_model] bf16;  inv_t [M] fp32
+ *   slot_row, slot_req [S] int32;  rows_out [S*R, d_model] bf16
+ *   inv_t_out [S*R] fp32;  noise_tok_out [S, R] int32 (may be NULL) */
+int dg_slot_noise(const dg_dims* dims, const uint16_t* h, int M, const uint16_t* e,
+                  const float* inv_t, const int32_t* slot_row,
+                  const int32_t* slot_req, int S, int R, uint64_t seed, int step,
+                  uint16_t* rows_out, float* inv_t_out, int32_t* noise_tok_out,
+                  void* stream);
+
+/* ---- a3: slot read with the entropy-gated resample ---------------------
+ * tau-home.com, "Refusing JSON token generation" and sotaaz.com, "The server
+ * accepts at most 26 alternatives per question".  dg_slot_finish takes the
+ * S*R noised draw rows (dg_slot_noise) and their full-vocabulary lse
+ * (dg_lmhead_logsoftmax_entropy over those rows).  Per slot and draw:
+ *   z_k = (row . w[label_k]) * inv_t_row, lp[s][r][k] = z_k - lse_row,
+ *   q^(r) = softmax over the slot's n_labels[s] label logits, H^(r) = entropy.
+ * If samples > 1 and H^(0) > gate: q_avg = mean of q^(0..samples-1),
+ * n_reads = samples, resampled = 1; else q_avg = q^(0), n_reads = 1.
+ * chosen = argmax q_avg (lowest label index on ties), h_slot = entropy of q_avg.
+ *   label_ids [S, 26] int32 (first n_labels[s] used);  n_labels [S] int32
+ *   q_avg [S, 26] fp32 (zero past n_labels);  h_slot [S] fp32;  chosen [S] int32
+ *   lp_draws [S, R, 26] fp32;  resampled [S] uint8;  n_reads [S] int32
+ * R is the number of draw rows per slot; 1 <= samples <= R <= 8. */
+int dg_slot_finish(const dg_dims* dims, const uint16_t* rows, const float* inv_t_rows,
+                   const float* lse_rows, const uint16_t* w, const int32_t* label_ids,
+                   const int32_t* n_labels, int S, int R, int samples, float gate,
+                   float* q_avg, float* h_slot, int32_t* chosen, float* lp_draws,
+                   uint8_t* resampled, int32_t* n_reads, void* stream);
+
+/* Read-only structured read (the `diffusion_read_only` mode of tau-home.com,
+ * "Refusing JSON token generation"): dg_slot_noise, then one lm-head pass over
+ * all S*R draw rows (W streamed once), then dg_slot_finish.  Arguments as in
+ * those calls; R = samples draws are always computed (the gate only selects).
+ *   workspace: dg_workspace_bytes(dims, DG_WS_SLOT_READ, S*samples) bytes. */
+int dg_slot_read(const dg_dims* dims, const uint16_t* h, int M, const uint16_t* w,
+                 const uint16_t* e, const float* inv_t, const int32_t* slot_row,
+                 const int32_t* slot_req, const int32_t* label_ids,
+                 const int32_t* n_labels, int S, uint64_t seed, int step,
+                 int samples, float gate, float* q_avg, float* h_slot,
+                 int32_t* chosen, float* lp_draws, uint8_t* resampled,
+                 int32_t* n_reads, int32_t* noise_tok_out, void* workspace,
+                 size_t workspace_bytes, void* stream);
+
+/* ---- a4: entropy-ordered commit ----------------------------------------
+ * 24-ai.news, "Token commit mechanism": accept the most confident tokens first
+ * until the cumulative entropy exceeds a preset threshold; committed tokens are
+ * fixed and leave later steps' candidate sets.  Per request b, the candidates
+ * are positions with cand != 0 and (if committed_state is given) not yet
+ * committed; they are ordered by entropy ascending (ties: lower position); the
+ * first is always accepted, the k-th while the sum of the first k entropies is
+ * <= gamma[b].
+ *   entropy [B, C] fp32;  argmax [B, C] int32;  cand [B, C] uint8;  gamma [B] fp32
+ *   committed_state [B, C] uint8, in/out, may be NULL: |= the accepted mask
+ *   token_state [B, C] int32, in/out, may be NULL: argmax written where accepted
+ *   commit [B, C] uint8 (1 = accepted now);  tokens [B, C] int32 (argmax where
+ *   accepted now, -1 elsewhere);  n_commit [B] int32.  C <= 1024. */
+int dg_commit(const dg_dims* dims, const float* entropy, const int32_t* argmax,
+              const uint8_t* cand, const float* gamma, uint8_t* committed_state,
+              int32_t* token_state, uint8_t* commit, int32_t* tokens, int32_t* n_commit,
+              void* stream);
+
+/* ---- a5: self-conditioning expected embedding ---------------------------
+ * 24-ai.news, "Token commit mechanism": the previous step's full softmax
+ * becomes a probability-weighted average of embeddings fed back as input.
+ * out[i] = sum_v p_iv e[v] with p_i = softmax(z_i), z as in the lm-head call;
+ * lse must be that call's output for the same rows.
+ *   h [M, d_model] bf16;  w [V, d_model] bf16;  inv_t, lse [M] fp32
+ *   e_t [d_model, V] bf16: the embedding table transposed (vocabulary
+ *       contiguous), made once from e [V, d_model] by dg_transpose_bf16
+ *   out [M, d_model] fp32
+ *   workspace: dg_workspace_bytes(dims, DG_WS_SELFCOND, M) bytes. */
+int dg_selfcond_embed(const dg_dims* dims, const uint16_t* h, int M,
+                      const uint16_t* w, const uint16_t* e_t, const float* inv_t,
+                      const float* lse, float* out, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/* Transpose a bf16 matrix src [rows, cols] into dst [cols, rows]; used once to
+ * lay out the embedding table for dg_selfcond_embed. */
+int dg_transpose_bf16(const uint16_t* src, int rows, int cols, uint16_t* dst,
+                      void* stream);
+
+/* ---- a6: next-step canvas input ----------------------------------------
+ * 24-ai.news, "Token commit mechanism" (self-conditioning is an extra input)
+ * read additively: h_out[i] = bf16(h0[i] + e_sc[i]) for open rows and
+ * bf16(h0[i] + emb[tokens[i]]) where committed[i] != 0.
+ *   h0 [M, d_model] bf16;  e_sc [M, d_model] fp32;  emb [V, d_model] bf16
+ *   tokens [M] int32;  committed [M] uint8;  h_out [M, d_model] bf16 */
+int dg_canvas_update(const dg_dims* dims, const uint16_t* h0, const float* e_sc,
+                     const uint16_t* emb, const int32_t* tokens,
+                     const uint8_t* committed, int M, uint16_t* h_out, void* stream);
+
+/* ---- test hook: raw Philox4x32-10 --------------------------------------
+ * out4[i] = Philox4x32-10(counter = ctr4[i], key = seed); n counters. */
+int dg_philox_fill(uint64_t seed, const uint32_t* ctr4, int n, uint32_t* out4,
+                   void* stream);
+
+/* ---- housekeeping ------------------------------------------------------ */
+/* Synchronous check of a slot table held in HOST memory (the 422 "at most 26
+ * alternatives" rejection of sotaaz.com happens here): n_labels in [1, 26],
+ * label ids distinct and in [0, V), slot_row in [0, M).  No GPU work. */
+int dg_validate_slots(const dg_dims* dims, const int32_t* slot_row_host,
+                      const int32_t* label_ids_host, const int32_t* n_labels_host,
+                      int S, int M);
+/* Bytes of device workspace a call needs (rows = M for DG_WS_LMHEAD and
+ * DG_WS_SELFCOND, S*samples for DG_WS_SLOT_READ, ignored for DG_WS_ATTN);
+ * 0 for an invalid request. */
+size_t dg_workspace_bytes(const dg_dims* dims, int which, int rows);
+/* Copy the device status word into *status_out (host) after the work already
+ * on `stream` finishes; this call synchronises that stream. */
+int dg_get_status(void* stream, int32_t* status_out);
+/* Zero the device status word (enqueued on `stream`). */
+int dg_clear_status(void* stream);
+/* Static description of a DG_ERR_* code. */
+const char* dg_strerror(int code);
+/* Number of SMs the library sizes its persistent grids for (device 0 query,
+ * cached); -1 if no device is visible. */
+int dg_num_sms(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DG_H_ */

@@ -1,0 +1,385 @@
+// abi.cu -- the extern "C" entry points of libdg (declared in include/dg.h):
+// synchronous argument validation, workspace sizing, the device status word,
+// TMA descriptor creation and dispatch to the kernels.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <set>
+
+#include "../../include/dg.h"
+#include "internal.h"
+
+namespace {
+
+__device__ int g_status;  // bits DG_DEV_*, sticky until dg_clear_status
+
+constexpr int kMaxDevices = 64;
+int* g_status_addr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+std::mutex g_mu;
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return (dev >= 0 && dev < kMaxDevices) ? dev : -1;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool dims_lm(const dg_dims* d) {
+  return d && d->d_model >= 8 && d->d_model % 8 == 0 && d->V >= 1;
+}
+
+int launch_result(cudaError_t e) { return e == cudaSuccess ? DG_OK : DG_ERR_CUDA; }
+
+}  // namespace
+
+namespace dgi {
+
+int* status_ptr() {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+    g_status_addr[dev] = static_cast<int*>(p);
+  }
+  return g_status_addr[dev];
+}
+
+int num_sms() {
+  const int dev = current_device();
+  if (dev < 0) return 1;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_sms[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 1;
+    g_sms[dev] = n;
+  }
+  return g_sms[dev];
+}
+
+bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                       uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace dgi
+
+namespace {
+
+size_t slot_read_ws(const dg_dims* d, int rows) {
+  using dgi::align_up;
+  const size_t r = (size_t)rows;
+  return align_up(r * d->d_model * 2, 256) + 5 * align_up(r * 4, 256) +
+         dgi::lmhead_ws_bytes(rows, d->V);
+}
+
+bool attn_dims_ok(const dg_dims* d) {
+  if (!d || d->B < 1 || d->C < 1 || d->Hq < 1 || d->Hkv < 1 || d->P_max < 0 || d->W < 0)
+    return false;
+  if (d->Hq % d->Hkv) return false;
+  const int g = d->Hq / d->Hkv;
+  if (64 % g) return false;
+  return d->d_head == 64 || d->d_head == 512;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dg_strerror(int code) {
+  switch (code) {
+    case DG_OK: return "ok";
+    case DG_ERR_ARG: return "invalid argument (null pointer, size or alignment)";
+    case DG_ERR_TOO_MANY_LABELS: return "at most 26 alternatives per slot";
+    case DG_ERR_LABEL: return "duplicate label id or label id outside the vocabulary";
+    case DG_ERR_SHAPE: return "unsupported or inconsistent dimensions";
+    case DG_ERR_CUDA: return "CUDA launch or runtime error";
+    case DG_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown dg status";
+  }
+}
+
+int dg_num_sms(void) {
+  int n = 0;
+  if (cudaGetDeviceCount(&n) != cudaSuccess || n == 0) return -1;
+  return dgi::num_sms();
+}
+
+size_t dg_workspace_bytes(const dg_dims* d, int which, int rows) {
+  if (!d) return 0;
+  switch (which) {
+    case DG_WS_ATTN:
+      if (!attn_dims_ok(d)) return 0;
+      return dgi::attn_ws_bytes(d->B, d->C, d->P_max, d->Hq, d->Hkv, d->d_head,
+                                d->W > d->C ? d->C : d->W);
+    case DG_WS_LMHEAD:
+      if (!dims_lm(d) || rows < 1) return 0;
+      return dgi::lmhead_ws_bytes(rows, d->V);
+    case DG_WS_SLOT_READ:
+      if (!dims_lm(d) || rows < 1) return 0;
+      return slot_read_ws(d, rows);
+    case DG_WS_SELFCOND:
+      if (!dims_lm(d) || rows < 1) return 0;
+      return dgi::selfcond_ws_bytes(rows, d->V, d->d_model);
+    default:
+      return 0;
+  }
+}
+
+int dg_validate_slots(const dg_dims* d, const int32_t* slot_row, const int32_t* label_ids,
+                      const int32_t* n_labels, int S, int M) {
+  if (!d || S < 0 || M < 0) return DG_ERR_ARG;
+  if (S > 0 && (!slot_row || !label_ids || !n_labels)) return DG_ERR_ARG;
+  for (int s = 0; s < S; ++s) {
+    const int n = n_labels[s];
+    if (n > DG_MAX_LABELS) return DG_ERR_TOO_MANY_LABELS;
+    if (n < 1) return DG_ERR_LABEL;
+    if (slot_row[s] < 0 || slot_row[s] >= M) return DG_ERR_SHAPE;
+    std::set<int32_t> seen;
+    for (int k = 0; k < n; ++k) {
+      const int32_t id = label_ids[s * DG_MAX_LABELS + k];
+      if (id < 0 || id >= d->V) return DG_ERR_LABEL;
+      if (!seen.insert(id).second) return DG_ERR_LABEL;
+    }
+  }
+  return DG_OK;
+}
+
+int dg_get_status(void* stream, int32_t* status_out) {
+  if (!status_out) return DG_ERR_ARG;
+  int* p = dgi::status_ptr();
+  if (!p) return DG_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, p, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return DG_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return DG_ERR_CUDA;
+  *status_out = v;
+  return DG_OK;
+}
+
+int dg_clear_status(void* stream) {
+  int* p = dgi::status_ptr();
+  if (!p) return DG_ERR_CUDA;
+  return launch_result(cudaMemsetAsync(p, 0, sizeof(int), static_cast<cudaStream_t>(stream)));
+}
+
+int dg_philox_fill(uint64_t seed, const uint32_t* ctr4, int n, uint32_t* out4, void* stream) {
+  if (n < 0 || (n > 0 && (!ctr4 || !out4))) return DG_ERR_ARG;
+  if (!aligned(ctr4, 16) || !aligned(out4, 16)) return DG_ERR_ARG;
+  return launch_result(dgi::philox_fill(seed, ctr4, n, out4, static_cast<cudaStream_t>(stream)));
+}
+
+int dg_attn_decode(const dg_dims* d, const uint16_t* q, const uint16_t* kc, const uint16_t* vc,
+                   const uint16_t* kenc, const uint16_t* venc, const int32_t* page_table,
+                   int pages_per_req, int n_pages, int page_size, const int32_t* prompt_len,
+                   uint16_t* out, float* lse, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+  if (!d) return DG_ERR_ARG;
+  if (!attn_dims_ok(d)) return DG_ERR_SHAPE;
+  if (!q || !kc || !vc || !prompt_len || !out || !lse) return DG_ERR_ARG;
+  if (d->P_max > 0 && (!kenc || !venc)) return DG_ERR_ARG;
+  for (const void* p : {(const void*)q, (const void*)kc, (const void*)vc, (const void*)kenc,
+                        (const void*)venc, (const void*)out})
+    if (!aligned(p, 16)) return DG_ERR_ARG;
+  if (page_table) {
+    if (page_size < 1 || n_pages < 1 ||
+        (long long)pages_per_req * page_size < (long long)d->P_max)
+      return DG_ERR_SHAPE;
+  }
+  const size_t need = dg_workspace_bytes(d, DG_WS_ATTN, 0);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return DG_ERR_WORKSPACE;
+  dgi::AttnArgs a{};
+  a.B = d->B;
+  a.C = d->C;
+  a.Pmax = d->P_max;
+  a.Hq = d->Hq;
+  a.Hkv = d->Hkv;
+  a.d = d->d_head;
+  a.W = d->W;
+  a.q = q;
+  a.kc = kc;
+  a.vc = vc;
+  a.kenc = kenc ? kenc : kc;
+  a.venc = venc ? venc : vc;
+  a.page_table = page_table;
+  a.pages_per_req = pages_per_req;
+  a.n_pages = n_pages;
+  a.page_size = page_size;
+  a.prompt_len = prompt_len;
+  a.out = out;
+  a.lse = lse;
+  return launch_result(dgi::attn_decode(a, workspace, static_cast<cudaStream_t>(stream)));
+}
+
+int dg_lmhead_logsoftmax_entropy(const dg_dims* d, const uint16_t* h, int M, const uint16_t* w,
+                                 const float* inv_t, float* lse, float* entropy, float* maxz,
+                                 int32_t* argmax, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  if (!d || M < 1) return DG_ERR_ARG;
+  if (!dims_lm(d)) return DG_ERR_SHAPE;
+  if (!h || !w || !inv_t || !lse || !entropy || !maxz || !argmax) return DG_ERR_ARG;
+  if (!aligned(h, 16) || !aligned(w, 16)) return DG_ERR_ARG;
+  const size_t need = dgi::lmhead_ws_bytes(M, d->V);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return DG_ERR_WORKSPACE;
+  return launch_result(dgi::lmhead_stats(h, M, w, d->V, d->d_model, inv_t,
+                                         dgi::RowStats{lse, entropy, maxz, argmax}, workspace,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+int dg_slot_noise(const dg_dims* d, const uint16_t* h, int M, const uint16_t* e,
+                  const float* inv_t, const int32_t* slot_row, const int32_t* slot_req, int S,
+                  int R, uint64_t seed, int step, uint16_t* rows_out, float* inv_t_out,
+                  int32_t* noise_tok_out, void* stream) {
+  if (!d || S < 0 || R < 1 || R > 8 || M < 1) return DG_ERR_ARG;
+  if (!dims_lm(d) || !pow2(d->V)) return DG_ERR_SHAPE;
+  if (S > 0 && (!h || !e || !inv_t || !slot_row || !slot_req || !rows_out || !inv_t_out))
+    return DG_ERR_ARG;
+  if (!aligned(h, 4) || !aligned(e, 4) || !aligned(rows_out, 4)) return DG_ERR_ARG;
+  return launch_result(dgi::slot_noise(h, M, e, d->V, d->d_model, inv_t, slot_row, slot_req, S,
+                                       R, seed, step, rows_out, inv_t_out, noise_tok_out,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+int dg_slot_finish(const dg_dims* d, const uint16_t* rows, const float* inv_t_rows,
+                   const float* lse_rows, const uint16_t* w, const int32_t* label_ids,
+                   const int32_t* n_labels, int S, int R, int samples, float gate, float* q_avg,
+                   float* h_slot, int32_t* chosen, float* lp_draws, uint8_t* resampled,
+                   int32_t* n_reads, void* stream) {
+  if (!d || S < 0 || R < 1 || R > 8 || samples < 1 || samples > R) return DG_ERR_ARG;
+  if (!dims_lm(d)) return DG_ERR_SHAPE;
+  if (S > 0 && (!rows || !inv_t_rows || !lse_rows || !w || !label_ids || !n_labels || !q_avg ||
+                !h_slot || !chosen || !lp_draws || !resampled || !n_reads))
+    return DG_ERR_ARG;
+  if (!aligned(rows, 4) || !aligned(w, 4)) return DG_ERR_ARG;
+  return launch_result(dgi::slot_finish(rows, inv_t_rows, lse_rows, w, d->V, d->d_model,
+                                        label_ids, n_labels, S, R, samples, gate, q_avg, h_slot,
+                                        chosen, lp_draws, resampled, n_reads,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+int dg_slot_read(const dg_dims* d, const uint16_t* h, int M, const uint16_t* w, const uint16_t* e,
+                 const float* inv_t, const int32_t* slot_row, const int32_t* slot_req,
+                 const int32_t* label_ids, const int32_t* n_labels, int S, uint64_t seed,
+                 int step, int samples, float gate, float* q_avg, float* h_slot, int32_t* chosen,
+                 float* lp_draws, uint8_t* resampled, int32_t* n_reads, int32_t* noise_tok_out,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+  if (!d || S < 0 || samples < 1 || samples > 8 || M < 1) return DG_ERR_ARG;
+  if (!dims_lm(d) || !pow2(d->V)) return DG_ERR_SHAPE;
+  if (S == 0) return DG_OK;
+  if (!h || !w || !e || !inv_t || !slot_row || !slot_req || !label_ids || !n_labels || !q_avg ||
+      !h_slot || !chosen || !lp_draws || !resampled || !n_reads)
+    return DG_ERR_ARG;
+  if (!aligned(h, 16) || !aligned(w, 16) || !aligned(e, 16)) return DG_ERR_ARG;
+  const int R = samples;
+  const int rows = S * R;
+  const size_t need = slot_read_ws(d, rows);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DG_ERR_WORKSPACE;
+  using dgi::align_up;
+  uint8_t* p = static_cast<uint8_t*>(workspace);
+  uint16_t* draw_rows = reinterpret_cast<uint16_t*>(p);
+  p += align_up((size_t)rows * d->d_model * 2, 256);
+  float* inv_rows = reinterpret_cast<float*>(p);
+  p += align_up((size_t)rows * 4, 256);
+  float* lse_rows = reinterpret_cast<float*>(p);
+  p += align_up((size_t)rows * 4, 256);
+  float* ent_rows = reinterpret_cast<float*>(p);
+  p += align_up((size_t)rows * 4, 256);
+  float* maxz_rows = reinterpret_cast<float*>(p);
+  p += align_up((size_t)rows * 4, 256);
+  int32_t* arg_rows = reinterpret_cast<int32_t*>(p);
+  p += align_up((size_t)rows * 4, 256);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t err = dgi::slot_noise(h, M, e, d->V, d->d_model, inv_t, slot_row, slot_req, S, R,
+                                    seed, step, draw_rows, inv_rows, noise_tok_out, st);
+  if (err != cudaSuccess) return DG_ERR_CUDA;
+  err = dgi::lmhead_stats(draw_rows, rows, w, d->V, d->d_model, inv_rows,
+                          dgi::RowStats{lse_rows, ent_rows, maxz_rows, arg_rows}, p, st);
+  if (err != cudaSuccess) return DG_ERR_CUDA;
+  err = dgi::slot_finish(draw_rows, inv_rows, lse_rows, w, d->V, d->d_model, label_ids, n_labels,
+                         S, R, samples, gate, q_avg, h_slot, chosen, lp_draws, resampled, n_reads,
+                         st);
+  return launch_result(err);
+}
+
+int dg_commit(const dg_dims* d, const float* entropy, const int32_t* argmax, const uint8_t* cand,
+              const float* gamma, uint8_t* committed_state, int32_t* token_state,
+              uint8_t* commit, int32_t* tokens, int32_t* n_commit, void* stream) {
+  if (!d || d->B < 1 || d->C < 1) return DG_ERR_ARG;
+  if (d->C > 1024) return DG_ERR_SHAPE;
+  if (!entropy || !argmax || !cand || !gamma || !commit || !tokens || !n_commit)
+    return DG_ERR_ARG;
+  return launch_result(dgi::commit(d->B, d->C, entropy, argmax, cand, gamma, committed_state,
+                                   token_state, commit, tokens, n_commit,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+int dg_selfcond_embed(const dg_dims* d, const uint16_t* h, int M, const uint16_t* w,
+                      const uint16_t* e_t, const float* inv_t, const float* lse, float* out,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  if (!d || M < 1) return DG_ERR_ARG;
+  if (!dims_lm(d) || d->V % 8) return DG_ERR_SHAPE;
+  if (!h || !w || !e_t || !inv_t || !lse || !out) return DG_ERR_ARG;
+  if (!aligned(h, 16) || !aligned(w, 16) || !aligned(e_t, 16) || !aligned(out, 16))
+    return DG_ERR_ARG;
+  const size_t need = dgi::selfcond_ws_bytes(M, d->V, d->d_model);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DG_ERR_WORKSPACE;
+  return launch_result(dgi::selfcond(h, M, w, e_t, d->V, d->d_model, inv_t, lse, out, workspace,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+int dg_transpose_bf16(const uint16_t* src, int rows, int cols, uint16_t* dst, void* stream) {
+  if (!src || !dst || rows < 1 || cols < 1 || rows > 65535 * 32) return DG_ERR_ARG;
+  return launch_result(
+      dgi::transpose_bf16(src, rows, cols, dst, static_cast<cudaStream_t>(stream)));
+}
+
+int dg_canvas_update(const dg_dims* d, const uint16_t* h0, const float* e_sc, const uint16_t* emb,
+                     const int32_t* tokens, const uint8_t* committed, int M, uint16_t* h_out,
+                     void* stream) {
+  if (!d || M < 0 || d->d_model < 2 || d->d_model % 2) return DG_ERR_SHAPE;
+  if (M > 0 && (!h0 || !e_sc || !emb || !tokens || !committed || !h_out)) return DG_ERR_ARG;
+  if (!aligned(h0, 4) || !aligned(e_sc, 8) || !aligned(emb, 4) || !aligned(h_out, 4))
+    return DG_ERR_ARG;
+  return launch_result(dgi::canvas_update(h0, e_sc, emb, d->V, tokens, committed, M, d->d_model,
+                                          h_out, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,577 @@
+// gemm_tc.cu -- tcgen05/TMEM GEMMs of the denoise step, fed by TMA.
+//
+// One persistent kernel template computes D[m, n] = sum_k A[m, k] B[n, k] for
+// K-major bf16 operands (rows of A and B contiguous along k) with fp32
+// accumulators in tensor memory, and consumes D in one of three epilogues:
+//
+//   EPI_STATS  lm-head pass (tau-home.com "Refusing JSON token generation";
+//              24-ai.news "Token commit mechanism"): A = hidden rows, B = W.
+//              Each epilogue thread owns one row and keeps an online
+//              (max, sum 2^(v-max), sum v 2^(v-max), argmax) over the vocabulary
+//              tiles it sees; the [M, V] logits never leave the SM.
+//   EPI_PROBS  first half of self-conditioning (24-ai.news "Token commit
+//              mechanism"): recompute the logits tile and write
+//              p = exp(z - lse) in bf16, the A operand of the second GEMM.
+//   EPI_ACCUM  second half: split-K over the vocabulary of P . E, fp32 tile
+//              partials, summed by a reduction kernel in a fixed order.
+//
+// Warp roles (one CTA per SM): warps [0, 4*MT) are the epilogue (warp w reads
+// TMEM lanes 32*(w%4)..+31 of M-tile w/4), warp 4*MT issues TMA loads, warp
+// 4*MT+1 owns TMEM and issues tcgen05.mma from one thread.  Shared-memory
+// stages hold MT 128x64 A tiles and one BNx64 B tile, 128-byte swizzled.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace {
+
+using namespace dgk;
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int EPI_STATS = 0;
+constexpr int EPI_PROBS = 1;
+constexpr int EPI_ACCUM = 2;
+constexpr int SMEM_STAGE_BUDGET = 196608;  // 192 KB of operand stages
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+struct GemmParams {
+  int M, N, K;
+  int cpg;           // CTAs per m-group (STATS/PROBS)
+  int n_tiles;       // ceil(N / BN)
+  int k_split;       // ACCUM: number of K ranges
+  int kb_per_split;  // ACCUM: k-blocks per range
+  const float* inv_t;
+  const float* lse;
+  float* part;            // STATS: 5 x [cpg][M]; ACCUM: [k_split][M][N]
+  __nv_bfloat16* probs;   // PROBS: [M][ldp]
+  long long ldp;
+  int* status;
+};
+
+template <int MT, int BN>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = MT * A_BYTES + B_BYTES;
+  static constexpr int NSTAGE = (SMEM_STAGE_BUDGET / STAGE_BYTES) > 8 ? 8
+                                                                      : (SMEM_STAGE_BUDGET / STAGE_BYTES);
+  static constexpr int ACC_COLS = MT * BN;
+  static constexpr int ACC_STAGES = (2 * ACC_COLS <= 512) ? 2 : 1;
+  static constexpr int TMEM_NEED = ACC_STAGES * ACC_COLS;
+  static constexpr int TMEM_COLS = TMEM_NEED <= 32    ? 32
+                                   : TMEM_NEED <= 64  ? 64
+                                   : TMEM_NEED <= 128 ? 128
+                                   : TMEM_NEED <= 256 ? 256
+                                                      : 512;
+  static constexpr int EPI_WARPS = 4 * MT;
+  static constexpr int THREADS = (EPI_WARPS + 2) * 32;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM_BYTES = 1024 + NSTAGE * STAGE_BYTES + BAR_BYTES;
+  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+  static_assert(TMEM_NEED <= 512, "accumulators exceed tensor memory");
+  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
+};
+
+template <int MT, int BN, int EPI>
+__global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                   const __grid_constant__ CUtensorMap tmB, GemmParams p) {
+  using CF = Cfg<MT, BN>;
+  constexpr int NSTAGE = CF::NSTAGE;
+  constexpr int PRODUCER_WARP = CF::EPI_WARPS;
+  constexpr int MMA_WARP = CF::EPI_WARPS + 1;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* stages = smem;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + NSTAGE * CF::STAGE_BYTES);
+  uint64_t* empty_bar = full_bar + NSTAGE;
+  uint64_t* tfull_bar = empty_bar + NSTAGE;
+  uint64_t* tempty_bar = tfull_bar + CF::ACC_STAGES;
+  uint64_t* drain_bar = tempty_bar + CF::ACC_STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NSTAGE; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    for (int a = 0; a < CF::ACC_STAGES; ++a) {
+      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tempty_bar[a], CF::EPI_WARPS);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc(tmem_slot, CF::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == PRODUCER_WARP && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // ---- work assignment --------------------------------------------------
+  const int total_kb = (p.K + BK - 1) / BK;
+  int gm, t_begin, t_end, kb_begin, kb_end;
+  if (EPI == EPI_ACCUM) {
+    const int per_group = p.n_tiles * p.k_split;
+    gm = blockIdx.x / per_group;
+    const int rem = blockIdx.x % per_group;
+    t_begin = rem / p.k_split;
+    t_end = t_begin + 1;
+    const int split = rem % p.k_split;
+    kb_begin = split * p.kb_per_split;
+    kb_end = min(total_kb, kb_begin + p.kb_per_split);
+  } else {
+    gm = blockIdx.x / p.cpg;
+    const int gn = blockIdx.x % p.cpg;
+    t_begin = (int)((long long)gn * p.n_tiles / p.cpg);
+    t_end = (int)((long long)(gn + 1) * p.n_tiles / p.cpg);
+    kb_begin = 0;
+    kb_end = total_kb;
+  }
+  const int m_base = gm * MT * BM;
+  const bool has_work = (t_end > t_begin) && (kb_end > kb_begin);
+
+  if (warp == PRODUCER_WARP) {
+    if (lane == 0 && has_work) {
+      const uint64_t pol_b = policy_evict_first();  // W or E^T: streamed once
+      const uint64_t pol_a = policy_evict_last();   // hidden rows or P: re-read per tile
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, last_phase = 0;
+      bool ok = true;
+      for (int t = t_begin; t < t_end && ok; ++t) {
+        for (int kb = kb_begin; kb < kb_end; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full_bar[stage], CF::STAGE_BYTES);
+          uint8_t* s_a = stages + stage * CF::STAGE_BYTES;
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt)
+            tma_load_2d_hint(s_a + mt * CF::A_BYTES, &tmA, &full_bar[stage], kb * BK,
+                             m_base + mt * BM, pol_a);
+          tma_load_2d_hint(s_a + MT * CF::A_BYTES, &tmB, &full_bar[stage], kb * BK, t * BN,
+                           pol_b);
+          issued_mask |= 1u << stage;
+          last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == NSTAGE) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {  // let every copy already issued land before the CTA exits
+        for (int s = 0; s < NSTAGE; ++s)
+          if (issued_mask & (1u << s)) mbar_wait_drain(&full_bar[s], (last_phase >> s) & 1u);
+      }
+    }
+  } else if (warp == MMA_WARP) {
+    if (lane == 0 && has_work) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int t = t_begin; t < t_end && ok; ++t) {
+        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_base = tmem_base + acc * CF::ACC_COLS;
+        for (int kb = kb_begin; kb < kb_end; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(stages + stage * CF::STAGE_BYTES);
+          const uint32_t b_addr = a_addr + MT * CF::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t bdesc = sw128_kmajor_desc(b_addr + kk * 32);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+              const uint64_t adesc = sw128_kmajor_desc(a_addr + mt * CF::A_BYTES + kk * 32);
+              tc_mma_f16(d_base + mt * BN, adesc, bdesc, CF::IDESC,
+                         (kb > kb_begin || kk > 0) ? 1u : 0u);
+            }
+          }
+          tc_commit(&empty_bar[stage]);
+          if (++stage == NSTAGE) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&tfull_bar[acc]);
+        if (++acc == CF::ACC_STAGES) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // every MMA issued by this thread has completed once drain_bar flips
+      tc_commit(drain_bar);
+      mbar_wait_drain(drain_bar, 0);
+    }
+  } else {
+    // ---- epilogue warps ---------------------------------------------------
+    const int mt = warp >> 2;
+    const int quarter = warp & 3;
+    const int row = m_base + mt * BM + quarter * 32 + lane;
+    const bool row_ok = row < p.M;
+    float scale = 0.f, lse2 = 0.f;
+    if (EPI != EPI_ACCUM && row_ok) scale = __ldg(p.inv_t + row) * LOG2E;
+    if (EPI == EPI_PROBS && row_ok) lse2 = __ldg(p.lse + row) * LOG2E;
+    float m_run = -INFINITY, s_run = 0.f, t_run = 0.f, best = -INFINITY;
+    int best_idx = 0x7fffffff;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = t_begin; t < t_end && has_work; ++t) {
+      if (!mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, p.status)) break;
+      tc_fence_after();
+      const uint32_t taddr =
+          tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * CF::ACC_COLS + mt * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld_32x32b_x32(taddr + c * 32, r);
+        tmem_ld_wait();
+        const int n0 = t * BN + c * 32;
+        if (!row_ok) continue;
+        if (EPI == EPI_STATS) {
+          if (n0 + 32 <= p.N) {
+            float cm = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float a = __uint_as_float(r[j]);
+              if (a > best) {
+                best = a;
+                best_idx = n0 + j;
+              }
+              cm = fmaxf(cm, a * scale);
+            }
+            if (cm > m_run) {
+              const float f = ex2(m_run - cm);
+              s_run *= f;
+              t_run *= f;
+              m_run = cm;
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float v = __uint_as_float(r[j]) * scale;
+              const float e = ex2(v - m_run);
+              s_run += e;
+              t_run = fmaf(e, v, t_run);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (n0 + j >= p.N) continue;
+              const float a = __uint_as_float(r[j]);
+              if (a > best) {
+                best = a;
+                best_idx = n0 + j;
+              }
+              const float v = a * scale;
+              if (v > m_run) {
+                const float f = ex2(m_run - v);
+                s_run *= f;
+                t_run *= f;
+                m_run = v;
+              }
+              const float e = ex2(v - m_run);
+              s_run += e;
+              t_run = fmaf(e, v, t_run);
+            }
+          }
+        } else if (EPI == EPI_PROBS) {
+          __nv_bfloat16* dst = p.probs + (long long)row * p.ldp + n0;
+          if (n0 + 32 <= p.N) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+              uint4 pk;
+              __nv_bfloat162 b0 = __floats2bfloat162_rn(
+                  ex2(fmaf(__uint_as_float(r[j + 0]), scale, -lse2)),
+                  ex2(fmaf(__uint_as_float(r[j + 1]), scale, -lse2)));
+              __nv_bfloat162 b1 = __floats2bfloat162_rn(
+                  ex2(fmaf(__uint_as_float(r[j + 2]), scale, -lse2)),
+                  ex2(fmaf(__uint_as_float(r[j + 3]), scale, -lse2)));
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(
+                  ex2(fmaf(__uint_as_float(r[j + 4]), scale, -lse2)),
+                  ex2(fmaf(__uint_as_float(r[j + 5]), scale, -lse2)));
+              __nv_bfloat162 b3 = __floats2bfloat162_rn(
+                  ex2(fmaf(__uint_as_float(r[j + 6]), scale, -lse2)),
+                  ex2(fmaf(__uint_as_float(r[j + 7]), scale, -lse2)));
+              pk.x = *reinterpret_cast<uint32_t*>(&b0);
+              pk.y = *reinterpret_cast<uint32_t*>(&b1);
+              pk.z = *reinterpret_cast<uint32_t*>(&b2);
+              pk.w = *reinterpret_cast<uint32_t*>(&b3);
+              *reinterpret_cast<uint4*>(dst + j) = pk;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (n0 + j < p.N)
+                dst[j] = __float2bfloat16_rn(ex2(fmaf(__uint_as_float(r[j]), scale, -lse2)));
+          }
+        } else {  // EPI_ACCUM
+          const int split = (blockIdx.x % (p.n_tiles * p.k_split)) % p.k_split;
+          float* dst = p.part + ((long long)split * p.M + row) * p.N + n0;
+          if (n0 + 32 <= p.N) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              *reinterpret_cast<float4*>(dst + j) =
+                  make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                              __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (n0 + j < p.N) dst[j] = __uint_as_float(r[j]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+      if (++acc == CF::ACC_STAGES) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (EPI == EPI_STATS && row_ok) {
+      const int gn = blockIdx.x % p.cpg;
+      const long long o = (long long)gn * p.M + row;
+      const long long plane = (long long)p.cpg * p.M;
+      p.part[o] = m_run;
+      p.part[o + plane] = s_run;
+      p.part[o + 2 * plane] = t_run;
+      p.part[o + 3 * plane] = best;
+      reinterpret_cast<int*>(p.part)[o + 4 * plane] = best_idx;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == MMA_WARP) tmem_dealloc(tmem_base, CF::TMEM_COLS);
+}
+
+// Merge the per-CTA online statistics of every row in a fixed CTA order.
+__global__ void stats_finalize_kernel(const float* part, int cpg, int M, const float* inv_t,
+                                      float* lse, float* entropy, float* maxz, int32_t* argmax) {
+  const int row = blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= M) return;
+  const long long plane = (long long)cpg * M;
+  float m = -INFINITY;
+  for (int g = 0; g < cpg; ++g) m = fmaxf(m, part[(long long)g * M + row]);
+  float s = 0.f, t = 0.f, best = -INFINITY;
+  int idx = 0x7fffffff;
+  for (int g = 0; g < cpg; ++g) {
+    const long long o = (long long)g * M + row;
+    const float mg = part[o];
+    if (mg != -INFINITY) {
+      const float f = exp2f(mg - m);
+      s += part[o + plane] * f;
+      t += part[o + 2 * plane] * f;
+    }
+    const float bg = part[o + 3 * plane];
+    const int ig = reinterpret_cast<const int*>(part)[o + 4 * plane];
+    if (bg > best || (bg == best && ig < idx)) {
+      best = bg;
+      idx = ig;
+    }
+  }
+  const float l = (m + log2f(s)) * LN2;
+  lse[row] = l;
+  entropy[row] = l - (t / s) * LN2;
+  maxz[row] = best * inv_t[row];
+  argmax[row] = idx;
+}
+
+// out[m][n] = sum over splits of part[s][m][n], splits added in order.
+__global__ void split_reduce_kernel(const float4* part, int k_split, long long n4, float4* out) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
+       i += (long long)gridDim.x * blockDim.x) {
+    float4 a = part[i];
+    for (int s = 1; s < k_split; ++s) {
+      const float4 b = part[(long long)s * n4 + i];
+      a.x += b.x;
+      a.y += b.y;
+      a.z += b.z;
+      a.w += b.w;
+    }
+    out[i] = a;
+  }
+}
+
+template <int MT, int BN, int EPI>
+cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
+                        int grid, cudaStream_t st) {
+  using CF = Cfg<MT, BN>;
+  static bool attr_done = false;  // per-process; the attribute is per function
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<MT, BN, EPI>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         CF::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  gemm_tc_kernel<MT, BN, EPI><<<grid, CF::THREADS, CF::SMEM_BYTES, st>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+constexpr int STATS_BN = 256;
+
+int stats_mt(int M) { return M <= BM ? 1 : 2; }
+
+int stats_cpg(int M, int V) {
+  const int mt = stats_mt(M);
+  const int groups = (M + mt * BM - 1) / (mt * BM);
+  const int n_tiles = (V + STATS_BN - 1) / STATS_BN;
+  int cpg = std::max(1, dgi::num_sms() / groups);
+  return std::min(cpg, n_tiles);
+}
+
+// Row statistics over the vocabulary: partials + finalize.
+cudaError_t run_stats(const uint16_t* h, int M, const uint16_t* w, int V, int D,
+                      const float* inv_t, dgi::RowStats out, float* part, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  if (!dgi::make_tmap_bf16_2d(&ta, h, D, M, (uint64_t)D * 2, BK, BM)) return cudaErrorInvalidValue;
+  if (!dgi::make_tmap_bf16_2d(&tb, w, D, V, (uint64_t)D * 2, BK, STATS_BN)) return cudaErrorInvalidValue;
+  const int mt = stats_mt(M);
+  const int groups = (M + mt * BM - 1) / (mt * BM);
+  GemmParams p{};
+  p.M = M;
+  p.N = V;
+  p.K = D;
+  p.cpg = stats_cpg(M, V);
+  p.n_tiles = (V + STATS_BN - 1) / STATS_BN;
+  p.inv_t = inv_t;
+  p.part = part;
+  p.status = dgi::status_ptr();
+  cudaError_t e = (mt == 1) ? launch_gemm<1, STATS_BN, EPI_STATS>(ta, tb, p, groups * p.cpg, st)
+                            : launch_gemm<2, STATS_BN, EPI_STATS>(ta, tb, p, groups * p.cpg, st);
+  if (e != cudaSuccess) return e;
+  stats_finalize_kernel<<<(M + 127) / 128, 128, 0, st>>>(part, p.cpg, M, inv_t, out.lse,
+                                                         out.entropy, out.maxz, out.argmax);
+  return cudaGetLastError();
+}
+
+constexpr int ACC_BN = 256;
+
+// Split of the vocabulary (the K of P . E) over CTAs: every split non-empty.
+void accum_split(int M, int V, int D, int* k_split, int* kb_per_split) {
+  const int mt = stats_mt(M);
+  const int groups = (M + mt * BM - 1) / (mt * BM);
+  const int n_tiles = (D + ACC_BN - 1) / ACC_BN;
+  const int total_kb = (V + BK - 1) / BK;
+  int ks = std::max(1, dgi::num_sms() / (groups * n_tiles));
+  ks = std::min(ks, total_kb);
+  const int kbps = (total_kb + ks - 1) / ks;
+  *kb_per_split = kbps;
+  *k_split = (total_kb + kbps - 1) / kbps;
+}
+
+}  // namespace
+
+namespace dgi {
+
+size_t lmhead_ws_bytes(int M, int V) {
+  return align_up((size_t)5 * stats_cpg(M, V) * M * sizeof(float), 256);
+}
+
+cudaError_t lmhead_stats(const uint16_t* h, int M, const uint16_t* w, int V, int D,
+                         const float* inv_t, RowStats out, void* ws, cudaStream_t st) {
+  return run_stats(h, M, w, V, D, inv_t, out, static_cast<float*>(ws), st);
+}
+
+size_t selfcond_ws_bytes(int M, int V, int D) {
+  const size_t probs = align_up((size_t)M * align_up(V, 64) * 2, 256);
+  int ks, kbps;
+  accum_split(M, V, D, &ks, &kbps);
+  const size_t part = align_up((size_t)ks * M * D * sizeof(float), 256);
+  return probs + part;
+}
+
+cudaError_t selfcond(const uint16_t* h, int M, const uint16_t* w, const uint16_t* e_t, int V,
+                     int D, const float* inv_t, const float* lse, float* out, void* ws,
+                     cudaStream_t st) {
+  const size_t ldp = align_up(V, 64);
+  __nv_bfloat16* probs = static_cast<__nv_bfloat16*>(ws);
+  float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
+                                         align_up((size_t)M * ldp * 2, 256));
+  const int mt = stats_mt(M);
+  const int groups = (M + mt * BM - 1) / (mt * BM);
+  // 1) probabilities p = exp(z - lse) in bf16
+  {
+    CUtensorMap ta, tb;
+    if (!make_tmap_bf16_2d(&ta, h, D, M, (uint64_t)D * 2, BK, BM)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16_2d(&tb, w, D, V, (uint64_t)D * 2, BK, STATS_BN)) return cudaErrorInvalidValue;
+    GemmParams p{};
+    p.M = M;
+    p.N = V;
+    p.K = D;
+    p.cpg = stats_cpg(M, V);
+    p.n_tiles = (V + STATS_BN - 1) / STATS_BN;
+    p.inv_t = inv_t;
+    p.lse = lse;
+    p.probs = probs;
+    p.ldp = (long long)ldp;
+    p.status = status_ptr();
+    cudaError_t e = (mt == 1)
+                        ? launch_gemm<1, STATS_BN, EPI_PROBS>(ta, tb, p, groups * p.cpg, st)
+                        : launch_gemm<2, STATS_BN, EPI_PROBS>(ta, tb, p, groups * p.cpg, st);
+    if (e != cudaSuccess) return e;
+  }
+  // 2) split-K partials of P . E over the vocabulary, 3) ordered reduction
+  {
+    CUtensorMap ta, tb;
+    if (!make_tmap_bf16_2d(&ta, probs, V, M, (uint64_t)ldp * 2, BK, BM)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16_2d(&tb, e_t, V, D, (uint64_t)V * 2, BK, ACC_BN)) return cudaErrorInvalidValue;
+    GemmParams p{};
+    p.M = M;
+    p.N = D;
+    p.K = V;
+    p.n_tiles = (D + ACC_BN - 1) / ACC_BN;
+    accum_split(M, V, D, &p.k_split, &p.kb_per_split);
+    p.part = part;
+    p.status = status_ptr();
+    const int grid = groups * p.n_tiles * p.k_split;
+    cudaError_t e = (mt == 1) ? launch_gemm<1, ACC_BN, EPI_ACCUM>(ta, tb, p, grid, st)
+                              : launch_gemm<2, ACC_BN, EPI_ACCUM>(ta, tb, p, grid, st);
+    if (e != cudaSuccess) return e;
+    const long long n4 = (long long)M * D / 4;
+    const int blocks = (int)std::min<long long>((n4 + 255) / 256, 4LL * num_sms());
+    split_reduce_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(part), p.k_split,
+                                                n4, reinterpret_cast<float4*>(out));
+    return cudaGetLastError();
+  }
+}
+
+}  // namespace dgi

@@ -1,0 +1,71 @@
+// internal.h -- declarations shared between the C-ABI layer and the kernel files.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace dgi {
+
+// Device address of the library's status word (set-up once per device).
+int* status_ptr();
+int num_sms();
+// Build a 2-D TMA map over a row-major bf16 matrix [outer, inner] whose rows are
+// row_bytes apart, with a (box_inner x box_outer) box and 128-byte swizzle.
+// Returns false on failure.
+bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                       uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+
+constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---- tcgen05 GEMM family (gemm_tc.cu) ------------------------------------
+struct RowStats {
+  float* lse;
+  float* entropy;
+  float* maxz;
+  int32_t* argmax;
+};
+size_t lmhead_ws_bytes(int M, int V);
+cudaError_t lmhead_stats(const uint16_t* h, int M, const uint16_t* w, int V, int D,
+                         const float* inv_t, RowStats out, void* ws, cudaStream_t st);
+size_t selfcond_ws_bytes(int M, int V, int D);
+cudaError_t selfcond(const uint16_t* h, int M, const uint16_t* w, const uint16_t* e_t, int V,
+                     int D, const float* inv_t, const float* lse, float* out, void* ws,
+                     cudaStream_t st);
+
+// ---- attention (attn.cu) ---------------------------------------------------
+struct AttnArgs {
+  int B, C, Pmax, Hq, Hkv, d, W;
+  const uint16_t *q, *kc, *vc, *kenc, *venc;
+  const int32_t* page_table;
+  int pages_per_req, n_pages, page_size;
+  const int32_t* prompt_len;
+  uint16_t* out;
+  float* lse;
+};
+size_t attn_ws_bytes(int B, int C, int Pmax, int Hq, int Hkv, int d, int W);
+cudaError_t attn_decode(const AttnArgs& a, void* ws, cudaStream_t st);
+
+// ---- small kernels (slot.cu) -----------------------------------------------
+cudaError_t philox_fill(uint64_t seed, const uint32_t* ctr4, int n, uint32_t* out4,
+                        cudaStream_t st);
+cudaError_t slot_noise(const uint16_t* h, int M, const uint16_t* e, int V, int D,
+                       const float* inv_t, const int32_t* slot_row, const int32_t* slot_req,
+                       int S, int R, uint64_t seed, int step, uint16_t* rows_out,
+                       float* inv_t_out, int32_t* tok_out, cudaStream_t st);
+cudaError_t slot_finish(const uint16_t* rows, const float* inv_t_rows, const float* lse_rows,
+                        const uint16_t* w, int V, int D, const int32_t* label_ids,
+                        const int32_t* n_labels, int S, int R, int samples, float gate,
+                        float* q_avg, float* h_slot, int32_t* chosen, float* lp_draws,
+                        uint8_t* resampled, int32_t* n_reads, cudaStream_t st);
+cudaError_t commit(int B, int C, const float* entropy, const int32_t* argmax,
+                   const uint8_t* cand, const float* gamma, uint8_t* committed_state,
+                   int32_t* token_state, uint8_t* commit_out, int32_t* tokens,
+                   int32_t* n_commit, cudaStream_t st);
+cudaError_t canvas_update(const uint16_t* h0, const float* e_sc, const uint16_t* emb, int V,
+                          const int32_t* tokens, const uint8_t* committed, int M, int D,
+                          uint16_t* h_out, cudaStream_t st);
+cudaError_t transpose_bf16(const uint16_t* src, int rows, int cols, uint16_t* dst,
+                           cudaStream_t st);
+
+}  // namespace dgi

@@ -1,0 +1,342 @@
+// slot.cu -- noise draws, the slot read, the entropy commit and the canvas update.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "internal.h"
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon et al., "Parallel Random Numbers: As Easy as 1, 2, 3",
+// SC'11, section 3.2 and Table 2): per round the counter (x0..x3) becomes
+// (hi(M1 x2) ^ x1 ^ k0, lo(M1 x2), hi(M0 x0) ^ x3 ^ k1, lo(M0 x0)); the key
+// advances by (W0, W1) between rounds.
+// ---------------------------------------------------------------------------
+struct U4 {
+  uint32_t x, y, z, w;
+};
+
+__device__ __forceinline__ U4 philox10(U4 c, uint32_t k0, uint32_t k1) {
+  constexpr uint32_t kM0 = 0xD2511F53u, kM1 = 0xCD9E8D57u;
+  constexpr uint32_t kW0 = 0x9E3779B9u, kW1 = 0xBB67AE85u;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      k0 += kW0;
+      k1 += kW1;
+    }
+    const uint32_t hi0 = __umulhi(kM0, c.x), lo0 = kM0 * c.x;
+    const uint32_t hi1 = __umulhi(kM1, c.z), lo1 = kM1 * c.z;
+    c = U4{hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0};
+  }
+  return c;
+}
+
+__global__ void philox_fill_kernel(uint64_t seed, const uint4* ctr, int n, uint4* out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const uint4 c = ctr[i];
+  const U4 r = philox10(U4{c.x, c.y, c.z, c.w}, (uint32_t)seed, (uint32_t)(seed >> 32));
+  out[i] = make_uint4(r.x, r.y, r.z, r.w);
+}
+
+// ---------------------------------------------------------------------------
+// a0: one CTA per (slot, draw) row: token n from Philox, row = bf16(h + E[n]).
+// ---------------------------------------------------------------------------
+__global__ void slot_noise_kernel(const __nv_bfloat16* h, int M, const __nv_bfloat16* e, int V,
+                                  int vbits, int D, const float* inv_t, const int32_t* slot_row,
+                                  const int32_t* slot_req, int S, int R, uint64_t seed, int step,
+                                  __nv_bfloat16* rows_out, float* inv_t_out, int32_t* tok_out,
+                                  int* status) {
+  const int s = blockIdx.x / R, r = blockIdx.x % R;
+  const int row = slot_row[s];
+  const bool row_ok = row >= 0 && row < M;
+  const U4 c = philox10(U4{(uint32_t)slot_req[s], (uint32_t)step, (uint32_t)r, (uint32_t)s},
+                        (uint32_t)seed, (uint32_t)(seed >> 32));
+  const int tok = (int)(c.x >> (32 - vbits));
+  if (threadIdx.x == 0) {
+    if (tok_out) tok_out[s * R + r] = tok;
+    inv_t_out[s * R + r] = row_ok ? inv_t[row] : 1.f;
+    if (!row_ok) atomicOr(status, 8 /* DG_DEV_BAD_INDEX */);
+  }
+  const __nv_bfloat162* hs = reinterpret_cast<const __nv_bfloat162*>(h + (long long)(row_ok ? row : 0) * D);
+  const __nv_bfloat162* es = reinterpret_cast<const __nv_bfloat162*>(e + (long long)tok * D);
+  __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(rows_out + (long long)blockIdx.x * D);
+  for (int i = threadIdx.x; i < D / 2; i += blockDim.x) {
+    const float2 a = __bfloat1622float2(hs[i]);
+    const float2 b = __bfloat1622float2(es[i]);
+    dst[i] = row_ok ? __floats2bfloat162_rn(a.x + b.x, a.y + b.y) : __floats2bfloat162_rn(0.f, 0.f);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// a3: one CTA (256 threads) per slot.  Label logits of every draw are fp32 dot
+// products (one warp per (draw, label)); then the renormalised distributions,
+// the gate on draw 0's entropy, the average and the choice.
+// ---------------------------------------------------------------------------
+constexpr int MAXL = 26;
+constexpr int MAXR = 8;
+
+__global__ void slot_finish_kernel(const __nv_bfloat16* rows, const float* inv_t_rows,
+                                   const float* lse_rows, const __nv_bfloat16* w, int V, int D,
+                                   const int32_t* label_ids, const int32_t* n_labels, int R,
+                                   int samples, float gate, float* q_avg, float* h_slot,
+                                   int32_t* chosen, float* lp_draws, uint8_t* resampled,
+                                   int32_t* n_reads, int* status) {
+  __shared__ float z[MAXR][MAXL];
+  __shared__ int ids[MAXL];
+  const int s = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nw = blockDim.x >> 5;
+  int n = n_labels[s];
+  const bool n_ok = n >= 1 && n <= MAXL;
+  if (!n_ok) n = 0;
+  if (threadIdx.x < MAXL) {
+    int id = (threadIdx.x < n) ? label_ids[s * MAXL + threadIdx.x] : 0;
+    if (id < 0 || id >= V) {
+      id = 0;
+      if (threadIdx.x < n) atomicOr(status, 4 /* DG_DEV_BAD_LABEL */);
+    }
+    ids[threadIdx.x] = id;
+  }
+  if (threadIdx.x == 0 && !n_ok) atomicOr(status, 4);
+  __syncthreads();
+  for (int job = warp; job < R * n; job += nw) {
+    const int r = job / n, k = job % n;
+    const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(rows + (long long)(s * R + r) * D);
+    const __nv_bfloat162* y = reinterpret_cast<const __nv_bfloat162*>(w + (long long)ids[k] * D);
+    float acc = 0.f;
+    for (int i = lane; i < D / 2; i += 32) {
+      const float2 a = __bfloat1622float2(x[i]);
+      const float2 b = __bfloat1622float2(y[i]);
+      acc = fmaf(a.x, b.x, acc);
+      acc = fmaf(a.y, b.y, acc);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) z[r][k] = acc * inv_t_rows[s * R + r];
+  }
+  __syncthreads();
+  if (threadIdx.x != 0) return;
+  // serial epilogue over <= 8 x 26 values
+  float qsum[MAXL];
+  for (int k = 0; k < MAXL; ++k) qsum[k] = 0.f;
+  float h0 = 0.f;
+  for (int r = 0; r < R; ++r) {
+    const float l = lse_rows[s * R + r];
+    float m = -INFINITY;
+    for (int k = 0; k < n; ++k) m = fmaxf(m, z[r][k]);
+    float tot = 0.f;
+    for (int k = 0; k < n; ++k) tot += expf(z[r][k] - m);
+    float hr = 0.f;
+    for (int k = 0; k < MAXL; ++k) {
+      float lp = 0.f;
+      if (k < n) {
+        const float q = expf(z[r][k] - m) / tot;
+        lp = z[r][k] - l;
+        if (q > 0.f) hr -= q * logf(q);
+        if (r < samples) qsum[k] += q;
+        if (r == 0) q_avg[s * MAXL + k] = q;  // provisional: read 0
+      }
+      lp_draws[((long long)s * R + r) * MAXL + k] = (k < n) ? lp : 0.f;
+    }
+    if (r == 0) h0 = hr;
+  }
+  const bool fire = samples > 1 && h0 > gate;
+  float best = -1.f, hs = 0.f;
+  int arg = 0;
+  for (int k = 0; k < MAXL; ++k) {
+    float q = 0.f;
+    if (k < n) q = fire ? qsum[k] / (float)samples : q_avg[s * MAXL + k];
+    q_avg[s * MAXL + k] = q;
+    if (k < n) {
+      if (q > best) {
+        best = q;
+        arg = k;
+      }
+      if (q > 0.f) hs -= q * logf(q);
+    }
+  }
+  chosen[s] = arg;
+  h_slot[s] = hs;
+  resampled[s] = fire ? 1 : 0;
+  n_reads[s] = fire ? samples : 1;
+}
+
+// ---------------------------------------------------------------------------
+// a4: one CTA per request, one thread per canvas position (C <= 1024).  The
+// rank of each candidate under (entropy, position) gives its place in the
+// confidence order; an ordered scan of the sorted entropies finds the cut.
+// ---------------------------------------------------------------------------
+__global__ void commit_kernel(int C, const float* entropy, const int32_t* argmax,
+                              const uint8_t* cand, const float* gamma, uint8_t* committed_state,
+                              int32_t* token_state, uint8_t* commit_out, int32_t* tokens,
+                              int32_t* n_commit) {
+  extern __shared__ float sh[];
+  float* ent = sh;                                       // [C]
+  int* open = reinterpret_cast<int*>(ent + C);           // [C]
+  float* sorted = reinterpret_cast<float*>(open + C);    // [C]
+  __shared__ int n_cand, cut;
+  const int b = blockIdx.x, i = threadIdx.x;
+  const long long base = (long long)b * C;
+  float hi = 0.f;
+  int oi = 0;
+  if (i < C) {
+    hi = entropy[base + i];
+    oi = cand[base + i] != 0 && !(committed_state && committed_state[base + i]);
+    ent[i] = hi;
+    open[i] = oi;
+  }
+  if (i == 0) {
+    n_cand = 0;
+    cut = 0x7fffffff;
+  }
+  __syncthreads();
+  int rank = 0;
+  if (i < C && oi) {
+    for (int j = 0; j < C; ++j) {
+      if (!open[j]) continue;
+      const float hj = ent[j];
+      rank += (hj < hi) || (hj == hi && j < i);
+    }
+    sorted[rank] = hi;
+    atomicAdd(&n_cand, 1);
+  }
+  __syncthreads();
+  if (i == 0) {
+    // ordered scan: first k >= 1 whose prefix sum passes gamma
+    float run = 0.f;
+    int k_cut = n_cand;
+    for (int k = 0; k < n_cand; ++k) {
+      run += sorted[k];
+      if (k > 0 && run > gamma[b]) {
+        k_cut = k;
+        break;
+      }
+    }
+    cut = k_cut;
+    n_commit[b] = k_cut;
+  }
+  __syncthreads();
+  if (i < C) {
+    const bool acc = oi && rank < cut;
+    const int tok = argmax[base + i];
+    commit_out[base + i] = acc ? 1 : 0;
+    tokens[base + i] = acc ? tok : -1;
+    if (acc && committed_state) committed_state[base + i] = 1;
+    if (acc && token_state) token_state[base + i] = tok;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// a6: h_out = bf16(h0 + e_sc) for open rows, bf16(h0 + emb[tok]) for committed.
+// ---------------------------------------------------------------------------
+__global__ void canvas_update_kernel(const __nv_bfloat16* h0, const float* e_sc,
+                                     const __nv_bfloat16* emb, int V, const int32_t* tokens,
+                                     const uint8_t* committed, int D, __nv_bfloat16* h_out,
+                                     int* status) {
+  const int row = blockIdx.x;
+  const bool cm = committed[row] != 0;
+  int tok = cm ? tokens[row] : 0;
+  if (cm && (tok < 0 || tok >= V)) {
+    if (threadIdx.x == 0) atomicOr(status, 8);
+    tok = 0;
+  }
+  const __nv_bfloat162* a = reinterpret_cast<const __nv_bfloat162*>(h0 + (long long)row * D);
+  const float2* es = reinterpret_cast<const float2*>(e_sc + (long long)row * D);
+  const __nv_bfloat162* et = reinterpret_cast<const __nv_bfloat162*>(emb + (long long)tok * D);
+  __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(h_out + (long long)row * D);
+  for (int i = threadIdx.x; i < D / 2; i += blockDim.x) {
+    const float2 x = __bfloat1622float2(a[i]);
+    const float2 y = cm ? __bfloat1622float2(et[i]) : es[i];
+    dst[i] = __floats2bfloat162_rn(x.x + y.x, x.y + y.y);
+  }
+}
+
+__global__ void transpose_kernel(const uint16_t* src, int rows, int cols, uint16_t* dst) {
+  __shared__ uint16_t tile[32][33];
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  for (int j = threadIdx.y; j < 32; j += blockDim.y) {
+    const int r = r0 + j, c = c0 + threadIdx.x;
+    if (r < rows && c < cols) tile[j][threadIdx.x] = src[(long long)r * cols + c];
+  }
+  __syncthreads();
+  for (int j = threadIdx.y; j < 32; j += blockDim.y) {
+    const int c = c0 + j, r = r0 + threadIdx.x;
+    if (r < rows && c < cols) dst[(long long)c * rows + r] = tile[threadIdx.x][j];
+  }
+}
+
+}  // namespace
+
+namespace dgi {
+
+cudaError_t philox_fill(uint64_t seed, const uint32_t* ctr4, int n, uint32_t* out4,
+                        cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  philox_fill_kernel<<<(n + 255) / 256, 256, 0, st>>>(seed, reinterpret_cast<const uint4*>(ctr4),
+                                                       n, reinterpret_cast<uint4*>(out4));
+  return cudaGetLastError();
+}
+
+cudaError_t slot_noise(const uint16_t* h, int M, const uint16_t* e, int V, int D,
+                       const float* inv_t, const int32_t* slot_row, const int32_t* slot_req,
+                       int S, int R, uint64_t seed, int step, uint16_t* rows_out,
+                       float* inv_t_out, int32_t* tok_out, cudaStream_t st) {
+  if (S * R == 0) return cudaSuccess;
+  int vbits = 0;
+  while ((1 << vbits) < V) ++vbits;
+  slot_noise_kernel<<<S * R, 128, 0, st>>>(
+      reinterpret_cast<const __nv_bfloat16*>(h), M, reinterpret_cast<const __nv_bfloat16*>(e), V,
+      vbits, D, inv_t, slot_row, slot_req, S, R, seed, step,
+      reinterpret_cast<__nv_bfloat16*>(rows_out), inv_t_out, tok_out, status_ptr());
+  return cudaGetLastError();
+}
+
+cudaError_t slot_finish(const uint16_t* rows, const float* inv_t_rows, const float* lse_rows,
+                        const uint16_t* w, int V, int D, const int32_t* label_ids,
+                        const int32_t* n_labels, int S, int R, int samples, float gate,
+                        float* q_avg, float* h_slot, int32_t* chosen, float* lp_draws,
+                        uint8_t* resampled, int32_t* n_reads, cudaStream_t st) {
+  if (S == 0) return cudaSuccess;
+  slot_finish_kernel<<<S, 256, 0, st>>>(
+      reinterpret_cast<const __nv_bfloat16*>(rows), inv_t_rows, lse_rows,
+      reinterpret_cast<const __nv_bfloat16*>(w), V, D, label_ids, n_labels, R, samples, gate,
+      q_avg, h_slot, chosen, lp_draws, resampled, n_reads, status_ptr());
+  return cudaGetLastError();
+}
+
+cudaError_t commit(int B, int C, const float* entropy, const int32_t* argmax,
+                   const uint8_t* cand, const float* gamma, uint8_t* committed_state,
+                   int32_t* token_state, uint8_t* commit_out, int32_t* tokens,
+                   int32_t* n_commit, cudaStream_t st) {
+  if (B == 0) return cudaSuccess;
+  const int threads = ((C + 31) / 32) * 32;
+  commit_kernel<<<B, threads, (size_t)C * 12, st>>>(C, entropy, argmax, cand, gamma,
+                                                     committed_state, token_state, commit_out,
+                                                     tokens, n_commit);
+  return cudaGetLastError();
+}
+
+cudaError_t canvas_update(const uint16_t* h0, const float* e_sc, const uint16_t* emb, int V,
+                          const int32_t* tokens, const uint8_t* committed, int M, int D,
+                          uint16_t* h_out, cudaStream_t st) {
+  if (M == 0) return cudaSuccess;
+  canvas_update_kernel<<<M, 256, 0, st>>>(
+      reinterpret_cast<const __nv_bfloat16*>(h0), e_sc,
+      reinterpret_cast<const __nv_bfloat16*>(emb), V, tokens, committed, D,
+      reinterpret_cast<__nv_bfloat16*>(h_out), status_ptr());
+  return cudaGetLastError();
+}
+
+cudaError_t transpose_bf16(const uint16_t* src, int rows, int cols, uint16_t* dst,
+                           cudaStream_t st) {
+  dim3 grid((cols + 31) / 32, (rows + 31) / 32);
+  transpose_kernel<<<grid, dim3(32, 8), 0, st>>>(src, rows, cols, dst);
+  return cudaGetLastError();
+}
+
+}  // namespace dgi

@@ -1,0 +1,213 @@
+"""ctypes binding of libdg: the same call names as include/dg.h, marshalling only.
+
+Tensor arguments may be torch tensors (their data_ptr is passed), raw integer
+addresses, or None (NULL).  ``stream`` defaults to torch's current CUDA stream.
+Every compute step runs in the library's CUDA kernels; loading fails loudly if
+the in-tree library has not been built.
+"""
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdg.so")
+
+DG_OK = 0
+DG_ERR_ARG = -1
+DG_ERR_TOO_MANY_LABELS = -2
+DG_ERR_LABEL = -3
+DG_ERR_SHAPE = -4
+DG_ERR_CUDA = -5
+DG_ERR_WORKSPACE = -6
+DG_DEV_TIMEOUT, DG_DEV_BAD_PAGE, DG_DEV_BAD_LABEL, DG_DEV_BAD_INDEX = 1, 2, 4, 8
+DG_WS_ATTN, DG_WS_LMHEAD, DG_WS_SLOT_READ, DG_WS_SELFCOND = 1, 2, 3, 4
+MAX_LABELS = 26
+
+
+class DgError(RuntimeError):
+    def __init__(self, code, what):
+        super().__init__(f"{what}: {strerror(code)} ({code})")
+        self.code = code
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in
+                ("B", "C", "P_max", "Hq", "Hkv", "d_head", "W", "d_model", "V")]
+
+
+def make_dims(B=1, C=1, P_max=0, Hq=1, Hkv=1, d_head=64, W=0, d_model=8, V=8):
+    return Dims(B, C, P_max, Hq, Hkv, d_head, W, d_model, V)
+
+
+def dims_of(shape):
+    """Dims from a configs.StepShape."""
+    return Dims(shape.B, shape.C, shape.P, shape.Hq, shape.Hkv, shape.d_head, shape.W,
+                shape.D, shape.V)
+
+
+_lib = None
+P, I, Z, U64, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint64, ctypes.c_float
+DP = ctypes.POINTER(Dims)
+
+_SIGS = {
+    "dg_attn_decode": [DP, P, P, P, P, P, P, I, I, I, P, P, P, P, Z, P],
+    "dg_lmhead_logsoftmax_entropy": [DP, P, I, P, P, P, P, P, P, P, Z, P],
+    "dg_slot_noise": [DP, P, I, P, P, P, P, I, I, U64, I, P, P, P, P],
+    "dg_slot_finish": [DP, P, P, P, P, P, P, I, I, I, F, P, P, P, P, P, P, P],
+    "dg_slot_read": [DP, P, I, P, P, P, P, P, P, P, I, U64, I, I, F, P, P, P, P, P, P, P, P, Z,
+                     P],
+    "dg_commit": [DP, P, P, P, P, P, P, P, P, P, P],
+    "dg_selfcond_embed": [DP, P, I, P, P, P, P, P, P, Z, P],
+    "dg_transpose_bf16": [P, I, I, P, P],
+    "dg_canvas_update": [DP, P, P, P, P, P, I, P, P],
+    "dg_philox_fill": [U64, P, I, P, P],
+    "dg_validate_slots": [DP, P, P, P, I, I],
+    "dg_workspace_bytes": [DP, I, I],
+    "dg_get_status": [P, P],
+    "dg_clear_status": [P],
+    "dg_strerror": [I],
+    "dg_num_sms": [],
+}
+_RES = {"dg_workspace_bytes": Z, "dg_strerror": ctypes.c_char_p}
+
+
+def lib():
+    """Load libdg.so (once).  Raises if the library has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libdg.so not built at {LIB_PATH}; run "
+                               "python -m structured_slot_reads_gb300.build")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, args in _SIGS.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = _RES.get(name, ctypes.c_int)
+        _lib = L
+    return _lib
+
+
+def strerror(code):
+    return lib().dg_strerror(int(code)).decode()
+
+
+def _p(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if hasattr(x, "ctypes"):
+        return x.ctypes.data
+    raise TypeError(f"cannot pass {type(x)} as a pointer")
+
+
+def _s(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _nbytes(t):
+    if t is None:
+        return 0
+    return t.numel() * t.element_size()
+
+
+def _check(code, what):
+    if code != DG_OK:
+        raise DgError(code, what)
+    return code
+
+
+# ---- the entry points, same names and argument order as include/dg.h -------
+def dg_attn_decode(dims, q, kc, vc, kenc, venc, page_table, pages_per_req, n_pages, page_size,
+                   prompt_len, out, lse, workspace, stream=None):
+    return lib().dg_attn_decode(ctypes.byref(dims), _p(q), _p(kc), _p(vc), _p(kenc), _p(venc),
+                                _p(page_table), pages_per_req, n_pages, page_size,
+                                _p(prompt_len), _p(out), _p(lse), _p(workspace),
+                                _nbytes(workspace), _s(stream))
+
+
+def dg_lmhead_logsoftmax_entropy(dims, h, M, w, inv_t, lse, entropy, maxz, argmax, workspace,
+                                 stream=None):
+    return lib().dg_lmhead_logsoftmax_entropy(ctypes.byref(dims), _p(h), M, _p(w), _p(inv_t),
+                                              _p(lse), _p(entropy), _p(maxz), _p(argmax),
+                                              _p(workspace), _nbytes(workspace), _s(stream))
+
+
+def dg_slot_noise(dims, h, M, e, inv_t, slot_row, slot_req, S, R, seed, step, rows_out,
+                  inv_t_out, noise_tok_out=None, stream=None):
+    return lib().dg_slot_noise(ctypes.byref(dims), _p(h), M, _p(e), _p(inv_t), _p(slot_row),
+                               _p(slot_req), S, R, seed, step, _p(rows_out), _p(inv_t_out),
+                               _p(noise_tok_out), _s(stream))
+
+
+def dg_slot_finish(dims, rows, inv_t_rows, lse_rows, w, label_ids, n_labels, S, R, samples,
+                   gate, q_avg, h_slot, chosen, lp_draws, resampled, n_reads, stream=None):
+    return lib().dg_slot_finish(ctypes.byref(dims), _p(rows), _p(inv_t_rows), _p(lse_rows), _p(w),
+                                _p(label_ids), _p(n_labels), S, R, samples, gate, _p(q_avg),
+                                _p(h_slot), _p(chosen), _p(lp_draws), _p(resampled),
+                                _p(n_reads), _s(stream))
+
+
+def dg_slot_read(dims, h, M, w, e, inv_t, slot_row, slot_req, label_ids, n_labels, S, seed, step,
+                 samples, gate, q_avg, h_slot, chosen, lp_draws, resampled, n_reads,
+                 noise_tok_out, workspace, stream=None):
+    return lib().dg_slot_read(ctypes.byref(dims), _p(h), M, _p(w), _p(e), _p(inv_t),
+                              _p(slot_row), _p(slot_req), _p(label_ids), _p(n_labels), S, seed,
+                              step, samples, gate, _p(q_avg), _p(h_slot), _p(chosen),
+                              _p(lp_draws), _p(resampled), _p(n_reads), _p(noise_tok_out),
+                              _p(workspace), _nbytes(workspace), _s(stream))
+
+
+def dg_commit(dims, entropy, argmax, cand, gamma, committed_state, token_state, commit, tokens,
+              n_commit, stream=None):
+    return lib().dg_commit(ctypes.byref(dims), _p(entropy), _p(argmax), _p(cand), _p(gamma),
+                           _p(committed_state), _p(token_state), _p(commit), _p(tokens),
+                           _p(n_commit), _s(stream))
+
+
+def dg_selfcond_embed(dims, h, M, w, e_t, inv_t, lse, out, workspace, stream=None):
+    return lib().dg_selfcond_embed(ctypes.byref(dims), _p(h), M, _p(w), _p(e_t), _p(inv_t),
+                                   _p(lse), _p(out), _p(workspace), _nbytes(workspace),
+                                   _s(stream))
+
+
+def dg_transpose_bf16(src, rows, cols, dst, stream=None):
+    return lib().dg_transpose_bf16(_p(src), rows, cols, _p(dst), _s(stream))
+
+
+def dg_canvas_update(dims, h0, e_sc, emb, tokens, committed, M, h_out, stream=None):
+    return lib().dg_canvas_update(ctypes.byref(dims), _p(h0), _p(e_sc), _p(emb), _p(tokens),
+                                  _p(committed), M, _p(h_out), _s(stream))
+
+
+def dg_philox_fill(seed, ctr4, n, out4, stream=None):
+    return lib().dg_philox_fill(seed, _p(ctr4), n, _p(out4), _s(stream))
+
+
+def dg_validate_slots(dims, slot_row_host, label_ids_host, n_labels_host, S, M):
+    return lib().dg_validate_slots(ctypes.byref(dims), _p(slot_row_host), _p(label_ids_host),
+                                   _p(n_labels_host), S, M)
+
+
+def dg_workspace_bytes(dims, which, rows):
+    return int(lib().dg_workspace_bytes(ctypes.byref(dims), which, rows))
+
+
+def dg_get_status(stream=None):
+    out = ctypes.c_int32(0)
+    _check(lib().dg_get_status(_s(stream), ctypes.addressof(out)), "dg_get_status")
+    return out.value
+
+
+def dg_clear_status(stream=None):
+    return lib().dg_clear_status(_s(stream))
+
+
+def dg_num_sms():
+    return lib().dg_num_sms()

@@ -1,0 +1,152 @@
+"""One denoise step of the structured-read sampler on the GPU, through libdg.
+
+``DenoiseStep`` owns the device buffers of one workload (torch allocates
+them; the library never does) and enqueues the library calls of one step:
+
+  dg_attn_decode                 decoder-mode attention over prompt KV + window
+  dg_lmhead_logsoftmax_entropy   lse / entropy / argmax of every canvas row
+  dg_slot_read                   noise draws + one W pass + gated slot read
+  dg_commit                      entropy-ordered commit (state carried forward)
+  dg_selfcond_embed              expected embedding softmax(z) . E
+  dg_canvas_update               next step's canvas input rows
+
+The same object serves the end-to-end path: ``upload`` copies a step's inputs
+from pinned host memory, ``download`` reads back the decisions.
+"""
+import torch
+
+from . import dg
+
+
+def _empty(shape, dtype, device):
+    return torch.empty(tuple(shape), dtype=dtype, device=device)
+
+
+class DenoiseStep:
+    def __init__(self, shape, w, e, e_t, device="cuda", with_slots=True, seed=0):
+        self.shape = shape
+        self.dims = dg.dims_of(shape)
+        self.device = device
+        B, C, D, V = shape.B, shape.C, shape.D, shape.V
+        self.M = B * C
+        self.w, self.e, self.e_t = w, e, e_t
+        bf, f32, i32, u8 = torch.bfloat16, torch.float32, torch.int32, torch.uint8
+        dev = device
+        # per-request inputs
+        self.h0 = _empty((self.M, D), bf, dev)
+        self.h = _empty((self.M, D), bf, dev)
+        self.inv_t = _empty((self.M,), f32, dev)
+        self.q = _empty((B, C, shape.Hq, shape.d_head), bf, dev)
+        self.kc = _empty((B, C, shape.Hkv, shape.d_head), bf, dev)
+        self.vc = _empty((B, C, shape.Hkv, shape.d_head), bf, dev)
+        self.kenc = _empty((B, shape.P, shape.Hkv, shape.d_head), bf, dev)
+        self.venc = _empty((B, shape.P, shape.Hkv, shape.d_head), bf, dev)
+        self.prompt_len = torch.full((B,), shape.P, dtype=i32, device=dev)
+        self.cand = _empty((B, C), u8, dev)
+        self.gamma = torch.full((B,), shape.gamma, dtype=f32, device=dev)
+        # outputs / state
+        self.attn_out = _empty((B, C, shape.Hq, shape.d_head), bf, dev)
+        self.attn_lse = _empty((B, shape.Hq, C), f32, dev)
+        self.lse = _empty((self.M,), f32, dev)
+        self.ent = _empty((self.M,), f32, dev)
+        self.maxz = _empty((self.M,), f32, dev)
+        self.argmax = _empty((self.M,), i32, dev)
+        self.committed = torch.zeros((B, C), dtype=u8, device=dev)
+        self.tok_state = torch.full((B, C), -1, dtype=i32, device=dev)
+        self.commit = _empty((B, C), u8, dev)
+        self.tokens = _empty((B, C), i32, dev)
+        self.n_commit = _empty((B,), i32, dev)
+        self.e_sc = _empty((self.M, D), f32, dev)
+        self.ws_attn = _empty((max(dg.dg_workspace_bytes(self.dims, dg.DG_WS_ATTN, 0), 256),), u8, dev)
+        self.ws_lm = _empty((dg.dg_workspace_bytes(self.dims, dg.DG_WS_LMHEAD, self.M),), u8, dev)
+        self.ws_sc = _empty((dg.dg_workspace_bytes(self.dims, dg.DG_WS_SELFCOND, self.M),), u8, dev)
+        # slots (same table for every request)
+        self.with_slots = with_slots and len(shape.slots) > 0
+        self.seed = seed
+        if self.with_slots:
+            S = B * len(shape.slots)
+            self.S = S
+            self.slot_row = _empty((S,), i32, dev)
+            self.slot_req = _empty((S,), i32, dev)
+            self.label_ids = _empty((S, dg.MAX_LABELS), i32, dev)
+            self.n_labels = _empty((S,), i32, dev)
+            self.q_avg = _empty((S, dg.MAX_LABELS), f32, dev)
+            self.h_slot = _empty((S,), f32, dev)
+            self.chosen = _empty((S,), i32, dev)
+            self.lp_draws = _empty((S, shape.R, dg.MAX_LABELS), f32, dev)
+            self.resampled = _empty((S,), u8, dev)
+            self.n_reads = _empty((S,), i32, dev)
+            self.noise_tok = _empty((S, shape.R), i32, dev)
+            self.ws_slot = _empty((dg.dg_workspace_bytes(self.dims, dg.DG_WS_SLOT_READ,
+                                                         S * shape.R),), u8, dev)
+
+    # ------------------------------------------------------------------ step
+    def reset_state(self):
+        self.committed.zero_()
+        self.tok_state.fill_(-1)
+        self.h.copy_(self.h0)
+
+    def run(self, step_idx=0, stream=None):
+        """Enqueue one denoise step; returns the number of library kernels launched."""
+        s, d = self.shape, self.dims
+        ck = dg._check
+        ck(dg.dg_attn_decode(d, self.q, self.kc, self.vc, self.kenc, self.venc, None, 0, 0, 0,
+                             self.prompt_len, self.attn_out, self.attn_lse, self.ws_attn, stream),
+           "dg_attn_decode")
+        ck(dg.dg_lmhead_logsoftmax_entropy(d, self.h, self.M, self.w, self.inv_t, self.lse,
+                                           self.ent, self.maxz, self.argmax, self.ws_lm, stream),
+           "dg_lmhead_logsoftmax_entropy")
+        if self.with_slots:
+            ck(dg.dg_slot_read(d, self.h, self.M, self.w, self.e, self.inv_t, self.slot_row,
+                               self.slot_req, self.label_ids, self.n_labels, self.S, self.seed,
+                               step_idx, s.R, s.gate, self.q_avg, self.h_slot, self.chosen,
+                               self.lp_draws, self.resampled, self.n_reads, self.noise_tok,
+                               self.ws_slot, stream), "dg_slot_read")
+        ck(dg.dg_commit(d, self.ent, self.argmax, self.cand, self.gamma, self.committed,
+                        self.tok_state, self.commit, self.tokens, self.n_commit, stream),
+           "dg_commit")
+        ck(dg.dg_selfcond_embed(d, self.h, self.M, self.w, self.e_t, self.inv_t, self.lse,
+                                self.e_sc, self.ws_sc, stream), "dg_selfcond_embed")
+        ck(dg.dg_canvas_update(d, self.h0, self.e_sc, self.e, self.tok_state, self.committed,
+                               self.M, self.h, stream), "dg_canvas_update")
+        return self.kernels_per_step()
+
+    def kernels_per_step(self):
+        """Library kernels one step launches (attention + combine, stats + finalize,
+        noise + stats + finalize + finish, commit, probs + accum + reduce, update)."""
+        n = 1 + (1 if self._attn_splits() > 1 else 0)
+        n += 2
+        n += 4 if self.with_slots else 0
+        n += 1 + 3 + 1
+        return n
+
+    def _attn_splits(self):
+        return 1 if dg.dg_workspace_bytes(self.dims, dg.DG_WS_ATTN, 0) <= 256 else 2
+
+    # ------------------------------------------------------- host round trip
+    def host_buffers(self):
+        """Pinned host tensors holding one step's inputs and outputs."""
+        pin = dict(pin_memory=True)
+        ins = {k: torch.empty(getattr(self, k).shape, dtype=getattr(self, k).dtype, **pin)
+               for k in ("h0", "inv_t", "q", "kc", "vc", "kenc", "venc", "cand")}
+        outs = {k: torch.empty(getattr(self, k).shape, dtype=getattr(self, k).dtype, **pin)
+                for k in ("commit", "tokens", "n_commit")}
+        if self.with_slots:
+            for k in ("q_avg", "chosen", "h_slot"):
+                outs[k] = torch.empty(getattr(self, k).shape, dtype=getattr(self, k).dtype, **pin)
+        return ins, outs
+
+    def upload(self, ins):
+        n = 0
+        for k, t in ins.items():
+            getattr(self, k).copy_(t, non_blocking=True)
+            n += t.numel() * t.element_size()
+        self.h.copy_(self.h0)
+        return n
+
+    def download(self, outs):
+        n = 0
+        for k, t in outs.items():
+            t.copy_(getattr(self, k), non_blocking=True)
+            n += t.numel() * t.element_size()
+        return n

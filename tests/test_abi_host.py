@@ -1,0 +1,125 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every symbol
+include/dg.h declares, and rejects bad arguments before launching anything."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from structured_slot_reads_gb300 import dg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dg.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dg_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(dg.LIB_PATH):
+        from structured_slot_reads_gb300 import build
+        build.build()
+    return dg.lib()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 16
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in dg.h but not exported"
+    assert set(names) == set(dg._SIGS), "binding and header disagree on the entry points"
+
+
+def test_strerror(lib):
+    assert dg.strerror(dg.DG_ERR_TOO_MANY_LABELS) == "at most 26 alternatives per slot"
+    assert dg.strerror(0) == "ok"
+    assert "unknown" in dg.strerror(-99)
+
+
+def _slots(n_labels, ids=None, rows=None):
+    S = len(n_labels)
+    lab = np.full((S, 26), -1, np.int32)
+    for s, n in enumerate(n_labels):
+        lab[s, :min(n, 26)] = np.arange(min(n, 26)) + 10 * s if ids is None else ids[s][:min(n, 26)]
+    rows = np.arange(S, dtype=np.int32) if rows is None else np.asarray(rows, np.int32)
+    return rows, lab, np.asarray(n_labels, np.int32)
+
+
+def test_validate_slots_rejects_27_labels(lib):
+    d = dg.make_dims(V=1000, d_model=8)
+    rows, lab, n = _slots([2, 27])
+    lab27 = np.zeros((2, 27), np.int32)  # the table is 26 wide; 27 is rejected before reading
+    assert dg.dg_validate_slots(d, rows, lab, n, 2, 10) == dg.DG_ERR_TOO_MANY_LABELS
+
+
+def test_validate_slots_accepts_26_and_checks_ids(lib):
+    d = dg.make_dims(V=1000, d_model=8)
+    rows, lab, n = _slots([2, 26, 5])
+    assert dg.dg_validate_slots(d, rows, lab, n, 3, 10) == dg.DG_OK
+    dup = lab.copy()
+    dup[1, 3] = dup[1, 4]
+    assert dg.dg_validate_slots(d, rows, dup, n, 3, 10) == dg.DG_ERR_LABEL
+    big = lab.copy()
+    big[2, 0] = 1000
+    assert dg.dg_validate_slots(d, rows, big, n, 3, 10) == dg.DG_ERR_LABEL
+    assert dg.dg_validate_slots(d, np.array([0, 1, 10], np.int32), lab, n, 3, 10) == dg.DG_ERR_SHAPE
+    assert dg.dg_validate_slots(d, rows, lab, np.array([2, 0, 5], np.int32), 3, 10) == dg.DG_ERR_LABEL
+
+
+def test_workspace_sizes(lib):
+    from structured_slot_reads_gb300 import configs
+    for shp in configs.ALL.values():
+        d = dg.dims_of(shp)
+        assert dg.dg_workspace_bytes(d, dg.DG_WS_LMHEAD, shp.B * shp.C) > 0
+        assert dg.dg_workspace_bytes(d, dg.DG_WS_SELFCOND, shp.B * shp.C) >= shp.B * shp.C * shp.V * 2
+        assert dg.dg_workspace_bytes(d, dg.DG_WS_ATTN, 0) > 0
+        assert dg.dg_workspace_bytes(d, dg.DG_WS_SLOT_READ, 12) > 12 * shp.D * 2
+    bad = dg.make_dims(d_model=12)
+    assert dg.dg_workspace_bytes(bad, dg.DG_WS_LMHEAD, 4) == 0
+    assert dg.dg_workspace_bytes(dg.make_dims(Hq=3, Hkv=2), dg.DG_WS_ATTN, 0) == 0
+    assert dg.dg_workspace_bytes(dg.make_dims(), 99, 1) == 0
+
+
+def test_compute_calls_validate_before_launch(lib):
+    d = dg.make_dims(B=1, C=32, P_max=64, Hq=2, Hkv=1, d_head=64, W=8, d_model=128, V=1024)
+    # null pointers
+    assert dg.dg_lmhead_logsoftmax_entropy(d, None, 4, None, None, None, None, None, None,
+                                           None, stream=0) == dg.DG_ERR_ARG
+    assert dg.dg_attn_decode(d, None, None, None, None, None, None, 0, 0, 0, None, None, None,
+                             None, stream=0) == dg.DG_ERR_ARG
+    assert dg.dg_commit(d, None, None, None, None, None, None, None, None, None,
+                        stream=0) == dg.DG_ERR_ARG
+    # unsupported shapes
+    bad = dg.make_dims(B=1, C=32, P_max=64, Hq=2, Hkv=1, d_head=128, W=8, d_model=128, V=1024)
+    assert dg.dg_attn_decode(bad, 16, 16, 16, 16, 16, None, 0, 0, 0, 16, 16, 16, None,
+                             stream=0) == dg.DG_ERR_SHAPE
+    gqa = dg.make_dims(B=1, C=32, P_max=64, Hq=3, Hkv=2, d_head=64, W=8, d_model=128, V=1024)
+    assert dg.dg_attn_decode(gqa, 16, 16, 16, 16, 16, None, 0, 0, 0, 16, 16, 16, None,
+                             stream=0) == dg.DG_ERR_SHAPE
+    assert dg.dg_commit(dg.make_dims(B=1, C=2000), 16, 16, 16, 16, None, None, 16, 16, 16,
+                        stream=0) == dg.DG_ERR_SHAPE
+    # misaligned TMA operand
+    assert dg.dg_lmhead_logsoftmax_entropy(d, 18, 4, 16, 16, 16, 16, 16, 16, None,
+                                           stream=0) == dg.DG_ERR_ARG
+    # non power-of-two vocabulary for the noise map
+    d1000 = dg.make_dims(d_model=128, V=1000)
+    assert dg.dg_slot_noise(d1000, 16, 4, 16, 16, 16, 16, 1, 4, 0, 0, 16, 16, None,
+                            stream=0) == dg.DG_ERR_SHAPE
+    # samples outside [1, R]
+    assert dg.dg_slot_finish(d, 16, 16, 16, 16, 16, 16, 1, 4, 5, 0.1, 16, 16, 16, 16, 16, 16,
+                             stream=0) == dg.DG_ERR_ARG
+    # workspace missing
+    assert dg.dg_lmhead_logsoftmax_entropy(d, 16, 4, 16, 16, 16, 16, 16, 16, None,
+                                           stream=0) == dg.DG_ERR_WORKSPACE
+
+
+def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(dg, "_lib", None)
+    monkeypatch.setattr(dg, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        dg.lib()

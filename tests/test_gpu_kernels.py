@@ -1,0 +1,228 @@
+"""GPU parity of each library call against the float64 oracle (through the C ABI).
+
+Sizes are chosen so the oracle finishes in seconds while the kernels still see
+several tiles and ragged tails: vocabularies that are not multiples of the
+256-wide vocabulary tile, d_model not a multiple of the 64-wide K block, more
+rows than one 128-row M tile, several 16-token pages per request.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from structured_slot_reads_gb300 import dg, inputs
+from tests.gpu_util import TOL_LOGPROB, assert_abs, assert_rel, dev, dev_bf16, host, top2_gap
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+def _lm_inputs(M, V, D, seed):
+    h = inputs.hidden(M, D, seed)
+    w, e = inputs.weights(V, D, seed)
+    inv_t = inputs.inv_temperature(M, seed)
+    return h, w, e, inv_t
+
+
+def _run_lmhead(h, w, inv_t):
+    M, D = h.shape
+    V = w.shape[0]
+    d = dg.make_dims(d_model=D, V=V)
+    out = [torch.empty(M, dtype=torch.float32, device="cuda") for _ in range(3)]
+    arg = torch.empty(M, dtype=torch.int32, device="cuda")
+    ws = torch.empty(dg.dg_workspace_bytes(d, dg.DG_WS_LMHEAD, M), dtype=torch.uint8, device="cuda")
+    hd, wd, it = dev_bf16(h), dev_bf16(w), dev(inv_t)
+    rc = dg.dg_lmhead_logsoftmax_entropy(d, hd, M, wd, it, out[0], out[1], out[2], arg, ws)
+    assert rc == dg.DG_OK, dg.strerror(rc)
+    torch.cuda.synchronize()
+    return [host(x) for x in out] + [host(arg)]
+
+
+def test_philox_matches_oracle_bit_exact():
+    rng = np.random.default_rng(0)
+    n = 4096
+    ctr = rng.integers(0, 2**32, size=(n, 4), dtype=np.uint64).astype(np.uint32)
+    ctr[:3] = [[0, 0, 0, 0], [0xffffffff] * 4, [0x243f6a88, 0x85a308d3, 0x13198a2e, 0x03707344]]
+    for seed in (0, 0xFFFFFFFFFFFFFFFF, 0x299f31d0a4093822, 123456789):
+        c = dev(ctr.view(np.int32))
+        out = torch.empty_like(c)
+        assert dg.dg_philox_fill(seed, c, n, out) == dg.DG_OK
+        torch.cuda.synchronize()
+        got = host(out).view(np.uint32)
+        want = oracle.philox4x32_10(ctr, oracle.seed_key(seed))
+        assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("M,V,D", [(1, 1024, 128), (12, 4096, 256), (200, 3000, 200),
+                                   (256, 8192, 512), (300, 2048, 128)])
+def test_lmhead_stats(M, V, D):
+    h, w, _, inv_t = _lm_inputs(M, V, D, seed=M + V)
+    lse, ent, maxz, arg = _run_lmhead(h, w, inv_t)
+    o_lse, o_ent, o_maxz, o_arg = oracle.lmhead_stats(h, w, inv_t)
+    assert_abs(lse, o_lse, what="lse")
+    assert_abs(ent, o_ent, what="entropy")
+    assert_abs(maxz, o_maxz, what="max logit")
+    z = (h.astype(np.float64) @ w.astype(np.float64).T) * inv_t[:, None]
+    gap = top2_gap(z)
+    clear = gap > 1e-3
+    assert np.array_equal(arg[clear], o_arg[clear])
+    # rows without a clear winner: the GPU's choice must attain the maximum
+    rows = np.nonzero(~clear)[0]
+    assert np.all(z[rows, arg[rows]] >= o_maxz[rows] - 1e-3)
+
+
+def test_lmhead_uniform_rows_give_ln_v():
+    M, V, D = 5, 4096, 128
+    h = np.zeros((M, D), np.float32)
+    w, _ = inputs.weights(V, D, 3)
+    lse, ent, maxz, arg = _run_lmhead(h, w, np.ones(M, np.float32))
+    assert_abs(ent, np.full(M, np.log(V)), what="uniform entropy")
+    assert_abs(lse, np.full(M, np.log(V)), what="uniform lse")
+    assert np.all(arg == 0)
+
+
+@pytest.mark.parametrize("M,V,D", [(12, 4096, 256), (256, 4096, 512), (100, 3000, 200)])
+def test_selfcond_embed(M, V, D):
+    h, w, e, inv_t = _lm_inputs(M, V, D, seed=7 + M)
+    lse, _, _, _ = _run_lmhead(h, w, inv_t)
+    d = dg.make_dims(d_model=D, V=V)
+    ed = dev_bf16(e)
+    e_t = torch.empty((D, V), dtype=torch.bfloat16, device="cuda")
+    assert dg.dg_transpose_bf16(ed, V, D, e_t) == dg.DG_OK
+    out = torch.empty((M, D), dtype=torch.float32, device="cuda")
+    ws = torch.empty(dg.dg_workspace_bytes(d, dg.DG_WS_SELFCOND, M), dtype=torch.uint8,
+                     device="cuda")
+    rc = dg.dg_selfcond_embed(d, dev_bf16(h), M, dev_bf16(w), e_t, dev(inv_t), dev(lse), out, ws)
+    assert rc == dg.DG_OK
+    torch.cuda.synchronize()
+    assert np.array_equal(host(e_t), e.T)
+    assert_rel(host(out), oracle.selfcond_embed(h, w, e, inv_t), what="expected embedding")
+
+
+def _attn_case(B, C, plen, hq, hkv, d, W, seed, paged=False, page_size=16):
+    from structured_slot_reads_gb300 import configs
+    shp = configs.StepShape("t", B=B, C=C, P=max(plen), Hq=hq, Hkv=hkv, d_head=d, W=W, D=8, V=8)
+    x = inputs.attention_inputs(shp, seed, prompt_len=np.array(plen, np.int32))
+    dims = dg.make_dims(B=B, C=C, P_max=max(plen), Hq=hq, Hkv=hkv, d_head=d, W=W)
+    out = torch.empty((B, C, hq, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, hq, C), dtype=torch.float32, device="cuda")
+    ws = torch.empty(dg.dg_workspace_bytes(dims, dg.DG_WS_ATTN, 0), dtype=torch.uint8,
+                     device="cuda")
+    if paged:
+        pk, pv, table = inputs.paged_layout(x["kenc"], x["venc"], x["prompt_len"], page_size, seed)
+        rc = dg.dg_attn_decode(dims, dev_bf16(x["q"]), dev_bf16(x["kc"]), dev_bf16(x["vc"]),
+                               dev_bf16(pk), dev_bf16(pv), dev(table), table.shape[1],
+                               pk.shape[0], page_size, dev(x["prompt_len"]), out, lse, ws)
+    else:
+        rc = dg.dg_attn_decode(dims, dev_bf16(x["q"]), dev_bf16(x["kc"]), dev_bf16(x["vc"]),
+                               dev_bf16(x["kenc"]), dev_bf16(x["venc"]), None, 0, 0, 0,
+                               dev(x["prompt_len"]), out, lse, ws)
+    assert rc == dg.DG_OK, dg.strerror(rc)
+    torch.cuda.synchronize()
+    ref, ref_lse = oracle.attn_decode(x["q"], x["kc"], x["vc"], x["kenc"], x["venc"],
+                                      x["prompt_len"], W)
+    assert_rel(host(out), ref, what="attention output")
+    assert_abs(host(lse), ref_lse, what="attention lse")
+
+
+@pytest.mark.parametrize("case", [
+    dict(B=1, C=32, plen=[64], hq=2, hkv=1, d=64, W=8),            # tiny read shape
+    dict(B=2, C=40, plen=[100, 0], hq=4, hkv=4, d=64, W=3),        # MHA, empty prompt
+    dict(B=1, C=96, plen=[70], hq=8, hkv=2, d=512, W=16),          # d=512, GQA 4:1
+    dict(B=2, C=64, plen=[130, 17], hq=8, hkv=2, d=512, W=200),    # window wider than canvas
+])
+def test_attention_contiguous(case):
+    _attn_case(**case, seed=11)
+
+
+@pytest.mark.parametrize("case", [
+    dict(B=3, C=48, plen=[37, 16, 90], hq=8, hkv=2, d=512, W=8),
+    dict(B=2, C=32, plen=[5, 64], hq=2, hkv=1, d=64, W=4),
+])
+def test_attention_paged(case):
+    _attn_case(**case, seed=5, paged=True)
+
+
+def test_slot_noise_rows_bit_exact():
+    M, V, D = 64, 1024, 128
+    h, w, e, inv_t = _lm_inputs(M, V, D, seed=3)
+    slot_row = np.array([17, 40, 63], np.int32)
+    slot_req = np.array([0, 1, 1], np.int32)
+    S, R, seed, step = 3, 4, 0xDEADBEEF12345, 5
+    d = dg.make_dims(d_model=D, V=V)
+    rows = torch.empty((S * R, D), dtype=torch.bfloat16, device="cuda")
+    it = torch.empty(S * R, dtype=torch.float32, device="cuda")
+    tok = torch.empty((S, R), dtype=torch.int32, device="cuda")
+    rc = dg.dg_slot_noise(d, dev_bf16(h), M, dev_bf16(e), dev(inv_t), dev(slot_row), dev(slot_req),
+                          S, R, seed, step, rows, it, tok)
+    assert rc == dg.DG_OK
+    torch.cuda.synchronize()
+    o_rows, o_tok = oracle.slot_noise_rows(h, e, slot_row, slot_req, seed, step, R, V)
+    assert np.array_equal(host(tok), o_tok)
+    assert np.array_equal(host(rows), o_rows)
+    assert np.array_equal(host(it), np.repeat(inv_t[slot_row], R))
+
+
+def _commit_case(B, C, gamma, seed, frac_open=1.0, state=False):
+    rng = np.random.default_rng(seed)
+    # entropies with distinct values spaced > 4e-3 apart so the order and cut are unique
+    ent = np.stack([rng.permutation(C) * 0.01 + rng.uniform(0, 1e-3, C) for _ in range(B)])
+    ent = (ent + 0.5).astype(np.float32)
+    arg = rng.integers(0, 262144, (B, C)).astype(np.int32)
+    cand = (rng.random((B, C)) < frac_open).astype(np.uint8)
+    gam = np.full(B, gamma, np.float32)
+    # keep the cut away from gamma
+    for b in range(B):
+        order = np.lexsort((np.arange(C), ent[b]))
+        order = order[cand[b][order] == 1]
+        cs = np.cumsum(ent[b][order].astype(np.float64))
+        if np.any(np.abs(cs - gam[b]) < 4e-3):
+            gam[b] += 2e-2
+    committed = (rng.random((B, C)) < 0.2).astype(np.uint8) if state else np.zeros((B, C), np.uint8)
+    tok_state = np.where(committed == 1, 7, -1).astype(np.int32)
+    d = dg.make_dims(B=B, C=C)
+    cm = torch.empty((B, C), dtype=torch.uint8, device="cuda")
+    tk = torch.empty((B, C), dtype=torch.int32, device="cuda")
+    nc = torch.empty(B, dtype=torch.int32, device="cuda")
+    cs_d, ts_d = dev(committed), dev(tok_state)
+    rc = dg.dg_commit(d, dev(ent), dev(arg), dev(cand), dev(gam), cs_d if state else None,
+                      ts_d if state else None, cm, tk, nc)
+    assert rc == dg.DG_OK
+    torch.cuda.synchronize()
+    open_ = cand & (1 - committed)
+    o_cm, o_tk, o_n = oracle.commit(ent, arg, open_, gam)
+    assert np.array_equal(host(cm), o_cm)
+    assert np.array_equal(host(tk), o_tk)
+    assert np.array_equal(host(nc), o_n)
+    if state:
+        assert np.array_equal(host(cs_d), committed | o_cm.astype(np.uint8))
+        assert np.array_equal(host(ts_d), np.where(o_cm == 1, arg, tok_state))
+
+
+@pytest.mark.parametrize("B,C,gamma,frac,state", [(1, 256, 25.6, 1.0, False), (4, 32, 3.2, 1.0, False),
+                                                  (8, 256, 25.6, 0.5, True), (2, 1000, 40.0, 0.3, True),
+                                                  (3, 64, 0.1, 1.0, False), (2, 16, 1e9, 0.0, False)])
+def test_commit(B, C, gamma, frac, state):
+    _commit_case(B, C, gamma, seed=B * C, frac_open=frac, state=state)
+
+
+def test_canvas_update_bit_exact():
+    M, V, D = 40, 512, 128
+    h0 = inputs.hidden(M, D, 1)
+    emb, _ = inputs.weights(V, D, 1)
+    e_sc = (np.random.default_rng(2).standard_normal((M, D)) * 0.05).astype(np.float32)
+    committed = (np.arange(M) % 3 == 0).astype(np.uint8)
+    tokens = np.where(committed == 1, np.arange(M) * 7 % V, -1).astype(np.int32)
+    d = dg.make_dims(d_model=D, V=V)
+    out = torch.empty((M, D), dtype=torch.bfloat16, device="cuda")
+    rc = dg.dg_canvas_update(d, dev_bf16(h0), dev(e_sc), dev_bf16(emb), dev(tokens),
+                             dev(committed), M, out)
+    assert rc == dg.DG_OK
+    torch.cuda.synchronize()
+    want = oracle.canvas_update(h0, e_sc, emb, tokens, committed)
+    assert np.array_equal(host(out), want)
+
+
+def test_status_word_clean_after_valid_calls():
+    dg.dg_clear_status()
+    test_slot_noise_rows_bit_exact()
+    assert dg.dg_get_status() == 0

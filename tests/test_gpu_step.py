@@ -1,0 +1,152 @@
+"""Whole denoise steps on the GPU (DenoiseStep, every library call) against the oracle.
+
+* tiny read shape: four consecutive steps of the loop (attention, lm-head,
+  slot read, commit with state carried forward, self-conditioning, canvas
+  update) compared step by step;
+* full-canvas shape at full size (prompt 4096, canvas 256, vocab 262144,
+  d_model 2816, 8/2 heads of 512): one step, with attention compared in full
+  and the lm-head and self-conditioning compared on sampled rows.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from structured_slot_reads_gb300 import configs, dg, inputs
+from structured_slot_reads_gb300.step import DenoiseStep
+from tests import margins
+from tests.gpu_util import assert_abs, assert_rel, dev, dev_bf16, host, top2_gap
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+def _load(st, x):
+    st.h0.copy_(dev_bf16(x["h"]))
+    st.inv_t.copy_(dev(x["inv_t"]))
+    st.q.copy_(dev_bf16(x["q"]))
+    st.kc.copy_(dev_bf16(x["kc"]))
+    st.vc.copy_(dev_bf16(x["vc"]))
+    st.kenc.copy_(dev_bf16(x["kenc"]))
+    st.venc.copy_(dev_bf16(x["venc"]))
+    st.cand.copy_(dev(x["cand"]))
+    st.prompt_len.copy_(dev(x["prompt_len"]))
+    if st.with_slots:
+        st.slot_row.copy_(dev(x["slot_row"]))
+        st.slot_req.copy_(dev(x["slot_req"]))
+        st.label_ids.copy_(dev(x["label_ids"]))
+        st.n_labels.copy_(dev(x["n_labels"]))
+    st.reset_state()
+
+
+def _tiny_inputs(n_steps, seed=0):
+    shape = configs.TINY
+    x = inputs.step_inputs(shape, seed)
+    for attempt in range(40):
+        steps, _, _ = oracle.denoise_loop(x["h"], x["w"], x["e"], x["inv_t"],
+                                          x["cand"][0].astype(bool), shape.gamma, n_steps)
+        ok = True
+        cand = x["cand"][0].astype(bool).copy()
+        z0 = (x["h"].astype(np.float64) @ x["w"].astype(np.float64).T) * x["inv_t"][:, None]
+        for st in steps:
+            ok &= margins.commit_margins_ok(st["entropy"], cand, shape.gamma)
+            new = st["commit"].astype(bool)
+            cand &= ~new
+        ok &= bool(np.all(top2_gap(z0) > margins.ARGMAX_MARGIN))
+        if ok:
+            break
+        x["h"] = inputs.hidden(shape.B * shape.C, shape.D, seed, attempt + 1)
+    else:
+        raise RuntimeError("margins not met")
+    return shape, x, steps
+
+
+def test_tiny_loop_step_by_step():
+    n_steps = 4
+    shape, x, steps = _tiny_inputs(n_steps)
+    e_t = dev_bf16(np.ascontiguousarray(x["e"].T))
+    st = DenoiseStep(shape, dev_bf16(x["w"]), dev_bf16(x["e"]), e_t, seed=0)
+    _load(st, x)
+    ref_attn, ref_attn_lse = oracle.attn_decode(x["q"], x["kc"], x["vc"], x["kenc"], x["venc"],
+                                                x["prompt_len"], shape.W)
+    h = x["h"]
+    for t in range(n_steps):
+        st.run(step_idx=t)
+        torch.cuda.synchronize()
+        ref = steps[t]
+        assert_rel(host(st.attn_out), ref_attn, what=f"step {t} attention")
+        assert_abs(host(st.attn_lse), ref_attn_lse, what=f"step {t} attention lse")
+        assert_abs(host(st.lse), ref["lse"], what=f"step {t} lse")
+        assert_abs(host(st.ent), ref["entropy"], what=f"step {t} entropy")
+        assert np.array_equal(host(st.commit)[0], ref["commit"]), f"step {t} commit set"
+        assert np.array_equal(host(st.tokens)[0], ref["tokens"]), f"step {t} tokens"
+        assert host(st.n_commit)[0] == ref["n_commit"]
+        assert_rel(host(st.e_sc), ref["e"], what=f"step {t} expected embedding")
+        # the slot read of this step, from this step's canvas input
+        want = margins.slot_read_oracle(h, x["w"], x["e"], x["inv_t"], x["slot_row"],
+                                        x["slot_req"], x["label_ids"], x["n_labels"], 0, t,
+                                        shape.R, shape.gate)
+        if margins.slot_margins_ok(want, x["n_labels"], shape.gate):
+            assert np.array_equal(host(st.chosen), want["chosen"])
+            assert np.array_equal(host(st.resampled), want["resampled"])
+            assert_abs(host(st.q_avg)[0, :4], want["q_avg"][0, :4], what="slot distribution")
+        # next step's canvas input
+        committed = host(st.committed)[0]
+        tok_state = host(st.tok_state)[0]
+        h = oracle.canvas_update(x["h"], host(st.e_sc), x["e"], tok_state, committed)
+        assert np.array_equal(host(st.h), h), f"step {t} canvas update"
+    assert dg.dg_get_status() == 0
+
+
+@pytest.fixture(scope="module")
+def full_canvas():
+    shape = configs.FULL_CANVAS
+    x = inputs.step_inputs(shape, seed=0)
+    w, e = x["w"], x["e"]
+    wd, ed = dev_bf16(w), dev_bf16(e)
+    e_t = torch.empty((shape.D, shape.V), dtype=torch.bfloat16, device="cuda")
+    assert dg.dg_transpose_bf16(ed, shape.V, shape.D, e_t) == dg.DG_OK
+    st = DenoiseStep(shape, wd, ed, e_t, seed=0)
+    _load(st, x)
+    st.run(step_idx=0)
+    torch.cuda.synchronize()
+    return shape, x, st
+
+
+def test_full_canvas_attention(full_canvas):
+    shape, x, st = full_canvas
+    ref, ref_lse = oracle.attn_decode(x["q"], x["kc"], x["vc"], x["kenc"], x["venc"],
+                                      x["prompt_len"], shape.W)
+    assert_rel(host(st.attn_out), ref, what="attention output")
+    assert_abs(host(st.attn_lse), ref_lse, what="attention lse")
+
+
+def test_full_canvas_lmhead_and_selfcond_sampled_rows(full_canvas):
+    shape, x, st = full_canvas
+    rows = np.array([0, 1, 61, 125, 128, 189, 200, 255])
+    w64 = x["w"].astype(np.float64)
+    lse, ent, maxz, arg = oracle.lmhead_stats(x["h"][rows], w64, x["inv_t"][rows])
+    assert_abs(host(st.lse)[rows], lse, what="lse")
+    assert_abs(host(st.ent)[rows], ent, what="entropy")
+    assert_abs(host(st.maxz)[rows], maxz, what="max logit")
+    e_ref = oracle.selfcond_embed(x["h"][rows], w64, x["e"], x["inv_t"][rows])
+    assert_rel(host(st.e_sc)[rows], e_ref, what="expected embedding")
+
+
+def test_full_canvas_commit_and_slots(full_canvas):
+    shape, x, st = full_canvas
+    ent = host(st.ent).astype(np.float64)[None]
+    arg = host(st.argmax)[None]
+    # the oracle's commit on the GPU's own entropies: same order, float64 prefix sums
+    cm, tk, n = oracle.commit(ent, arg, x["cand"], x["gamma"].astype(np.float64))
+    assert np.array_equal(host(st.commit), cm)
+    assert np.array_equal(host(st.tokens), tk)
+    assert host(st.n_commit)[0] == n[0] >= 1
+    # slot reads of the same step: decisions and distributions
+    want = margins.slot_read_oracle(x["h"], x["w"].astype(np.float64), x["e"], x["inv_t"],
+                                    x["slot_row"], x["slot_req"], x["label_ids"], x["n_labels"],
+                                    0, 0, shape.R, shape.gate)
+    for s, k in enumerate(x["n_labels"]):
+        assert_abs(host(st.q_avg)[s, :k], want["q_avg"][s, :k], what="slot distribution")
+    if margins.slot_margins_ok(want, x["n_labels"], shape.gate):
+        assert np.array_equal(host(st.chosen), want["chosen"])
+        assert np.array_equal(host(st.resampled), want["resampled"])
