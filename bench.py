@@ -1,0 +1,464 @@
+"""Benchmark of the structured-read denoise step on GB300 (one JSON line on rank 0).
+
+Workload (default): the full-canvas denoise step -- one request, prompt 4096
+tokens of encoder KV, 256-token canvas, 8 query / 2 KV heads of width 512,
+window +-128, d_model 2816, vocabulary 262144 -- with the three answer slots
+of the single structured read (2 / 26 / 5 labels, 4 noise reads) read in the
+same step.  One step = attention, lm-head log-softmax/entropy over all 256
+rows, the slot read (noise + one W pass + gate), the entropy commit,
+self-conditioning and the next-step canvas update.  W and E (1.48 GB each)
+are streamed every step, so every timed step reads inputs far larger than L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "denoise steps/s per 256-tok canvas; slot reads/s; % of tensor/HBM roofline"
+UNIT = "denoise steps/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(value, world):
+    """Max of a float over ranks (identity for one rank)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        sms.sort()
+        med = sms[len(sms) // 2] if sms else None
+        return {"sm_mhz": med, "sm_max_mhz": max(maxes) if maxes else None,
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+# --------------------------------------------------------------- roofline
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d["bf16_tflops_sustained"],
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+
+
+def traffic_from_profile(kernel_src, name):
+    """Per-launch DRAM bytes from the committed ncu summary, if taken on the current source."""
+    path = os.path.join(ROOT, "profiles", f"{name}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_b = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_b:
+        return None
+    sha = hashlib.sha256(open(os.path.join(ROOT, kernel_src), "rb").read()).hexdigest()
+    return float(m_b.group(1)) if sha == m_sha.group(1) else None
+
+
+# ------------------------------------------------------------ the GPU arm
+def build_step(shape, device):
+    import torch
+
+    from structured_slot_reads_gb300 import dg, inputs
+    from structured_slot_reads_gb300.step import DenoiseStep
+    torch.manual_seed(0)
+    w = inputs.device_normal_bf16((shape.V, shape.D), shape.D ** -0.5, 1, device)
+    e = inputs.device_normal_bf16((shape.V, shape.D), shape.D ** -0.5, 2, device)
+    e_t = torch.empty((shape.D, shape.V), dtype=torch.bfloat16, device=device)
+    dg._check(dg.dg_transpose_bf16(e, shape.V, shape.D, e_t), "dg_transpose_bf16")
+    st = DenoiseStep(shape, w, e, e_t, device=device, seed=7)
+    st.h0.copy_(inputs.device_normal_bf16(st.h0.shape, 1.0, 3, device))
+    st.inv_t.copy_(1.0 / inputs.device_uniform(st.inv_t.shape, 0.5, 2.0, 4, device))
+    for i, k in enumerate(("q", "kc", "vc", "kenc", "venc")):
+        getattr(st, k).copy_(inputs.device_normal_bf16(getattr(st, k).shape, 1.0, 10 + i, device))
+    st.cand.fill_(1)
+    row, req, lab, n = inputs.slot_table(shape, 0)
+    st.slot_row.copy_(torch.from_numpy(row))
+    st.slot_req.copy_(torch.from_numpy(req))
+    st.label_ids.copy_(torch.from_numpy(lab))
+    st.n_labels.copy_(torch.from_numpy(n))
+    st.reset_state()
+    torch.cuda.synchronize()
+    return st
+
+
+class CallTimer:
+    """CUDA events around each library call of a step, on the launching stream."""
+
+    def __init__(self, names):
+        import torch
+        self.torch = torch
+        self.names = names
+        self.pairs = {n: [] for n in names}
+
+    def wrap(self, st):
+        from structured_slot_reads_gb300 import dg
+        torch = self.torch
+        timer = self
+        orig = {}
+        for n in self.names:
+            fn = getattr(dg, n)
+            orig[n] = fn
+
+            def make(fn, n):
+                def inner(*a, **k):
+                    s = torch.cuda.current_stream()
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(s)
+                    r = fn(*a, **k)
+                    e1.record(s)
+                    timer.pairs[n].append((e0, e1))
+                    return r
+                return inner
+            setattr(dg, n, make(fn, n))
+        self._orig = orig
+
+    def unwrap(self):
+        from structured_slot_reads_gb300 import dg
+        for n, fn in self._orig.items():
+            setattr(dg, n, fn)
+
+    def mean_ms(self, n):
+        ps = self.pairs[n]
+        return sum(a.elapsed_time(b) for a, b in ps) / max(1, len(ps))
+
+
+def gpu_arm(args, rank, world, local):
+    import torch
+
+    from structured_slot_reads_gb300 import configs, dg
+    shape = configs.FULL_CANVAS
+    device = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    st = build_step(shape, device)
+    stream = torch.cuda.current_stream()
+    # warm-up
+    for i in range(args.warmup):
+        st.run(step_idx=i)
+    torch.cuda.synchronize()
+    dg.dg_clear_status()
+    calls = ["dg_attn_decode", "dg_lmhead_logsoftmax_entropy", "dg_slot_read", "dg_commit",
+             "dg_selfcond_embed", "dg_canvas_update"]
+    timer = CallTimer(calls)
+    timer.wrap(st)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.6)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    launches = 0
+    for i in range(args.steps):
+        launches += st.run(step_idx=args.warmup + i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_local = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    timer.unwrap()
+    status = dg.dg_get_status()
+    ms = max_over_ranks(ms_local, world)
+    per_call = {n: timer.mean_ms(n) for n in calls}
+
+    # end to end through the public step API with host buffers
+    ins, outs = st.host_buffers()
+    for k, t in ins.items():
+        t.copy_(getattr(st, k).cpu())
+    h2d = d2h = 0
+    barrier(world)
+    torch.cuda.synchronize()
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for i in range(args.e2e_steps):
+        h2d = st.upload(ins)
+        st.run(step_idx=i)
+        d2h = st.download(outs)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1), world)
+    e2e_value = world * args.e2e_steps / (e2e_ms / 1e3) if args.e2e_steps > 0 else None
+
+    value = world * args.steps / (ms / 1e3)
+    pk = peaks()
+    # dominant kernel: the fused lm-head pass (tcgen05 GEMM + online log-softmax/entropy)
+    lm_ms = per_call["dg_lmhead_logsoftmax_entropy"]
+    M = shape.B * shape.C
+    lm_bytes = shape.V * shape.D * 2 + M * shape.D * 2 + M * 16
+    lm_flops = 2.0 * M * shape.V * shape.D
+    achieved = lm_bytes / (lm_ms / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm"], "unit": "GB/s",
+            "frac": round(achieved / pk["hbm"], 4),
+            "traffic": traffic_from_profile("structured_slot_reads_gb300/csrc/gemm_tc.cu",
+                                            "lmhead_stats_full_canvas"),
+            "kernel": "dg_lmhead_logsoftmax_entropy (gemm_tc_kernel<2,256,STATS> + finalize)",
+            "peak_source": pk["source"],
+            "tensor_tflops": round(lm_flops / (lm_ms / 1e3) / 1e12, 1)}
+    kernels = {}
+    for n in calls:
+        kernels[n] = {"ms": round(per_call[n], 4)}
+    W_bytes = shape.V * shape.D * 2
+    kernels["dg_slot_read"]["hbm_frac"] = round(W_bytes / (per_call["dg_slot_read"] / 1e3) / 1e9 / pk["hbm"], 4)
+    sc_bytes = 2 * W_bytes + 2 * M * shape.V * 2
+    kernels["dg_selfcond_embed"]["hbm_frac"] = round(sc_bytes / (per_call["dg_selfcond_embed"] / 1e3) / 1e9 / pk["hbm"], 4)
+    kernels["dg_selfcond_embed"]["tensor_frac_sustained"] = round(
+        4.0 * M * shape.V * shape.D / (per_call["dg_selfcond_embed"] / 1e3) / 1e12 / pk["bf16_sus"], 4)
+    att_flops = attn_flops(shape)
+    kernels["dg_attn_decode"]["tensor_frac_burst"] = round(
+        att_flops / (per_call["dg_attn_decode"] / 1e3) / 1e12 / pk["bf16"], 4)
+    kernels["dg_lmhead_logsoftmax_entropy"]["hbm_frac"] = roof["frac"]
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "full_canvas_step: B=1, prompt 4096, canvas 256, Hq 8 / Hkv 2, "
+                               "d_head 512, W 128, d_model 2816, vocab 262144, gamma 25.6, "
+                               "3 answer slots (2/26/5 labels) x 4 noise reads",
+                   "global_batch": world * shape.B, "seq_len": shape.C,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2: W and E (1.48 GB each) streamed every step"},
+        "slot_reads_per_s": round(value, 3),
+        "slot_decisions_per_s": round(value * len(shape.slots), 3),
+        "roofline": roof,
+        "kernels": kernels,
+        "e2e": {"value": round(e2e_value, 3) if e2e_value else None, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "device_status": status,
+    }
+    return line, st
+
+
+def attn_flops(shape):
+    """Algorithmic attention FLOPs of one step (QK^T and PV over visible keys)."""
+    C, W = shape.C, shape.W
+    vis = 0
+    for i in range(C):
+        vis += shape.P + (min(C - 1, i + W) - max(0, i - W) + 1)
+    return 4.0 * shape.B * shape.Hq * shape.d_head * vis
+
+
+# --------------------------------------------------------- the CPU oracle
+def oracle_inputs(shape, st=None):
+    """Host copies of one step's inputs for the oracle (weights held in float64)."""
+    import numpy as np
+
+    from structured_slot_reads_gb300 import inputs
+    if st is not None:
+        w = st.w.float().cpu().numpy().astype(np.float64)
+        e = st.e.float().cpu().numpy().astype(np.float64)
+        h = st.h0.float().cpu().numpy()
+        inv_t = st.inv_t.cpu().numpy()
+    else:
+        w32, e32 = inputs.weights(shape.V, shape.D, 1)
+        w, e = w32.astype(np.float64), e32.astype(np.float64)
+        del w32, e32
+        h = inputs.hidden(shape.B * shape.C, shape.D, 3)
+        inv_t = inputs.inv_temperature(shape.B * shape.C, 4)
+    x = inputs.attention_inputs(shape, 5)
+    slots = inputs.slot_table(shape, 0)
+    return dict(w=w, e=e, h=h, inv_t=inv_t, att=x, slots=slots)
+
+
+def oracle_sample(shape, data, target_rows=16, heads=1, seed=0):
+    """Time the float64 oracle on a bounded sample of one step and scale to a full step.
+
+    Sample: lm-head statistics and self-conditioning for ``target_rows`` canvas
+    rows, attention for ``heads`` query head(s) over the whole canvas, the slot
+    read (three slots x four draws) and the commit in full.  Each part's time
+    is scaled by its share of the full step and the parts are summed.
+    """
+    import numpy as np
+
+    import oracle
+    rng = np.random.default_rng(seed)
+    w, e, h, inv_t, x = data["w"], data["e"], data["h"], data["inv_t"], data["att"]
+    M = shape.B * shape.C
+    rows = rng.choice(M, size=target_rows, replace=False)
+    parts = {}
+    t0 = time.perf_counter()
+    lse, ent, maxz, arg = oracle.lmhead_stats(h[rows], w, inv_t[rows])
+    parts["lmhead"] = (time.perf_counter() - t0) * M / target_rows
+    t0 = time.perf_counter()
+    oracle.selfcond_embed(h[rows], w, e, inv_t[rows])
+    parts["selfcond"] = (time.perf_counter() - t0) * M / target_rows
+    t0 = time.perf_counter()
+    oracle.attn_decode(x["q"][:, :, :heads], x["kc"][:, :, :1], x["vc"][:, :, :1],
+                       x["kenc"][:, :, :1], x["venc"][:, :, :1], x["prompt_len"], shape.W)
+    parts["attention"] = (time.perf_counter() - t0) * shape.Hq / heads
+    row, req, lab, n = data["slots"]
+    t0 = time.perf_counter()
+    rows_d, _ = oracle.slot_noise_rows(h, e, row, req, 7, 0, shape.R, shape.V)
+    inv_d = np.repeat(inv_t[row], shape.R)
+    lse_d, _, _, _ = oracle.lmhead_stats(rows_d, w, inv_d)
+    zl = oracle.label_logits(rows_d, w, inv_d, np.repeat(lab, shape.R, axis=0),
+                             np.repeat(n, shape.R))
+    oracle.slot_read(zl.reshape(len(row), shape.R, -1), lse_d.reshape(len(row), shape.R), n,
+                     shape.R, shape.gate)
+    parts["slot_read"] = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    ent_full = np.concatenate([ent, rng.uniform(10, 12, M - target_rows)])
+    oracle.commit(ent_full[None], np.zeros((1, M), int), np.ones((1, M), np.uint8),
+                  np.array([shape.gamma]))
+    parts["commit"] = time.perf_counter() - t0
+    total = sum(parts.values())
+    sample = (f"lm-head + self-conditioning on {target_rows} of {M} canvas rows "
+              f"(x{M // target_rows}), attention for {heads} of {shape.Hq} query heads "
+              f"(x{shape.Hq // heads}), slot read and commit in full; parts summed into one "
+              f"full-step time")
+    return 1.0 / total, sample, {k: round(v, 3) for k, v in parts.items()}
+
+
+def reference_arm(args, rank):
+    """The oracle as the reference implementation, timed on the host cores (rank 0 only)."""
+    from structured_slot_reads_gb300 import configs
+    if rank != 0:
+        return None
+    shape = configs.FULL_CANVAS
+    data = oracle_inputs(shape)
+    times = []
+    sample = ""
+    for i in range(args.warmup + args.steps):
+        v, sample, _ = oracle_sample(shape, data, target_rows=4, heads=1, seed=i)
+        if i >= args.warmup:
+            times.append(1.0 / v)
+    t = sum(times)
+    value = args.steps / t
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * t / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "full_canvas_step (float64 CPU oracle, sampled)",
+                       "global_batch": 1, "seq_len": shape.C, "parallelism": "host cores"},
+            "cpu_baseline": {"kind": "oracle", "cores": os.cpu_count(), "sample": sample,
+                             "value": round(value, 6), "unit": UNIT},
+            "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        if args.impl == "reference":
+            if rank != 0:
+                return 0
+        else:
+            import torch
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+    if args.impl == "reference":
+        line = reference_arm(args, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+    line, st = gpu_arm(args, rank, world, local)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, sample, parts = oracle_sample(st.shape, oracle_inputs(st.shape, st), target_rows=16,
+                                         heads=1)
+        line["cpu_baseline"] = {"value": round(v, 6), "unit": UNIT, "cores": os.cpu_count(),
+                                "kind": "oracle", "sample": sample, "parts_s": parts}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
