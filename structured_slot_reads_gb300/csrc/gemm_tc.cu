@@ -366,7 +366,7 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
     }
     if (EPI == EPI_STATS && row_ok) {
       const int gn = blockIdx.x % p.cpg;
-      const long long o = (long long)gn * p.M + row;
+      const long long o = (long long)row * p.cpg + gn;
       const long long plane = (long long)p.cpg * p.M;
       p.part[o] = m_run;
       p.part[o + plane] = s_run;
@@ -382,36 +382,53 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
   if (warp == MMA_WARP) tmem_dealloc(tmem_base, CF::TMEM_COLS);
 }
 
-// Merge the per-CTA online statistics of every row in a fixed CTA order.
+// Merge the per-CTA online statistics of every row: one warp per row, lanes over
+// the CTA partials (stored row-major, [M][cpg]), a fixed shuffle-tree order.
 __global__ void stats_finalize_kernel(const float* part, int cpg, int M, const float* inv_t,
                                       float* lse, float* entropy, float* maxz, int32_t* argmax) {
-  const int row = blockIdx.x * blockDim.x + threadIdx.x;
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
   if (row >= M) return;
   const long long plane = (long long)cpg * M;
+  const float* pm = part + (long long)row * cpg;
   float m = -INFINITY;
-  for (int g = 0; g < cpg; ++g) m = fmaxf(m, part[(long long)g * M + row]);
+  for (int g = lane; g < cpg; g += 32) m = fmaxf(m, pm[g]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   float s = 0.f, t = 0.f, best = -INFINITY;
   int idx = 0x7fffffff;
-  for (int g = 0; g < cpg; ++g) {
-    const long long o = (long long)g * M + row;
-    const float mg = part[o];
+  for (int g = lane; g < cpg; g += 32) {
+    const float mg = pm[g];
     if (mg != -INFINITY) {
       const float f = exp2f(mg - m);
-      s += part[o + plane] * f;
-      t += part[o + 2 * plane] * f;
+      s += pm[g + plane] * f;
+      t += pm[g + 2 * plane] * f;
     }
-    const float bg = part[o + 3 * plane];
-    const int ig = reinterpret_cast<const int*>(part)[o + 4 * plane];
+    const float bg = pm[g + 3 * plane];
+    const int ig = reinterpret_cast<const int*>(pm)[g + 4 * plane];
     if (bg > best || (bg == best && ig < idx)) {
       best = bg;
       idx = ig;
     }
   }
-  const float l = (m + log2f(s)) * LN2;
-  lse[row] = l;
-  entropy[row] = l - (t / s) * LN2;
-  maxz[row] = best * inv_t[row];
-  argmax[row] = idx;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    s += __shfl_xor_sync(0xffffffffu, s, o);
+    t += __shfl_xor_sync(0xffffffffu, t, o);
+    const float bo = __shfl_xor_sync(0xffffffffu, best, o);
+    const int io = __shfl_xor_sync(0xffffffffu, idx, o);
+    if (bo > best || (bo == best && io < idx)) {
+      best = bo;
+      idx = io;
+    }
+  }
+  if (lane == 0) {
+    const float l = (m + log2f(s)) * LN2;
+    lse[row] = l;
+    entropy[row] = l - (t / s) * LN2;
+    maxz[row] = best * inv_t[row];
+    argmax[row] = idx;
+  }
 }
 
 // out[m][n] = sum over splits of part[s][m][n], splits added in order.
@@ -478,8 +495,8 @@ cudaError_t run_stats(const uint16_t* h, int M, const uint16_t* w, int V, int D,
   cudaError_t e = (mt == 1) ? launch_gemm<1, STATS_BN, EPI_STATS>(ta, tb, p, groups * p.cpg, st)
                             : launch_gemm<2, STATS_BN, EPI_STATS>(ta, tb, p, groups * p.cpg, st);
   if (e != cudaSuccess) return e;
-  stats_finalize_kernel<<<(M + 127) / 128, 128, 0, st>>>(part, p.cpg, M, inv_t, out.lse,
-                                                         out.entropy, out.maxz, out.argmax);
+  stats_finalize_kernel<<<(M + 7) / 8, 256, 0, st>>>(part, p.cpg, M, inv_t, out.lse,
+                                                     out.entropy, out.maxz, out.argmax);
   return cudaGetLastError();
 }
 

@@ -104,66 +104,103 @@ __global__ void slot_finish_kernel(const __nv_bfloat16* rows, const float* inv_t
   }
   if (threadIdx.x == 0 && !n_ok) atomicOr(status, 4);
   __syncthreads();
+  // one warp per (draw, label) dot product; each lane issues all of its 16-byte
+  // loads before accumulating so a product costs one memory latency
+  const bool vec = (D % 8) == 0;
   for (int job = warp; job < R * n; job += nw) {
     const int r = job / n, k = job % n;
-    const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(rows + (long long)(s * R + r) * D);
-    const __nv_bfloat162* y = reinterpret_cast<const __nv_bfloat162*>(w + (long long)ids[k] * D);
+    const __nv_bfloat16* xr = rows + (long long)(s * R + r) * D;
+    const __nv_bfloat16* yr = w + (long long)ids[k] * D;
     float acc = 0.f;
-    for (int i = lane; i < D / 2; i += 32) {
-      const float2 a = __bfloat1622float2(x[i]);
-      const float2 b = __bfloat1622float2(y[i]);
-      acc = fmaf(a.x, b.x, acc);
-      acc = fmaf(a.y, b.y, acc);
+    if (vec) {
+      const uint4* x = reinterpret_cast<const uint4*>(xr);
+      const uint4* y = reinterpret_cast<const uint4*>(yr);
+      const int n16 = D / 8;
+      for (int base = 0; base < n16; base += 32 * 4) {
+        uint4 xa[4], ya[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = base + u * 32 + lane;
+          xa[u] = i < n16 ? x[i] : make_uint4(0, 0, 0, 0);
+          ya[u] = i < n16 ? __ldg(y + i) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&xa[u]);
+          const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&ya[u]);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 a = __bfloat1622float2(a2[q]);
+            const float2 b = __bfloat1622float2(b2[q]);
+            acc = fmaf(a.x, b.x, acc);
+            acc = fmaf(a.y, b.y, acc);
+          }
+        }
+      }
+    } else {
+      const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(xr);
+      const __nv_bfloat162* y = reinterpret_cast<const __nv_bfloat162*>(yr);
+      for (int i = lane; i < D / 2; i += 32) {
+        const float2 a = __bfloat1622float2(x[i]);
+        const float2 b = __bfloat1622float2(y[i]);
+        acc = fmaf(a.x, b.x, acc);
+        acc = fmaf(a.y, b.y, acc);
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) z[r][k] = acc * inv_t_rows[s * R + r];
   }
   __syncthreads();
-  if (threadIdx.x != 0) return;
-  // serial epilogue over <= 8 x 26 values
-  float qsum[MAXL];
-  for (int k = 0; k < MAXL; ++k) qsum[k] = 0.f;
-  float h0 = 0.f;
+  if (warp != 0) return;
+  // warp-parallel epilogue: lane k holds label k
+  const int k = lane;
+  const bool kv = k < n;
+  float qsum = 0.f, q0 = 0.f, h0 = 0.f;
   for (int r = 0; r < R; ++r) {
-    const float l = lse_rows[s * R + r];
-    float m = -INFINITY;
-    for (int k = 0; k < n; ++k) m = fmaxf(m, z[r][k]);
-    float tot = 0.f;
-    for (int k = 0; k < n; ++k) tot += expf(z[r][k] - m);
-    float hr = 0.f;
-    for (int k = 0; k < MAXL; ++k) {
-      float lp = 0.f;
-      if (k < n) {
-        const float q = expf(z[r][k] - m) / tot;
-        lp = z[r][k] - l;
-        if (q > 0.f) hr -= q * logf(q);
-        if (r < samples) qsum[k] += q;
-        if (r == 0) q_avg[s * MAXL + k] = q;  // provisional: read 0
-      }
-      lp_draws[((long long)s * R + r) * MAXL + k] = (k < n) ? lp : 0.f;
+    const float zk = kv ? z[r][k] : -INFINITY;
+    float m = zk;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float ek = kv ? expf(zk - m) : 0.f;
+    float tot = ek;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    const float q = ek / tot;
+    float hq = (kv && q > 0.f) ? -q * logf(q) : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) hq += __shfl_xor_sync(0xffffffffu, hq, o);
+    if (k < MAXL) lp_draws[((long long)s * R + r) * MAXL + k] = kv ? zk - lse_rows[s * R + r] : 0.f;
+    if (r < samples) qsum += q;
+    if (r == 0) {
+      q0 = q;
+      h0 = hq;
     }
-    if (r == 0) h0 = hr;
   }
   const bool fire = samples > 1 && h0 > gate;
-  float best = -1.f, hs = 0.f;
-  int arg = 0;
-  for (int k = 0; k < MAXL; ++k) {
-    float q = 0.f;
-    if (k < n) q = fire ? qsum[k] / (float)samples : q_avg[s * MAXL + k];
-    q_avg[s * MAXL + k] = q;
-    if (k < n) {
-      if (q > best) {
-        best = q;
-        arg = k;
-      }
-      if (q > 0.f) hs -= q * logf(q);
+  const float qk = kv ? (fire ? qsum / (float)samples : q0) : 0.f;
+  float hs = (kv && qk > 0.f) ? -qk * logf(qk) : 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) hs += __shfl_xor_sync(0xffffffffu, hs, o);
+  // argmax over labels, lowest index on ties
+  float best = kv ? qk : -1.f;
+  int arg = k;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float bo = __shfl_xor_sync(0xffffffffu, best, o);
+    const int ao = __shfl_xor_sync(0xffffffffu, arg, o);
+    if (bo > best || (bo == best && ao < arg)) {
+      best = bo;
+      arg = ao;
     }
   }
-  chosen[s] = arg;
-  h_slot[s] = hs;
-  resampled[s] = fire ? 1 : 0;
-  n_reads[s] = fire ? samples : 1;
+  if (k < MAXL) q_avg[s * MAXL + k] = qk;
+  if (lane == 0) {
+    chosen[s] = arg;
+    h_slot[s] = hs;
+    resampled[s] = fire ? 1 : 0;
+    n_reads[s] = fire ? samples : 1;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -302,7 +339,7 @@ cudaError_t slot_finish(const uint16_t* rows, const float* inv_t_rows, const flo
                         float* q_avg, float* h_slot, int32_t* chosen, float* lp_draws,
                         uint8_t* resampled, int32_t* n_reads, cudaStream_t st) {
   if (S == 0) return cudaSuccess;
-  slot_finish_kernel<<<S, 256, 0, st>>>(
+  slot_finish_kernel<<<S, 1024, 0, st>>>(
       reinterpret_cast<const __nv_bfloat16*>(rows), inv_t_rows, lse_rows,
       reinterpret_cast<const __nv_bfloat16*>(w), V, D, label_ids, n_labels, R, samples, gate,
       q_avg, h_slot, chosen, lp_draws, resampled, n_reads, status_ptr());
