@@ -225,8 +225,9 @@ def gpu_arm(args, rank, world, local):
         st.run(step_idx=i)
     torch.cuda.synchronize()
     dg.dg_clear_status()
-    calls = ["dg_attn_decode", "dg_lmhead_logsoftmax_entropy", "dg_slot_read", "dg_commit",
-             "dg_selfcond_embed", "dg_canvas_update"]
+    calls = ["dg_attn_decode", "dg_lmhead_logsoftmax_entropy", "dg_slot_read", "dg_slot_noise",
+             "dg_denoise_heads", "dg_slot_finish", "dg_commit", "dg_selfcond_embed",
+             "dg_selfcond_from_probs", "dg_canvas_update"]
     timer = CallTimer(calls)
     timer.wrap(st)
     clocks = ClockSampler(local)
@@ -271,32 +272,33 @@ def gpu_arm(args, rank, world, local):
 
     value = world * args.steps / (ms / 1e3)
     pk = peaks()
-    # dominant kernel: the fused lm-head pass (tcgen05 GEMM + online log-softmax/entropy)
-    lm_ms = per_call["dg_lmhead_logsoftmax_entropy"]
-    M = shape.B * shape.C
-    lm_bytes = shape.V * shape.D * 2 + M * shape.D * 2 + M * 16
-    lm_flops = 2.0 * M * shape.V * shape.D
-    achieved = lm_bytes / (lm_ms / 1e3) / 1e9
-    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm"], "unit": "GB/s",
-            "frac": round(achieved / pk["hbm"], 4),
-            "traffic": traffic_from_profile("structured_slot_reads_gb300/csrc/gemm_tc.cu",
-                                            "lmhead_stats_full_canvas"),
-            "kernel": "dg_lmhead_logsoftmax_entropy (gemm_tc_kernel<2,256,STATS> + finalize)",
-            "peak_source": pk["source"],
-            "tensor_tflops": round(lm_flops / (lm_ms / 1e3) / 1e12, 1)}
+    work = call_work(shape, st)
     kernels = {}
     for n in calls:
-        kernels[n] = {"ms": round(per_call[n], 4)}
-    W_bytes = shape.V * shape.D * 2
-    kernels["dg_slot_read"]["hbm_frac"] = round(W_bytes / (per_call["dg_slot_read"] / 1e3) / 1e9 / pk["hbm"], 4)
-    sc_bytes = 2 * W_bytes + 2 * M * shape.V * 2
-    kernels["dg_selfcond_embed"]["hbm_frac"] = round(sc_bytes / (per_call["dg_selfcond_embed"] / 1e3) / 1e9 / pk["hbm"], 4)
-    kernels["dg_selfcond_embed"]["tensor_frac_sustained"] = round(
-        4.0 * M * shape.V * shape.D / (per_call["dg_selfcond_embed"] / 1e3) / 1e12 / pk["bf16_sus"], 4)
-    att_flops = attn_flops(shape)
-    kernels["dg_attn_decode"]["tensor_frac_burst"] = round(
-        att_flops / (per_call["dg_attn_decode"] / 1e3) / 1e12 / pk["bf16"], 4)
-    kernels["dg_lmhead_logsoftmax_entropy"]["hbm_frac"] = roof["frac"]
+        if not timer.pairs[n]:
+            continue
+        t_s = per_call[n] / 1e3
+        b, f = work.get(n, (0.0, 0.0))
+        kernels[n] = {"ms": round(per_call[n], 4), "bytes": b, "flops": f}
+        if b:
+            kernels[n]["hbm_frac"] = round(b / t_s / 1e9 / pk["hbm"], 4)
+        if f:
+            kernels[n]["tensor_frac_sustained"] = round(f / t_s / 1e12 / pk["bf16_sus"], 4)
+    # the dominant kernel: the one W stream of the step (fused lm-head pass)
+    dom = "dg_denoise_heads" if "dg_denoise_heads" in kernels else "dg_lmhead_logsoftmax_entropy"
+    dom_ms = per_call[dom]
+    dom_bytes, dom_flops = work[dom]
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    src = ("structured_slot_reads_gb300/csrc/heads_tc.cu" if dom == "dg_denoise_heads"
+           else "structured_slot_reads_gb300/csrc/gemm_tc.cu")
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm"], "unit": "GB/s",
+            "frac": round(achieved / pk["hbm"], 4),
+            "traffic": traffic_from_profile(src, "denoise_heads_full_canvas"
+                                            if dom == "dg_denoise_heads"
+                                            else "lmhead_stats_full_canvas"),
+            "kernel": dom, "peak_source": pk["source"],
+            "tensor_tflops": round(dom_flops / (dom_ms / 1e3) / 1e12, 1),
+            "tensor_frac_sustained": round(dom_flops / (dom_ms / 1e3) / 1e12 / pk["bf16_sus"], 4)}
 
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
@@ -320,6 +322,26 @@ def gpu_arm(args, rank, world, local):
         "device_status": status,
     }
     return line, st
+
+
+def call_work(shape, st):
+    """Algorithmic HBM bytes and FLOPs of each library call of one step."""
+    M, V, D = shape.B * shape.C, shape.V, shape.D
+    W = V * D * 2
+    nd = getattr(st, "n_draw", 0)
+    kv = shape.B * (shape.P + shape.C) * shape.Hkv * shape.d_head * 2 * 2
+    qo = 2 * shape.B * shape.C * shape.Hq * shape.d_head * 2
+    return {
+        "dg_attn_decode": (kv + qo, attn_flops(shape)),
+        "dg_lmhead_logsoftmax_entropy": (W + M * D * 2 + M * 16, 2.0 * M * V * D),
+        "dg_slot_read": (W + nd * D * 4, 2.0 * nd * V * D),
+        "dg_denoise_heads": (W + (M + nd) * D * 2 + M * V * 2 + M * 20,
+                             2.0 * (M + nd) * V * D),
+        "dg_selfcond_embed": (2 * W + 2 * M * V * 2 + M * D * 4, 4.0 * M * V * D),
+        "dg_selfcond_from_probs": (W + M * V * 2 + M * D * 4, 2.0 * M * V * D),
+        "dg_slot_noise": (3 * nd * D * 2, 0.0),
+        "dg_canvas_update": (M * D * (2 + 4 + 2), 0.0),
+    }
 
 
 def attn_flops(shape):

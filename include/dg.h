@@ -50,6 +50,7 @@ extern "C" {
 #define DG_DEV_BAD_PAGE 2   /* a page-table entry outside the page pool      */
 #define DG_DEV_BAD_LABEL 4  /* a label id or label count out of range        */
 #define DG_DEV_BAD_INDEX 8  /* a slot row / token id outside its tensor      */
+#define DG_DEV_RANGE 16     /* a logit beyond the fused pass's exponent range */
 
 #define DG_MAX_LABELS 26 /* sotaaz.com, "The server accepts at most 26 alternatives per question" */
 
@@ -58,6 +59,8 @@ extern "C" {
 #define DG_WS_LMHEAD 2
 #define DG_WS_SLOT_READ 3
 #define DG_WS_SELFCOND 4
+#define DG_WS_HEADS 5
+#define DG_WS_PROBS_EMBED 6
 
 /* Problem dimensions.  B requests, C canvas tokens each, P_max the longest
  * prompt (encoder KV) length, Hq/Hkv query/KV heads (GQA, Hq % Hkv == 0),
@@ -189,6 +192,42 @@ int dg_selfcond_embed(const dg_dims* dims, const uint16_t* h, int M,
                       const float* lse, float* out, void* workspace,
                       size_t workspace_bytes, void* stream);
 
+/* ---- a2 + a3 + a5 fused: one stream of W per denoise step ----------------
+ * The lm-head pass of dg_lmhead_logsoftmax_entropy over the M canvas rows,
+ * plus, from the same W tiles:
+ *  - the full-vocabulary log-normaliser of n_draw <= 16 slot draw rows
+ *    (dg_slot_noise output), for dg_slot_finish (sotaaz.com, "The server
+ *    accepts at most 26 alternatives per question");
+ *  - the self-conditioning probabilities of the canvas rows (24-ai.news,
+ *    "Token commit mechanism") as unnormalised bf16 values
+ *    probs[i][v] = 2^(z_iv log2(e) - r_i), r_i a per-row reference computed from
+ *    the first 64 vocabulary entries, and prob_scale[i] = 1 / sum_v probs[i][v],
+ *    so p_iv = probs[i][v] * prob_scale[i].
+ * If some z_iv lies more than 100 / log2(e) nats above r_i the exponent is
+ * clamped and DG_DEV_RANGE is set in the status word; dg_selfcond_embed (which
+ * recomputes the logits) is exact for any input.
+ *   h [M, d_model] bf16;  draw_rows [n_draw, d_model] bf16 (NULL if n_draw = 0)
+ *   w [V, d_model] bf16;  inv_t [M], inv_t_draw [n_draw] fp32
+ *   lse, entropy, maxz [M] fp32;  argmax [M] int32;  lse_draw [n_draw] fp32
+ *   prob_scale [M] fp32;  probs [M, probs_ld] bf16 (probs_ld >= V, multiple of
+ *   64; NULL to skip the probabilities)
+ *   workspace: dg_workspace_bytes(dims, DG_WS_HEADS, M) bytes. */
+int dg_denoise_heads(const dg_dims* dims, const uint16_t* h, int M,
+                     const uint16_t* draw_rows, int n_draw, const uint16_t* w,
+                     const float* inv_t, const float* inv_t_draw, float* lse,
+                     float* entropy, float* maxz, int32_t* argmax, float* lse_draw,
+                     float* prob_scale, uint16_t* probs, size_t probs_ld,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Expected embedding from dg_denoise_heads' probabilities:
+ * out[i] = prob_scale[i] * sum_v probs[i][v] e[v] (24-ai.news, "Token commit
+ * mechanism").  e_t as in dg_selfcond_embed; probs [M, probs_ld] bf16.
+ *   workspace: dg_workspace_bytes(dims, DG_WS_PROBS_EMBED, M) bytes. */
+int dg_selfcond_from_probs(const dg_dims* dims, const uint16_t* probs, size_t probs_ld,
+                           const float* prob_scale, int M, const uint16_t* e_t,
+                           float* out, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
 /* Transpose a bf16 matrix src [rows, cols] into dst [cols, rows]; used once to
  * lay out the embedding table for dg_selfcond_embed. */
 int dg_transpose_bf16(const uint16_t* src, int rows, int cols, uint16_t* dst,
@@ -216,10 +255,13 @@ int dg_philox_fill(uint64_t seed, const uint32_t* ctr4, int n, uint32_t* out4,
 int dg_validate_slots(const dg_dims* dims, const int32_t* slot_row_host,
                       const int32_t* label_ids_host, const int32_t* n_labels_host,
                       int S, int M);
-/* Bytes of device workspace a call needs (rows = M for DG_WS_LMHEAD and
- * DG_WS_SELFCOND, S*samples for DG_WS_SLOT_READ, ignored for DG_WS_ATTN);
- * 0 for an invalid request. */
+/* Bytes of device workspace a call needs (rows = M for DG_WS_LMHEAD,
+ * DG_WS_SELFCOND, DG_WS_HEADS and DG_WS_PROBS_EMBED, S*samples for
+ * DG_WS_SLOT_READ, ignored for DG_WS_ATTN); 0 for an invalid request. */
 size_t dg_workspace_bytes(const dg_dims* dims, int which, int rows);
+/* Row length (elements) of the probability buffer dg_denoise_heads writes for
+ * a vocabulary of V: V rounded up to a multiple of 64; 0 if V < 1. */
+size_t dg_probs_ld(int V);
 /* Copy the device status word into *status_out (host) after the work already
  * on `stream` finishes; this call synchronises that stream. */
 int dg_get_status(void* stream, int32_t* status_out);

@@ -158,9 +158,57 @@ size_t dg_workspace_bytes(const dg_dims* d, int which, int rows) {
     case DG_WS_SELFCOND:
       if (!dims_lm(d) || rows < 1) return 0;
       return dgi::selfcond_ws_bytes(rows, d->V, d->d_model);
+    case DG_WS_HEADS: {
+      if (!dims_lm(d) || rows < 1) return 0;
+      const size_t a = dgi::heads_ws_bytes(rows, d->V, 0);
+      const size_t b = dgi::heads_ws_bytes(rows, d->V, 1);
+      return a > b ? a : b;
+    }
+    case DG_WS_PROBS_EMBED:
+      if (!dims_lm(d) || rows < 1) return 0;
+      return dgi::probs_embed_ws_bytes(rows, d->V, d->d_model);
     default:
       return 0;
   }
+}
+
+size_t dg_probs_ld(int V) { return V < 1 ? 0 : dgi::heads_probs_ld(V); }
+
+int dg_denoise_heads(const dg_dims* d, const uint16_t* h, int M, const uint16_t* draw_rows,
+                     int n_draw, const uint16_t* w, const float* inv_t, const float* inv_t_draw,
+                     float* lse, float* entropy, float* maxz, int32_t* argmax, float* lse_draw,
+                     float* prob_scale, uint16_t* probs, size_t probs_ld, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  if (!d || M < 1 || n_draw < 0 || n_draw > 16) return DG_ERR_ARG;
+  if (!dims_lm(d)) return DG_ERR_SHAPE;
+  if (!h || !w || !inv_t || !lse || !entropy || !maxz || !argmax || !prob_scale)
+    return DG_ERR_ARG;
+  if (n_draw > 0 && (!draw_rows || !inv_t_draw || !lse_draw)) return DG_ERR_ARG;
+  if (!aligned(h, 16) || !aligned(w, 16) || (n_draw > 0 && !aligned(draw_rows, 16)))
+    return DG_ERR_ARG;
+  if (probs && (probs_ld < (size_t)d->V || probs_ld % 64 || !aligned(probs, 16)))
+    return DG_ERR_ARG;
+  const size_t need = dg_workspace_bytes(d, DG_WS_HEADS, M);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DG_ERR_WORKSPACE;
+  return launch_result(dgi::denoise_heads(h, M, draw_rows, n_draw, w, d->V, d->d_model, inv_t,
+                                          inv_t_draw, dgi::RowStats{lse, entropy, maxz, argmax},
+                                          lse_draw, prob_scale, probs, probs_ld, workspace,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+int dg_selfcond_from_probs(const dg_dims* d, const uint16_t* probs, size_t probs_ld,
+                           const float* prob_scale, int M, const uint16_t* e_t, float* out,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  if (!d || M < 1) return DG_ERR_ARG;
+  if (!dims_lm(d) || d->V % 8) return DG_ERR_SHAPE;
+  if (!probs || !prob_scale || !e_t || !out) return DG_ERR_ARG;
+  if (probs_ld < (size_t)d->V || probs_ld % 8 || !aligned(probs, 16) || !aligned(e_t, 16) ||
+      !aligned(out, 16))
+    return DG_ERR_ARG;
+  const size_t need = dg_workspace_bytes(d, DG_WS_PROBS_EMBED, M);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DG_ERR_WORKSPACE;
+  return launch_result(dgi::probs_embed(probs, probs_ld, prob_scale, M, e_t, d->V, d->d_model,
+                                        out, workspace, static_cast<cudaStream_t>(stream)));
 }
 
 int dg_validate_slots(const dg_dims* d, const int32_t* slot_row, const int32_t* label_ids,

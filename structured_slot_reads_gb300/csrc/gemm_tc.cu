@@ -431,8 +431,10 @@ __global__ void stats_finalize_kernel(const float* part, int cpg, int M, const f
   }
 }
 
-// out[m][n] = sum over splits of part[s][m][n], splits added in order.
-__global__ void split_reduce_kernel(const float4* part, int k_split, long long n4, float4* out) {
+// out[m][n] = row_scale[m] * sum over splits of part[s][m][n], splits added in
+// order (row_scale may be null: 1).
+__global__ void split_reduce_kernel(const float4* part, int k_split, long long n4, int n_cols,
+                                    const float* row_scale, float4* out) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
        i += (long long)gridDim.x * blockDim.x) {
     float4 a = part[i];
@@ -442,6 +444,13 @@ __global__ void split_reduce_kernel(const float4* part, int k_split, long long n
       a.y += b.y;
       a.z += b.z;
       a.w += b.w;
+    }
+    if (row_scale) {
+      const float f = row_scale[(i * 4) / n_cols];
+      a.x *= f;
+      a.y *= f;
+      a.z *= f;
+      a.w *= f;
     }
     out[i] = a;
   }
@@ -567,28 +576,42 @@ cudaError_t selfcond(const uint16_t* h, int M, const uint16_t* w, const uint16_t
     if (e != cudaSuccess) return e;
   }
   // 2) split-K partials of P . E over the vocabulary, 3) ordered reduction
-  {
-    CUtensorMap ta, tb;
-    if (!make_tmap_bf16_2d(&ta, probs, V, M, (uint64_t)ldp * 2, BK, BM)) return cudaErrorInvalidValue;
-    if (!make_tmap_bf16_2d(&tb, e_t, V, D, (uint64_t)V * 2, BK, ACC_BN)) return cudaErrorInvalidValue;
-    GemmParams p{};
-    p.M = M;
-    p.N = D;
-    p.K = V;
-    p.n_tiles = (D + ACC_BN - 1) / ACC_BN;
-    accum_split(M, V, D, &p.k_split, &p.kb_per_split);
-    p.part = part;
-    p.status = status_ptr();
-    const int grid = groups * p.n_tiles * p.k_split;
-    cudaError_t e = (mt == 1) ? launch_gemm<1, ACC_BN, EPI_ACCUM>(ta, tb, p, grid, st)
-                              : launch_gemm<2, ACC_BN, EPI_ACCUM>(ta, tb, p, grid, st);
-    if (e != cudaSuccess) return e;
-    const long long n4 = (long long)M * D / 4;
-    const int blocks = (int)std::min<long long>((n4 + 255) / 256, 4LL * num_sms());
-    split_reduce_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(part), p.k_split,
-                                                n4, reinterpret_cast<float4*>(out));
-    return cudaGetLastError();
-  }
+  return probs_embed(reinterpret_cast<const uint16_t*>(probs), ldp, nullptr, M, e_t, V, D, out,
+                     part, st);
+}
+
+size_t probs_embed_ws_bytes(int M, int V, int D) {
+  int ks, kbps;
+  accum_split(M, V, D, &ks, &kbps);
+  return align_up((size_t)ks * M * D * sizeof(float), 256);
+}
+
+cudaError_t probs_embed(const uint16_t* probs, size_t ldp, const float* row_scale, int M,
+                        const uint16_t* e_t, int V, int D, float* out, void* ws,
+                        cudaStream_t st) {
+  const int mt = stats_mt(M);
+  const int groups = (M + mt * BM - 1) / (mt * BM);
+  float* part = static_cast<float*>(ws);
+  CUtensorMap ta, tb;
+  if (!make_tmap_bf16_2d(&ta, probs, V, M, (uint64_t)ldp * 2, BK, BM)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16_2d(&tb, e_t, V, D, (uint64_t)V * 2, BK, ACC_BN)) return cudaErrorInvalidValue;
+  GemmParams p{};
+  p.M = M;
+  p.N = D;
+  p.K = V;
+  p.n_tiles = (D + ACC_BN - 1) / ACC_BN;
+  accum_split(M, V, D, &p.k_split, &p.kb_per_split);
+  p.part = part;
+  p.status = status_ptr();
+  const int grid = groups * p.n_tiles * p.k_split;
+  cudaError_t e = (mt == 1) ? launch_gemm<1, ACC_BN, EPI_ACCUM>(ta, tb, p, grid, st)
+                            : launch_gemm<2, ACC_BN, EPI_ACCUM>(ta, tb, p, grid, st);
+  if (e != cudaSuccess) return e;
+  const long long n4 = (long long)M * D / 4;
+  const int blocks = (int)std::min<long long>((n4 + 255) / 256, 4LL * num_sms());
+  split_reduce_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(part), p.k_split,
+                                              n4, D, row_scale, reinterpret_cast<float4*>(out));
+  return cudaGetLastError();
 }
 
 }  // namespace dgi

@@ -1,0 +1,608 @@
+// heads_tc.cu -- the fused lm-head pass of one denoise step (one stream of W).
+//
+// For the canvas rows (tau-home.com "Refusing JSON token generation";
+// 24-ai.news "Token commit mechanism") the pass computes the row statistics of
+// softmax(h W^T / T) and, for self-conditioning, the unnormalised
+// probabilities  P~[i, v] = 2^(z_iv log2 e - r_i)  in bf16, where r_i is a
+// per-row reference that every CTA computes identically from the first 64
+// vocabulary entries (plus a fixed headroom).  Because r_i is common to all
+// CTAs, the per-CTA sums S_i = sum_v P~ add without rescaling and
+// p_iv = P~_iv / S_i exactly; the P.E GEMM applies 1/S_i in its reduction.
+//
+// For the slot-read draw rows (sotaaz.com "The server accepts at most 26
+// alternatives per question": noise reads of an answer slot) the same W tiles
+// feed a "swapped" MMA: A = the W tile (vocabulary on TMEM lanes), B = the
+// <= 16 draw rows (N = 16), so the draw rows' log-normalisers come out of the
+// same pass instead of a second stream of W.
+//
+// Tile geometry: BN vocabulary rows per tile (224 with draw rows so that
+// 2 x 224 canvas columns + 2 x 16 draw columns fill the 512 TMEM columns), 64-
+// element K blocks, 128-byte swizzled TMA tiles, one CTA per SM.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace {
+
+using namespace dgk;
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int PRO_N = 64;         // prologue vocabulary entries for the reference
+constexpr float REF_HEADROOM = 24.f;  // log2 units added to the prologue max
+constexpr float V_CLAMP = 100.f;      // exponent guard (log2 units above the reference)
+constexpr int DRAW_N = 16;
+constexpr int STAGE_BUDGET = 212992;  // 208 KB of operand stages
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void epi_bar(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+struct HeadsParams {
+  int M;        // canvas rows
+  int n_draw;   // draw rows (0..16)
+  int V, K;
+  int cpg, n_tiles;
+  const float* inv_t;       // [M]
+  const float* inv_t_draw;  // [n_draw]
+  float* part;              // canvas: 4 planes of [M][cpg]: s, t, best, idx
+  float* part_draw;         // draws: 2 planes of [n_draw][cpg]: m, s
+  float* ref;               // [M] reference r (log2 units)
+  __nv_bfloat16* probs;     // [M][ldp] or null
+  long long ldp;
+  int* status;
+};
+
+template <int MT, int BN, bool DRAWS>
+struct HCfg {
+  static constexpr int A_BYTES = BM * BK * 2;           // 16 KB per canvas M-tile
+  static constexpr int B_REGION = 256 * BK * 2;         // W tile region (BN rows loaded)
+  static constexpr int D_BYTES = DRAWS ? DRAW_N * BK * 2 : 0;
+  static constexpr int STAGE_BYTES = MT * A_BYTES + B_REGION + D_BYTES;
+  static constexpr int NSTAGE = (STAGE_BUDGET / STAGE_BYTES) > 8 ? 8 : STAGE_BUDGET / STAGE_BYTES;
+  static constexpr int DRAW_COLS = DRAWS ? 2 * DRAW_N : 0;
+  static constexpr int ACC_COLS = MT * BN + DRAW_COLS;
+  static constexpr int ACC_STAGES = (2 * ACC_COLS <= 512) ? 2 : 1;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int EPI_WARPS = 4 * MT;
+  static constexpr int THREADS = (EPI_WARPS + 2) * 32;
+  static constexpr int BAR_BYTES = 256 + EPI_WARPS * DRAW_N * 8;
+  static constexpr int SMEM_BYTES = 1024 + NSTAGE * STAGE_BYTES + BAR_BYTES;
+  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+  static constexpr uint32_t IDESC_PRO = idesc_bf16_f32(BM, PRO_N);
+  static constexpr uint32_t IDESC_DRAW = idesc_bf16_f32(BM, DRAW_N);
+  static constexpr uint32_t TX_TILE = MT * A_BYTES + BN * BK * 2 + D_BYTES;
+  static constexpr uint32_t TX_PRO = MT * A_BYTES + PRO_N * BK * 2;
+  static_assert(ACC_COLS <= 512, "accumulators exceed tensor memory");
+  static_assert(BN % 32 == 0 && BN <= 256 && BN >= PRO_N, "BN");
+  static_assert(!DRAWS || BN >= 128, "the swapped draw MMA reads two 128-row halves");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+template <int MT, int BN, bool DRAWS>
+__global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
+    heads_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ CUtensorMap tmB64,
+                 const __grid_constant__ CUtensorMap tmD, HeadsParams p) {
+  using CF = HCfg<MT, BN, DRAWS>;
+  constexpr int NSTAGE = CF::NSTAGE;
+  constexpr int PRODUCER_WARP = CF::EPI_WARPS;
+  constexpr int MMA_WARP = CF::EPI_WARPS + 1;
+  constexpr int EPI_THREADS = CF::EPI_WARPS * 32;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* stages = smem;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + NSTAGE * CF::STAGE_BYTES);
+  uint64_t* empty_bar = full_bar + NSTAGE;
+  uint64_t* tfull_bar = empty_bar + NSTAGE;
+  uint64_t* tempty_bar = tfull_bar + CF::ACC_STAGES;
+  uint64_t* drain_bar = tempty_bar + CF::ACC_STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* draw_red = reinterpret_cast<float*>(smem + NSTAGE * CF::STAGE_BYTES + 256);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NSTAGE; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    for (int a = 0; a < CF::ACC_STAGES; ++a) {
+      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tempty_bar[a], CF::EPI_WARPS);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc(tmem_slot, CF::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == PRODUCER_WARP && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmB64);
+    if (DRAWS) prefetch_tmap(&tmD);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // tile -1 is the reference prologue (vocabulary 0..63, canvas rows only)
+  const int total_kb = (p.K + BK - 1) / BK;
+  const int gm = blockIdx.x / p.cpg;
+  const int gn = blockIdx.x % p.cpg;
+  const int t_begin = (int)((long long)gn * p.n_tiles / p.cpg);
+  const int t_end = (int)((long long)(gn + 1) * p.n_tiles / p.cpg);
+  const int m_base = gm * MT * BM;
+  const bool draws_here = DRAWS && gm == 0 && p.n_draw > 0;
+
+  if (warp == PRODUCER_WARP) {
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_h = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0, issued_mask = 0, last_phase = 0;
+      bool ok = true;
+      for (int t = t_begin - 1; t < t_end && ok; ++t) {
+        const bool pro = t < t_begin;
+        for (int kb = 0; kb < total_kb; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* s_a = stages + stage * CF::STAGE_BYTES;
+          uint8_t* s_b = s_a + MT * CF::A_BYTES;
+          if (pro) {
+            mbar_arrive_expect_tx(&full_bar[stage], CF::TX_PRO);
+            tma_load_2d_hint(s_b, &tmB64, &full_bar[stage], kb * BK, 0, pol_h);
+          } else {
+            mbar_arrive_expect_tx(&full_bar[stage],
+                                  draws_here ? CF::TX_TILE : CF::TX_TILE - CF::D_BYTES);
+            tma_load_2d_hint(s_b, &tmB, &full_bar[stage], kb * BK, t * BN, pol_w);
+            if (draws_here)
+              tma_load_2d_hint(s_b + CF::B_REGION, &tmD, &full_bar[stage], kb * BK, 0, pol_h);
+          }
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt)
+            tma_load_2d_hint(s_a + mt * CF::A_BYTES, &tmA, &full_bar[stage], kb * BK,
+                             m_base + mt * BM, pol_h);
+          issued_mask |= 1u << stage;
+          last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == NSTAGE) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < NSTAGE; ++s)
+          if (issued_mask & (1u << s)) mbar_wait_drain(&full_bar[s], (last_phase >> s) & 1u);
+      }
+    }
+  } else if (warp == MMA_WARP) {
+    if (lane == 0) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int t = t_begin - 1; t < t_end && ok; ++t) {
+        const bool pro = t < t_begin;
+        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_base = tmem_base + acc * CF::ACC_COLS;
+        for (int kb = 0; kb < total_kb; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(stages + stage * CF::STAGE_BYTES);
+          const uint32_t b_addr = a_addr + MT * CF::A_BYTES;
+          const uint32_t d_addr = b_addr + CF::B_REGION;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint32_t acc_flag = (kb > 0 || kk > 0) ? 1u : 0u;
+            const uint64_t bdesc = sw128_kmajor_desc(b_addr + kk * 32);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+              const uint64_t adesc = sw128_kmajor_desc(a_addr + mt * CF::A_BYTES + kk * 32);
+              tc_mma_f16(d_base + mt * BN, adesc, bdesc, pro ? CF::IDESC_PRO : CF::IDESC,
+                         acc_flag);
+            }
+            if (DRAWS && draws_here && !pro) {
+              const uint64_t ddesc = sw128_kmajor_desc(d_addr + kk * 32);
+#pragma unroll
+              for (int half = 0; half < 2; ++half) {
+                const uint64_t wdesc = sw128_kmajor_desc(b_addr + half * CF::A_BYTES + kk * 32);
+                tc_mma_f16(d_base + MT * BN + half * DRAW_N, wdesc, ddesc, CF::IDESC_DRAW,
+                           acc_flag);
+              }
+            }
+          }
+          tc_commit(&empty_bar[stage]);
+          if (++stage == NSTAGE) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&tfull_bar[acc]);
+        if (++acc == CF::ACC_STAGES) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      tc_commit(drain_bar);
+      mbar_wait_drain(drain_bar, 0);
+    }
+  } else {
+    // ---- epilogue warps -----------------------------------------------------
+    const int mt = warp >> 2;
+    const int quarter = warp & 3;
+    const int row = m_base + mt * BM + quarter * 32 + lane;
+    const bool row_ok = row < p.M;
+    const float scale = row_ok ? __ldg(p.inv_t + row) * LOG2E : 0.f;
+    float r_ref = 0.f;
+    float s_run = 0.f, t_run = 0.f, best = -INFINITY;
+    int best_idx = 0x7fffffff;
+    bool clamped = false;
+    // draw-row running statistics: lane = vocabulary row of a half tile
+    float dm[DRAW_N], ds[DRAW_N], dscale[DRAW_N];
+#pragma unroll
+    for (int j = 0; j < DRAW_N; ++j) {
+      dm[j] = -INFINITY;
+      ds[j] = 0.f;
+      dscale[j] = (DRAWS && j < p.n_draw) ? __ldg(p.inv_t_draw + j) * LOG2E : 0.f;
+    }
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = t_begin - 1; t < t_end; ++t) {
+      const bool pro = t < t_begin;
+      if (!mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, p.status)) break;
+      tc_fence_after();
+      const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+      const uint32_t taddr = tmem_base + lane_base + acc * CF::ACC_COLS + mt * BN;
+      if (pro) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < PRO_N / 32; ++c) {
+          uint32_t r[32];
+          __syncwarp();
+          tmem_ld_32x32b_x32(taddr + c * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(r[j]));
+        }
+        r_ref = mx * scale + REF_HEADROOM;
+        if (row_ok && gn == 0) p.ref[row] = r_ref;
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          __syncwarp();
+          tmem_ld_32x32b_x32(taddr + c * 32, r);
+          tmem_ld_wait();
+          const int n0 = t * BN + c * 32;
+          if (!row_ok || n0 >= p.V) continue;
+          const bool full = n0 + 32 <= p.V;
+          float cmax = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (full || n0 + j < p.V) cmax = fmaxf(cmax, __uint_as_float(r[j]));
+          if (cmax > best) {  // columns ascend, so the first occurrence is the lowest id
+            int first = 0x7fffffff;
+#pragma unroll
+            for (int j = 31; j >= 0; --j)
+              if ((full || n0 + j < p.V) && __uint_as_float(r[j]) == cmax) first = n0 + j;
+            best = cmax;
+            best_idx = first;
+          }
+          if (fmaf(cmax, scale, -r_ref) > V_CLAMP) clamped = true;
+          float e[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float a = __uint_as_float(r[j]);
+            const float v = fminf(fmaf(a, scale, -r_ref), V_CLAMP);
+            const bool ok = full || n0 + j < p.V;
+            e[j] = ok ? ex2(v) : 0.f;
+            s_run += e[j];
+            t_run = fmaf(e[j], a, t_run);
+          }
+          if (p.probs) {
+            __nv_bfloat16* dst = p.probs + (long long)row * p.ldp + n0;
+            if (full) {
+#pragma unroll
+              for (int j = 0; j < 32; j += 8) {
+                uint4 pk;
+                __nv_bfloat162 b0 = __floats2bfloat162_rn(e[j + 0], e[j + 1]);
+                __nv_bfloat162 b1 = __floats2bfloat162_rn(e[j + 2], e[j + 3]);
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(e[j + 4], e[j + 5]);
+                __nv_bfloat162 b3 = __floats2bfloat162_rn(e[j + 6], e[j + 7]);
+                pk.x = *reinterpret_cast<uint32_t*>(&b0);
+                pk.y = *reinterpret_cast<uint32_t*>(&b1);
+                pk.z = *reinterpret_cast<uint32_t*>(&b2);
+                pk.w = *reinterpret_cast<uint32_t*>(&b3);
+                *reinterpret_cast<uint4*>(dst + j) = pk;
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (n0 + j < p.V) dst[j] = __float2bfloat16_rn(e[j]);
+            }
+          }
+        }
+        if (DRAWS && draws_here) {
+          // warpgroup mt handles half mt (with one M-tile, warpgroup 0 does both)
+#pragma unroll
+          for (int hh = 0; hh < (MT == 1 ? 2 : 1); ++hh) {
+            const int half = (MT == 1) ? hh : mt;
+            uint32_t r[DRAW_N];
+            __syncwarp();
+            tmem_ld_32x32b_x16(
+                tmem_base + lane_base + acc * CF::ACC_COLS + MT * BN + half * DRAW_N, r);
+            tmem_ld_wait();
+            const int vl = half * 128 + quarter * 32 + lane;  // row within the W tile
+            const int vocab = t * BN + vl;
+            if (vl < BN && vocab < p.V) {
+#pragma unroll
+              for (int j = 0; j < DRAW_N; ++j) {
+                if (j < p.n_draw) {
+                  const float v = __uint_as_float(r[j]) * dscale[j];
+                  const float mn = fmaxf(dm[j], v);
+                  ds[j] = ds[j] * ex2(dm[j] - mn) + ex2(v - mn);
+                  dm[j] = mn;
+                }
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+      if (++acc == CF::ACC_STAGES) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (row_ok) {
+      const long long o = (long long)row * p.cpg + gn;
+      const long long plane = (long long)p.cpg * p.M;
+      p.part[o] = s_run;
+      p.part[o + plane] = t_run;
+      p.part[o + 2 * plane] = best;
+      reinterpret_cast<int*>(p.part)[o + 3 * plane] = best_idx;
+      if (clamped) atomicOr(p.status, 16 /* DG_DEV_RANGE */);
+    }
+    if (DRAWS && draws_here) {
+      // merge the draw statistics over the lanes, then over the epilogue warps
+#pragma unroll
+      for (int j = 0; j < DRAW_N; ++j) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float mo = __shfl_xor_sync(0xffffffffu, dm[j], o);
+          const float so = __shfl_xor_sync(0xffffffffu, ds[j], o);
+          const float mn = fmaxf(dm[j], mo);
+          ds[j] = (mn == -INFINITY) ? 0.f : ds[j] * ex2(dm[j] - mn) + so * ex2(mo - mn);
+          dm[j] = mn;
+        }
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int j = 0; j < DRAW_N; ++j) {
+          draw_red[(warp * DRAW_N + j) * 2] = dm[j];
+          draw_red[(warp * DRAW_N + j) * 2 + 1] = ds[j];
+        }
+      }
+      epi_bar(EPI_THREADS);
+      if (warp == 0 && lane < p.n_draw) {
+        const int j = lane;
+        float m = -INFINITY, s = 0.f;
+        for (int w = 0; w < CF::EPI_WARPS; ++w) {
+          const float mo = draw_red[(w * DRAW_N + j) * 2];
+          const float so = draw_red[(w * DRAW_N + j) * 2 + 1];
+          const float mn = fmaxf(m, mo);
+          s = (mn == -INFINITY) ? 0.f : s * ex2(m - mn) + so * ex2(mo - mn);
+          m = mn;
+        }
+        const long long o = (long long)j * p.cpg + gn;
+        p.part_draw[o] = m;
+        p.part_draw[o + (long long)p.n_draw * p.cpg] = s;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == MMA_WARP) tmem_dealloc(tmem_base, CF::TMEM_COLS);
+}
+
+// Canvas rows: S = sum of the CTA sums (common reference), one warp per row.
+__global__ void heads_finalize_kernel(const float* part, int cpg, int M, const float* inv_t,
+                                      const float* ref, float* lse, float* entropy, float* maxz,
+                                      int32_t* argmax, float* prob_scale) {
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= M) return;
+  const long long plane = (long long)cpg * M;
+  const float* pm = part + (long long)row * cpg;
+  float s = 0.f, t = 0.f, best = -INFINITY;
+  int idx = 0x7fffffff;
+  for (int g = lane; g < cpg; g += 32) {
+    s += pm[g];
+    t += pm[g + plane];
+    const float bg = pm[g + 2 * plane];
+    const int ig = reinterpret_cast<const int*>(pm)[g + 3 * plane];
+    if (bg > best || (bg == best && ig < idx)) {
+      best = bg;
+      idx = ig;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    s += __shfl_xor_sync(0xffffffffu, s, o);
+    t += __shfl_xor_sync(0xffffffffu, t, o);
+    const float bo = __shfl_xor_sync(0xffffffffu, best, o);
+    const int io = __shfl_xor_sync(0xffffffffu, idx, o);
+    if (bo > best || (bo == best && io < idx)) {
+      best = bo;
+      idx = io;
+    }
+  }
+  if (lane == 0) {
+    const float it = inv_t[row];
+    const float l = (ref[row] + log2f(s)) * LN2;
+    lse[row] = l;
+    entropy[row] = l - it * (t / s);
+    maxz[row] = best * it;
+    argmax[row] = idx;
+    if (prob_scale) prob_scale[row] = 1.f / s;
+  }
+}
+
+// Draw rows: merge (max, sum) pairs over CTAs, one warp per draw row.
+__global__ void draws_finalize_kernel(const float* part_draw, int cpg, int n_draw,
+                                      float* lse_draw) {
+  const int j = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (j >= n_draw) return;
+  const float* pm = part_draw + (long long)j * cpg;
+  const float* ps = part_draw + (long long)n_draw * cpg + (long long)j * cpg;
+  float m = -INFINITY;
+  for (int g = lane; g < cpg; g += 32) m = fmaxf(m, pm[g]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float s = 0.f;
+  for (int g = lane; g < cpg; g += 32)
+    if (pm[g] != -INFINITY) s += ps[g] * exp2f(pm[g] - m);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) lse_draw[j] = (m + log2f(s)) * LN2;
+}
+
+template <int MT, int BN, bool DRAWS>
+cudaError_t launch_heads(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb64,
+                         const CUtensorMap& td, const HeadsParams& p, int grid, cudaStream_t st) {
+  using CF = HCfg<MT, BN, DRAWS>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(heads_kernel<MT, BN, DRAWS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         CF::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  heads_kernel<MT, BN, DRAWS><<<grid, CF::THREADS, CF::SMEM_BYTES, st>>>(ta, tb, tb64, td, p);
+  return cudaGetLastError();
+}
+
+int heads_bn(int n_draw) { return n_draw > 0 ? 224 : 256; }
+int heads_mt(int M) { return M <= BM ? 1 : 2; }
+
+int heads_cpg(int M, int V, int n_draw) {
+  const int mt = heads_mt(M);
+  const int groups = (M + mt * BM - 1) / (mt * BM);
+  const int bn = heads_bn(n_draw);
+  const int n_tiles = (V + bn - 1) / bn;
+  return std::min(std::max(1, dgi::num_sms() / groups), n_tiles);
+}
+
+}  // namespace
+
+namespace dgi {
+
+size_t heads_ws_bytes(int M, int V, int n_draw) {
+  const int cpg = heads_cpg(M, V, n_draw);
+  return align_up((size_t)4 * cpg * M * 4, 256) + align_up((size_t)2 * cpg * DRAW_N * 4, 256) +
+         align_up((size_t)M * 4, 256);
+}
+
+size_t heads_probs_ld(int V) { return align_up((size_t)V, 64); }
+
+cudaError_t denoise_heads(const uint16_t* h, int M, const uint16_t* draw_rows, int n_draw,
+                          const uint16_t* w, int V, int D, const float* inv_t,
+                          const float* inv_t_draw, RowStats out, float* lse_draw,
+                          float* prob_scale, uint16_t* probs, size_t probs_ld, void* ws,
+                          cudaStream_t st) {
+  const int mt = heads_mt(M);
+  const int groups = (M + mt * BM - 1) / (mt * BM);
+  const int bn = heads_bn(n_draw);
+  HeadsParams p{};
+  p.M = M;
+  p.n_draw = n_draw;
+  p.V = V;
+  p.K = D;
+  p.cpg = heads_cpg(M, V, n_draw);
+  p.n_tiles = (V + bn - 1) / bn;
+  p.inv_t = inv_t;
+  p.inv_t_draw = inv_t_draw;
+  uint8_t* wp = static_cast<uint8_t*>(ws);
+  p.part = reinterpret_cast<float*>(wp);
+  wp += align_up((size_t)4 * p.cpg * M * 4, 256);
+  p.part_draw = reinterpret_cast<float*>(wp);
+  wp += align_up((size_t)2 * p.cpg * DRAW_N * 4, 256);
+  p.ref = reinterpret_cast<float*>(wp);
+  p.probs = reinterpret_cast<__nv_bfloat16*>(probs);
+  p.ldp = (long long)probs_ld;
+  p.status = status_ptr();
+  CUtensorMap ta, tb, tb64, td;
+  if (!make_tmap_bf16_2d(&ta, h, D, M, (uint64_t)D * 2, BK, BM)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16_2d(&tb, w, D, V, (uint64_t)D * 2, BK, bn)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16_2d(&tb64, w, D, V, (uint64_t)D * 2, BK, PRO_N)) return cudaErrorInvalidValue;
+  if (n_draw > 0) {
+    if (!make_tmap_bf16_2d(&td, draw_rows, D, n_draw, (uint64_t)D * 2, BK, DRAW_N))
+      return cudaErrorInvalidValue;
+  } else {
+    td = tb64;  // unused
+  }
+  const int grid = groups * p.cpg;
+  cudaError_t e;
+  if (n_draw > 0)
+    e = (mt == 1) ? launch_heads<1, 224, true>(ta, tb, tb64, td, p, grid, st)
+                  : launch_heads<2, 224, true>(ta, tb, tb64, td, p, grid, st);
+  else
+    e = (mt == 1) ? launch_heads<1, 256, false>(ta, tb, tb64, td, p, grid, st)
+                  : launch_heads<2, 256, false>(ta, tb, tb64, td, p, grid, st);
+  if (e != cudaSuccess) return e;
+  heads_finalize_kernel<<<(M + 7) / 8, 256, 0, st>>>(p.part, p.cpg, M, inv_t, p.ref, out.lse,
+                                                     out.entropy, out.maxz, out.argmax,
+                                                     prob_scale);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || n_draw == 0) return e;
+  draws_finalize_kernel<<<(n_draw + 7) / 8, 256, 0, st>>>(p.part_draw, p.cpg, n_draw, lse_draw);
+  return cudaGetLastError();
+}
+
+}  // namespace dgi

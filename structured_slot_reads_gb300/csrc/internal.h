@@ -33,6 +33,21 @@ cudaError_t selfcond(const uint16_t* h, int M, const uint16_t* w, const uint16_t
                      int D, const float* inv_t, const float* lse, float* out, void* ws,
                      cudaStream_t st);
 
+// P . E from bf16 probabilities (optionally unnormalised, times row_scale).
+size_t probs_embed_ws_bytes(int M, int V, int D);
+cudaError_t probs_embed(const uint16_t* probs, size_t ldp, const float* row_scale, int M,
+                        const uint16_t* e_t, int V, int D, float* out, void* ws,
+                        cudaStream_t st);
+
+// ---- fused lm-head pass of a step (heads_tc.cu) ------------------------------
+size_t heads_ws_bytes(int M, int V, int n_draw);
+size_t heads_probs_ld(int V);
+cudaError_t denoise_heads(const uint16_t* h, int M, const uint16_t* draw_rows, int n_draw,
+                          const uint16_t* w, int V, int D, const float* inv_t,
+                          const float* inv_t_draw, RowStats out, float* lse_draw,
+                          float* prob_scale, uint16_t* probs, size_t probs_ld, void* ws,
+                          cudaStream_t st);
+
 // ---- attention (attn.cu) ---------------------------------------------------
 struct AttnArgs {
   int B, C, Pmax, Hq, Hkv, d, W;

@@ -57,6 +57,9 @@ _SIGS = {
                      P],
     "dg_commit": [DP, P, P, P, P, P, P, P, P, P, P],
     "dg_selfcond_embed": [DP, P, I, P, P, P, P, P, P, Z, P],
+    "dg_denoise_heads": [DP, P, I, P, I, P, P, P, P, P, P, P, P, P, P, Z, P, Z, P],
+    "dg_selfcond_from_probs": [DP, P, Z, P, I, P, P, P, Z, P],
+    "dg_probs_ld": [I],
     "dg_transpose_bf16": [P, I, I, P, P],
     "dg_canvas_update": [DP, P, P, P, P, P, I, P, P],
     "dg_philox_fill": [U64, P, I, P, P],
@@ -67,7 +70,7 @@ _SIGS = {
     "dg_strerror": [I],
     "dg_num_sms": [],
 }
-_RES = {"dg_workspace_bytes": Z, "dg_strerror": ctypes.c_char_p}
+_RES = {"dg_workspace_bytes": Z, "dg_strerror": ctypes.c_char_p, "dg_probs_ld": Z}
 
 
 def lib():
@@ -175,6 +178,25 @@ def dg_selfcond_embed(dims, h, M, w, e_t, inv_t, lse, out, workspace, stream=Non
     return lib().dg_selfcond_embed(ctypes.byref(dims), _p(h), M, _p(w), _p(e_t), _p(inv_t),
                                    _p(lse), _p(out), _p(workspace), _nbytes(workspace),
                                    _s(stream))
+
+
+def dg_denoise_heads(dims, h, M, draw_rows, n_draw, w, inv_t, inv_t_draw, lse, entropy, maxz,
+                     argmax, lse_draw, prob_scale, probs, probs_ld, workspace, stream=None):
+    return lib().dg_denoise_heads(ctypes.byref(dims), _p(h), M, _p(draw_rows), n_draw, _p(w),
+                                  _p(inv_t), _p(inv_t_draw), _p(lse), _p(entropy), _p(maxz),
+                                  _p(argmax), _p(lse_draw), _p(prob_scale), _p(probs), probs_ld,
+                                  _p(workspace), _nbytes(workspace), _s(stream))
+
+
+def dg_selfcond_from_probs(dims, probs, probs_ld, prob_scale, M, e_t, out, workspace,
+                           stream=None):
+    return lib().dg_selfcond_from_probs(ctypes.byref(dims), _p(probs), probs_ld, _p(prob_scale),
+                                        M, _p(e_t), _p(out), _p(workspace), _nbytes(workspace),
+                                        _s(stream))
+
+
+def dg_probs_ld(V):
+    return int(lib().dg_probs_ld(V))
 
 
 def dg_transpose_bf16(src, rows, cols, dst, stream=None):

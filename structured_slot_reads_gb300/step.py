@@ -23,7 +23,7 @@ def _empty(shape, dtype, device):
 
 
 class DenoiseStep:
-    def __init__(self, shape, w, e, e_t, device="cuda", with_slots=True, seed=0):
+    def __init__(self, shape, w, e, e_t, device="cuda", with_slots=True, seed=0, fused=True):
         self.shape = shape
         self.dims = dg.dims_of(shape)
         self.device = device
@@ -79,6 +79,20 @@ class DenoiseStep:
             self.noise_tok = _empty((S, shape.R), i32, dev)
             self.ws_slot = _empty((dg.dg_workspace_bytes(self.dims, dg.DG_WS_SLOT_READ,
                                                          S * shape.R),), u8, dev)
+        # fused path: one stream of W for the canvas rows, the slot draws and
+        # the self-conditioning probabilities
+        self.n_draw = self.S * shape.R if self.with_slots else 0
+        self.fused = fused and self.n_draw <= 16
+        if self.fused:
+            nd = max(self.n_draw, 1)
+            self.draw_rows = _empty((nd, D), bf, dev)
+            self.inv_t_draw = _empty((nd,), f32, dev)
+            self.lse_draw = _empty((nd,), f32, dev)
+            self.probs_ld = dg.dg_probs_ld(V)
+            self.probs = _empty((self.M, self.probs_ld), bf, dev)
+            self.prob_scale = _empty((self.M,), f32, dev)
+            self.ws_heads = _empty((dg.dg_workspace_bytes(self.dims, dg.DG_WS_HEADS, self.M),), u8, dev)
+            self.ws_pe = _empty((dg.dg_workspace_bytes(self.dims, dg.DG_WS_PROBS_EMBED, self.M),), u8, dev)
 
     # ------------------------------------------------------------------ step
     def reset_state(self):
@@ -93,6 +107,8 @@ class DenoiseStep:
         ck(dg.dg_attn_decode(d, self.q, self.kc, self.vc, self.kenc, self.venc, None, 0, 0, 0,
                              self.prompt_len, self.attn_out, self.attn_lse, self.ws_attn, stream),
            "dg_attn_decode")
+        if self.fused:
+            return self._run_fused(step_idx, stream)
         ck(dg.dg_lmhead_logsoftmax_entropy(d, self.h, self.M, self.w, self.inv_t, self.lse,
                                            self.ent, self.maxz, self.argmax, self.ws_lm, stream),
            "dg_lmhead_logsoftmax_entropy")
@@ -111,10 +127,42 @@ class DenoiseStep:
                                self.M, self.h, stream), "dg_canvas_update")
         return self.kernels_per_step()
 
+    def _run_fused(self, step_idx, stream):
+        s, d = self.shape, self.dims
+        ck = dg._check
+        if self.with_slots:
+            ck(dg.dg_slot_noise(d, self.h, self.M, self.e, self.inv_t, self.slot_row,
+                                self.slot_req, self.S, s.R, self.seed, step_idx, self.draw_rows,
+                                self.inv_t_draw, self.noise_tok, stream), "dg_slot_noise")
+        ck(dg.dg_denoise_heads(d, self.h, self.M, self.draw_rows if self.n_draw else None,
+                               self.n_draw, self.w, self.inv_t, self.inv_t_draw, self.lse,
+                               self.ent, self.maxz, self.argmax, self.lse_draw, self.prob_scale,
+                               self.probs, self.probs_ld, self.ws_heads, stream),
+           "dg_denoise_heads")
+        if self.with_slots:
+            ck(dg.dg_slot_finish(d, self.draw_rows, self.inv_t_draw, self.lse_draw, self.w,
+                                 self.label_ids, self.n_labels, self.S, s.R, s.R, s.gate,
+                                 self.q_avg, self.h_slot, self.chosen, self.lp_draws,
+                                 self.resampled, self.n_reads, stream), "dg_slot_finish")
+        ck(dg.dg_commit(d, self.ent, self.argmax, self.cand, self.gamma, self.committed,
+                        self.tok_state, self.commit, self.tokens, self.n_commit, stream),
+           "dg_commit")
+        ck(dg.dg_selfcond_from_probs(d, self.probs, self.probs_ld, self.prob_scale, self.M,
+                                     self.e_t, self.e_sc, self.ws_pe, stream),
+           "dg_selfcond_from_probs")
+        ck(dg.dg_canvas_update(d, self.h0, self.e_sc, self.e, self.tok_state, self.committed,
+                               self.M, self.h, stream), "dg_canvas_update")
+        return self.kernels_per_step()
+
     def kernels_per_step(self):
-        """Library kernels one step launches (attention + combine, stats + finalize,
-        noise + stats + finalize + finish, commit, probs + accum + reduce, update)."""
+        """Library kernels one step launches."""
         n = 1 + (1 if self._attn_splits() > 1 else 0)
+        if self.fused:
+            # [noise] + heads + finalize + [draw finalize] + [finish] + commit + accum + reduce + update
+            n += 2 + 1 + 2 + 1
+            n += 3 if self.with_slots else 0
+            return n
+        # stats + finalize, [noise + stats + finalize + finish], commit, probs + accum + reduce, update
         n += 2
         n += 4 if self.with_slots else 0
         n += 1 + 3 + 1

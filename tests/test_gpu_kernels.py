@@ -226,3 +226,79 @@ def test_status_word_clean_after_valid_calls():
     dg.dg_clear_status()
     test_slot_noise_rows_bit_exact()
     assert dg.dg_get_status() == 0
+
+
+def _run_heads(h, draws, w, inv_t, inv_t_draw, with_probs=True):
+    M, D = h.shape
+    V = w.shape[0]
+    nd = 0 if draws is None else draws.shape[0]
+    d = dg.make_dims(d_model=D, V=V)
+    f32 = torch.float32
+    lse, ent, maxz = (torch.empty(M, dtype=f32, device="cuda") for _ in range(3))
+    arg = torch.empty(M, dtype=torch.int32, device="cuda")
+    lse_d = torch.empty(max(nd, 1), dtype=f32, device="cuda")
+    scale = torch.empty(M, dtype=f32, device="cuda")
+    ld = dg.dg_probs_ld(V)
+    probs = torch.empty((M, ld), dtype=torch.bfloat16, device="cuda") if with_probs else None
+    ws = torch.empty(dg.dg_workspace_bytes(d, dg.DG_WS_HEADS, M), dtype=torch.uint8, device="cuda")
+    rc = dg.dg_denoise_heads(d, dev_bf16(h), M, dev_bf16(draws) if nd else None, nd, dev_bf16(w),
+                             dev(inv_t), dev(inv_t_draw) if nd else None, lse, ent, maxz, arg,
+                             lse_d if nd else None, scale, probs, ld, ws)
+    assert rc == dg.DG_OK, dg.strerror(rc)
+    torch.cuda.synchronize()
+    return dict(lse=host(lse), ent=host(ent), maxz=host(maxz), arg=host(arg),
+                lse_draw=host(lse_d)[:nd], scale=scale, probs=probs, ld=ld, dims=d)
+
+
+@pytest.mark.parametrize("M,nd,V,D", [(256, 12, 8192, 512), (100, 5, 3000, 200),
+                                      (300, 12, 2048, 128), (64, 0, 4096, 256), (1, 16, 1024, 128)])
+def test_denoise_heads_fused_pass(M, nd, V, D):
+    h, w, e, inv_t = _lm_inputs(M, V, D, seed=31 + M)
+    draws = inputs.hidden(nd, D, 99) if nd else None
+    inv_d = inputs.inv_temperature(nd, 98) if nd else None
+    got = _run_heads(h, draws, w, inv_t, inv_d)
+    o_lse, o_ent, o_maxz, o_arg = oracle.lmhead_stats(h, w, inv_t)
+    assert_abs(got["lse"], o_lse, what="lse")
+    assert_abs(got["ent"], o_ent, what="entropy")
+    assert_abs(got["maxz"], o_maxz, what="max logit")
+    z = (h.astype(np.float64) @ w.astype(np.float64).T) * inv_t[:, None]
+    clear = top2_gap(z) > 1e-3
+    assert np.array_equal(got["arg"][clear], o_arg[clear])
+    if nd:
+        d_lse, _, _, _ = oracle.lmhead_stats(draws, w, inv_d)
+        assert_abs(got["lse_draw"], d_lse, what="draw-row lse")
+    # the probabilities, normalised, are the softmax
+    p = host(got["probs"])[:, :V].astype(np.float64) * host(got["scale"])[:, None]
+    ref_p = np.exp(z - o_lse[:, None])
+    np.testing.assert_allclose(p.sum(axis=1), 1.0, atol=5e-3)
+    assert np.max(np.abs(p - ref_p) / (ref_p + 1e-30)) < 1e-2
+    # and feed the expected embedding
+    ed = dev_bf16(e)
+    e_t = torch.empty((D, V), dtype=torch.bfloat16, device="cuda")
+    assert dg.dg_transpose_bf16(ed, V, D, e_t) == dg.DG_OK
+    out = torch.empty((M, D), dtype=torch.float32, device="cuda")
+    ws = torch.empty(dg.dg_workspace_bytes(got["dims"], dg.DG_WS_PROBS_EMBED, M),
+                     dtype=torch.uint8, device="cuda")
+    rc = dg.dg_selfcond_from_probs(got["dims"], got["probs"], got["ld"], got["scale"], M, e_t,
+                                   out, ws)
+    assert rc == dg.DG_OK
+    torch.cuda.synchronize()
+    assert_rel(host(out), oracle.selfcond_embed(h, w, e, inv_t), what="expected embedding")
+
+
+def test_denoise_heads_flags_out_of_range_logits():
+    M, V, D = 8, 2048, 128
+    h, w, _, inv_t = _lm_inputs(M, V, D, seed=5)
+    # row 3: one logit far above everything in the first 64 vocabulary entries
+    wl = w[1000].astype(np.float64)
+    x = h[3].astype(np.float64) + (200.0 / float(inv_t[3])) * wl / np.dot(wl, wl)
+    h[3] = inputs.to_bf16(x.astype(np.float32))
+    dg.dg_clear_status()
+    got = _run_heads(h, None, w, inv_t, None)
+    assert dg.dg_get_status() & 16
+    dg.dg_clear_status()
+    # the exact recomputing path is unaffected
+    o_lse, _, _, o_arg = oracle.lmhead_stats(h, w, inv_t)
+    lse, _, _, arg = _run_lmhead(h, w, inv_t)
+    assert_abs(lse, o_lse, what="lse (recomputing path)")
+    assert arg[3] == 1000 and got["arg"][3] == 1000
