@@ -19,8 +19,10 @@ DG_ERR_SHAPE = -4
 DG_ERR_CUDA = -5
 DG_ERR_WORKSPACE = -6
 DG_DEV_TIMEOUT, DG_DEV_BAD_PAGE, DG_DEV_BAD_LABEL, DG_DEV_BAD_INDEX = 1, 2, 4, 8
+DG_DEV_RANGE = 16
 DG_WS_ATTN, DG_WS_LMHEAD, DG_WS_SLOT_READ, DG_WS_SELFCOND = 1, 2, 3, 4
-MAX_LABELS = 26
+DG_WS_HEADS, DG_WS_PROBS_EMBED = 5, 6
+DG_MAX_LABELS = MAX_LABELS = 26
 
 
 class DgError(RuntimeError):

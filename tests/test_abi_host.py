@@ -123,3 +123,28 @@ def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(dg, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         dg.lib()
+
+
+def test_binding_constants_match_header():
+    text = open(HEADER).read()
+    defs = re.findall(r"#define\s+(DG_[A-Z0-9_]+)\s+\(?(-?\d+)\)?", text)
+    assert len(defs) >= 18
+    for name, val in defs:
+        assert hasattr(dg, name), f"{name} missing from the binding"
+        assert getattr(dg, name) == int(val), f"{name}: binding {getattr(dg, name)} != header {val}"
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_step_runner_builds_on_host(lib, fused):
+    """The step runner's set-up uses only host-side library calls (workspace sizes)."""
+    import torch
+
+    from structured_slot_reads_gb300 import configs
+    from structured_slot_reads_gb300.step import DenoiseStep
+    shp = configs.TINY
+    w = torch.zeros((shp.V, shp.D), dtype=torch.bfloat16)
+    st = DenoiseStep(shp, w, w, w.t().contiguous(), device="cpu", fused=fused)
+    assert st.fused == fused
+    assert st.kernels_per_step() == (11 if fused else 13) - (0 if st._attn_splits() > 1 else 1)
+    if fused:
+        assert st.probs.shape == (shp.C, dg.dg_probs_ld(shp.V)) and st.n_draw == 4
