@@ -151,9 +151,7 @@ def build_step(shape, device):
     torch.manual_seed(0)
     w = inputs.device_normal_bf16((shape.V, shape.D), shape.D ** -0.5, 1, device)
     e = inputs.device_normal_bf16((shape.V, shape.D), shape.D ** -0.5, 2, device)
-    e_t = torch.empty((shape.D, shape.V), dtype=torch.bfloat16, device=device)
-    dg._check(dg.dg_transpose_bf16(e, shape.V, shape.D, e_t), "dg_transpose_bf16")
-    st = DenoiseStep(shape, w, e, e_t, device=device, seed=7)
+    st = DenoiseStep(shape, w, e, device=device, seed=7)
     st.h0.copy_(inputs.device_normal_bf16(st.h0.shape, 1.0, 3, device))
     st.inv_t.copy_(1.0 / inputs.device_uniform(st.inv_t.shape, 0.5, 2.0, 4, device))
     for i, k in enumerate(("q", "kc", "vc", "kenc", "venc")):

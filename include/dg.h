@@ -182,13 +182,11 @@ int dg_commit(const dg_dims* dims, const float* entropy, const int32_t* argmax,
  * becomes a probability-weighted average of embeddings fed back as input.
  * out[i] = sum_v p_iv e[v] with p_i = softmax(z_i), z as in the lm-head call;
  * lse must be that call's output for the same rows.
- *   h [M, d_model] bf16;  w [V, d_model] bf16;  inv_t, lse [M] fp32
- *   e_t [d_model, V] bf16: the embedding table transposed (vocabulary
- *       contiguous), made once from e [V, d_model] by dg_transpose_bf16
- *   out [M, d_model] fp32
+ *   h [M, d_model] bf16;  w, e [V, d_model] bf16 (the same row-major layout
+ *   every call uses);  inv_t, lse [M] fp32;  out [M, d_model] fp32
  *   workspace: dg_workspace_bytes(dims, DG_WS_SELFCOND, M) bytes. */
 int dg_selfcond_embed(const dg_dims* dims, const uint16_t* h, int M,
-                      const uint16_t* w, const uint16_t* e_t, const float* inv_t,
+                      const uint16_t* w, const uint16_t* e, const float* inv_t,
                       const float* lse, float* out, void* workspace,
                       size_t workspace_bytes, void* stream);
 
@@ -221,17 +219,13 @@ int dg_denoise_heads(const dg_dims* dims, const uint16_t* h, int M,
 
 /* Expected embedding from dg_denoise_heads' probabilities:
  * out[i] = prob_scale[i] * sum_v probs[i][v] e[v] (24-ai.news, "Token commit
- * mechanism").  e_t as in dg_selfcond_embed; probs [M, probs_ld] bf16.
+ * mechanism").  probs [M, probs_ld] bf16;  prob_scale [M] fp32;
+ * e [V, d_model] bf16;  out [M, d_model] fp32.
  *   workspace: dg_workspace_bytes(dims, DG_WS_PROBS_EMBED, M) bytes. */
 int dg_selfcond_from_probs(const dg_dims* dims, const uint16_t* probs, size_t probs_ld,
-                           const float* prob_scale, int M, const uint16_t* e_t,
+                           const float* prob_scale, int M, const uint16_t* e,
                            float* out, void* workspace, size_t workspace_bytes,
                            void* stream);
-
-/* Transpose a bf16 matrix src [rows, cols] into dst [cols, rows]; used once to
- * lay out the embedding table for dg_selfcond_embed. */
-int dg_transpose_bf16(const uint16_t* src, int rows, int cols, uint16_t* dst,
-                      void* stream);
 
 /* ---- a6: next-step canvas input ----------------------------------------
  * 24-ai.news, "Token commit mechanism" (self-conditioning is an extra input)

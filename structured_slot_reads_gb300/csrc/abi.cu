@@ -197,17 +197,17 @@ int dg_denoise_heads(const dg_dims* d, const uint16_t* h, int M, const uint16_t*
 }
 
 int dg_selfcond_from_probs(const dg_dims* d, const uint16_t* probs, size_t probs_ld,
-                           const float* prob_scale, int M, const uint16_t* e_t, float* out,
+                           const float* prob_scale, int M, const uint16_t* e, float* out,
                            void* workspace, size_t workspace_bytes, void* stream) {
   if (!d || M < 1) return DG_ERR_ARG;
   if (!dims_lm(d) || d->V % 8) return DG_ERR_SHAPE;
-  if (!probs || !prob_scale || !e_t || !out) return DG_ERR_ARG;
-  if (probs_ld < (size_t)d->V || probs_ld % 8 || !aligned(probs, 16) || !aligned(e_t, 16) ||
+  if (!probs || !prob_scale || !e || !out) return DG_ERR_ARG;
+  if (probs_ld < (size_t)d->V || probs_ld % 8 || !aligned(probs, 16) || !aligned(e, 16) ||
       !aligned(out, 16))
     return DG_ERR_ARG;
   const size_t need = dg_workspace_bytes(d, DG_WS_PROBS_EMBED, M);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DG_ERR_WORKSPACE;
-  return launch_result(dgi::probs_embed(probs, probs_ld, prob_scale, M, e_t, d->V, d->d_model,
+  return launch_result(dgi::probs_embed(probs, probs_ld, prob_scale, M, e, d->V, d->d_model,
                                         out, workspace, static_cast<cudaStream_t>(stream)));
 }
 
@@ -400,24 +400,19 @@ int dg_commit(const dg_dims* d, const float* entropy, const int32_t* argmax, con
 }
 
 int dg_selfcond_embed(const dg_dims* d, const uint16_t* h, int M, const uint16_t* w,
-                      const uint16_t* e_t, const float* inv_t, const float* lse, float* out,
+                      const uint16_t* e, const float* inv_t, const float* lse, float* out,
                       void* workspace, size_t workspace_bytes, void* stream) {
   if (!d || M < 1) return DG_ERR_ARG;
   if (!dims_lm(d) || d->V % 8) return DG_ERR_SHAPE;
-  if (!h || !w || !e_t || !inv_t || !lse || !out) return DG_ERR_ARG;
-  if (!aligned(h, 16) || !aligned(w, 16) || !aligned(e_t, 16) || !aligned(out, 16))
+  if (!h || !w || !e || !inv_t || !lse || !out) return DG_ERR_ARG;
+  if (!aligned(h, 16) || !aligned(w, 16) || !aligned(e, 16) || !aligned(out, 16))
     return DG_ERR_ARG;
   const size_t need = dgi::selfcond_ws_bytes(M, d->V, d->d_model);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DG_ERR_WORKSPACE;
-  return launch_result(dgi::selfcond(h, M, w, e_t, d->V, d->d_model, inv_t, lse, out, workspace,
+  return launch_result(dgi::selfcond(h, M, w, e, d->V, d->d_model, inv_t, lse, out, workspace,
                                      static_cast<cudaStream_t>(stream)));
 }
 
-int dg_transpose_bf16(const uint16_t* src, int rows, int cols, uint16_t* dst, void* stream) {
-  if (!src || !dst || rows < 1 || cols < 1 || rows > 65535 * 32) return DG_ERR_ARG;
-  return launch_result(
-      dgi::transpose_bf16(src, rows, cols, dst, static_cast<cudaStream_t>(stream)));
-}
 
 int dg_canvas_update(const dg_dims* d, const uint16_t* h0, const float* e_sc, const uint16_t* emb,
                      const int32_t* tokens, const uint8_t* committed, int M, uint16_t* h_out,

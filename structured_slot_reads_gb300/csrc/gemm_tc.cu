@@ -16,9 +16,11 @@
 //              partials, summed by a reduction kernel in a fixed order.
 //
 // Warp roles (one CTA per SM): warps [0, 4*MT) are the epilogue (warp w reads
-// TMEM lanes 32*(w%4)..+31 of M-tile w/4), warp 4*MT issues TMA loads, warp
-// 4*MT+1 owns TMEM and issues tcgen05.mma from one thread.  Shared-memory
-// stages hold MT 128x64 A tiles and one BNx64 B tile, 128-byte swizzled.
+// TMEM lanes 32*(w%4)..+31 of M-tile w/4); warp 4*MT loads the A operand (rows
+// re-read from L2) into a 2-deep ring, warp 4*MT+1 streams the B operand (W or
+// E, from DRAM) into a deep ring so enough bytes are in flight to cover DRAM
+// latency; warp 4*MT+2 owns TMEM and issues tcgen05.mma from one thread.  All
+// tiles are 64-element K blocks, 128-byte swizzled by TMA.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -38,7 +40,8 @@ constexpr int BK = 64;
 constexpr int EPI_STATS = 0;
 constexpr int EPI_PROBS = 1;
 constexpr int EPI_ACCUM = 2;
-constexpr int SMEM_STAGE_BUDGET = 196608;  // 192 KB of operand stages
+constexpr int EPI_ACCUM_MN = 3;  // as EPI_ACCUM with B given N-contiguous ([K, N] row-major)
+constexpr int RING_BUDGET = 232448 - 1024 - 512;  // operand rings (227 KB - alignment - barriers)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
@@ -64,11 +67,12 @@ struct GemmParams {
 
 template <int MT, int BN>
 struct Cfg {
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGE_BYTES = MT * A_BYTES + B_BYTES;
-  static constexpr int NSTAGE = (SMEM_STAGE_BUDGET / STAGE_BYTES) > 8 ? 8
-                                                                      : (SMEM_STAGE_BUDGET / STAGE_BYTES);
+  static constexpr int A_BYTES = BM * BK * 2;   // one 128-row A tile of a K block
+  static constexpr int A_STAGE = MT * A_BYTES;  // A operand: re-read from L2, shallow ring
+  static constexpr int B_STAGE = BN * BK * 2;   // B operand: streamed from DRAM, deep ring
+  static constexpr int NA = 2;
+  static constexpr int NB_FIT = (RING_BUDGET - NA * A_STAGE) / B_STAGE;
+  static constexpr int NB = NB_FIT > 8 ? 8 : NB_FIT;
   static constexpr int ACC_COLS = MT * BN;
   static constexpr int ACC_STAGES = (2 * ACC_COLS <= 512) ? 2 : 1;
   static constexpr int TMEM_NEED = ACC_STAGES * ACC_COLS;
@@ -78,12 +82,15 @@ struct Cfg {
                                    : TMEM_NEED <= 256 ? 256
                                                       : 512;
   static constexpr int EPI_WARPS = 4 * MT;
-  static constexpr int THREADS = (EPI_WARPS + 2) * 32;
-  static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM_BYTES = 1024 + NSTAGE * STAGE_BYTES + BAR_BYTES;
+  static constexpr int THREADS = (EPI_WARPS + 3) * 32;  // + A producer, B producer, MMA
+  static constexpr int BAR_BYTES = 512;
+  static constexpr int SMEM_BYTES = 1024 + NA * A_STAGE + NB * B_STAGE + BAR_BYTES;
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+  static constexpr uint32_t IDESC_BMN = idesc_bf16_f32_bmn(BM, BN);
   static_assert(TMEM_NEED <= 512, "accumulators exceed tensor memory");
-  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
+  static_assert(NB >= 2, "ring depth");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
 template <int MT, int BN, int EPI>
@@ -91,17 +98,24 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, GemmParams p) {
   using CF = Cfg<MT, BN>;
-  constexpr int NSTAGE = CF::NSTAGE;
-  constexpr int PRODUCER_WARP = CF::EPI_WARPS;
-  constexpr int MMA_WARP = CF::EPI_WARPS + 1;
+  constexpr int NA = CF::NA;
+  constexpr int NB = CF::NB;
+  constexpr int PROD_A = CF::EPI_WARPS;
+  constexpr int PROD_B = CF::EPI_WARPS + 1;
+  constexpr int MMA_WARP = CF::EPI_WARPS + 2;
+  constexpr bool B_MN = EPI == EPI_ACCUM_MN;
+  constexpr bool ACCUM = EPI == EPI_ACCUM || B_MN;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* stages = smem;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + NSTAGE * CF::STAGE_BYTES);
-  uint64_t* empty_bar = full_bar + NSTAGE;
-  uint64_t* tfull_bar = empty_bar + NSTAGE;
+  uint8_t* ring_a = smem;
+  uint8_t* ring_b = smem + NA * CF::A_STAGE;
+  uint64_t* full_a = reinterpret_cast<uint64_t*>(ring_b + NB * CF::B_STAGE);
+  uint64_t* empty_a = full_a + NA;
+  uint64_t* full_b = empty_a + NA;
+  uint64_t* empty_b = full_b + NB;
+  uint64_t* tfull_bar = empty_b + NB;
   uint64_t* tempty_bar = tfull_bar + CF::ACC_STAGES;
   uint64_t* drain_bar = tempty_bar + CF::ACC_STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
@@ -111,9 +125,13 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NSTAGE; ++i) {
-      mbar_init(&full_bar[i], 1);
-      mbar_init(&empty_bar[i], 1);
+    for (int i = 0; i < NA; ++i) {
+      mbar_init(&full_a[i], 1);
+      mbar_init(&empty_a[i], 1);
+    }
+    for (int i = 0; i < NB; ++i) {
+      mbar_init(&full_b[i], 1);
+      mbar_init(&empty_b[i], 1);
     }
     for (int a = 0; a < CF::ACC_STAGES; ++a) {
       mbar_init(&tfull_bar[a], 1);
@@ -127,10 +145,8 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
     tmem_alloc(tmem_slot, CF::TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == PRODUCER_WARP && lane == 0) {
-    prefetch_tmap(&tmA);
-    prefetch_tmap(&tmB);
-  }
+  if (warp == PROD_A && lane == 0) prefetch_tmap(&tmA);
+  if (warp == PROD_B && lane == 0) prefetch_tmap(&tmB);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -139,7 +155,7 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
   // ---- work assignment --------------------------------------------------
   const int total_kb = (p.K + BK - 1) / BK;
   int gm, t_begin, t_end, kb_begin, kb_end;
-  if (EPI == EPI_ACCUM) {
+  if (ACCUM) {
     const int per_group = p.n_tiles * p.k_split;
     gm = blockIdx.x / per_group;
     const int rem = blockIdx.x % per_group;
@@ -159,72 +175,97 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
   const int m_base = gm * MT * BM;
   const bool has_work = (t_end > t_begin) && (kb_end > kb_begin);
 
-  if (warp == PRODUCER_WARP) {
+  if (warp == PROD_A || warp == PROD_B) {
+    // one producer thread per ring; the B ring (streamed from DRAM) runs up to
+    // NB K-blocks ahead, the A ring (re-read from L2) up to NA
     if (lane == 0 && has_work) {
-      const uint64_t pol_b = policy_evict_first();  // W or E^T: streamed once
-      const uint64_t pol_a = policy_evict_last();   // hidden rows or P: re-read per tile
+      const bool is_a = warp == PROD_A;
+      const int nst = is_a ? NA : NB;
+      uint64_t* full = is_a ? full_a : full_b;
+      uint64_t* empty = is_a ? empty_a : empty_b;
+      const uint64_t pol = is_a ? policy_evict_last() : policy_evict_first();
       int stage = 0;
-      uint32_t phase = 0;
-      uint32_t issued_mask = 0, last_phase = 0;
+      uint32_t phase = 0, issued_mask = 0, last_phase = 0;
       bool ok = true;
       for (int t = t_begin; t < t_end && ok; ++t) {
         for (int kb = kb_begin; kb < kb_end; ++kb) {
-          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.status)) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full_bar[stage], CF::STAGE_BYTES);
-          uint8_t* s_a = stages + stage * CF::STAGE_BYTES;
+          if (is_a) {
+            mbar_arrive_expect_tx(&full[stage], CF::A_STAGE);
+            uint8_t* dst = ring_a + stage * CF::A_STAGE;
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt)
-            tma_load_2d_hint(s_a + mt * CF::A_BYTES, &tmA, &full_bar[stage], kb * BK,
-                             m_base + mt * BM, pol_a);
-          tma_load_2d_hint(s_a + MT * CF::A_BYTES, &tmB, &full_bar[stage], kb * BK, t * BN,
-                           pol_b);
+            for (int mt = 0; mt < MT; ++mt)
+              tma_load_2d_hint(dst + mt * CF::A_BYTES, &tmA, &full[stage], kb * BK,
+                               m_base + mt * BM, pol);
+          } else {
+            mbar_arrive_expect_tx(&full[stage], CF::B_STAGE);
+            uint8_t* dst = ring_b + stage * CF::B_STAGE;
+            if (B_MN) {
+              // B [K, N] with N contiguous: BN/64 boxes of 64 N-columns x 64 K-rows
+#pragma unroll
+              for (int g = 0; g < BN / 64; ++g)
+                tma_load_2d_hint(dst + g * (BK * 128), &tmB, &full[stage], t * BN + g * 64,
+                                 kb * BK, pol);
+            } else {
+              tma_load_2d_hint(dst, &tmB, &full[stage], kb * BK, t * BN, pol);
+            }
+          }
           issued_mask |= 1u << stage;
           last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
-          if (++stage == NSTAGE) {
+          if (++stage == nst) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
       if (!ok) {  // let every copy already issued land before the CTA exits
-        for (int s = 0; s < NSTAGE; ++s)
-          if (issued_mask & (1u << s)) mbar_wait_drain(&full_bar[s], (last_phase >> s) & 1u);
+        for (int s = 0; s < nst; ++s)
+          if (issued_mask & (1u << s)) mbar_wait_drain(&full[s], (last_phase >> s) & 1u);
       }
     }
   } else if (warp == MMA_WARP) {
     if (lane == 0 && has_work) {
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
+      int sa = 0, sb = 0, acc = 0;
+      uint32_t pa = 0, pb = 0, acc_phase = 0;
       bool ok = true;
       for (int t = t_begin; t < t_end && ok; ++t) {
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d_base = tmem_base + acc * CF::ACC_COLS;
         for (int kb = kb_begin; kb < kb_end; ++kb) {
-          if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.status)) {
+          if (!mbar_wait(&full_a[sa], pa, abort_flag, p.status) ||
+              !mbar_wait(&full_b[sb], pb, abort_flag, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(stages + stage * CF::STAGE_BYTES);
-          const uint32_t b_addr = a_addr + MT * CF::A_BYTES;
+          const uint32_t a_addr = smem_u32(ring_a + sa * CF::A_STAGE);
+          const uint32_t b_addr = smem_u32(ring_b + sb * CF::B_STAGE);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t bdesc = sw128_kmajor_desc(b_addr + kk * 32);
+            // K-major B: +32 bytes per 16 K inside the 128-byte row; MN-major B:
+            // +2 KB (two 8-row K groups) per 16 K
+            const uint64_t bdesc = B_MN ? sw128_mnmajor_desc(b_addr + kk * 2048, BK * 128, 1024)
+                                        : sw128_kmajor_desc(b_addr + kk * 32);
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
               const uint64_t adesc = sw128_kmajor_desc(a_addr + mt * CF::A_BYTES + kk * 32);
-              tc_mma_f16(d_base + mt * BN, adesc, bdesc, CF::IDESC,
+              tc_mma_f16(d_base + mt * BN, adesc, bdesc, B_MN ? CF::IDESC_BMN : CF::IDESC,
                          (kb > kb_begin || kk > 0) ? 1u : 0u);
             }
           }
-          tc_commit(&empty_bar[stage]);
-          if (++stage == NSTAGE) {
-            stage = 0;
-            phase ^= 1u;
+          tc_commit(&empty_a[sa]);
+          tc_commit(&empty_b[sb]);
+          if (++sa == NA) {
+            sa = 0;
+            pa ^= 1u;
+          }
+          if (++sb == NB) {
+            sb = 0;
+            pb ^= 1u;
           }
         }
         if (!ok) break;
@@ -245,7 +286,7 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
     const int row = m_base + mt * BM + quarter * 32 + lane;
     const bool row_ok = row < p.M;
     float scale = 0.f, lse2 = 0.f;
-    if (EPI != EPI_ACCUM && row_ok) scale = __ldg(p.inv_t + row) * LOG2E;
+    if (!ACCUM && row_ok) scale = __ldg(p.inv_t + row) * LOG2E;
     if (EPI == EPI_PROBS && row_ok) lse2 = __ldg(p.lse + row) * LOG2E;
     float m_run = -INFINITY, s_run = 0.f, t_run = 0.f, best = -INFINITY;
     int best_idx = 0x7fffffff;
@@ -545,7 +586,7 @@ size_t selfcond_ws_bytes(int M, int V, int D) {
   return probs + part;
 }
 
-cudaError_t selfcond(const uint16_t* h, int M, const uint16_t* w, const uint16_t* e_t, int V,
+cudaError_t selfcond(const uint16_t* h, int M, const uint16_t* w, const uint16_t* e, int V,
                      int D, const float* inv_t, const float* lse, float* out, void* ws,
                      cudaStream_t st) {
   const size_t ldp = align_up(V, 64);
@@ -576,7 +617,7 @@ cudaError_t selfcond(const uint16_t* h, int M, const uint16_t* w, const uint16_t
     if (e != cudaSuccess) return e;
   }
   // 2) split-K partials of P . E over the vocabulary, 3) ordered reduction
-  return probs_embed(reinterpret_cast<const uint16_t*>(probs), ldp, nullptr, M, e_t, V, D, out,
+  return probs_embed(reinterpret_cast<const uint16_t*>(probs), ldp, nullptr, M, e, V, D, out,
                      part, st);
 }
 
@@ -587,14 +628,15 @@ size_t probs_embed_ws_bytes(int M, int V, int D) {
 }
 
 cudaError_t probs_embed(const uint16_t* probs, size_t ldp, const float* row_scale, int M,
-                        const uint16_t* e_t, int V, int D, float* out, void* ws,
+                        const uint16_t* e, int V, int D, float* out, void* ws,
                         cudaStream_t st) {
   const int mt = stats_mt(M);
   const int groups = (M + mt * BM - 1) / (mt * BM);
   float* part = static_cast<float*>(ws);
   CUtensorMap ta, tb;
   if (!make_tmap_bf16_2d(&ta, probs, V, M, (uint64_t)ldp * 2, BK, BM)) return cudaErrorInvalidValue;
-  if (!make_tmap_bf16_2d(&tb, e_t, V, D, (uint64_t)V * 2, BK, ACC_BN)) return cudaErrorInvalidValue;
+  // E [V, D] row-major is the MN-major B operand: boxes of 64 d-columns x 64 vocabulary rows
+  if (!make_tmap_bf16_2d(&tb, e, D, V, (uint64_t)D * 2, 64, BK)) return cudaErrorInvalidValue;
   GemmParams p{};
   p.M = M;
   p.N = D;
@@ -604,9 +646,9 @@ cudaError_t probs_embed(const uint16_t* probs, size_t ldp, const float* row_scal
   p.part = part;
   p.status = status_ptr();
   const int grid = groups * p.n_tiles * p.k_split;
-  cudaError_t e = (mt == 1) ? launch_gemm<1, ACC_BN, EPI_ACCUM>(ta, tb, p, grid, st)
-                            : launch_gemm<2, ACC_BN, EPI_ACCUM>(ta, tb, p, grid, st);
-  if (e != cudaSuccess) return e;
+  cudaError_t err = (mt == 1) ? launch_gemm<1, ACC_BN, EPI_ACCUM_MN>(ta, tb, p, grid, st)
+                              : launch_gemm<2, ACC_BN, EPI_ACCUM_MN>(ta, tb, p, grid, st);
+  if (err != cudaSuccess) return err;
   const long long n4 = (long long)M * D / 4;
   const int blocks = (int)std::min<long long>((n4 + 255) / 256, 4LL * num_sms());
   split_reduce_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(part), p.k_split,

@@ -38,7 +38,6 @@ constexpr int PRO_N = 64;         // prologue vocabulary entries for the referen
 constexpr float REF_HEADROOM = 24.f;  // log2 units added to the prologue max
 constexpr float V_CLAMP = 100.f;      // exponent guard (log2 units above the reference)
 constexpr int DRAW_N = 16;
-constexpr int STAGE_BUDGET = 212992;  // 208 KB of operand stages
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
@@ -80,28 +79,31 @@ struct HeadsParams {
 
 template <int MT, int BN, bool DRAWS>
 struct HCfg {
-  static constexpr int A_BYTES = BM * BK * 2;           // 16 KB per canvas M-tile
-  static constexpr int B_REGION = 256 * BK * 2;         // W tile region (BN rows loaded)
+  static constexpr int A_BYTES = BM * BK * 2;             // one 128-row canvas tile
+  static constexpr int A_STAGE = MT * A_BYTES;            // hidden rows: L2, shallow ring
+  static constexpr int W_SLOT = BN * BK * 2;              // W tile: DRAM, deep ring
   static constexpr int D_BYTES = DRAWS ? DRAW_N * BK * 2 : 0;
-  static constexpr int STAGE_BYTES = MT * A_BYTES + B_REGION + D_BYTES;
-  static constexpr int NSTAGE = (STAGE_BUDGET / STAGE_BYTES) > 8 ? 8 : STAGE_BUDGET / STAGE_BYTES;
+  static constexpr int B_STAGE = W_SLOT + D_BYTES;
+  static constexpr int NA = 2;
   static constexpr int DRAW_COLS = DRAWS ? 2 * DRAW_N : 0;
   static constexpr int ACC_COLS = MT * BN + DRAW_COLS;
   static constexpr int ACC_STAGES = (2 * ACC_COLS <= 512) ? 2 : 1;
   static constexpr int TMEM_COLS = 512;
   static constexpr int EPI_WARPS = 4 * MT;
-  static constexpr int THREADS = (EPI_WARPS + 2) * 32;
-  static constexpr int BAR_BYTES = 256 + EPI_WARPS * DRAW_N * 8;
-  static constexpr int SMEM_BYTES = 1024 + NSTAGE * STAGE_BYTES + BAR_BYTES;
+  static constexpr int THREADS = (EPI_WARPS + 3) * 32;    // + two producers + MMA
+  static constexpr int BAR_BYTES = 512 + EPI_WARPS * DRAW_N * 8;
+  static constexpr int NB_FIT = (232448 - 1024 - BAR_BYTES - NA * A_STAGE) / B_STAGE;
+  static constexpr int NB = NB_FIT > 8 ? 8 : NB_FIT;
+  static constexpr int SMEM_BYTES = 1024 + NA * A_STAGE + NB * B_STAGE + BAR_BYTES;
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
   static constexpr uint32_t IDESC_PRO = idesc_bf16_f32(BM, PRO_N);
   static constexpr uint32_t IDESC_DRAW = idesc_bf16_f32(BM, DRAW_N);
-  static constexpr uint32_t TX_TILE = MT * A_BYTES + BN * BK * 2 + D_BYTES;
-  static constexpr uint32_t TX_PRO = MT * A_BYTES + PRO_N * BK * 2;
+  static constexpr int HALF1_ROW = BN - 128;  // the second swapped MMA reads W rows [BN-128, BN)
   static_assert(ACC_COLS <= 512, "accumulators exceed tensor memory");
   static_assert(BN % 32 == 0 && BN <= 256 && BN >= PRO_N, "BN");
-  static_assert(!DRAWS || BN >= 128, "the swapped draw MMA reads two 128-row halves");
-  static_assert(SMEM_BYTES <= 232448, "shared memory");
+  static_assert(!DRAWS || (BN >= 128 && BN % 8 == 0), "swapped draw MMA geometry");
+  static_assert(B_STAGE % 1024 == 0, "ring slots must stay 1 KB aligned");
+  static_assert(NB >= 2 && SMEM_BYTES <= 232448, "shared memory");
 };
 
 template <int MT, int BN, bool DRAWS>
@@ -110,31 +112,41 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
                  const __grid_constant__ CUtensorMap tmB64,
                  const __grid_constant__ CUtensorMap tmD, HeadsParams p) {
   using CF = HCfg<MT, BN, DRAWS>;
-  constexpr int NSTAGE = CF::NSTAGE;
-  constexpr int PRODUCER_WARP = CF::EPI_WARPS;
-  constexpr int MMA_WARP = CF::EPI_WARPS + 1;
+  constexpr int NA = CF::NA;
+  constexpr int NB = CF::NB;
+  constexpr int PROD_A = CF::EPI_WARPS;
+  constexpr int PROD_B = CF::EPI_WARPS + 1;
+  constexpr int MMA_WARP = CF::EPI_WARPS + 2;
   constexpr int EPI_THREADS = CF::EPI_WARPS * 32;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* stages = smem;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + NSTAGE * CF::STAGE_BYTES);
-  uint64_t* empty_bar = full_bar + NSTAGE;
-  uint64_t* tfull_bar = empty_bar + NSTAGE;
+  uint8_t* ring_a = smem;
+  uint8_t* ring_b = smem + NA * CF::A_STAGE;
+  uint8_t* bar_base = ring_b + NB * CF::B_STAGE;
+  uint64_t* full_a = reinterpret_cast<uint64_t*>(bar_base);
+  uint64_t* empty_a = full_a + NA;
+  uint64_t* full_b = empty_a + NA;
+  uint64_t* empty_b = full_b + NB;
+  uint64_t* tfull_bar = empty_b + NB;
   uint64_t* tempty_bar = tfull_bar + CF::ACC_STAGES;
   uint64_t* drain_bar = tempty_bar + CF::ACC_STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* draw_red = reinterpret_cast<float*>(smem + NSTAGE * CF::STAGE_BYTES + 256);
+  float* draw_red = reinterpret_cast<float*>(bar_base + 512);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NSTAGE; ++i) {
-      mbar_init(&full_bar[i], 1);
-      mbar_init(&empty_bar[i], 1);
+    for (int i = 0; i < NA; ++i) {
+      mbar_init(&full_a[i], 1);
+      mbar_init(&empty_a[i], 1);
+    }
+    for (int i = 0; i < NB; ++i) {
+      mbar_init(&full_b[i], 1);
+      mbar_init(&empty_b[i], 1);
     }
     for (int a = 0; a < CF::ACC_STAGES; ++a) {
       mbar_init(&tfull_bar[a], 1);
@@ -148,8 +160,8 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
     tmem_alloc(tmem_slot, CF::TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == PRODUCER_WARP && lane == 0) {
-    prefetch_tmap(&tmA);
+  if (warp == PROD_A && lane == 0) prefetch_tmap(&tmA);
+  if (warp == PROD_B && lane == 0) {
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmB64);
     if (DRAWS) prefetch_tmap(&tmD);
@@ -159,7 +171,7 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  // tile -1 is the reference prologue (vocabulary 0..63, canvas rows only)
+  // tile t_begin-1 is the reference prologue (vocabulary 0..63, canvas rows only)
   const int total_kb = (p.K + BK - 1) / BK;
   const int gm = blockIdx.x / p.cpg;
   const int gn = blockIdx.x % p.cpg;
@@ -168,53 +180,60 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
   const int m_base = gm * MT * BM;
   const bool draws_here = DRAWS && gm == 0 && p.n_draw > 0;
 
-  if (warp == PRODUCER_WARP) {
+  if (warp == PROD_A || warp == PROD_B) {
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();
-      const uint64_t pol_h = policy_evict_last();
+      const bool is_a = warp == PROD_A;
+      const int nst = is_a ? NA : NB;
+      uint64_t* full = is_a ? full_a : full_b;
+      uint64_t* empty = is_a ? empty_a : empty_b;
+      const uint64_t pol_keep = policy_evict_last();
+      const uint64_t pol_stream = policy_evict_first();
       int stage = 0;
       uint32_t phase = 0, issued_mask = 0, last_phase = 0;
       bool ok = true;
       for (int t = t_begin - 1; t < t_end && ok; ++t) {
         const bool pro = t < t_begin;
         for (int kb = 0; kb < total_kb; ++kb) {
-          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.status)) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
             ok = false;
             break;
           }
-          uint8_t* s_a = stages + stage * CF::STAGE_BYTES;
-          uint8_t* s_b = s_a + MT * CF::A_BYTES;
-          if (pro) {
-            mbar_arrive_expect_tx(&full_bar[stage], CF::TX_PRO);
-            tma_load_2d_hint(s_b, &tmB64, &full_bar[stage], kb * BK, 0, pol_h);
-          } else {
-            mbar_arrive_expect_tx(&full_bar[stage],
-                                  draws_here ? CF::TX_TILE : CF::TX_TILE - CF::D_BYTES);
-            tma_load_2d_hint(s_b, &tmB, &full_bar[stage], kb * BK, t * BN, pol_w);
-            if (draws_here)
-              tma_load_2d_hint(s_b + CF::B_REGION, &tmD, &full_bar[stage], kb * BK, 0, pol_h);
-          }
+          if (is_a) {
+            mbar_arrive_expect_tx(&full[stage], CF::A_STAGE);
+            uint8_t* dst = ring_a + stage * CF::A_STAGE;
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt)
-            tma_load_2d_hint(s_a + mt * CF::A_BYTES, &tmA, &full_bar[stage], kb * BK,
-                             m_base + mt * BM, pol_h);
+            for (int mt = 0; mt < MT; ++mt)
+              tma_load_2d_hint(dst + mt * CF::A_BYTES, &tmA, &full[stage], kb * BK,
+                               m_base + mt * BM, pol_keep);
+          } else {
+            uint8_t* dst = ring_b + stage * CF::B_STAGE;
+            if (pro) {
+              mbar_arrive_expect_tx(&full[stage], PRO_N * BK * 2);
+              tma_load_2d_hint(dst, &tmB64, &full[stage], kb * BK, 0, pol_keep);
+            } else {
+              mbar_arrive_expect_tx(&full[stage], CF::W_SLOT + (draws_here ? CF::D_BYTES : 0));
+              tma_load_2d_hint(dst, &tmB, &full[stage], kb * BK, t * BN, pol_stream);
+              if (draws_here)
+                tma_load_2d_hint(dst + CF::W_SLOT, &tmD, &full[stage], kb * BK, 0, pol_keep);
+            }
+          }
           issued_mask |= 1u << stage;
           last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
-          if (++stage == NSTAGE) {
+          if (++stage == nst) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
       if (!ok) {
-        for (int s = 0; s < NSTAGE; ++s)
-          if (issued_mask & (1u << s)) mbar_wait_drain(&full_bar[s], (last_phase >> s) & 1u);
+        for (int s = 0; s < nst; ++s)
+          if (issued_mask & (1u << s)) mbar_wait_drain(&full[s], (last_phase >> s) & 1u);
       }
     }
   } else if (warp == MMA_WARP) {
     if (lane == 0) {
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
+      int sa = 0, sb = 0, acc = 0;
+      uint32_t pa = 0, pb = 0, acc_phase = 0;
       bool ok = true;
       for (int t = t_begin - 1; t < t_end && ok; ++t) {
         const bool pro = t < t_begin;
@@ -222,14 +241,15 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
         tc_fence_after();
         const uint32_t d_base = tmem_base + acc * CF::ACC_COLS;
         for (int kb = 0; kb < total_kb; ++kb) {
-          if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.status)) {
+          if (!mbar_wait(&full_a[sa], pa, abort_flag, p.status) ||
+              !mbar_wait(&full_b[sb], pb, abort_flag, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(stages + stage * CF::STAGE_BYTES);
-          const uint32_t b_addr = a_addr + MT * CF::A_BYTES;
-          const uint32_t d_addr = b_addr + CF::B_REGION;
+          const uint32_t a_addr = smem_u32(ring_a + sa * CF::A_STAGE);
+          const uint32_t b_addr = smem_u32(ring_b + sb * CF::B_STAGE);
+          const uint32_t d_addr = b_addr + CF::W_SLOT;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint32_t acc_flag = (kb > 0 || kk > 0) ? 1u : 0u;
@@ -244,16 +264,22 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
               const uint64_t ddesc = sw128_kmajor_desc(d_addr + kk * 32);
 #pragma unroll
               for (int half = 0; half < 2; ++half) {
-                const uint64_t wdesc = sw128_kmajor_desc(b_addr + half * CF::A_BYTES + kk * 32);
+                const uint32_t row0 = half ? CF::HALF1_ROW : 0;
+                const uint64_t wdesc = sw128_kmajor_desc(b_addr + row0 * 128 + kk * 32);
                 tc_mma_f16(d_base + MT * BN + half * DRAW_N, wdesc, ddesc, CF::IDESC_DRAW,
                            acc_flag);
               }
             }
           }
-          tc_commit(&empty_bar[stage]);
-          if (++stage == NSTAGE) {
-            stage = 0;
-            phase ^= 1u;
+          tc_commit(&empty_a[sa]);
+          tc_commit(&empty_b[sb]);
+          if (++sa == NA) {
+            sa = 0;
+            pa ^= 1u;
+          }
+          if (++sb == NB) {
+            sb = 0;
+            pb ^= 1u;
           }
         }
         if (!ok) break;
@@ -372,9 +398,11 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
             tmem_ld_32x32b_x16(
                 tmem_base + lane_base + acc * CF::ACC_COLS + MT * BN + half * DRAW_N, r);
             tmem_ld_wait();
-            const int vl = half * 128 + quarter * 32 + lane;  // row within the W tile
+            // row of the W tile on this lane; half 1 starts at row BN-128, so its
+            // lanes below row 128 repeat half 0 and are skipped
+            const int vl = (half ? CF::HALF1_ROW : 0) + quarter * 32 + lane;
             const int vocab = t * BN + vl;
-            if (vl < BN && vocab < p.V) {
+            if ((half == 0 || vl >= 128) && vl < BN && vocab < p.V) {
 #pragma unroll
               for (int j = 0; j < DRAW_N; ++j) {
                 if (j < p.n_draw) {

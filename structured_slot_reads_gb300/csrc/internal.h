@@ -29,14 +29,15 @@ size_t lmhead_ws_bytes(int M, int V);
 cudaError_t lmhead_stats(const uint16_t* h, int M, const uint16_t* w, int V, int D,
                          const float* inv_t, RowStats out, void* ws, cudaStream_t st);
 size_t selfcond_ws_bytes(int M, int V, int D);
-cudaError_t selfcond(const uint16_t* h, int M, const uint16_t* w, const uint16_t* e_t, int V,
+cudaError_t selfcond(const uint16_t* h, int M, const uint16_t* w, const uint16_t* e, int V,
                      int D, const float* inv_t, const float* lse, float* out, void* ws,
                      cudaStream_t st);
 
 // P . E from bf16 probabilities (optionally unnormalised, times row_scale).
 size_t probs_embed_ws_bytes(int M, int V, int D);
+// e is the embedding table [V, D] row-major (read as an MN-major B operand).
 cudaError_t probs_embed(const uint16_t* probs, size_t ldp, const float* row_scale, int M,
-                        const uint16_t* e_t, int V, int D, float* out, void* ws,
+                        const uint16_t* e, int V, int D, float* out, void* ws,
                         cudaStream_t st);
 
 // ---- fused lm-head pass of a step (heads_tc.cu) ------------------------------
@@ -80,7 +81,5 @@ cudaError_t commit(int B, int C, const float* entropy, const int32_t* argmax,
 cudaError_t canvas_update(const uint16_t* h0, const float* e_sc, const uint16_t* emb, int V,
                           const int32_t* tokens, const uint8_t* committed, int M, int D,
                           uint16_t* h_out, cudaStream_t st);
-cudaError_t transpose_bf16(const uint16_t* src, int rows, int cols, uint16_t* dst,
-                           cudaStream_t st);
 
 }  // namespace dgi

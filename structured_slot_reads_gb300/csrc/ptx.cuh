@@ -204,6 +204,22 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
   return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand (N contiguous in
+// memory) written by TMA as boxes of 64 N-elements x rows along K with 128-byte
+// swizzling: 8 K-rows of 128 bytes form a 1 KB atom; consecutive 8-row groups
+// along K are `k_group_bytes` apart (stride byte offset) and consecutive
+// 64-element groups along N are `n_group_bytes` apart (leading byte offset).
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr, uint32_t n_group_bytes,
+                                                       uint32_t k_group_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((n_group_bytes >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((k_group_bytes >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 D, M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4)                       // D format: f32
@@ -211,6 +227,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | (1u << 10)                    // B format: bf16
          | ((uint32_t)(N >> 3) << 17)    // N / 8
          | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+// Same with B MN-major (the "transpose B" bit).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(int M, int N) {
+  return idesc_bf16_f32(M, N) | (1u << 16);
 }
 
 __device__ __forceinline__ bool elect_one_sync() {

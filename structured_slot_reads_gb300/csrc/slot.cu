@@ -293,19 +293,6 @@ __global__ void canvas_update_kernel(const __nv_bfloat16* h0, const float* e_sc,
   }
 }
 
-__global__ void transpose_kernel(const uint16_t* src, int rows, int cols, uint16_t* dst) {
-  __shared__ uint16_t tile[32][33];
-  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
-  for (int j = threadIdx.y; j < 32; j += blockDim.y) {
-    const int r = r0 + j, c = c0 + threadIdx.x;
-    if (r < rows && c < cols) tile[j][threadIdx.x] = src[(long long)r * cols + c];
-  }
-  __syncthreads();
-  for (int j = threadIdx.y; j < 32; j += blockDim.y) {
-    const int c = c0 + j, r = r0 + threadIdx.x;
-    if (r < rows && c < cols) dst[(long long)c * rows + r] = tile[threadIdx.x][j];
-  }
-}
 
 }  // namespace
 
@@ -369,11 +356,5 @@ cudaError_t canvas_update(const uint16_t* h0, const float* e_sc, const uint16_t*
   return cudaGetLastError();
 }
 
-cudaError_t transpose_bf16(const uint16_t* src, int rows, int cols, uint16_t* dst,
-                           cudaStream_t st) {
-  dim3 grid((cols + 31) / 32, (rows + 31) / 32);
-  transpose_kernel<<<grid, dim3(32, 8), 0, st>>>(src, rows, cols, dst);
-  return cudaGetLastError();
-}
 
 }  // namespace dgi

@@ -62,7 +62,6 @@ _SIGS = {
     "dg_denoise_heads": [DP, P, I, P, I, P, P, P, P, P, P, P, P, P, P, Z, P, Z, P],
     "dg_selfcond_from_probs": [DP, P, Z, P, I, P, P, P, Z, P],
     "dg_probs_ld": [I],
-    "dg_transpose_bf16": [P, I, I, P, P],
     "dg_canvas_update": [DP, P, P, P, P, P, I, P, P],
     "dg_philox_fill": [U64, P, I, P, P],
     "dg_validate_slots": [DP, P, P, P, I, I],
@@ -176,8 +175,8 @@ def dg_commit(dims, entropy, argmax, cand, gamma, committed_state, token_state, 
                            _p(n_commit), _s(stream))
 
 
-def dg_selfcond_embed(dims, h, M, w, e_t, inv_t, lse, out, workspace, stream=None):
-    return lib().dg_selfcond_embed(ctypes.byref(dims), _p(h), M, _p(w), _p(e_t), _p(inv_t),
+def dg_selfcond_embed(dims, h, M, w, e, inv_t, lse, out, workspace, stream=None):
+    return lib().dg_selfcond_embed(ctypes.byref(dims), _p(h), M, _p(w), _p(e), _p(inv_t),
                                    _p(lse), _p(out), _p(workspace), _nbytes(workspace),
                                    _s(stream))
 
@@ -190,10 +189,10 @@ def dg_denoise_heads(dims, h, M, draw_rows, n_draw, w, inv_t, inv_t_draw, lse, e
                                   _p(workspace), _nbytes(workspace), _s(stream))
 
 
-def dg_selfcond_from_probs(dims, probs, probs_ld, prob_scale, M, e_t, out, workspace,
+def dg_selfcond_from_probs(dims, probs, probs_ld, prob_scale, M, e, out, workspace,
                            stream=None):
     return lib().dg_selfcond_from_probs(ctypes.byref(dims), _p(probs), probs_ld, _p(prob_scale),
-                                        M, _p(e_t), _p(out), _p(workspace), _nbytes(workspace),
+                                        M, _p(e), _p(out), _p(workspace), _nbytes(workspace),
                                         _s(stream))
 
 
@@ -201,8 +200,6 @@ def dg_probs_ld(V):
     return int(lib().dg_probs_ld(V))
 
 
-def dg_transpose_bf16(src, rows, cols, dst, stream=None):
-    return lib().dg_transpose_bf16(_p(src), rows, cols, _p(dst), _s(stream))
 
 
 def dg_canvas_update(dims, h0, e_sc, emb, tokens, committed, M, h_out, stream=None):

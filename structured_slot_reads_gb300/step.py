@@ -23,13 +23,13 @@ def _empty(shape, dtype, device):
 
 
 class DenoiseStep:
-    def __init__(self, shape, w, e, e_t, device="cuda", with_slots=True, seed=0, fused=True):
+    def __init__(self, shape, w, e, device="cuda", with_slots=True, seed=0, fused=True):
         self.shape = shape
         self.dims = dg.dims_of(shape)
         self.device = device
         B, C, D, V = shape.B, shape.C, shape.D, shape.V
         self.M = B * C
-        self.w, self.e, self.e_t = w, e, e_t
+        self.w, self.e = w, e
         bf, f32, i32, u8 = torch.bfloat16, torch.float32, torch.int32, torch.uint8
         dev = device
         # per-request inputs
@@ -121,7 +121,7 @@ class DenoiseStep:
         ck(dg.dg_commit(d, self.ent, self.argmax, self.cand, self.gamma, self.committed,
                         self.tok_state, self.commit, self.tokens, self.n_commit, stream),
            "dg_commit")
-        ck(dg.dg_selfcond_embed(d, self.h, self.M, self.w, self.e_t, self.inv_t, self.lse,
+        ck(dg.dg_selfcond_embed(d, self.h, self.M, self.w, self.e, self.inv_t, self.lse,
                                 self.e_sc, self.ws_sc, stream), "dg_selfcond_embed")
         ck(dg.dg_canvas_update(d, self.h0, self.e_sc, self.e, self.tok_state, self.committed,
                                self.M, self.h, stream), "dg_canvas_update")
@@ -148,7 +148,7 @@ class DenoiseStep:
                         self.tok_state, self.commit, self.tokens, self.n_commit, stream),
            "dg_commit")
         ck(dg.dg_selfcond_from_probs(d, self.probs, self.probs_ld, self.prob_scale, self.M,
-                                     self.e_t, self.e_sc, self.ws_pe, stream),
+                                     self.e, self.e_sc, self.ws_pe, stream),
            "dg_selfcond_from_probs")
         ck(dg.dg_canvas_update(d, self.h0, self.e_sc, self.e, self.tok_state, self.committed,
                                self.M, self.h, stream), "dg_canvas_update")

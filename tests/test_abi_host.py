@@ -143,7 +143,7 @@ def test_step_runner_builds_on_host(lib, fused):
     from structured_slot_reads_gb300.step import DenoiseStep
     shp = configs.TINY
     w = torch.zeros((shp.V, shp.D), dtype=torch.bfloat16)
-    st = DenoiseStep(shp, w, w, w.t().contiguous(), device="cpu", fused=fused)
+    st = DenoiseStep(shp, w, w, device="cpu", fused=fused)
     assert st.fused == fused
     assert st.kernels_per_step() == (11 if fused else 13) - (0 if st._attn_splits() > 1 else 1)
     if fused:

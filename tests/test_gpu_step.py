@@ -64,8 +64,7 @@ def _tiny_inputs(n_steps, seed=0):
 def test_tiny_loop_step_by_step(fused):
     n_steps = 4
     shape, x, steps = _tiny_inputs(n_steps)
-    e_t = dev_bf16(np.ascontiguousarray(x["e"].T))
-    st = DenoiseStep(shape, dev_bf16(x["w"]), dev_bf16(x["e"]), e_t, seed=0, fused=fused)
+    st = DenoiseStep(shape, dev_bf16(x["w"]), dev_bf16(x["e"]), seed=0, fused=fused)
     assert st.fused == fused
     _load(st, x)
     ref_attn, ref_attn_lse = oracle.attn_decode(x["q"], x["kc"], x["vc"], x["kenc"], x["venc"],
@@ -105,9 +104,7 @@ def full_canvas(request):
     x = inputs.step_inputs(shape, seed=0)
     w, e = x["w"], x["e"]
     wd, ed = dev_bf16(w), dev_bf16(e)
-    e_t = torch.empty((shape.D, shape.V), dtype=torch.bfloat16, device="cuda")
-    assert dg.dg_transpose_bf16(ed, shape.V, shape.D, e_t) == dg.DG_OK
-    st = DenoiseStep(shape, wd, ed, e_t, seed=0, fused=request.param)
+    st = DenoiseStep(shape, wd, ed, seed=0, fused=request.param)
     _load(st, x)
     st.run(step_idx=0)
     torch.cuda.synchronize()
