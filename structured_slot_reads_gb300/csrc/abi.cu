@@ -9,7 +9,7 @@
 #include <mutex>
 #include <set>
 
-#include "../../include/dg.h"
+#include "dg.h"
 #include "internal.h"
 
 namespace {

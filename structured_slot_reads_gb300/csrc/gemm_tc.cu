@@ -16,11 +16,10 @@
 //              partials, summed by a reduction kernel in a fixed order.
 //
 // Warp roles (one CTA per SM): warps [0, 4*MT) are the epilogue (warp w reads
-// TMEM lanes 32*(w%4)..+31 of M-tile w/4); warp 4*MT loads the A operand (rows
-// re-read from L2) into a 2-deep ring, warp 4*MT+1 streams the B operand (W or
-// E, from DRAM) into a deep ring so enough bytes are in flight to cover DRAM
-// latency; warp 4*MT+2 owns TMEM and issues tcgen05.mma from one thread.  All
-// tiles are 64-element K blocks, 128-byte swizzled by TMA.
+// TMEM lanes 32*(w%4)..+31 of M-tile w/4), warp 4*MT issues the TMA loads of a
+// shared-memory ring whose stages hold MT 128x64 A tiles and one BNx64 B tile
+// (128-byte swizzled), warp 4*MT+1 owns TMEM and issues tcgen05.mma from one
+// thread.  B is K-major (W) or MN-major (E read as [V, d_model]).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -68,11 +67,11 @@ struct GemmParams {
 template <int MT, int BN>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;   // one 128-row A tile of a K block
-  static constexpr int A_STAGE = MT * A_BYTES;  // A operand: re-read from L2, shallow ring
-  static constexpr int B_STAGE = BN * BK * 2;   // B operand: streamed from DRAM, deep ring
-  static constexpr int NA = 2;
-  static constexpr int NB_FIT = (RING_BUDGET - NA * A_STAGE) / B_STAGE;
-  static constexpr int NB = NB_FIT > 8 ? 8 : NB_FIT;
+  static constexpr int A_STAGE = MT * A_BYTES;
+  static constexpr int B_STAGE = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+  static constexpr int NS_FIT = RING_BUDGET / STAGE_BYTES;
+  static constexpr int NSTAGE = NS_FIT > 8 ? 8 : NS_FIT;
   static constexpr int ACC_COLS = MT * BN;
   static constexpr int ACC_STAGES = (2 * ACC_COLS <= 512) ? 2 : 1;
   static constexpr int TMEM_NEED = ACC_STAGES * ACC_COLS;
@@ -82,14 +81,14 @@ struct Cfg {
                                    : TMEM_NEED <= 256 ? 256
                                                       : 512;
   static constexpr int EPI_WARPS = 4 * MT;
-  static constexpr int THREADS = (EPI_WARPS + 3) * 32;  // + A producer, B producer, MMA
+  static constexpr int THREADS = (EPI_WARPS + 2) * 32;  // + producer, MMA issuer
   static constexpr int BAR_BYTES = 512;
-  static constexpr int SMEM_BYTES = 1024 + NA * A_STAGE + NB * B_STAGE + BAR_BYTES;
+  static constexpr int SMEM_BYTES = 1024 + NSTAGE * STAGE_BYTES + BAR_BYTES;
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
   static constexpr uint32_t IDESC_BMN = idesc_bf16_f32_bmn(BM, BN);
   static_assert(TMEM_NEED <= 512, "accumulators exceed tensor memory");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
-  static_assert(NB >= 2, "ring depth");
+  static_assert(NSTAGE >= 2, "ring depth");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
@@ -98,24 +97,19 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, GemmParams p) {
   using CF = Cfg<MT, BN>;
-  constexpr int NA = CF::NA;
-  constexpr int NB = CF::NB;
-  constexpr int PROD_A = CF::EPI_WARPS;
-  constexpr int PROD_B = CF::EPI_WARPS + 1;
-  constexpr int MMA_WARP = CF::EPI_WARPS + 2;
+  constexpr int NSTAGE = CF::NSTAGE;
+  constexpr int PRODUCER_WARP = CF::EPI_WARPS;
+  constexpr int MMA_WARP = CF::EPI_WARPS + 1;
   constexpr bool B_MN = EPI == EPI_ACCUM_MN;
   constexpr bool ACCUM = EPI == EPI_ACCUM || B_MN;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* ring_a = smem;
-  uint8_t* ring_b = smem + NA * CF::A_STAGE;
-  uint64_t* full_a = reinterpret_cast<uint64_t*>(ring_b + NB * CF::B_STAGE);
-  uint64_t* empty_a = full_a + NA;
-  uint64_t* full_b = empty_a + NA;
-  uint64_t* empty_b = full_b + NB;
-  uint64_t* tfull_bar = empty_b + NB;
+  uint8_t* stages = smem;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + NSTAGE * CF::STAGE_BYTES);
+  uint64_t* empty_bar = full_bar + NSTAGE;
+  uint64_t* tfull_bar = empty_bar + NSTAGE;
   uint64_t* tempty_bar = tfull_bar + CF::ACC_STAGES;
   uint64_t* drain_bar = tempty_bar + CF::ACC_STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
@@ -125,13 +119,9 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NA; ++i) {
-      mbar_init(&full_a[i], 1);
-      mbar_init(&empty_a[i], 1);
-    }
-    for (int i = 0; i < NB; ++i) {
-      mbar_init(&full_b[i], 1);
-      mbar_init(&empty_b[i], 1);
+    for (int i = 0; i < NSTAGE; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
     }
     for (int a = 0; a < CF::ACC_STAGES; ++a) {
       mbar_init(&tfull_bar[a], 1);
@@ -145,8 +135,10 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
     tmem_alloc(tmem_slot, CF::TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == PROD_A && lane == 0) prefetch_tmap(&tmA);
-  if (warp == PROD_B && lane == 0) prefetch_tmap(&tmB);
+  if (warp == PRODUCER_WARP && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -175,75 +167,69 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
   const int m_base = gm * MT * BM;
   const bool has_work = (t_end > t_begin) && (kb_end > kb_begin);
 
-  if (warp == PROD_A || warp == PROD_B) {
-    // one producer thread per ring; the B ring (streamed from DRAM) runs up to
-    // NB K-blocks ahead, the A ring (re-read from L2) up to NA
+  if (warp == PRODUCER_WARP) {
+    // One ring: the A rows (re-read from L2) and the B tile (streamed from DRAM)
+    // of a K block are requested together and fill one stage.  All CTAs walk K
+    // in the same order, so CTAs sharing the A rows read the same lines close
+    // together in time (P, larger than L2, is then fetched from DRAM once).
     if (lane == 0 && has_work) {
-      const bool is_a = warp == PROD_A;
-      const int nst = is_a ? NA : NB;
-      uint64_t* full = is_a ? full_a : full_b;
-      uint64_t* empty = is_a ? empty_a : empty_b;
-      const uint64_t pol = is_a ? policy_evict_last() : policy_evict_first();
+      const uint64_t pol_b = policy_evict_first();  // W or E: streamed once
+      const uint64_t pol_a = policy_evict_last();   // hidden rows or P: re-read per tile
       int stage = 0;
       uint32_t phase = 0, issued_mask = 0, last_phase = 0;
       bool ok = true;
       for (int t = t_begin; t < t_end && ok; ++t) {
         for (int kb = kb_begin; kb < kb_end; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.status)) {
             ok = false;
             break;
           }
-          if (is_a) {
-            mbar_arrive_expect_tx(&full[stage], CF::A_STAGE);
-            uint8_t* dst = ring_a + stage * CF::A_STAGE;
+          mbar_arrive_expect_tx(&full_bar[stage], CF::STAGE_BYTES);
+          uint8_t* s_a = stages + stage * CF::STAGE_BYTES;
+          uint8_t* s_b = s_a + CF::A_STAGE;
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
-              tma_load_2d_hint(dst + mt * CF::A_BYTES, &tmA, &full[stage], kb * BK,
-                               m_base + mt * BM, pol);
+          for (int mt = 0; mt < MT; ++mt)
+            tma_load_2d_hint(s_a + mt * CF::A_BYTES, &tmA, &full_bar[stage], kb * BK,
+                             m_base + mt * BM, pol_a);
+          if (B_MN) {
+            // B [K, N] with N contiguous: BN/64 boxes of 64 N-columns x 64 K-rows
+#pragma unroll
+            for (int g = 0; g < BN / 64; ++g)
+              tma_load_2d_hint(s_b + g * (BK * 128), &tmB, &full_bar[stage], t * BN + g * 64,
+                               kb * BK, pol_b);
           } else {
-            mbar_arrive_expect_tx(&full[stage], CF::B_STAGE);
-            uint8_t* dst = ring_b + stage * CF::B_STAGE;
-            if (B_MN) {
-              // B [K, N] with N contiguous: BN/64 boxes of 64 N-columns x 64 K-rows
-#pragma unroll
-              for (int g = 0; g < BN / 64; ++g)
-                tma_load_2d_hint(dst + g * (BK * 128), &tmB, &full[stage], t * BN + g * 64,
-                                 kb * BK, pol);
-            } else {
-              tma_load_2d_hint(dst, &tmB, &full[stage], kb * BK, t * BN, pol);
-            }
+            tma_load_2d_hint(s_b, &tmB, &full_bar[stage], kb * BK, t * BN, pol_b);
           }
           issued_mask |= 1u << stage;
           last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
-          if (++stage == nst) {
+          if (++stage == NSTAGE) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
       if (!ok) {  // let every copy already issued land before the CTA exits
-        for (int s = 0; s < nst; ++s)
-          if (issued_mask & (1u << s)) mbar_wait_drain(&full[s], (last_phase >> s) & 1u);
+        for (int s = 0; s < NSTAGE; ++s)
+          if (issued_mask & (1u << s)) mbar_wait_drain(&full_bar[s], (last_phase >> s) & 1u);
       }
     }
   } else if (warp == MMA_WARP) {
     if (lane == 0 && has_work) {
-      int sa = 0, sb = 0, acc = 0;
-      uint32_t pa = 0, pb = 0, acc_phase = 0;
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int t = t_begin; t < t_end && ok; ++t) {
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d_base = tmem_base + acc * CF::ACC_COLS;
         for (int kb = kb_begin; kb < kb_end; ++kb) {
-          if (!mbar_wait(&full_a[sa], pa, abort_flag, p.status) ||
-              !mbar_wait(&full_b[sb], pb, abort_flag, p.status)) {
+          if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(ring_a + sa * CF::A_STAGE);
-          const uint32_t b_addr = smem_u32(ring_b + sb * CF::B_STAGE);
+          const uint32_t a_addr = smem_u32(stages + stage * CF::STAGE_BYTES);
+          const uint32_t b_addr = a_addr + CF::A_STAGE;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             // K-major B: +32 bytes per 16 K inside the 128-byte row; MN-major B:
@@ -257,15 +243,10 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
                          (kb > kb_begin || kk > 0) ? 1u : 0u);
             }
           }
-          tc_commit(&empty_a[sa]);
-          tc_commit(&empty_b[sb]);
-          if (++sa == NA) {
-            sa = 0;
-            pa ^= 1u;
-          }
-          if (++sb == NB) {
-            sb = 0;
-            pb ^= 1u;
+          tc_commit(&empty_bar[stage]);
+          if (++stage == NSTAGE) {
+            stage = 0;
+            phase ^= 1u;
           }
         }
         if (!ok) break;

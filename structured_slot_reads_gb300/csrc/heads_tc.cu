@@ -3,11 +3,12 @@
 // For the canvas rows (tau-home.com "Refusing JSON token generation";
 // 24-ai.news "Token commit mechanism") the pass computes the row statistics of
 // softmax(h W^T / T) and, for self-conditioning, the unnormalised
-// probabilities  P~[i, v] = 2^(z_iv log2 e - r_i)  in bf16, where r_i is a
-// per-row reference that every CTA computes identically from the first 64
-// vocabulary entries (plus a fixed headroom).  Because r_i is common to all
-// CTAs, the per-CTA sums S_i = sum_v P~ add without rescaling and
-// p_iv = P~_iv / S_i exactly; the P.E GEMM applies 1/S_i in its reduction.
+// probabilities  P~[i, v] = 2^(z_iv log2 e - r_i)  in bf16.  The per-row
+// reference r_i (the row's largest scaled logit over the first 64 vocabulary
+// entries, plus a fixed headroom) is computed once by ref_kernel before the
+// pass and read by every CTA, so the per-CTA sums S_i = sum_v P~ add without
+// rescaling and p_iv = P~_iv / S_i exactly; the P.E GEMM applies 1/S_i in its
+// reduction.
 //
 // For the slot-read draw rows (sotaaz.com "The server accepts at most 26
 // alternatives per question": noise reads of an answer slot) the same W tiles
@@ -15,9 +16,11 @@
 // <= 16 draw rows (N = 16), so the draw rows' log-normalisers come out of the
 // same pass instead of a second stream of W.
 //
-// Tile geometry: BN vocabulary rows per tile (224 with draw rows so that
-// 2 x 224 canvas columns + 2 x 16 draw columns fill the 512 TMEM columns), 64-
-// element K blocks, 128-byte swizzled TMA tiles, one CTA per SM.
+// Tile geometry: BN vocabulary rows per tile (224 with draw rows, so that
+// 2 x 224 canvas columns + 2 x 16 draw columns fit the 512 TMEM columns), 64-
+// element K blocks, one shared-memory ring whose stages hold the canvas rows,
+// the W tile and the draw rows of a K block (128-byte swizzled by TMA), one
+// CTA per SM.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -34,8 +37,8 @@ using namespace dgk;
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int PRO_N = 64;         // prologue vocabulary entries for the reference
-constexpr float REF_HEADROOM = 24.f;  // log2 units added to the prologue max
+constexpr int REF_N = 64;             // vocabulary entries behind the reference
+constexpr float REF_HEADROOM = 24.f;  // log2 units added to the reference maximum
 constexpr float V_CLAMP = 100.f;      // exponent guard (log2 units above the reference)
 constexpr int DRAW_N = 16;
 constexpr float LOG2E = 1.4426950408889634f;
@@ -69,67 +72,113 @@ struct HeadsParams {
   int cpg, n_tiles;
   const float* inv_t;       // [M]
   const float* inv_t_draw;  // [n_draw]
+  const float* ref;         // [M] reference r (log2 units)
   float* part;              // canvas: 4 planes of [M][cpg]: s, t, best, idx
   float* part_draw;         // draws: 2 planes of [n_draw][cpg]: m, s
-  float* ref;               // [M] reference r (log2 units)
   __nv_bfloat16* probs;     // [M][ldp] or null
   long long ldp;
   int* status;
 };
 
+// Reference of each canvas row: max over the first 64 vocabulary entries of
+// (h . w_v) / T in log2 units, plus headroom.  One CTA per row; warp w owns
+// entries 8w..8w+7 and keeps their eight dot products (and loads) in flight.
+__global__ void ref_kernel(const __nv_bfloat16* h, const __nv_bfloat16* w, const float* inv_t,
+                           int M, int V, int D, float* ref) {
+  constexpr int PER_WARP = REF_N / 8;
+  const int row = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ float wmax[8];
+  const uint4* x = reinterpret_cast<const uint4*>(h + (long long)row * D);
+  const int n16 = D / 8;
+  float acc[PER_WARP];
+#pragma unroll
+  for (int u = 0; u < PER_WARP; ++u) acc[u] = 0.f;
+  const int v0 = warp * PER_WARP;
+#pragma unroll 2
+  for (int i = lane; i < n16; i += 32) {
+    const uint4 a = x[i];
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    uint4 b[PER_WARP];
+#pragma unroll
+    for (int u = 0; u < PER_WARP; ++u)
+      b[u] = (v0 + u < V) ? __ldg(reinterpret_cast<const uint4*>(w + (long long)(v0 + u) * D) + i)
+                          : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < PER_WARP; ++u) {
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b[u]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 fa = __bfloat1622float2(a2[q]);
+        const float2 fb = __bfloat1622float2(b2[q]);
+        acc[u] = fmaf(fa.x, fb.x, acc[u]);
+        acc[u] = fmaf(fa.y, fb.y, acc[u]);
+      }
+    }
+  }
+  float best = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < PER_WARP; ++u) {
+    float s = acc[u];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (v0 + u < V) best = fmaxf(best, s);
+  }
+  if (lane == 0) wmax[warp] = best;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m = wmax[0];
+    for (int i = 1; i < 8; ++i) m = fmaxf(m, wmax[i]);
+    ref[row] = m * inv_t[row] * LOG2E + REF_HEADROOM;
+  }
+}
+
 template <int MT, int BN, bool DRAWS>
 struct HCfg {
   static constexpr int A_BYTES = BM * BK * 2;             // one 128-row canvas tile
-  static constexpr int A_STAGE = MT * A_BYTES;            // hidden rows: L2, shallow ring
-  static constexpr int W_SLOT = BN * BK * 2;              // W tile: DRAM, deep ring
+  static constexpr int A_STAGE = MT * A_BYTES;
+  static constexpr int W_SLOT = BN * BK * 2;
   static constexpr int D_BYTES = DRAWS ? DRAW_N * BK * 2 : 0;
-  static constexpr int B_STAGE = W_SLOT + D_BYTES;
-  static constexpr int NA = 2;
+  static constexpr int STAGE_BYTES = A_STAGE + W_SLOT + D_BYTES;
   static constexpr int DRAW_COLS = DRAWS ? 2 * DRAW_N : 0;
   static constexpr int ACC_COLS = MT * BN + DRAW_COLS;
   static constexpr int ACC_STAGES = (2 * ACC_COLS <= 512) ? 2 : 1;
   static constexpr int TMEM_COLS = 512;
   static constexpr int EPI_WARPS = 4 * MT;
-  static constexpr int THREADS = (EPI_WARPS + 3) * 32;    // + two producers + MMA
+  static constexpr int THREADS = (EPI_WARPS + 2) * 32;    // + producer + MMA issuer
   static constexpr int BAR_BYTES = 512 + EPI_WARPS * DRAW_N * 8;
-  static constexpr int NB_FIT = (232448 - 1024 - BAR_BYTES - NA * A_STAGE) / B_STAGE;
-  static constexpr int NB = NB_FIT > 8 ? 8 : NB_FIT;
-  static constexpr int SMEM_BYTES = 1024 + NA * A_STAGE + NB * B_STAGE + BAR_BYTES;
+  static constexpr int NS_FIT = (232448 - 1024 - BAR_BYTES) / STAGE_BYTES;
+  static constexpr int NSTAGE = NS_FIT > 8 ? 8 : NS_FIT;
+  static constexpr int SMEM_BYTES = 1024 + NSTAGE * STAGE_BYTES + BAR_BYTES;
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
-  static constexpr uint32_t IDESC_PRO = idesc_bf16_f32(BM, PRO_N);
   static constexpr uint32_t IDESC_DRAW = idesc_bf16_f32(BM, DRAW_N);
   static constexpr int HALF1_ROW = BN - 128;  // the second swapped MMA reads W rows [BN-128, BN)
+  static constexpr uint32_t TX = A_STAGE + W_SLOT;
   static_assert(ACC_COLS <= 512, "accumulators exceed tensor memory");
-  static_assert(BN % 32 == 0 && BN <= 256 && BN >= PRO_N, "BN");
+  static_assert(BN % 32 == 0 && BN <= 256, "BN");
   static_assert(!DRAWS || (BN >= 128 && BN % 8 == 0), "swapped draw MMA geometry");
-  static_assert(B_STAGE % 1024 == 0, "ring slots must stay 1 KB aligned");
-  static_assert(NB >= 2 && SMEM_BYTES <= 232448, "shared memory");
+  static_assert(STAGE_BYTES % 1024 == 0 && W_SLOT % 1024 == 0, "stages stay 1 KB aligned");
+  static_assert(NSTAGE >= 2 && SMEM_BYTES <= 232448, "shared memory");
 };
 
 template <int MT, int BN, bool DRAWS>
 __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
     heads_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const __grid_constant__ CUtensorMap tmB64,
                  const __grid_constant__ CUtensorMap tmD, HeadsParams p) {
   using CF = HCfg<MT, BN, DRAWS>;
-  constexpr int NA = CF::NA;
-  constexpr int NB = CF::NB;
-  constexpr int PROD_A = CF::EPI_WARPS;
-  constexpr int PROD_B = CF::EPI_WARPS + 1;
-  constexpr int MMA_WARP = CF::EPI_WARPS + 2;
+  constexpr int NSTAGE = CF::NSTAGE;
+  constexpr int PRODUCER_WARP = CF::EPI_WARPS;
+  constexpr int MMA_WARP = CF::EPI_WARPS + 1;
   constexpr int EPI_THREADS = CF::EPI_WARPS * 32;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* ring_a = smem;
-  uint8_t* ring_b = smem + NA * CF::A_STAGE;
-  uint8_t* bar_base = ring_b + NB * CF::B_STAGE;
-  uint64_t* full_a = reinterpret_cast<uint64_t*>(bar_base);
-  uint64_t* empty_a = full_a + NA;
-  uint64_t* full_b = empty_a + NA;
-  uint64_t* empty_b = full_b + NB;
-  uint64_t* tfull_bar = empty_b + NB;
+  uint8_t* stages = smem;
+  uint8_t* bar_base = smem + NSTAGE * CF::STAGE_BYTES;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(bar_base);
+  uint64_t* empty_bar = full_bar + NSTAGE;
+  uint64_t* tfull_bar = empty_bar + NSTAGE;
   uint64_t* tempty_bar = tfull_bar + CF::ACC_STAGES;
   uint64_t* drain_bar = tempty_bar + CF::ACC_STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
@@ -140,13 +189,9 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NA; ++i) {
-      mbar_init(&full_a[i], 1);
-      mbar_init(&empty_a[i], 1);
-    }
-    for (int i = 0; i < NB; ++i) {
-      mbar_init(&full_b[i], 1);
-      mbar_init(&empty_b[i], 1);
+    for (int i = 0; i < NSTAGE; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
     }
     for (int a = 0; a < CF::ACC_STAGES; ++a) {
       mbar_init(&tfull_bar[a], 1);
@@ -160,10 +205,9 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
     tmem_alloc(tmem_slot, CF::TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == PROD_A && lane == 0) prefetch_tmap(&tmA);
-  if (warp == PROD_B && lane == 0) {
+  if (warp == PRODUCER_WARP && lane == 0) {
+    prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
-    prefetch_tmap(&tmB64);
     if (DRAWS) prefetch_tmap(&tmD);
   }
   tc_fence_before();
@@ -171,7 +215,6 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  // tile t_begin-1 is the reference prologue (vocabulary 0..63, canvas rows only)
   const int total_kb = (p.K + BK - 1) / BK;
   const int gm = blockIdx.x / p.cpg;
   const int gn = blockIdx.x % p.cpg;
@@ -180,106 +223,84 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
   const int m_base = gm * MT * BM;
   const bool draws_here = DRAWS && gm == 0 && p.n_draw > 0;
 
-  if (warp == PROD_A || warp == PROD_B) {
+  if (warp == PRODUCER_WARP) {
     if (lane == 0) {
-      const bool is_a = warp == PROD_A;
-      const int nst = is_a ? NA : NB;
-      uint64_t* full = is_a ? full_a : full_b;
-      uint64_t* empty = is_a ? empty_a : empty_b;
       const uint64_t pol_keep = policy_evict_last();
       const uint64_t pol_stream = policy_evict_first();
       int stage = 0;
       uint32_t phase = 0, issued_mask = 0, last_phase = 0;
       bool ok = true;
-      for (int t = t_begin - 1; t < t_end && ok; ++t) {
-        const bool pro = t < t_begin;
+      for (int t = t_begin; t < t_end && ok; ++t) {
         for (int kb = 0; kb < total_kb; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.status)) {
             ok = false;
             break;
           }
-          if (is_a) {
-            mbar_arrive_expect_tx(&full[stage], CF::A_STAGE);
-            uint8_t* dst = ring_a + stage * CF::A_STAGE;
+          uint8_t* s_a = stages + stage * CF::STAGE_BYTES;
+          uint8_t* s_w = s_a + CF::A_STAGE;
+          mbar_arrive_expect_tx(&full_bar[stage], CF::TX + (draws_here ? CF::D_BYTES : 0));
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
-              tma_load_2d_hint(dst + mt * CF::A_BYTES, &tmA, &full[stage], kb * BK,
-                               m_base + mt * BM, pol_keep);
-          } else {
-            uint8_t* dst = ring_b + stage * CF::B_STAGE;
-            if (pro) {
-              mbar_arrive_expect_tx(&full[stage], PRO_N * BK * 2);
-              tma_load_2d_hint(dst, &tmB64, &full[stage], kb * BK, 0, pol_keep);
-            } else {
-              mbar_arrive_expect_tx(&full[stage], CF::W_SLOT + (draws_here ? CF::D_BYTES : 0));
-              tma_load_2d_hint(dst, &tmB, &full[stage], kb * BK, t * BN, pol_stream);
-              if (draws_here)
-                tma_load_2d_hint(dst + CF::W_SLOT, &tmD, &full[stage], kb * BK, 0, pol_keep);
-            }
-          }
+          for (int mt = 0; mt < MT; ++mt)
+            tma_load_2d_hint(s_a + mt * CF::A_BYTES, &tmA, &full_bar[stage], kb * BK,
+                             m_base + mt * BM, pol_keep);
+          tma_load_2d_hint(s_w, &tmB, &full_bar[stage], kb * BK, t * BN, pol_stream);
+          if (draws_here)
+            tma_load_2d_hint(s_w + CF::W_SLOT, &tmD, &full_bar[stage], kb * BK, 0, pol_keep);
           issued_mask |= 1u << stage;
           last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
-          if (++stage == nst) {
+          if (++stage == NSTAGE) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
       if (!ok) {
-        for (int s = 0; s < nst; ++s)
-          if (issued_mask & (1u << s)) mbar_wait_drain(&full[s], (last_phase >> s) & 1u);
+        for (int s = 0; s < NSTAGE; ++s)
+          if (issued_mask & (1u << s)) mbar_wait_drain(&full_bar[s], (last_phase >> s) & 1u);
       }
     }
   } else if (warp == MMA_WARP) {
     if (lane == 0) {
-      int sa = 0, sb = 0, acc = 0;
-      uint32_t pa = 0, pb = 0, acc_phase = 0;
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int t = t_begin - 1; t < t_end && ok; ++t) {
-        const bool pro = t < t_begin;
+      for (int t = t_begin; t < t_end && ok; ++t) {
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d_base = tmem_base + acc * CF::ACC_COLS;
         for (int kb = 0; kb < total_kb; ++kb) {
-          if (!mbar_wait(&full_a[sa], pa, abort_flag, p.status) ||
-              !mbar_wait(&full_b[sb], pb, abort_flag, p.status)) {
+          if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(ring_a + sa * CF::A_STAGE);
-          const uint32_t b_addr = smem_u32(ring_b + sb * CF::B_STAGE);
-          const uint32_t d_addr = b_addr + CF::W_SLOT;
+          const uint32_t a_addr = smem_u32(stages + stage * CF::STAGE_BYTES);
+          const uint32_t w_addr = a_addr + CF::A_STAGE;
+          const uint32_t d_addr = w_addr + CF::W_SLOT;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint32_t acc_flag = (kb > 0 || kk > 0) ? 1u : 0u;
-            const uint64_t bdesc = sw128_kmajor_desc(b_addr + kk * 32);
+            const uint64_t bdesc = sw128_kmajor_desc(w_addr + kk * 32);
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
               const uint64_t adesc = sw128_kmajor_desc(a_addr + mt * CF::A_BYTES + kk * 32);
-              tc_mma_f16(d_base + mt * BN, adesc, bdesc, pro ? CF::IDESC_PRO : CF::IDESC,
-                         acc_flag);
+              tc_mma_f16(d_base + mt * BN, adesc, bdesc, CF::IDESC, acc_flag);
             }
-            if (DRAWS && draws_here && !pro) {
+            if (DRAWS && draws_here) {
               const uint64_t ddesc = sw128_kmajor_desc(d_addr + kk * 32);
 #pragma unroll
               for (int half = 0; half < 2; ++half) {
                 const uint32_t row0 = half ? CF::HALF1_ROW : 0;
-                const uint64_t wdesc = sw128_kmajor_desc(b_addr + row0 * 128 + kk * 32);
+                const uint64_t wdesc = sw128_kmajor_desc(w_addr + row0 * 128 + kk * 32);
                 tc_mma_f16(d_base + MT * BN + half * DRAW_N, wdesc, ddesc, CF::IDESC_DRAW,
                            acc_flag);
               }
             }
           }
-          tc_commit(&empty_a[sa]);
-          tc_commit(&empty_b[sb]);
-          if (++sa == NA) {
-            sa = 0;
-            pa ^= 1u;
-          }
-          if (++sb == NB) {
-            sb = 0;
-            pb ^= 1u;
+          tc_commit(&empty_bar[stage]);
+          if (++stage == NSTAGE) {
+            stage = 0;
+            phase ^= 1u;
           }
         }
         if (!ok) break;
@@ -299,7 +320,7 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
     const int row = m_base + mt * BM + quarter * 32 + lane;
     const bool row_ok = row < p.M;
     const float scale = row_ok ? __ldg(p.inv_t + row) * LOG2E : 0.f;
-    float r_ref = 0.f;
+    const float r_ref = row_ok ? __ldg(p.ref + row) : 0.f;
     float s_run = 0.f, t_run = 0.f, best = -INFINITY;
     int best_idx = 0x7fffffff;
     bool clamped = false;
@@ -311,106 +332,97 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
       ds[j] = 0.f;
       dscale[j] = (DRAWS && j < p.n_draw) ? __ldg(p.inv_t_draw + j) * LOG2E : 0.f;
     }
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = t_begin - 1; t < t_end; ++t) {
-      const bool pro = t < t_begin;
+    for (int t = t_begin; t < t_end; ++t) {
       if (!mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, p.status)) break;
       tc_fence_after();
-      const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
       const uint32_t taddr = tmem_base + lane_base + acc * CF::ACC_COLS + mt * BN;
-      if (pro) {
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < PRO_N / 32; ++c) {
-          uint32_t r[32];
-          __syncwarp();
-          tmem_ld_32x32b_x32(taddr + c * 32, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(r[j]));
-        }
-        r_ref = mx * scale + REF_HEADROOM;
-        if (row_ok && gn == 0) p.ref[row] = r_ref;
-      } else {
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          __syncwarp();
-          tmem_ld_32x32b_x32(taddr + c * 32, r);
-          tmem_ld_wait();
-          const int n0 = t * BN + c * 32;
-          if (!row_ok || n0 >= p.V) continue;
-          const bool full = n0 + 32 <= p.V;
-          float cmax = -INFINITY;
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (full || n0 + j < p.V) cmax = fmaxf(cmax, __uint_as_float(r[j]));
-          if (cmax > best) {  // columns ascend, so the first occurrence is the lowest id
-            int first = 0x7fffffff;
-#pragma unroll
-            for (int j = 31; j >= 0; --j)
-              if ((full || n0 + j < p.V) && __uint_as_float(r[j]) == cmax) first = n0 + j;
-            best = cmax;
-            best_idx = first;
-          }
-          if (fmaf(cmax, scale, -r_ref) > V_CLAMP) clamped = true;
-          float e[32];
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld_32x32b_x32(taddr + c * 32, r);
+        tmem_ld_wait();
+        const int n0 = t * BN + c * 32;
+        if (!row_ok || n0 >= p.V) continue;
+        float e[32];
+        float cmax = -INFINITY;
+        if (n0 + 32 <= p.V) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const float a = __uint_as_float(r[j]);
-            const float v = fminf(fmaf(a, scale, -r_ref), V_CLAMP);
-            const bool ok = full || n0 + j < p.V;
-            e[j] = ok ? ex2(v) : 0.f;
+            cmax = fmaxf(cmax, a);
+            e[j] = ex2(fminf(fmaf(a, scale, -r_ref), V_CLAMP));
             s_run += e[j];
             t_run = fmaf(e[j], a, t_run);
           }
-          if (p.probs) {
-            __nv_bfloat16* dst = p.probs + (long long)row * p.ldp + n0;
-            if (full) {
+        } else {
 #pragma unroll
-              for (int j = 0; j < 32; j += 8) {
-                uint4 pk;
-                __nv_bfloat162 b0 = __floats2bfloat162_rn(e[j + 0], e[j + 1]);
-                __nv_bfloat162 b1 = __floats2bfloat162_rn(e[j + 2], e[j + 3]);
-                __nv_bfloat162 b2 = __floats2bfloat162_rn(e[j + 4], e[j + 5]);
-                __nv_bfloat162 b3 = __floats2bfloat162_rn(e[j + 6], e[j + 7]);
-                pk.x = *reinterpret_cast<uint32_t*>(&b0);
-                pk.y = *reinterpret_cast<uint32_t*>(&b1);
-                pk.z = *reinterpret_cast<uint32_t*>(&b2);
-                pk.w = *reinterpret_cast<uint32_t*>(&b3);
-                *reinterpret_cast<uint4*>(dst + j) = pk;
-              }
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (n0 + j < p.V) dst[j] = __float2bfloat16_rn(e[j]);
-            }
+          for (int j = 0; j < 32; ++j) {
+            const float a = __uint_as_float(r[j]);
+            const bool ok = n0 + j < p.V;
+            if (ok) cmax = fmaxf(cmax, a);
+            e[j] = ok ? ex2(fminf(fmaf(a, scale, -r_ref), V_CLAMP)) : 0.f;
+            s_run += e[j];
+            t_run = fmaf(e[j], a, t_run);
           }
         }
-        if (DRAWS && draws_here) {
-          // warpgroup mt handles half mt (with one M-tile, warpgroup 0 does both)
+        if (cmax > best) {  // columns ascend, so the first occurrence is the lowest id
+          int first = 0x7fffffff;
 #pragma unroll
-          for (int hh = 0; hh < (MT == 1 ? 2 : 1); ++hh) {
-            const int half = (MT == 1) ? hh : mt;
-            uint32_t r[DRAW_N];
-            __syncwarp();
-            tmem_ld_32x32b_x16(
-                tmem_base + lane_base + acc * CF::ACC_COLS + MT * BN + half * DRAW_N, r);
-            tmem_ld_wait();
-            // row of the W tile on this lane; half 1 starts at row BN-128, so its
-            // lanes below row 128 repeat half 0 and are skipped
-            const int vl = (half ? CF::HALF1_ROW : 0) + quarter * 32 + lane;
-            const int vocab = t * BN + vl;
-            if ((half == 0 || vl >= 128) && vl < BN && vocab < p.V) {
+          for (int j = 31; j >= 0; --j)
+            if (n0 + j < p.V && __uint_as_float(r[j]) == cmax) first = n0 + j;
+          best = cmax;
+          best_idx = first;
+        }
+        if (fmaf(cmax, scale, -r_ref) > V_CLAMP) clamped = true;
+        if (p.probs) {
+          __nv_bfloat16* dst = p.probs + (long long)row * p.ldp + n0;
+          if (n0 + 32 <= p.V) {
 #pragma unroll
-              for (int j = 0; j < DRAW_N; ++j) {
-                if (j < p.n_draw) {
-                  const float v = __uint_as_float(r[j]) * dscale[j];
-                  const float mn = fmaxf(dm[j], v);
-                  ds[j] = ds[j] * ex2(dm[j] - mn) + ex2(v - mn);
-                  dm[j] = mn;
-                }
+            for (int j = 0; j < 32; j += 8) {
+              uint4 pk;
+              __nv_bfloat162 b0 = __floats2bfloat162_rn(e[j + 0], e[j + 1]);
+              __nv_bfloat162 b1 = __floats2bfloat162_rn(e[j + 2], e[j + 3]);
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(e[j + 4], e[j + 5]);
+              __nv_bfloat162 b3 = __floats2bfloat162_rn(e[j + 6], e[j + 7]);
+              pk.x = *reinterpret_cast<uint32_t*>(&b0);
+              pk.y = *reinterpret_cast<uint32_t*>(&b1);
+              pk.z = *reinterpret_cast<uint32_t*>(&b2);
+              pk.w = *reinterpret_cast<uint32_t*>(&b3);
+              *reinterpret_cast<uint4*>(dst + j) = pk;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (n0 + j < p.V) dst[j] = __float2bfloat16_rn(e[j]);
+          }
+        }
+      }
+      if (DRAWS && draws_here) {
+        // warpgroup mt handles half mt (with one M-tile, warpgroup 0 does both)
+#pragma unroll
+        for (int hh = 0; hh < (MT == 1 ? 2 : 1); ++hh) {
+          const int half = (MT == 1) ? hh : mt;
+          uint32_t r[DRAW_N];
+          __syncwarp();
+          tmem_ld_32x32b_x16(tmem_base + lane_base + acc * CF::ACC_COLS + MT * BN + half * DRAW_N,
+                             r);
+          tmem_ld_wait();
+          // row of the W tile on this lane; half 1 starts at row BN-128, so its
+          // lanes below row 128 repeat half 0 and are skipped
+          const int vl = (half ? CF::HALF1_ROW : 0) + quarter * 32 + lane;
+          const int vocab = t * BN + vl;
+          if ((half == 0 || vl >= 128) && vl < BN && vocab < p.V) {
+#pragma unroll
+            for (int j = 0; j < DRAW_N; ++j) {
+              if (j < p.n_draw) {
+                const float v = __uint_as_float(r[j]) * dscale[j];
+                const float mn = fmaxf(dm[j], v);
+                ds[j] = ds[j] * ex2(dm[j] - mn) + ex2(v - mn);
+                dm[j] = mn;
               }
             }
           }
@@ -541,8 +553,8 @@ __global__ void draws_finalize_kernel(const float* part_draw, int cpg, int n_dra
 }
 
 template <int MT, int BN, bool DRAWS>
-cudaError_t launch_heads(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb64,
-                         const CUtensorMap& td, const HeadsParams& p, int grid, cudaStream_t st) {
+cudaError_t launch_heads(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
+                         const HeadsParams& p, int grid, cudaStream_t st) {
   using CF = HCfg<MT, BN, DRAWS>;
   static bool attr = false;
   if (!attr) {
@@ -552,7 +564,7 @@ cudaError_t launch_heads(const CUtensorMap& ta, const CUtensorMap& tb, const CUt
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  heads_kernel<MT, BN, DRAWS><<<grid, CF::THREADS, CF::SMEM_BYTES, st>>>(ta, tb, tb64, td, p);
+  heads_kernel<MT, BN, DRAWS><<<grid, CF::THREADS, CF::SMEM_BYTES, st>>>(ta, tb, td, p);
   return cudaGetLastError();
 }
 
@@ -601,30 +613,33 @@ cudaError_t denoise_heads(const uint16_t* h, int M, const uint16_t* draw_rows, i
   wp += align_up((size_t)4 * p.cpg * M * 4, 256);
   p.part_draw = reinterpret_cast<float*>(wp);
   wp += align_up((size_t)2 * p.cpg * DRAW_N * 4, 256);
-  p.ref = reinterpret_cast<float*>(wp);
+  float* ref = reinterpret_cast<float*>(wp);
+  p.ref = ref;
   p.probs = reinterpret_cast<__nv_bfloat16*>(probs);
   p.ldp = (long long)probs_ld;
   p.status = status_ptr();
-  CUtensorMap ta, tb, tb64, td;
+  CUtensorMap ta, tb, td;
   if (!make_tmap_bf16_2d(&ta, h, D, M, (uint64_t)D * 2, BK, BM)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16_2d(&tb, w, D, V, (uint64_t)D * 2, BK, bn)) return cudaErrorInvalidValue;
-  if (!make_tmap_bf16_2d(&tb64, w, D, V, (uint64_t)D * 2, BK, PRO_N)) return cudaErrorInvalidValue;
   if (n_draw > 0) {
     if (!make_tmap_bf16_2d(&td, draw_rows, D, n_draw, (uint64_t)D * 2, BK, DRAW_N))
       return cudaErrorInvalidValue;
   } else {
-    td = tb64;  // unused
+    td = tb;  // unused
   }
-  const int grid = groups * p.cpg;
-  cudaError_t e;
-  if (n_draw > 0)
-    e = (mt == 1) ? launch_heads<1, 224, true>(ta, tb, tb64, td, p, grid, st)
-                  : launch_heads<2, 224, true>(ta, tb, tb64, td, p, grid, st);
-  else
-    e = (mt == 1) ? launch_heads<1, 256, false>(ta, tb, tb64, td, p, grid, st)
-                  : launch_heads<2, 256, false>(ta, tb, tb64, td, p, grid, st);
+  ref_kernel<<<M, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(h),
+                                reinterpret_cast<const __nv_bfloat16*>(w), inv_t, M, V, D, ref);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  heads_finalize_kernel<<<(M + 7) / 8, 256, 0, st>>>(p.part, p.cpg, M, inv_t, p.ref, out.lse,
+  const int grid = groups * p.cpg;
+  if (n_draw > 0)
+    e = (mt == 1) ? launch_heads<1, 224, true>(ta, tb, td, p, grid, st)
+                  : launch_heads<2, 224, true>(ta, tb, td, p, grid, st);
+  else
+    e = (mt == 1) ? launch_heads<1, 256, false>(ta, tb, td, p, grid, st)
+                  : launch_heads<2, 256, false>(ta, tb, td, p, grid, st);
+  if (e != cudaSuccess) return e;
+  heads_finalize_kernel<<<(M + 7) / 8, 256, 0, st>>>(p.part, p.cpg, M, inv_t, ref, out.lse,
                                                      out.entropy, out.maxz, out.argmax,
                                                      prob_scale);
   e = cudaGetLastError();
