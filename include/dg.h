@@ -267,6 +267,29 @@ const char* dg_strerror(int code);
  * cached); -1 if no device is visible. */
 int dg_num_sms(void);
 
+/* ---- lm-head pass without a caller-provided workspace -------------------
+ * The pages describe nothing like this call; it exists for callers that cannot
+ * allocate device memory or pass the library a buffer of their own -- a
+ * serving runtime whose allocator is locked after start-up, or a plugin that
+ * only receives the tensors it works on.  It computes exactly what
+ * dg_lmhead_logsoftmax_entropy computes, with the same arguments minus the
+ * workspace: the per-CTA partial statistics live in a fixed array of 2.5 MiB
+ * compiled into the library (held on every GPU that loads it until the
+ * process exits).
+ *  - M may be at most DG_NOALLOC_MAX_ROWS; larger M returns DG_ERR_SHAPE.
+ *  - The first call on a device looks up the array's device address (a
+ *    runtime query, no allocation); make that first call before any stream
+ *    capture.  Later calls on that device reuse the address.
+ *  - The array is shared by every call on a device and keeps the last call's
+ *    contents (each launch overwrites all of it that it reads, so nothing needs
+ *    clearing).  Calls whose work overlaps on the GPU, e.g. on two streams
+ *    without ordering between them, race on it: order them on one stream. */
+#define DG_NOALLOC_MAX_ROWS 512
+int dg_lmhead_logsoftmax_entropy_noalloc(const dg_dims* dims, const uint16_t* h, int M,
+                                         const uint16_t* w, const float* inv_t, float* lse,
+                                         float* entropy, float* maxz, int32_t* argmax,
+                                         void* stream);
+
 #ifdef __cplusplus
 }
 #endif

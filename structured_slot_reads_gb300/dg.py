@@ -23,6 +23,7 @@ DG_DEV_RANGE = 16
 DG_WS_ATTN, DG_WS_LMHEAD, DG_WS_SLOT_READ, DG_WS_SELFCOND = 1, 2, 3, 4
 DG_WS_HEADS, DG_WS_PROBS_EMBED = 5, 6
 DG_MAX_LABELS = MAX_LABELS = 26
+DG_NOALLOC_MAX_ROWS = 512
 
 
 class DgError(RuntimeError):
@@ -62,6 +63,7 @@ _SIGS = {
     "dg_denoise_heads": [DP, P, I, P, I, P, P, P, P, P, P, P, P, P, P, Z, P, Z, P],
     "dg_selfcond_from_probs": [DP, P, Z, P, I, P, P, P, Z, P],
     "dg_probs_ld": [I],
+    "dg_lmhead_logsoftmax_entropy_noalloc": [DP, P, I, P, P, P, P, P, P, P],
     "dg_canvas_update": [DP, P, P, P, P, P, I, P, P],
     "dg_philox_fill": [U64, P, I, P, P],
     "dg_validate_slots": [DP, P, P, P, I, I],
@@ -198,6 +200,15 @@ def dg_selfcond_from_probs(dims, probs, probs_ld, prob_scale, M, e, out, workspa
 
 def dg_probs_ld(V):
     return int(lib().dg_probs_ld(V))
+
+
+def dg_lmhead_logsoftmax_entropy_noalloc(dims, h, M, w, inv_t, lse, entropy, maxz, argmax,
+                                         stream=None):
+    """dg_lmhead_logsoftmax_entropy for callers that cannot allocate a workspace:
+    the scratch is a fixed array inside the library (M <= DG_NOALLOC_MAX_ROWS)."""
+    return lib().dg_lmhead_logsoftmax_entropy_noalloc(ctypes.byref(dims), _p(h), M, _p(w),
+                                                      _p(inv_t), _p(lse), _p(entropy), _p(maxz),
+                                                      _p(argmax), _s(stream))
 
 
 
