@@ -138,7 +138,9 @@ int dg_slot_noise(const dg_dims* dims, const uint16_t* h, int M, const uint16_t*
  *   label_ids [S, 26] int32 (first n_labels[s] used);  n_labels [S] int32
  *   q_avg [S, 26] fp32 (zero past n_labels);  h_slot [S] fp32;  chosen [S] int32
  *   lp_draws [S, R, 26] fp32;  resampled [S] uint8;  n_reads [S] int32
- * R is the number of draw rows per slot; 1 <= samples <= R <= 8. */
+ * R is the number of draw rows per slot; 1 <= samples <= R <= 8.  A slot with
+ * n_labels[s] == 0 is a question that was not asked (see dg_ask_if_select): it
+ * is not read; chosen = -1, n_reads = 0 and its outputs are zero. */
 int dg_slot_finish(const dg_dims* dims, const uint16_t* rows, const float* inv_t_rows,
                    const float* lse_rows, const uint16_t* w, const int32_t* label_ids,
                    const int32_t* n_labels, int S, int R, int samples, float gate,
@@ -158,6 +160,25 @@ int dg_slot_read(const dg_dims* dims, const uint16_t* h, int M, const uint16_t* 
                  int32_t* chosen, float* lp_draws, uint8_t* resampled,
                  int32_t* n_reads, int32_t* noise_tok_out, void* workspace,
                  size_t workspace_bytes, void* stream);
+
+/* ---- a7: ask_if gating of a second read stage --------------------------
+ * sotaaz.com, "The server accepts at most 26 alternatives per question": a
+ * question carrying ask_if is read only when the earlier answer matches (77
+ * intents read as a 9-way group question, then the chosen group's items).
+ * Question q depends on stage-1 slot cond_slot[q] and fires when
+ * chosen1[cond_slot[q]] == cond_value[q]; it fills stage-2 slot q_owner[q].
+ * Each stage-2 slot j receives the labels of the first fired question that
+ * owns it, or n_labels2[j] = 0 (not asked, skipped by dg_slot_finish).  The
+ * decision stays on the device: no host round trip between the stages.
+ *   chosen1 [S1] int32 (dg_slot_read / dg_slot_finish output)
+ *   cond_slot, cond_value, q_owner [Q] int32;  q_label_ids [Q, 26] int32
+ *   q_n_labels [Q] int32;  label_ids2 [S2, 26] int32 (-1 padded);
+ *   n_labels2 [S2] int32;  fired [Q] uint8 (may be NULL).
+ * A cond_slot outside [0, S1) sets DG_DEV_BAD_INDEX and never fires. */
+int dg_ask_if_select(const int32_t* chosen1, int S1, const int32_t* cond_slot,
+                     const int32_t* cond_value, const int32_t* q_owner,
+                     const int32_t* q_label_ids, const int32_t* q_n_labels, int Q, int S2,
+                     int32_t* label_ids2, int32_t* n_labels2, uint8_t* fired, void* stream);
 
 /* ---- a4: entropy-ordered commit ----------------------------------------
  * 24-ai.news, "Token commit mechanism": accept the most confident tokens first

@@ -42,5 +42,6 @@ from .step import (  # noqa: F401
     selfcond_embed,
     canvas_update,
     ask_if_fires,
+    ask_if_select,
     denoise_loop,
 )

@@ -215,6 +215,10 @@ def slot_read(z_lab, lse_draw, n_labels, samples, gate):
     h_draw = np.zeros((S, R))
     for s in range(S):
         n = int(n_labels[s])
+        if n == 0:  # a question whose ask_if did not fire: not read
+            chosen[s] = -1
+            lp[s] = 0.0
+            continue
         qs = []
         for r in range(R):
             z = np.asarray(z_lab[s, r, :n], np.float64)
@@ -242,6 +246,31 @@ def ask_if_fires(stage1_chosen, ask_if_value):
     """sotaaz.com, "The server accepts at most 26 alternatives per question":
     a question carrying ``ask_if`` is read only when the earlier answer matches."""
     return int(stage1_chosen) == int(ask_if_value)
+
+
+def ask_if_select(chosen1, cond_slot, cond_value, q_owner, q_label_ids, q_n_labels, S2):
+    """Stage-2 slot table from the stage-1 answers (same page and section).
+
+    Question q asks its labels at stage-2 slot q_owner[q] if the stage-1 answer
+    of slot cond_slot[q] equals cond_value[q].  Reading: when several fired
+    questions own one slot the first (lowest q) is read; a slot with none is not
+    asked (n_labels 0).  Returns label_ids2 [S2, 26] (-1 padded), n_labels2 [S2],
+    fired [Q].
+    """
+    Q = len(cond_slot)
+    fired = np.array([1 if 0 <= cond_slot[q] < len(chosen1)
+                      and ask_if_fires(chosen1[cond_slot[q]], cond_value[q]) else 0
+                      for q in range(Q)], dtype=np.int64)
+    label_ids2 = np.full((S2, 26), -1, dtype=np.int64)
+    n_labels2 = np.zeros(S2, dtype=np.int64)
+    for j in range(S2):
+        for q in range(Q):
+            if q_owner[q] == j and fired[q]:
+                n = int(q_n_labels[q])
+                n_labels2[j] = n
+                label_ids2[j, :n] = q_label_ids[q, :n]
+                break
+    return label_ids2, n_labels2, fired
 
 
 # --------------------------------------------------------------------------

@@ -387,6 +387,20 @@ int dg_slot_read(const dg_dims* d, const uint16_t* h, int M, const uint16_t* w, 
   return launch_result(err);
 }
 
+int dg_ask_if_select(const int32_t* chosen1, int S1, const int32_t* cond_slot,
+                     const int32_t* cond_value, const int32_t* q_owner,
+                     const int32_t* q_label_ids, const int32_t* q_n_labels, int Q, int S2,
+                     int32_t* label_ids2, int32_t* n_labels2, uint8_t* fired, void* stream) {
+  if (S1 < 0 || Q < 0 || S2 < 0) return DG_ERR_ARG;
+  if (S2 > 0 && (!label_ids2 || !n_labels2)) return DG_ERR_ARG;
+  if (Q > 0 && (!chosen1 || !cond_slot || !cond_value || !q_owner || !q_label_ids ||
+                !q_n_labels))
+    return DG_ERR_ARG;
+  return launch_result(dgi::ask_if_select(chosen1, S1, cond_slot, cond_value, q_owner,
+                                          q_label_ids, q_n_labels, Q, S2, label_ids2, n_labels2,
+                                          fired, static_cast<cudaStream_t>(stream)));
+}
+
 int dg_commit(const dg_dims* d, const float* entropy, const int32_t* argmax, const uint8_t* cand,
               const float* gamma, uint8_t* committed_state, int32_t* token_state,
               uint8_t* commit, int32_t* tokens, int32_t* n_commit, void* stream) {

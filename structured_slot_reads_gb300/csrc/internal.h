@@ -74,6 +74,11 @@ cudaError_t slot_finish(const uint16_t* rows, const float* inv_t_rows, const flo
                         const int32_t* n_labels, int S, int R, int samples, float gate,
                         float* q_avg, float* h_slot, int32_t* chosen, float* lp_draws,
                         uint8_t* resampled, int32_t* n_reads, cudaStream_t st);
+cudaError_t ask_if_select(const int32_t* chosen1, int S1, const int32_t* cond_slot,
+                          const int32_t* cond_value, const int32_t* q_owner,
+                          const int32_t* q_label_ids, const int32_t* q_n_labels, int Q, int S2,
+                          int32_t* label_ids2, int32_t* n_labels2, uint8_t* fired,
+                          cudaStream_t st);
 cudaError_t commit(int B, int C, const float* entropy, const int32_t* argmax,
                    const uint8_t* cand, const float* gamma, uint8_t* committed_state,
                    int32_t* token_state, uint8_t* commit_out, int32_t* tokens,

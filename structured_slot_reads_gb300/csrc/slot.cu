@@ -92,7 +92,8 @@ __global__ void slot_finish_kernel(const __nv_bfloat16* rows, const float* inv_t
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nw = blockDim.x >> 5;
   int n = n_labels[s];
-  const bool n_ok = n >= 1 && n <= MAXL;
+  // n == 0: a question whose ask_if condition did not fire -- not read
+  const bool n_ok = n >= 0 && n <= MAXL;
   if (!n_ok) n = 0;
   if (threadIdx.x < MAXL) {
     int id = (threadIdx.x < n) ? label_ids[s * MAXL + threadIdx.x] : 0;
@@ -196,10 +197,44 @@ __global__ void slot_finish_kernel(const __nv_bfloat16* rows, const float* inv_t
   }
   if (k < MAXL) q_avg[s * MAXL + k] = qk;
   if (lane == 0) {
-    chosen[s] = arg;
+    chosen[s] = n > 0 ? arg : -1;
     h_slot[s] = hs;
-    resampled[s] = fire ? 1 : 0;
-    n_reads[s] = fire ? samples : 1;
+    resampled[s] = (n > 0 && fire) ? 1 : 0;
+    n_reads[s] = n == 0 ? 0 : (fire ? samples : 1);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// a7: ask_if gating (sotaaz.com, "The server accepts at most 26 alternatives per
+// question": a question carrying ask_if is read only when the earlier answer
+// matches).  Thread per question: fired = chosen1[cond_slot] == cond_value.
+// Thread per stage-2 slot: the first fired question that owns the slot copies
+// its labels into the stage-2 table; with none, n_labels2 = 0 (not read).
+// ---------------------------------------------------------------------------
+__global__ void ask_if_kernel(const int32_t* chosen1, int S1, const int32_t* cond_slot,
+                              const int32_t* cond_value, const int32_t* q_owner,
+                              const int32_t* q_label_ids, const int32_t* q_n_labels, int Q,
+                              int S2, int32_t* label_ids2, int32_t* n_labels2, uint8_t* fired,
+                              int* status) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  auto fires = [&](int q) -> bool {
+    const int cs = cond_slot[q];
+    if (cs < 0 || cs >= S1) {
+      atomicOr(status, 8 /* DG_DEV_BAD_INDEX */);
+      return false;
+    }
+    return chosen1[cs] == cond_value[q];
+  };
+  if (i < Q && fired) fired[i] = fires(i) ? 1 : 0;
+  if (i < S2) {
+    int pick = -1;
+    for (int q = 0; q < Q && pick < 0; ++q)
+      if (q_owner[q] == i && fires(q)) pick = q;
+    const int n = pick >= 0 ? q_n_labels[pick] : 0;
+    n_labels2[i] = (n >= 0 && n <= MAXL) ? n : 0;
+    if (n < 0 || n > MAXL) atomicOr(status, 4 /* DG_DEV_BAD_LABEL */);
+    for (int k = 0; k < MAXL; ++k)
+      label_ids2[i * MAXL + k] = (pick >= 0 && k < n) ? q_label_ids[pick * MAXL + k] : -1;
   }
 }
 
@@ -330,6 +365,19 @@ cudaError_t slot_finish(const uint16_t* rows, const float* inv_t_rows, const flo
       reinterpret_cast<const __nv_bfloat16*>(rows), inv_t_rows, lse_rows,
       reinterpret_cast<const __nv_bfloat16*>(w), V, D, label_ids, n_labels, R, samples, gate,
       q_avg, h_slot, chosen, lp_draws, resampled, n_reads, status_ptr());
+  return cudaGetLastError();
+}
+
+cudaError_t ask_if_select(const int32_t* chosen1, int S1, const int32_t* cond_slot,
+                          const int32_t* cond_value, const int32_t* q_owner,
+                          const int32_t* q_label_ids, const int32_t* q_n_labels, int Q, int S2,
+                          int32_t* label_ids2, int32_t* n_labels2, uint8_t* fired,
+                          cudaStream_t st) {
+  const int n = Q > S2 ? Q : S2;
+  if (n == 0) return cudaSuccess;
+  ask_if_kernel<<<(n + 127) / 128, 128, 0, st>>>(chosen1, S1, cond_slot, cond_value, q_owner,
+                                                  q_label_ids, q_n_labels, Q, S2, label_ids2,
+                                                  n_labels2, fired, status_ptr());
   return cudaGetLastError();
 }
 

@@ -63,6 +63,7 @@ _SIGS = {
     "dg_denoise_heads": [DP, P, I, P, I, P, P, P, P, P, P, P, P, P, P, Z, P, Z, P],
     "dg_selfcond_from_probs": [DP, P, Z, P, I, P, P, P, Z, P],
     "dg_probs_ld": [I],
+    "dg_ask_if_select": [P, I, P, P, P, P, P, I, I, P, P, P, P],
     "dg_lmhead_logsoftmax_entropy_noalloc": [DP, P, I, P, P, P, P, P, P, P],
     "dg_canvas_update": [DP, P, P, P, P, P, I, P, P],
     "dg_philox_fill": [U64, P, I, P, P],
@@ -196,6 +197,13 @@ def dg_selfcond_from_probs(dims, probs, probs_ld, prob_scale, M, e, out, workspa
     return lib().dg_selfcond_from_probs(ctypes.byref(dims), _p(probs), probs_ld, _p(prob_scale),
                                         M, _p(e), _p(out), _p(workspace), _nbytes(workspace),
                                         _s(stream))
+
+
+def dg_ask_if_select(chosen1, S1, cond_slot, cond_value, q_owner, q_label_ids, q_n_labels, Q,
+                     S2, label_ids2, n_labels2, fired=None, stream=None):
+    return lib().dg_ask_if_select(_p(chosen1), S1, _p(cond_slot), _p(cond_value), _p(q_owner),
+                                  _p(q_label_ids), _p(q_n_labels), Q, S2, _p(label_ids2),
+                                  _p(n_labels2), _p(fired), _s(stream))
 
 
 def dg_probs_ld(V):

@@ -1,0 +1,144 @@
+"""Batched two-stage structured reads over a paged prompt KV cache, through libdg.
+
+sotaaz.com, "The server accepts at most 26 alternatives per question": 77
+intents do not fit one question (A-Z), so a 9-way group question is read
+first and the chosen group's item question (carrying ``ask_if``) second; each
+stage re-reads a slot four times when its first read's entropy exceeds 0.1.
+One ``TwoStageRead.run`` is, for every request of the batch:
+
+  dg_attn_decode      decoder attention of the canvas over its paged prompt KV
+  dg_slot_read        stage 1: group slot + 0-3 other slots (noise draws, one
+                      W pass over all draw rows, gated read)
+  dg_ask_if_select    stage-2 slot table from the stage-1 answers (on device)
+  dg_slot_read        stage 2: the chosen group's item slot
+
+Torch allocates every buffer; the library only enqueues work.
+"""
+import numpy as np
+import torch
+
+from . import dg, inputs
+
+
+def _dev(a, dtype, device):
+    return torch.as_tensor(np.ascontiguousarray(a)).to(device=device, dtype=dtype)
+
+
+class TwoStageRead:
+    def __init__(self, shape, w, e, tables, prompt_len, device="cuda", seed=0):
+        """tables: inputs.two_stage_tables(shape, seed) (one dict per request)."""
+        self.shape = shape
+        self.dims = dg.dims_of(shape)
+        self.dims.P_max = int(max(prompt_len))      # the page table covers the longest prompt
+        self.device = device
+        self.w, self.e = w, e
+        self.seed = seed
+        B, C, D = shape.B, shape.C, shape.D
+        bf, f32, i32, u8 = torch.bfloat16, torch.float32, torch.int32, torch.uint8
+        self.M = B * C
+        self.h = torch.empty((self.M, D), dtype=bf, device=device)
+        self.inv_t = torch.empty(self.M, dtype=f32, device=device)
+        self.q = torch.empty((B, C, shape.Hq, shape.d_head), dtype=bf, device=device)
+        self.kc = torch.empty((B, C, shape.Hkv, shape.d_head), dtype=bf, device=device)
+        self.vc = torch.empty_like(self.kc)
+        self.prompt_len = _dev(prompt_len, i32, device)
+        ps = shape.page_size
+        self.pages_per_req = int(max((int(p) + ps - 1) // ps for p in prompt_len))
+        self.attn_out = torch.empty_like(self.q)
+        self.attn_lse = torch.empty((B, shape.Hq, C), dtype=f32, device=device)
+        # stage 1: group slot then the other slots of every request
+        rows, reqs, labs, ns, self.group_slot = [], [], [], [], []
+        for b, t in enumerate(tables):
+            self.group_slot.append(len(rows))
+            for pos, lab in [(t["group_pos"], t["group_labels"])] + list(t["others"]):
+                rows.append(b * C + pos)
+                reqs.append(b)
+                pad = np.full(dg.MAX_LABELS, -1, np.int32)
+                pad[:len(lab)] = lab
+                labs.append(pad)
+                ns.append(len(lab))
+        self.S1 = len(rows)
+        self.slot_row1 = _dev(rows, i32, device)
+        self.slot_req1 = _dev(reqs, i32, device)
+        self.label_ids1 = _dev(np.stack(labs), i32, device)
+        self.n_labels1 = _dev(ns, i32, device)
+        self.host_slots1 = (np.array(rows, np.int32), np.stack(labs), np.array(ns, np.int32))
+        # stage-2 questions: one per (request, group option), ask_if = that option
+        cs, cv, own, qlab, qn = [], [], [], [], []
+        for b, t in enumerate(tables):
+            for g, items in enumerate(t["item_labels"]):
+                cs.append(self.group_slot[b])
+                cv.append(g)
+                own.append(b)
+                pad = np.full(dg.MAX_LABELS, -1, np.int32)
+                pad[:len(items)] = items
+                qlab.append(pad)
+                qn.append(len(items))
+        self.Q = len(cs)
+        self.cond_slot = _dev(cs, i32, device)
+        self.cond_value = _dev(cv, i32, device)
+        self.q_owner = _dev(own, i32, device)
+        self.q_label_ids = _dev(np.stack(qlab), i32, device)
+        self.q_n_labels = _dev(qn, i32, device)
+        self.host_questions = (np.array(cs), np.array(cv), np.array(own), np.stack(qlab),
+                               np.array(qn))
+        self.S2 = B
+        self.slot_row2 = _dev([b * C + t["item_pos"] for b, t in enumerate(tables)], i32, device)
+        self.slot_req2 = _dev(list(range(B)), i32, device)
+        self.label_ids2 = torch.empty((B, dg.MAX_LABELS), dtype=i32, device=device)
+        self.n_labels2 = torch.empty(B, dtype=i32, device=device)
+        self.fired = torch.empty(self.Q, dtype=u8, device=device)
+        R = shape.R
+        self.out1 = self._slot_outputs(self.S1, R)
+        self.out2 = self._slot_outputs(self.S2, R)
+        d = self.dims
+        self.ws_attn = torch.empty(max(dg.dg_workspace_bytes(d, dg.DG_WS_ATTN, 0), 256),
+                                   dtype=u8, device=device)
+        self.ws_read = torch.empty(dg.dg_workspace_bytes(d, dg.DG_WS_SLOT_READ,
+                                                         max(self.S1, self.S2) * R),
+                                   dtype=u8, device=device)
+
+    def _slot_outputs(self, S, R):
+        f32, i32, u8, dev = torch.float32, torch.int32, torch.uint8, self.device
+        return dict(q_avg=torch.empty((S, dg.MAX_LABELS), dtype=f32, device=dev),
+                    h_slot=torch.empty(S, dtype=f32, device=dev),
+                    chosen=torch.empty(S, dtype=i32, device=dev),
+                    lp=torch.empty((S, R, dg.MAX_LABELS), dtype=f32, device=dev),
+                    resampled=torch.empty(S, dtype=u8, device=dev),
+                    n_reads=torch.empty(S, dtype=i32, device=dev),
+                    tokens=torch.empty((S, R), dtype=i32, device=dev))
+
+    def set_kv(self, pool_k, pool_v, page_table):
+        self.pool_k, self.pool_v = pool_k, pool_v
+        self.page_table = page_table
+        self.n_pages = pool_k.shape[0]
+
+    def _read(self, S, slot_row, slot_req, label_ids, n_labels, out, step, stream):
+        s = self.shape
+        dg._check(dg.dg_slot_read(self.dims, self.h, self.M, self.w, self.e, self.inv_t,
+                                  slot_row, slot_req, label_ids, n_labels, S, self.seed, step,
+                                  s.R, s.gate, out["q_avg"], out["h_slot"], out["chosen"],
+                                  out["lp"], out["resampled"], out["n_reads"], out["tokens"],
+                                  self.ws_read, stream), "dg_slot_read")
+
+    def run(self, stream=None):
+        """Enqueue attention + both read stages; returns the number of library kernels."""
+        dg._check(dg.dg_attn_decode(self.dims, self.q, self.kc, self.vc, self.pool_k,
+                                    self.pool_v, self.page_table, self.page_table.shape[1],
+                                    self.n_pages, self.shape.page_size, self.prompt_len,
+                                    self.attn_out, self.attn_lse, self.ws_attn, stream),
+                  "dg_attn_decode")
+        self._read(self.S1, self.slot_row1, self.slot_req1, self.label_ids1, self.n_labels1,
+                   self.out1, 0, stream)
+        dg._check(dg.dg_ask_if_select(self.out1["chosen"], self.S1, self.cond_slot,
+                                      self.cond_value, self.q_owner, self.q_label_ids,
+                                      self.q_n_labels, self.Q, self.S2, self.label_ids2,
+                                      self.n_labels2, self.fired, stream), "dg_ask_if_select")
+        self._read(self.S2, self.slot_row2, self.slot_req2, self.label_ids2, self.n_labels2,
+                   self.out2, 1, stream)
+        attn_kernels = 1 if dg.dg_workspace_bytes(self.dims, dg.DG_WS_ATTN, 0) <= 256 else 2
+        return attn_kernels + 4 + 1 + 4
+
+    def decisions(self):
+        """Slot decisions completed by one run (stage-1 slots + asked stage-2 slots)."""
+        return self.S1 + int((self.n_labels2 > 0).sum().item())

@@ -148,3 +148,25 @@ def test_step_runner_builds_on_host(lib, fused):
     assert st.kernels_per_step() == (11 if fused else 13) - (0 if st._attn_splits() > 1 else 1)
     if fused:
         assert st.probs.shape == (shp.C, dg.dg_probs_ld(shp.V)) and st.n_draw == 4
+
+
+def test_two_stage_runner_builds_on_host(lib):
+    """The batched two-stage runner sets up its tables with host-side calls only, and
+    its page table covers the longest prompt (the attention call's shape check)."""
+    import torch
+
+    from structured_slot_reads_gb300 import configs, inputs
+    from structured_slot_reads_gb300.read import TwoStageRead
+    shp = configs.scaled(configs.MIXED_BATCH, B=4, C=64, P=200, D=256, V=4096)
+    tables = inputs.two_stage_tables(shp, 3)
+    plen = inputs.prompt_lengths(shp, 3, lo=100)
+    w = torch.zeros((shp.V, shp.D), dtype=torch.bfloat16)
+    tr = TwoStageRead(shp, w, w, tables, plen, device="cpu", seed=3)
+    assert tr.S1 == sum(1 + len(t["others"]) for t in tables)
+    assert tr.Q == shp.B * 9 and tr.S2 == shp.B
+    assert tr.pages_per_req * shp.page_size >= tr.dims.P_max == int(plen.max())
+    assert all(tr.host_slots1[0][g] // shp.C == b for b, g in enumerate(tr.group_slot))
+    assert dg.dg_ask_if_select(None, 1, None, None, None, None, None, 2, 1, 16, 16,
+                               stream=0) == dg.DG_ERR_ARG
+    assert dg.dg_ask_if_select(16, 1, 16, 16, 16, 16, 16, 2, -1, 16, 16,
+                               stream=0) == dg.DG_ERR_ARG

@@ -112,3 +112,34 @@ def test_bf16_round_matches_torch():
 
 def test_ask_if():
     assert ask_if_fires(3, 3) and not ask_if_fires(2, 3)
+
+
+def test_ask_if_select_two_stage_grouping():
+    from oracle import ask_if_select
+    # 2 requests; stage-1 slots 0 (request 0 group) and 1 (request 1 group), 3 groups;
+    # questions q = 3*b + g own stage-2 slot b and ask if group g was chosen
+    chosen1 = np.array([2, 0])
+    cond_slot = np.array([0, 0, 0, 1, 1, 1])
+    cond_value = np.array([0, 1, 2, 0, 1, 2])
+    q_owner = np.array([0, 0, 0, 1, 1, 1])
+    q_n = np.array([9, 9, 5, 9, 9, 5])
+    q_lab = np.full((6, 26), -1)
+    for q in range(6):
+        q_lab[q, :q_n[q]] = 100 * q + np.arange(q_n[q])
+    lab2, n2, fired = ask_if_select(chosen1, cond_slot, cond_value, q_owner, q_lab, q_n, 3)
+    assert fired.tolist() == [0, 0, 1, 1, 0, 0]        # exactly one per request
+    assert n2.tolist() == [5, 9, 0]                    # slot 2 owned by nobody: not asked
+    assert lab2[0, :5].tolist() == [200, 201, 202, 203, 204] and lab2[0, 5] == -1
+    assert lab2[1, :9].tolist() == list(range(300, 309))
+    assert np.all(lab2[2] == -1)
+    # an out-of-range condition slot never fires
+    _, _, f2 = ask_if_select(chosen1, np.array([5]), np.array([0]), np.array([0]), q_lab[:1],
+                             q_n[:1], 1)
+    assert f2.tolist() == [0]
+
+
+def test_not_asked_slot_is_not_read():
+    z = np.random.default_rng(9).standard_normal((1, 4, 26))
+    out = slot_read(z, np.zeros((1, 4)), np.array([0]), 4, 0.1)
+    assert out["chosen"][0] == -1 and out["n_reads"][0] == 0 and out["resampled"][0] == 0
+    assert np.all(out["q_avg"][0] == 0) and out["h_slot"][0] == 0
