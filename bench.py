@@ -27,6 +27,22 @@ sys.path.insert(0, ROOT)
 METRIC = "denoise steps/s per 256-tok canvas; slot reads/s; % of tensor/HBM roofline"
 UNIT = "denoise steps/s"
 
+# workload name -> (runner kind, shape name, overrides).  Kinds: "step" = the
+# full denoise step, "read" = the read-only step (attention + one slot read),
+# "two_stage" = the mixed batch of two-stage ask_if reads over paged prompt KV.
+WORKLOADS = {
+    "full_canvas_step": ("step", "FULL_CANVAS", {}),
+    "single_structured_read": ("read", "SINGLE_READ", {}),
+    "mixed_batched_reads": ("two_stage", "MIXED_BATCH", {}),
+    "long_context_read": ("read", "LONG_CONTEXT", {}),
+    "sweep_read_b1": ("read", "LONG_CONTEXT", dict(B=1, P=8192)),
+    "sweep_read_b8": ("read", "LONG_CONTEXT", dict(B=8, P=8192)),
+    "sweep_read_b64": ("read", "LONG_CONTEXT", dict(B=64, P=8192)),
+    "sweep_step_b1": ("step", "FULL_CANVAS", dict(B=1, P=8192)),
+    "sweep_step_b8": ("step", "FULL_CANVAS", dict(B=8, P=8192)),
+    "sweep_step_b64": ("step", "FULL_CANVAS", dict(B=64, P=8192)),
+}
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -36,6 +52,9 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--workload", default="full_canvas_step", choices=list(WORKLOADS),
+                    help="full_canvas_step is the headline line; the others measure the "
+                         "remaining workloads (read-only steps, the mixed batch, the sweep)")
     return ap.parse_args()
 
 
@@ -327,12 +346,11 @@ def call_work(shape, st):
     M, V, D = shape.B * shape.C, shape.V, shape.D
     W = V * D * 2
     nd = getattr(st, "n_draw", 0)
-    kv = shape.B * (shape.P + shape.C) * shape.Hkv * shape.d_head * 2 * 2
-    qo = 2 * shape.B * shape.C * shape.Hq * shape.d_head * 2
+    sr = getattr(st, "S", 0) * shape.R        # draw rows of a dg_slot_read pass
     return {
-        "dg_attn_decode": (kv + qo, attn_flops(shape)),
+        "dg_attn_decode": (attn_bytes(shape), attn_flops(shape)),
         "dg_lmhead_logsoftmax_entropy": (W + M * D * 2 + M * 16, 2.0 * M * V * D),
-        "dg_slot_read": (W + nd * D * 4, 2.0 * nd * V * D),
+        "dg_slot_read": (W + sr * D * 4, 2.0 * sr * V * D),
         "dg_denoise_heads": (W + (M + nd) * D * 2 + M * V * 2 + M * 20,
                              2.0 * (M + nd) * V * D),
         "dg_selfcond_embed": (2 * W + 2 * M * V * 2 + M * D * 4, 4.0 * M * V * D),
@@ -342,13 +360,184 @@ def call_work(shape, st):
     }
 
 
-def attn_flops(shape):
+def attn_flops(shape, prompt_len=None):
     """Algorithmic attention FLOPs of one step (QK^T and PV over visible keys)."""
     C, W = shape.C, shape.W
-    vis = 0
-    for i in range(C):
-        vis += shape.P + (min(C - 1, i + W) - max(0, i - W) + 1)
-    return 4.0 * shape.B * shape.Hq * shape.d_head * vis
+    win = sum(min(C - 1, i + W) - max(0, i - W) + 1 for i in range(C))
+    plens = [shape.P] * shape.B if prompt_len is None else [int(p) for p in prompt_len]
+    vis = sum(C * p + win for p in plens)
+    return 4.0 * shape.Hq * shape.d_head * vis
+
+
+def attn_bytes(shape, prompt_len=None):
+    """Algorithmic attention bytes: prompt + canvas K/V once, Q read and O written once."""
+    plens = [shape.P] * shape.B if prompt_len is None else [int(p) for p in prompt_len]
+    kv = (sum(plens) + shape.B * shape.C) * shape.Hkv * shape.d_head * 2 * 2
+    return kv + 2 * shape.B * shape.C * shape.Hq * shape.d_head * 2
+
+
+# ------------------------------------------------- the other workloads
+def workload_shape(name):
+    from structured_slot_reads_gb300 import configs
+    kind, base, kw = WORKLOADS[name]
+    shape = getattr(configs, base)
+    if kw:
+        shape = configs.scaled(shape, name=name, **kw)
+    return kind, shape
+
+
+def fill_common(st, shape, device, kv=("kenc", "venc")):
+    """Synthetic device inputs: N(0,1) hidden rows and attention tensors, 1/T ~ 1/U(0.5, 2)."""
+    from structured_slot_reads_gb300 import inputs
+    h = st.h0 if hasattr(st, "h0") else st.h
+    h.copy_(inputs.device_normal_bf16(h.shape, 1.0, 3, device))
+    st.inv_t.copy_(1.0 / inputs.device_uniform(st.inv_t.shape, 0.5, 2.0, 4, device))
+    for i, k in enumerate(("q", "kc", "vc") + tuple(kv)):
+        getattr(st, k).copy_(inputs.device_normal_bf16(getattr(st, k).shape, 1.0, 10 + i, device))
+
+
+def build_runner(kind, shape, device):
+    import torch
+
+    from structured_slot_reads_gb300 import inputs
+    from structured_slot_reads_gb300.read import ReadStep, TwoStageRead
+    if kind == "step":
+        return build_step(shape, device)
+    w = inputs.device_normal_bf16((shape.V, shape.D), shape.D ** -0.5, 1, device)
+    e = inputs.device_normal_bf16((shape.V, shape.D), shape.D ** -0.5, 2, device)
+    if kind == "read":
+        st = ReadStep(shape, w, e, device=device, seed=7)
+        fill_common(st, shape, device)
+    else:
+        plen = inputs.prompt_lengths(shape, 5)
+        st = TwoStageRead(shape, w, e, inputs.two_stage_tables(shape, 5), plen, device=device,
+                          seed=7)
+        table, n_pages = inputs.page_table(plen, shape.page_size, 5)
+        pool = (n_pages, shape.page_size, shape.Hkv, shape.d_head)
+        st.set_kv(inputs.device_normal_bf16(pool, 1.0, 20, device),
+                  inputs.device_normal_bf16(pool, 1.0, 21, device),
+                  torch.from_numpy(table).to(device))
+        st.prompt_lens_host = plen
+        fill_common(st, shape, device, kv=())
+    torch.cuda.synchronize()
+    return st
+
+
+def timed_steps(args, run, calls, local, world):
+    """W warm-up steps, then K steps timed with CUDA events on the launching stream.
+
+    Returns (max-over-ranks ms for K steps, mean ms per library call, kernels
+    launched, clock record)."""
+    import torch
+    stream = torch.cuda.current_stream()
+    for i in range(args.warmup):
+        run(i)
+    torch.cuda.synchronize()
+    timer = CallTimer(calls)
+    timer.wrap(None)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.6)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    launches = 0
+    for i in range(args.steps):
+        launches += run(args.warmup + i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    timer.unwrap()
+    ms = max_over_ranks(e0.elapsed_time(e1), world)
+    return ms, {n: timer.mean_ms(n) for n in calls if timer.pairs[n]}, launches, clk
+
+
+def workload_arm(args, rank, world, local):
+    """One JSON line for a workload other than the headline step."""
+    import torch
+
+    from structured_slot_reads_gb300 import dg
+    kind, shape = workload_shape(args.workload)
+    device = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    st = build_runner(kind, shape, device)
+    if kind == "two_stage":
+        run = lambda i: st.run()                        # noqa: E731
+        calls = ["dg_attn_decode", "dg_slot_read", "dg_ask_if_select"]
+    else:
+        run = lambda i: st.run(step_idx=i)              # noqa: E731
+        calls = ["dg_attn_decode", "dg_slot_read", "dg_slot_noise", "dg_denoise_heads",
+                 "dg_slot_finish", "dg_commit", "dg_selfcond_from_probs", "dg_canvas_update"]
+    dg.dg_clear_status()
+    ms, per_call, launches, clk = timed_steps(args, run, calls, local, world)
+    status = dg.dg_get_status()
+    steps_per_s = world * args.steps / (ms / 1e3)
+    pk = peaks()
+    V, D, R = shape.V, shape.D, shape.R
+    Wb = V * D * 2
+    plen = getattr(st, "prompt_lens_host", None)
+    work = call_work(shape, st) if kind == "step" else {}
+    work["dg_attn_decode"] = (attn_bytes(shape, plen), attn_flops(shape, plen))
+    if kind == "read":
+        work["dg_slot_read"] = (Wb + st.S * R * D * 4, 2.0 * st.S * R * V * D)
+        decisions = st.S
+    elif kind == "two_stage":
+        rows = (st.S1 + st.S2) * R / 2                  # mean draw rows of the two passes
+        work["dg_slot_read"] = (Wb + rows * D * 4, 2.0 * rows * V * D)
+        decisions = st.decisions()
+    else:
+        decisions = getattr(st, "S", 0)
+    kernels, best = {}, None
+    n_calls = {"dg_slot_read": 2} if kind == "two_stage" else {}
+    for n, t in per_call.items():
+        b, f = work.get(n, (0.0, 0.0))
+        kernels[n] = {"ms": round(t, 4), "bytes": b, "flops": f}
+        if b:
+            kernels[n]["hbm_frac"] = round(b / (t / 1e3) / 1e9 / pk["hbm"], 4)
+        if f:
+            kernels[n]["tensor_frac_sustained"] = round(f / (t / 1e3) / 1e12 / pk["bf16_sus"], 4)
+        share = t * n_calls.get(n, 1)
+        if (b or f) and (best is None or share > best[1]):
+            best = (n, share)
+    roof = None
+    if best:
+        n = best[0]
+        t_s = per_call[n] / 1e3
+        b, f = work[n]
+        tensor_bound = f / max(b, 1.0) > pk["bf16_sus"] * 1e3 / pk["hbm"]
+        if tensor_bound:
+            ach, peak, unit = f / t_s / 1e12, pk["bf16_sus"], "TFLOP/s"
+        else:
+            ach, peak, unit = b / t_s / 1e9, pk["hbm"], "GB/s"
+        roof = {"bound": "tensor" if tensor_bound else "hbm", "achieved": round(ach, 1),
+                "peak": peak, "unit": unit, "frac": round(ach / peak, 4), "traffic": None,
+                "kernel": n, "peak_source": pk["source"]}
+    if kind == "step":
+        unit, value = UNIT, steps_per_s * shape.B
+    else:
+        unit, value = "slot decisions/s", steps_per_s * decisions
+    return {
+        "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload}: kind {kind}, B={shape.B}, prompt "
+                               f"{'U[512, %d] paged' % shape.P if kind == 'two_stage' else shape.P}"
+                               f", canvas {shape.C}, Hq {shape.Hq} / Hkv {shape.Hkv}, d_head "
+                               f"{shape.d_head}, W {shape.W}, d_model {D}, vocab {V}",
+                   "global_batch": world * shape.B, "seq_len": shape.C,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2: W (1.48 GB) streamed every step"},
+        "steps_per_s": round(steps_per_s, 3),
+        "canvases_per_s": round(steps_per_s * shape.B, 3),
+        "slot_decisions_per_s": round(steps_per_s * decisions, 3),
+        "slot_decisions_per_step": decisions,
+        "roofline": roof, "kernels": kernels, "e2e": None, "gpu_launches": launches,
+        "clocks": clk, "device_status": status,
+    }
 
 
 # --------------------------------------------------------- the CPU oracle
@@ -464,6 +653,11 @@ def main():
     if args.impl == "reference":
         line = reference_arm(args, rank)
         if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+    if args.workload != "full_canvas_step":
+        line = workload_arm(args, rank, world, local)
+        if rank == 0:
             print(json.dumps(line), flush=True)
         return 0
     line, st = gpu_arm(args, rank, world, local)

@@ -108,24 +108,35 @@ def paged_layout(kenc, venc, prompt_len, page_size, seed, spare_pages=7):
     """
     B = kenc.shape[0]
     hkv, d = kenc.shape[2], kenc.shape[3]
-    need = [(int(p) + page_size - 1) // page_size for p in prompt_len]
-    total = sum(need) + spare_pages
-    perm = _rng(seed, S_PAGES).permutation(total)
+    table, total = page_table(prompt_len, page_size, seed, spare_pages)
     pool_k = np.zeros((total, page_size, hkv, d), dtype=np.float32)
     pool_v = np.zeros_like(pool_k)
-    maxp = max(need) if need else 0
-    table = np.full((B, max(maxp, 1)), -1, dtype=np.int32)
-    nxt = 0
     for b in range(B):
-        for pg in range(need[b]):
-            page = int(perm[nxt])
-            nxt += 1
-            table[b, pg] = page
+        for pg in range((int(prompt_len[b]) + page_size - 1) // page_size):
+            page = int(table[b, pg])
             lo = pg * page_size
             hi = min(lo + page_size, int(prompt_len[b]))
             pool_k[page, : hi - lo] = kenc[b, lo:hi]
             pool_v[page, : hi - lo] = venc[b, lo:hi]
     return pool_k, pool_v, table
+
+
+def page_table(prompt_len, page_size, seed, spare_pages=7):
+    """Page table [B, max_pages] int32 (-1 past a request's last page) and the pool size.
+
+    Pages come from a random permutation of the pool, handed out request by
+    request, so a request's pages are scattered through the pool.
+    """
+    B = len(prompt_len)
+    need = [(int(p) + page_size - 1) // page_size for p in prompt_len]
+    total = sum(need) + spare_pages
+    perm = _rng(seed, S_PAGES).permutation(total)
+    table = np.full((B, max(max(need) if need else 0, 1)), -1, dtype=np.int32)
+    nxt = 0
+    for b in range(B):
+        table[b, :need[b]] = perm[nxt:nxt + need[b]]
+        nxt += need[b]
+    return table, total
 
 
 def label_set(n, V, *key):

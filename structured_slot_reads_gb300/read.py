@@ -24,6 +24,18 @@ def _dev(a, dtype, device):
     return torch.as_tensor(np.ascontiguousarray(a)).to(device=device, dtype=dtype)
 
 
+def slot_outputs(S, R, dev):
+    """Device buffers of one dg_slot_read over S slots with R reads each."""
+    f32, i32, u8 = torch.float32, torch.int32, torch.uint8
+    return dict(q_avg=torch.empty((S, dg.MAX_LABELS), dtype=f32, device=dev),
+                h_slot=torch.empty(S, dtype=f32, device=dev),
+                chosen=torch.empty(S, dtype=i32, device=dev),
+                lp=torch.empty((S, R, dg.MAX_LABELS), dtype=f32, device=dev),
+                resampled=torch.empty(S, dtype=u8, device=dev),
+                n_reads=torch.empty(S, dtype=i32, device=dev),
+                tokens=torch.empty((S, R), dtype=i32, device=dev))
+
+
 class TwoStageRead:
     def __init__(self, shape, w, e, tables, prompt_len, device="cuda", seed=0):
         """tables: inputs.two_stage_tables(shape, seed) (one dict per request)."""
@@ -89,24 +101,14 @@ class TwoStageRead:
         self.n_labels2 = torch.empty(B, dtype=i32, device=device)
         self.fired = torch.empty(self.Q, dtype=u8, device=device)
         R = shape.R
-        self.out1 = self._slot_outputs(self.S1, R)
-        self.out2 = self._slot_outputs(self.S2, R)
+        self.out1 = slot_outputs(self.S1, R, device)
+        self.out2 = slot_outputs(self.S2, R, device)
         d = self.dims
         self.ws_attn = torch.empty(max(dg.dg_workspace_bytes(d, dg.DG_WS_ATTN, 0), 256),
                                    dtype=u8, device=device)
         self.ws_read = torch.empty(dg.dg_workspace_bytes(d, dg.DG_WS_SLOT_READ,
                                                          max(self.S1, self.S2) * R),
                                    dtype=u8, device=device)
-
-    def _slot_outputs(self, S, R):
-        f32, i32, u8, dev = torch.float32, torch.int32, torch.uint8, self.device
-        return dict(q_avg=torch.empty((S, dg.MAX_LABELS), dtype=f32, device=dev),
-                    h_slot=torch.empty(S, dtype=f32, device=dev),
-                    chosen=torch.empty(S, dtype=i32, device=dev),
-                    lp=torch.empty((S, R, dg.MAX_LABELS), dtype=f32, device=dev),
-                    resampled=torch.empty(S, dtype=u8, device=dev),
-                    n_reads=torch.empty(S, dtype=i32, device=dev),
-                    tokens=torch.empty((S, R), dtype=i32, device=dev))
 
     def set_kv(self, pool_k, pool_v, page_table):
         self.pool_k, self.pool_v = pool_k, pool_v
@@ -142,3 +144,60 @@ class TwoStageRead:
     def decisions(self):
         """Slot decisions completed by one run (stage-1 slots + asked stage-2 slots)."""
         return self.S1 + int((self.n_labels2 > 0).sum().item())
+
+
+class ReadStep:
+    """The read-only step of a structured read (no commit, no self-conditioning).
+
+    tau-home.com, "Refusing JSON token generation": the canvas is prefilled,
+    the answer slots are left blank and one denoise forward gives the label
+    distribution of every slot.  One ``run`` is dg_attn_decode over the
+    contiguous prompt KV plus one dg_slot_read over the slot table of every
+    request (the same slots in every request).
+    """
+
+    def __init__(self, shape, w, e, device="cuda", seed=0):
+        self.shape = shape
+        self.dims = dg.dims_of(shape)
+        self.device = device
+        self.w, self.e = w, e
+        self.seed = seed
+        B, C, D = shape.B, shape.C, shape.D
+        bf, f32, i32, u8 = torch.bfloat16, torch.float32, torch.int32, torch.uint8
+        self.M = B * C
+        self.h = torch.empty((self.M, D), dtype=bf, device=device)
+        self.inv_t = torch.empty(self.M, dtype=f32, device=device)
+        self.q = torch.empty((B, C, shape.Hq, shape.d_head), dtype=bf, device=device)
+        self.kc = torch.empty((B, C, shape.Hkv, shape.d_head), dtype=bf, device=device)
+        self.vc = torch.empty_like(self.kc)
+        self.kenc = torch.empty((B, shape.P, shape.Hkv, shape.d_head), dtype=bf, device=device)
+        self.venc = torch.empty_like(self.kenc)
+        self.prompt_len = torch.full((B,), shape.P, dtype=i32, device=device)
+        self.attn_out = torch.empty_like(self.q)
+        self.attn_lse = torch.empty((B, shape.Hq, C), dtype=f32, device=device)
+        row, req, lab, n = inputs.slot_table(shape, seed)
+        self.S = len(row)
+        self.slot_row = _dev(row, i32, device)
+        self.slot_req = _dev(req, i32, device)
+        self.label_ids = _dev(lab, i32, device)
+        self.n_labels = _dev(n, i32, device)
+        self.out = slot_outputs(self.S, shape.R, device)
+        self.ws_attn = torch.empty(max(dg.dg_workspace_bytes(self.dims, dg.DG_WS_ATTN, 0), 256),
+                                   dtype=u8, device=device)
+        self.ws_read = torch.empty(dg.dg_workspace_bytes(self.dims, dg.DG_WS_SLOT_READ,
+                                                         self.S * shape.R), dtype=u8,
+                                   device=device)
+
+    def run(self, step_idx=0, stream=None):
+        """Enqueue attention + the slot read; returns the number of library kernels."""
+        s, d, o = self.shape, self.dims, self.out
+        dg._check(dg.dg_attn_decode(d, self.q, self.kc, self.vc, self.kenc, self.venc, None, 0,
+                                    0, 0, self.prompt_len, self.attn_out, self.attn_lse,
+                                    self.ws_attn, stream), "dg_attn_decode")
+        dg._check(dg.dg_slot_read(d, self.h, self.M, self.w, self.e, self.inv_t, self.slot_row,
+                                  self.slot_req, self.label_ids, self.n_labels, self.S,
+                                  self.seed, step_idx, s.R, s.gate, o["q_avg"], o["h_slot"],
+                                  o["chosen"], o["lp"], o["resampled"], o["n_reads"],
+                                  o["tokens"], self.ws_read, stream), "dg_slot_read")
+        attn_kernels = 1 if dg.dg_workspace_bytes(d, dg.DG_WS_ATTN, 0) <= 256 else 2
+        return attn_kernels + 4

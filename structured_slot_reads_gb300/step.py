@@ -3,12 +3,19 @@
 ``DenoiseStep`` owns the device buffers of one workload (torch allocates
 them; the library never does) and enqueues the library calls of one step:
 
-  dg_attn_decode                 decoder-mode attention over prompt KV + window
-  dg_lmhead_logsoftmax_entropy   lse / entropy / argmax of every canvas row
-  dg_slot_read                   noise draws + one W pass + gated slot read
-  dg_commit                      entropy-ordered commit (state carried forward)
-  dg_selfcond_embed              expected embedding softmax(z) . E
-  dg_canvas_update               next step's canvas input rows
+  dg_attn_decode          decoder-mode attention over prompt KV + window
+  dg_slot_noise           noised slot rows of the four reads
+  dg_denoise_heads        one W pass: lse / entropy / argmax of every canvas row,
+                          the draw rows' lse, bf16 probabilities for self-cond
+  dg_slot_finish          label gather, renormalise, entropy gate, average
+  dg_commit               entropy-ordered commit (state carried forward)
+  dg_selfcond_from_probs  expected embedding softmax(z) . E from the probabilities
+  dg_canvas_update        next step's canvas input rows
+
+With more than 16 draw rows (batched requests) the slot read takes its own
+pass (dg_slot_read).  ``fused=False`` runs the unfused calls instead
+(dg_lmhead_logsoftmax_entropy, dg_slot_read, dg_selfcond_embed), which stream
+W three times.
 
 The same object serves the end-to-end path: ``upload`` copies a step's inputs
 from pinned host memory, ``download`` reads back the decisions.
@@ -58,8 +65,6 @@ class DenoiseStep:
         self.n_commit = _empty((B,), i32, dev)
         self.e_sc = _empty((self.M, D), f32, dev)
         self.ws_attn = _empty((max(dg.dg_workspace_bytes(self.dims, dg.DG_WS_ATTN, 0), 256),), u8, dev)
-        self.ws_lm = _empty((dg.dg_workspace_bytes(self.dims, dg.DG_WS_LMHEAD, self.M),), u8, dev)
-        self.ws_sc = _empty((dg.dg_workspace_bytes(self.dims, dg.DG_WS_SELFCOND, self.M),), u8, dev)
         # slots (same table for every request)
         self.with_slots = with_slots and len(shape.slots) > 0
         self.seed = seed
@@ -79,11 +84,17 @@ class DenoiseStep:
             self.noise_tok = _empty((S, shape.R), i32, dev)
             self.ws_slot = _empty((dg.dg_workspace_bytes(self.dims, dg.DG_WS_SLOT_READ,
                                                          S * shape.R),), u8, dev)
-        # fused path: one stream of W for the canvas rows, the slot draws and
-        # the self-conditioning probabilities
-        self.n_draw = self.S * shape.R if self.with_slots else 0
-        self.fused = fused and self.n_draw <= 16
-        if self.fused:
+        # fused path: one stream of W for the canvas rows, the slot draws (up to
+        # 16 draw rows ride along; more go through their own dg_slot_read pass)
+        # and the self-conditioning probabilities
+        self.fused = fused
+        self.n_draw = self.S * shape.R if (self.with_slots and self.S * shape.R <= 16) else 0
+        if not self.fused:
+            self.ws_lm = _empty((dg.dg_workspace_bytes(self.dims, dg.DG_WS_LMHEAD, self.M),), u8,
+                                dev)
+            self.ws_sc = _empty((dg.dg_workspace_bytes(self.dims, dg.DG_WS_SELFCOND, self.M),), u8,
+                                dev)
+        else:
             nd = max(self.n_draw, 1)
             self.draw_rows = _empty((nd, D), bf, dev)
             self.inv_t_draw = _empty((nd,), f32, dev)
@@ -113,11 +124,7 @@ class DenoiseStep:
                                            self.ent, self.maxz, self.argmax, self.ws_lm, stream),
            "dg_lmhead_logsoftmax_entropy")
         if self.with_slots:
-            ck(dg.dg_slot_read(d, self.h, self.M, self.w, self.e, self.inv_t, self.slot_row,
-                               self.slot_req, self.label_ids, self.n_labels, self.S, self.seed,
-                               step_idx, s.R, s.gate, self.q_avg, self.h_slot, self.chosen,
-                               self.lp_draws, self.resampled, self.n_reads, self.noise_tok,
-                               self.ws_slot, stream), "dg_slot_read")
+            self._slot_read(step_idx, stream)
         ck(dg.dg_commit(d, self.ent, self.argmax, self.cand, self.gamma, self.committed,
                         self.tok_state, self.commit, self.tokens, self.n_commit, stream),
            "dg_commit")
@@ -127,10 +134,20 @@ class DenoiseStep:
                                self.M, self.h, stream), "dg_canvas_update")
         return self.kernels_per_step()
 
+    def _slot_read(self, step_idx, stream):
+        s, d = self.shape, self.dims
+        dg._check(dg.dg_slot_read(d, self.h, self.M, self.w, self.e, self.inv_t, self.slot_row,
+                                  self.slot_req, self.label_ids, self.n_labels, self.S, self.seed,
+                                  step_idx, s.R, s.gate, self.q_avg, self.h_slot, self.chosen,
+                                  self.lp_draws, self.resampled, self.n_reads, self.noise_tok,
+                                  self.ws_slot, stream), "dg_slot_read")
+
     def _run_fused(self, step_idx, stream):
         s, d = self.shape, self.dims
         ck = dg._check
-        if self.with_slots:
+        if self.with_slots and not self.n_draw:
+            self._slot_read(step_idx, stream)
+        if self.n_draw:
             ck(dg.dg_slot_noise(d, self.h, self.M, self.e, self.inv_t, self.slot_row,
                                 self.slot_req, self.S, s.R, self.seed, step_idx, self.draw_rows,
                                 self.inv_t_draw, self.noise_tok, stream), "dg_slot_noise")
@@ -139,7 +156,7 @@ class DenoiseStep:
                                self.ent, self.maxz, self.argmax, self.lse_draw, self.prob_scale,
                                self.probs, self.probs_ld, self.ws_heads, stream),
            "dg_denoise_heads")
-        if self.with_slots:
+        if self.n_draw:
             ck(dg.dg_slot_finish(d, self.draw_rows, self.inv_t_draw, self.lse_draw, self.w,
                                  self.label_ids, self.n_labels, self.S, s.R, s.R, s.gate,
                                  self.q_avg, self.h_slot, self.chosen, self.lp_draws,
@@ -158,9 +175,13 @@ class DenoiseStep:
         """Library kernels one step launches."""
         n = 1 + (1 if self._attn_splits() > 1 else 0)
         if self.fused:
-            # [noise] + heads + finalize + [draw finalize] + [finish] + commit + accum + reduce + update
-            n += 2 + 1 + 2 + 1
-            n += 3 if self.with_slots else 0
+            # ref + heads + finalize + commit + accum + reduce + update, and either
+            # noise + draw finalize + finish (draws in the pass) or a slot read
+            n += 3 + 1 + 2 + 1
+            if self.n_draw:
+                n += 3
+            elif self.with_slots:
+                n += 4
             return n
         # stats + finalize, [noise + stats + finalize + finish], commit, probs + accum + reduce, update
         n += 2

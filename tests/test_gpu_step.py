@@ -149,3 +149,51 @@ def test_full_canvas_commit_and_slots(full_canvas):
     if margins.slot_margins_ok(want, x["n_labels"], shape.gate):
         assert np.array_equal(host(st.chosen), want["chosen"])
         assert np.array_equal(host(st.resampled), want["resampled"])
+
+
+def test_batched_step_with_slot_read_pass():
+    """Eight requests of the tiny shape: 32 draw rows exceed the 16 that ride in the
+    fused pass, so the step reads its slots through dg_slot_read.  Every row's
+    statistics, every request's commit (where its margins hold), the expected
+    embeddings and the slot decisions are compared with the oracle."""
+    shape = configs.scaled(configs.TINY, B=8)
+    x = inputs.step_inputs(shape, seed=5)
+    st = DenoiseStep(shape, dev_bf16(x["w"]), dev_bf16(x["e"]), seed=0, fused=True)
+    assert st.n_draw == 0 and st.S == 8
+    _load(st, x)
+    launched = st.run(step_idx=0)
+    torch.cuda.synchronize()
+    assert dg.dg_get_status() == 0
+    assert launched == st.kernels_per_step()
+    lse, ent, maxz, arg = oracle.lmhead_stats(x["h"], x["w"], x["inv_t"])
+    assert_abs(host(st.lse), lse, what="lse")
+    assert_abs(host(st.ent), ent, what="entropy")
+    assert_rel(host(st.e_sc), oracle.selfcond_embed(x["h"], x["w"], x["e"], x["inv_t"]),
+               what="expected embedding")
+    ref_attn, _ = oracle.attn_decode(x["q"], x["kc"], x["vc"], x["kenc"], x["venc"],
+                                     x["prompt_len"], shape.W)
+    assert_rel(host(st.attn_out), ref_attn, what="attention")
+    ent_b = ent.reshape(shape.B, shape.C)
+    com, toks, n = oracle.commit(ent_b, arg.reshape(shape.B, shape.C), x["cand"], x["gamma"])
+    z = (x["h"].astype(np.float64) @ x["w"].astype(np.float64).T) * x["inv_t"][:, None]
+    gap = top2_gap(z).reshape(shape.B, shape.C)
+    checked = 0
+    for b in range(shape.B):
+        if not (margins.commit_margins_ok(ent_b[b], x["cand"][b], shape.gamma)
+                and np.all(gap[b][com[b] == 1] > margins.ARGMAX_MARGIN)):
+            continue
+        checked += 1
+        assert np.array_equal(host(st.commit)[b], com[b]), f"request {b} commit set"
+        assert np.array_equal(host(st.tokens)[b], toks[b]), f"request {b} tokens"
+        assert host(st.n_commit)[b] == n[b]
+    assert checked >= 4
+    want = margins.slot_read_oracle(x["h"], x["w"], x["e"], x["inv_t"], x["slot_row"],
+                                    x["slot_req"], x["label_ids"], x["n_labels"], 0, 0, shape.R,
+                                    shape.gate)
+    assert np.array_equal(host(st.noise_tok), want["tokens"])
+    for s in range(st.S):
+        assert_abs(host(st.q_avg)[s, :4], want["q_avg"][s, :4], what="slot distribution")
+        one = {k: want[k][s:s + 1] for k in ("h_draw", "q_avg")}
+        if margins.slot_margins_ok(one, x["n_labels"][s:s + 1], shape.gate):
+            assert host(st.chosen)[s] == want["chosen"][s]
+            assert host(st.resampled)[s] == want["resampled"][s]
