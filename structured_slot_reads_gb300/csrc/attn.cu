@@ -495,14 +495,39 @@ namespace dgi {
 
 size_t attn_ws_bytes(int B, int C, int Pmax, int Hq, int Hkv, int d, int W) {
   const int s = pick_splits(B, C, Hq, Hkv, Pmax, std::min(W, C));
-  if (s == 1) return 256;
-  return align_up((size_t)s * B * C * Hq * d * 4 + (size_t)s * B * Hq * C * 8, 256);
+  size_t bytes = 256;
+  if (s > 1) bytes = align_up((size_t)s * B * C * Hq * d * 4 + (size_t)s * B * Hq * C * 8, 256);
+  // d = 512 runs on the tensor-core kernel unless its page size is unsupported
+  if (d == 512) bytes = std::max(bytes, attn_tc_ws_bytes(B, C, Pmax, Hq, Hkv, W));
+  return bytes;
 }
 
 cudaError_t attn_decode(const AttnArgs& a, void* ws, cudaStream_t st) {
   if (a.d == 64) return run<64>(a, ws, st);
-  if (a.d == 512) return run<512>(a, ws, st);
+  if (a.d == 512) return attn_tc_supported(a) ? attn_decode_tc(a, ws, st) : run<512>(a, ws, st);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t attn_combine(int B, int C, int Hq, int d, int splits, float* ws_o, float* ws_ml,
+                         uint16_t* out, float* lse, cudaStream_t st) {
+  Args a{};
+  a.B = B;
+  a.C = C;
+  a.Hq = Hq;
+  a.splits = splits;
+  a.ws_o = ws_o;
+  a.ws_ml = ws_ml;
+  a.out = reinterpret_cast<__nv_bfloat16*>(out);
+  a.lse = lse;
+  const long long rows = (long long)B * C * Hq;
+  const int grid = (int)((rows + 7) / 8);
+  if (d == 64)
+    attn_combine_kernel<64><<<grid, 256, 0, st>>>(a);
+  else if (d == 512)
+    attn_combine_kernel<512><<<grid, 256, 0, st>>>(a);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
 }
 
 }  // namespace dgi

@@ -1,0 +1,607 @@
+// attn_tc.cu -- decoder-mode attention with 512-wide heads on the 5th-generation
+// tensor cores (24-ai.news, "How does diffusion text generation differ?";
+// thakicloud.com, "What is DiffusionGemma").
+//
+// Every canvas row attends to all prompt keys of its request (encoder KV,
+// contiguous or in pages) and to the canvas keys within +-W of its position:
+// one joint softmax, scale 1/sqrt(d).  A CTA owns 128 query rows = (128/G canvas
+// positions) x (the G query heads of one KV head), so each key tile serves the
+// whole GQA group.
+//
+// Tensor memory holds 512 fp32 columns per lane, exactly one 128 x 512 output
+// accumulator, so the output columns are split over two CTAs: each keeps
+// O[:, 256 h .. 256 h + 255] (256 columns) and recomputes the scores S = Q K^T
+// (two 128-column buffers, so the softmax of one key tile overlaps the QK^T of
+// the next).  Both CTAs of a pair compute bit-identical scores and therefore
+// take identical softmax decisions.  Per 128-key tile:
+//   MMA warp   S[j%2] = Q K_j^T                  (A, B from shared memory, TMA)
+//   softmax    p = 2^(s*log2e/sqrt(d) - m), row sums; p (bf16) overwrites S in TMEM
+//   MMA warp   O += P V_j                        (A = P from tensor memory, B = V)
+// The reference m is raised only when a tile's maximum exceeds it by more than
+// 2^8 (O is then rescaled in tensor memory), so p <= 256 and rescales are rare.
+// The key range is split across CTAs (split-KV) and merged by the combine kernel.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace {
+
+using namespace dgk;
+
+constexpr int HD = 512;                 // head width
+constexpr int DH = 256;                 // output columns per CTA
+constexpr int BM = 128;                 // query rows per CTA
+constexpr int BN = 128;                 // keys per tile
+constexpr int BOX = BN * 128;           // one TMA box: 128 rows x 64 bf16 (16 KB)
+constexpr int UNIT = 2 * BOX;           // one ring slot (32 KB)
+constexpr int NSLOT = 3;
+constexpr int Q_BYTES = BM * HD * 2;    // 128 KB, resident
+constexpr int K_UNITS = HD / 128;       // 4 slots of K per tile (128 head columns each)
+constexpr int V_UNITS = DH / 128;       // 2 slots of V per tile (this CTA's 256 columns)
+constexpr int SOFT_WARPS = 8;           // two per TMEM lane quarter
+constexpr int PRODUCER_WARP = SOFT_WARPS;
+constexpr int MMA_WARP = SOFT_WARPS + 1;
+constexpr int THREADS = (SOFT_WARPS + 2) * 32;
+constexpr int TMEM_COLS = 512;
+constexpr int O_COL = 0;                // O: columns [0, 256)
+constexpr int S_COL = 256;              // S buffers: [256, 384) and [384, 512)
+constexpr int BAR_BYTES = 256;
+constexpr int SMEM_BYTES = 1024 + Q_BYTES + NSLOT * UNIT + BAR_BYTES;
+constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN);
+constexpr uint32_t IDESC_PV = idesc_bf16_f32_bmn(BM, 128);
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+constexpr float LAZY = 8.f;             // log2 headroom before O is rescaled
+static_assert(SMEM_BYTES <= 232448, "shared memory");
+
+struct TcArgs {
+  int B, C, Pmax, Hq, Hkv, W, G, npos, q_blocks, splits;
+  const int32_t* page_table;
+  int pages_per_req, n_pages, page_size;
+  const int32_t* prompt_len;
+  __nv_bfloat16* out;  // [B][C][Hq][512]
+  float* lse;          // [B][Hq][C]
+  float* ws_o;         // [splits][B][C][Hq][512]
+  float* ws_ml;        // [splits][B][Hq][C][2]: reference (log2 units), sum
+  int* status;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Key-tile geometry of one CTA (shared by every role).
+struct Tiles {
+  int P, p0, npos, clo, chi, nbp, t_begin, t_end;
+  __device__ int key0(int t) const { return t < nbp ? t * BN : clo + (t - nbp) * BN; }
+};
+
+__device__ __forceinline__ Tiles tiles_of(const TcArgs& a, int b, int qb, int split) {
+  Tiles T;
+  T.P = min(max(a.prompt_len[b], 0), a.Pmax);
+  T.p0 = qb * a.npos;
+  T.npos = min(a.npos, a.C - T.p0);
+  T.clo = max(0, T.p0 - a.W);
+  T.chi = min(a.C, T.p0 + T.npos - 1 + a.W + 1);
+  T.nbp = (T.P + BN - 1) / BN;
+  const int nb = T.nbp + (T.chi - T.clo + BN - 1) / BN;
+  T.t_begin = (int)((long long)split * nb / a.splits);
+  T.t_end = (int)((long long)(split + 1) * nb / a.splits);
+  return T;
+}
+
+// Page of prompt key k (k < P) of request b, or -1 when the table entry is invalid.
+__device__ __forceinline__ int page_of(const TcArgs& a, int b, int k) {
+  const int pg = a.page_table[(long long)b * a.pages_per_req + k / a.page_size];
+  return (pg < 0 || pg >= a.n_pages) ? -1 : pg;
+}
+
+// Valid-key bit mask of one 32-key chunk for a row: keys [lo, hi) of the tile,
+// minus the pages flagged in `bad` (bit i = tile keys [i ps, (i+1) ps)).
+__device__ __forceinline__ uint32_t chunk_mask(int c, int lo, int hi, uint32_t bad, int ps) {
+  const int a0 = max(lo - 32 * c, 0), a1 = min(hi - 32 * c, 32);
+  if (a1 <= a0) return 0u;
+  uint32_t m = (a1 == 32 ? 0xffffffffu : ((1u << a1) - 1u)) & ~((1u << a0) - 1u);
+  if (bad) {
+    for (int i = 0; i < BN / ps; ++i) {
+      if (!((bad >> i) & 1u)) continue;
+      const int k0 = i * ps - 32 * c, k1 = k0 + ps;
+      const int b0 = max(k0, 0), b1 = min(k1, 32);
+      if (b1 > b0) m &= ~((b1 == 32 ? 0xffffffffu : ((1u << b1) - 1u)) & ~((1u << b0) - 1u));
+    }
+  }
+  return m;
+}
+
+// Softmax and output roles.  Warps w and w + 4 share query rows 32 (w % 4) .. +31
+// (their TMEM lane quarter); warp half h = w / 4 takes keys [64 h, 64 h + 64) of
+// every tile and output columns [128 h, 128 h + 128) of this CTA's 256.
+__device__ __forceinline__ void softmax_and_store(const TcArgs& a, const Tiles& T, int n, int b,
+                                                  int g, int dh, int split, int warp, int lane,
+                                                  uint32_t tmem_base, uint64_t* sfull_bar,
+                                                  uint64_t* pready_bar, uint64_t* pv_bar,
+                                                  uint64_t* pair_bar, volatile int* abort_flag,
+                                                  float* xch) {
+  constexpr unsigned FULL = 0xffffffffu;
+  const int quarter = warp & 3, half = warp >> 2;
+  const int r = quarter * 32 + lane;
+  const int lp = r / a.G;
+  const int pos = T.p0 + lp;
+  const bool row_ok = lp < T.npos;
+  const int head = g * a.G + r % a.G;
+  const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+  const float sl2 = LOG2E * rsqrtf((float)HD);
+  float m_ref = -INFINITY, l = 0.f;
+  bool ok = true;
+  for (int j = 0; j < n; ++j) {
+    const int t = T.t_begin + j;
+    ok = __all_sync(FULL, mbar_wait(&sfull_bar[j & 1], (j >> 1) & 1u, abort_flag, a.status));
+    if (!ok) break;
+    tc_fence_after();
+    const uint32_t s_addr = tmem_base + lane_base + S_COL + (j & 1) * BN;
+    const int key0 = T.key0(t);
+    int lo, hi;
+    uint32_t bad = 0;
+    if (t < T.nbp) {
+      lo = 0;
+      hi = min(BN, T.P - key0);
+      if (a.page_table) {
+        for (int i = 0; i < BN / a.page_size; ++i) {
+          const int k = key0 + i * a.page_size;
+          if (k < T.P && page_of(a, b, k) < 0) bad |= 1u << i;
+        }
+        if (bad && r == 0 && half == 0) atomicOr(a.status, 2 /* DG_DEV_BAD_PAGE */);
+      }
+    } else {
+      lo = max(T.clo, pos - a.W) - key0;
+      hi = min(T.chi, pos + a.W + 1) - key0;
+    }
+    // pass 1: masked maximum of the raw scores over the whole row (both warps of
+    // the pair read all 128 scores, so they agree without exchanging anything)
+    float mb = -INFINITY;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t v[32];
+      tmem_ld_32x32b_x32(s_addr + c * 32, v);
+      const uint32_t vm = chunk_mask(c, lo, hi, bad, a.page_size);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if ((vm >> i) & 1u) mb = fmaxf(mb, __uint_as_float(v[i]));
+    }
+    mb = (mb == -INFINITY) ? -INFINITY : mb * sl2;  // log2 units
+    // both warps of the pair have read every score before either overwrites its
+    // half with probabilities (a bounded wait: phase j of the pair's barrier)
+    mbar_arrive(&pair_bar[quarter]);
+    ok = __all_sync(FULL, mbar_wait(&pair_bar[quarter], j & 1u, abort_flag, a.status));
+    if (!ok) break;
+    // lazy reference: raise it (and rescale O) only past LAZY log2 units
+    const float m_new = fmaxf(m_ref, mb);
+    const bool raise = m_new > m_ref + LAZY;
+    const bool rescale = raise && m_ref != -INFINITY;
+    const float f = rescale ? ex2(m_ref - m_new) : 1.f;
+    if (__any_sync(FULL, rescale)) {
+      // O holds tiles up to j-1: wait for the last P V, then scale this half's
+      // columns in place.  The scores of tile j were committed after P V of tile
+      // j-2, so the phase of tile j-2 is complete and this parity wait is unambiguous.
+      ok = __all_sync(FULL, mbar_wait(pv_bar, (j - 1) & 1u, abort_flag, a.status));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        const uint32_t o_addr = tmem_base + lane_base + O_COL + half * 128 + c * 32;
+        tmem_ld_32x32b_x32(o_addr, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+        tmem_st_32x32b_x32(o_addr, o);
+      }
+      tmem_st_wait();
+    }
+    l *= f;
+    if (raise) m_ref = m_new;
+    const float mr = (m_ref == -INFINITY) ? 0.f : m_ref;
+    // pass 2: p = 2^(s sl2 - m), written as bf16 pairs over this half's own score
+    // columns: keys [64 h, 64 h + 64) -> P columns [64 h, 64 h + 32)
+    float psum = 0.f;
+#pragma unroll 1
+    for (int cc = 0; cc < 2; ++cc) {
+      const int c = 2 * half + cc;
+      uint32_t v[32];
+      tmem_ld_32x32b_x32(s_addr + c * 32, v);
+      const uint32_t vm = chunk_mask(c, lo, hi, bad, a.page_size);
+      tmem_ld_wait();
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float x0 = fmaf(__uint_as_float(v[2 * i]), sl2, -mr);
+        const float x1 = fmaf(__uint_as_float(v[2 * i + 1]), sl2, -mr);
+        const float p0 = ((vm >> (2 * i)) & 1u) ? ex2(x0) : 0.f;
+        const float p1 = ((vm >> (2 * i + 1)) & 1u) ? ex2(x1) : 0.f;
+        psum += p0 + p1;
+        pk[i] = pack_bf16(p0, p1);
+      }
+      tmem_st_32x32b_x16(s_addr + half * 64 + cc * 16, pk);
+    }
+    l += psum;
+    tmem_st_wait();
+    tc_fence_before();
+    mbar_arrive(&pready_bar[j & 1]);
+  }
+  // the last two P V products: wait phase n-2 first, so that the parity wait for
+  // phase n-1 cannot be satisfied by an older phase
+  if (ok && n > 1) ok = __all_sync(FULL, mbar_wait(pv_bar, (n - 2) & 1u, abort_flag, a.status));
+  if (ok && n > 0) ok = __all_sync(FULL, mbar_wait(pv_bar, (n - 1) & 1u, abort_flag, a.status));
+  if (!ok) return;
+  // row sum over both halves: phase n of the pair's barrier
+  xch[half * 128 + r] = l;
+  mbar_arrive(&pair_bar[quarter]);
+  if (!__all_sync(FULL, mbar_wait(&pair_bar[quarter], n & 1u, abort_flag, a.status))) return;
+  l += xch[(half ^ 1) * 128 + r];
+  tc_fence_after();
+  const long long orow = (long long)(b * a.C + pos) * a.Hq + head;
+  if (n == 0) {
+    if (row_ok && dh == 0 && half == 0) {
+      float* ml = a.ws_ml + (((long long)split * a.B + b) * a.Hq + head) * a.C * 2 + pos * 2;
+      ml[0] = -INFINITY;
+      ml[1] = 0.f;
+    }
+    return;
+  }
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t o[32];
+    tmem_ld_32x32b_x32(tmem_base + lane_base + O_COL + half * 128 + c * 32, o);
+    tmem_ld_wait();
+    if (!row_ok) continue;
+    const int col = dh * DH + half * 128 + c * 32;
+    if (a.splits == 1) {
+      uint4* dst = reinterpret_cast<uint4*>(a.out + orow * HD + col);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 w;
+        w.x = pack_bf16(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+        w.y = pack_bf16(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+        w.z = pack_bf16(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+        w.w = pack_bf16(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+        dst[q] = w;
+      }
+    } else {
+      float4* dst = reinterpret_cast<float4*>(
+          a.ws_o + (long long)split * a.B * a.C * a.Hq * HD + orow * HD + col);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        dst[q] = make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
+                             __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3]));
+    }
+  }
+  if (!row_ok || dh != 0 || half != 0) return;
+  if (a.splits == 1) {
+    a.lse[((long long)b * a.Hq + head) * a.C + pos] = (m_ref + log2f(l)) * LN2;
+  } else {
+    float* ml = a.ws_ml + (((long long)split * a.B + b) * a.Hq + head) * a.C * 2 + pos * 2;
+    ml[0] = m_ref;
+    ml[1] = l;
+  }
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
+                   const __grid_constant__ CUtensorMap tmKe,
+                   const __grid_constant__ CUtensorMap tmVe,
+                   const __grid_constant__ CUtensorMap tmKc,
+                   const __grid_constant__ CUtensorMap tmVc, TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* ring = smem + Q_BYTES;
+  uint8_t* bar_base = ring + NSLOT * UNIT;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(bar_base);
+  uint64_t* empty_bar = full_bar + NSLOT;
+  uint64_t* q_bar = empty_bar + NSLOT;
+  uint64_t* sfull_bar = q_bar + 1;       // [2] scores of tile j in buffer j % 2 ready
+  uint64_t* pready_bar = sfull_bar + 2;  // [2] probabilities of tile j written over them
+  uint64_t* pv_bar = pready_bar + 2;     // O += P V of a tile complete
+  uint64_t* drain_bar = pv_bar + 1;
+  uint64_t* pair_bar = drain_bar + 1;    // [4] the two softmax warps of a lane quarter
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pair_bar + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // row-sum exchange of the softmax warp pairs, after the last tile (the ring is idle then)
+  float* xch = reinterpret_cast<float*>(ring);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  int bid = blockIdx.x;
+  const int split = bid % a.splits;
+  bid /= a.splits;
+  const int dh = bid & 1;
+  bid >>= 1;
+  const int qb = bid % a.q_blocks;
+  bid /= a.q_blocks;
+  const int g = bid % a.Hkv;
+  const int b = bid / a.Hkv;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NSLOT; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    mbar_init(q_bar, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sfull_bar[i], 1);
+      mbar_init(&pready_bar[i], SOFT_WARPS * 32);
+    }
+    mbar_init(pv_bar, 1);
+    mbar_init(drain_bar, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&pair_bar[i], 64);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == PRODUCER_WARP && lane == 0) {
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmKe);
+    prefetch_tmap(&tmVe);
+    prefetch_tmap(&tmKc);
+    prefetch_tmap(&tmVc);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const Tiles T = tiles_of(a, b, qb, split);
+  const int n = T.t_end - T.t_begin;
+
+  if (warp == PRODUCER_WARP) {
+    if (lane == 0) {
+      int slot = 0;
+      uint32_t phase = 0, issued = 0, last_phase = 0;
+      bool ok = true;
+      if (n > 0) {
+        mbar_arrive_expect_tx(q_bar, Q_BYTES);
+        for (int c = 0; c < HD / 64; ++c)
+          tma_load_3d(sQ + c * BOX, &tmQ, q_bar, c * 64, g * a.G, b * a.C + T.p0);
+      }
+      // one ring slot: two boxes of 64 head columns x 128 keys of tile t
+      auto load_unit = [&](int t, bool is_v, int u) -> bool {
+        if (!mbar_wait(&empty_bar[slot], phase ^ 1u, abort_flag, a.status)) return false;
+        uint8_t* dst = ring + slot * UNIT;
+        mbar_arrive_expect_tx(&full_bar[slot], UNIT);
+        const int key0 = T.key0(t);
+        const bool prompt = t < T.nbp;
+        const CUtensorMap* m = prompt ? (is_v ? &tmVe : &tmKe) : (is_v ? &tmVc : &tmKc);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int col = (is_v ? dh * DH : 0) + u * 128 + h * 64;
+          uint8_t* d = dst + h * BOX;
+          if (prompt && a.page_table) {
+            const int ps = a.page_size;
+            for (int i = 0; i < BN / ps; ++i) {
+              // keys past the prompt read its last page and are masked by the softmax
+              int pg = page_of(a, b, min(key0 + i * ps, T.P - 1));
+              if (pg < 0) pg = 0;
+              tma_load_3d(d + i * ps * 128, m, &full_bar[slot], col, g, pg * ps);
+            }
+          } else {
+            const int row = prompt ? b * a.Pmax + key0 : b * a.C + key0;
+            tma_load_3d(d, m, &full_bar[slot], col, g, row);
+          }
+        }
+        issued |= 1u << slot;
+        last_phase = (last_phase & ~(1u << slot)) | (phase << slot);
+        if (++slot == NSLOT) {
+          slot = 0;
+          phase ^= 1u;
+        }
+        return true;
+      };
+      // the MMA warp consumes K(t0), then K(t+1) before V(t) for every tile t
+      for (int u = 0; u < K_UNITS && ok && n > 0; ++u) ok = load_unit(T.t_begin, false, u);
+      for (int j = 0; j < n && ok; ++j) {
+        const int t = T.t_begin + j;
+        if (j + 1 < n)
+          for (int u = 0; u < K_UNITS && ok; ++u) ok = load_unit(t + 1, false, u);
+        for (int u = 0; u < V_UNITS && ok; ++u) ok = load_unit(t, true, u);
+      }
+      if (!ok) {
+        if (n > 0) mbar_wait_drain(q_bar, 0);
+        for (int s = 0; s < NSLOT; ++s)
+          if (issued & (1u << s)) mbar_wait_drain(&full_bar[s], (last_phase >> s) & 1u);
+      }
+    }
+  } else if (warp == MMA_WARP) {
+    if (lane == 0) {
+      int slot = 0;
+      uint32_t phase = 0;
+      bool ok = n > 0 && mbar_wait(q_bar, 0, abort_flag, a.status);
+      tc_fence_after();
+      const uint32_t q_addr = smem_u32(sQ);
+      auto qk = [&](int j) -> bool {
+        const uint32_t d_tmem = tmem_base + S_COL + (j & 1) * BN;
+        for (int u = 0; u < K_UNITS; ++u) {
+          if (!mbar_wait(&full_bar[slot], phase, abort_flag, a.status)) return false;
+          tc_fence_after();
+          const uint32_t base = smem_u32(ring + slot * UNIT);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const int h = kk >> 2, k16 = kk & 3;
+            const uint64_t ad = sw128_kmajor_desc(q_addr + (2 * u + h) * BOX + k16 * 32);
+            const uint64_t bd = sw128_kmajor_desc(base + h * BOX + k16 * 32);
+            tc_mma_f16(d_tmem, ad, bd, IDESC_QK, (u | kk) ? 1u : 0u);
+          }
+          tc_commit(&empty_bar[slot]);
+          if (++slot == NSLOT) {
+            slot = 0;
+            phase ^= 1u;
+          }
+        }
+        tc_commit(&sfull_bar[j & 1]);
+        return true;
+      };
+      auto pv = [&](int j) -> bool {
+        if (!mbar_wait(&pready_bar[j & 1], (j >> 1) & 1u, abort_flag, a.status)) return false;
+        tc_fence_after();
+        const uint32_t p_tmem = tmem_base + S_COL + (j & 1) * BN;
+        for (int u = 0; u < V_UNITS; ++u) {
+          if (!mbar_wait(&full_bar[slot], phase, abort_flag, a.status)) return false;
+          tc_fence_after();
+          const uint32_t base = smem_u32(ring + slot * UNIT);
+#pragma unroll
+          for (int ks = 0; ks < BN / 16; ++ks) {
+            // V is MN-major: 64-column groups BOX bytes apart, 8-key atoms 1 KB apart
+            const uint64_t bd = sw128_mnmajor_desc(base + ks * 2048, BOX, 1024);
+            // P of keys [64 h, 64 h + 64) sits in columns [64 h, 64 h + 32)
+            const uint32_t p_col = ks * 8 + (ks >= 4 ? 32 : 0);
+            tc_mma_f16_ts(tmem_base + O_COL + u * 128, p_tmem + p_col, bd, IDESC_PV,
+                          (j | ks) ? 1u : 0u);
+          }
+          tc_commit(&empty_bar[slot]);
+          if (++slot == NSLOT) {
+            slot = 0;
+            phase ^= 1u;
+          }
+        }
+        tc_commit(pv_bar);
+        return true;
+      };
+      if (ok) ok = qk(0);
+      for (int j = 0; j < n && ok; ++j) {
+        if (j + 1 < n) ok = qk(j + 1);
+        if (ok) ok = pv(j);
+      }
+      tc_commit(drain_bar);
+      mbar_wait_drain(drain_bar, 0);
+    }
+  } else {
+    softmax_and_store(a, T, n, b, g, dh, split, warp, lane, tmem_base, sfull_bar, pready_bar,
+                      pv_bar, pair_bar, abort_flag, xch);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == MMA_WARP) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// Splits of the key range: enough CTAs to fill the SMs; for long key ranges a
+// multiple of the SM count, as long as every split keeps at least 16 tiles.
+int tc_splits(int B, int C, int Hq, int Hkv, int Pmax, int W) {
+  const int G = Hq / Hkv;
+  const int npos = BM / G;
+  const int q_blocks = (C + npos - 1) / npos;
+  const int base = B * Hkv * q_blocks * 2;
+  const int keys_c = std::min(C, npos + 2 * W);
+  const int nb = std::max(1, (Pmax + BN - 1) / BN + (keys_c + BN - 1) / BN);
+  const int sms = dgi::num_sms();
+  int s = std::max(1, sms / base);
+  for (int c = s + 1; c <= nb / 16; ++c)
+    if ((long long)base * c % sms == 0) {
+      s = c;
+      break;
+    }
+  return std::min(s, nb);
+}
+
+}  // namespace
+
+namespace dgi {
+
+bool attn_tc_supported(const AttnArgs& x) {
+  if (x.d != HD || x.Hkv < 1 || x.Hq % x.Hkv) return false;
+  const int G = x.Hq / x.Hkv;
+  if (BM % G) return false;
+  if (x.page_table && (x.page_size < 8 || x.page_size > BN || BN % x.page_size ||
+                       x.page_size % 8))
+    return false;
+  return true;
+}
+
+size_t attn_tc_ws_bytes(int B, int C, int Pmax, int Hq, int Hkv, int W) {
+  const int s = tc_splits(B, C, Hq, Hkv, Pmax, std::min(W, C));
+  if (s == 1) return 256;
+  return align_up((size_t)s * B * C * Hq * HD * 4 + (size_t)s * B * Hq * C * 8, 256);
+}
+
+cudaError_t attn_decode_tc(const AttnArgs& x, void* ws, cudaStream_t st) {
+  TcArgs a{};
+  a.B = x.B;
+  a.C = x.C;
+  a.Pmax = x.Pmax;
+  a.Hq = x.Hq;
+  a.Hkv = x.Hkv;
+  a.W = std::min(x.W, x.C);
+  a.G = x.Hq / x.Hkv;
+  a.npos = BM / a.G;
+  a.q_blocks = (x.C + a.npos - 1) / a.npos;
+  a.splits = tc_splits(x.B, x.C, x.Hq, x.Hkv, x.Pmax, a.W);
+  a.page_table = x.page_table;
+  a.pages_per_req = x.pages_per_req;
+  a.n_pages = x.n_pages;
+  a.page_size = x.page_size;
+  a.prompt_len = x.prompt_len;
+  a.out = reinterpret_cast<__nv_bfloat16*>(x.out);
+  a.lse = x.lse;
+  a.ws_o = static_cast<float*>(ws);
+  a.ws_ml = a.ws_o + (size_t)a.splits * x.B * x.C * x.Hq * HD;
+  a.status = status_ptr();
+  const uint64_t row = HD * 2;
+  CUtensorMap tq, tke, tve, tkc, tvc;
+  {
+    const uint64_t dims[3] = {HD, (uint64_t)x.Hq, (uint64_t)x.B * x.C};
+    const uint64_t str[2] = {row, row * x.Hq};
+    const uint32_t box[3] = {64, (uint32_t)a.G, (uint32_t)a.npos};
+    if (!make_tmap_bf16_3d(&tq, x.q, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {HD, (uint64_t)x.Hkv, (uint64_t)x.B * x.C};
+    const uint64_t str[2] = {row, row * x.Hkv};
+    const uint32_t box[3] = {64, 1, BN};
+    if (!make_tmap_bf16_3d(&tkc, x.kc, dims, str, box)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16_3d(&tvc, x.vc, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  if (x.Pmax > 0) {
+    const bool paged = x.page_table != nullptr;
+    const uint64_t rows = paged ? (uint64_t)x.n_pages * x.page_size : (uint64_t)x.B * x.Pmax;
+    const uint64_t dims[3] = {HD, (uint64_t)x.Hkv, rows};
+    const uint64_t str[2] = {row, row * x.Hkv};
+    const uint32_t box[3] = {64, 1, paged ? (uint32_t)x.page_size : (uint32_t)BN};
+    if (!make_tmap_bf16_3d(&tke, x.kenc, dims, str, box)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16_3d(&tve, x.venc, dims, str, box)) return cudaErrorInvalidValue;
+  } else {
+    tke = tkc;  // no prompt tiles: never read
+    tve = tvc;
+  }
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int grid = a.splits * 2 * a.q_blocks * x.Hkv * x.B;
+  attn_tc_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(tq, tke, tve, tkc, tvc, a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || a.splits == 1) return e;
+  return attn_combine(x.B, x.C, x.Hq, HD, a.splits, a.ws_o, a.ws_ml, x.out, x.lse, st);
+}
+
+}  // namespace dgi

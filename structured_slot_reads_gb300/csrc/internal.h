@@ -15,6 +15,9 @@ int num_sms();
 // Returns false on failure.
 bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+// 3-D tensor map (dims innermost first; strides of dims 1 and 2 in bytes), 128-byte swizzle.
+bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, const uint64_t (&dims)[3],
+                       const uint64_t (&stride_bytes)[2], const uint32_t (&box)[3]);
 
 constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -61,6 +64,13 @@ struct AttnArgs {
 };
 size_t attn_ws_bytes(int B, int C, int Pmax, int Hq, int Hkv, int d, int W);
 cudaError_t attn_decode(const AttnArgs& a, void* ws, cudaStream_t st);
+// Merge split-KV partials ([splits][B][C][Hq][d] fp32 O, [splits][B][Hq][C] (m, l)).
+cudaError_t attn_combine(int B, int C, int Hq, int d, int splits, float* ws_o, float* ws_ml,
+                         uint16_t* out, float* lse, cudaStream_t st);
+// d = 512 on tcgen05 (attn_tc.cu): 128 query rows x 256 output columns per CTA.
+bool attn_tc_supported(const AttnArgs& a);
+size_t attn_tc_ws_bytes(int B, int C, int Pmax, int Hq, int Hkv, int W);
+cudaError_t attn_decode_tc(const AttnArgs& a, void* ws, cudaStream_t st);
 
 // ---- small kernels (slot.cu) -----------------------------------------------
 cudaError_t philox_fill(uint64_t seed, const uint32_t* ctr4, int n, uint32_t* out4,

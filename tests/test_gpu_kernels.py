@@ -126,17 +126,61 @@ def _attn_case(B, C, plen, hq, hkv, d, W, seed, paged=False, page_size=16):
     dict(B=2, C=40, plen=[100, 0], hq=4, hkv=4, d=64, W=3),        # MHA, empty prompt
     dict(B=1, C=96, plen=[70], hq=8, hkv=2, d=512, W=16),          # d=512, GQA 4:1
     dict(B=2, C=64, plen=[130, 17], hq=8, hkv=2, d=512, W=200),    # window wider than canvas
+    # tensor-core kernel (d = 512): split-KV with the combine, one split, GQA 8:1 and 1:1,
+    # a ragged last query block, rows with no visible key in a split, empty splits
+    dict(B=1, C=256, plen=[3000], hq=8, hkv=2, d=512, W=128),
+    dict(B=5, C=128, plen=[200, 0, 77, 300, 129], hq=8, hkv=2, d=512, W=128),
+    dict(B=1, C=40, plen=[260], hq=8, hkv=1, d=512, W=5),
+    dict(B=1, C=200, plen=[140], hq=2, hkv=2, d=512, W=30),
+    dict(B=1, C=256, plen=[0], hq=8, hkv=2, d=512, W=100),
+    dict(B=2, C=64, plen=[1000, 0], hq=8, hkv=2, d=512, W=20),
 ])
 def test_attention_contiguous(case):
     _attn_case(**case, seed=11)
 
 
+def test_attention_rescales_when_late_keys_dominate():
+    """Prompt keys from position 256 on are scaled by 8 (exact in bf16), so the
+    scores of later key tiles exceed the first tiles' maximum by far more than
+    the lazy-rescale headroom and the output accumulator must be rescaled.  Three
+    requests of 256 rows fill the GPU without splitting the key range, so one CTA
+    sees every key tile."""
+    B, C, P, hq, hkv, d, W = 3, 256, 600, 8, 2, 512, 16
+    from structured_slot_reads_gb300 import configs
+    shp = configs.StepShape("t", B=B, C=C, P=P, Hq=hq, Hkv=hkv, d_head=d, W=W, D=8, V=8)
+    x = inputs.attention_inputs(shp, 21)
+    x["kenc"][:, 256:] *= 8.0
+    dims = dg.make_dims(B=B, C=C, P_max=P, Hq=hq, Hkv=hkv, d_head=d, W=W)
+    out = torch.empty((B, C, hq, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, hq, C), dtype=torch.float32, device="cuda")
+    ws = torch.empty(dg.dg_workspace_bytes(dims, dg.DG_WS_ATTN, 0), dtype=torch.uint8,
+                     device="cuda")
+    rc = dg.dg_attn_decode(dims, dev_bf16(x["q"]), dev_bf16(x["kc"]), dev_bf16(x["vc"]),
+                           dev_bf16(x["kenc"]), dev_bf16(x["venc"]), None, 0, 0, 0,
+                           dev(x["prompt_len"]), out, lse, ws)
+    assert rc == dg.DG_OK
+    torch.cuda.synchronize()
+    ref, ref_lse = oracle.attn_decode(x["q"], x["kc"], x["vc"], x["kenc"], x["venc"],
+                                      x["prompt_len"], W)
+    assert_rel(host(out), ref, what="attention output")
+    assert_abs(host(lse), ref_lse, what="attention lse")
+
+
 @pytest.mark.parametrize("case", [
     dict(B=3, C=48, plen=[37, 16, 90], hq=8, hkv=2, d=512, W=8),
     dict(B=2, C=32, plen=[5, 64], hq=2, hkv=1, d=64, W=4),
+    dict(B=4, C=64, plen=[700, 513, 129, 1000], hq=8, hkv=2, d=512, W=128),
 ])
 def test_attention_paged(case):
     _attn_case(**case, seed=5, paged=True)
+
+
+@pytest.mark.parametrize("page_size", [8, 32, 24])
+def test_attention_paged_page_sizes(page_size):
+    """Pages of 8 and 32 keys take the tensor-core kernel; 24 (not a divisor of its
+    128-key tile) takes the warp-level kernel.  Both match the oracle."""
+    _attn_case(B=2, C=64, plen=[300, 77], hq=8, hkv=2, d=512, W=16, seed=9, paged=True,
+               page_size=page_size)
 
 
 def test_slot_noise_rows_bit_exact():
