@@ -372,61 +372,91 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int n = T.t_end - T.t_begin;
 
   if (warp == PRODUCER_WARP) {
-    if (lane == 0) {
-      int slot = 0;
-      uint32_t phase = 0, issued = 0, last_phase = 0;
-      bool ok = true;
-      if (n > 0) {
-        mbar_arrive_expect_tx(q_bar, Q_BYTES);
-        for (int c = 0; c < HD / 64; ++c)
-          tma_load_3d(sQ + c * BOX, &tmQ, q_bar, c * 64, g * a.G, b * a.C + T.p0);
+    // The whole warp produces: lane 0 waits on the ring and arms the barriers;
+    // for paged prompts lane i loads page i of the tile (up to 16 pages of a
+    // 128-key tile), so the page indices and the many small boxes go out in parallel.
+    constexpr unsigned FULL = 0xffffffffu;
+    int slot = 0;
+    uint32_t phase = 0, issued = 0, last_phase = 0;
+    bool ok = true;
+    if (n > 0 && lane == 0) {
+      mbar_arrive_expect_tx(q_bar, Q_BYTES);
+      for (int c = 0; c < HD / 64; ++c)
+        tma_load_3d(sQ + c * BOX, &tmQ, q_bar, c * 64, g * a.G, b * a.C + T.p0);
+    }
+    const int ps = a.page_table ? a.page_size : BN;
+    const int npg = BN / ps;
+    // this lane's page of a prompt tile, kept for the K and for the V stream (keys
+    // past the prompt read its last page, a bad entry reads page 0: both are masked)
+    int pk_t = -1, pv_t = -1, pk_pg = 0, pv_pg = 0;
+    auto page_idx = [&](int t) -> int {
+      int v = 0;
+      if (lane < npg) {
+        const int k = min(t * BN + lane * ps, T.P - 1);
+        v = a.page_table[(long long)b * a.pages_per_req + k / ps];
+        if (v < 0 || v >= a.n_pages) v = 0;
       }
-      // one ring slot: two boxes of 64 head columns x 128 keys of tile t
-      auto load_unit = [&](int t, bool is_v, int u) -> bool {
-        if (!mbar_wait(&empty_bar[slot], phase ^ 1u, abort_flag, a.status)) return false;
-        uint8_t* dst = ring + slot * UNIT;
-        mbar_arrive_expect_tx(&full_bar[slot], UNIT);
-        const int key0 = T.key0(t);
-        const bool prompt = t < T.nbp;
-        const CUtensorMap* m = prompt ? (is_v ? &tmVe : &tmKe) : (is_v ? &tmVc : &tmKc);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int col = (is_v ? dh * DH : 0) + u * 128 + h * 64;
-          uint8_t* d = dst + h * BOX;
-          if (prompt && a.page_table) {
-            const int ps = a.page_size;
-            for (int i = 0; i < BN / ps; ++i) {
-              // keys past the prompt read its last page and are masked by the softmax
-              int pg = page_of(a, b, min(key0 + i * ps, T.P - 1));
-              if (pg < 0) pg = 0;
-              tma_load_3d(d + i * ps * 128, m, &full_bar[slot], col, g, pg * ps);
-            }
-          } else {
-            const int row = prompt ? b * a.Pmax + key0 : b * a.C + key0;
-            tma_load_3d(d, m, &full_bar[slot], col, g, row);
+      return v;
+    };
+    // one ring slot: two boxes of 64 head columns x 128 keys of tile t
+    auto load_unit = [&](int t, bool is_v, int u) -> bool {
+      int w_ok = 1;
+      if (lane == 0) w_ok = mbar_wait(&empty_bar[slot], phase ^ 1u, abort_flag, a.status);
+      if (!__shfl_sync(FULL, w_ok, 0)) return false;
+      uint8_t* dst = ring + slot * UNIT;
+      if (lane == 0) mbar_arrive_expect_tx(&full_bar[slot], UNIT);
+      __syncwarp();
+      const int key0 = T.key0(t);
+      const bool prompt = t < T.nbp;
+      const bool paged = prompt && a.page_table;
+      const CUtensorMap* m = prompt ? (is_v ? &tmVe : &tmKe) : (is_v ? &tmVc : &tmKc);
+      int pg = 0;
+      if (paged) {
+        if (is_v) {
+          if (pv_t != t) {
+            pv_pg = page_idx(t);
+            pv_t = t;
           }
+          pg = pv_pg;
+        } else {
+          if (pk_t != t) {
+            pk_pg = page_idx(t);
+            pk_t = t;
+          }
+          pg = pk_pg;
         }
-        issued |= 1u << slot;
-        last_phase = (last_phase & ~(1u << slot)) | (phase << slot);
-        if (++slot == NSLOT) {
-          slot = 0;
-          phase ^= 1u;
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int col = (is_v ? dh * DH : 0) + u * 128 + h * 64;
+        uint8_t* d = dst + h * BOX;
+        if (paged) {
+          if (lane < npg) tma_load_3d(d + lane * ps * 128, m, &full_bar[slot], col, g, pg * ps);
+        } else if (lane == 0) {
+          const int row = prompt ? b * a.Pmax + key0 : b * a.C + key0;
+          tma_load_3d(d, m, &full_bar[slot], col, g, row);
         }
-        return true;
-      };
-      // the MMA warp consumes K(t0), then K(t+1) before V(t) for every tile t
-      for (int u = 0; u < K_UNITS && ok && n > 0; ++u) ok = load_unit(T.t_begin, false, u);
-      for (int j = 0; j < n && ok; ++j) {
-        const int t = T.t_begin + j;
-        if (j + 1 < n)
-          for (int u = 0; u < K_UNITS && ok; ++u) ok = load_unit(t + 1, false, u);
-        for (int u = 0; u < V_UNITS && ok; ++u) ok = load_unit(t, true, u);
       }
-      if (!ok) {
-        if (n > 0) mbar_wait_drain(q_bar, 0);
-        for (int s = 0; s < NSLOT; ++s)
-          if (issued & (1u << s)) mbar_wait_drain(&full_bar[s], (last_phase >> s) & 1u);
+      issued |= 1u << slot;
+      last_phase = (last_phase & ~(1u << slot)) | (phase << slot);
+      if (++slot == NSLOT) {
+        slot = 0;
+        phase ^= 1u;
       }
+      return true;
+    };
+    // the MMA warp consumes K(t0), then K(t+1) before V(t) for every tile t
+    for (int u = 0; u < K_UNITS && ok && n > 0; ++u) ok = load_unit(T.t_begin, false, u);
+    for (int j = 0; j < n && ok; ++j) {
+      const int t = T.t_begin + j;
+      if (j + 1 < n)
+        for (int u = 0; u < K_UNITS && ok; ++u) ok = load_unit(t + 1, false, u);
+      for (int u = 0; u < V_UNITS && ok; ++u) ok = load_unit(t, true, u);
+    }
+    if (!ok && lane == 0) {
+      if (n > 0) mbar_wait_drain(q_bar, 0);
+      for (int s = 0; s < NSLOT; ++s)
+        if (issued & (1u << s)) mbar_wait_drain(&full_bar[s], (last_phase >> s) & 1u);
     }
   } else if (warp == MMA_WARP) {
     if (lane == 0) {

@@ -81,55 +81,69 @@ struct HeadsParams {
 };
 
 // Reference of each canvas row: max over the first 64 vocabulary entries of
-// (h . w_v) / T in log2 units, plus headroom.  One CTA per row; warp w owns
-// entries 8w..8w+7 and keeps their eight dot products (and loads) in flight.
+// (h . w_v) / T in log2 units, plus headroom.  One CTA per 8 rows, so each of the
+// 64 W rows is read once per CTA; warp w owns entries 8w..8w+7 and keeps the
+// 8 x 8 dot products (and their loads) in flight.
+constexpr int REF_ROWS = 8;
 __global__ void ref_kernel(const __nv_bfloat16* h, const __nv_bfloat16* w, const float* inv_t,
                            int M, int V, int D, float* ref) {
   constexpr int PER_WARP = REF_N / 8;
-  const int row = blockIdx.x;
+  const int row0 = blockIdx.x * REF_ROWS;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __shared__ float wmax[8];
-  const uint4* x = reinterpret_cast<const uint4*>(h + (long long)row * D);
+  __shared__ float wmax[8][REF_ROWS];
   const int n16 = D / 8;
-  float acc[PER_WARP];
+  float acc[PER_WARP][REF_ROWS];
 #pragma unroll
-  for (int u = 0; u < PER_WARP; ++u) acc[u] = 0.f;
+  for (int u = 0; u < PER_WARP; ++u)
+#pragma unroll
+    for (int r = 0; r < REF_ROWS; ++r) acc[u][r] = 0.f;
   const int v0 = warp * PER_WARP;
-#pragma unroll 2
+#pragma unroll 1
   for (int i = lane; i < n16; i += 32) {
-    const uint4 a = x[i];
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-    uint4 b[PER_WARP];
+    uint4 x[REF_ROWS];
 #pragma unroll
-    for (int u = 0; u < PER_WARP; ++u)
-      b[u] = (v0 + u < V) ? __ldg(reinterpret_cast<const uint4*>(w + (long long)(v0 + u) * D) + i)
-                          : make_uint4(0, 0, 0, 0);
+    for (int r = 0; r < REF_ROWS; ++r)
+      x[r] = (row0 + r < M) ? reinterpret_cast<const uint4*>(h + (long long)(row0 + r) * D)[i]
+                            : make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int u = 0; u < PER_WARP; ++u) {
-      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b[u]);
+      const uint4 b = (v0 + u < V)
+                          ? __ldg(reinterpret_cast<const uint4*>(w + (long long)(v0 + u) * D) + i)
+                          : make_uint4(0, 0, 0, 0);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 fa = __bfloat1622float2(a2[q]);
-        const float2 fb = __bfloat1622float2(b2[q]);
-        acc[u] = fmaf(fa.x, fb.x, acc[u]);
-        acc[u] = fmaf(fa.y, fb.y, acc[u]);
+      for (int r = 0; r < REF_ROWS; ++r) {
+        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&x[r]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 fa = __bfloat1622float2(a2[q]);
+          const float2 fb = __bfloat1622float2(b2[q]);
+          acc[u][r] = fmaf(fa.x, fb.x, acc[u][r]);
+          acc[u][r] = fmaf(fa.y, fb.y, acc[u][r]);
+        }
       }
     }
   }
-  float best = -INFINITY;
 #pragma unroll
-  for (int u = 0; u < PER_WARP; ++u) {
-    float s = acc[u];
+  for (int r = 0; r < REF_ROWS; ++r) {
+    float best = -INFINITY;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (v0 + u < V) best = fmaxf(best, s);
+    for (int u = 0; u < PER_WARP; ++u) {
+      float s = acc[u][r];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (v0 + u < V) best = fmaxf(best, s);
+    }
+    if (lane == 0) wmax[warp][r] = best;
   }
-  if (lane == 0) wmax[warp] = best;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float m = wmax[0];
-    for (int i = 1; i < 8; ++i) m = fmaxf(m, wmax[i]);
-    ref[row] = m * inv_t[row] * LOG2E + REF_HEADROOM;
+  if (threadIdx.x < REF_ROWS) {
+    const int row = row0 + threadIdx.x;
+    if (row < M) {
+      float m = wmax[0][threadIdx.x];
+      for (int k = 1; k < 8; ++k) m = fmaxf(m, wmax[k][threadIdx.x]);
+      ref[row] = m * inv_t[row] * LOG2E + REF_HEADROOM;
+    }
   }
 }
 
@@ -627,7 +641,7 @@ cudaError_t denoise_heads(const uint16_t* h, int M, const uint16_t* draw_rows, i
   } else {
     td = tb;  // unused
   }
-  ref_kernel<<<M, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(h),
+  ref_kernel<<<(M + REF_ROWS - 1) / REF_ROWS, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(h),
                                 reinterpret_cast<const __nv_bfloat16*>(w), inv_t, M, V, D, ref);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

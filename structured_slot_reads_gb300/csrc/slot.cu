@@ -252,6 +252,7 @@ __global__ void commit_kernel(int C, const float* entropy, const int32_t* argmax
   int* open = reinterpret_cast<int*>(ent + C);           // [C]
   float* sorted = reinterpret_cast<float*>(open + C);    // [C]
   __shared__ int n_cand, cut;
+  __shared__ float warp_tot[32];
   const int b = blockIdx.x, i = threadIdx.x;
   const long long base = (long long)b * C;
   float hi = 0.f;
@@ -278,21 +279,24 @@ __global__ void commit_kernel(int C, const float* entropy, const int32_t* argmax
     atomicAdd(&n_cand, 1);
   }
   __syncthreads();
-  if (i == 0) {
-    // ordered scan: first k >= 1 whose prefix sum passes gamma
-    float run = 0.f;
-    int k_cut = n_cand;
-    for (int k = 0; k < n_cand; ++k) {
-      run += sorted[k];
-      if (k > 0 && run > gamma[b]) {
-        k_cut = k;
-        break;
-      }
-    }
-    cut = k_cut;
-    n_commit[b] = k_cut;
+  // prefix sums of the sorted entropies (block scan: warp scans, then warp totals);
+  // the cut is the first k >= 1 whose prefix passes gamma, else every candidate
+  const int lane = i & 31, wid = i >> 5;
+  const int nc = n_cand;
+  float run = (i < nc) ? sorted[i] : 0.f;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, run, o);
+    if (lane >= o) run += y;
   }
+  if (lane == 31) warp_tot[wid] = run;
   __syncthreads();
+  for (int w2 = 0; w2 < wid; ++w2) run += warp_tot[w2];
+  if (i == 0) cut = nc;
+  __syncthreads();
+  if (i >= 1 && i < nc && run > gamma[b]) atomicMin(&cut, i);
+  __syncthreads();
+  if (i == 0) n_commit[b] = cut;
   if (i < C) {
     const bool acc = oi && rank < cut;
     const int tok = argmax[base + i];
