@@ -118,7 +118,8 @@ int dg_lmhead_logsoftmax_entropy(const dg_dims* dims, const uint16_t* h, int M,
  * even), inv_t_out[s*R + r] = inv_t[slot_row[s]].
  *   h [M, d_model] bf16 (M = rows of h);  e [V, d_model] bf16;  inv_t [M] fp32
  *   slot_row, slot_req [S] int32;  rows_out [S*R, d_model] bf16
- *   inv_t_out [S*R] fp32;  noise_tok_out [S, R] int32 (may be NULL) */
+ *   inv_t_out [S*R] fp32;  noise_tok_out [S, R] int32 (may be NULL)
+ * h, e and rows_out must be 16-byte aligned (DG_ERR_ARG otherwise). */
 int dg_slot_noise(const dg_dims* dims, const uint16_t* h, int M, const uint16_t* e,
                   const float* inv_t, const int32_t* slot_row,
                   const int32_t* slot_req, int S, int R, uint64_t seed, int step,
@@ -220,7 +221,7 @@ int dg_selfcond_embed(const dg_dims* dims, const uint16_t* h, int M,
  *  - the self-conditioning probabilities of the canvas rows (24-ai.news,
  *    "Token commit mechanism") as unnormalised bf16 values
  *    probs[i][v] = 2^(z_iv log2(e) - r_i), r_i a per-row reference computed from
- *    the first 64 vocabulary entries, and prob_scale[i] = 1 / sum_v probs[i][v],
+ *    the first 8 vocabulary entries, and prob_scale[i] = 1 / sum_v probs[i][v],
  *    so p_iv = probs[i][v] * prob_scale[i].
  * If some z_iv lies more than 100 / log2(e) nats above r_i the exponent is
  * clamped and DG_DEV_RANGE is set in the status word; dg_selfcond_embed (which

@@ -333,7 +333,7 @@ int dg_slot_noise(const dg_dims* d, const uint16_t* h, int M, const uint16_t* e,
   if (!dims_lm(d) || !pow2(d->V)) return DG_ERR_SHAPE;
   if (S > 0 && (!h || !e || !inv_t || !slot_row || !slot_req || !rows_out || !inv_t_out))
     return DG_ERR_ARG;
-  if (!aligned(h, 4) || !aligned(e, 4) || !aligned(rows_out, 4)) return DG_ERR_ARG;
+  if (!aligned(h, 16) || !aligned(e, 16) || !aligned(rows_out, 16)) return DG_ERR_ARG;
   return launch_result(dgi::slot_noise(h, M, e, d->V, d->d_model, inv_t, slot_row, slot_req, S,
                                        R, seed, step, rows_out, inv_t_out, noise_tok_out,
                                        static_cast<cudaStream_t>(stream)));

@@ -400,7 +400,10 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_kernel(Args a) {
   }
 }
 
-// Merge split partials: one warp per (b, pos, head) row.
+// Merge split partials: one warp per (b, pos, head) row.  The common reference
+// comes first (the lanes read the splits' maxima in parallel); then every
+// split's partial row is read with independent loads, and a split that saw no
+// key (reference -inf, partial never written) is dropped by a select.
 template <int D>
 __global__ void attn_combine_kernel(Args a) {
   const long long row = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
@@ -411,21 +414,30 @@ __global__ void attn_combine_kernel(Args a) {
   const int pos = (int)((row / a.Hq) % a.C);
   const int b = (int)(row / ((long long)a.Hq * a.C));
   const long long split_o = (long long)a.B * a.C * a.Hq * D;
+  auto ml_of = [&](int s) {
+    return a.ws_ml + (((long long)s * a.B + b) * a.Hq + head) * a.C * 2 + pos * 2;
+  };
   float mt = -INFINITY;
-  for (int s = 0; s < a.splits; ++s)
-    mt = fmaxf(mt, a.ws_ml[(((long long)s * a.B + b) * a.Hq + head) * a.C * 2 + pos * 2]);
+  for (int s = lane; s < a.splits; s += 32) mt = fmaxf(mt, ml_of(s)[0]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
   float lt = 0.f;
   float acc[D / 32];
 #pragma unroll
   for (int i = 0; i < D / 32; ++i) acc[i] = 0.f;
+#pragma unroll 4
   for (int s = 0; s < a.splits; ++s) {
-    const float* ml = a.ws_ml + (((long long)s * a.B + b) * a.Hq + head) * a.C * 2 + pos * 2;
-    if (ml[0] == -INFINITY) continue;
-    const float f = exp2f(ml[0] - mt);
-    lt += ml[1] * f;
+    const float* ml = ml_of(s);
+    const float m = ml[0], l = ml[1];
+    const bool live = m != -INFINITY;
+    const float f = live ? exp2f(m - mt) : 0.f;
+    lt += live ? l * f : 0.f;
     const float* wo = a.ws_o + s * split_o + row * D;
 #pragma unroll
-    for (int i = 0; i < D / 32; ++i) acc[i] += wo[i * 32 + lane] * f;
+    for (int i = 0; i < D / 32; ++i) {
+      const float v = wo[i * 32 + lane];
+      acc[i] += live ? v * f : 0.f;
+    }
   }
   const float inv = lt > 0.f ? 1.f / lt : 0.f;
 #pragma unroll

@@ -460,6 +460,7 @@ __global__ void split_reduce_kernel(const float4* part, int k_split, long long n
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
        i += (long long)gridDim.x * blockDim.x) {
     float4 a = part[i];
+#pragma unroll 4
     for (int s = 1; s < k_split; ++s) {
       const float4 b = part[(long long)s * n4 + i];
       a.x += b.x;

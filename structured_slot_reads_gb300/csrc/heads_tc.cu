@@ -4,7 +4,7 @@
 // 24-ai.news "Token commit mechanism") the pass computes the row statistics of
 // softmax(h W^T / T) and, for self-conditioning, the unnormalised
 // probabilities  P~[i, v] = 2^(z_iv log2 e - r_i)  in bf16.  The per-row
-// reference r_i (the row's largest scaled logit over the first 64 vocabulary
+// reference r_i (the row's largest scaled logit over the first 8 vocabulary
 // entries, plus a fixed headroom) is computed once by ref_kernel before the
 // pass and read by every CTA, so the per-CTA sums S_i = sum_v P~ add without
 // rescaling and p_iv = P~_iv / S_i exactly; the P.E GEMM applies 1/S_i in its
@@ -37,7 +37,7 @@ using namespace dgk;
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int REF_N = 64;             // vocabulary entries behind the reference
+constexpr int REF_N = 8;              // vocabulary entries behind the reference
 constexpr float REF_HEADROOM = 24.f;  // log2 units added to the reference maximum
 constexpr float V_CLAMP = 100.f;      // exponent guard (log2 units above the reference)
 constexpr int DRAW_N = 16;
@@ -80,71 +80,58 @@ struct HeadsParams {
   int* status;
 };
 
-// Reference of each canvas row: max over the first 64 vocabulary entries of
-// (h . w_v) / T in log2 units, plus headroom.  One CTA per 8 rows, so each of the
-// 64 W rows is read once per CTA; warp w owns entries 8w..8w+7 and keeps the
-// 8 x 8 dot products (and their loads) in flight.
+// Reference of each canvas row: max over the first REF_N vocabulary entries of
+// (h . w_v) / T in log2 units, plus headroom.  One warp per row (8 rows per
+// CTA), every lane keeping its REF_N partial dot products and all of its loads
+// in flight; the REF_N W rows are shared by the CTA's warps through L1.
 constexpr int REF_ROWS = 8;
 __global__ void ref_kernel(const __nv_bfloat16* h, const __nv_bfloat16* w, const float* inv_t,
                            int M, int V, int D, float* ref) {
-  constexpr int PER_WARP = REF_N / 8;
-  const int row0 = blockIdx.x * REF_ROWS;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __shared__ float wmax[8][REF_ROWS];
+  const int row = blockIdx.x * REF_ROWS + warp;
+  if (row >= M) return;
+  const uint4* x = reinterpret_cast<const uint4*>(h + (long long)row * D);
   const int n16 = D / 8;
-  float acc[PER_WARP][REF_ROWS];
+  float acc[REF_N];
 #pragma unroll
-  for (int u = 0; u < PER_WARP; ++u)
+  for (int u = 0; u < REF_N; ++u) acc[u] = 0.f;
+  for (int base = 0; base < n16; base += 32 * 4) {
+    uint4 a[4], bw[4][REF_N];
 #pragma unroll
-    for (int r = 0; r < REF_ROWS; ++r) acc[u][r] = 0.f;
-  const int v0 = warp * PER_WARP;
-#pragma unroll 1
-  for (int i = lane; i < n16; i += 32) {
-    uint4 x[REF_ROWS];
+    for (int c = 0; c < 4; ++c) {
+      const int i = base + c * 32 + lane;
+      a[c] = i < n16 ? x[i] : make_uint4(0, 0, 0, 0);
 #pragma unroll
-    for (int r = 0; r < REF_ROWS; ++r)
-      x[r] = (row0 + r < M) ? reinterpret_cast<const uint4*>(h + (long long)(row0 + r) * D)[i]
-                            : make_uint4(0, 0, 0, 0);
+      for (int u = 0; u < REF_N; ++u)
+        bw[c][u] = (i < n16 && u < V)
+                       ? __ldg(reinterpret_cast<const uint4*>(w + (long long)u * D) + i)
+                       : make_uint4(0, 0, 0, 0);
+    }
 #pragma unroll
-    for (int u = 0; u < PER_WARP; ++u) {
-      const uint4 b = (v0 + u < V)
-                          ? __ldg(reinterpret_cast<const uint4*>(w + (long long)(v0 + u) * D) + i)
-                          : make_uint4(0, 0, 0, 0);
-      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+    for (int c = 0; c < 4; ++c) {
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[c]);
 #pragma unroll
-      for (int r = 0; r < REF_ROWS; ++r) {
-        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&x[r]);
+      for (int u = 0; u < REF_N; ++u) {
+        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bw[c][u]);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const float2 fa = __bfloat1622float2(a2[q]);
           const float2 fb = __bfloat1622float2(b2[q]);
-          acc[u][r] = fmaf(fa.x, fb.x, acc[u][r]);
-          acc[u][r] = fmaf(fa.y, fb.y, acc[u][r]);
+          acc[u] = fmaf(fa.x, fb.x, acc[u]);
+          acc[u] = fmaf(fa.y, fb.y, acc[u]);
         }
       }
     }
   }
+  float best = -INFINITY;
 #pragma unroll
-  for (int r = 0; r < REF_ROWS; ++r) {
-    float best = -INFINITY;
+  for (int u = 0; u < REF_N; ++u) {
+    float s = acc[u];
 #pragma unroll
-    for (int u = 0; u < PER_WARP; ++u) {
-      float s = acc[u][r];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (v0 + u < V) best = fmaxf(best, s);
-    }
-    if (lane == 0) wmax[warp][r] = best;
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (u < V) best = fmaxf(best, s);
   }
-  __syncthreads();
-  if (threadIdx.x < REF_ROWS) {
-    const int row = row0 + threadIdx.x;
-    if (row < M) {
-      float m = wmax[0][threadIdx.x];
-      for (int k = 1; k < 8; ++k) m = fmaxf(m, wmax[k][threadIdx.x]);
-      ref[row] = m * inv_t[row] * LOG2E + REF_HEADROOM;
-    }
-  }
+  if (lane == 0) ref[row] = best * inv_t[row] * LOG2E + REF_HEADROOM;
 }
 
 template <int MT, int BN, bool DRAWS>

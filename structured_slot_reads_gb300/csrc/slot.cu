@@ -62,13 +62,37 @@ __global__ void slot_noise_kernel(const __nv_bfloat16* h, int M, const __nv_bflo
     inv_t_out[s * R + r] = row_ok ? inv_t[row] : 1.f;
     if (!row_ok) atomicOr(status, 8 /* DG_DEV_BAD_INDEX */);
   }
-  const __nv_bfloat162* hs = reinterpret_cast<const __nv_bfloat162*>(h + (long long)(row_ok ? row : 0) * D);
-  const __nv_bfloat162* es = reinterpret_cast<const __nv_bfloat162*>(e + (long long)tok * D);
-  __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(rows_out + (long long)blockIdx.x * D);
-  for (int i = threadIdx.x; i < D / 2; i += blockDim.x) {
-    const float2 a = __bfloat1622float2(hs[i]);
-    const float2 b = __bfloat1622float2(es[i]);
-    dst[i] = row_ok ? __floats2bfloat162_rn(a.x + b.x, a.y + b.y) : __floats2bfloat162_rn(0.f, 0.f);
+  // 16-byte chunks, each thread's loads issued before its adds (the E row is a
+  // random row of a 1.5 GB table: one memory latency per row, not one per chunk)
+  const uint4* hs = reinterpret_cast<const uint4*>(h + (long long)(row_ok ? row : 0) * D);
+  const uint4* es = reinterpret_cast<const uint4*>(e + (long long)tok * D);
+  uint4* dst = reinterpret_cast<uint4*>(rows_out + (long long)blockIdx.x * D);
+  const int n16 = D / 8;
+  constexpr int U = 4;
+  for (int base = 0; base < n16; base += U * blockDim.x) {
+    uint4 a[U], b[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * blockDim.x + threadIdx.x;
+      a[u] = i < n16 ? hs[i] : make_uint4(0, 0, 0, 0);
+      b[u] = i < n16 ? __ldg(es + i) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * blockDim.x + threadIdx.x;
+      if (i >= n16) continue;
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[u]);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b[u]);
+      uint4 o;
+      __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 x = __bfloat1622float2(a2[q]);
+        const float2 y = __bfloat1622float2(b2[q]);
+        o2[q] = row_ok ? __floats2bfloat162_rn(x.x + y.x, x.y + y.y) : __floats2bfloat162_rn(0.f, 0.f);
+      }
+      dst[i] = o;
+    }
   }
 }
 
@@ -106,7 +130,8 @@ __global__ void slot_finish_kernel(const __nv_bfloat16* rows, const float* inv_t
   if (threadIdx.x == 0 && !n_ok) atomicOr(status, 4);
   __syncthreads();
   // one warp per (draw, label) dot product; each lane issues all of its 16-byte
-  // loads before accumulating so a product costs one memory latency
+  // loads (up to 12, d_model <= 3072) before accumulating, so a product costs one
+  // memory latency
   const bool vec = (D % 8) == 0;
   for (int job = warp; job < R * n; job += nw) {
     const int r = job / n, k = job % n;
@@ -117,16 +142,16 @@ __global__ void slot_finish_kernel(const __nv_bfloat16* rows, const float* inv_t
       const uint4* x = reinterpret_cast<const uint4*>(xr);
       const uint4* y = reinterpret_cast<const uint4*>(yr);
       const int n16 = D / 8;
-      for (int base = 0; base < n16; base += 32 * 4) {
-        uint4 xa[4], ya[4];
+      for (int base = 0; base < n16; base += 32 * 12) {
+        uint4 xa[12], ya[12];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 12; ++u) {
           const int i = base + u * 32 + lane;
           xa[u] = i < n16 ? x[i] : make_uint4(0, 0, 0, 0);
           ya[u] = i < n16 ? __ldg(y + i) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 12; ++u) {
           const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&xa[u]);
           const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&ya[u]);
 #pragma unroll
@@ -260,7 +285,7 @@ __global__ void commit_kernel(int C, const float* entropy, const int32_t* argmax
   if (i < C) {
     hi = entropy[base + i];
     oi = cand[base + i] != 0 && !(committed_state && committed_state[base + i]);
-    ent[i] = hi;
+    ent[i] = oi ? hi : INFINITY;
     open[i] = oi;
   }
   if (i == 0) {
@@ -270,11 +295,16 @@ __global__ void commit_kernel(int C, const float* entropy, const int32_t* argmax
   __syncthreads();
   int rank = 0;
   if (i < C && oi) {
-    for (int j = 0; j < C; ++j) {
-      if (!open[j]) continue;
-      const float hj = ent[j];
-      rank += (hj < hi) || (hj == hi && j < i);
+    // keys of closed positions are +inf (entropies are finite), so they never count
+    int j = 0;
+    for (; j + 4 <= C; j += 4) {
+      const float4 k4 = *reinterpret_cast<const float4*>(ent + j);
+      rank += (k4.x < hi) || (k4.x == hi && j < i);
+      rank += (k4.y < hi) || (k4.y == hi && j + 1 < i);
+      rank += (k4.z < hi) || (k4.z == hi && j + 2 < i);
+      rank += (k4.w < hi) || (k4.w == hi && j + 3 < i);
     }
+    for (; j < C; ++j) rank += (ent[j] < hi) || (ent[j] == hi && j < i);
     sorted[rank] = hi;
     atomicAdd(&n_cand, 1);
   }

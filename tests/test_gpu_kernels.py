@@ -328,7 +328,7 @@ def test_denoise_heads_fused_pass(M, nd, V, D):
 def test_denoise_heads_flags_out_of_range_logits():
     M, V, D = 8, 2048, 128
     h, w, _, inv_t = _lm_inputs(M, V, D, seed=5)
-    # row 3: one logit far above everything in the first 64 vocabulary entries
+    # row 3: one logit far above everything in the first 8 vocabulary entries
     wl = w[1000].astype(np.float64)
     x = h[3].astype(np.float64) + (200.0 / float(inv_t[3])) * wl / np.dot(wl, wl)
     h[3] = inputs.to_bf16(x.astype(np.float32))
