@@ -35,6 +35,7 @@ WORKLOADS = {
     "single_structured_read": ("read", "SINGLE_READ", {}),
     "mixed_batched_reads": ("two_stage", "MIXED_BATCH", {}),
     "long_context_read": ("read", "LONG_CONTEXT", {}),
+    "wide_read_77": ("read", "SINGLE_READ", dict(slots=[(61, 77)])),
     "sweep_read_b1": ("read", "LONG_CONTEXT", dict(B=1, P=8192)),
     "sweep_read_b8": ("read", "LONG_CONTEXT", dict(B=8, P=8192)),
     "sweep_read_b64": ("read", "LONG_CONTEXT", dict(B=64, P=8192)),
@@ -469,7 +470,8 @@ def workload_arm(args, rank, world, local):
         calls = ["dg_attn_decode", "dg_slot_read", "dg_ask_if_select"]
     else:
         run = lambda i: st.run(step_idx=i)              # noqa: E731
-        calls = ["dg_attn_decode", "dg_slot_read", "dg_slot_noise", "dg_denoise_heads",
+        calls = ["dg_attn_decode", "dg_slot_read", "dg_slot_read_wide", "dg_slot_noise",
+                 "dg_denoise_heads",
                  "dg_slot_finish", "dg_commit", "dg_selfcond_from_probs", "dg_canvas_update"]
     dg.dg_clear_status()
     ms, per_call, launches, clk = timed_steps(args, run, calls, local, world)
@@ -483,6 +485,7 @@ def workload_arm(args, rank, world, local):
     work["dg_attn_decode"] = (attn_bytes(shape, plen), attn_flops(shape, plen))
     if kind == "read":
         work["dg_slot_read"] = (Wb + st.S * R * D * 4, 2.0 * st.S * R * V * D)
+        work["dg_slot_read_wide"] = work["dg_slot_read"]
         decisions = st.S
     elif kind == "two_stage":
         rows = (st.S1 + st.S2) * R / 2                  # mean draw rows of the two passes

@@ -53,6 +53,7 @@ extern "C" {
 #define DG_DEV_RANGE 16     /* a logit beyond the fused pass's exponent range */
 
 #define DG_MAX_LABELS 26 /* sotaaz.com, "The server accepts at most 26 alternatives per question" */
+#define DG_MAX_WIDE_LABELS 256 /* label table stride limit of dg_slot_read_wide */
 
 /* workspace kinds for dg_workspace_bytes */
 #define DG_WS_ATTN 1
@@ -161,6 +162,28 @@ int dg_slot_read(const dg_dims* dims, const uint16_t* h, int M, const uint16_t* 
                  int32_t* chosen, float* lp_draws, uint8_t* resampled,
                  int32_t* n_reads, int32_t* noise_tok_out, void* workspace,
                  size_t workspace_bytes, void* stream);
+
+/* ---- next: one wide read in place of the two-stage path -----------------
+ * sotaaz.com, "The server accepts at most 26 alternatives per question": the
+ * example server letters a question's alternatives A-Z, so 77 intents are read
+ * as a 9-way group question and then the chosen group's items; the same page
+ * ("Same model, same groups, a 14-point gap") reports a follow-up in which all
+ * 77 intents are read in one read and the two-stage path loses.  This is
+ * dg_slot_read with label tables of row stride L (1 <= L <= 256): slot s has
+ * n_labels[s] <= L labels at label_ids[s*L ..].  The arithmetic is that of
+ * dg_slot_read (renormalise over the slot's labels, entropy gate, mean of the
+ * reads, argmax with ties to the lowest index).
+ *   label_ids [S, L] int32;  q_avg [S, L] fp32;  lp_draws [S, R, L] fp32; the
+ *   other arguments, the workspace (DG_WS_SLOT_READ with rows = S * samples)
+ *   and the errors are those of dg_slot_read; L > 256 returns
+ *   DG_ERR_TOO_MANY_LABELS. */
+int dg_slot_read_wide(const dg_dims* dims, const uint16_t* h, int M, const uint16_t* w,
+                      const uint16_t* e, const float* inv_t, const int32_t* slot_row,
+                      const int32_t* slot_req, const int32_t* label_ids, const int32_t* n_labels,
+                      int S, int L, uint64_t seed, int step, int samples, float gate,
+                      float* q_avg, float* h_slot, int32_t* chosen, float* lp_draws,
+                      uint8_t* resampled, int32_t* n_reads, int32_t* noise_tok_out,
+                      void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---- a7: ask_if gating of a second read stage --------------------------
  * sotaaz.com, "The server accepts at most 26 alternatives per question": a

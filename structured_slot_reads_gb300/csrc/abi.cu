@@ -132,6 +132,55 @@ bool attn_dims_ok(const dg_dims* d) {
   return d->d_head == 64 || d->d_head == 512;
 }
 
+// The slot read with label tables of row stride L (26 for dg_slot_read).
+int slot_read_impl(const dg_dims* d, const uint16_t* h, int M, const uint16_t* w, const uint16_t* e,
+                   const float* inv_t, const int32_t* slot_row, const int32_t* slot_req,
+                   const int32_t* label_ids, const int32_t* n_labels, int S, int L, uint64_t seed,
+                 int step, int samples, float gate, float* q_avg, float* h_slot, int32_t* chosen,
+                 float* lp_draws, uint8_t* resampled, int32_t* n_reads, int32_t* noise_tok_out,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+  if (!d || S < 0 || samples < 1 || samples > 8 || M < 1) return DG_ERR_ARG;
+  if (!dims_lm(d) || !pow2(d->V)) return DG_ERR_SHAPE;
+  if (S == 0) return DG_OK;
+  if (!h || !w || !e || !inv_t || !slot_row || !slot_req || !label_ids || !n_labels || !q_avg ||
+      !h_slot || !chosen || !lp_draws || !resampled || !n_reads)
+    return DG_ERR_ARG;
+  if (!aligned(h, 16) || !aligned(w, 16) || !aligned(e, 16)) return DG_ERR_ARG;
+  const int R = samples;
+  const int rows = S * R;
+  const size_t need = slot_read_ws(d, rows);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DG_ERR_WORKSPACE;
+  using dgi::align_up;
+  uint8_t* p = static_cast<uint8_t*>(workspace);
+  uint16_t* draw_rows = reinterpret_cast<uint16_t*>(p);
+  p += align_up((size_t)rows * d->d_model * 2, 256);
+  float* inv_rows = reinterpret_cast<float*>(p);
+  p += align_up((size_t)rows * 4, 256);
+  float* lse_rows = reinterpret_cast<float*>(p);
+  p += align_up((size_t)rows * 4, 256);
+  float* ent_rows = reinterpret_cast<float*>(p);
+  p += align_up((size_t)rows * 4, 256);
+  float* maxz_rows = reinterpret_cast<float*>(p);
+  p += align_up((size_t)rows * 4, 256);
+  int32_t* arg_rows = reinterpret_cast<int32_t*>(p);
+  p += align_up((size_t)rows * 4, 256);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t err = dgi::slot_noise(h, M, e, d->V, d->d_model, inv_t, slot_row, slot_req, S, R,
+                                    seed, step, draw_rows, inv_rows, noise_tok_out, st);
+  if (err != cudaSuccess) return DG_ERR_CUDA;
+  err = dgi::lmhead_stats(draw_rows, rows, w, d->V, d->d_model, inv_rows,
+                          dgi::RowStats{lse_rows, ent_rows, maxz_rows, arg_rows}, p, st);
+  if (err != cudaSuccess) return DG_ERR_CUDA;
+  err = (L == DG_MAX_LABELS)
+            ? dgi::slot_finish(draw_rows, inv_rows, lse_rows, w, d->V, d->d_model, label_ids,
+                               n_labels, S, R, samples, gate, q_avg, h_slot, chosen, lp_draws,
+                               resampled, n_reads, st)
+            : dgi::slot_finish_wide(draw_rows, inv_rows, lse_rows, w, d->V, d->d_model,
+                                    label_ids, n_labels, L, S, R, samples, gate, q_avg, h_slot,
+                                    chosen, lp_draws, resampled, n_reads, st);
+  return launch_result(err);
+}
+
 }  // namespace
 
 extern "C" {
@@ -362,42 +411,22 @@ int dg_slot_read(const dg_dims* d, const uint16_t* h, int M, const uint16_t* w, 
                  int step, int samples, float gate, float* q_avg, float* h_slot, int32_t* chosen,
                  float* lp_draws, uint8_t* resampled, int32_t* n_reads, int32_t* noise_tok_out,
                  void* workspace, size_t workspace_bytes, void* stream) {
-  if (!d || S < 0 || samples < 1 || samples > 8 || M < 1) return DG_ERR_ARG;
-  if (!dims_lm(d) || !pow2(d->V)) return DG_ERR_SHAPE;
-  if (S == 0) return DG_OK;
-  if (!h || !w || !e || !inv_t || !slot_row || !slot_req || !label_ids || !n_labels || !q_avg ||
-      !h_slot || !chosen || !lp_draws || !resampled || !n_reads)
-    return DG_ERR_ARG;
-  if (!aligned(h, 16) || !aligned(w, 16) || !aligned(e, 16)) return DG_ERR_ARG;
-  const int R = samples;
-  const int rows = S * R;
-  const size_t need = slot_read_ws(d, rows);
-  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DG_ERR_WORKSPACE;
-  using dgi::align_up;
-  uint8_t* p = static_cast<uint8_t*>(workspace);
-  uint16_t* draw_rows = reinterpret_cast<uint16_t*>(p);
-  p += align_up((size_t)rows * d->d_model * 2, 256);
-  float* inv_rows = reinterpret_cast<float*>(p);
-  p += align_up((size_t)rows * 4, 256);
-  float* lse_rows = reinterpret_cast<float*>(p);
-  p += align_up((size_t)rows * 4, 256);
-  float* ent_rows = reinterpret_cast<float*>(p);
-  p += align_up((size_t)rows * 4, 256);
-  float* maxz_rows = reinterpret_cast<float*>(p);
-  p += align_up((size_t)rows * 4, 256);
-  int32_t* arg_rows = reinterpret_cast<int32_t*>(p);
-  p += align_up((size_t)rows * 4, 256);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t err = dgi::slot_noise(h, M, e, d->V, d->d_model, inv_t, slot_row, slot_req, S, R,
-                                    seed, step, draw_rows, inv_rows, noise_tok_out, st);
-  if (err != cudaSuccess) return DG_ERR_CUDA;
-  err = dgi::lmhead_stats(draw_rows, rows, w, d->V, d->d_model, inv_rows,
-                          dgi::RowStats{lse_rows, ent_rows, maxz_rows, arg_rows}, p, st);
-  if (err != cudaSuccess) return DG_ERR_CUDA;
-  err = dgi::slot_finish(draw_rows, inv_rows, lse_rows, w, d->V, d->d_model, label_ids, n_labels,
-                         S, R, samples, gate, q_avg, h_slot, chosen, lp_draws, resampled, n_reads,
-                         st);
-  return launch_result(err);
+  return slot_read_impl(d, h, M, w, e, inv_t, slot_row, slot_req, label_ids, n_labels, S,
+                        DG_MAX_LABELS, seed, step, samples, gate, q_avg, h_slot, chosen, lp_draws,
+                        resampled, n_reads, noise_tok_out, workspace, workspace_bytes, stream);
+}
+
+int dg_slot_read_wide(const dg_dims* d, const uint16_t* h, int M, const uint16_t* w,
+                      const uint16_t* e, const float* inv_t, const int32_t* slot_row,
+                      const int32_t* slot_req, const int32_t* label_ids, const int32_t* n_labels,
+                      int S, int L, uint64_t seed, int step, int samples, float gate,
+                      float* q_avg, float* h_slot, int32_t* chosen, float* lp_draws,
+                      uint8_t* resampled, int32_t* n_reads, int32_t* noise_tok_out,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  if (L < 1 || L > DG_MAX_WIDE_LABELS) return DG_ERR_TOO_MANY_LABELS;
+  return slot_read_impl(d, h, M, w, e, inv_t, slot_row, slot_req, label_ids, n_labels, S, L,
+                        seed, step, samples, gate, q_avg, h_slot, chosen, lp_draws, resampled,
+                        n_reads, noise_tok_out, workspace, workspace_bytes, stream);
 }
 
 int dg_ask_if_select(const int32_t* chosen1, int S1, const int32_t* cond_slot,

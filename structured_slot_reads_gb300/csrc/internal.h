@@ -84,6 +84,13 @@ cudaError_t slot_finish(const uint16_t* rows, const float* inv_t_rows, const flo
                         const int32_t* n_labels, int S, int R, int samples, float gate,
                         float* q_avg, float* h_slot, int32_t* chosen, float* lp_draws,
                         uint8_t* resampled, int32_t* n_reads, cudaStream_t st);
+// The same with label tables of row stride L <= 256 (wide-label reads).
+cudaError_t slot_finish_wide(const uint16_t* rows, const float* inv_t_rows, const float* lse_rows,
+                             const uint16_t* w, int V, int D, const int32_t* label_ids,
+                             const int32_t* n_labels, int L, int S, int R, int samples,
+                             float gate, float* q_avg, float* h_slot, int32_t* chosen,
+                             float* lp_draws, uint8_t* resampled, int32_t* n_reads,
+                             cudaStream_t st);
 cudaError_t ask_if_select(const int32_t* chosen1, int S1, const int32_t* cond_slot,
                           const int32_t* cond_value, const int32_t* q_owner,
                           const int32_t* q_label_ids, const int32_t* q_n_labels, int Q, int S2,

@@ -104,28 +104,30 @@ __global__ void slot_noise_kernel(const __nv_bfloat16* h, int M, const __nv_bflo
 constexpr int MAXL = 26;
 constexpr int MAXR = 8;
 
+template <int LPL>  // labels per lane of the epilogue warp: label tables of stride L <= 32 LPL
 __global__ void slot_finish_kernel(const __nv_bfloat16* rows, const float* inv_t_rows,
                                    const float* lse_rows, const __nv_bfloat16* w, int V, int D,
-                                   const int32_t* label_ids, const int32_t* n_labels, int R,
+                                   const int32_t* label_ids, const int32_t* n_labels, int L, int R,
                                    int samples, float gate, float* q_avg, float* h_slot,
                                    int32_t* chosen, float* lp_draws, uint8_t* resampled,
                                    int32_t* n_reads, int* status) {
-  __shared__ float z[MAXR][MAXL];
-  __shared__ int ids[MAXL];
+  constexpr int CAP = 32 * LPL;
+  __shared__ float z[MAXR][CAP];
+  __shared__ int ids[CAP];
   const int s = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nw = blockDim.x >> 5;
   int n = n_labels[s];
   // n == 0: a question whose ask_if condition did not fire -- not read
-  const bool n_ok = n >= 0 && n <= MAXL;
+  const bool n_ok = n >= 0 && n <= L;
   if (!n_ok) n = 0;
-  if (threadIdx.x < MAXL) {
-    int id = (threadIdx.x < n) ? label_ids[s * MAXL + threadIdx.x] : 0;
+  for (int k = threadIdx.x; k < CAP; k += blockDim.x) {
+    int id = (k < n) ? label_ids[(long long)s * L + k] : 0;
     if (id < 0 || id >= V) {
       id = 0;
-      if (threadIdx.x < n) atomicOr(status, 4 /* DG_DEV_BAD_LABEL */);
+      if (k < n) atomicOr(status, 4 /* DG_DEV_BAD_LABEL */);
     }
-    ids[threadIdx.x] = id;
+    ids[k] = id;
   }
   if (threadIdx.x == 0 && !n_ok) atomicOr(status, 4);
   __syncthreads();
@@ -179,38 +181,63 @@ __global__ void slot_finish_kernel(const __nv_bfloat16* rows, const float* inv_t
   }
   __syncthreads();
   if (warp != 0) return;
-  // warp-parallel epilogue: lane k holds label k
-  const int k = lane;
-  const bool kv = k < n;
-  float qsum = 0.f, q0 = 0.f, h0 = 0.f;
+  // warp epilogue: lane holds labels lane + 32 i, i < LPL
+  float qsum[LPL], q0[LPL];
+#pragma unroll
+  for (int i = 0; i < LPL; ++i) qsum[i] = q0[i] = 0.f;
+  float h0 = 0.f;
   for (int r = 0; r < R; ++r) {
-    const float zk = kv ? z[r][k] : -INFINITY;
-    float m = zk;
+    float zk[LPL];
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < LPL; ++i) {
+      const int k = lane + 32 * i;
+      zk[i] = k < n ? z[r][k] : -INFINITY;
+      m = fmaxf(m, zk[i]);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    const float ek = kv ? expf(zk - m) : 0.f;
-    float tot = ek;
+    float ek[LPL], tot = 0.f;
+#pragma unroll
+    for (int i = 0; i < LPL; ++i) {
+      ek[i] = (lane + 32 * i < n) ? expf(zk[i] - m) : 0.f;
+      tot += ek[i];
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-    const float q = ek / tot;
-    float hq = (kv && q > 0.f) ? -q * logf(q) : 0.f;
+    float hq = 0.f;
+    const float lse_r = lse_rows[s * R + r];
+#pragma unroll
+    for (int i = 0; i < LPL; ++i) {
+      const int k = lane + 32 * i;
+      const float q = ek[i] / tot;
+      if (k < n && q > 0.f) hq -= q * logf(q);
+      if (k < L) lp_draws[((long long)s * R + r) * L + k] = k < n ? zk[i] - lse_r : 0.f;
+      if (r < samples) qsum[i] += q;
+      if (r == 0) q0[i] = q;
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) hq += __shfl_xor_sync(0xffffffffu, hq, o);
-    if (k < MAXL) lp_draws[((long long)s * R + r) * MAXL + k] = kv ? zk - lse_rows[s * R + r] : 0.f;
-    if (r < samples) qsum += q;
-    if (r == 0) {
-      q0 = q;
-      h0 = hq;
-    }
+    if (r == 0) h0 = hq;
   }
   const bool fire = samples > 1 && h0 > gate;
-  const float qk = kv ? (fire ? qsum / (float)samples : q0) : 0.f;
-  float hs = (kv && qk > 0.f) ? -qk * logf(qk) : 0.f;
+  float hs = 0.f, best = -1.f;
+  int arg = 0x7fffffff;
+#pragma unroll
+  for (int i = 0; i < LPL; ++i) {
+    const int k = lane + 32 * i;
+    const bool kv = k < n;
+    const float qk = kv ? (fire ? qsum[i] / (float)samples : q0[i]) : 0.f;
+    if (kv && qk > 0.f) hs -= qk * logf(qk);
+    if (kv && qk > best) {  // i ascends, so the lowest index wins within the lane
+      best = qk;
+      arg = k;
+    }
+    if (k < L) q_avg[(long long)s * L + k] = qk;
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) hs += __shfl_xor_sync(0xffffffffu, hs, o);
-  // argmax over labels, lowest index on ties
-  float best = kv ? qk : -1.f;
-  int arg = k;
+  // argmax over lanes, lowest index on ties
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float bo = __shfl_xor_sync(0xffffffffu, best, o);
@@ -220,7 +247,6 @@ __global__ void slot_finish_kernel(const __nv_bfloat16* rows, const float* inv_t
       arg = ao;
     }
   }
-  if (k < MAXL) q_avg[s * MAXL + k] = qk;
   if (lane == 0) {
     chosen[s] = n > 0 ? arg : -1;
     h_slot[s] = hs;
@@ -395,10 +421,36 @@ cudaError_t slot_finish(const uint16_t* rows, const float* inv_t_rows, const flo
                         float* q_avg, float* h_slot, int32_t* chosen, float* lp_draws,
                         uint8_t* resampled, int32_t* n_reads, cudaStream_t st) {
   if (S == 0) return cudaSuccess;
-  slot_finish_kernel<<<S, 1024, 0, st>>>(
+  slot_finish_kernel<1><<<S, 1024, 0, st>>>(
       reinterpret_cast<const __nv_bfloat16*>(rows), inv_t_rows, lse_rows,
-      reinterpret_cast<const __nv_bfloat16*>(w), V, D, label_ids, n_labels, R, samples, gate,
-      q_avg, h_slot, chosen, lp_draws, resampled, n_reads, status_ptr());
+      reinterpret_cast<const __nv_bfloat16*>(w), V, D, label_ids, n_labels, MAXL, R, samples,
+      gate, q_avg, h_slot, chosen, lp_draws, resampled, n_reads, status_ptr());
+  return cudaGetLastError();
+}
+
+cudaError_t slot_finish_wide(const uint16_t* rows, const float* inv_t_rows, const float* lse_rows,
+                             const uint16_t* w, int V, int D, const int32_t* label_ids,
+                             const int32_t* n_labels, int L, int S, int R, int samples,
+                             float gate, float* q_avg, float* h_slot, int32_t* chosen,
+                             float* lp_draws, uint8_t* resampled, int32_t* n_reads,
+                             cudaStream_t st) {
+  if (S == 0) return cudaSuccess;
+  if (L < 1 || L > 256) return cudaErrorInvalidValue;
+  const __nv_bfloat16* rb = reinterpret_cast<const __nv_bfloat16*>(rows);
+  const __nv_bfloat16* wb = reinterpret_cast<const __nv_bfloat16*>(w);
+  int* stp = status_ptr();
+  if (L <= 64)
+    slot_finish_kernel<2><<<S, 1024, 0, st>>>(rb, inv_t_rows, lse_rows, wb, V, D, label_ids,
+                                              n_labels, L, R, samples, gate, q_avg, h_slot,
+                                              chosen, lp_draws, resampled, n_reads, stp);
+  else if (L <= 128)
+    slot_finish_kernel<4><<<S, 1024, 0, st>>>(rb, inv_t_rows, lse_rows, wb, V, D, label_ids,
+                                              n_labels, L, R, samples, gate, q_avg, h_slot,
+                                              chosen, lp_draws, resampled, n_reads, stp);
+  else
+    slot_finish_kernel<8><<<S, 1024, 0, st>>>(rb, inv_t_rows, lse_rows, wb, V, D, label_ids,
+                                              n_labels, L, R, samples, gate, q_avg, h_slot,
+                                              chosen, lp_draws, resampled, n_reads, stp);
   return cudaGetLastError();
 }
 

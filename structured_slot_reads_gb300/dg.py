@@ -23,6 +23,7 @@ DG_DEV_RANGE = 16
 DG_WS_ATTN, DG_WS_LMHEAD, DG_WS_SLOT_READ, DG_WS_SELFCOND = 1, 2, 3, 4
 DG_WS_HEADS, DG_WS_PROBS_EMBED = 5, 6
 DG_MAX_LABELS = MAX_LABELS = 26
+DG_MAX_WIDE_LABELS = 256
 DG_NOALLOC_MAX_ROWS = 512
 
 
@@ -58,6 +59,8 @@ _SIGS = {
     "dg_slot_finish": [DP, P, P, P, P, P, P, I, I, I, F, P, P, P, P, P, P, P],
     "dg_slot_read": [DP, P, I, P, P, P, P, P, P, P, I, U64, I, I, F, P, P, P, P, P, P, P, P, Z,
                      P],
+    "dg_slot_read_wide": [DP, P, I, P, P, P, P, P, P, P, I, I, U64, I, I, F, P, P, P, P, P, P, P,
+                          P, Z, P],
     "dg_commit": [DP, P, P, P, P, P, P, P, P, P, P],
     "dg_selfcond_embed": [DP, P, I, P, P, P, P, P, P, Z, P],
     "dg_denoise_heads": [DP, P, I, P, I, P, P, P, P, P, P, P, P, P, P, Z, P, Z, P],
@@ -169,6 +172,16 @@ def dg_slot_read(dims, h, M, w, e, inv_t, slot_row, slot_req, label_ids, n_label
                               step, samples, gate, _p(q_avg), _p(h_slot), _p(chosen),
                               _p(lp_draws), _p(resampled), _p(n_reads), _p(noise_tok_out),
                               _p(workspace), _nbytes(workspace), _s(stream))
+
+
+def dg_slot_read_wide(dims, h, M, w, e, inv_t, slot_row, slot_req, label_ids, n_labels, S, L,
+                      seed, step, samples, gate, q_avg, h_slot, chosen, lp_draws, resampled,
+                      n_reads, noise_tok_out, workspace, stream=None):
+    return lib().dg_slot_read_wide(ctypes.byref(dims), _p(h), M, _p(w), _p(e), _p(inv_t),
+                                   _p(slot_row), _p(slot_req), _p(label_ids), _p(n_labels), S, L,
+                                   seed, step, samples, gate, _p(q_avg), _p(h_slot), _p(chosen),
+                                   _p(lp_draws), _p(resampled), _p(n_reads), _p(noise_tok_out),
+                                   _p(workspace), _nbytes(workspace), _s(stream))
 
 
 def dg_commit(dims, entropy, argmax, cand, gamma, committed_state, token_state, commit, tokens,

@@ -143,24 +143,24 @@ def label_set(n, V, *key):
     return _rng(*key).choice(V, size=n, replace=False).astype(np.int32)
 
 
-def slot_table(shape: StepShape, seed):
+def slot_table(shape: StepShape, seed, L=MAX_LABELS):
     """Slot rows, request ids and label ids for the slots of ``shape`` (same for every request).
 
     Returns slot_row [S] (flattened canvas row b*C + pos), slot_req [S],
-    label_ids [S, 26] (-1 padded), n_labels [S].
+    label_ids [S, L] (-1 padded; L = 26 unless a wide table is asked for), n_labels [S].
     """
     rows, reqs, labs, ns = [], [], [], []
     for b in range(shape.B):
         for j, (pos, k) in enumerate(shape.slots):
             rows.append(b * shape.C + pos)
             reqs.append(b)
-            lab = np.full(MAX_LABELS, -1, dtype=np.int32)
+            lab = np.full(L, -1, dtype=np.int32)
             lab[:k] = label_set(k, shape.V, seed, S_LABELS, b, j)
             labs.append(lab)
             ns.append(k)
     if not rows:
         return (np.zeros(0, np.int32), np.zeros(0, np.int32),
-                np.zeros((0, MAX_LABELS), np.int32), np.zeros(0, np.int32))
+                np.zeros((0, L), np.int32), np.zeros(0, np.int32))
     return (np.array(rows, np.int32), np.array(reqs, np.int32),
             np.stack(labs), np.array(ns, np.int32))
 

@@ -24,13 +24,13 @@ def _dev(a, dtype, device):
     return torch.as_tensor(np.ascontiguousarray(a)).to(device=device, dtype=dtype)
 
 
-def slot_outputs(S, R, dev):
-    """Device buffers of one dg_slot_read over S slots with R reads each."""
+def slot_outputs(S, R, dev, L=dg.MAX_LABELS):
+    """Device buffers of one slot read over S slots with R reads each (label stride L)."""
     f32, i32, u8 = torch.float32, torch.int32, torch.uint8
-    return dict(q_avg=torch.empty((S, dg.MAX_LABELS), dtype=f32, device=dev),
+    return dict(q_avg=torch.empty((S, L), dtype=f32, device=dev),
                 h_slot=torch.empty(S, dtype=f32, device=dev),
                 chosen=torch.empty(S, dtype=i32, device=dev),
-                lp=torch.empty((S, R, dg.MAX_LABELS), dtype=f32, device=dev),
+                lp=torch.empty((S, R, L), dtype=f32, device=dev),
                 resampled=torch.empty(S, dtype=u8, device=dev),
                 n_reads=torch.empty(S, dtype=i32, device=dev),
                 tokens=torch.empty((S, R), dtype=i32, device=dev))
@@ -157,6 +157,8 @@ class ReadStep:
     """
 
     def __init__(self, shape, w, e, device="cuda", seed=0):
+        """Slots with more than 26 labels are read with dg_slot_read_wide (one table of
+        stride L = the largest label count)."""
         self.shape = shape
         self.dims = dg.dims_of(shape)
         self.device = device
@@ -175,13 +177,14 @@ class ReadStep:
         self.prompt_len = torch.full((B,), shape.P, dtype=i32, device=device)
         self.attn_out = torch.empty_like(self.q)
         self.attn_lse = torch.empty((B, shape.Hq, C), dtype=f32, device=device)
-        row, req, lab, n = inputs.slot_table(shape, seed)
+        self.L = max([dg.MAX_LABELS] + [k for _, k in shape.slots])
+        row, req, lab, n = inputs.slot_table(shape, seed, self.L)
         self.S = len(row)
         self.slot_row = _dev(row, i32, device)
         self.slot_req = _dev(req, i32, device)
         self.label_ids = _dev(lab, i32, device)
         self.n_labels = _dev(n, i32, device)
-        self.out = slot_outputs(self.S, shape.R, device)
+        self.out = slot_outputs(self.S, shape.R, device, self.L)
         self.ws_attn = torch.empty(max(dg.dg_workspace_bytes(self.dims, dg.DG_WS_ATTN, 0), 256),
                                    dtype=u8, device=device)
         self.ws_read = torch.empty(dg.dg_workspace_bytes(self.dims, dg.DG_WS_SLOT_READ,
@@ -194,10 +197,19 @@ class ReadStep:
         dg._check(dg.dg_attn_decode(d, self.q, self.kc, self.vc, self.kenc, self.venc, None, 0,
                                     0, 0, self.prompt_len, self.attn_out, self.attn_lse,
                                     self.ws_attn, stream), "dg_attn_decode")
-        dg._check(dg.dg_slot_read(d, self.h, self.M, self.w, self.e, self.inv_t, self.slot_row,
-                                  self.slot_req, self.label_ids, self.n_labels, self.S,
-                                  self.seed, step_idx, s.R, s.gate, o["q_avg"], o["h_slot"],
-                                  o["chosen"], o["lp"], o["resampled"], o["n_reads"],
-                                  o["tokens"], self.ws_read, stream), "dg_slot_read")
+        if self.L == dg.MAX_LABELS:
+            dg._check(dg.dg_slot_read(d, self.h, self.M, self.w, self.e, self.inv_t,
+                                      self.slot_row, self.slot_req, self.label_ids,
+                                      self.n_labels, self.S, self.seed, step_idx, s.R, s.gate,
+                                      o["q_avg"], o["h_slot"], o["chosen"], o["lp"],
+                                      o["resampled"], o["n_reads"], o["tokens"], self.ws_read,
+                                      stream), "dg_slot_read")
+        else:
+            dg._check(dg.dg_slot_read_wide(d, self.h, self.M, self.w, self.e, self.inv_t,
+                                           self.slot_row, self.slot_req, self.label_ids,
+                                           self.n_labels, self.S, self.L, self.seed, step_idx,
+                                           s.R, s.gate, o["q_avg"], o["h_slot"], o["chosen"],
+                                           o["lp"], o["resampled"], o["n_reads"], o["tokens"],
+                                           self.ws_read, stream), "dg_slot_read_wide")
         attn_kernels = 1 if dg.dg_workspace_bytes(d, dg.DG_WS_ATTN, 0) <= 256 else 2
         return attn_kernels + 4

@@ -183,3 +183,13 @@ def test_two_stage_runner_builds_on_host(lib):
                                stream=0) == dg.DG_ERR_ARG
     assert dg.dg_ask_if_select(16, 1, 16, 16, 16, 16, 16, 2, -1, 16, 16,
                                stream=0) == dg.DG_ERR_ARG
+
+
+def test_wide_read_rejects_tables_wider_than_256(lib):
+    d = dg.make_dims(d_model=128, V=1024)
+    rc = dg.dg_slot_read_wide(d, 16, 4, 16, 16, 16, 16, 16, 16, 16, 1, 257, 0, 0, 4, 0.1, 16, 16,
+                              16, 16, 16, 16, None, None, stream=0)
+    assert rc == dg.DG_ERR_TOO_MANY_LABELS
+    rc = dg.dg_slot_read_wide(d, 16, 4, 16, 16, 16, 16, 16, 16, 16, 1, 0, 0, 0, 4, 0.1, 16, 16,
+                              16, 16, 16, 16, None, None, stream=0)
+    assert rc == dg.DG_ERR_TOO_MANY_LABELS
