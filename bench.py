@@ -36,6 +36,8 @@ WORKLOADS = {
     "mixed_batched_reads": ("two_stage", "MIXED_BATCH", {}),
     "long_context_read": ("read", "LONG_CONTEXT", {}),
     "wide_read_77": ("read", "SINGLE_READ", dict(slots=[(61, 77)])),
+    "prefill_8192": ("prefill", "LONG_CONTEXT", dict(B=1, P=8192)),
+    "prefill_long": ("prefill", "LONG_CONTEXT", {}),
     "sweep_read_b1": ("read", "LONG_CONTEXT", dict(B=1, P=8192)),
     "sweep_read_b8": ("read", "LONG_CONTEXT", dict(B=8, P=8192)),
     "sweep_read_b64": ("read", "LONG_CONTEXT", dict(B=64, P=8192)),
@@ -370,6 +372,18 @@ def attn_flops(shape, prompt_len=None):
     return 4.0 * shape.Hq * shape.d_head * vis
 
 
+def prefill_flops(shape):
+    """Causal prefill: QK^T and PV over the P (P + 1) / 2 visible (row, key) pairs."""
+    return 4.0 * shape.B * shape.Hq * shape.d_head * shape.P * (shape.P + 1) / 2
+
+
+def prefill_bytes(shape):
+    """Q and O once, K and V read once and written once more into the page pool."""
+    q = shape.B * shape.P * shape.Hq * shape.d_head * 2
+    kv = shape.B * shape.P * shape.Hkv * shape.d_head * 2 * 2
+    return 2 * q + 2 * kv
+
+
 def attn_bytes(shape, prompt_len=None):
     """Algorithmic attention bytes: prompt + canvas K/V once, Q read and O written once."""
     plens = [shape.P] * shape.B if prompt_len is None else [int(p) for p in prompt_len]
@@ -404,6 +418,15 @@ def build_runner(kind, shape, device):
     from structured_slot_reads_gb300.read import ReadStep, TwoStageRead
     if kind == "step":
         return build_step(shape, device)
+    if kind == "prefill":
+        from structured_slot_reads_gb300.read import Prefill
+        st = Prefill(shape.B, shape.P, shape.Hq, shape.Hkv, shape.d_head, shape.page_size,
+                     device=device, seed=5)
+        for i, k in enumerate(("q", "k", "v")):
+            getattr(st, k).copy_(inputs.device_normal_bf16(getattr(st, k).shape, 1.0, 30 + i,
+                                                           device))
+        torch.cuda.synchronize()
+        return st
     w = inputs.device_normal_bf16((shape.V, shape.D), shape.D ** -0.5, 1, device)
     e = inputs.device_normal_bf16((shape.V, shape.D), shape.D ** -0.5, 2, device)
     if kind == "read":
@@ -468,6 +491,9 @@ def workload_arm(args, rank, world, local):
     if kind == "two_stage":
         run = lambda i: st.run()                        # noqa: E731
         calls = ["dg_attn_decode", "dg_slot_read", "dg_ask_if_select"]
+    elif kind == "prefill":
+        run = lambda i: st.run(step_idx=i)              # noqa: E731
+        calls = ["dg_prefill_attn"]
     else:
         run = lambda i: st.run(step_idx=i)              # noqa: E731
         calls = ["dg_attn_decode", "dg_slot_read", "dg_slot_read_wide", "dg_slot_noise",
@@ -483,6 +509,8 @@ def workload_arm(args, rank, world, local):
     plen = getattr(st, "prompt_lens_host", None)
     work = call_work(shape, st) if kind == "step" else {}
     work["dg_attn_decode"] = (attn_bytes(shape, plen), attn_flops(shape, plen))
+    if kind == "prefill":
+        work["dg_prefill_attn"] = (prefill_bytes(shape), prefill_flops(shape))
     if kind == "read":
         work["dg_slot_read"] = (Wb + st.S * R * D * 4, 2.0 * st.S * R * V * D)
         work["dg_slot_read_wide"] = work["dg_slot_read"]
@@ -520,6 +548,8 @@ def workload_arm(args, rank, world, local):
                 "kernel": n, "peak_source": pk["source"]}
     if kind == "step":
         unit, value = UNIT, steps_per_s * shape.B
+    elif kind == "prefill":
+        unit, value = "prompt tokens/s", steps_per_s * shape.B * shape.P
     else:
         unit, value = "slot decisions/s", steps_per_s * decisions
     return {

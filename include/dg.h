@@ -62,6 +62,7 @@ extern "C" {
 #define DG_WS_SELFCOND 4
 #define DG_WS_HEADS 5
 #define DG_WS_PROBS_EMBED 6
+#define DG_WS_PREFILL 7
 
 /* Problem dimensions.  B requests, C canvas tokens each, P_max the longest
  * prompt (encoder KV) length, Hq/Hkv query/KV heads (GQA, Hq % Hkv == 0),
@@ -162,6 +163,31 @@ int dg_slot_read(const dg_dims* dims, const uint16_t* h, int M, const uint16_t* 
                  int32_t* chosen, float* lp_draws, uint8_t* resampled,
                  int32_t* n_reads, int32_t* noise_tok_out, void* workspace,
                  size_t workspace_bytes, void* stream);
+
+/* ---- next: encoder-mode prefill writing the paged prompt KV -------------
+ * thakicloud.com, "What is DiffusionGemma": one backbone runs in two modes; the
+ * encoder mode reads the prompt causally and keeps its KV cache, which the
+ * decoder mode (dg_attn_decode) then reads.  24-ai.news, "How does diffusion
+ * text generation differ?": the encoder mode is causal.  For every request b
+ * and prompt row i < prompt_len[b]:
+ *   out[b, i, h] = softmax_{j <= i}(q_i . k_j / sqrt(d)) v_j   (query head h reads
+ *   KV head h / (Hq/Hkv)), lse[b, h, i] its log-normaliser (natural log);
+ * rows i >= prompt_len[b] are not written.  With a page table, the first
+ * prompt_len[b] rows of k and v are also copied into the page pools
+ * (pool[page_table[b, i / page_size], i % page_size] = row i), the layout
+ * dg_attn_decode reads.  dims: B, P_max (rows of q/k/v per request), Hq, Hkv,
+ * d_head = 512 (Hq/Hkv dividing 128); the other fields are ignored.
+ *   q, out [B, P_max, Hq, 512] bf16;  k, v [B, P_max, Hkv, 512] bf16;
+ *   prompt_len [B] int32 (clamped to [0, P_max]);  lse [B, Hq, P_max] fp32;
+ *   page_table [B, pages_per_req] int32 or NULL;  pool_k, pool_v
+ *   [n_pages, page_size, Hkv, 512] bf16 (16-byte aligned, like q, k, v, out);
+ *   workspace: dg_workspace_bytes(dims, DG_WS_PREFILL, 0) bytes.
+ * A page index outside [0, n_pages) sets DG_DEV_BAD_PAGE and skips that row. */
+int dg_prefill_attn(const dg_dims* dims, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                    const int32_t* prompt_len, uint16_t* out, float* lse,
+                    const int32_t* page_table, int pages_per_req, int n_pages, int page_size,
+                    uint16_t* pool_k, uint16_t* pool_v, void* workspace, size_t workspace_bytes,
+                    void* stream);
 
 /* ---- next: one wide read in place of the two-stage path -----------------
  * sotaaz.com, "The server accepts at most 26 alternatives per question": the

@@ -34,6 +34,8 @@ from .step import (  # noqa: F401
     bf16_round,
     attn_decode,
     paged_to_contiguous,
+    paged_write,
+    prefill_attn,
     lmhead_stats,
     label_logits,
     slot_noise_rows,

@@ -101,6 +101,67 @@ def attn_decode(q, kc, vc, kenc, venc, prompt_len, window):
     return out, lse
 
 
+def prefill_attn(q, k, v, prompt_len, rows=None):
+    """Encoder-mode attention of each request's prompt over itself, causally.
+
+    thakicloud.com, "What is DiffusionGemma": the one backbone also runs in an
+    encoder mode that reads the prompt causally and keeps its KV cache for the
+    decoder mode.  24-ai.news, "How does diffusion text generation differ?":
+    the encoder mode is causal.
+
+    Readings: row i of request b sees keys j <= i of the same request (self
+    included); scale 1/sqrt(d_head), no softcap; query head h reads KV head
+    h // (Hq/Hkv); rows at or past prompt_len[b] are not computed (left zero,
+    lse 0).  ``rows`` (optional) limits the work to those row indices.
+
+    q: [B, P, Hq, d]; k, v: [B, P, Hkv, d]; prompt_len: [B].
+    Returns out [B, P, Hq, d] and lse [B, Hq, P] (natural log).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B, P, hq, d = q.shape
+    hkv = k.shape[2]
+    group = hq // hkv
+    scale = 1.0 / np.sqrt(d)
+    out = np.zeros((B, P, hq, d), dtype=np.float64)
+    lse = np.zeros((B, hq, P), dtype=np.float64)
+    for b in range(B):
+        n = int(min(max(int(prompt_len[b]), 0), P))
+        idx = np.arange(n) if rows is None else np.array([r for r in rows if r < n], np.int64)
+        if idx.size == 0:
+            continue
+        last = int(idx.max()) + 1
+        for h in range(hq):
+            g = h // group
+            keys = np.asarray(k[b, :last, g], np.float64)
+            vals = np.asarray(v[b, :last, g], np.float64)
+            s = (q[b, idx, h] @ keys.T) * scale                 # [rows, last]
+            s = np.where(np.arange(last)[None, :] <= idx[:, None], s, NEG_INF)
+            m = s.max(axis=1, keepdims=True)
+            ex = np.exp(s - m)
+            tot = ex.sum(axis=1, keepdims=True)
+            out[b, idx, h] = (ex / tot) @ vals
+            lse[b, h, idx] = (m + np.log(tot))[:, 0]
+    return out, lse
+
+
+def paged_write(k, v, prompt_len, page_table, page_size, n_pages):
+    """The page pools an encoder prefill leaves behind: row i of request b goes to
+    pool[page_table[b, i // page_size], i % page_size] for i < prompt_len[b]
+    (the inverse of ``paged_to_contiguous``).  Untouched pool rows stay zero.
+
+    k, v: [B, P, Hkv, d].  Returns pool_k, pool_v [n_pages, page_size, Hkv, d].
+    """
+    B, P, hkv, d = k.shape
+    pool_k = np.zeros((n_pages, page_size, hkv, d), dtype=np.float64)
+    pool_v = np.zeros_like(pool_k)
+    for b in range(B):
+        for i in range(int(min(max(int(prompt_len[b]), 0), P))):
+            pg = int(page_table[b, i // page_size])
+            pool_k[pg, i % page_size] = k[b, i]
+            pool_v[pg, i % page_size] = v[b, i]
+    return pool_k, pool_v
+
+
 # --------------------------------------------------------------------------
 # a2: lm-head -> log-softmax -> entropy
 # --------------------------------------------------------------------------

@@ -123,6 +123,11 @@ size_t slot_read_ws(const dg_dims* d, int rows) {
          dgi::lmhead_ws_bytes(rows, d->V);
 }
 
+bool prefill_dims_ok(const dg_dims* d) {
+  if (!d || d->B < 1 || d->P_max < 1 || d->Hq < 1 || d->Hkv < 1 || d->Hq % d->Hkv) return false;
+  return d->d_head == 512 && 128 % (d->Hq / d->Hkv) == 0;
+}
+
 bool attn_dims_ok(const dg_dims* d) {
   if (!d || d->B < 1 || d->C < 1 || d->Hq < 1 || d->Hkv < 1 || d->P_max < 0 || d->W < 0)
     return false;
@@ -229,6 +234,9 @@ size_t dg_workspace_bytes(const dg_dims* d, int which, int rows) {
     case DG_WS_PROBS_EMBED:
       if (!dims_lm(d) || rows < 1) return 0;
       return dgi::probs_embed_ws_bytes(rows, d->V, d->d_model);
+    case DG_WS_PREFILL:
+      if (!prefill_dims_ok(d)) return 0;
+      return dgi::attn_tc_ws_bytes(d->B, d->P_max, 0, d->Hq, d->Hkv, d->P_max);
     default:
       return 0;
   }
@@ -427,6 +435,48 @@ int dg_slot_read_wide(const dg_dims* d, const uint16_t* h, int M, const uint16_t
   return slot_read_impl(d, h, M, w, e, inv_t, slot_row, slot_req, label_ids, n_labels, S, L,
                         seed, step, samples, gate, q_avg, h_slot, chosen, lp_draws, resampled,
                         n_reads, noise_tok_out, workspace, workspace_bytes, stream);
+}
+
+int dg_prefill_attn(const dg_dims* d, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                    const int32_t* prompt_len, uint16_t* out, float* lse,
+                    const int32_t* page_table, int pages_per_req, int n_pages, int page_size,
+                    uint16_t* pool_k, uint16_t* pool_v, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  if (!d) return DG_ERR_ARG;
+  if (!prefill_dims_ok(d)) return DG_ERR_SHAPE;
+  if (!q || !k || !v || !prompt_len || !out || !lse) return DG_ERR_ARG;
+  for (const void* p : {(const void*)q, (const void*)k, (const void*)v, (const void*)out})
+    if (!aligned(p, 16)) return DG_ERR_ARG;
+  if (page_table) {
+    if (!pool_k || !pool_v || !aligned(pool_k, 16) || !aligned(pool_v, 16)) return DG_ERR_ARG;
+    if (page_size < 1 || n_pages < 1 ||
+        (long long)pages_per_req * page_size < (long long)d->P_max)
+      return DG_ERR_SHAPE;
+  }
+  const size_t need = dg_workspace_bytes(d, DG_WS_PREFILL, 0);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return DG_ERR_WORKSPACE;
+  dgi::AttnArgs a{};
+  a.B = d->B;
+  a.C = d->P_max;
+  a.Pmax = 0;
+  a.Hq = d->Hq;
+  a.Hkv = d->Hkv;
+  a.d = d->d_head;
+  a.W = d->P_max;
+  a.q = q;
+  a.kc = k;
+  a.vc = v;
+  a.prompt_len = prompt_len;
+  a.out = out;
+  a.lse = lse;
+  a.causal = 1;
+  a.seq_len = prompt_len;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t err = dgi::attn_decode_tc(a, workspace, st);
+  if (err == cudaSuccess && page_table)
+    err = dgi::kv_page_write(k, v, d->B, d->P_max, d->Hkv, d->d_head, prompt_len, page_table,
+                             pages_per_req, n_pages, page_size, pool_k, pool_v, st);
+  return launch_result(err);
 }
 
 int dg_ask_if_select(const int32_t* chosen1, int S1, const int32_t* cond_slot,

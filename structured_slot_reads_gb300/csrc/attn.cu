@@ -88,6 +88,7 @@ struct Args {
   float* ws_o;   // [splits][B][C][Hq][d]
   float* ws_ml;  // [splits][B][Hq][C][2]
   int* status;
+  const int32_t* seq_len;  // combine: rows at or past seq_len[b] are skipped (null: none)
 };
 
 template <int D>
@@ -413,6 +414,7 @@ __global__ void attn_combine_kernel(Args a) {
   const int head = (int)(row % a.Hq);
   const int pos = (int)((row / a.Hq) % a.C);
   const int b = (int)(row / ((long long)a.Hq * a.C));
+  if (a.seq_len && pos >= a.seq_len[b]) return;
   const long long split_o = (long long)a.B * a.C * a.Hq * D;
   auto ml_of = [&](int s) {
     return a.ws_ml + (((long long)s * a.B + b) * a.Hq + head) * a.C * 2 + pos * 2;
@@ -521,8 +523,9 @@ cudaError_t attn_decode(const AttnArgs& a, void* ws, cudaStream_t st) {
 }
 
 cudaError_t attn_combine(int B, int C, int Hq, int d, int splits, float* ws_o, float* ws_ml,
-                         uint16_t* out, float* lse, cudaStream_t st) {
+                         uint16_t* out, float* lse, cudaStream_t st, const int32_t* seq_len) {
   Args a{};
+  a.seq_len = seq_len;
   a.B = B;
   a.C = C;
   a.Hq = Hq;

@@ -62,6 +62,8 @@ static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 struct TcArgs {
   int B, C, Pmax, Hq, Hkv, W, G, npos, q_blocks, splits;
+  int causal;              // encoder prefill: rows attend to keys j <= i of their own sequence
+  const int32_t* seq_len;  // causal: valid rows (and keys) per request
   const int32_t* page_table;
   int pages_per_req, n_pages, page_size;
   const int32_t* prompt_len;
@@ -85,17 +87,26 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // Key-tile geometry of one CTA (shared by every role).
 struct Tiles {
-  int P, p0, npos, clo, chi, nbp, t_begin, t_end;
+  int P, p0, npos, clo, chi, nbp, t_begin, t_end, len;
   __device__ int key0(int t) const { return t < nbp ? t * BN : clo + (t - nbp) * BN; }
 };
 
 __device__ __forceinline__ Tiles tiles_of(const TcArgs& a, int b, int qb, int split) {
   Tiles T;
-  T.P = min(max(a.prompt_len[b], 0), a.Pmax);
   T.p0 = qb * a.npos;
   T.npos = min(a.npos, a.C - T.p0);
-  T.clo = max(0, T.p0 - a.W);
-  T.chi = min(a.C, T.p0 + T.npos - 1 + a.W + 1);
+  if (a.causal) {
+    // keys 0 .. (last row of the block), within the request's length
+    T.len = min(max(a.seq_len[b], 0), a.C);
+    T.P = 0;
+    T.clo = 0;
+    T.chi = T.p0 < T.len ? min(T.len, T.p0 + T.npos) : 0;  // no rows of this block: no keys
+  } else {
+    T.len = a.C;
+    T.P = min(max(a.prompt_len[b], 0), a.Pmax);
+    T.clo = max(0, T.p0 - a.W);
+    T.chi = min(a.C, T.p0 + T.npos - 1 + a.W + 1);
+  }
   T.nbp = (T.P + BN - 1) / BN;
   const int nb = T.nbp + (T.chi - T.clo + BN - 1) / BN;
   T.t_begin = (int)((long long)split * nb / a.splits);
@@ -140,7 +151,7 @@ __device__ __forceinline__ void softmax_and_store(const TcArgs& a, const Tiles& 
   const int r = quarter * 32 + lane;
   const int lp = r / a.G;
   const int pos = T.p0 + lp;
-  const bool row_ok = lp < T.npos;
+  const bool row_ok = lp < T.npos && pos < T.len;
   const int head = g * a.G + r % a.G;
   const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
   const float sl2 = LOG2E * rsqrtf((float)HD);
@@ -165,6 +176,9 @@ __device__ __forceinline__ void softmax_and_store(const TcArgs& a, const Tiles& 
         }
         if (bad && r == 0 && half == 0) atomicOr(a.status, 2 /* DG_DEV_BAD_PAGE */);
       }
+    } else if (a.causal) {
+      lo = -key0;
+      hi = min(T.chi, pos + 1) - key0;
     } else {
       lo = max(T.clo, pos - a.W) - key0;
       hi = min(T.chi, pos + a.W + 1) - key0;
@@ -332,7 +346,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   bid /= a.splits;
   const int dh = bid & 1;
   bid >>= 1;
-  const int qb = bid % a.q_blocks;
+  // causal prefill: the last query blocks see the most keys, so they go first
+  const int qb = a.causal ? a.q_blocks - 1 - bid % a.q_blocks : bid % a.q_blocks;
   bid /= a.q_blocks;
   const int g = bid % a.Hkv;
   const int b = bid / a.Hkv;
@@ -583,6 +598,8 @@ cudaError_t attn_decode_tc(const AttnArgs& x, void* ws, cudaStream_t st) {
   a.npos = BM / a.G;
   a.q_blocks = (x.C + a.npos - 1) / a.npos;
   a.splits = tc_splits(x.B, x.C, x.Hq, x.Hkv, x.Pmax, a.W);
+  a.causal = x.causal;
+  a.seq_len = x.seq_len;
   a.page_table = x.page_table;
   a.pages_per_req = x.pages_per_req;
   a.n_pages = x.n_pages;
@@ -631,7 +648,51 @@ cudaError_t attn_decode_tc(const AttnArgs& x, void* ws, cudaStream_t st) {
   attn_tc_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(tq, tke, tve, tkc, tvc, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || a.splits == 1) return e;
-  return attn_combine(x.B, x.C, x.Hq, HD, a.splits, a.ws_o, a.ws_ml, x.out, x.lse, st);
+  return attn_combine(x.B, x.C, x.Hq, HD, a.splits, a.ws_o, a.ws_ml, x.out, x.lse, st,
+                      x.causal ? x.seq_len : nullptr);
+}
+
+// Paged KV write of an encoder prefill: one warp per (request, key row, KV head)
+// copies d bf16 values of K and of V with 16-byte loads and stores.
+namespace {
+__global__ void kv_page_write_kernel(const uint4* k, const uint4* v, int B, int P, int Hkv,
+                                     int n16, const int32_t* seq_len, const int32_t* page_table,
+                                     int pages_per_req, int n_pages, int page_size, uint4* pool_k,
+                                     uint4* pool_v, int* status) {
+  const long long item = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const long long n_items = (long long)B * P * Hkv;
+  if (item >= n_items) return;
+  const int h = (int)(item % Hkv);
+  const int p = (int)((item / Hkv) % P);
+  const int b = (int)(item / ((long long)Hkv * P));
+  if (p >= min(max(seq_len[b], 0), P)) return;
+  const int pg = page_table[(long long)b * pages_per_req + p / page_size];
+  if (pg < 0 || pg >= n_pages) {
+    if (lane == 0) atomicOr(status, 2 /* DG_DEV_BAD_PAGE */);
+    return;
+  }
+  const long long src = item * n16;
+  const long long dst = (((long long)pg * page_size + p % page_size) * Hkv + h) * n16;
+  for (int i = lane; i < n16; i += 32) {
+    pool_k[dst + i] = k[src + i];
+    pool_v[dst + i] = v[src + i];
+  }
+}
+}  // namespace
+
+cudaError_t kv_page_write(const uint16_t* k, const uint16_t* v, int B, int P, int Hkv, int d,
+                          const int32_t* seq_len, const int32_t* page_table, int pages_per_req,
+                          int n_pages, int page_size, uint16_t* pool_k, uint16_t* pool_v,
+                          cudaStream_t st) {
+  const long long items = (long long)B * P * Hkv;
+  if (items == 0) return cudaSuccess;
+  const int grid = (int)((items + 7) / 8);
+  kv_page_write_kernel<<<grid, 256, 0, st>>>(
+      reinterpret_cast<const uint4*>(k), reinterpret_cast<const uint4*>(v), B, P, Hkv, d / 8,
+      seq_len, page_table, pages_per_req, n_pages, page_size, reinterpret_cast<uint4*>(pool_k),
+      reinterpret_cast<uint4*>(pool_v), status_ptr());
+  return cudaGetLastError();
 }
 
 }  // namespace dgi

@@ -61,16 +61,26 @@ struct AttnArgs {
   const int32_t* prompt_len;
   uint16_t* out;
   float* lse;
+  int causal = 0;                     // encoder prefill (d = 512 tensor-core kernel only)
+  const int32_t* seq_len = nullptr;   // causal: rows per request (q/k/v are [B, C, H, d])
 };
 size_t attn_ws_bytes(int B, int C, int Pmax, int Hq, int Hkv, int d, int W);
 cudaError_t attn_decode(const AttnArgs& a, void* ws, cudaStream_t st);
-// Merge split-KV partials ([splits][B][C][Hq][d] fp32 O, [splits][B][Hq][C] (m, l)).
+// Merge split-KV partials ([splits][B][C][Hq][d] fp32 O, [splits][B][Hq][C] (m, l));
+// with seq_len, rows at or past seq_len[b] are left untouched.
 cudaError_t attn_combine(int B, int C, int Hq, int d, int splits, float* ws_o, float* ws_ml,
-                         uint16_t* out, float* lse, cudaStream_t st);
+                         uint16_t* out, float* lse, cudaStream_t st,
+                         const int32_t* seq_len = nullptr);
 // d = 512 on tcgen05 (attn_tc.cu): 128 query rows x 256 output columns per CTA.
 bool attn_tc_supported(const AttnArgs& a);
 size_t attn_tc_ws_bytes(int B, int C, int Pmax, int Hq, int Hkv, int W);
 cudaError_t attn_decode_tc(const AttnArgs& a, void* ws, cudaStream_t st);
+// Copy the first seq_len[b] rows of k, v [B, P, Hkv, d] into the page pools
+// [n_pages, page_size, Hkv, d] through page_table [B, pages_per_req].
+cudaError_t kv_page_write(const uint16_t* k, const uint16_t* v, int B, int P, int Hkv, int d,
+                          const int32_t* seq_len, const int32_t* page_table, int pages_per_req,
+                          int n_pages, int page_size, uint16_t* pool_k, uint16_t* pool_v,
+                          cudaStream_t st);
 
 // ---- small kernels (slot.cu) -----------------------------------------------
 cudaError_t philox_fill(uint64_t seed, const uint32_t* ctr4, int n, uint32_t* out4,

@@ -21,7 +21,7 @@ DG_ERR_WORKSPACE = -6
 DG_DEV_TIMEOUT, DG_DEV_BAD_PAGE, DG_DEV_BAD_LABEL, DG_DEV_BAD_INDEX = 1, 2, 4, 8
 DG_DEV_RANGE = 16
 DG_WS_ATTN, DG_WS_LMHEAD, DG_WS_SLOT_READ, DG_WS_SELFCOND = 1, 2, 3, 4
-DG_WS_HEADS, DG_WS_PROBS_EMBED = 5, 6
+DG_WS_HEADS, DG_WS_PROBS_EMBED, DG_WS_PREFILL = 5, 6, 7
 DG_MAX_LABELS = MAX_LABELS = 26
 DG_MAX_WIDE_LABELS = 256
 DG_NOALLOC_MAX_ROWS = 512
@@ -61,6 +61,7 @@ _SIGS = {
                      P],
     "dg_slot_read_wide": [DP, P, I, P, P, P, P, P, P, P, I, I, U64, I, I, F, P, P, P, P, P, P, P,
                           P, Z, P],
+    "dg_prefill_attn": [DP, P, P, P, P, P, P, P, I, I, I, P, P, P, Z, P],
     "dg_commit": [DP, P, P, P, P, P, P, P, P, P, P],
     "dg_selfcond_embed": [DP, P, I, P, P, P, P, P, P, Z, P],
     "dg_denoise_heads": [DP, P, I, P, I, P, P, P, P, P, P, P, P, P, P, Z, P, Z, P],
@@ -182,6 +183,14 @@ def dg_slot_read_wide(dims, h, M, w, e, inv_t, slot_row, slot_req, label_ids, n_
                                    seed, step, samples, gate, _p(q_avg), _p(h_slot), _p(chosen),
                                    _p(lp_draws), _p(resampled), _p(n_reads), _p(noise_tok_out),
                                    _p(workspace), _nbytes(workspace), _s(stream))
+
+
+def dg_prefill_attn(dims, q, k, v, prompt_len, out, lse, page_table, pages_per_req, n_pages,
+                    page_size, pool_k, pool_v, workspace, stream=None):
+    return lib().dg_prefill_attn(ctypes.byref(dims), _p(q), _p(k), _p(v), _p(prompt_len), _p(out),
+                                 _p(lse), _p(page_table), pages_per_req, n_pages, page_size,
+                                 _p(pool_k), _p(pool_v), _p(workspace), _nbytes(workspace),
+                                 _s(stream))
 
 
 def dg_commit(dims, entropy, argmax, cand, gamma, committed_state, token_state, commit, tokens,

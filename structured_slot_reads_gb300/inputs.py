@@ -23,6 +23,7 @@ from .configs import StepShape
 
 S_H, S_W, S_E, S_INVT, S_Q, S_KC, S_VC, S_KENC, S_VENC = 1, 2, 3, 4, 5, 6, 7, 8, 9
 S_LABELS, S_TEMPLATE, S_PROMPT, S_PAGES, S_SLOTS, S_GROUPS = 10, 11, 12, 13, 14, 15
+S_PQ, S_PK, S_PV = 16, 17, 18
 
 MAX_LABELS = 26
 
@@ -97,6 +98,13 @@ def attention_inputs(shape: StepShape, seed, prompt_len=None):
         venc=normal_bf16((B, pmax, hkv, d), 1.0, seed, S_VENC),
         prompt_len=np.asarray(prompt_len, dtype=np.int32),
     )
+
+
+def prefill_inputs(B, P, Hq, Hkv, d, seed):
+    """Prompt-side Q [B, P, Hq, d] and K, V [B, P, Hkv, d] of an encoder prefill, N(0,1) bf16."""
+    return dict(q=normal_bf16((B, P, Hq, d), 1.0, seed, S_PQ),
+                k=normal_bf16((B, P, Hkv, d), 1.0, seed, S_PK),
+                v=normal_bf16((B, P, Hkv, d), 1.0, seed, S_PV))
 
 
 def paged_layout(kenc, venc, prompt_len, page_size, seed, spare_pages=7):

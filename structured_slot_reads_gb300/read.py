@@ -213,3 +213,36 @@ class ReadStep:
                                            self.ws_read, stream), "dg_slot_read_wide")
         attn_kernels = 1 if dg.dg_workspace_bytes(d, dg.DG_WS_ATTN, 0) <= 256 else 2
         return attn_kernels + 4
+
+
+class Prefill:
+    """Encoder-mode prefill of a batch of prompts: causal attention of every prompt over
+    itself, its K/V written into a shared page pool (dg_prefill_attn), the layout the
+    decoder-mode read takes."""
+
+    def __init__(self, B, P, Hq, Hkv, d_head, page_size=16, device="cuda", seed=0):
+        bf, f32, i32, u8 = torch.bfloat16, torch.float32, torch.int32, torch.uint8
+        self.B, self.P, self.Hq, self.Hkv, self.d = B, P, Hq, Hkv, d_head
+        self.dims = dg.make_dims(B=B, P_max=P, Hq=Hq, Hkv=Hkv, d_head=d_head)
+        self.q = torch.empty((B, P, Hq, d_head), dtype=bf, device=device)
+        self.k = torch.empty((B, P, Hkv, d_head), dtype=bf, device=device)
+        self.v = torch.empty_like(self.k)
+        self.prompt_len = torch.full((B,), P, dtype=i32, device=device)
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty((B, Hq, P), dtype=f32, device=device)
+        self.page_size = page_size
+        table, self.n_pages = inputs.page_table([P] * B, page_size, seed)
+        self.page_table = _dev(table, i32, device)
+        self.pool_k = torch.empty((self.n_pages, page_size, Hkv, d_head), dtype=bf, device=device)
+        self.pool_v = torch.empty_like(self.pool_k)
+        self.ws = torch.empty(max(dg.dg_workspace_bytes(self.dims, dg.DG_WS_PREFILL, 0), 256),
+                              dtype=u8, device=device)
+
+    def run(self, step_idx=0, stream=None):
+        """Enqueue the prefill; returns the number of library kernels."""
+        dg._check(dg.dg_prefill_attn(self.dims, self.q, self.k, self.v, self.prompt_len, self.out,
+                                     self.lse, self.page_table, self.page_table.shape[1],
+                                     self.n_pages, self.page_size, self.pool_k, self.pool_v,
+                                     self.ws, stream), "dg_prefill_attn")
+        splits = 1 if dg.dg_workspace_bytes(self.dims, dg.DG_WS_PREFILL, 0) <= 256 else 2
+        return splits + 1

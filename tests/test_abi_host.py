@@ -193,3 +193,15 @@ def test_wide_read_rejects_tables_wider_than_256(lib):
     rc = dg.dg_slot_read_wide(d, 16, 4, 16, 16, 16, 16, 16, 16, 16, 1, 0, 0, 0, 4, 0.1, 16, 16,
                               16, 16, 16, 16, None, None, stream=0)
     assert rc == dg.DG_ERR_TOO_MANY_LABELS
+
+
+def test_prefill_validates_shapes(lib):
+    ok = dg.make_dims(B=1, P_max=64, Hq=8, Hkv=2, d_head=512)
+    assert dg.dg_workspace_bytes(ok, dg.DG_WS_PREFILL, 0) > 0
+    bad_d = dg.make_dims(B=1, P_max=64, Hq=8, Hkv=2, d_head=64)
+    assert dg.dg_prefill_attn(bad_d, 16, 16, 16, 16, 16, 16, None, 0, 0, 0, None, None, None,
+                              stream=0) == dg.DG_ERR_SHAPE
+    assert dg.dg_prefill_attn(ok, None, 16, 16, 16, 16, 16, None, 0, 0, 0, None, None, None,
+                              stream=0) == dg.DG_ERR_ARG
+    assert dg.dg_prefill_attn(ok, 16, 16, 16, 16, 16, 16, None, 0, 0, 0, None, None, None,
+                              stream=0) == dg.DG_ERR_WORKSPACE

@@ -18,7 +18,7 @@ def test_every_workload_resolves_to_a_shape():
     b = _bench()
     for name, (kind, _, kw) in b.WORKLOADS.items():
         k, shape = b.workload_shape(name)
-        assert k == kind in ("step", "read", "two_stage")
+        assert k == kind in ("step", "read", "two_stage", "prefill")
         for f, v in kw.items():
             assert getattr(shape, f) == v
     assert b.workload_shape("sweep_read_b64")[1].B == 64
@@ -40,3 +40,11 @@ def test_attention_work_counts_visible_keys():
     assert b.attn_flops(shape) == b.attn_flops(shape, [shape.P] * 3)
     kv = (plen.sum() + 3 * C) * shape.Hkv * shape.d_head * 4
     assert b.attn_bytes(shape, plen) == kv + 2 * 3 * C * shape.Hq * shape.d_head * 2
+
+
+def test_prefill_work_counts_causal_pairs():
+    from structured_slot_reads_gb300 import configs
+    b = _bench()
+    shape = configs.scaled(configs.TINY, B=2, P=9, Hq=4, d_head=64)
+    pairs = sum(1 for i in range(9) for j in range(9) if j <= i)
+    assert b.prefill_flops(shape) == 4.0 * 2 * 4 * 64 * pairs

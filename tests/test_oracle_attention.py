@@ -105,3 +105,67 @@ def test_paged_equals_contiguous():
         for j in range(plen[b]):
             np.testing.assert_array_equal(kenc[b, j], pool_k[table[b, j // ps], j % ps])
             np.testing.assert_array_equal(venc[b, j], pool_v[table[b, j // ps], j % ps])
+
+
+# ---- encoder-mode prefill -----------------------------------------------------
+def _prefill_inputs(B=2, P=11, lens=(11, 6), hq=4, hkv=2, d=8, seed=3):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((B, P, hq, d)), rng.standard_normal((B, P, hkv, d)),
+            rng.standard_normal((B, P, hkv, d)), np.array(lens))
+
+
+def test_prefill_matches_torch_causal_sdpa():
+    """Library reference: torch SDPA in float64 with is_causal=True, per request prefix."""
+    from oracle import prefill_attn
+    q, k, v, lens = _prefill_inputs()
+    out, lse = prefill_attn(q, k, v, lens)
+    hq, hkv, d = q.shape[2], k.shape[2], q.shape[3]
+    for b, n in enumerate(lens):
+        qb = torch.tensor(q[b, :n]).permute(1, 0, 2)
+        kb = torch.tensor(k[b, :n]).repeat_interleave(hq // hkv, dim=1).permute(1, 0, 2)
+        vb = torch.tensor(v[b, :n]).repeat_interleave(hq // hkv, dim=1).permute(1, 0, 2)
+        ref = F.scaled_dot_product_attention(qb, kb, vb, is_causal=True).permute(1, 0, 2)
+        assert np.allclose(out[b, :n], ref.numpy(), atol=1e-12)
+        s = (qb @ kb.transpose(1, 2)) / np.sqrt(d)
+        s = s.masked_fill(torch.triu(torch.ones(n, n, dtype=torch.bool), 1), float("-inf"))
+        assert np.allclose(lse[b, :, :n], torch.logsumexp(s, -1).numpy(), atol=1e-12)
+        assert np.all(out[b, n:] == 0)
+
+
+def test_prefill_first_row_is_its_own_value_and_rows_subset_agrees():
+    from oracle import prefill_attn
+    q, k, v, lens = _prefill_inputs()
+    out, _ = prefill_attn(q, k, v, lens)
+    for h in range(q.shape[2]):
+        assert np.allclose(out[:, 0, h], v[:, 0, h // 2], atol=1e-12)  # only key 0 is visible
+    part, part_lse = prefill_attn(q, k, v, lens, rows=[0, 5, 10])
+    full, full_lse = prefill_attn(q, k, v, lens)
+    for r in (0, 5, 10):
+        assert np.allclose(part[:, r][r < lens], full[:, r][r < lens], atol=1e-12)
+
+
+def test_prefill_gqa_head_mapping():
+    """Making KV head 1 differ changes exactly the query heads 2 and 3 (group of 2)."""
+    from oracle import prefill_attn
+    q, k, v, lens = _prefill_inputs()
+    out0, _ = prefill_attn(q, k, v, lens)
+    v2 = v.copy()
+    v2[:, :, 1] += 1.0
+    out1, _ = prefill_attn(q, k, v2, lens)
+    assert np.allclose(out0[:, :, :2], out1[:, :, :2])
+    assert np.allclose(out1[:, :, 2:][:, :6], out0[:, :, 2:][:, :6] + 1.0)
+
+
+def test_paged_write_inverts_paged_to_contiguous():
+    from oracle import paged_write
+    q, k, v, lens = _prefill_inputs()
+    ps, B = 4, k.shape[0]
+    pages = (k.shape[1] + ps - 1) // ps
+    perm = np.random.default_rng(0).permutation(B * pages + 3)
+    table = perm[:B * pages].reshape(B, pages)
+    pk, pv = paged_write(k, v, lens, table, ps, B * pages + 3)
+    ke, ve = paged_to_contiguous(pk, pv, table, lens, ps)
+    for b, n in enumerate(lens):
+        assert np.array_equal(ke[b, :n], k[b, :n]) and np.array_equal(ve[b, :n], v[b, :n])
+    assert np.count_nonzero(pk.reshape(pk.shape[0], -1).any(axis=1)) == sum(
+        (n + ps - 1) // ps for n in lens)
