@@ -36,6 +36,10 @@ WORKLOADS = {
     "mixed_batched_reads": ("two_stage", "MIXED_BATCH", {}),
     "long_context_read": ("read", "LONG_CONTEXT", {}),
     "wide_read_77": ("read", "SINGLE_READ", dict(slots=[(61, 77)])),
+    "lmhead_bf16_m256": ("lmhead", "FULL_CANVAS", {}),
+    "lmhead_fp8_m256": ("lmhead_fp8", "FULL_CANVAS", {}),
+    "lmhead_bf16_m12": ("lmhead", "FULL_CANVAS", dict(C=12)),
+    "lmhead_fp8_m12": ("lmhead_fp8", "FULL_CANVAS", dict(C=12)),
     "prefill_8192": ("prefill", "LONG_CONTEXT", dict(B=1, P=8192)),
     "prefill_long": ("prefill", "LONG_CONTEXT", {}),
     "sweep_read_b1": ("read", "LONG_CONTEXT", dict(B=1, P=8192)),
@@ -418,6 +422,14 @@ def build_runner(kind, shape, device):
     from structured_slot_reads_gb300.read import ReadStep, TwoStageRead
     if kind == "step":
         return build_step(shape, device)
+    if kind in ("lmhead", "lmhead_fp8"):
+        from structured_slot_reads_gb300.read import LmHead
+        w = inputs.device_normal_bf16((shape.V, shape.D), shape.D ** -0.5, 1, device)
+        st = LmHead(shape, w, shape.B * shape.C, fp8=kind == "lmhead_fp8", device=device)
+        st.h.copy_(inputs.device_normal_bf16(st.h.shape, 1.0, 3, device))
+        st.inv_t.copy_(1.0 / inputs.device_uniform(st.inv_t.shape, 0.5, 2.0, 4, device))
+        torch.cuda.synchronize()
+        return st
     if kind == "prefill":
         from structured_slot_reads_gb300.read import Prefill
         st = Prefill(shape.B, shape.P, shape.Hq, shape.Hkv, shape.d_head, shape.page_size,
@@ -494,6 +506,10 @@ def workload_arm(args, rank, world, local):
     elif kind == "prefill":
         run = lambda i: st.run(step_idx=i)              # noqa: E731
         calls = ["dg_prefill_attn"]
+    elif kind in ("lmhead", "lmhead_fp8"):
+        run = lambda i: st.run(step_idx=i)              # noqa: E731
+        calls = ["dg_lmhead_logsoftmax_entropy", "dg_quantize_rows_e4m3",
+                 "dg_lmhead_logsoftmax_entropy_fp8"]
     else:
         run = lambda i: st.run(step_idx=i)              # noqa: E731
         calls = ["dg_attn_decode", "dg_slot_read", "dg_slot_read_wide", "dg_slot_noise",
@@ -511,6 +527,13 @@ def workload_arm(args, rank, world, local):
     work["dg_attn_decode"] = (attn_bytes(shape, plen), attn_flops(shape, plen))
     if kind == "prefill":
         work["dg_prefill_attn"] = (prefill_bytes(shape), prefill_flops(shape))
+    if kind in ("lmhead", "lmhead_fp8"):
+        Mr = shape.B * shape.C
+        esz = 1 if kind == "lmhead_fp8" else 2
+        lm = (V * D * esz + Mr * D * esz + V * 4 * (esz == 1) + Mr * 16, 2.0 * Mr * V * D)
+        work["dg_lmhead_logsoftmax_entropy"] = lm
+        work["dg_lmhead_logsoftmax_entropy_fp8"] = lm
+        work["dg_quantize_rows_e4m3"] = (Mr * D * 3 + Mr * 4, 0.0)
     if kind == "read":
         work["dg_slot_read"] = (Wb + st.S * R * D * 4, 2.0 * st.S * R * V * D)
         work["dg_slot_read_wide"] = work["dg_slot_read"]
@@ -550,6 +573,8 @@ def workload_arm(args, rank, world, local):
         unit, value = UNIT, steps_per_s * shape.B
     elif kind == "prefill":
         unit, value = "prompt tokens/s", steps_per_s * shape.B * shape.P
+    elif kind in ("lmhead", "lmhead_fp8"):
+        unit, value = "lm-head passes/s", steps_per_s
     else:
         unit, value = "slot decisions/s", steps_per_s * decisions
     return {

@@ -189,6 +189,31 @@ int dg_prefill_attn(const dg_dims* dims, const uint16_t* q, const uint16_t* k, c
                     uint16_t* pool_k, uint16_t* pool_v, void* workspace, size_t workspace_bytes,
                     void* stream);
 
+/* ---- next: the lm-head pass on 8-bit operands ---------------------------
+ * tau-home.com, "DiffusionGemma like Jev" ("Running NVFP4 locally with a
+ * Jev-compatible System One endpoint") and 24-ai.news, "DiffusionGemma
+ * integrated into vLLM" ("Measured performance": an FP8 checkpoint with
+ * dynamic activation scaling) run the model on 8- and 4-bit weights.  Here W
+ * and the hidden rows are e4m3 with one fp32 scale per row (the rows' scales
+ * computed per call), so the W stream of the HBM-bound pass halves.  dg_quantize_rows_e4m3: scale[r] = max_k |x[r, k]| / 448 (1 for a
+ * zero row), q[r, k] = e4m3(x[r, k] / scale[r]) (fp32 division, round to
+ * nearest even, saturating).  x [rows, cols] bf16;  q [rows, cols] uint8;
+ * scale [rows] fp32. */
+int dg_quantize_rows_e4m3(const uint16_t* x, int rows, int cols, uint8_t* q, float* scale,
+                          void* stream);
+
+/* dg_lmhead_logsoftmax_entropy on quantised operands: the row statistics of
+ * softmax(z_i / T_i) with z_iv = (sum_k h8[i, k] w8[v, k]) * h_scale[i] * w_scale[v]
+ * (e4m3 products accumulated in fp32 by the tensor cores).  Outputs, workspace
+ * (DG_WS_LMHEAD) and errors as dg_lmhead_logsoftmax_entropy; d_model must be a
+ * multiple of 16; h8, w8 and w_scale 16-byte aligned.
+ *   h8 [M, d_model], w8 [V, d_model] uint8 (e4m3);  h_scale [M], w_scale [V] fp32 */
+int dg_lmhead_logsoftmax_entropy_fp8(const dg_dims* dims, const uint8_t* h8, const float* h_scale,
+                                     int M, const uint8_t* w8, const float* w_scale,
+                                     const float* inv_t, float* lse, float* entropy, float* maxz,
+                                     int32_t* argmax, void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
 /* ---- next: one wide read in place of the two-stage path -----------------
  * sotaaz.com, "The server accepts at most 26 alternatives per question": the
  * example server letters a question's alternatives A-Z, so 77 intents are read

@@ -99,6 +99,20 @@ bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint6
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, const uint64_t (&dims)[3],
                        const uint64_t (&stride_bytes)[2], const uint32_t (&box)[3]) {
   EncodeTiledFn fn = encode_fn();
@@ -477,6 +491,31 @@ int dg_prefill_attn(const dg_dims* d, const uint16_t* q, const uint16_t* k, cons
     err = dgi::kv_page_write(k, v, d->B, d->P_max, d->Hkv, d->d_head, prompt_len, page_table,
                              pages_per_req, n_pages, page_size, pool_k, pool_v, st);
   return launch_result(err);
+}
+
+int dg_quantize_rows_e4m3(const uint16_t* x, int rows, int cols, uint8_t* q, float* scale,
+                          void* stream) {
+  if (rows < 0 || cols < 1) return DG_ERR_ARG;
+  if (rows > 0 && (!x || !q || !scale)) return DG_ERR_ARG;
+  return launch_result(
+      dgi::quantize_rows_e4m3(x, rows, cols, q, scale, static_cast<cudaStream_t>(stream)));
+}
+
+int dg_lmhead_logsoftmax_entropy_fp8(const dg_dims* d, const uint8_t* h8, const float* h_scale,
+                                     int M, const uint8_t* w8, const float* w_scale,
+                                     const float* inv_t, float* lse, float* entropy, float* maxz,
+                                     int32_t* argmax, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+  if (!d || M < 1) return DG_ERR_ARG;
+  if (!dims_lm(d) || d->d_model % 16) return DG_ERR_SHAPE;
+  if (!h8 || !h_scale || !w8 || !w_scale || !inv_t || !lse || !entropy || !maxz || !argmax)
+    return DG_ERR_ARG;
+  if (!aligned(h8, 16) || !aligned(w8, 16) || !aligned(w_scale, 16)) return DG_ERR_ARG;
+  const size_t need = dg_workspace_bytes(d, DG_WS_LMHEAD, M);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DG_ERR_WORKSPACE;
+  return launch_result(dgi::lmhead_stats_fp8(h8, h_scale, M, w8, w_scale, d->V, d->d_model, inv_t,
+                                             dgi::RowStats{lse, entropy, maxz, argmax}, workspace,
+                                             static_cast<cudaStream_t>(stream)));
 }
 
 int dg_ask_if_select(const int32_t* chosen1, int S1, const int32_t* cond_slot,

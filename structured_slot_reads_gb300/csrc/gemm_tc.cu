@@ -40,6 +40,7 @@ constexpr int EPI_STATS = 0;
 constexpr int EPI_PROBS = 1;
 constexpr int EPI_ACCUM = 2;
 constexpr int EPI_ACCUM_MN = 3;  // as EPI_ACCUM with B given N-contiguous ([K, N] row-major)
+constexpr int EPI_STATS8 = 4;    // as EPI_STATS with e4m3 operands and per-row scales
 constexpr int RING_BUDGET = 232448 - 1024 - 512;  // operand rings (227 KB - alignment - barriers)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
@@ -58,6 +59,8 @@ struct GemmParams {
   int kb_per_split;  // ACCUM: k-blocks per range
   const float* inv_t;
   const float* lse;
+  const float* row_scale;  // STATS8: scale of each A row
+  const float* col_scale;  // STATS8: scale of each B row (vocabulary entry)
   float* part;            // STATS: 5 x [cpg][M]; ACCUM: [k_split][M][N]
   __nv_bfloat16* probs;   // PROBS: [M][ldp]
   long long ldp;
@@ -102,6 +105,11 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
   constexpr int MMA_WARP = CF::EPI_WARPS + 1;
   constexpr bool B_MN = EPI == EPI_ACCUM_MN;
   constexpr bool ACCUM = EPI == EPI_ACCUM || B_MN;
+  constexpr bool F8 = EPI == EPI_STATS8;
+  constexpr bool STATS = EPI == EPI_STATS || F8;
+  // a stage holds 128-byte operand rows: 64 bf16 or 128 e4m3 values of K
+  constexpr int KB = F8 ? 128 : BK;
+  constexpr uint32_t IDESC_F8 = idesc_e4m3_f32(BM, BN);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -145,7 +153,7 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   // ---- work assignment --------------------------------------------------
-  const int total_kb = (p.K + BK - 1) / BK;
+  const int total_kb = (p.K + KB - 1) / KB;
   int gm, t_begin, t_end, kb_begin, kb_end;
   if (ACCUM) {
     const int per_group = p.n_tiles * p.k_split;
@@ -189,7 +197,7 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
           uint8_t* s_b = s_a + CF::A_STAGE;
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt)
-            tma_load_2d_hint(s_a + mt * CF::A_BYTES, &tmA, &full_bar[stage], kb * BK,
+            tma_load_2d_hint(s_a + mt * CF::A_BYTES, &tmA, &full_bar[stage], kb * KB,
                              m_base + mt * BM, pol_a);
           if (B_MN) {
             // B [K, N] with N contiguous: BN/64 boxes of 64 N-columns x 64 K-rows
@@ -198,7 +206,7 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
               tma_load_2d_hint(s_b + g * (BK * 128), &tmB, &full_bar[stage], t * BN + g * 64,
                                kb * BK, pol_b);
           } else {
-            tma_load_2d_hint(s_b, &tmB, &full_bar[stage], kb * BK, t * BN, pol_b);
+            tma_load_2d_hint(s_b, &tmB, &full_bar[stage], kb * KB, t * BN, pol_b);
           }
           issued_mask |= 1u << stage;
           last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
@@ -239,8 +247,13 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
               const uint64_t adesc = sw128_kmajor_desc(a_addr + mt * CF::A_BYTES + kk * 32);
-              tc_mma_f16(d_base + mt * BN, adesc, bdesc, B_MN ? CF::IDESC_BMN : CF::IDESC,
-                         (kb > kb_begin || kk > 0) ? 1u : 0u);
+              // 32 bytes of K per instruction: 16 bf16 (K = 16) or 32 e4m3 (K = 32)
+              if (F8)
+                tc_mma_f8(d_base + mt * BN, adesc, bdesc, IDESC_F8,
+                          (kb > kb_begin || kk > 0) ? 1u : 0u);
+              else
+                tc_mma_f16(d_base + mt * BN, adesc, bdesc, B_MN ? CF::IDESC_BMN : CF::IDESC,
+                           (kb > kb_begin || kk > 0) ? 1u : 0u);
             }
           }
           tc_commit(&empty_bar[stage]);
@@ -266,8 +279,9 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
     const int quarter = warp & 3;
     const int row = m_base + mt * BM + quarter * 32 + lane;
     const bool row_ok = row < p.M;
-    float scale = 0.f, lse2 = 0.f;
+    float scale = 0.f, lse2 = 0.f, rs = 1.f;
     if (!ACCUM && row_ok) scale = __ldg(p.inv_t + row) * LOG2E;
+    if (F8 && row_ok) rs = __ldg(p.row_scale + row);
     if (EPI == EPI_PROBS && row_ok) lse2 = __ldg(p.lse + row) * LOG2E;
     float m_run = -INFINITY, s_run = 0.f, t_run = 0.f, best = -INFINITY;
     int best_idx = 0x7fffffff;
@@ -286,7 +300,25 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
         tmem_ld_wait();
         const int n0 = t * BN + c * 32;
         if (!row_ok) continue;
-        if (EPI == EPI_STATS) {
+        if (F8) {
+          // unscaled e4m3 products -> h.w: times the row's and each column's scale
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            float4 cs = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (n0 + j + 4 <= p.N) {
+              cs = __ldg(reinterpret_cast<const float4*>(p.col_scale + n0 + j));
+            } else {
+              if (n0 + j < p.N) cs.x = __ldg(p.col_scale + n0 + j);
+              if (n0 + j + 1 < p.N) cs.y = __ldg(p.col_scale + n0 + j + 1);
+              if (n0 + j + 2 < p.N) cs.z = __ldg(p.col_scale + n0 + j + 2);
+            }
+            r[j] = __float_as_uint(__uint_as_float(r[j]) * rs * cs.x);
+            r[j + 1] = __float_as_uint(__uint_as_float(r[j + 1]) * rs * cs.y);
+            r[j + 2] = __float_as_uint(__uint_as_float(r[j + 2]) * rs * cs.z);
+            r[j + 3] = __float_as_uint(__uint_as_float(r[j + 3]) * rs * cs.w);
+          }
+        }
+        if (STATS) {
           if (n0 + 32 <= p.N) {
             float cm = -INFINITY;
 #pragma unroll
@@ -386,7 +418,7 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
         acc_phase ^= 1u;
       }
     }
-    if (EPI == EPI_STATS && row_ok) {
+    if (STATS && row_ok) {
       const int gn = blockIdx.x % p.cpg;
       const long long o = (long long)row * p.cpg + gn;
       const long long plane = (long long)p.cpg * p.M;
@@ -532,6 +564,36 @@ cudaError_t run_stats(const uint16_t* h, int M, const uint16_t* w, int V, int D,
   return cudaGetLastError();
 }
 
+// The statistics pass on e4m3 operands: K blocks of 128 values (128-byte rows).
+cudaError_t run_stats_fp8(const uint8_t* h8, const float* h_scale, int M, const uint8_t* w8,
+                          const float* w_scale, int V, int D, const float* inv_t,
+                          dgi::RowStats out, float* part, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  if (!dgi::make_tmap_u8_2d(&ta, h8, D, M, (uint64_t)D, 128, BM)) return cudaErrorInvalidValue;
+  if (!dgi::make_tmap_u8_2d(&tb, w8, D, V, (uint64_t)D, 128, STATS_BN))
+    return cudaErrorInvalidValue;
+  const int mt = stats_mt(M);
+  const int groups = (M + mt * BM - 1) / (mt * BM);
+  GemmParams p{};
+  p.M = M;
+  p.N = V;
+  p.K = D;
+  p.cpg = stats_cpg(M, V);
+  p.n_tiles = (V + STATS_BN - 1) / STATS_BN;
+  p.inv_t = inv_t;
+  p.row_scale = h_scale;
+  p.col_scale = w_scale;
+  p.part = part;
+  p.status = dgi::status_ptr();
+  cudaError_t e =
+      (mt == 1) ? launch_gemm<1, STATS_BN, EPI_STATS8>(ta, tb, p, groups * p.cpg, st)
+                : launch_gemm<2, STATS_BN, EPI_STATS8>(ta, tb, p, groups * p.cpg, st);
+  if (e != cudaSuccess) return e;
+  stats_finalize_kernel<<<(M + 7) / 8, 256, 0, st>>>(part, p.cpg, M, inv_t, out.lse,
+                                                     out.entropy, out.maxz, out.argmax);
+  return cudaGetLastError();
+}
+
 constexpr int ACC_BN = 256;
 
 // Split of the vocabulary (the K of P . E) over CTAs: every split non-empty.
@@ -558,6 +620,12 @@ size_t lmhead_ws_bytes(int M, int V) {
 cudaError_t lmhead_stats(const uint16_t* h, int M, const uint16_t* w, int V, int D,
                          const float* inv_t, RowStats out, void* ws, cudaStream_t st) {
   return run_stats(h, M, w, V, D, inv_t, out, static_cast<float*>(ws), st);
+}
+
+cudaError_t lmhead_stats_fp8(const uint8_t* h8, const float* h_scale, int M, const uint8_t* w8,
+                             const float* w_scale, int V, int D, const float* inv_t, RowStats out,
+                             void* ws, cudaStream_t st) {
+  return run_stats_fp8(h8, h_scale, M, w8, w_scale, V, D, inv_t, out, static_cast<float*>(ws), st);
 }
 
 size_t selfcond_ws_bytes(int M, int V, int D) {

@@ -15,6 +15,9 @@ int num_sms();
 // Returns false on failure.
 bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+// 2-D tensor map of 8-bit elements (e4m3 operands), 128-byte swizzle.
+bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
 // 3-D tensor map (dims innermost first; strides of dims 1 and 2 in bytes), 128-byte swizzle.
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, const uint64_t (&dims)[3],
                        const uint64_t (&stride_bytes)[2], const uint32_t (&box)[3]);
@@ -31,6 +34,14 @@ struct RowStats {
 size_t lmhead_ws_bytes(int M, int V);
 cudaError_t lmhead_stats(const uint16_t* h, int M, const uint16_t* w, int V, int D,
                          const float* inv_t, RowStats out, void* ws, cudaStream_t st);
+// lm-head statistics from e4m3 operands with per-row scales:
+// z[i, v] = (h8_i . w8_v) * h_scale[i] * w_scale[v] / T_i.  Workspace: lmhead_ws_bytes.
+cudaError_t lmhead_stats_fp8(const uint8_t* h8, const float* h_scale, int M, const uint8_t* w8,
+                             const float* w_scale, int V, int D, const float* inv_t, RowStats out,
+                             void* ws, cudaStream_t st);
+// Per-row e4m3 quantisation: scale = amax / 448 (1 for a zero row), q = e4m3(x / scale).
+cudaError_t quantize_rows_e4m3(const uint16_t* x, int rows, int cols, uint8_t* q, float* scale,
+                               cudaStream_t st);
 size_t selfcond_ws_bytes(int M, int V, int D);
 cudaError_t selfcond(const uint16_t* h, int M, const uint16_t* w, const uint16_t* e, int V,
                      int D, const float* inv_t, const float* lse, float* out, void* ws,

@@ -62,6 +62,8 @@ _SIGS = {
     "dg_slot_read_wide": [DP, P, I, P, P, P, P, P, P, P, I, I, U64, I, I, F, P, P, P, P, P, P, P,
                           P, Z, P],
     "dg_prefill_attn": [DP, P, P, P, P, P, P, P, I, I, I, P, P, P, Z, P],
+    "dg_quantize_rows_e4m3": [P, I, I, P, P, P],
+    "dg_lmhead_logsoftmax_entropy_fp8": [DP, P, P, I, P, P, P, P, P, P, P, P, Z, P],
     "dg_commit": [DP, P, P, P, P, P, P, P, P, P, P],
     "dg_selfcond_embed": [DP, P, I, P, P, P, P, P, P, Z, P],
     "dg_denoise_heads": [DP, P, I, P, I, P, P, P, P, P, P, P, P, P, P, Z, P, Z, P],
@@ -191,6 +193,18 @@ def dg_prefill_attn(dims, q, k, v, prompt_len, out, lse, page_table, pages_per_r
                                  _p(lse), _p(page_table), pages_per_req, n_pages, page_size,
                                  _p(pool_k), _p(pool_v), _p(workspace), _nbytes(workspace),
                                  _s(stream))
+
+
+def dg_quantize_rows_e4m3(x, rows, cols, q, scale, stream=None):
+    return lib().dg_quantize_rows_e4m3(_p(x), rows, cols, _p(q), _p(scale), _s(stream))
+
+
+def dg_lmhead_logsoftmax_entropy_fp8(dims, h8, h_scale, M, w8, w_scale, inv_t, lse, entropy, maxz,
+                                     argmax, workspace, stream=None):
+    return lib().dg_lmhead_logsoftmax_entropy_fp8(ctypes.byref(dims), _p(h8), _p(h_scale), M,
+                                                  _p(w8), _p(w_scale), _p(inv_t), _p(lse),
+                                                  _p(entropy), _p(maxz), _p(argmax),
+                                                  _p(workspace), _nbytes(workspace), _s(stream))
 
 
 def dg_commit(dims, entropy, argmax, cand, gamma, committed_state, token_state, commit, tokens,

@@ -246,3 +246,47 @@ class Prefill:
                                      self.ws, stream), "dg_prefill_attn")
         splits = 1 if dg.dg_workspace_bytes(self.dims, dg.DG_WS_PREFILL, 0) <= 256 else 2
         return splits + 1
+
+
+class LmHead:
+    """One lm-head statistics pass over M rows (lse, entropy, max logit, argmax), on bf16
+    operands (dg_lmhead_logsoftmax_entropy) or on e4m3 operands with per-row scales
+    (dg_quantize_rows_e4m3 of the rows, then dg_lmhead_logsoftmax_entropy_fp8; W is
+    quantised once, when the object is made)."""
+
+    def __init__(self, shape, w, M, fp8=False, device="cuda"):
+        f32, i32, u8 = torch.float32, torch.int32, torch.uint8
+        self.shape, self.M, self.fp8 = shape, M, fp8
+        self.dims = dg.make_dims(d_model=shape.D, V=shape.V)
+        self.h = torch.empty((M, shape.D), dtype=torch.bfloat16, device=device)
+        self.inv_t = torch.empty(M, dtype=f32, device=device)
+        self.lse, self.ent, self.maxz = (torch.empty(M, dtype=f32, device=device)
+                                         for _ in range(3))
+        self.argmax = torch.empty(M, dtype=i32, device=device)
+        self.ws = torch.empty(dg.dg_workspace_bytes(self.dims, dg.DG_WS_LMHEAD, M), dtype=u8,
+                              device=device)
+        self.w = w
+        if fp8:
+            self.w8 = torch.empty((shape.V, shape.D), dtype=u8, device=device)
+            self.w_scale = torch.empty(shape.V, dtype=f32, device=device)
+            dg._check(dg.dg_quantize_rows_e4m3(w, shape.V, shape.D, self.w8, self.w_scale),
+                      "dg_quantize_rows_e4m3")
+            self.h8 = torch.empty((M, shape.D), dtype=u8, device=device)
+            self.h_scale = torch.empty(M, dtype=f32, device=device)
+
+    def run(self, step_idx=0, stream=None):
+        """Enqueue one pass; returns the number of library kernels."""
+        d = self.dims
+        if not self.fp8:
+            dg._check(dg.dg_lmhead_logsoftmax_entropy(d, self.h, self.M, self.w, self.inv_t,
+                                                      self.lse, self.ent, self.maxz, self.argmax,
+                                                      self.ws, stream),
+                      "dg_lmhead_logsoftmax_entropy")
+            return 2
+        dg._check(dg.dg_quantize_rows_e4m3(self.h, self.M, self.shape.D, self.h8, self.h_scale,
+                                           stream), "dg_quantize_rows_e4m3")
+        dg._check(dg.dg_lmhead_logsoftmax_entropy_fp8(d, self.h8, self.h_scale, self.M, self.w8,
+                                                      self.w_scale, self.inv_t, self.lse,
+                                                      self.ent, self.maxz, self.argmax, self.ws,
+                                                      stream), "dg_lmhead_logsoftmax_entropy_fp8")
+        return 3
