@@ -40,6 +40,7 @@ WORKLOADS = {
     "lmhead_fp8_m256": ("lmhead_fp8", "FULL_CANVAS", {}),
     "lmhead_bf16_m12": ("lmhead", "FULL_CANVAS", dict(C=12)),
     "lmhead_fp8_m12": ("lmhead_fp8", "FULL_CANVAS", dict(C=12)),
+    "mixed_decode8_prefill2": ("mixed", "LONG_CONTEXT", dict(B=10, C=2048, P=4096)),
     "prefill_8192": ("prefill", "LONG_CONTEXT", dict(B=1, P=8192)),
     "prefill_long": ("prefill", "LONG_CONTEXT", {}),
     "sweep_read_b1": ("read", "LONG_CONTEXT", dict(B=1, P=8192)),
@@ -376,6 +377,11 @@ def attn_flops(shape, prompt_len=None):
     return 4.0 * shape.Hq * shape.d_head * vis
 
 
+def configs_scaled(shape, **kw):
+    from structured_slot_reads_gb300 import configs
+    return configs.scaled(shape, **kw)
+
+
 def prefill_flops(shape):
     """Causal prefill: QK^T and PV over the P (P + 1) / 2 visible (row, key) pairs."""
     return 4.0 * shape.B * shape.Hq * shape.d_head * shape.P * (shape.P + 1) / 2
@@ -428,6 +434,20 @@ def build_runner(kind, shape, device):
         st = LmHead(shape, w, shape.B * shape.C, fp8=kind == "lmhead_fp8", device=device)
         st.h.copy_(inputs.device_normal_bf16(st.h.shape, 1.0, 3, device))
         st.inv_t.copy_(1.0 / inputs.device_uniform(st.inv_t.shape, 0.5, 2.0, 4, device))
+        torch.cuda.synchronize()
+        return st
+    if kind == "mixed":
+        # 8 decoder requests (256-row canvas over a P-token prompt) and 2 encoder
+        # requests of C prompt tokens, one launch
+        from structured_slot_reads_gb300.read import MixedAttention
+        mode = [0] * (shape.B - 2) + [1, 1]
+        rows = [256] * (shape.B - 2) + [shape.C, shape.C]
+        plen = [shape.P] * (shape.B - 2) + [0, 0]
+        st = MixedAttention(mode, rows, plen, shape.C, shape.Hq, shape.Hkv, shape.d_head, shape.W,
+                            device=device)
+        for i, k in enumerate(("q", "kc", "vc", "kenc", "venc")):
+            getattr(st, k).copy_(inputs.device_normal_bf16(getattr(st, k).shape, 1.0, 40 + i,
+                                                           device))
         torch.cuda.synchronize()
         return st
     if kind == "prefill":
@@ -506,6 +526,9 @@ def workload_arm(args, rank, world, local):
     elif kind == "prefill":
         run = lambda i: st.run(step_idx=i)              # noqa: E731
         calls = ["dg_prefill_attn"]
+    elif kind == "mixed":
+        run = lambda i: st.run(step_idx=i)              # noqa: E731
+        calls = ["dg_attn_mixed"]
     elif kind in ("lmhead", "lmhead_fp8"):
         run = lambda i: st.run(step_idx=i)              # noqa: E731
         calls = ["dg_lmhead_logsoftmax_entropy", "dg_quantize_rows_e4m3",
@@ -527,6 +550,12 @@ def workload_arm(args, rank, world, local):
     work["dg_attn_decode"] = (attn_bytes(shape, plen), attn_flops(shape, plen))
     if kind == "prefill":
         work["dg_prefill_attn"] = (prefill_bytes(shape), prefill_flops(shape))
+    if kind == "mixed":
+        dec = configs_scaled(shape, B=1, C=256)
+        enc = configs_scaled(shape, B=1, P=shape.C)
+        fl = (shape.B - 2) * attn_flops(dec) + 2 * prefill_flops(enc)
+        by = (shape.B - 2) * attn_bytes(dec) + 2 * prefill_bytes(enc)
+        work["dg_attn_mixed"] = (by, fl)
     if kind in ("lmhead", "lmhead_fp8"):
         Mr = shape.B * shape.C
         esz = 1 if kind == "lmhead_fp8" else 2
@@ -573,6 +602,8 @@ def workload_arm(args, rank, world, local):
         unit, value = UNIT, steps_per_s * shape.B
     elif kind == "prefill":
         unit, value = "prompt tokens/s", steps_per_s * shape.B * shape.P
+    elif kind == "mixed":
+        unit, value = "attention launches/s", steps_per_s
     elif kind in ("lmhead", "lmhead_fp8"):
         unit, value = "lm-head passes/s", steps_per_s
     else:

@@ -189,6 +189,30 @@ int dg_prefill_attn(const dg_dims* dims, const uint16_t* q, const uint16_t* k, c
                     uint16_t* pool_k, uint16_t* pool_v, void* workspace, size_t workspace_bytes,
                     void* stream);
 
+/* ---- next: decoder and encoder requests in one attention launch ---------
+ * 24-ai.news, "DiffusionGemma integrated into vLLM" ("Integration into the
+ * vLLM infrastructure"): causal attention switched per sequence lets
+ * encoder-mode and decoder-mode requests share one batch.  One launch of the
+ * 512-wide-head kernel over a batch whose request b is
+ *   mode[b] = 0, decoder: rows i < rows_len[b] attend to the prompt keys
+ *     (prompt_len[b] of kenc/venc, contiguous or paged as in dg_attn_decode)
+ *     and to the rows j < rows_len[b] with |i - j| <= W (dg_attn_decode with a
+ *     canvas of rows_len[b] rows);
+ *   mode[b] = 1, encoder: rows i < rows_len[b] attend to rows j <= i of the
+ *     same request (dg_prefill_attn without the page write); prompt_len[b] is
+ *     not read.
+ * dims: B, C = rows per request in q/kc/vc/out, P_max, Hq, Hkv, d_head = 512, W.
+ *   mode, rows_len [B] int32;  q, out [B, C, Hq, 512];  kc, vc [B, C, Hkv, 512];
+ *   kenc, venc, page_table, prompt_len, lse and the workspace (DG_WS_ATTN) as in
+ *   dg_attn_decode.  Rows at or past rows_len[b] are not written.  Page sizes
+ *   the tensor-core kernel cannot take (not a divisor of 128 or below 8) return
+ *   DG_ERR_SHAPE. */
+int dg_attn_mixed(const dg_dims* dims, const int32_t* mode, const int32_t* rows_len,
+                  const uint16_t* q, const uint16_t* kc, const uint16_t* vc, const uint16_t* kenc,
+                  const uint16_t* venc, const int32_t* page_table, int pages_per_req,
+                  int n_pages, int page_size, const int32_t* prompt_len, uint16_t* out,
+                  float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---- next: the lm-head pass on 8-bit operands ---------------------------
  * tau-home.com, "DiffusionGemma like Jev" ("Running NVFP4 locally with a
  * Jev-compatible System One endpoint") and 24-ai.news, "DiffusionGemma

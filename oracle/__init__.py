@@ -37,6 +37,7 @@ from .step import (  # noqa: F401
     paged_to_contiguous,
     paged_write,
     prefill_attn,
+    attn_mixed,
     lmhead_stats,
     label_logits,
     slot_noise_rows,

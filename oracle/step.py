@@ -144,6 +144,35 @@ def prefill_attn(q, k, v, prompt_len, rows=None):
     return out, lse
 
 
+def attn_mixed(mode, rows_len, q, kc, vc, kenc, venc, prompt_len, window):
+    """Encoder- and decoder-mode requests of one batch, each by its own definition.
+
+    24-ai.news, "DiffusionGemma integrated into vLLM" ("Integration into the vLLM
+    infrastructure"): causal attention switched per sequence lets encoder-mode
+    and decoder-mode requests share a batch.
+
+    Request b with mode[b] = 0 is ``attn_decode`` of its first rows_len[b] rows
+    (the canvas) over its prompt KV; mode[b] = 1 is ``prefill_attn`` of its first
+    rows_len[b] rows.  Rows past rows_len[b] are left zero (lse 0).
+    q: [B, C, Hq, d]; kc, vc: [B, C, Hkv, d]; kenc, venc: [B, Pmax, Hkv, d].
+    """
+    B, C, hq, d = q.shape
+    out = np.zeros((B, C, hq, d), dtype=np.float64)
+    lse = np.zeros((B, hq, C), dtype=np.float64)
+    for b in range(B):
+        n = int(min(max(int(rows_len[b]), 0), C))
+        if n == 0:
+            continue
+        if int(mode[b]):
+            o, l = prefill_attn(q[b:b + 1, :n], kc[b:b + 1, :n], vc[b:b + 1, :n], [n])
+        else:
+            o, l = attn_decode(q[b:b + 1, :n], kc[b:b + 1, :n], vc[b:b + 1, :n],
+                               kenc[b:b + 1], venc[b:b + 1], prompt_len[b:b + 1], window)
+        out[b, :n] = o[0]
+        lse[b, :, :n] = l[0]
+    return out, lse
+
+
 def paged_write(k, v, prompt_len, page_table, page_size, n_pages):
     """The page pools an encoder prefill leaves behind: row i of request b goes to
     pool[page_table[b, i // page_size], i % page_size] for i < prompt_len[b]

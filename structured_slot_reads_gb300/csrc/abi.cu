@@ -493,6 +493,49 @@ int dg_prefill_attn(const dg_dims* d, const uint16_t* q, const uint16_t* k, cons
   return launch_result(err);
 }
 
+int dg_attn_mixed(const dg_dims* d, const int32_t* mode, const int32_t* rows_len,
+                  const uint16_t* q, const uint16_t* kc, const uint16_t* vc, const uint16_t* kenc,
+                  const uint16_t* venc, const int32_t* page_table, int pages_per_req,
+                  int n_pages, int page_size, const int32_t* prompt_len, uint16_t* out,
+                  float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!d) return DG_ERR_ARG;
+  if (!attn_dims_ok(d) || d->d_head != 512) return DG_ERR_SHAPE;
+  if (!mode || !rows_len || !q || !kc || !vc || !prompt_len || !out || !lse) return DG_ERR_ARG;
+  if (d->P_max > 0 && (!kenc || !venc)) return DG_ERR_ARG;
+  for (const void* p : {(const void*)q, (const void*)kc, (const void*)vc, (const void*)kenc,
+                        (const void*)venc, (const void*)out})
+    if (!aligned(p, 16)) return DG_ERR_ARG;
+  if (page_table && (page_size < 1 || n_pages < 1 ||
+                     (long long)pages_per_req * page_size < (long long)d->P_max))
+    return DG_ERR_SHAPE;
+  dgi::AttnArgs a{};
+  a.B = d->B;
+  a.C = d->C;
+  a.Pmax = d->P_max;
+  a.Hq = d->Hq;
+  a.Hkv = d->Hkv;
+  a.d = d->d_head;
+  a.W = d->W;
+  a.q = q;
+  a.kc = kc;
+  a.vc = vc;
+  a.kenc = kenc ? kenc : kc;
+  a.venc = venc ? venc : vc;
+  a.page_table = page_table;
+  a.pages_per_req = pages_per_req;
+  a.n_pages = n_pages;
+  a.page_size = page_size;
+  a.prompt_len = prompt_len;
+  a.out = out;
+  a.lse = lse;
+  a.mode = mode;
+  a.rows_len = rows_len;
+  if (!dgi::attn_tc_supported(a)) return DG_ERR_SHAPE;
+  const size_t need = dg_workspace_bytes(d, DG_WS_ATTN, 0);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return DG_ERR_WORKSPACE;
+  return launch_result(dgi::attn_decode_tc(a, workspace, static_cast<cudaStream_t>(stream)));
+}
+
 int dg_quantize_rows_e4m3(const uint16_t* x, int rows, int cols, uint8_t* q, float* scale,
                           void* stream) {
   if (rows < 0 || cols < 1) return DG_ERR_ARG;

@@ -64,6 +64,8 @@ struct TcArgs {
   int B, C, Pmax, Hq, Hkv, W, G, npos, q_blocks, splits;
   int causal;              // encoder prefill: rows attend to keys j <= i of their own sequence
   const int32_t* seq_len;  // causal: valid rows (and keys) per request
+  const int32_t* mode;     // mixed batch: per request 1 = causal, 0 = decoder (null: `causal`)
+  const int32_t* rows_len; // mixed batch: valid rows per request (null: seq_len or C)
   const int32_t* page_table;
   int pages_per_req, n_pages, page_size;
   const int32_t* prompt_len;
@@ -87,7 +89,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // Key-tile geometry of one CTA (shared by every role).
 struct Tiles {
-  int P, p0, npos, clo, chi, nbp, t_begin, t_end, len;
+  int P, p0, npos, clo, chi, nbp, t_begin, t_end, len, causal;
   __device__ int key0(int t) const { return t < nbp ? t * BN : clo + (t - nbp) * BN; }
 };
 
@@ -95,17 +97,23 @@ __device__ __forceinline__ Tiles tiles_of(const TcArgs& a, int b, int qb, int sp
   Tiles T;
   T.p0 = qb * a.npos;
   T.npos = min(a.npos, a.C - T.p0);
-  if (a.causal) {
+  T.causal = a.mode ? (a.mode[b] != 0) : (a.causal != 0);
+  const int32_t* lens = a.rows_len ? a.rows_len : (T.causal ? a.seq_len : nullptr);
+  T.len = lens ? min(max(lens[b], 0), a.C) : a.C;
+  if (T.causal) {
     // keys 0 .. (last row of the block), within the request's length
-    T.len = min(max(a.seq_len[b], 0), a.C);
     T.P = 0;
     T.clo = 0;
     T.chi = T.p0 < T.len ? min(T.len, T.p0 + T.npos) : 0;  // no rows of this block: no keys
-  } else {
-    T.len = a.C;
+  } else if (T.p0 < T.len) {
+    // prompt keys plus the rows of the request within +-W of the block
     T.P = min(max(a.prompt_len[b], 0), a.Pmax);
     T.clo = max(0, T.p0 - a.W);
-    T.chi = min(a.C, T.p0 + T.npos - 1 + a.W + 1);
+    T.chi = min(T.len, T.p0 + T.npos - 1 + a.W + 1);
+  } else {
+    T.P = 0;
+    T.clo = 0;
+    T.chi = 0;
   }
   T.nbp = (T.P + BN - 1) / BN;
   const int nb = T.nbp + (T.chi - T.clo + BN - 1) / BN;
@@ -176,7 +184,7 @@ __device__ __forceinline__ void softmax_and_store(const TcArgs& a, const Tiles& 
         }
         if (bad && r == 0 && half == 0) atomicOr(a.status, 2 /* DG_DEV_BAD_PAGE */);
       }
-    } else if (a.causal) {
+    } else if (T.causal) {
       lo = -key0;
       hi = min(T.chi, pos + 1) - key0;
     } else {
@@ -347,7 +355,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int dh = bid & 1;
   bid >>= 1;
   // causal prefill: the last query blocks see the most keys, so they go first
-  const int qb = a.causal ? a.q_blocks - 1 - bid % a.q_blocks : bid % a.q_blocks;
+  const int qb = (a.causal || a.mode) ? a.q_blocks - 1 - bid % a.q_blocks : bid % a.q_blocks;
   bid /= a.q_blocks;
   const int g = bid % a.Hkv;
   const int b = bid / a.Hkv;
@@ -600,6 +608,8 @@ cudaError_t attn_decode_tc(const AttnArgs& x, void* ws, cudaStream_t st) {
   a.splits = tc_splits(x.B, x.C, x.Hq, x.Hkv, x.Pmax, a.W);
   a.causal = x.causal;
   a.seq_len = x.seq_len;
+  a.mode = x.mode;
+  a.rows_len = x.rows_len;
   a.page_table = x.page_table;
   a.pages_per_req = x.pages_per_req;
   a.n_pages = x.n_pages;
@@ -649,7 +659,7 @@ cudaError_t attn_decode_tc(const AttnArgs& x, void* ws, cudaStream_t st) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || a.splits == 1) return e;
   return attn_combine(x.B, x.C, x.Hq, HD, a.splits, a.ws_o, a.ws_ml, x.out, x.lse, st,
-                      x.causal ? x.seq_len : nullptr);
+                      x.rows_len ? x.rows_len : (x.causal ? x.seq_len : nullptr));
 }
 
 // Paged KV write of an encoder prefill: one warp per (request, key row, KV head)

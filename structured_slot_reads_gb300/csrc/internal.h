@@ -74,6 +74,8 @@ struct AttnArgs {
   float* lse;
   int causal = 0;                     // encoder prefill (d = 512 tensor-core kernel only)
   const int32_t* seq_len = nullptr;   // causal: rows per request (q/k/v are [B, C, H, d])
+  const int32_t* mode = nullptr;      // mixed batch: per request 1 = causal, 0 = decoder
+  const int32_t* rows_len = nullptr;  // mixed batch: valid rows per request
 };
 size_t attn_ws_bytes(int B, int C, int Pmax, int Hq, int Hkv, int d, int W);
 cudaError_t attn_decode(const AttnArgs& a, void* ws, cudaStream_t st);

@@ -62,6 +62,7 @@ _SIGS = {
     "dg_slot_read_wide": [DP, P, I, P, P, P, P, P, P, P, I, I, U64, I, I, F, P, P, P, P, P, P, P,
                           P, Z, P],
     "dg_prefill_attn": [DP, P, P, P, P, P, P, P, I, I, I, P, P, P, Z, P],
+    "dg_attn_mixed": [DP, P, P, P, P, P, P, P, P, I, I, I, P, P, P, P, Z, P],
     "dg_quantize_rows_e4m3": [P, I, I, P, P, P],
     "dg_lmhead_logsoftmax_entropy_fp8": [DP, P, P, I, P, P, P, P, P, P, P, P, Z, P],
     "dg_commit": [DP, P, P, P, P, P, P, P, P, P, P],
@@ -193,6 +194,14 @@ def dg_prefill_attn(dims, q, k, v, prompt_len, out, lse, page_table, pages_per_r
                                  _p(lse), _p(page_table), pages_per_req, n_pages, page_size,
                                  _p(pool_k), _p(pool_v), _p(workspace), _nbytes(workspace),
                                  _s(stream))
+
+
+def dg_attn_mixed(dims, mode, rows_len, q, kc, vc, kenc, venc, page_table, pages_per_req, n_pages,
+                  page_size, prompt_len, out, lse, workspace, stream=None):
+    return lib().dg_attn_mixed(ctypes.byref(dims), _p(mode), _p(rows_len), _p(q), _p(kc), _p(vc),
+                               _p(kenc), _p(venc), _p(page_table), pages_per_req, n_pages,
+                               page_size, _p(prompt_len), _p(out), _p(lse), _p(workspace),
+                               _nbytes(workspace), _s(stream))
 
 
 def dg_quantize_rows_e4m3(x, rows, cols, q, scale, stream=None):

@@ -290,3 +290,35 @@ class LmHead:
                                                       self.ent, self.maxz, self.argmax, self.ws,
                                                       stream), "dg_lmhead_logsoftmax_entropy_fp8")
         return 3
+
+
+class MixedAttention:
+    """One attention launch over decoder-mode requests (canvas rows over their prompt KV)
+    and encoder-mode requests (causal over their prompt rows), dg_attn_mixed."""
+
+    def __init__(self, mode, rows, prompt_len, C, Hq, Hkv, d_head, W, device="cuda"):
+        bf, f32, i32, u8 = torch.bfloat16, torch.float32, torch.int32, torch.uint8
+        B = len(mode)
+        P = max(max(prompt_len), 1)
+        self.B, self.C = B, C
+        self.dims = dg.make_dims(B=B, C=C, P_max=P, Hq=Hq, Hkv=Hkv, d_head=d_head, W=W)
+        self.mode = _dev(mode, i32, device)
+        self.rows = _dev(rows, i32, device)
+        self.prompt_len = _dev(prompt_len, i32, device)
+        self.rows_host, self.mode_host, self.plen_host = list(rows), list(mode), list(prompt_len)
+        self.q = torch.empty((B, C, Hq, d_head), dtype=bf, device=device)
+        self.kc = torch.empty((B, C, Hkv, d_head), dtype=bf, device=device)
+        self.vc = torch.empty_like(self.kc)
+        self.kenc = torch.empty((B, P, Hkv, d_head), dtype=bf, device=device)
+        self.venc = torch.empty_like(self.kenc)
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty((B, Hq, C), dtype=f32, device=device)
+        self.ws = torch.empty(max(dg.dg_workspace_bytes(self.dims, dg.DG_WS_ATTN, 0), 256),
+                              dtype=u8, device=device)
+
+    def run(self, step_idx=0, stream=None):
+        """Enqueue the launch; returns the number of library kernels."""
+        dg._check(dg.dg_attn_mixed(self.dims, self.mode, self.rows, self.q, self.kc, self.vc,
+                                   self.kenc, self.venc, None, 0, 0, 0, self.prompt_len, self.out,
+                                   self.lse, self.ws, stream), "dg_attn_mixed")
+        return 1 if dg.dg_workspace_bytes(self.dims, dg.DG_WS_ATTN, 0) <= 256 else 2

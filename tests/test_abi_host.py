@@ -205,3 +205,14 @@ def test_prefill_validates_shapes(lib):
                               stream=0) == dg.DG_ERR_ARG
     assert dg.dg_prefill_attn(ok, 16, 16, 16, 16, 16, 16, None, 0, 0, 0, None, None, None,
                               stream=0) == dg.DG_ERR_WORKSPACE
+
+
+def test_mixed_attention_validates(lib):
+    d = dg.make_dims(B=2, C=64, P_max=32, Hq=8, Hkv=2, d_head=512, W=8)
+    assert dg.dg_attn_mixed(d, None, 16, 16, 16, 16, 16, 16, None, 0, 0, 0, 16, 16, 16, None,
+                            stream=0) == dg.DG_ERR_ARG
+    d64 = dg.make_dims(B=2, C=64, P_max=32, Hq=8, Hkv=2, d_head=64, W=8)
+    assert dg.dg_attn_mixed(d64, 16, 16, 16, 16, 16, 16, 16, None, 0, 0, 0, 16, 16, 16, None,
+                            stream=0) == dg.DG_ERR_SHAPE
+    assert dg.dg_attn_mixed(d, 16, 16, 16, 16, 16, 16, 16, 16, 2, 10, 24, 16, 16, 16, None,
+                            stream=0) == dg.DG_ERR_SHAPE   # 24-key pages: not on this kernel

@@ -169,3 +169,18 @@ def test_paged_write_inverts_paged_to_contiguous():
         assert np.array_equal(ke[b, :n], k[b, :n]) and np.array_equal(ve[b, :n], v[b, :n])
     assert np.count_nonzero(pk.reshape(pk.shape[0], -1).any(axis=1)) == sum(
         (n + ps - 1) // ps for n in lens)
+
+
+def test_mixed_batch_reduces_to_its_modes():
+    """All-decoder batches equal attn_decode; all-encoder batches equal prefill_attn."""
+    from oracle import attn_mixed, prefill_attn
+    x = _inputs(B=2, C=12, P=(5, 9))
+    n = np.array([12, 12])
+    out, lse = attn_mixed(np.zeros(2, int), n, x["q"], x["kc"], x["vc"], x["kenc"], x["venc"],
+                          x["prompt_len"], 3)
+    ref, ref_lse = attn_decode(x["q"], x["kc"], x["vc"], x["kenc"], x["venc"], x["prompt_len"], 3)
+    assert np.allclose(out, ref, atol=1e-12) and np.allclose(lse, ref_lse, atol=1e-12)
+    out, lse = attn_mixed(np.ones(2, int), np.array([12, 7]), x["q"], x["kc"], x["vc"], None,
+                          None, x["prompt_len"], 3)
+    ref, ref_lse = prefill_attn(x["q"], x["kc"], x["vc"], np.array([12, 7]))
+    assert np.allclose(out, ref, atol=1e-12) and np.allclose(lse, ref_lse, atol=1e-12)
