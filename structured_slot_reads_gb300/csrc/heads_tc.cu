@@ -81,57 +81,52 @@ struct HeadsParams {
 };
 
 // Reference of each canvas row: max over the first REF_N vocabulary entries of
-// (h . w_v) / T in log2 units, plus headroom.  One warp per row (8 rows per
-// CTA), every lane keeping its REF_N partial dot products and all of its loads
-// in flight; the REF_N W rows are shared by the CTA's warps through L1.
-constexpr int REF_ROWS = 8;
-__global__ void ref_kernel(const __nv_bfloat16* h, const __nv_bfloat16* w, const float* inv_t,
-                           int M, int V, int D, float* ref) {
+// (h . w_v) / T in log2 units, plus headroom.  One CTA per row; warp w takes
+// entry w % REF_N over a quarter of d_model (w / REF_N), so each lane has only
+// a few 16-byte chunks and the partial sums meet in shared memory.
+constexpr int REF_KSPLIT = 4;
+__global__ void __launch_bounds__(REF_N * REF_KSPLIT * 32)
+    ref_kernel(const __nv_bfloat16* h, const __nv_bfloat16* w, const float* inv_t, int M, int V,
+               int D, float* ref) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * REF_ROWS + warp;
-  if (row >= M) return;
+  const int u = warp % REF_N, ks = warp / REF_N;
+  const int row = blockIdx.x;
+  __shared__ float part[REF_KSPLIT][REF_N];
   const uint4* x = reinterpret_cast<const uint4*>(h + (long long)row * D);
+  const uint4* y = reinterpret_cast<const uint4*>(w + (long long)u * D);
   const int n16 = D / 8;
-  float acc[REF_N];
+  const int per = (n16 + REF_KSPLIT - 1) / REF_KSPLIT;
+  const int i0 = ks * per, i1 = min(n16, i0 + per);
+  float acc = 0.f;
+  if (u < V) {
+#pragma unroll 4
+    for (int i = i0 + lane; i < i1; i += 32) {
+      const uint4 a = x[i];
+      const uint4 b = __ldg(y + i);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
 #pragma unroll
-  for (int u = 0; u < REF_N; ++u) acc[u] = 0.f;
-  for (int base = 0; base < n16; base += 32 * 4) {
-    uint4 a[4], bw[4][REF_N];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int i = base + c * 32 + lane;
-      a[c] = i < n16 ? x[i] : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int u = 0; u < REF_N; ++u)
-        bw[c][u] = (i < n16 && u < V)
-                       ? __ldg(reinterpret_cast<const uint4*>(w + (long long)u * D) + i)
-                       : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[c]);
-#pragma unroll
-      for (int u = 0; u < REF_N; ++u) {
-        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&bw[c][u]);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float2 fa = __bfloat1622float2(a2[q]);
-          const float2 fb = __bfloat1622float2(b2[q]);
-          acc[u] = fmaf(fa.x, fb.x, acc[u]);
-          acc[u] = fmaf(fa.y, fb.y, acc[u]);
-        }
+      for (int q = 0; q < 4; ++q) {
+        const float2 fa = __bfloat1622float2(a2[q]);
+        const float2 fb = __bfloat1622float2(b2[q]);
+        acc = fmaf(fa.x, fb.x, acc);
+        acc = fmaf(fa.y, fb.y, acc);
       }
     }
   }
-  float best = -INFINITY;
 #pragma unroll
-  for (int u = 0; u < REF_N; ++u) {
-    float s = acc[u];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (u < V) best = fmaxf(best, s);
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) part[ks][u] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m = -INFINITY;
+    for (int e = 0; e < REF_N && e < V; ++e) {
+      float t = 0.f;
+      for (int k = 0; k < REF_KSPLIT; ++k) t += part[k][e];
+      m = fmaxf(m, t);
+    }
+    ref[row] = m * inv_t[row] * LOG2E + REF_HEADROOM;
   }
-  if (lane == 0) ref[row] = best * inv_t[row] * LOG2E + REF_HEADROOM;
 }
 
 template <int MT, int BN, bool DRAWS>
@@ -628,7 +623,7 @@ cudaError_t denoise_heads(const uint16_t* h, int M, const uint16_t* draw_rows, i
   } else {
     td = tb;  // unused
   }
-  ref_kernel<<<(M + REF_ROWS - 1) / REF_ROWS, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(h),
+  ref_kernel<<<M, REF_N * REF_KSPLIT * 32, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(h),
                                 reinterpret_cast<const __nv_bfloat16*>(w), inv_t, M, V, D, ref);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -102,97 +102,87 @@ __global__ void slot_noise_kernel(const __nv_bfloat16* h, int M, const __nv_bflo
 // the gate on draw 0's entropy, the average and the choice.
 // ---------------------------------------------------------------------------
 constexpr int MAXL = 26;
-constexpr int MAXR = 8;
 
-template <int LPL>  // labels per lane of the epilogue warp: label tables of stride L <= 32 LPL
-__global__ void slot_finish_kernel(const __nv_bfloat16* rows, const float* inv_t_rows,
-                                   const float* lse_rows, const __nv_bfloat16* w, int V, int D,
-                                   const int32_t* label_ids, const int32_t* n_labels, int L, int R,
-                                   int samples, float gate, float* q_avg, float* h_slot,
-                                   int32_t* chosen, float* lp_draws, uint8_t* resampled,
-                                   int32_t* n_reads, int* status) {
-  constexpr int CAP = 32 * LPL;
-  __shared__ float z[MAXR][CAP];
-  __shared__ int ids[CAP];
-  const int s = blockIdx.x;
+// Label logits of every (slot, draw, label): one warp per product, 8 labels per
+// CTA, grid (S * R, ceil(L / 8)).  The fp32 logit z / T goes to lp_draws, which
+// the epilogue below then turns into z - lse.
+__global__ void slot_dots_kernel(const __nv_bfloat16* rows, const float* inv_t_rows,
+                                 const __nv_bfloat16* w, int V, int D, const int32_t* label_ids,
+                                 const int32_t* n_labels, int L, int R, float* lp_draws,
+                                 int* status) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nw = blockDim.x >> 5;
-  int n = n_labels[s];
-  // n == 0: a question whose ask_if condition did not fire -- not read
-  const bool n_ok = n >= 0 && n <= L;
-  if (!n_ok) n = 0;
-  for (int k = threadIdx.x; k < CAP; k += blockDim.x) {
-    int id = (k < n) ? label_ids[(long long)s * L + k] : 0;
-    if (id < 0 || id >= V) {
-      id = 0;
-      if (k < n) atomicOr(status, 4 /* DG_DEV_BAD_LABEL */);
-    }
-    ids[k] = id;
+  const int s = blockIdx.x / R, r = blockIdx.x % R;
+  const int k = blockIdx.y * 8 + warp;
+  const int n = n_labels[s];
+  if (n < 0 || n > L || k >= n) return;  // a bad count is flagged by the epilogue
+  int id = label_ids[(long long)s * L + k];
+  if (id < 0 || id >= V) {
+    if (lane == 0) atomicOr(status, 4 /* DG_DEV_BAD_LABEL */);
+    id = 0;
   }
-  if (threadIdx.x == 0 && !n_ok) atomicOr(status, 4);
-  __syncthreads();
-  // one warp per (draw, label) dot product; each lane issues all of its 16-byte
-  // loads (up to 12, d_model <= 3072) before accumulating, so a product costs one
-  // memory latency
-  const bool vec = (D % 8) == 0;
-  for (int job = warp; job < R * n; job += nw) {
-    const int r = job / n, k = job % n;
-    const __nv_bfloat16* xr = rows + (long long)(s * R + r) * D;
-    const __nv_bfloat16* yr = w + (long long)ids[k] * D;
-    float acc = 0.f;
-    if (vec) {
-      const uint4* x = reinterpret_cast<const uint4*>(xr);
-      const uint4* y = reinterpret_cast<const uint4*>(yr);
-      const int n16 = D / 8;
-      for (int base = 0; base < n16; base += 32 * 12) {
-        uint4 xa[12], ya[12];
+  const __nv_bfloat16* xr = rows + (long long)(s * R + r) * D;
+  const __nv_bfloat16* yr = w + (long long)id * D;
+  float acc = 0.f;
+  if ((D % 8) == 0) {
+    const uint4* x = reinterpret_cast<const uint4*>(xr);
+    const uint4* y = reinterpret_cast<const uint4*>(yr);
+    const int n16 = D / 8;
+#pragma unroll 4
+    for (int i = lane; i < n16; i += 32) {
+      const uint4 xa = x[i];
+      const uint4 ya = __ldg(y + i);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&xa);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&ya);
 #pragma unroll
-        for (int u = 0; u < 12; ++u) {
-          const int i = base + u * 32 + lane;
-          xa[u] = i < n16 ? x[i] : make_uint4(0, 0, 0, 0);
-          ya[u] = i < n16 ? __ldg(y + i) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int u = 0; u < 12; ++u) {
-          const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&xa[u]);
-          const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&ya[u]);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float2 a = __bfloat1622float2(a2[q]);
-            const float2 b = __bfloat1622float2(b2[q]);
-            acc = fmaf(a.x, b.x, acc);
-            acc = fmaf(a.y, b.y, acc);
-          }
-        }
-      }
-    } else {
-      const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(xr);
-      const __nv_bfloat162* y = reinterpret_cast<const __nv_bfloat162*>(yr);
-      for (int i = lane; i < D / 2; i += 32) {
-        const float2 a = __bfloat1622float2(x[i]);
-        const float2 b = __bfloat1622float2(y[i]);
+      for (int q = 0; q < 4; ++q) {
+        const float2 a = __bfloat1622float2(a2[q]);
+        const float2 b = __bfloat1622float2(b2[q]);
         acc = fmaf(a.x, b.x, acc);
         acc = fmaf(a.y, b.y, acc);
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) z[r][k] = acc * inv_t_rows[s * R + r];
+  } else {
+    const __nv_bfloat162* x = reinterpret_cast<const __nv_bfloat162*>(xr);
+    const __nv_bfloat162* y = reinterpret_cast<const __nv_bfloat162*>(yr);
+    for (int i = lane; i < D / 2; i += 32) {
+      const float2 a = __bfloat1622float2(x[i]);
+      const float2 b = __bfloat1622float2(y[i]);
+      acc = fmaf(a.x, b.x, acc);
+      acc = fmaf(a.y, b.y, acc);
+    }
   }
-  __syncthreads();
-  if (warp != 0) return;
-  // warp epilogue: lane holds labels lane + 32 i, i < LPL
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) lp_draws[((long long)s * R + r) * L + k] = acc * inv_t_rows[s * R + r];
+}
+
+// The slot read from the label logits: one warp per slot, lane holds labels
+// lane + 32 i (i < LPL, label tables of stride L <= 32 LPL).
+template <int LPL>
+__global__ void slot_epilogue_kernel(const float* lse_rows, const int32_t* n_labels, int L, int R,
+                                     int samples, float gate, float* q_avg, float* h_slot,
+                                     int32_t* chosen, float* lp_draws, uint8_t* resampled,
+                                     int32_t* n_reads, int* status) {
+  const int s = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  int n = n_labels[s];
+  // n == 0: a question whose ask_if condition did not fire -- not read
+  if (n < 0 || n > L) {
+    if (lane == 0) atomicOr(status, 4 /* DG_DEV_BAD_LABEL */);
+    n = 0;
+  }
   float qsum[LPL], q0[LPL];
 #pragma unroll
   for (int i = 0; i < LPL; ++i) qsum[i] = q0[i] = 0.f;
   float h0 = 0.f;
   for (int r = 0; r < R; ++r) {
+    float* lp = lp_draws + ((long long)s * R + r) * L;
     float zk[LPL];
     float m = -INFINITY;
 #pragma unroll
     for (int i = 0; i < LPL; ++i) {
       const int k = lane + 32 * i;
-      zk[i] = k < n ? z[r][k] : -INFINITY;
+      zk[i] = k < n ? lp[k] : -INFINITY;
       m = fmaxf(m, zk[i]);
     }
 #pragma unroll
@@ -212,7 +202,7 @@ __global__ void slot_finish_kernel(const __nv_bfloat16* rows, const float* inv_t
       const int k = lane + 32 * i;
       const float q = ek[i] / tot;
       if (k < n && q > 0.f) hq -= q * logf(q);
-      if (k < L) lp_draws[((long long)s * R + r) * L + k] = k < n ? zk[i] - lse_r : 0.f;
+      if (k < L) lp[k] = k < n ? zk[i] - lse_r : 0.f;
       if (r < samples) qsum[i] += q;
       if (r == 0) q0[i] = q;
     }
@@ -415,17 +405,32 @@ cudaError_t slot_noise(const uint16_t* h, int M, const uint16_t* e, int V, int D
   return cudaGetLastError();
 }
 
+// Label logits then the per-slot read (label tables of stride L <= 32 LPL).
+template <int LPL>
+cudaError_t finish(const uint16_t* rows, const float* inv_t_rows, const float* lse_rows,
+                   const uint16_t* w, int V, int D, const int32_t* label_ids,
+                   const int32_t* n_labels, int L, int S, int R, int samples, float gate,
+                   float* q_avg, float* h_slot, int32_t* chosen, float* lp_draws,
+                   uint8_t* resampled, int32_t* n_reads, cudaStream_t st) {
+  int* stp = status_ptr();
+  slot_dots_kernel<<<dim3(S * R, (L + 7) / 8), 256, 0, st>>>(
+      reinterpret_cast<const __nv_bfloat16*>(rows), inv_t_rows,
+      reinterpret_cast<const __nv_bfloat16*>(w), V, D, label_ids, n_labels, L, R, lp_draws, stp);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  slot_epilogue_kernel<LPL><<<S, 32, 0, st>>>(lse_rows, n_labels, L, R, samples, gate, q_avg,
+                                              h_slot, chosen, lp_draws, resampled, n_reads, stp);
+  return cudaGetLastError();
+}
+
 cudaError_t slot_finish(const uint16_t* rows, const float* inv_t_rows, const float* lse_rows,
                         const uint16_t* w, int V, int D, const int32_t* label_ids,
                         const int32_t* n_labels, int S, int R, int samples, float gate,
                         float* q_avg, float* h_slot, int32_t* chosen, float* lp_draws,
                         uint8_t* resampled, int32_t* n_reads, cudaStream_t st) {
   if (S == 0) return cudaSuccess;
-  slot_finish_kernel<1><<<S, 1024, 0, st>>>(
-      reinterpret_cast<const __nv_bfloat16*>(rows), inv_t_rows, lse_rows,
-      reinterpret_cast<const __nv_bfloat16*>(w), V, D, label_ids, n_labels, MAXL, R, samples,
-      gate, q_avg, h_slot, chosen, lp_draws, resampled, n_reads, status_ptr());
-  return cudaGetLastError();
+  return finish<1>(rows, inv_t_rows, lse_rows, w, V, D, label_ids, n_labels, MAXL, S, R, samples,
+                   gate, q_avg, h_slot, chosen, lp_draws, resampled, n_reads, st);
 }
 
 cudaError_t slot_finish_wide(const uint16_t* rows, const float* inv_t_rows, const float* lse_rows,
@@ -436,22 +441,14 @@ cudaError_t slot_finish_wide(const uint16_t* rows, const float* inv_t_rows, cons
                              cudaStream_t st) {
   if (S == 0) return cudaSuccess;
   if (L < 1 || L > 256) return cudaErrorInvalidValue;
-  const __nv_bfloat16* rb = reinterpret_cast<const __nv_bfloat16*>(rows);
-  const __nv_bfloat16* wb = reinterpret_cast<const __nv_bfloat16*>(w);
-  int* stp = status_ptr();
   if (L <= 64)
-    slot_finish_kernel<2><<<S, 1024, 0, st>>>(rb, inv_t_rows, lse_rows, wb, V, D, label_ids,
-                                              n_labels, L, R, samples, gate, q_avg, h_slot,
-                                              chosen, lp_draws, resampled, n_reads, stp);
-  else if (L <= 128)
-    slot_finish_kernel<4><<<S, 1024, 0, st>>>(rb, inv_t_rows, lse_rows, wb, V, D, label_ids,
-                                              n_labels, L, R, samples, gate, q_avg, h_slot,
-                                              chosen, lp_draws, resampled, n_reads, stp);
-  else
-    slot_finish_kernel<8><<<S, 1024, 0, st>>>(rb, inv_t_rows, lse_rows, wb, V, D, label_ids,
-                                              n_labels, L, R, samples, gate, q_avg, h_slot,
-                                              chosen, lp_draws, resampled, n_reads, stp);
-  return cudaGetLastError();
+    return finish<2>(rows, inv_t_rows, lse_rows, w, V, D, label_ids, n_labels, L, S, R, samples,
+                     gate, q_avg, h_slot, chosen, lp_draws, resampled, n_reads, st);
+  if (L <= 128)
+    return finish<4>(rows, inv_t_rows, lse_rows, w, V, D, label_ids, n_labels, L, S, R, samples,
+                     gate, q_avg, h_slot, chosen, lp_draws, resampled, n_reads, st);
+  return finish<8>(rows, inv_t_rows, lse_rows, w, V, D, label_ids, n_labels, L, S, R, samples,
+                   gate, q_avg, h_slot, chosen, lp_draws, resampled, n_reads, st);
 }
 
 cudaError_t ask_if_select(const int32_t* chosen1, int S1, const int32_t* cond_slot,

@@ -139,7 +139,7 @@ class TwoStageRead:
         self._read(self.S2, self.slot_row2, self.slot_req2, self.label_ids2, self.n_labels2,
                    self.out2, 1, stream)
         attn_kernels = 1 if dg.dg_workspace_bytes(self.dims, dg.DG_WS_ATTN, 0) <= 256 else 2
-        return attn_kernels + 4 + 1 + 4
+        return attn_kernels + 5 + 1 + 5   # a slot read: noise, stats, finalize, logits, epilogue
 
     def decisions(self):
         """Slot decisions completed by one run (stage-1 slots + asked stage-2 slots)."""
@@ -212,7 +212,7 @@ class ReadStep:
                                            o["lp"], o["resampled"], o["n_reads"], o["tokens"],
                                            self.ws_read, stream), "dg_slot_read_wide")
         attn_kernels = 1 if dg.dg_workspace_bytes(d, dg.DG_WS_ATTN, 0) <= 256 else 2
-        return attn_kernels + 4
+        return attn_kernels + 5
 
 
 class Prefill:

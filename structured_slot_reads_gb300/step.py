@@ -176,16 +176,18 @@ class DenoiseStep:
         n = 1 + (1 if self._attn_splits() > 1 else 0)
         if self.fused:
             # ref + heads + finalize + commit + accum + reduce + update, and either
-            # noise + draw finalize + finish (draws in the pass) or a slot read
+            # noise + draw finalize + finish (label logits, slot epilogue) with the
+            # draws in the pass, or a slot read
             n += 3 + 1 + 2 + 1
             if self.n_draw:
-                n += 3
-            elif self.with_slots:
                 n += 4
+            elif self.with_slots:
+                n += 5
             return n
-        # stats + finalize, [noise + stats + finalize + finish], commit, probs + accum + reduce, update
+        # stats + finalize, [noise + stats + finalize + label logits + slot epilogue],
+        # commit, probs + accum + reduce, update
         n += 2
-        n += 4 if self.with_slots else 0
+        n += 5 if self.with_slots else 0
         n += 1 + 3 + 1
         return n
 

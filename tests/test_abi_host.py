@@ -145,7 +145,7 @@ def test_step_runner_builds_on_host(lib, fused):
     w = torch.zeros((shp.V, shp.D), dtype=torch.bfloat16)
     st = DenoiseStep(shp, w, w, device="cpu", fused=fused)
     assert st.fused == fused
-    assert st.kernels_per_step() == (12 if fused else 13) - (0 if st._attn_splits() > 1 else 1)
+    assert st.kernels_per_step() == (13 if fused else 14) - (0 if st._attn_splits() > 1 else 1)
     if fused:
         assert st.probs.shape == (shp.C, dg.dg_probs_ld(shp.V)) and st.n_draw == 4
 
@@ -160,7 +160,7 @@ def test_batched_step_reads_slots_in_their_own_pass(lib):
     w = torch.zeros((shp.V, shp.D), dtype=torch.bfloat16)
     st = DenoiseStep(shp, w, w, device="cpu", fused=True)
     assert st.S == 8 and st.n_draw == 0 and not hasattr(st, "ws_sc")
-    assert st.kernels_per_step() == 13 - (0 if st._attn_splits() > 1 else 1)
+    assert st.kernels_per_step() == 14 - (0 if st._attn_splits() > 1 else 1)
 
 
 def test_two_stage_runner_builds_on_host(lib):
