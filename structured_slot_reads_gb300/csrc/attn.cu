@@ -401,14 +401,17 @@ __global__ void __launch_bounds__(AttnCfg<D>::THREADS, 1) attn_kernel(Args a) {
   }
 }
 
-// Merge split partials: one warp per (b, pos, head) row.  The common reference
-// comes first (the lanes read the splits' maxima in parallel); then every
-// split's partial row is read with independent loads, and a split that saw no
-// key (reference -inf, partial never written) is dropped by a select.
+// Merge split partials: one thread per (b, pos, head) row and 4 output columns.
+// Each thread first takes the row's reference over the splits (the (m, l) pairs
+// are shared by the row's threads through L1), then sums the partial columns;
+// a split that saw no key (m = -inf, partial never written) is dropped by a
+// select.
 template <int D>
 __global__ void attn_combine_kernel(Args a) {
-  const long long row = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
+  constexpr int TPR = D / 4;  // threads per row
+  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long row = tid / TPR;
+  const int c4 = (int)(tid % TPR);
   const long long nrows = (long long)a.B * a.C * a.Hq;
   if (row >= nrows) return;
   const int head = (int)(row % a.Hq);
@@ -416,35 +419,30 @@ __global__ void attn_combine_kernel(Args a) {
   const int b = (int)(row / ((long long)a.Hq * a.C));
   if (a.seq_len && pos >= a.seq_len[b]) return;
   const long long split_o = (long long)a.B * a.C * a.Hq * D;
-  auto ml_of = [&](int s) {
-    return a.ws_ml + (((long long)s * a.B + b) * a.Hq + head) * a.C * 2 + pos * 2;
-  };
+  const long long ml_split = (long long)a.B * a.Hq * a.C * 2;
+  const float* ml0 = a.ws_ml + ((long long)b * a.Hq + head) * a.C * 2 + pos * 2;
   float mt = -INFINITY;
-  for (int s = lane; s < a.splits; s += 32) mt = fmaxf(mt, ml_of(s)[0]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+  for (int s = 0; s < a.splits; ++s) mt = fmaxf(mt, ml0[s * ml_split]);
   float lt = 0.f;
-  float acc[D / 32];
-#pragma unroll
-  for (int i = 0; i < D / 32; ++i) acc[i] = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4* wo = reinterpret_cast<const float4*>(a.ws_o + row * D) + c4;
 #pragma unroll 4
   for (int s = 0; s < a.splits; ++s) {
-    const float* ml = ml_of(s);
-    const float m = ml[0], l = ml[1];
+    const float m = ml0[s * ml_split], l = ml0[s * ml_split + 1];
     const bool live = m != -INFINITY;
     const float f = live ? exp2f(m - mt) : 0.f;
     lt += live ? l * f : 0.f;
-    const float* wo = a.ws_o + s * split_o + row * D;
-#pragma unroll
-    for (int i = 0; i < D / 32; ++i) {
-      const float v = wo[i * 32 + lane];
-      acc[i] += live ? v * f : 0.f;
-    }
+    const float4 v = wo[s * (split_o / 4)];
+    acc.x += live ? v.x * f : 0.f;
+    acc.y += live ? v.y * f : 0.f;
+    acc.z += live ? v.z * f : 0.f;
+    acc.w += live ? v.w * f : 0.f;
   }
   const float inv = lt > 0.f ? 1.f / lt : 0.f;
-#pragma unroll
-  for (int i = 0; i < D / 32; ++i) a.out[row * D + i * 32 + lane] = __float2bfloat16_rn(acc[i] * inv);
-  if (lane == 0) a.lse[((long long)b * a.Hq + head) * a.C + pos] = (mt + log2f(lt)) * LN2;
+  __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(a.out + row * D) + 2 * c4;
+  o[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+  o[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+  if (c4 == 0) a.lse[((long long)b * a.Hq + head) * a.C + pos] = (mt + log2f(lt)) * LN2;
 }
 
 int pick_splits(int B, int C, int Hq, int Hkv, int Pmax, int W) {
@@ -498,8 +496,8 @@ cudaError_t run(const dgi::AttnArgs& x, void* ws, cudaStream_t st) {
   attn_kernel<D><<<grid, CF::THREADS, CF::SMEM, st>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || a.splits == 1) return e;
-  const long long rows = (long long)x.B * x.C * x.Hq;
-  attn_combine_kernel<D><<<(int)((rows + 7) / 8), 256, 0, st>>>(a);
+  const long long threads = (long long)x.B * x.C * x.Hq * (D / 4);
+  attn_combine_kernel<D><<<(int)((threads + 255) / 256), 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -535,11 +533,10 @@ cudaError_t attn_combine(int B, int C, int Hq, int d, int splits, float* ws_o, f
   a.out = reinterpret_cast<__nv_bfloat16*>(out);
   a.lse = lse;
   const long long rows = (long long)B * C * Hq;
-  const int grid = (int)((rows + 7) / 8);
   if (d == 64)
-    attn_combine_kernel<64><<<grid, 256, 0, st>>>(a);
+    attn_combine_kernel<64><<<(int)((rows * 16 + 255) / 256), 256, 0, st>>>(a);
   else if (d == 512)
-    attn_combine_kernel<512><<<grid, 256, 0, st>>>(a);
+    attn_combine_kernel<512><<<(int)((rows * 128 + 255) / 256), 256, 0, st>>>(a);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();
