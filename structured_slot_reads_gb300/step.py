@@ -105,6 +105,26 @@ class DenoiseStep:
             self.ws_heads = _empty((dg.dg_workspace_bytes(self.dims, dg.DG_WS_HEADS, self.M),), u8, dev)
             self.ws_pe = _empty((dg.dg_workspace_bytes(self.dims, dg.DG_WS_PROBS_EMBED, self.M),), u8, dev)
 
+    # ------------------------------------------------------------- graphs
+    def capture(self, step_idx):
+        """Record step ``step_idx`` as a CUDA graph (once per step index: the noise
+        draws depend on it).  Call after one eager step, so every kernel's one-time
+        set-up has run; replaying the graph is the same work as ``run(step_idx)``."""
+        if not hasattr(self, "_graphs"):
+            self._graphs = {}
+        g = self._graphs.get(step_idx)
+        if g is None:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self.run(step_idx=step_idx)
+            self._graphs[step_idx] = g
+        return g
+
+    def replay(self, step_idx):
+        """Launch the captured graph of step ``step_idx``; returns the kernels it holds."""
+        self.capture(step_idx).replay()
+        return self.kernels_per_step()
+
     # ------------------------------------------------------------------ step
     def reset_state(self):
         self.committed.zero_()

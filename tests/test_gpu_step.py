@@ -197,3 +197,25 @@ def test_batched_step_with_slot_read_pass():
         if margins.slot_margins_ok(one, x["n_labels"][s:s + 1], shape.gate):
             assert host(st.chosen)[s] == want["chosen"][s]
             assert host(st.resampled)[s] == want["resampled"][s]
+
+
+def test_graph_replay_equals_eager_step():
+    """A captured step replays the same kernels: after one eager step from the same
+    state, the replayed step's outputs equal the eager ones bit for bit."""
+    shape, x, _ = _tiny_inputs(2)
+    st = DenoiseStep(shape, dev_bf16(x["w"]), dev_bf16(x["e"]), seed=0)
+    _load(st, x)
+    st.run(step_idx=0)                      # one eager step: one-time set-up done
+    torch.cuda.synchronize()
+    _load(st, x)
+    st.run(step_idx=1)
+    torch.cuda.synchronize()
+    eager = {k: host(getattr(st, k)).copy() for k in ("lse", "ent", "commit", "tokens", "e_sc", "h",
+                                                        "chosen", "q_avg", "attn_out")}
+    _load(st, x)
+    st.capture(1)
+    _load(st, x)                            # capture does not execute: state is reloaded
+    st.replay(1)
+    torch.cuda.synchronize()
+    for k, v in eager.items():
+        assert np.array_equal(host(getattr(st, k)), v), k
