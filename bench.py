@@ -731,7 +731,7 @@ def reference_arm(args, rank):
     times = []
     sample = ""
     for i in range(args.warmup + args.steps):
-        v, sample, _ = oracle_sample(shape, data, target_rows=4, heads=1, seed=i)
+        v, sample, _ = oracle_sample(shape, data, target_rows=16, heads=1, seed=i)
         if i >= args.warmup:
             times.append(1.0 / v)
     t = sum(times)

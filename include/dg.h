@@ -376,6 +376,15 @@ size_t dg_workspace_bytes(const dg_dims* dims, int which, int rows);
 /* Row length (elements) of the probability buffer dg_denoise_heads writes for
  * a vocabulary of V: V rounded up to a multiple of 64; 0 if V < 1. */
 size_t dg_probs_ld(int V);
+/* Diagnostic of the device status path: one warp waits on a shared-memory
+ * barrier that nothing arrives on, under the same kind of bound as every wait
+ * inside the library's kernels, here limit_ns of wall time (1 ns .. 1 s).
+ * When the bound passes the kernel sets DG_DEV_TIMEOUT in the status word and
+ * returns, leaving the context usable; *waited_us (device memory) receives the
+ * time it waited.  No counterpart on the pages: it exists so that the timeout
+ * path can be exercised without a fault. */
+int dg_check_wait_timeout(int64_t limit_ns, int32_t* waited_us, void* stream);
+
 /* Copy the device status word into *status_out (host) after the work already
  * on `stream` finishes; this call synchronises that stream. */
 int dg_get_status(void* stream, int32_t* status_out);

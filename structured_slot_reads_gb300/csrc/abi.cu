@@ -536,6 +536,12 @@ int dg_attn_mixed(const dg_dims* d, const int32_t* mode, const int32_t* rows_len
   return launch_result(dgi::attn_decode_tc(a, workspace, static_cast<cudaStream_t>(stream)));
 }
 
+int dg_check_wait_timeout(int64_t limit_ns, int32_t* waited_us, void* stream) {
+  if (limit_ns < 1 || limit_ns > 1000000000LL || !waited_us) return DG_ERR_ARG;
+  return launch_result(dgi::check_wait_timeout((uint64_t)limit_ns, waited_us,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
 int dg_quantize_rows_e4m3(const uint16_t* x, int rows, int cols, uint8_t* q, float* scale,
                           void* stream) {
   if (rows < 0 || cols < 1) return DG_ERR_ARG;

@@ -114,6 +114,8 @@ cudaError_t slot_finish_wide(const uint16_t* rows, const float* inv_t_rows, cons
                              float gate, float* q_avg, float* h_slot, int32_t* chosen,
                              float* lp_draws, uint8_t* resampled, int32_t* n_reads,
                              cudaStream_t st);
+// Diagnostic of the bounded-wait path (see dg_check_wait_timeout).
+cudaError_t check_wait_timeout(uint64_t limit_ns, int* waited_us, cudaStream_t st);
 cudaError_t ask_if_select(const int32_t* chosen1, int S1, const int32_t* cond_slot,
                           const int32_t* cond_value, const int32_t* q_owner,
                           const int32_t* q_label_ids, const int32_t* q_n_labels, int Q, int S2,

@@ -379,6 +379,41 @@ __global__ void canvas_update_kernel(const __nv_bfloat16* h0, const float* e_sc,
 }
 
 
+// Diagnostic: one warp waits on an mbarrier that nothing arrives on, with a
+// limit of `limit_ns` of %globaltimer; when the limit passes it sets
+// DG_DEV_TIMEOUT (bit 0) and returns, as every bounded wait of the library does.
+__global__ void wait_timeout_kernel(uint64_t limit_ns, int* status, int* waited) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(&bar)))
+                 : "memory");
+  }
+  __syncwarp();
+  if (threadIdx.x != 0) return;
+  uint64_t t0, t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  const uint32_t addr = static_cast<uint32_t>(__cvta_generic_to_shared(&bar));
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(addr)
+        : "memory");
+    if (ok) break;  // never: no thread arrives
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 > limit_ns) {
+      atomicOr(status, 1 /* DG_DEV_TIMEOUT */);
+      break;
+    }
+  }
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  *waited = (int)((t - t0) / 1000);  // microseconds
+}
+
 }  // namespace
 
 namespace dgi {
@@ -473,6 +508,11 @@ cudaError_t commit(int B, int C, const float* entropy, const int32_t* argmax,
   commit_kernel<<<B, threads, (size_t)C * 12, st>>>(C, entropy, argmax, cand, gamma,
                                                      committed_state, token_state, commit_out,
                                                      tokens, n_commit);
+  return cudaGetLastError();
+}
+
+cudaError_t check_wait_timeout(uint64_t limit_ns, int* waited_us, cudaStream_t st) {
+  wait_timeout_kernel<<<1, 32, 0, st>>>(limit_ns, status_ptr(), waited_us);
   return cudaGetLastError();
 }
 

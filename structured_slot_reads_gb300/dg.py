@@ -63,6 +63,7 @@ _SIGS = {
                           P, Z, P],
     "dg_prefill_attn": [DP, P, P, P, P, P, P, P, I, I, I, P, P, P, Z, P],
     "dg_attn_mixed": [DP, P, P, P, P, P, P, P, P, I, I, I, P, P, P, P, Z, P],
+    "dg_check_wait_timeout": [ctypes.c_int64, P, P],
     "dg_quantize_rows_e4m3": [P, I, I, P, P, P],
     "dg_lmhead_logsoftmax_entropy_fp8": [DP, P, P, I, P, P, P, P, P, P, P, P, Z, P],
     "dg_commit": [DP, P, P, P, P, P, P, P, P, P, P],
@@ -202,6 +203,10 @@ def dg_attn_mixed(dims, mode, rows_len, q, kc, vc, kenc, venc, page_table, pages
                                _p(kenc), _p(venc), _p(page_table), pages_per_req, n_pages,
                                page_size, _p(prompt_len), _p(out), _p(lse), _p(workspace),
                                _nbytes(workspace), _s(stream))
+
+
+def dg_check_wait_timeout(limit_ns, waited_us, stream=None):
+    return lib().dg_check_wait_timeout(int(limit_ns), _p(waited_us), _s(stream))
 
 
 def dg_quantize_rows_e4m3(x, rows, cols, q, scale, stream=None):

@@ -216,3 +216,9 @@ def test_mixed_attention_validates(lib):
                             stream=0) == dg.DG_ERR_SHAPE
     assert dg.dg_attn_mixed(d, 16, 16, 16, 16, 16, 16, 16, 16, 2, 10, 24, 16, 16, 16, None,
                             stream=0) == dg.DG_ERR_SHAPE   # 24-key pages: not on this kernel
+
+
+def test_wait_timeout_diagnostic_validates_its_limit(lib):
+    assert dg.dg_check_wait_timeout(0, 16, stream=0) == dg.DG_ERR_ARG
+    assert dg.dg_check_wait_timeout(2_000_000_000, 16, stream=0) == dg.DG_ERR_ARG
+    assert dg.dg_check_wait_timeout(1000, None, stream=0) == dg.DG_ERR_ARG
