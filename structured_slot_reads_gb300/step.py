@@ -29,6 +29,37 @@ def _empty(shape, dtype, device):
     return torch.empty(tuple(shape), dtype=dtype, device=device)
 
 
+class Buffers(dict):
+    """Named tensors that are views of one contiguous byte buffer, ``arena``
+    (256-byte aligned slices), so a whole set moves in one copy."""
+
+    def __init__(self, arena, views):
+        super().__init__(views)
+        self.arena = arena
+
+
+def _layout(specs):
+    """Offsets of (name, shape, dtype) entries in an arena; returns (entries, bytes)."""
+    off, out = 0, []
+    for name, shape, dt in specs:
+        n = 1
+        for x in shape:
+            n *= int(x)
+        nb = n * torch.empty((), dtype=dt).element_size()
+        out.append((name, tuple(int(x) for x in shape), dt, off, nb))
+        off = (off + nb + 255) // 256 * 256
+    return out, max(off, 256)
+
+
+def _carve(layout, device, pin=False):
+    entries, total = layout
+    arena = (torch.empty(total, dtype=torch.uint8, pin_memory=True) if pin
+             else torch.empty(total, dtype=torch.uint8, device=device))
+    views = {name: arena[off:off + nb].view(dt).view(shape)
+             for name, shape, dt, off, nb in entries}
+    return Buffers(arena, views)
+
+
 class DenoiseStep:
     def __init__(self, shape, w, e, device="cuda", with_slots=True, seed=0, fused=True):
         self.shape = shape
@@ -39,17 +70,18 @@ class DenoiseStep:
         self.w, self.e = w, e
         bf, f32, i32, u8 = torch.bfloat16, torch.float32, torch.int32, torch.uint8
         dev = device
-        # per-request inputs
-        self.h0 = _empty((self.M, D), bf, dev)
+        # per-step inputs: views of one device arena (``self.inputs``)
+        dh = shape.d_head
+        self.in_layout = _layout([
+            ("h0", (self.M, D), bf), ("inv_t", (self.M,), f32),
+            ("q", (B, C, shape.Hq, dh), bf), ("kc", (B, C, shape.Hkv, dh), bf),
+            ("vc", (B, C, shape.Hkv, dh), bf), ("kenc", (B, shape.P, shape.Hkv, dh), bf),
+            ("venc", (B, shape.P, shape.Hkv, dh), bf), ("cand", (B, C), u8)])
+        self.inputs = _carve(self.in_layout, dev)
+        for k, v in self.inputs.items():
+            setattr(self, k, v)
         self.h = _empty((self.M, D), bf, dev)
-        self.inv_t = _empty((self.M,), f32, dev)
-        self.q = _empty((B, C, shape.Hq, shape.d_head), bf, dev)
-        self.kc = _empty((B, C, shape.Hkv, shape.d_head), bf, dev)
-        self.vc = _empty((B, C, shape.Hkv, shape.d_head), bf, dev)
-        self.kenc = _empty((B, shape.P, shape.Hkv, shape.d_head), bf, dev)
-        self.venc = _empty((B, shape.P, shape.Hkv, shape.d_head), bf, dev)
         self.prompt_len = torch.full((B,), shape.P, dtype=i32, device=dev)
-        self.cand = _empty((B, C), u8, dev)
         self.gamma = torch.full((B,), shape.gamma, dtype=f32, device=dev)
         # outputs / state
         self.attn_out = _empty((B, C, shape.Hq, shape.d_head), bf, dev)
@@ -60,9 +92,6 @@ class DenoiseStep:
         self.argmax = _empty((self.M,), i32, dev)
         self.committed = torch.zeros((B, C), dtype=u8, device=dev)
         self.tok_state = torch.full((B, C), -1, dtype=i32, device=dev)
-        self.commit = _empty((B, C), u8, dev)
-        self.tokens = _empty((B, C), i32, dev)
-        self.n_commit = _empty((B,), i32, dev)
         self.e_sc = _empty((self.M, D), f32, dev)
         self.ws_attn = _empty((max(dg.dg_workspace_bytes(self.dims, dg.DG_WS_ATTN, 0), 256),), u8, dev)
         # slots (same table for every request)
@@ -75,15 +104,21 @@ class DenoiseStep:
             self.slot_req = _empty((S,), i32, dev)
             self.label_ids = _empty((S, dg.MAX_LABELS), i32, dev)
             self.n_labels = _empty((S,), i32, dev)
-            self.q_avg = _empty((S, dg.MAX_LABELS), f32, dev)
-            self.h_slot = _empty((S,), f32, dev)
-            self.chosen = _empty((S,), i32, dev)
             self.lp_draws = _empty((S, shape.R, dg.MAX_LABELS), f32, dev)
             self.resampled = _empty((S,), u8, dev)
             self.n_reads = _empty((S,), i32, dev)
             self.noise_tok = _empty((S, shape.R), i32, dev)
             self.ws_slot = _empty((dg.dg_workspace_bytes(self.dims, dg.DG_WS_SLOT_READ,
                                                          S * shape.R),), u8, dev)
+        # the decisions read back each step: views of one device arena (``self.decisions``)
+        outs = [("commit", (B, C), u8), ("tokens", (B, C), i32), ("n_commit", (B,), i32)]
+        if self.with_slots:
+            outs += [("q_avg", (self.S, dg.MAX_LABELS), f32), ("h_slot", (self.S,), f32),
+                     ("chosen", (self.S,), i32)]
+        self.out_layout = _layout(outs)
+        self.decisions = _carve(self.out_layout, dev)
+        for k, v in self.decisions.items():
+            setattr(self, k, v)
         # fused path: one stream of W for the canvas rows, the slot draws (up to
         # 16 draw rows ride along; more go through their own dg_slot_read pass)
         # and the self-conditioning probabilities
@@ -216,28 +251,146 @@ class DenoiseStep:
 
     # ------------------------------------------------------- host round trip
     def host_buffers(self):
-        """Pinned host tensors holding one step's inputs and outputs."""
-        pin = dict(pin_memory=True)
-        ins = {k: torch.empty(getattr(self, k).shape, dtype=getattr(self, k).dtype, **pin)
-               for k in ("h0", "inv_t", "q", "kc", "vc", "kenc", "venc", "cand")}
-        outs = {k: torch.empty(getattr(self, k).shape, dtype=getattr(self, k).dtype, **pin)
-                for k in ("commit", "tokens", "n_commit")}
-        if self.with_slots:
-            for k in ("q_avg", "chosen", "h_slot"):
-                outs[k] = torch.empty(getattr(self, k).shape, dtype=getattr(self, k).dtype, **pin)
-        return ins, outs
+        """Pinned host buffers of one step's inputs and decisions, laid out as
+        the device arenas (``Buffers``: a dict of views plus ``.arena``)."""
+        return _carve(self.in_layout, None, pin=True), _carve(self.out_layout, None, pin=True)
 
     def upload(self, ins):
-        n = 0
-        for k, t in ins.items():
-            getattr(self, k).copy_(t, non_blocking=True)
-            n += t.numel() * t.element_size()
+        """Copy a step's inputs from host buffers; returns the bytes copied."""
+        if isinstance(ins, Buffers) and ins.arena.numel() == self.inputs.arena.numel():
+            self.inputs.arena.copy_(ins.arena, non_blocking=True)
+            n = ins.arena.numel()
+        else:
+            n = 0
+            for k, t in ins.items():
+                getattr(self, k).copy_(t, non_blocking=True)
+                n += t.numel() * t.element_size()
         self.h.copy_(self.h0)
         return n
 
     def download(self, outs):
+        """Copy the step's decisions into host buffers; returns the bytes copied."""
+        if isinstance(outs, Buffers) and outs.arena.numel() == self.decisions.arena.numel():
+            outs.arena.copy_(self.decisions.arena, non_blocking=True)
+            return outs.arena.numel()
         n = 0
         for k, t in outs.items():
             t.copy_(getattr(self, k), non_blocking=True)
             n += t.numel() * t.element_size()
         return n
+
+
+class HostPipeline:
+    """End-to-end steps with host transfers overlapped with compute.
+
+    ``submit(step_idx, ins, outs)`` enqueues one step whose inputs come from
+    the pinned host tensors ``ins`` (as from ``DenoiseStep.host_buffers``) and
+    whose decisions go to the pinned host tensors ``outs``:
+
+      upload stream    host -> staging set b (b = submission parity), once the
+                       step that last read set b has finished
+      compute stream   one CUDA graph of the step whose kernels read their
+                       inputs from staging set b and write the decisions to
+                       output staging set b (no device-side copies)
+      download stream  output staging set b -> ``outs``
+
+    So step i+1's inputs cross the link while step i computes, and step i's
+    decisions come back while step i+1 computes.  Every step still makes its
+    own host->device copy of all its inputs and its own device->host read of
+    its decisions.  The copies are asynchronous: ``ins`` must stay unchanged
+    and ``outs`` unread until ``sync()`` returns (give each in-flight step its
+    own host tensors to refill them earlier).  The decisions land in ``outs``
+    only (not in the step's own decision tensors); the carried state
+    (committed positions, tokens, canvas rows) is the step's, as with ``run``.  Graphs are captured on first
+    use, or ahead of time with ``prepare``; the step must have run once
+    eagerly before (one-time set-up of its kernels).
+    """
+
+    def __init__(self, step, use_graphs=True):
+        self.step = step
+        self.use_graphs = use_graphs
+        self.up = torch.cuda.Stream(device=step.h.device)
+        self.down = torch.cuda.Stream(device=step.h.device)
+        dev = step.h.device
+        self.stage_in = [_carve(step.in_layout, dev) for _ in range(2)]
+        self.stage_out = [_carve(step.out_layout, dev) for _ in range(2)]
+        ev = lambda: [torch.cuda.Event() for _ in range(2)]
+        self.ev_up, self.ev_in_free, self.ev_done, self.ev_out_free = ev(), ev(), ev(), ev()
+        self.graphs = {}
+        self.n = 0
+
+    def _body(self, step_idx, b):
+        """The step with its inputs read from staging set b and its decisions
+        written there: the input and decision tensors are bound to the staging
+        arenas while the step is enqueued (or captured), then restored."""
+        st = self.step
+        saved = {k: getattr(st, k) for k in (*st.inputs, *st.decisions)}
+        try:
+            for k, v in (*self.stage_in[b].items(), *self.stage_out[b].items()):
+                setattr(st, k, v)
+            st.h.copy_(st.h0)
+            st.run(step_idx)
+        finally:
+            for k, v in saved.items():
+                setattr(st, k, v)
+
+    def _graph(self, step_idx, b):
+        g = self.graphs.get((step_idx, b))
+        if g is None:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self._body(step_idx, b)
+            self.graphs[(step_idx, b)] = g
+        return g
+
+    def prepare(self, step_indices):
+        """Capture the graphs of the next submissions (step indices in order)."""
+        for j, i in enumerate(step_indices):
+            self._graph(i, (self.n + j) & 1)
+
+    def submit(self, step_idx, ins, outs):
+        """Enqueue one step; returns (host->device bytes, device->host bytes)."""
+        b = self.n & 1
+        main = torch.cuda.current_stream()
+        with torch.cuda.stream(self.up):
+            self.up.wait_event(self.ev_in_free[b])
+            h2d = _copy_set(self.stage_in[b], ins)
+            self.ev_up[b].record(self.up)
+        main.wait_event(self.ev_up[b])
+        main.wait_event(self.ev_out_free[b])
+        if self.use_graphs:
+            self._graph(step_idx, b).replay()
+        else:
+            self._body(step_idx, b)
+        self.ev_in_free[b].record(main)
+        self.ev_done[b].record(main)
+        with torch.cuda.stream(self.down):
+            self.down.wait_event(self.ev_done[b])
+            d2h = _copy_set(outs, self.stage_out[b])
+            self.ev_out_free[b].record(self.down)
+        self.n += 1
+        return h2d, d2h
+
+    def join(self, stream=None):
+        """Make ``stream`` (default: current) wait for every enqueued transfer."""
+        s = stream or torch.cuda.current_stream()
+        s.wait_stream(self.up)
+        s.wait_stream(self.down)
+
+    def sync(self):
+        self.join()
+        torch.cuda.current_stream().synchronize()
+
+
+def _copy_set(dst, src):
+    """Copy a set of named tensors (one copy when both are arenas of one layout);
+    returns the bytes copied."""
+    if isinstance(src, Buffers) and isinstance(dst, Buffers) and \
+            src.arena.numel() == dst.arena.numel():
+        dst.arena.copy_(src.arena, non_blocking=True)
+        return src.arena.numel()
+    n = 0
+    for k, t in src.items():
+        dst[k].copy_(t, non_blocking=True)
+        n += t.numel() * t.element_size()
+    return n
