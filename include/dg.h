@@ -63,6 +63,7 @@ extern "C" {
 #define DG_WS_HEADS 5
 #define DG_WS_PROBS_EMBED 6
 #define DG_WS_PREFILL 7
+#define DG_WS_PROBS_EMBED8 8
 
 /* Problem dimensions.  B requests, C canvas tokens each, P_max the longest
  * prompt (encoder KV) length, Hq/Hkv query/KV heads (GQA, Hq % Hkv == 0),
@@ -237,6 +238,34 @@ int dg_lmhead_logsoftmax_entropy_fp8(const dg_dims* dims, const uint8_t* h8, con
                                      const float* inv_t, float* lse, float* entropy, float* maxz,
                                      int32_t* argmax, void* workspace, size_t workspace_bytes,
                                      void* stream);
+
+/* ---- next: the self-conditioning P . E on 8-bit operands -----------------
+ * The same deployments (8-bit weights and activations) applied to the second
+ * GEMM of the step, e_i = sum_v p_iv E[v] (24-ai.news, "Token commit
+ * mechanism").  The scale of E must sit outside the sum over the vocabulary,
+ * so E is quantised per d_model column and stored transposed:
+ * dg_quantize_cols_e4m3: scale[c] = max_r |x[r, c]| / 448 (1 for a zero
+ * column), qt[c, r] = e4m3(x[r, c] / scale[c]) (fp32 division, round to nearest
+ * even, saturating).  x [rows, cols] bf16;  qt [cols, rows] uint8;  scale [cols]
+ * fp32 (also used as scratch during the call).  A one-time preparation of E. */
+int dg_quantize_cols_e4m3(const uint16_t* x, int rows, int cols, uint8_t* qt, float* scale,
+                          void* stream);
+
+/* out[i, c] = row_scale[i] * p_scale[i] * e_scale[c] * sum_v p8[i, v] e8t[c, v]
+ * (e4m3 products accumulated in fp32 by the tensor cores, split over the
+ * vocabulary and summed in a fixed order).  With p8/p_scale the per-row e4m3
+ * quantisation of dg_denoise_heads' probabilities (dg_quantize_rows_e4m3),
+ * row_scale its prob_scale, and e8t/e_scale from dg_quantize_cols_e4m3(e), out
+ * is the expected embedding on 8-bit operands.
+ *   p8 [M, V] uint8;  p_scale [M] fp32;  row_scale [M] fp32 or NULL (1);
+ *   e8t [d_model, V] uint8;  e_scale [d_model] fp32;  out [M, d_model] fp32.
+ * V must be a multiple of 16 and d_model of 4; p8, e8t, e_scale and out
+ * 16-byte aligned (else DG_ERR_SHAPE / DG_ERR_ARG).
+ *   workspace: dg_workspace_bytes(dims, DG_WS_PROBS_EMBED8, M) bytes. */
+int dg_selfcond_from_probs8(const dg_dims* dims, const uint8_t* p8, const float* p_scale,
+                            const float* row_scale, int M, const uint8_t* e8t,
+                            const float* e_scale, float* out, void* workspace,
+                            size_t workspace_bytes, void* stream);
 
 /* ---- next: one wide read in place of the two-stage path -----------------
  * sotaaz.com, "The server accepts at most 26 alternatives per question": the

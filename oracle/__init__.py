@@ -30,7 +30,8 @@ Functions with no pin other than their own definition are marked
 "parity unpinned" in their docstring; at present there are none.
 """
 from .philox import philox4x32_10, noise_tokens, seed_key  # noqa: F401
-from .quant import dequantize_rows, e4m3_value, quantize_rows_e4m3  # noqa: F401
+from .quant import (dequantize_rows, e4m3_value, quantize_cols_e4m3, quantize_rows_e4m3,  # noqa: F401
+                    selfcond_fp8)
 from .step import (  # noqa: F401
     bf16_round,
     attn_decode,

@@ -58,3 +58,27 @@ def quantize_rows_e4m3(x):
 def dequantize_rows(q, scale):
     """q * scale per row, float64."""
     return decode_e4m3(q) * np.asarray(scale, np.float64)[:, None]
+
+
+def quantize_cols_e4m3(x):
+    """Per-column e4m3 quantisation of a bf16-valued float32 matrix [R, C], stored
+    transposed: column c of x is row c of the result.
+
+    Returns (qt uint8 [C, R], scale float32 [C]) with scale[c] = amax_r |x[r, c]| / 448
+    (1 for a zero column) and qt[c, r] = e4m3(x[r, c] / scale[c])."""
+    return quantize_rows_e4m3(np.ascontiguousarray(np.asarray(x, np.float32).T))
+
+
+def selfcond_fp8(p8, p_scale, row_scale, e8t, e_scale):
+    """Expected embedding on 8-bit operands, float64.
+
+    24-ai.news, "Token commit mechanism": e_i = sum_v p_iv E[v].  With the
+    probabilities quantised per row (p8, p_scale; row_scale the row's 1/S, or
+    None for 1) and E quantised per d_model column and transposed (e8t, e_scale):
+    out[i, c] = row_scale[i] * p_scale[i] * e_scale[c] * sum_v p8[i, v] e8t[c, v]."""
+    p = decode_e4m3(p8)
+    et = decode_e4m3(e8t)
+    rs = np.asarray(p_scale, np.float64)
+    if row_scale is not None:
+        rs = rs * np.asarray(row_scale, np.float64)
+    return rs[:, None] * (p @ et.T) * np.asarray(e_scale, np.float64)[None, :]

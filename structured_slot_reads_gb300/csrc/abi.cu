@@ -248,6 +248,9 @@ size_t dg_workspace_bytes(const dg_dims* d, int which, int rows) {
     case DG_WS_PROBS_EMBED:
       if (!dims_lm(d) || rows < 1) return 0;
       return dgi::probs_embed_ws_bytes(rows, d->V, d->d_model);
+    case DG_WS_PROBS_EMBED8:
+      if (!dims_lm(d) || rows < 1) return 0;
+      return dgi::probs_embed8_ws_bytes(rows, d->V, d->d_model);
     case DG_WS_PREFILL:
       if (!prefill_dims_ok(d)) return 0;
       return dgi::attn_tc_ws_bytes(d->B, d->P_max, 0, d->Hq, d->Hkv, d->P_max);
@@ -548,6 +551,30 @@ int dg_quantize_rows_e4m3(const uint16_t* x, int rows, int cols, uint8_t* q, flo
   if (rows > 0 && (!x || !q || !scale)) return DG_ERR_ARG;
   return launch_result(
       dgi::quantize_rows_e4m3(x, rows, cols, q, scale, static_cast<cudaStream_t>(stream)));
+}
+
+int dg_quantize_cols_e4m3(const uint16_t* x, int rows, int cols, uint8_t* qt, float* scale,
+                          void* stream) {
+  if (rows < 0 || cols < 1) return DG_ERR_ARG;
+  if (rows > 0 && (!x || !qt || !scale || !aligned(scale, 4))) return DG_ERR_ARG;
+  return launch_result(
+      dgi::quantize_cols_e4m3(x, rows, cols, qt, scale, static_cast<cudaStream_t>(stream)));
+}
+
+int dg_selfcond_from_probs8(const dg_dims* d, const uint8_t* p8, const float* p_scale,
+                            const float* row_scale, int M, const uint8_t* e8t,
+                            const float* e_scale, float* out, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  if (!d || M < 1) return DG_ERR_ARG;
+  if (!dims_lm(d) || d->V % 16 || d->d_model % 4) return DG_ERR_SHAPE;
+  if (!p8 || !p_scale || !e8t || !e_scale || !out) return DG_ERR_ARG;
+  if (!aligned(p8, 16) || !aligned(e8t, 16) || !aligned(e_scale, 16) || !aligned(out, 16))
+    return DG_ERR_ARG;
+  const size_t need = dg_workspace_bytes(d, DG_WS_PROBS_EMBED8, M);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DG_ERR_WORKSPACE;
+  return launch_result(dgi::probs_embed8(p8, p_scale, row_scale, M, e8t, e_scale, d->V,
+                                         d->d_model, out, workspace,
+                                         static_cast<cudaStream_t>(stream)));
 }
 
 int dg_lmhead_logsoftmax_entropy_fp8(const dg_dims* d, const uint8_t* h8, const float* h_scale,

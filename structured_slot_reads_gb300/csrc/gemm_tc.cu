@@ -41,6 +41,7 @@ constexpr int EPI_PROBS = 1;
 constexpr int EPI_ACCUM = 2;
 constexpr int EPI_ACCUM_MN = 3;  // as EPI_ACCUM with B given N-contiguous ([K, N] row-major)
 constexpr int EPI_STATS8 = 4;    // as EPI_STATS with e4m3 operands and per-row scales
+constexpr int EPI_ACCUM8 = 5;    // as EPI_ACCUM with e4m3 operands (both K-major) and scales
 constexpr int RING_BUDGET = 232448 - 1024 - 512;  // operand rings (227 KB - alignment - barriers)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
@@ -59,8 +60,8 @@ struct GemmParams {
   int kb_per_split;  // ACCUM: k-blocks per range
   const float* inv_t;
   const float* lse;
-  const float* row_scale;  // STATS8: scale of each A row
-  const float* col_scale;  // STATS8: scale of each B row (vocabulary entry)
+  const float* row_scale;  // STATS8 / ACCUM8: scale of each A row
+  const float* col_scale;  // STATS8 / ACCUM8: scale of each B row (an output column)
   float* part;            // STATS: 5 x [cpg][M]; ACCUM: [k_split][M][N]
   __nv_bfloat16* probs;   // PROBS: [M][ldp]
   long long ldp;
@@ -104,9 +105,9 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
   constexpr int PRODUCER_WARP = CF::EPI_WARPS;
   constexpr int MMA_WARP = CF::EPI_WARPS + 1;
   constexpr bool B_MN = EPI == EPI_ACCUM_MN;
-  constexpr bool ACCUM = EPI == EPI_ACCUM || B_MN;
-  constexpr bool F8 = EPI == EPI_STATS8;
-  constexpr bool STATS = EPI == EPI_STATS || F8;
+  constexpr bool ACCUM = EPI == EPI_ACCUM || B_MN || EPI == EPI_ACCUM8;
+  constexpr bool F8 = EPI == EPI_STATS8 || EPI == EPI_ACCUM8;
+  constexpr bool STATS = EPI == EPI_STATS || EPI == EPI_STATS8;
   // a stage holds 128-byte operand rows: 64 bf16 or 128 e4m3 values of K
   constexpr int KB = F8 ? 128 : BK;
   constexpr uint32_t IDESC_F8 = idesc_e4m3_f32(BM, BN);
@@ -301,7 +302,7 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
         const int n0 = t * BN + c * 32;
         if (!row_ok) continue;
         if (F8) {
-          // unscaled e4m3 products -> h.w: times the row's and each column's scale
+          // unscaled e4m3 products: times the row's and each column's scale
 #pragma unroll
           for (int j = 0; j < 32; j += 4) {
             float4 cs = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -597,11 +598,12 @@ cudaError_t run_stats_fp8(const uint8_t* h8, const float* h_scale, int M, const 
 constexpr int ACC_BN = 256;
 
 // Split of the vocabulary (the K of P . E) over CTAs: every split non-empty.
-void accum_split(int M, int V, int D, int* k_split, int* kb_per_split) {
+// kb = K-block width (64 bf16 or 128 e4m3 values).
+void accum_split(int M, int V, int D, int* k_split, int* kb_per_split, int kb = BK) {
   const int mt = stats_mt(M);
   const int groups = (M + mt * BM - 1) / (mt * BM);
   const int n_tiles = (D + ACC_BN - 1) / ACC_BN;
-  const int total_kb = (V + BK - 1) / BK;
+  const int total_kb = (V + kb - 1) / kb;
   int ks = std::max(1, dgi::num_sms() / (groups * n_tiles));
   ks = std::min(ks, total_kb);
   const int kbps = (total_kb + ks - 1) / ks;
@@ -698,6 +700,45 @@ cudaError_t probs_embed(const uint16_t* probs, size_t ldp, const float* row_scal
   const int grid = groups * p.n_tiles * p.k_split;
   cudaError_t err = (mt == 1) ? launch_gemm<1, ACC_BN, EPI_ACCUM_MN>(ta, tb, p, grid, st)
                               : launch_gemm<2, ACC_BN, EPI_ACCUM_MN>(ta, tb, p, grid, st);
+  if (err != cudaSuccess) return err;
+  const long long n4 = (long long)M * D / 4;
+  const int blocks = (int)std::min<long long>((n4 + 255) / 256, 4LL * num_sms());
+  split_reduce_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(part), p.k_split,
+                                              n4, D, row_scale, reinterpret_cast<float4*>(out));
+  return cudaGetLastError();
+}
+
+size_t probs_embed8_ws_bytes(int M, int V, int D) {
+  int ks, kbps;
+  accum_split(M, V, D, &ks, &kbps, 128);
+  return align_up((size_t)ks * M * D * sizeof(float), 256);
+}
+
+// P . E on e4m3 operands: p8 [M, V] (one scale per row), e8t = E transposed
+// [D, V] (one scale per d_model column), both K-major with K = the vocabulary.
+// out = row_scale * p_scale * e_scale * sum_v p8 e8t, split-K over the vocabulary.
+cudaError_t probs_embed8(const uint8_t* p8, const float* p_scale, const float* row_scale, int M,
+                         const uint8_t* e8t, const float* e_scale, int V, int D, float* out,
+                         void* ws, cudaStream_t st) {
+  const int mt = stats_mt(M);
+  const int groups = (M + mt * BM - 1) / (mt * BM);
+  float* part = static_cast<float*>(ws);
+  CUtensorMap ta, tb;
+  if (!make_tmap_u8_2d(&ta, p8, V, M, (uint64_t)V, 128, BM)) return cudaErrorInvalidValue;
+  if (!make_tmap_u8_2d(&tb, e8t, V, D, (uint64_t)V, 128, ACC_BN)) return cudaErrorInvalidValue;
+  GemmParams p{};
+  p.M = M;
+  p.N = D;
+  p.K = V;
+  p.n_tiles = (D + ACC_BN - 1) / ACC_BN;
+  accum_split(M, V, D, &p.k_split, &p.kb_per_split, 128);
+  p.row_scale = p_scale;
+  p.col_scale = e_scale;
+  p.part = part;
+  p.status = status_ptr();
+  const int grid = groups * p.n_tiles * p.k_split;
+  cudaError_t err = (mt == 1) ? launch_gemm<1, ACC_BN, EPI_ACCUM8>(ta, tb, p, grid, st)
+                              : launch_gemm<2, ACC_BN, EPI_ACCUM8>(ta, tb, p, grid, st);
   if (err != cudaSuccess) return err;
   const long long n4 = (long long)M * D / 4;
   const int blocks = (int)std::min<long long>((n4 + 255) / 256, 4LL * num_sms());

@@ -42,6 +42,12 @@ cudaError_t lmhead_stats_fp8(const uint8_t* h8, const float* h_scale, int M, con
 // Per-row e4m3 quantisation: scale = amax / 448 (1 for a zero row), q = e4m3(x / scale).
 cudaError_t quantize_rows_e4m3(const uint16_t* x, int rows, int cols, uint8_t* q, float* scale,
                                cudaStream_t st);
+cudaError_t quantize_cols_e4m3(const uint16_t* x, int rows, int cols, uint8_t* qt, float* scale,
+                               cudaStream_t st);
+size_t probs_embed8_ws_bytes(int M, int V, int D);
+cudaError_t probs_embed8(const uint8_t* p8, const float* p_scale, const float* row_scale, int M,
+                         const uint8_t* e8t, const float* e_scale, int V, int D, float* out,
+                         void* ws, cudaStream_t st);
 size_t selfcond_ws_bytes(int M, int V, int D);
 cudaError_t selfcond(const uint16_t* h, int M, const uint16_t* w, const uint16_t* e, int V,
                      int D, const float* inv_t, const float* lse, float* out, void* ws,

@@ -1,9 +1,12 @@
-// quant.cu -- e4m3 operands for the 8-bit lm-head pass: per-row scales.
+// quant.cu -- e4m3 operands of the 8-bit passes.
 //
 // A row x (bf16) becomes scale = amax|x| / 448 (the largest finite e4m3
 // value; 1 for an all-zero row) and q = e4m3(x / scale), rounded to nearest
 // even and saturated.  The lm-head pass multiplies the e4m3 products back by
-// the row scales of both operands.
+// the row scales of both operands.  For P . E the embedding table is
+// quantised per column instead (its scale must sit outside the sum over the
+// vocabulary) and stored transposed, [d_model, V], so that both operands of
+// that GEMM have the vocabulary contiguous.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -38,13 +41,180 @@ __global__ void quantize_rows_e4m3_kernel(const __nv_bfloat16* x, int cols, uint
     qr[i] = __nv_cvt_float_to_fp8(__bfloat162float(xr[i]) / sc, __NV_SATFINITE, __NV_E4M3);
 }
 
+// Long rows (the unnormalised probabilities, V wide): many blocks per row.
+// Block (row, chunk) covers QR_CHUNK values with 16-byte loads; the row maxima
+// go to amax_bits[row] (atomicMax on float bits, zero on entry).
+constexpr int QR_CHUNK = 8192;  // 256 threads x 4 loads x 8 bf16
+
+__global__ void row_amax_long_kernel(const __nv_bfloat16* x, int cols, unsigned int* amax_bits) {
+  const int row = blockIdx.y;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (long long)row * cols);
+  const int n8 = cols / 8;
+  const int i0 = blockIdx.x * (QR_CHUNK / 8);
+  const int i1 = min(n8, i0 + QR_CHUNK / 8);
+  float m = 0.f;
+  for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
+    const uint4 u = xr[i];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+      m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ float wmax[8];
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float a = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) a = fmaxf(a, wmax[w]);
+    atomicMax(amax_bits + row, __float_as_uint(a));
+  }
+}
+
+__device__ __forceinline__ float row_scale_of(unsigned int bits) {
+  const float a = __uint_as_float(bits);
+  return a > 0.f ? a / 448.f : 1.f;
+}
+
+__global__ void row_quantize_long_kernel(const __nv_bfloat16* x, int cols,
+                                         const unsigned int* amax_bits, uint8_t* q) {
+  const int row = blockIdx.y;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (long long)row * cols);
+  uint2* qr = reinterpret_cast<uint2*>(q + (long long)row * cols);
+  const float sc = row_scale_of(amax_bits[row]);
+  const int n8 = cols / 8;
+  const int i0 = blockIdx.x * (QR_CHUNK / 8);
+  const int i1 = min(n8, i0 + QR_CHUNK / 8);
+  for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
+    const uint4 u = xr[i];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    uint32_t out[2] = {0u, 0u};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+      const uint32_t b0 = __nv_cvt_float_to_fp8(f.x / sc, __NV_SATFINITE, __NV_E4M3);
+      const uint32_t b1 = __nv_cvt_float_to_fp8(f.y / sc, __NV_SATFINITE, __NV_E4M3);
+      out[k >> 1] |= (b0 | (b1 << 8)) << (16 * (k & 1));
+    }
+    qr[i] = make_uint2(out[0], out[1]);
+  }
+}
+
+__global__ void amax_to_row_scale_kernel(float* scale_io, int rows) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r < rows) scale_io[r] = row_scale_of(reinterpret_cast<const unsigned int*>(scale_io)[r]);
+}
+
+// Column maxima of |x| [rows, cols]: block = 64 columns x ROWS_PER_BLOCK rows,
+// thread (c, g) takes column c and every 4th row of the block; the block's
+// maxima go to amax_bits by atomicMax on the float bits (non-negative floats
+// order like their bit patterns).  amax_bits must be zero on entry.
+constexpr int QC_ROWS = 1024;
+
+__global__ void col_amax_kernel(const __nv_bfloat16* x, int rows, int cols,
+                                unsigned int* amax_bits) {
+  const int c = blockIdx.x * 64 + (threadIdx.x & 63);
+  const int g = threadIdx.x >> 6;  // 0..3
+  const int r0 = blockIdx.y * QC_ROWS;
+  const int r1 = min(rows, r0 + QC_ROWS);
+  __shared__ float red[4][64];
+  float m = 0.f;
+  if (c < cols)
+    for (int r = r0 + g; r < r1; r += 4)
+      m = fmaxf(m, fabsf(__bfloat162float(x[(long long)r * cols + c])));
+  red[g][threadIdx.x & 63] = m;
+  __syncthreads();
+  if (g == 0 && c < cols) {
+    const float a = fmaxf(fmaxf(red[0][threadIdx.x], red[1][threadIdx.x]),
+                          fmaxf(red[2][threadIdx.x], red[3][threadIdx.x]));
+    atomicMax(amax_bits + c, __float_as_uint(a));
+  }
+}
+
+__device__ __forceinline__ float col_scale_of(unsigned int bits) {
+  const float a = __uint_as_float(bits);
+  return a > 0.f ? a / 448.f : 1.f;
+}
+
+// qt[c, r] = e4m3(x[r, c] / scale[c]): a 64 x 64 tile through shared memory,
+// read along the columns of x and written along the rows of qt (16 bytes per
+// thread).
+__global__ void quantize_transpose_kernel(const __nv_bfloat16* x, int rows, int cols,
+                                          const unsigned int* amax_bits, uint8_t* qt) {
+  __shared__ __align__(16) uint8_t tile[64][64 + 16];
+  const int c0 = blockIdx.x * 64, r0 = blockIdx.y * 64;
+  const int tc = threadIdx.x & 63, tr = threadIdx.x >> 6;  // 4 rows per pass
+  const int c = c0 + tc;
+  const float sc = c < cols ? col_scale_of(amax_bits[c]) : 1.f;
+  for (int i = tr; i < 64; i += 4) {
+    const int r = r0 + i;
+    uint8_t q = 0;
+    if (r < rows && c < cols)
+      q = __nv_cvt_float_to_fp8(__bfloat162float(x[(long long)r * cols + c]) / sc,
+                                __NV_SATFINITE, __NV_E4M3);
+    tile[tc][i] = q;
+  }
+  __syncthreads();
+  // thread t writes column (t / 4), rows [16 (t % 4), +16)
+  const int oc = c0 + (threadIdx.x >> 2), orr = r0 + (threadIdx.x & 3) * 16;
+  if (oc >= cols) return;
+  const uint8_t* src = &tile[threadIdx.x >> 2][(threadIdx.x & 3) * 16];
+  uint8_t* dst = qt + (long long)oc * rows + orr;
+  if (orr + 16 <= rows && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0)) {
+    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+  } else {
+    for (int k = 0; k < 16 && orr + k < rows; ++k) dst[k] = src[k];
+  }
+}
+
+// scale[c] from the column maxima held in the same words.
+__global__ void amax_to_scale_kernel(float* scale_io, int cols) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c < cols)
+    scale_io[c] = col_scale_of(reinterpret_cast<const unsigned int*>(scale_io)[c]);
+}
+
 }  // namespace
 
 namespace dgi {
 
+cudaError_t quantize_cols_e4m3(const uint16_t* x, int rows, int cols, uint8_t* qt, float* scale,
+                               cudaStream_t st) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  // the scale array holds the column maxima (as float bits) until the last kernel
+  unsigned int* amax = reinterpret_cast<unsigned int*>(scale);
+  cudaError_t e = cudaMemsetAsync(amax, 0, (size_t)cols * sizeof(unsigned int), st);
+  if (e != cudaSuccess) return e;
+  const auto* xb = reinterpret_cast<const __nv_bfloat16*>(x);
+  col_amax_kernel<<<dim3((cols + 63) / 64, (rows + QC_ROWS - 1) / QC_ROWS), 256, 0, st>>>(
+      xb, rows, cols, amax);
+  quantize_transpose_kernel<<<dim3((cols + 63) / 64, (rows + 63) / 64), 256, 0, st>>>(
+      xb, rows, cols, amax, qt);
+  amax_to_scale_kernel<<<(cols + 255) / 256, 256, 0, st>>>(scale, cols);
+  return cudaGetLastError();
+}
+
 cudaError_t quantize_rows_e4m3(const uint16_t* x, int rows, int cols, uint8_t* q, float* scale,
                                cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
+  const bool vec = cols % 8 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(q) & 7) == 0 &&
+                   (reinterpret_cast<uintptr_t>(scale) & 3) == 0;
+  if (vec && cols >= 2 * QR_CHUNK && rows <= 65535) {
+    // the scale array holds the row maxima (as float bits) until the last kernel
+    unsigned int* amax = reinterpret_cast<unsigned int*>(scale);
+    cudaError_t e = cudaMemsetAsync(amax, 0, (size_t)rows * sizeof(unsigned int), st);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((cols + QR_CHUNK - 1) / QR_CHUNK, rows);
+    const auto* xb = reinterpret_cast<const __nv_bfloat16*>(x);
+    row_amax_long_kernel<<<grid, 256, 0, st>>>(xb, cols, amax);
+    row_quantize_long_kernel<<<grid, 256, 0, st>>>(xb, cols, amax, q);
+    amax_to_row_scale_kernel<<<(rows + 255) / 256, 256, 0, st>>>(scale, rows);
+    return cudaGetLastError();
+  }
   quantize_rows_e4m3_kernel<<<rows, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(x), cols,
                                                   q, scale);
   return cudaGetLastError();

@@ -21,7 +21,7 @@ DG_ERR_WORKSPACE = -6
 DG_DEV_TIMEOUT, DG_DEV_BAD_PAGE, DG_DEV_BAD_LABEL, DG_DEV_BAD_INDEX = 1, 2, 4, 8
 DG_DEV_RANGE = 16
 DG_WS_ATTN, DG_WS_LMHEAD, DG_WS_SLOT_READ, DG_WS_SELFCOND = 1, 2, 3, 4
-DG_WS_HEADS, DG_WS_PROBS_EMBED, DG_WS_PREFILL = 5, 6, 7
+DG_WS_HEADS, DG_WS_PROBS_EMBED, DG_WS_PREFILL, DG_WS_PROBS_EMBED8 = 5, 6, 7, 8
 DG_MAX_LABELS = MAX_LABELS = 26
 DG_MAX_WIDE_LABELS = 256
 DG_NOALLOC_MAX_ROWS = 512
@@ -65,6 +65,8 @@ _SIGS = {
     "dg_attn_mixed": [DP, P, P, P, P, P, P, P, P, I, I, I, P, P, P, P, Z, P],
     "dg_check_wait_timeout": [ctypes.c_int64, P, P],
     "dg_quantize_rows_e4m3": [P, I, I, P, P, P],
+    "dg_quantize_cols_e4m3": [P, I, I, P, P, P],
+    "dg_selfcond_from_probs8": [DP, P, P, P, I, P, P, P, P, Z, P],
     "dg_lmhead_logsoftmax_entropy_fp8": [DP, P, P, I, P, P, P, P, P, P, P, P, Z, P],
     "dg_commit": [DP, P, P, P, P, P, P, P, P, P, P],
     "dg_selfcond_embed": [DP, P, I, P, P, P, P, P, P, Z, P],
@@ -211,6 +213,17 @@ def dg_check_wait_timeout(limit_ns, waited_us, stream=None):
 
 def dg_quantize_rows_e4m3(x, rows, cols, q, scale, stream=None):
     return lib().dg_quantize_rows_e4m3(_p(x), rows, cols, _p(q), _p(scale), _s(stream))
+
+
+def dg_quantize_cols_e4m3(x, rows, cols, qt, scale, stream=None):
+    return lib().dg_quantize_cols_e4m3(_p(x), rows, cols, _p(qt), _p(scale), _s(stream))
+
+
+def dg_selfcond_from_probs8(dims, p8, p_scale, row_scale, M, e8t, e_scale, out, workspace,
+                            stream=None):
+    return lib().dg_selfcond_from_probs8(ctypes.byref(dims), _p(p8), _p(p_scale), _p(row_scale),
+                                         M, _p(e8t), _p(e_scale), _p(out), _p(workspace),
+                                         _nbytes(workspace), _s(stream))
 
 
 def dg_lmhead_logsoftmax_entropy_fp8(dims, h8, h_scale, M, w8, w_scale, inv_t, lse, entropy, maxz,

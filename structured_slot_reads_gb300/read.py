@@ -292,6 +292,52 @@ class LmHead:
         return 3
 
 
+class SelfCond:
+    """The expected-embedding GEMM of self-conditioning from given probabilities
+    (dg_denoise_heads' output layout: P~ [M, probs_ld] bf16 and prob_scale = 1/S),
+    on bf16 operands (dg_selfcond_from_probs) or on e4m3 operands
+    (dg_quantize_rows_e4m3 of the probabilities, then dg_selfcond_from_probs8; E
+    is quantised per d_model column and transposed once, when the object is made,
+    by dg_quantize_cols_e4m3)."""
+
+    def __init__(self, shape, e, M, fp8=False, device="cuda"):
+        f32, u8 = torch.float32, torch.uint8
+        V, D = shape.V, shape.D
+        self.shape, self.M, self.fp8 = shape, M, fp8
+        self.dims = dg.make_dims(d_model=D, V=V)
+        self.probs_ld = dg.dg_probs_ld(V)
+        self.probs = torch.empty((M, self.probs_ld), dtype=torch.bfloat16, device=device)
+        self.prob_scale = torch.empty(M, dtype=f32, device=device)
+        self.out = torch.empty((M, D), dtype=f32, device=device)
+        self.e = e
+        which = dg.DG_WS_PROBS_EMBED8 if fp8 else dg.DG_WS_PROBS_EMBED
+        self.ws = torch.empty(dg.dg_workspace_bytes(self.dims, which, M), dtype=u8, device=device)
+        if fp8:
+            if self.probs_ld != V:
+                raise ValueError("the 8-bit path quantises whole probability rows: V % 64 == 0")
+            self.e8t = torch.empty((D, V), dtype=u8, device=device)
+            self.e_scale = torch.empty(D, dtype=f32, device=device)
+            dg._check(dg.dg_quantize_cols_e4m3(e, V, D, self.e8t, self.e_scale),
+                      "dg_quantize_cols_e4m3")
+            self.p8 = torch.empty((M, V), dtype=u8, device=device)
+            self.p_scale = torch.empty(M, dtype=f32, device=device)
+
+    def run(self, step_idx=0, stream=None):
+        """Enqueue one pass; returns the number of library kernels."""
+        d, M, V = self.dims, self.M, self.shape.V
+        if not self.fp8:
+            dg._check(dg.dg_selfcond_from_probs(d, self.probs, self.probs_ld, self.prob_scale, M,
+                                                self.e, self.out, self.ws, stream),
+                      "dg_selfcond_from_probs")
+            return 2
+        dg._check(dg.dg_quantize_rows_e4m3(self.probs, M, V, self.p8, self.p_scale, stream),
+                  "dg_quantize_rows_e4m3")
+        dg._check(dg.dg_selfcond_from_probs8(d, self.p8, self.p_scale, self.prob_scale, M,
+                                             self.e8t, self.e_scale, self.out, self.ws, stream),
+                  "dg_selfcond_from_probs8")
+        return (3 if V >= 16384 else 1) + 2
+
+
 class MixedAttention:
     """One attention launch over decoder-mode requests (canvas rows over their prompt KV)
     and encoder-mode requests (causal over their prompt rows), dg_attn_mixed."""
