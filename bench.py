@@ -87,6 +87,12 @@ def max_over_ranks(value, world):
     return float(t.item())
 
 
+def job_rate(ms_max, steps, world):
+    """Whole-job throughput: the units all ranks processed (each rank runs `steps`
+    units of the same work) over the slowest rank's time."""
+    return world * steps / (ms_max / 1e3)
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -314,9 +320,9 @@ def gpu_arm(args, rank, world, local):
     f1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(f0.elapsed_time(f1), world)
-    e2e_value = world * args.e2e_steps / (e2e_ms / 1e3) if args.e2e_steps > 0 else None
+    e2e_value = job_rate(e2e_ms, args.e2e_steps, world) if args.e2e_steps > 0 else None
 
-    value = world * args.steps / (ms / 1e3)
+    value = job_rate(ms, args.steps, world)
     pk = peaks()
     work = call_work(shape, st)
     kernels = {}
@@ -579,7 +585,7 @@ def workload_arm(args, rank, world, local):
     dg.dg_clear_status()
     ms, per_call, launches, clk = timed_steps(args, run, calls, local, world)
     status = dg.dg_get_status()
-    steps_per_s = world * args.steps / (ms / 1e3)
+    steps_per_s = job_rate(ms, args.steps, world)
     pk = peaks()
     V, D, R = shape.V, shape.D, shape.R
     Wb = V * D * 2
