@@ -55,6 +55,8 @@ constexpr int BAR_BYTES = 256;
 constexpr int SMEM_BYTES = 1024 + Q_BYTES + NSLOT * UNIT + BAR_BYTES;
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32_bmn(BM, 128);
+constexpr uint32_t IDESC_QK_PAIR = idesc_bf16_f32(2 * BM, BN);
+constexpr uint32_t IDESC_PV_PAIR = idesc_bf16_f32_bmn(2 * BM, DH);
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 constexpr float LAZY = 8.f;             // log2 headroom before O is rescaled
@@ -148,16 +150,21 @@ __device__ __forceinline__ uint32_t chunk_mask(int c, int lo, int hi, uint32_t b
 // Softmax and output roles.  Warps w and w + 4 share query rows 32 (w % 4) .. +31
 // (their TMEM lane quarter); warp half h = w / 4 takes keys [64 h, 64 h + 64) of
 // every tile and output columns [128 h, 128 h + 128) of this CTA's 256.
+// In the CTA-pair kernel the two CTAs hold consecutive row blocks of one pair
+// tile (row_off = rank x 128/G positions) and the probabilities-ready barrier is
+// the even CTA's (pready_c = its shared::cluster addresses).
+template <bool PAIR>
 __device__ __forceinline__ void softmax_and_store(const TcArgs& a, const Tiles& T, int n, int b,
                                                   int g, int dh, int split, int warp, int lane,
                                                   uint32_t tmem_base, uint64_t* sfull_bar,
                                                   uint64_t* pready_bar, uint64_t* pv_bar,
                                                   uint64_t* pair_bar, volatile int* abort_flag,
-                                                  float* xch) {
+                                                  float* xch, int row_off, uint32_t pready_c0,
+                                                  uint32_t pready_c1) {
   constexpr unsigned FULL = 0xffffffffu;
   const int quarter = warp & 3, half = warp >> 2;
   const int r = quarter * 32 + lane;
-  const int lp = r / a.G;
+  const int lp = row_off + r / a.G;
   const int pos = T.p0 + lp;
   const bool row_ok = lp < T.npos && pos < T.len;
   const int head = g * a.G + r % a.G;
@@ -262,7 +269,10 @@ __device__ __forceinline__ void softmax_and_store(const TcArgs& a, const Tiles& 
     l += psum;
     tmem_st_wait();
     tc_fence_before();
-    mbar_arrive(&pready_bar[j & 1]);
+    if constexpr (PAIR)
+      mbar_arrive_cluster((j & 1) ? pready_c1 : pready_c0);
+    else
+      mbar_arrive(&pready_bar[j & 1]);
   }
   // the last two P V products: wait phase n-2 first, so that the parity wait for
   // phase n-1 cannot be satisfied by an older phase
@@ -322,12 +332,18 @@ __device__ __forceinline__ void softmax_and_store(const TcArgs& a, const Tiles& 
   }
 }
 
-__global__ void __launch_bounds__(THREADS, 1)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
-                   const __grid_constant__ CUtensorMap tmKe,
-                   const __grid_constant__ CUtensorMap tmVe,
-                   const __grid_constant__ CUtensorMap tmKc,
-                   const __grid_constant__ CUtensorMap tmVc, TcArgs a) {
+// The kernel body.  PAIR: a cluster of two CTAs shares each MMA (cta_group::2,
+// M = 256): CTA rank r holds query rows [128 r, 128 r + 128) of a 256-row pair
+// tile, half of every key tile's K (keys [64 r, 64 r + 64), all 512 head
+// columns: two ring units) and half of its V columns (this output half's
+// columns [128 r, 128 r + 128): one unit), so one key tile (K and V) is three
+// units, the whole ring: V(j) waits in one slot while K(j+1) fills the others.
+template <bool PAIR>
+__device__ __forceinline__ void attn_body(const CUtensorMap& tmQ, const CUtensorMap& tmKe,
+                                          const CUtensorMap& tmVe, const CUtensorMap& tmKc,
+                                          const CUtensorMap& tmVc, const TcArgs& a) {
+  constexpr int KU = PAIR ? 2 : K_UNITS;  // ring units of K per tile
+  constexpr int VU = PAIR ? 1 : V_UNITS;  // ring units of V per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -349,7 +365,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  int bid = blockIdx.x;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  int bid = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int split = bid % a.splits;
   bid /= a.splits;
   const int dh = bid & 1;
@@ -368,7 +385,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(q_bar, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sfull_bar[i], 1);
-      mbar_init(&pready_bar[i], SOFT_WARPS * 32);
+      // the softmax threads of both CTAs arrive on the even CTA's barrier
+      mbar_init(&pready_bar[i], (PAIR ? 2 : 1) * SOFT_WARPS * 32);
     }
     mbar_init(pv_bar, 1);
     mbar_init(drain_bar, 1);
@@ -377,8 +395,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     fence_barrier_init();
   }
   if (warp == MMA_WARP) {
-    tmem_alloc(tmem_slot, TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(tmem_slot, TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   if (warp == PRODUCER_WARP && lane == 0) {
     prefetch_tmap(&tmQ);
@@ -388,76 +411,112 @@ __global__ void __launch_bounds__(THREADS, 1)
     prefetch_tmap(&tmVc);
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync();
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const Tiles T = tiles_of(a, b, qb, split);
   const int n = T.t_end - T.t_begin;
+  const int npos_cta = BM / a.G;                 // canvas positions of one CTA's rows
+  const int row_off = (int)rank * npos_cta;     // this CTA's first position in the tile
+  // barrier addresses the loads complete on: the even CTA's in a pair
+  auto bar_of = [&](uint64_t* bar) -> uint32_t {
+    return PAIR ? mapa_shared(smem_u32(bar), 0) : smem_u32(bar);
+  };
 
   if (warp == PRODUCER_WARP) {
     // The whole warp produces: lane 0 waits on the ring and arms the barriers;
-    // for paged prompts lane i loads page i of the tile (up to 16 pages of a
-    // 128-key tile), so the page indices and the many small boxes go out in parallel.
+    // for paged prompts lane i loads page i of a box (up to 16 pages of a
+    // 128-key box), so the page indices and the many small boxes go out in parallel.
     constexpr unsigned FULL = 0xffffffffu;
     int slot = 0;
     uint32_t phase = 0, issued = 0, last_phase = 0;
     bool ok = true;
     if (n > 0 && lane == 0) {
-      mbar_arrive_expect_tx(q_bar, Q_BYTES);
-      for (int c = 0; c < HD / 64; ++c)
-        tma_load_3d(sQ + c * BOX, &tmQ, q_bar, c * 64, g * a.G, b * a.C + T.p0);
+      if (!PAIR || rank == 0) mbar_arrive_expect_tx(q_bar, (PAIR ? 2 : 1) * Q_BYTES);
+      const uint32_t qb_addr = bar_of(q_bar);
+      for (int c = 0; c < HD / 64; ++c) {
+        if constexpr (PAIR)
+          tma_load_3d_pair(sQ + c * BOX, &tmQ, qb_addr, c * 64, g * a.G,
+                           b * a.C + T.p0 + row_off);
+        else
+          tma_load_3d(sQ + c * BOX, &tmQ, q_bar, c * 64, g * a.G, b * a.C + T.p0);
+      }
     }
     const int ps = a.page_table ? a.page_size : BN;
-    const int npg = BN / ps;
-    // this lane's page of a prompt tile, kept for the K and for the V stream (keys
+    // key rows of one box and this CTA's first key of a tile, per stream
+    constexpr int K_ROWS = PAIR ? BN / 2 : BN;
+    const int k_off = PAIR ? (int)rank * (BN / 2) : 0;
+    // this lane's page of a prompt box, kept for the K and for the V stream (keys
     // past the prompt read its last page, a bad entry reads page 0: both are masked)
     int pk_t = -1, pv_t = -1, pk_pg = 0, pv_pg = 0;
-    auto page_idx = [&](int t) -> int {
+    auto page_idx = [&](int t, int koff, int rows) -> int {
       int v = 0;
-      if (lane < npg) {
-        const int k = min(t * BN + lane * ps, T.P - 1);
+      if (lane < rows / ps) {
+        const int k = min(t * BN + koff + lane * ps, T.P - 1);
         v = a.page_table[(long long)b * a.pages_per_req + k / ps];
         if (v < 0 || v >= a.n_pages) v = 0;
       }
       return v;
     };
-    // one ring slot: two boxes of 64 head columns x 128 keys of tile t
+    // one ring slot of tile t: K unit u (PAIR: four boxes of 64 head columns x 64
+    // keys; else two boxes of 64 head columns x 128 keys) or V unit u (two boxes
+    // of 64 output columns x 128 keys)
     auto load_unit = [&](int t, bool is_v, int u) -> bool {
       int w_ok = 1;
       if (lane == 0) w_ok = mbar_wait(&empty_bar[slot], phase ^ 1u, abort_flag, a.status);
       if (!__shfl_sync(FULL, w_ok, 0)) return false;
       uint8_t* dst = ring + slot * UNIT;
-      if (lane == 0) mbar_arrive_expect_tx(&full_bar[slot], UNIT);
+      if (lane == 0 && (!PAIR || rank == 0))
+        mbar_arrive_expect_tx(&full_bar[slot], (PAIR ? 2 : 1) * UNIT);
       __syncwarp();
+      const uint32_t fb = bar_of(&full_bar[slot]);
       const int key0 = T.key0(t);
       const bool prompt = t < T.nbp;
       const bool paged = prompt && a.page_table;
       const CUtensorMap* m = prompt ? (is_v ? &tmVe : &tmKe) : (is_v ? &tmVc : &tmKc);
+      const int rows = is_v ? BN : K_ROWS;       // key rows of one box
+      const int koff = is_v ? 0 : k_off;         // this CTA's first key of the tile
+      const int nbox = (PAIR && !is_v) ? 4 : 2;
+      const int box_bytes = rows * 128;
       int pg = 0;
       if (paged) {
         if (is_v) {
           if (pv_t != t) {
-            pv_pg = page_idx(t);
+            pv_pg = page_idx(t, 0, BN);
             pv_t = t;
           }
           pg = pv_pg;
         } else {
           if (pk_t != t) {
-            pk_pg = page_idx(t);
+            pk_pg = page_idx(t, koff, K_ROWS);
             pk_t = t;
           }
           pg = pk_pg;
         }
       }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int col = (is_v ? dh * DH : 0) + u * 128 + h * 64;
-        uint8_t* d = dst + h * BOX;
+      for (int h = 0; h < nbox; ++h) {
+        int col;
+        if (PAIR)
+          col = is_v ? dh * DH + (int)rank * 128 + h * 64 : u * 256 + h * 64;
+        else
+          col = (is_v ? dh * DH : 0) + u * 128 + h * 64;
+        uint8_t* d = dst + h * box_bytes;
         if (paged) {
-          if (lane < npg) tma_load_3d(d + lane * ps * 128, m, &full_bar[slot], col, g, pg * ps);
+          if (lane < rows / ps) {
+            if constexpr (PAIR)
+              tma_load_3d_pair(d + lane * ps * 128, m, fb, col, g, pg * ps);
+            else
+              tma_load_3d(d + lane * ps * 128, m, &full_bar[slot], col, g, pg * ps);
+          }
         } else if (lane == 0) {
-          const int row = prompt ? b * a.Pmax + key0 : b * a.C + key0;
-          tma_load_3d(d, m, &full_bar[slot], col, g, row);
+          const int row = (prompt ? b * a.Pmax : b * a.C) + key0 + koff;
+          if constexpr (PAIR)
+            tma_load_3d_pair(d, m, fb, col, g, row);
+          else
+            tma_load_3d(d, m, &full_bar[slot], col, g, row);
         }
       }
       issued |= 1u << slot;
@@ -469,20 +528,21 @@ __global__ void __launch_bounds__(THREADS, 1)
       return true;
     };
     // the MMA warp consumes K(t0), then K(t+1) before V(t) for every tile t
-    for (int u = 0; u < K_UNITS && ok && n > 0; ++u) ok = load_unit(T.t_begin, false, u);
+    for (int u = 0; u < KU && ok && n > 0; ++u) ok = load_unit(T.t_begin, false, u);
     for (int j = 0; j < n && ok; ++j) {
       const int t = T.t_begin + j;
       if (j + 1 < n)
-        for (int u = 0; u < K_UNITS && ok; ++u) ok = load_unit(t + 1, false, u);
-      for (int u = 0; u < V_UNITS && ok; ++u) ok = load_unit(t, true, u);
+        for (int u = 0; u < KU && ok; ++u) ok = load_unit(t + 1, false, u);
+      for (int u = 0; u < VU && ok; ++u) ok = load_unit(t, true, u);
     }
-    if (!ok && lane == 0) {
+    if (!ok && lane == 0 && (!PAIR || rank == 0)) {
+      // the loads of both CTAs complete on the even CTA's barriers
       if (n > 0) mbar_wait_drain(q_bar, 0);
       for (int s = 0; s < NSLOT; ++s)
         if (issued & (1u << s)) mbar_wait_drain(&full_bar[s], (last_phase >> s) & 1u);
     }
   } else if (warp == MMA_WARP) {
-    if (lane == 0) {
+    if (lane == 0 && (!PAIR || rank == 0)) {
       int slot = 0;
       uint32_t phase = 0;
       bool ok = n > 0 && mbar_wait(q_bar, 0, abort_flag, a.status);
@@ -490,31 +550,46 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t q_addr = smem_u32(sQ);
       auto qk = [&](int j) -> bool {
         const uint32_t d_tmem = tmem_base + S_COL + (j & 1) * BN;
-        for (int u = 0; u < K_UNITS; ++u) {
+        for (int u = 0; u < KU; ++u) {
           if (!mbar_wait(&full_bar[slot], phase, abort_flag, a.status)) return false;
           tc_fence_after();
           const uint32_t base = smem_u32(ring + slot * UNIT);
+          if constexpr (PAIR) {
+            // 256 head columns per unit: four boxes of 64 keys x 64 columns
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const int h = kk >> 2, k16 = kk & 3;
-            const uint64_t ad = sw128_kmajor_desc(q_addr + (2 * u + h) * BOX + k16 * 32);
-            const uint64_t bd = sw128_kmajor_desc(base + h * BOX + k16 * 32);
-            tc_mma_f16(d_tmem, ad, bd, IDESC_QK, (u | kk) ? 1u : 0u);
+            for (int kk = 0; kk < 16; ++kk) {
+              const int h = kk >> 2, k16 = kk & 3;
+              const uint64_t ad = sw128_kmajor_desc(q_addr + (4 * u + h) * BOX + k16 * 32);
+              const uint64_t bd = sw128_kmajor_desc(base + h * (BOX / 2) + k16 * 32);
+              tc_mma_f16_pair(d_tmem, ad, bd, IDESC_QK_PAIR, (u | kk) ? 1u : 0u);
+            }
+            tc_commit_pair(&empty_bar[slot], 0x3);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const int h = kk >> 2, k16 = kk & 3;
+              const uint64_t ad = sw128_kmajor_desc(q_addr + (2 * u + h) * BOX + k16 * 32);
+              const uint64_t bd = sw128_kmajor_desc(base + h * BOX + k16 * 32);
+              tc_mma_f16(d_tmem, ad, bd, IDESC_QK, (u | kk) ? 1u : 0u);
+            }
+            tc_commit(&empty_bar[slot]);
           }
-          tc_commit(&empty_bar[slot]);
           if (++slot == NSLOT) {
             slot = 0;
             phase ^= 1u;
           }
         }
-        tc_commit(&sfull_bar[j & 1]);
+        if constexpr (PAIR)
+          tc_commit_pair(&sfull_bar[j & 1], 0x3);
+        else
+          tc_commit(&sfull_bar[j & 1]);
         return true;
       };
       auto pv = [&](int j) -> bool {
         if (!mbar_wait(&pready_bar[j & 1], (j >> 1) & 1u, abort_flag, a.status)) return false;
         tc_fence_after();
         const uint32_t p_tmem = tmem_base + S_COL + (j & 1) * BN;
-        for (int u = 0; u < V_UNITS; ++u) {
+        for (int u = 0; u < VU; ++u) {
           if (!mbar_wait(&full_bar[slot], phase, abort_flag, a.status)) return false;
           tc_fence_after();
           const uint32_t base = smem_u32(ring + slot * UNIT);
@@ -524,16 +599,26 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint64_t bd = sw128_mnmajor_desc(base + ks * 2048, BOX, 1024);
             // P of keys [64 h, 64 h + 64) sits in columns [64 h, 64 h + 32)
             const uint32_t p_col = ks * 8 + (ks >= 4 ? 32 : 0);
-            tc_mma_f16_ts(tmem_base + O_COL + u * 128, p_tmem + p_col, bd, IDESC_PV,
-                          (j | ks) ? 1u : 0u);
+            if constexpr (PAIR)
+              tc_mma_f16_ts_pair(tmem_base + O_COL, p_tmem + p_col, bd, IDESC_PV_PAIR,
+                                 (j | ks) ? 1u : 0u);
+            else
+              tc_mma_f16_ts(tmem_base + O_COL + u * 128, p_tmem + p_col, bd, IDESC_PV,
+                            (j | ks) ? 1u : 0u);
           }
-          tc_commit(&empty_bar[slot]);
+          if constexpr (PAIR)
+            tc_commit_pair(&empty_bar[slot], 0x3);
+          else
+            tc_commit(&empty_bar[slot]);
           if (++slot == NSLOT) {
             slot = 0;
             phase ^= 1u;
           }
         }
-        tc_commit(pv_bar);
+        if constexpr (PAIR)
+          tc_commit_pair(pv_bar, 0x3);
+        else
+          tc_commit(pv_bar);
         return true;
       };
       if (ok) ok = qk(0);
@@ -541,27 +626,59 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (j + 1 < n) ok = qk(j + 1);
         if (ok) ok = pv(j);
       }
-      tc_commit(drain_bar);
+      if constexpr (PAIR)
+        tc_commit_pair(drain_bar, 0x1);
+      else
+        tc_commit(drain_bar);
       mbar_wait_drain(drain_bar, 0);
     }
   } else {
-    softmax_and_store(a, T, n, b, g, dh, split, warp, lane, tmem_base, sfull_bar, pready_bar,
-                      pv_bar, pair_bar, abort_flag, xch);
+    softmax_and_store<PAIR>(a, T, n, b, g, dh, split, warp, lane, tmem_base, sfull_bar,
+                            pready_bar, pv_bar, pair_bar, abort_flag, xch, row_off,
+                            bar_of(&pready_bar[0]), bar_of(&pready_bar[1]));
   }
 
+  __syncwarp();
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync();
+  else
+    __syncthreads();
   tc_fence_after();
-  if (warp == MMA_WARP) tmem_dealloc(tmem_base, TMEM_COLS);
+  if (warp == MMA_WARP) {
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
+                   const __grid_constant__ CUtensorMap tmKe,
+                   const __grid_constant__ CUtensorMap tmVe,
+                   const __grid_constant__ CUtensorMap tmKc,
+                   const __grid_constant__ CUtensorMap tmVc, TcArgs a) {
+  attn_body<false>(tmQ, tmKe, tmVe, tmKc, tmVc, a);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    attn_pair_kernel(const __grid_constant__ CUtensorMap tmQ,
+                     const __grid_constant__ CUtensorMap tmKe,
+                     const __grid_constant__ CUtensorMap tmVe,
+                     const __grid_constant__ CUtensorMap tmKc,
+                     const __grid_constant__ CUtensorMap tmVc, TcArgs a) {
+  attn_body<true>(tmQ, tmKe, tmVe, tmKc, tmVc, a);
 }
 
 // Splits of the key range: enough CTAs to fill the SMs; for long key ranges a
 // multiple of the SM count, as long as every split keeps at least 16 tiles.
-int tc_splits(int B, int C, int Hq, int Hkv, int Pmax, int W) {
+// pair: CTA pairs over 256-row tiles (two CTAs per tile).
+int tc_splits(int B, int C, int Hq, int Hkv, int Pmax, int W, bool pair) {
   const int G = Hq / Hkv;
-  const int npos = BM / G;
+  const int npos = (pair ? 2 : 1) * (BM / G);      // canvas positions of one tile
   const int q_blocks = (C + npos - 1) / npos;
-  const int base = B * Hkv * q_blocks * 2;
+  const int base = B * Hkv * q_blocks * 2 * (pair ? 2 : 1);
   const int keys_c = std::min(C, npos + 2 * W);
   const int nb = std::max(1, (Pmax + BN - 1) / BN + (keys_c + BN - 1) / BN);
   const int sms = dgi::num_sms();
@@ -588,8 +705,16 @@ bool attn_tc_supported(const AttnArgs& x) {
   return true;
 }
 
+// The CTA-pair kernel loads half-tiles of 64 keys: pages must divide 64.
+bool attn_pair_ok(const AttnArgs& x) {
+  return attn_tc_supported(x) && (!x.page_table || (BN / 2) % x.page_size == 0);
+}
+
 size_t attn_tc_ws_bytes(int B, int C, int Pmax, int Hq, int Hkv, int W) {
-  const int s = tc_splits(B, C, Hq, Hkv, Pmax, std::min(W, C));
+  // sized for either kernel (the pair kernel is chosen per call from the page size)
+  const int w = std::min(W, C);
+  const int s = std::max(tc_splits(B, C, Hq, Hkv, Pmax, w, false),
+                         tc_splits(B, C, Hq, Hkv, Pmax, w, true));
   if (s == 1) return 256;
   return align_up((size_t)s * B * C * Hq * HD * 4 + (size_t)s * B * Hq * C * 8, 256);
 }
@@ -603,9 +728,10 @@ cudaError_t attn_decode_tc(const AttnArgs& x, void* ws, cudaStream_t st) {
   a.Hkv = x.Hkv;
   a.W = std::min(x.W, x.C);
   a.G = x.Hq / x.Hkv;
-  a.npos = BM / a.G;
+  const bool pair = attn_pair_ok(x);
+  a.npos = (pair ? 2 : 1) * (BM / a.G);   // canvas positions of one tile
   a.q_blocks = (x.C + a.npos - 1) / a.npos;
-  a.splits = tc_splits(x.B, x.C, x.Hq, x.Hkv, x.Pmax, a.W);
+  a.splits = tc_splits(x.B, x.C, x.Hq, x.Hkv, x.Pmax, a.W, pair);
   a.causal = x.causal;
   a.seq_len = x.seq_len;
   a.mode = x.mode;
@@ -625,37 +751,50 @@ cudaError_t attn_decode_tc(const AttnArgs& x, void* ws, cudaStream_t st) {
   {
     const uint64_t dims[3] = {HD, (uint64_t)x.Hq, (uint64_t)x.B * x.C};
     const uint64_t str[2] = {row, row * x.Hq};
-    const uint32_t box[3] = {64, (uint32_t)a.G, (uint32_t)a.npos};
+    // one CTA's rows: 128 / G positions x G heads
+    const uint32_t box[3] = {64, (uint32_t)a.G, (uint32_t)(BM / a.G)};
     if (!make_tmap_bf16_3d(&tq, x.q, dims, str, box)) return cudaErrorInvalidValue;
   }
+  // K boxes: a pair CTA loads half of a tile's keys
+  const uint32_t k_rows = pair ? BN / 2 : BN;
   {
     const uint64_t dims[3] = {HD, (uint64_t)x.Hkv, (uint64_t)x.B * x.C};
     const uint64_t str[2] = {row, row * x.Hkv};
-    const uint32_t box[3] = {64, 1, BN};
-    if (!make_tmap_bf16_3d(&tkc, x.kc, dims, str, box)) return cudaErrorInvalidValue;
-    if (!make_tmap_bf16_3d(&tvc, x.vc, dims, str, box)) return cudaErrorInvalidValue;
+    const uint32_t kbox[3] = {64, 1, k_rows};
+    const uint32_t vbox[3] = {64, 1, BN};
+    if (!make_tmap_bf16_3d(&tkc, x.kc, dims, str, kbox)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16_3d(&tvc, x.vc, dims, str, vbox)) return cudaErrorInvalidValue;
   }
   if (x.Pmax > 0) {
     const bool paged = x.page_table != nullptr;
     const uint64_t rows = paged ? (uint64_t)x.n_pages * x.page_size : (uint64_t)x.B * x.Pmax;
     const uint64_t dims[3] = {HD, (uint64_t)x.Hkv, rows};
     const uint64_t str[2] = {row, row * x.Hkv};
-    const uint32_t box[3] = {64, 1, paged ? (uint32_t)x.page_size : (uint32_t)BN};
-    if (!make_tmap_bf16_3d(&tke, x.kenc, dims, str, box)) return cudaErrorInvalidValue;
-    if (!make_tmap_bf16_3d(&tve, x.venc, dims, str, box)) return cudaErrorInvalidValue;
+    const uint32_t kbox[3] = {64, 1, paged ? (uint32_t)x.page_size : k_rows};
+    const uint32_t vbox[3] = {64, 1, paged ? (uint32_t)x.page_size : (uint32_t)BN};
+    if (!make_tmap_bf16_3d(&tke, x.kenc, dims, str, kbox)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16_3d(&tve, x.venc, dims, str, vbox)) return cudaErrorInvalidValue;
   } else {
     tke = tkc;  // no prompt tiles: never read
     tve = tvc;
   }
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  static bool attr = false, attr_pair = false;
+  bool& done = pair ? attr_pair : attr;
+  if (!done) {
+    cudaError_t e = pair ? cudaFuncSetAttribute(attn_pair_kernel,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                SMEM_BYTES)
+                         : cudaFuncSetAttribute(attn_tc_kernel,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr = true;
+    done = true;
   }
-  const int grid = a.splits * 2 * a.q_blocks * x.Hkv * x.B;
-  attn_tc_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(tq, tke, tve, tkc, tvc, a);
+  const int grid = (pair ? 2 : 1) * a.splits * 2 * a.q_blocks * x.Hkv * x.B;
+  if (pair)
+    attn_pair_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(tq, tke, tve, tkc, tvc, a);
+  else
+    attn_tc_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(tq, tke, tve, tkc, tvc, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || a.splits == 1) return e;
   return attn_combine(x.B, x.C, x.Hq, HD, a.splits, a.ws_o, a.ws_ml, x.out, x.lse, st,
