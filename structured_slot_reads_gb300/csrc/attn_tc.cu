@@ -52,7 +52,10 @@ constexpr int TMEM_COLS = 512;
 constexpr int O_COL = 0;                // O: columns [0, 256)
 constexpr int S_COL = 256;              // S buffers: [256, 384) and [384, 512)
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = 1024 + Q_BYTES + NSLOT * UNIT + BAR_BYTES;
+// per-tile row-maximum exchange of the two softmax warps of a lane quarter:
+// [tile parity][warp half][128 rows] bf16
+constexpr int XMAX_BYTES = 2 * 2 * BM * 2;
+constexpr int SMEM_BYTES = 1024 + Q_BYTES + NSLOT * UNIT + BAR_BYTES + XMAX_BYTES;
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32_bmn(BM, 128);
 constexpr uint32_t IDESC_QK_PAIR = idesc_bf16_f32(2 * BM, BN);
@@ -82,6 +85,17 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// bf16 bit pattern of the smallest bf16 value >= x (x finite or -inf): positive
+// values round up, negative values truncate toward zero.
+__device__ __forceinline__ uint16_t bf16_bits_up(float x) {
+  uint32_t u = __float_as_uint(x);
+  if (x > 0.f) u += 0xFFFFu;
+  return (uint16_t)(u >> 16);
+}
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t h) {
+  return __uint_as_float((uint32_t)h << 16);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -160,7 +174,7 @@ __device__ __forceinline__ void softmax_and_store(const TcArgs& a, const Tiles& 
                                                   uint64_t* pready_bar, uint64_t* pv_bar,
                                                   uint64_t* pair_bar, volatile int* abort_flag,
                                                   float* xch, int row_off, uint32_t pready_c0,
-                                                  uint32_t pready_c1) {
+                                                  uint32_t pready_c1, uint16_t* xmax) {
   constexpr unsigned FULL = 0xffffffffu;
   const int quarter = warp & 3, half = warp >> 2;
   const int r = quarter * 32 + lane;
@@ -198,25 +212,31 @@ __device__ __forceinline__ void softmax_and_store(const TcArgs& a, const Tiles& 
       lo = max(T.clo, pos - a.W) - key0;
       hi = min(T.chi, pos + a.W + 1) - key0;
     }
-    // pass 1: masked maximum of the raw scores over the whole row (both warps of
-    // the pair read all 128 scores, so they agree without exchanging anything)
-    float mb = -INFINITY;
-#pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      uint32_t v[32];
-      tmem_ld_32x32b_x32(s_addr + c * 32, v);
-      const uint32_t vm = chunk_mask(c, lo, hi, bad, a.page_size);
-      tmem_ld_wait();
+    // pass 1: this warp's 64 scores of the tile (keys [64 h, 64 h + 64)), read from
+    // tensor memory once, and their masked maximum; the pair exchanges its partial
+    // maxima in log2 units rounded up to bf16, so both warps take the same
+    // reference and it is never below the row's true maximum (phase j of the
+    // pair's barrier; slot parity j % 2 is rewritten two tiles later, after the
+    // partner has passed phase j + 1 and so has read this value)
+    uint32_t v0[32], v1[32];
+    tmem_ld_32x32b_x32(s_addr + (2 * half) * 32, v0);
+    tmem_ld_32x32b_x32(s_addr + (2 * half + 1) * 32, v1);
+    const uint32_t vm0 = chunk_mask(2 * half, lo, hi, bad, a.page_size);
+    const uint32_t vm1 = chunk_mask(2 * half + 1, lo, hi, bad, a.page_size);
+    tmem_ld_wait();
+    float mh = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if ((vm >> i) & 1u) mb = fmaxf(mb, __uint_as_float(v[i]));
+    for (int i = 0; i < 32; ++i) {
+      if ((vm0 >> i) & 1u) mh = fmaxf(mh, __uint_as_float(v0[i]));
+      if ((vm1 >> i) & 1u) mh = fmaxf(mh, __uint_as_float(v1[i]));
     }
-    mb = (mb == -INFINITY) ? -INFINITY : mb * sl2;  // log2 units
-    // both warps of the pair have read every score before either overwrites its
-    // half with probabilities (a bounded wait: phase j of the pair's barrier)
+    const uint16_t own = bf16_bits_up(mh == -INFINITY ? -INFINITY : mh * sl2);
+    uint16_t* xm = xmax + (j & 1) * 2 * BM;
+    xm[half * BM + r] = own;
     mbar_arrive(&pair_bar[quarter]);
     ok = __all_sync(FULL, mbar_wait(&pair_bar[quarter], j & 1u, abort_flag, a.status));
     if (!ok) break;
+    const float mb = fmaxf(bf16_bits_to_float(own), bf16_bits_to_float(xm[(half ^ 1) * BM + r]));
     // lazy reference: raise it (and rescale O) only past LAZY log2 units
     const float m_new = fmaxf(m_ref, mb);
     const bool raise = m_new > m_ref + LAZY;
@@ -244,16 +264,10 @@ __device__ __forceinline__ void softmax_and_store(const TcArgs& a, const Tiles& 
     l *= f;
     if (raise) m_ref = m_new;
     const float mr = (m_ref == -INFINITY) ? 0.f : m_ref;
-    // pass 2: p = 2^(s sl2 - m), written as bf16 pairs over this half's own score
-    // columns: keys [64 h, 64 h + 64) -> P columns [64 h, 64 h + 32)
+    // pass 2: p = 2^(s sl2 - m) from the registers, written as bf16 pairs over this
+    // half's own score columns: keys [64 h, 64 h + 64) -> P columns [64 h, 64 h + 32)
     float psum = 0.f;
-#pragma unroll 1
-    for (int cc = 0; cc < 2; ++cc) {
-      const int c = 2 * half + cc;
-      uint32_t v[32];
-      tmem_ld_32x32b_x32(s_addr + c * 32, v);
-      const uint32_t vm = chunk_mask(c, lo, hi, bad, a.page_size);
-      tmem_ld_wait();
+    auto probs = [&](const uint32_t (&v)[32], uint32_t vm, int cc) {
       uint32_t pk[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -265,7 +279,9 @@ __device__ __forceinline__ void softmax_and_store(const TcArgs& a, const Tiles& 
         pk[i] = pack_bf16(p0, p1);
       }
       tmem_st_32x32b_x16(s_addr + half * 64 + cc * 16, pk);
-    }
+    };
+    probs(v0, vm0, 0);
+    probs(v1, vm1, 1);
     l += psum;
     tmem_st_wait();
     tc_fence_before();
@@ -362,6 +378,7 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmQ, const CUtensor
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   // row-sum exchange of the softmax warp pairs, after the last tile (the ring is idle then)
   float* xch = reinterpret_cast<float*>(ring);
+  uint16_t* xmax = reinterpret_cast<uint16_t*>(bar_base + BAR_BYTES);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -635,7 +652,7 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmQ, const CUtensor
   } else {
     softmax_and_store<PAIR>(a, T, n, b, g, dh, split, warp, lane, tmem_base, sfull_bar,
                             pready_bar, pv_bar, pair_bar, abort_flag, xch, row_off,
-                            bar_of(&pready_bar[0]), bar_of(&pready_bar[1]));
+                            bar_of(&pready_bar[0]), bar_of(&pready_bar[1]), xmax);
   }
 
   __syncwarp();
