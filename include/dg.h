@@ -357,7 +357,7 @@ int dg_selfcond_embed(const dg_dims* dims, const uint16_t* h, int M,
  *   w [V, d_model] bf16;  inv_t [M], inv_t_draw [n_draw] fp32
  *   lse, entropy, maxz [M] fp32;  argmax [M] int32;  lse_draw [n_draw] fp32
  *   prob_scale [M] fp32;  probs [M, probs_ld] bf16 (probs_ld >= V, multiple of
- *   64; NULL to skip the probabilities)
+ *   64; 32-byte aligned; NULL to skip the probabilities)
  *   workspace: dg_workspace_bytes(dims, DG_WS_HEADS, M) bytes. */
 int dg_denoise_heads(const dg_dims* dims, const uint16_t* h, int M,
                      const uint16_t* draw_rows, int n_draw, const uint16_t* w,

@@ -273,7 +273,7 @@ int dg_denoise_heads(const dg_dims* d, const uint16_t* h, int M, const uint16_t*
   if (n_draw > 0 && (!draw_rows || !inv_t_draw || !lse_draw)) return DG_ERR_ARG;
   if (!aligned(h, 16) || !aligned(w, 16) || (n_draw > 0 && !aligned(draw_rows, 16)))
     return DG_ERR_ARG;
-  if (probs && (probs_ld < (size_t)d->V || probs_ld % 64 || !aligned(probs, 16)))
+  if (probs && (probs_ld < (size_t)d->V || probs_ld % 64 || !aligned(probs, 32)))
     return DG_ERR_ARG;
   const size_t need = dg_workspace_bytes(d, DG_WS_HEADS, M);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DG_ERR_WORKSPACE;

@@ -377,18 +377,20 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
         if (p.probs) {
           __nv_bfloat16* dst = p.probs + (long long)row * p.ldp + n0;
           if (n0 + 32 <= p.V) {
+            // two 256-bit stores per lane: whole 32-byte sectors (the row pitch is a
+            // multiple of 128 bytes and chunks start on 32-byte boundaries)
 #pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-              uint4 pk;
-              __nv_bfloat162 b0 = __floats2bfloat162_rn(e[j + 0], e[j + 1]);
-              __nv_bfloat162 b1 = __floats2bfloat162_rn(e[j + 2], e[j + 3]);
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(e[j + 4], e[j + 5]);
-              __nv_bfloat162 b3 = __floats2bfloat162_rn(e[j + 6], e[j + 7]);
-              pk.x = *reinterpret_cast<uint32_t*>(&b0);
-              pk.y = *reinterpret_cast<uint32_t*>(&b1);
-              pk.z = *reinterpret_cast<uint32_t*>(&b2);
-              pk.w = *reinterpret_cast<uint32_t*>(&b3);
-              *reinterpret_cast<uint4*>(dst + j) = pk;
+            for (int j = 0; j < 32; j += 16) {
+              uint32_t w[8];
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                __nv_bfloat162 bq = __floats2bfloat162_rn(e[j + 2 * q], e[j + 2 * q + 1]);
+                w[q] = *reinterpret_cast<uint32_t*>(&bq);
+              }
+              asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + j),
+                           "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]),
+                           "r"(w[6]), "r"(w[7])
+                           : "memory");
             }
           } else {
 #pragma unroll
