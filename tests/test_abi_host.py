@@ -222,3 +222,30 @@ def test_wait_timeout_diagnostic_validates_its_limit(lib):
     assert dg.dg_check_wait_timeout(0, 16, stream=0) == dg.DG_ERR_ARG
     assert dg.dg_check_wait_timeout(2_000_000_000, 16, stream=0) == dg.DG_ERR_ARG
     assert dg.dg_check_wait_timeout(1000, None, stream=0) == dg.DG_ERR_ARG
+
+
+def test_heads_pass_wants_32_byte_aligned_probabilities(lib):
+    """The probabilities are written with 256-bit stores."""
+    d = dg.make_dims(d_model=128, V=1024)
+    ld = dg.dg_probs_ld(1024)
+    args = lambda probs: (d, 32, 4, None, 0, 32, 32, None, 32, 32, 32, 32, None, 32,  # noqa: E731
+                          probs, ld, None)
+    assert dg.dg_denoise_heads(*args(48), stream=0) == dg.DG_ERR_ARG        # 16- not 32-aligned
+    assert dg.dg_denoise_heads(*args(64), stream=0) == dg.DG_ERR_WORKSPACE  # alignment accepted
+
+
+def test_8bit_self_conditioning_validates(lib):
+    d = dg.make_dims(d_model=128, V=1024)
+    ok = (d, 32, 32, None, 4, 32, 32, 32, None)
+    assert dg.dg_selfcond_from_probs8(*ok, stream=0) == dg.DG_ERR_WORKSPACE
+    assert dg.dg_selfcond_from_probs8(dg.make_dims(d_model=128, V=1000), *ok[1:],
+                                      stream=0) == dg.DG_ERR_SHAPE          # V % 16
+    assert dg.dg_selfcond_from_probs8(dg.make_dims(d_model=126, V=1024), *ok[1:],
+                                      stream=0) == dg.DG_ERR_SHAPE          # d_model % 4
+    assert dg.dg_selfcond_from_probs8(d, 40, 32, None, 4, 32, 32, 32, None,
+                                      stream=0) == dg.DG_ERR_ARG            # p8 not 16-aligned
+    assert dg.dg_selfcond_from_probs8(d, None, 32, None, 4, 32, 32, 32, None,
+                                      stream=0) == dg.DG_ERR_ARG
+    assert dg.dg_quantize_cols_e4m3(None, -1, 4, None, None, stream=0) == dg.DG_ERR_ARG
+    assert dg.dg_quantize_cols_e4m3(None, 4, 4, None, None, stream=0) == dg.DG_ERR_ARG
+    assert dg.dg_quantize_cols_e4m3(None, 0, 4, None, None, stream=0) == dg.DG_OK
