@@ -62,6 +62,9 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--schedule", default="concurrent", choices=["concurrent", "serial"],
+                    help="step schedule: side stream beside the self-conditioning GEMM, "
+                         "or every call on one stream")
     ap.add_argument("--workload", default="full_canvas_step", choices=list(WORKLOADS),
                     help="full_canvas_step is the headline line; the others measure the "
                          "remaining workloads (read-only steps, the mixed batch, the sweep)")
@@ -178,7 +181,7 @@ def traffic_from_profile(kernel_src, name):
 
 
 # ------------------------------------------------------------ the GPU arm
-def build_step(shape, device):
+def build_step(shape, device, concurrent=True):
     import torch
 
     from structured_slot_reads_gb300 import dg, inputs
@@ -186,7 +189,7 @@ def build_step(shape, device):
     torch.manual_seed(0)
     w = inputs.device_normal_bf16((shape.V, shape.D), shape.D ** -0.5, 1, device)
     e = inputs.device_normal_bf16((shape.V, shape.D), shape.D ** -0.5, 2, device)
-    st = DenoiseStep(shape, w, e, device=device, seed=7)
+    st = DenoiseStep(shape, w, e, device=device, seed=7, concurrent=concurrent)
     st.h0.copy_(inputs.device_normal_bf16(st.h0.shape, 1.0, 3, device))
     st.inv_t.copy_(1.0 / inputs.device_uniform(st.inv_t.shape, 0.5, 2.0, 4, device))
     for i, k in enumerate(("q", "kc", "vc", "kenc", "venc")):
@@ -251,7 +254,7 @@ def gpu_arm(args, rank, world, local):
     shape = configs.FULL_CANVAS
     device = f"cuda:{local}"
     torch.cuda.set_device(local)
-    st = build_step(shape, device)
+    st = build_step(shape, device, concurrent=args.schedule == "concurrent")
     stream = torch.cuda.current_stream()
     # warm-up
     for i in range(args.warmup):
@@ -270,6 +273,8 @@ def gpu_arm(args, rank, world, local):
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    # per-call times need one stream: the eager pass runs the one-stream schedule
+    concurrent, st.concurrent = st.concurrent, False
     e0.record(stream)
     launches = 0
     for i in range(args.steps):
@@ -279,6 +284,7 @@ def gpu_arm(args, rank, world, local):
     barrier(world)
     ms_eager = max_over_ranks(e0.elapsed_time(e1), world)
     timer.unwrap()
+    st.concurrent = concurrent
     per_call = {n: timer.mean_ms(n) for n in calls}
 
     # the same steps replayed as CUDA graphs (one per step index, captured before
@@ -364,8 +370,12 @@ def gpu_arm(args, rank, world, local):
                    "global_batch": world * shape.B, "seq_len": shape.C,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2: W and E (1.48 GB each) streamed every step",
-                   "launch": "each step replayed as a CUDA graph of its library kernels "
-                             "(per-call times from an eager pass of the same steps)"},
+                   "launch": "each step replayed as a CUDA graph of its library kernels"
+                             + (", slot finish, commit and attention on a side stream beside "
+                                "the self-conditioning GEMM" if st.concurrent else "")
+                             + " (per-call times from an eager one-stream pass of the same "
+                               "steps)",
+                   "schedule": args.schedule},
         "slot_reads_per_s": round(value, 3),
         "slot_decisions_per_s": round(value * len(shape.slots), 3),
         "roofline": roof,

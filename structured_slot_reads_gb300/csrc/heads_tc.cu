@@ -488,12 +488,9 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
 }
 
 // Canvas rows: S = sum of the CTA sums (common reference), one warp per row.
-__global__ void heads_finalize_kernel(const float* part, int cpg, int M, const float* inv_t,
-                                      const float* ref, float* lse, float* entropy, float* maxz,
-                                      int32_t* argmax, float* prob_scale) {
-  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= M) return;
+__device__ void finalize_row(int row, int lane, const float* part, int cpg, int M,
+                             const float* inv_t, const float* ref, float* lse, float* entropy,
+                             float* maxz, int32_t* argmax, float* prob_scale) {
   const long long plane = (long long)cpg * M;
   const float* pm = part + (long long)row * cpg;
   float s = 0.f, t = 0.f, best = -INFINITY;
@@ -530,12 +527,9 @@ __global__ void heads_finalize_kernel(const float* part, int cpg, int M, const f
   }
 }
 
-// Draw rows: merge (max, sum) pairs over CTAs, one warp per draw row.
-__global__ void draws_finalize_kernel(const float* part_draw, int cpg, int n_draw,
-                                      float* lse_draw) {
-  const int j = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (j >= n_draw) return;
+// Draw rows: per-CTA (max, sum) pairs merged, one warp per row.
+__device__ void finalize_draw(int j, int lane, const float* part_draw, int cpg, int n_draw,
+                              float* lse_draw) {
   const float* pm = part_draw + (long long)j * cpg;
   const float* ps = part_draw + (long long)n_draw * cpg + (long long)j * cpg;
   float m = -INFINITY;
@@ -548,6 +542,24 @@ __global__ void draws_finalize_kernel(const float* part_draw, int cpg, int n_dra
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   if (lane == 0) lse_draw[j] = (m + log2f(s)) * LN2;
+}
+
+// Both finalisations in one launch: the first row_blocks blocks take the canvas
+// rows, the rest the draw rows (8 rows a block).
+__global__ void heads_finalize_kernel(const float* part, int cpg, int M, const float* inv_t,
+                                      const float* ref, float* lse, float* entropy, float* maxz,
+                                      int32_t* argmax, float* prob_scale, const float* part_draw,
+                                      int n_draw, float* lse_draw, int row_blocks) {
+  const int lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5;
+  if ((int)blockIdx.x < row_blocks) {
+    const int row = blockIdx.x * (blockDim.x >> 5) + w;
+    if (row < M)
+      finalize_row(row, lane, part, cpg, M, inv_t, ref, lse, entropy, maxz, argmax, prob_scale);
+  } else {
+    const int j = (blockIdx.x - row_blocks) * (blockDim.x >> 5) + w;
+    if (j < n_draw) finalize_draw(j, lane, part_draw, cpg, n_draw, lse_draw);
+  }
 }
 
 template <int MT, int BN, bool DRAWS>
@@ -637,12 +649,10 @@ cudaError_t denoise_heads(const uint16_t* h, int M, const uint16_t* draw_rows, i
     e = (mt == 1) ? launch_heads<1, 256, false>(ta, tb, td, p, grid, st)
                   : launch_heads<2, 256, false>(ta, tb, td, p, grid, st);
   if (e != cudaSuccess) return e;
-  heads_finalize_kernel<<<(M + 7) / 8, 256, 0, st>>>(p.part, p.cpg, M, inv_t, ref, out.lse,
-                                                     out.entropy, out.maxz, out.argmax,
-                                                     prob_scale);
-  e = cudaGetLastError();
-  if (e != cudaSuccess || n_draw == 0) return e;
-  draws_finalize_kernel<<<(n_draw + 7) / 8, 256, 0, st>>>(p.part_draw, p.cpg, n_draw, lse_draw);
+  const int row_blocks = (M + 7) / 8, draw_blocks = (n_draw + 7) / 8;
+  heads_finalize_kernel<<<row_blocks + draw_blocks, 256, 0, st>>>(
+      p.part, p.cpg, M, inv_t, ref, out.lse, out.entropy, out.maxz, out.argmax, prob_scale,
+      p.part_draw, n_draw, lse_draw, row_blocks);
   return cudaGetLastError();
 }
 

@@ -13,9 +13,18 @@ them; the library never does) and enqueues the library calls of one step:
   dg_canvas_update        next step's canvas input rows
 
 With more than 16 draw rows (batched requests) the slot read takes its own
-pass (dg_slot_read).  ``fused=False`` runs the unfused calls instead
-(dg_lmhead_logsoftmax_entropy, dg_slot_read, dg_selfcond_embed), which stream
-W three times.
+pass (dg_slot_read).
+
+In the fused path (``concurrent=True``, the default) the calls that do not
+feed the self-conditioning GEMM leave the caller's stream once the heads pass
+is done: the slot finish, the commit and the attention run on a side stream
+while dg_selfcond_from_probs streams E (that GEMM is one wave of CTAs on
+fewer than all SMs, so they run on the SMs it leaves free), and the canvas
+update waits for the commit.  The step is the same work either way;
+``concurrent=False`` enqueues it in the order above on one stream.
+
+``fused=False`` runs the unfused calls instead (dg_lmhead_logsoftmax_entropy,
+dg_slot_read, dg_selfcond_embed), which stream W three times, on one stream.
 
 The same object serves the end-to-end path: ``upload`` copies a step's inputs
 from pinned host memory, ``download`` reads back the decisions.
@@ -23,6 +32,15 @@ from pinned host memory, ``download`` reads back the decisions.
 import torch
 
 from . import dg
+
+
+def _as_stream(stream):
+    """The torch stream of a call: the current one, a raw handle wrapped, or as given."""
+    if stream is None:
+        return torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return torch.cuda.ExternalStream(stream)
+    return stream
 
 
 def _empty(shape, dtype, device):
@@ -61,7 +79,8 @@ def _carve(layout, device, pin=False):
 
 
 class DenoiseStep:
-    def __init__(self, shape, w, e, device="cuda", with_slots=True, seed=0, fused=True):
+    def __init__(self, shape, w, e, device="cuda", with_slots=True, seed=0, fused=True,
+                 concurrent=True):
         self.shape = shape
         self.dims = dg.dims_of(shape)
         self.device = device
@@ -123,6 +142,8 @@ class DenoiseStep:
         # 16 draw rows ride along; more go through their own dg_slot_read pass)
         # and the self-conditioning probabilities
         self.fused = fused
+        self.concurrent = fused and concurrent
+        self._side = None                   # side stream and its event, made on first use
         self.n_draw = self.S * shape.R if (self.with_slots and self.S * shape.R <= 16) else 0
         if not self.fused:
             self.ws_lm = _empty((dg.dg_workspace_bytes(self.dims, dg.DG_WS_LMHEAD, self.M),), u8,
@@ -170,11 +191,9 @@ class DenoiseStep:
         """Enqueue one denoise step; returns the number of library kernels launched."""
         s, d = self.shape, self.dims
         ck = dg._check
-        ck(dg.dg_attn_decode(d, self.q, self.kc, self.vc, self.kenc, self.venc, None, 0, 0, 0,
-                             self.prompt_len, self.attn_out, self.attn_lse, self.ws_attn, stream),
-           "dg_attn_decode")
         if self.fused:
             return self._run_fused(step_idx, stream)
+        self._attention(stream)
         ck(dg.dg_lmhead_logsoftmax_entropy(d, self.h, self.M, self.w, self.inv_t, self.lse,
                                            self.ent, self.maxz, self.argmax, self.ws_lm, stream),
            "dg_lmhead_logsoftmax_entropy")
@@ -189,6 +208,16 @@ class DenoiseStep:
                                self.M, self.h, stream), "dg_canvas_update")
         return self.kernels_per_step()
 
+    def _attention(self, stream):
+        dg._check(dg.dg_attn_decode(self.dims, self.q, self.kc, self.vc, self.kenc, self.venc,
+                                    None, 0, 0, 0, self.prompt_len, self.attn_out, self.attn_lse,
+                                    self.ws_attn, stream), "dg_attn_decode")
+
+    def _selfcond(self, stream):
+        dg._check(dg.dg_selfcond_from_probs(self.dims, self.probs, self.probs_ld, self.prob_scale,
+                                            self.M, self.e, self.e_sc, self.ws_pe, stream),
+                  "dg_selfcond_from_probs")
+
     def _slot_read(self, step_idx, stream):
         s, d = self.shape, self.dims
         dg._check(dg.dg_slot_read(d, self.h, self.M, self.w, self.e, self.inv_t, self.slot_row,
@@ -200,30 +229,47 @@ class DenoiseStep:
     def _run_fused(self, step_idx, stream):
         s, d = self.shape, self.dims
         ck = dg._check
+        main = _as_stream(stream)
+        if not self.concurrent:
+            self._attention(main)
         if self.with_slots and not self.n_draw:
-            self._slot_read(step_idx, stream)
+            self._slot_read(step_idx, main)
         if self.n_draw:
             ck(dg.dg_slot_noise(d, self.h, self.M, self.e, self.inv_t, self.slot_row,
                                 self.slot_req, self.S, s.R, self.seed, step_idx, self.draw_rows,
-                                self.inv_t_draw, self.noise_tok, stream), "dg_slot_noise")
+                                self.inv_t_draw, self.noise_tok, main), "dg_slot_noise")
         ck(dg.dg_denoise_heads(d, self.h, self.M, self.draw_rows if self.n_draw else None,
                                self.n_draw, self.w, self.inv_t, self.inv_t_draw, self.lse,
                                self.ent, self.maxz, self.argmax, self.lse_draw, self.prob_scale,
-                               self.probs, self.probs_ld, self.ws_heads, stream),
+                               self.probs, self.probs_ld, self.ws_heads, main),
            "dg_denoise_heads")
+        side = main
+        if self.concurrent:
+            if self._side is None:
+                self._side = torch.cuda.Stream(device=self.h.device), torch.cuda.Event()
+            side, self.ev_commit = self._side
+            # the GEMM goes first so that its CTAs are placed before the side work's
+            side.wait_stream(main)
+            self._selfcond(main)
         if self.n_draw:
             ck(dg.dg_slot_finish(d, self.draw_rows, self.inv_t_draw, self.lse_draw, self.w,
                                  self.label_ids, self.n_labels, self.S, s.R, s.R, s.gate,
                                  self.q_avg, self.h_slot, self.chosen, self.lp_draws,
-                                 self.resampled, self.n_reads, stream), "dg_slot_finish")
+                                 self.resampled, self.n_reads, side), "dg_slot_finish")
         ck(dg.dg_commit(d, self.ent, self.argmax, self.cand, self.gamma, self.committed,
-                        self.tok_state, self.commit, self.tokens, self.n_commit, stream),
+                        self.tok_state, self.commit, self.tokens, self.n_commit, side),
            "dg_commit")
-        ck(dg.dg_selfcond_from_probs(d, self.probs, self.probs_ld, self.prob_scale, self.M,
-                                     self.e, self.e_sc, self.ws_pe, stream),
-           "dg_selfcond_from_probs")
+        if self.concurrent:
+            self.ev_commit.record(side)
+            self._attention(side)
+        else:
+            self._selfcond(main)
+        if self.concurrent:
+            main.wait_event(self.ev_commit)
         ck(dg.dg_canvas_update(d, self.h0, self.e_sc, self.e, self.tok_state, self.committed,
-                               self.M, self.h, stream), "dg_canvas_update")
+                               self.M, self.h, main), "dg_canvas_update")
+        if self.concurrent:
+            main.wait_stream(side)
         return self.kernels_per_step()
 
     def kernels_per_step(self):
@@ -231,11 +277,11 @@ class DenoiseStep:
         n = 1 + (1 if self._attn_splits() > 1 else 0)
         if self.fused:
             # ref + heads + finalize + commit + accum + reduce + update, and either
-            # noise + draw finalize + finish (label logits, slot epilogue) with the
-            # draws in the pass, or a slot read
+            # noise + finish (label logits, slot epilogue) with the draws in the pass
+            # (their log-normalisers finalised with the canvas rows'), or a slot read
             n += 3 + 1 + 2 + 1
             if self.n_draw:
-                n += 4
+                n += 3
             elif self.with_slots:
                 n += 5
             return n

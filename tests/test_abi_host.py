@@ -145,7 +145,7 @@ def test_step_runner_builds_on_host(lib, fused):
     w = torch.zeros((shp.V, shp.D), dtype=torch.bfloat16)
     st = DenoiseStep(shp, w, w, device="cpu", fused=fused)
     assert st.fused == fused
-    assert st.kernels_per_step() == (13 if fused else 14) - (0 if st._attn_splits() > 1 else 1)
+    assert st.kernels_per_step() == (12 if fused else 14) - (0 if st._attn_splits() > 1 else 1)
     if fused:
         assert st.probs.shape == (shp.C, dg.dg_probs_ld(shp.V)) and st.n_draw == 4
 

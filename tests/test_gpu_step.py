@@ -219,3 +219,44 @@ def test_graph_replay_equals_eager_step():
     torch.cuda.synchronize()
     for k, v in eager.items():
         assert np.array_equal(host(getattr(st, k)), v), k
+
+
+@pytest.mark.parametrize("size", ["tiny", "full_canvas"])
+def test_concurrent_schedule_equals_serial(size):
+    """The side-stream schedule (slot finish, commit and attention beside the
+    self-conditioning GEMM) computes the same step: three consecutive steps,
+    eager and replayed as graphs, equal the one-stream schedule bit for bit,
+    carried state included."""
+    if size == "tiny":
+        shape, x, _ = _tiny_inputs(3)
+    else:
+        shape = configs.FULL_CANVAS
+        x = inputs.step_inputs(shape, seed=0)
+    wd, ed = dev_bf16(x["w"]), dev_bf16(x["e"])
+    keys = ("lse", "ent", "argmax", "commit", "tokens", "n_commit", "e_sc", "h", "committed",
+            "tok_state", "chosen", "q_avg", "resampled", "attn_out", "attn_lse")
+
+    def steps(concurrent, graphs):
+        st = DenoiseStep(shape, wd, ed, seed=0, concurrent=concurrent)
+        assert st.concurrent == concurrent
+        _load(st, x)
+        st.run(step_idx=0)                  # one eager step: one-time set-up done
+        torch.cuda.synchronize()
+        _load(st, x)
+        out = []
+        for t in range(3):
+            if graphs:
+                st.replay(t)
+            else:
+                st.run(step_idx=t)
+            torch.cuda.synchronize()
+            out.append({k: host(getattr(st, k)).copy() for k in keys})
+        assert dg.dg_get_status() == 0
+        return out
+
+    serial = steps(False, False)
+    for graphs in (False, True):
+        got = steps(True, graphs)
+        for t in range(3):
+            for k in keys:
+                assert np.array_equal(got[t][k], serial[t][k]), (graphs, t, k)
