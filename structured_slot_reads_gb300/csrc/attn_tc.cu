@@ -63,6 +63,7 @@ constexpr uint32_t IDESC_PV_PAIR = idesc_bf16_f32_bmn(2 * BM, DH);
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 constexpr float LAZY = 8.f;             // log2 headroom before O is rescaled
+constexpr int ORDER_MAX_B = 64;         // decoder batches up to this size go longest first
 static_assert(SMEM_BYTES <= 232448, "shared memory");
 
 struct TcArgs {
@@ -186,8 +187,19 @@ __device__ __forceinline__ void softmax_and_store(const TcArgs& a, const Tiles& 
   const float sl2 = LOG2E * rsqrtf((float)HD);
   float m_ref = -INFINITY, l = 0.f;
   bool ok = true;
+  // page validity of a prompt tile: lane i checks the table entry of the tile's
+  // page i, read one tile ahead so the table's latency overlaps the score wait
+  const int npg = a.page_table ? BN / a.page_size : 0;
+  auto page_bad = [&](int t) -> bool {
+    if (!a.page_table || t >= T.nbp || lane >= npg) return false;
+    const int k = t * BN + lane * a.page_size;
+    return k < T.P && page_of(a, b, k) < 0;
+  };
+  bool bad_next = n > 0 && page_bad(T.t_begin);
   for (int j = 0; j < n; ++j) {
     const int t = T.t_begin + j;
+    const bool bad_lane = bad_next;
+    if (j + 1 < n) bad_next = page_bad(t + 1);
     ok = __all_sync(FULL, mbar_wait(&sfull_bar[j & 1], (j >> 1) & 1u, abort_flag, a.status));
     if (!ok) break;
     tc_fence_after();
@@ -199,10 +211,7 @@ __device__ __forceinline__ void softmax_and_store(const TcArgs& a, const Tiles& 
       lo = 0;
       hi = min(BN, T.P - key0);
       if (a.page_table) {
-        for (int i = 0; i < BN / a.page_size; ++i) {
-          const int k = key0 + i * a.page_size;
-          if (k < T.P && page_of(a, b, k) < 0) bad |= 1u << i;
-        }
+        bad = __ballot_sync(FULL, bad_lane);
         if (bad && r == 0 && half == 0) atomicOr(a.status, 2 /* DG_DEV_BAD_PAGE */);
       }
     } else if (T.causal) {
@@ -392,7 +401,22 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmQ, const CUtensor
   const int qb = (a.causal || a.mode) ? a.q_blocks - 1 - bid % a.q_blocks : bid % a.q_blocks;
   bid /= a.q_blocks;
   const int g = bid % a.Hkv;
-  const int b = bid / a.Hkv;
+  const int rq = bid / a.Hkv;  // request slot in launch order
+  // Decoder batches of ragged prompts: the blocks go out in launch order, so the
+  // requests are taken longest prompt first (slot rq serves the request of rank
+  // rq, ties to the lower index) and the last blocks to start are short ones.
+  int* b_slot = reinterpret_cast<int*>(tmem_slot + 2);
+  const bool by_len = !a.causal && !a.mode && a.prompt_len && a.B > 1 && a.B <= ORDER_MAX_B;
+  if (by_len && (int)threadIdx.x < a.B) {
+    const int i = threadIdx.x;
+    const int li = a.prompt_len[i];
+    int rank = 0;
+    for (int j = 0; j < a.B; ++j) {
+      const int lj = a.prompt_len[j];
+      rank += (lj > li || (lj == li && j < i)) ? 1 : 0;
+    }
+    if (rank == rq) *b_slot = i;
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NSLOT; ++i) {
@@ -434,6 +458,7 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmQ, const CUtensor
     __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const int b = by_len ? *b_slot : rq;
   const Tiles T = tiles_of(a, b, qb, split);
   const int n = T.t_end - T.t_begin;
   const int npos_cta = BM / a.G;                 // canvas positions of one CTA's rows
@@ -466,12 +491,13 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmQ, const CUtensor
     // key rows of one box and this CTA's first key of a tile, per stream
     constexpr int K_ROWS = PAIR ? BN / 2 : BN;
     const int k_off = PAIR ? (int)rank * (BN / 2) : 0;
-    // this lane's page of a prompt box, kept for the K and for the V stream (keys
-    // past the prompt read its last page, a bad entry reads page 0: both are masked)
-    int pk_t = -1, pv_t = -1, pk_pg = 0, pv_pg = 0;
+    // this lane's page of a prompt box of tile t (keys past the prompt read its
+    // last page, a bad entry reads page 0: both are masked).  The page indices of a
+    // tile are read from the table one tile ahead of its loads, so the table's
+    // latency overlaps the waits on the ring instead of delaying the copies.
     auto page_idx = [&](int t, int koff, int rows) -> int {
       int v = 0;
-      if (lane < rows / ps) {
+      if (a.page_table && t < T.nbp && lane < rows / ps) {
         const int k = min(t * BN + koff + lane * ps, T.P - 1);
         v = a.page_table[(long long)b * a.pages_per_req + k / ps];
         if (v < 0 || v >= a.n_pages) v = 0;
@@ -480,8 +506,8 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmQ, const CUtensor
     };
     // one ring slot of tile t: K unit u (PAIR: four boxes of 64 head columns x 64
     // keys; else two boxes of 64 head columns x 128 keys) or V unit u (two boxes
-    // of 64 output columns x 128 keys)
-    auto load_unit = [&](int t, bool is_v, int u) -> bool {
+    // of 64 output columns x 128 keys); pg = this lane's page of the tile's box
+    auto load_unit = [&](int t, bool is_v, int u, int pg) -> bool {
       int w_ok = 1;
       if (lane == 0) w_ok = mbar_wait(&empty_bar[slot], phase ^ 1u, abort_flag, a.status);
       if (!__shfl_sync(FULL, w_ok, 0)) return false;
@@ -498,42 +524,30 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmQ, const CUtensor
       const int koff = is_v ? 0 : k_off;         // this CTA's first key of the tile
       const int nbox = (PAIR && !is_v) ? 4 : 2;
       const int box_bytes = rows * 128;
-      int pg = 0;
+      auto col_of = [&](int h) -> int {
+        return PAIR ? (is_v ? dh * DH + (int)rank * 128 + h * 64 : u * 256 + h * 64)
+                    : (is_v ? dh * DH : 0) + u * 128 + h * 64;
+      };
       if (paged) {
-        if (is_v) {
-          if (pv_t != t) {
-            pv_pg = page_idx(t, 0, BN);
-            pv_t = t;
-          }
-          pg = pv_pg;
-        } else {
-          if (pk_t != t) {
-            pk_pg = page_idx(t, koff, K_ROWS);
-            pk_t = t;
-          }
-          pg = pk_pg;
-        }
-      }
-      for (int h = 0; h < nbox; ++h) {
-        int col;
-        if (PAIR)
-          col = is_v ? dh * DH + (int)rank * 128 + h * 64 : u * 256 + h * 64;
-        else
-          col = (is_v ? dh * DH : 0) + u * 128 + h * 64;
-        uint8_t* d = dst + h * box_bytes;
-        if (paged) {
-          if (lane < rows / ps) {
-            if constexpr (PAIR)
-              tma_load_3d_pair(d + lane * ps * 128, m, fb, col, g, pg * ps);
-            else
-              tma_load_3d(d + lane * ps * 128, m, &full_bar[slot], col, g, pg * ps);
-          }
-        } else if (lane == 0) {
-          const int row = (prompt ? b * a.Pmax : b * a.C) + key0 + koff;
+        // one copy per (box, page), all from one instruction: lane l takes page
+        // l % np of box l / np (np x nbox <= 32 for pages of 8 keys or more)
+        const int np = rows / ps;
+        const int pgl = __shfl_sync(FULL, pg, lane % np);
+        if (lane < np * nbox) {
+          const int h = lane / np;
+          uint8_t* d = dst + h * box_bytes + (lane % np) * ps * 128;
           if constexpr (PAIR)
-            tma_load_3d_pair(d, m, fb, col, g, row);
+            tma_load_3d_pair(d, m, fb, col_of(h), g, pgl * ps);
           else
-            tma_load_3d(d, m, &full_bar[slot], col, g, row);
+            tma_load_3d(d, m, &full_bar[slot], col_of(h), g, pgl * ps);
+        }
+      } else if (lane == 0) {
+        const int row = (prompt ? b * a.Pmax : b * a.C) + key0 + koff;
+        for (int h = 0; h < nbox; ++h) {
+          if constexpr (PAIR)
+            tma_load_3d_pair(dst + h * box_bytes, m, fb, col_of(h), g, row);
+          else
+            tma_load_3d(dst + h * box_bytes, m, &full_bar[slot], col_of(h), g, row);
         }
       }
       issued |= 1u << slot;
@@ -544,13 +558,24 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmQ, const CUtensor
       }
       return true;
     };
-    // the MMA warp consumes K(t0), then K(t+1) before V(t) for every tile t
-    for (int u = 0; u < KU && ok && n > 0; ++u) ok = load_unit(T.t_begin, false, u);
+    // the MMA warp consumes K(t0), then K(t+1) before V(t) for every tile t;
+    // pk1 / pv hold the pages of the next K and V loads, read one tile early
+    int pk1 = 0, pv = 0;
+    if (n > 0) {
+      const int pk0 = page_idx(T.t_begin, k_off, K_ROWS);
+      pv = page_idx(T.t_begin, 0, BN);
+      if (n > 1) pk1 = page_idx(T.t_begin + 1, k_off, K_ROWS);
+      for (int u = 0; u < KU && ok; ++u) ok = load_unit(T.t_begin, false, u, pk0);
+    }
     for (int j = 0; j < n && ok; ++j) {
       const int t = T.t_begin + j;
+      const int pk2 = j + 2 < n ? page_idx(t + 2, k_off, K_ROWS) : 0;
+      const int pv1 = j + 1 < n ? page_idx(t + 1, 0, BN) : 0;
       if (j + 1 < n)
-        for (int u = 0; u < KU && ok; ++u) ok = load_unit(t + 1, false, u);
-      for (int u = 0; u < VU && ok; ++u) ok = load_unit(t, true, u);
+        for (int u = 0; u < KU && ok; ++u) ok = load_unit(t + 1, false, u, pk1);
+      for (int u = 0; u < VU && ok; ++u) ok = load_unit(t, true, u, pv);
+      pk1 = pk2;
+      pv = pv1;
     }
     if (!ok && lane == 0 && (!PAIR || rank == 0)) {
       // the loads of both CTAs complete on the even CTA's barriers

@@ -184,6 +184,52 @@ def test_attention_paged_page_sizes(page_size):
                page_size=page_size)
 
 
+@pytest.mark.parametrize("page_size", [16, 128, 24])
+def test_attention_bad_page_entries_are_masked(page_size):
+    """A page-table entry outside the pool (negative or >= n_pages) reads as masked
+    keys and sets DG_DEV_BAD_PAGE: the output equals the oracle's attention over
+    the prompt with that page's keys left out (the prompt keys carry no position,
+    so dropping them is the same as masking them).  Covers the CTA-pair kernel
+    (16), the single-CTA kernel (128) and the warp-level kernel (24)."""
+    from structured_slot_reads_gb300 import configs
+    B, C, plen, hq, hkv, d, W = 2, 64, [700, 300], 8, 2, 512, 16
+    shp = configs.StepShape("t", B=B, C=C, P=max(plen), Hq=hq, Hkv=hkv, d_head=d, W=W, D=8, V=8)
+    x = inputs.attention_inputs(shp, 13, prompt_len=np.array(plen, np.int32))
+    pk, pv, table = inputs.paged_layout(x["kenc"], x["venc"], x["prompt_len"], page_size, 13)
+    n_pages = pk.shape[0]
+    bad = {0: 3, 1: 1}                      # request -> its page index made invalid
+    table = table.copy()
+    table[0, bad[0]] = -1
+    table[1, bad[1]] = n_pages
+    dims = dg.make_dims(B=B, C=C, P_max=max(plen), Hq=hq, Hkv=hkv, d_head=d, W=W)
+    out = torch.empty((B, C, hq, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, hq, C), dtype=torch.float32, device="cuda")
+    ws = torch.empty(dg.dg_workspace_bytes(dims, dg.DG_WS_ATTN, 0), dtype=torch.uint8,
+                     device="cuda")
+    dg.dg_clear_status()
+    rc = dg.dg_attn_decode(dims, dev_bf16(x["q"]), dev_bf16(x["kc"]), dev_bf16(x["vc"]),
+                           dev_bf16(pk), dev_bf16(pv), dev(table), table.shape[1], n_pages,
+                           page_size, dev(x["prompt_len"]), out, lse, ws)
+    assert rc == dg.DG_OK, dg.strerror(rc)
+    torch.cuda.synchronize()
+    assert dg.dg_get_status() & dg.DG_DEV_BAD_PAGE
+    dg.dg_clear_status()
+    # the oracle's prompt: each request's keys without its invalid page
+    kenc = np.zeros_like(x["kenc"])
+    venc = np.zeros_like(x["venc"])
+    plen2 = np.zeros(B, np.int32)
+    for b in range(B):
+        keep = np.ones(plen[b], bool)
+        keep[bad[b] * page_size:(bad[b] + 1) * page_size] = False
+        n = int(keep.sum())
+        kenc[b, :n] = x["kenc"][b, :plen[b]][keep]
+        venc[b, :n] = x["venc"][b, :plen[b]][keep]
+        plen2[b] = n
+    ref, ref_lse = oracle.attn_decode(x["q"], x["kc"], x["vc"], kenc, venc, plen2, W)
+    assert_rel(host(out), ref, what="attention output")
+    assert_abs(host(lse), ref_lse, what="attention lse")
+
+
 def test_slot_noise_rows_bit_exact():
     M, V, D = 64, 1024, 128
     h, w, e, inv_t = _lm_inputs(M, V, D, seed=3)
