@@ -225,7 +225,10 @@ class CallTimer:
 
             def make(fn, n):
                 def inner(*a, **k):
-                    s = torch.cuda.current_stream()
+                    # the call's own stream: its last argument, else the current one
+                    s = k.get("stream", a[-1] if a else None)
+                    if not isinstance(s, torch.cuda.Stream):
+                        s = torch.cuda.current_stream()
                     e0 = torch.cuda.Event(enable_timing=True)
                     e1 = torch.cuda.Event(enable_timing=True)
                     e0.record(s)
@@ -464,13 +467,13 @@ def fill_common(st, shape, device, kv=("kenc", "venc")):
         getattr(st, k).copy_(inputs.device_normal_bf16(getattr(st, k).shape, 1.0, 10 + i, device))
 
 
-def build_runner(kind, shape, device):
+def build_runner(kind, shape, device, concurrent=True):
     import torch
 
     from structured_slot_reads_gb300 import inputs
     from structured_slot_reads_gb300.read import ReadStep, TwoStageRead
     if kind == "step":
-        return build_step(shape, device)
+        return build_step(shape, device, concurrent=concurrent)
     if kind in ("lmhead", "lmhead_fp8"):
         from structured_slot_reads_gb300.read import LmHead
         w = inputs.device_normal_bf16((shape.V, shape.D), shape.D ** -0.5, 1, device)
@@ -530,9 +533,12 @@ def build_runner(kind, shape, device):
     return st
 
 
-def timed_steps(args, run, calls, local, world):
+def timed_steps(args, run, calls, local, world, sched=None):
     """W warm-up steps, then K steps timed with CUDA events on the launching stream.
 
+    ``sched``: a DenoiseStep whose side-stream schedule is timed; its per-call
+    times then come from a second pass of K steps on one stream (events around
+    a call on a shared GPU would time the neighbours too).
     Returns (max-over-ranks ms for K steps, mean ms per library call, kernels
     launched, clock record)."""
     import torch
@@ -541,7 +547,8 @@ def timed_steps(args, run, calls, local, world):
         run(i)
     torch.cuda.synchronize()
     timer = CallTimer(calls)
-    timer.wrap(None)
+    if sched is None:
+        timer.wrap(None)
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.6)
@@ -557,8 +564,15 @@ def timed_steps(args, run, calls, local, world):
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
-    timer.unwrap()
     ms = max_over_ranks(e0.elapsed_time(e1), world)
+    if sched is not None:
+        concurrent, sched.concurrent = sched.concurrent, False
+        timer.wrap(None)
+        for i in range(args.steps):
+            run(args.warmup + args.steps + i)
+        torch.cuda.synchronize()
+        sched.concurrent = concurrent
+    timer.unwrap()
     return ms, {n: timer.mean_ms(n) for n in calls if timer.pairs[n]}, launches, clk
 
 
@@ -570,7 +584,7 @@ def workload_arm(args, rank, world, local):
     kind, shape = workload_shape(args.workload)
     device = f"cuda:{local}"
     torch.cuda.set_device(local)
-    st = build_runner(kind, shape, device)
+    st = build_runner(kind, shape, device, concurrent=args.schedule == "concurrent")
     if kind == "two_stage":
         run = lambda i: st.run()                        # noqa: E731
         calls = ["dg_attn_decode", "dg_slot_read", "dg_ask_if_select"]
@@ -593,7 +607,8 @@ def workload_arm(args, rank, world, local):
                  "dg_denoise_heads",
                  "dg_slot_finish", "dg_commit", "dg_selfcond_from_probs", "dg_canvas_update"]
     dg.dg_clear_status()
-    ms, per_call, launches, clk = timed_steps(args, run, calls, local, world)
+    sched = st if kind == "step" and getattr(st, "concurrent", False) else None
+    ms, per_call, launches, clk = timed_steps(args, run, calls, local, world, sched)
     status = dg.dg_get_status()
     steps_per_s = job_rate(ms, args.steps, world)
     pk = peaks()
@@ -690,7 +705,11 @@ def workload_arm(args, rank, world, local):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": ("inputs larger than L2: E (1.48 GB bf16, 0.74 GB e4m3) streamed "
                           "every pass" if kind.startswith("selfcond") else
-                          "inputs larger than L2: W (1.48 GB) streamed every step")},
+                          "inputs larger than L2: W (1.48 GB) streamed every step"),
+                   "launch": ("eager; slot finish, commit and attention on a side stream beside "
+                              "the self-conditioning GEMM (per-call times from a second, "
+                              "one-stream pass of as many steps)" if sched is not None
+                              else "eager, one stream")},
         "steps_per_s": round(steps_per_s, 3),
         "canvases_per_s": round(steps_per_s * shape.B, 3),
         "slot_decisions_per_s": round(steps_per_s * decisions, 3),

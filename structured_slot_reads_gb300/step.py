@@ -19,7 +19,7 @@ In the fused path (``concurrent=True``, the default) the calls that do not
 feed the self-conditioning GEMM leave the caller's stream once the heads pass
 is done: the slot finish, the commit and the attention run on a side stream
 while dg_selfcond_from_probs streams E (that GEMM is one wave of CTAs on
-fewer than all SMs, so they run on the SMs it leaves free), and the canvas
+7/8 of the SMs, so they run on the SMs it leaves free), and the canvas
 update waits for the commit.  The step is the same work either way;
 ``concurrent=False`` enqueues it in the order above on one stream.
 
