@@ -299,8 +299,9 @@ def gpu_arm(args, rank, world, local):
     g0 = torch.cuda.Event(enable_timing=True)
     g1 = torch.cuda.Event(enable_timing=True)
     g0.record(stream)
+    launches = 0
     for i in range(args.steps):
-        st.replay(args.warmup + i)
+        launches += st.replay(args.warmup + i)
     g1.record(stream)
     torch.cuda.synchronize()
     barrier(world)

@@ -67,9 +67,16 @@ extern "C" {
 
 /* Problem dimensions.  B requests, C canvas tokens each, P_max the longest
  * prompt (encoder KV) length, Hq/Hkv query/KV heads (GQA, Hq % Hkv == 0),
- * d_head in {64, 512}, W the +-W canvas window, d_model, V the vocabulary. */
+ * d_head in {64, 512}, W the +-W canvas window, d_model, V the vocabulary.
+ * sm_share: the number of SMs an attention call (dg_attn_decode,
+ * dg_prefill_attn, dg_attn_mixed) plans its grid for, when other work on
+ * another stream holds the rest of the device: fewer SMs mean fewer key
+ * splits (longer CTAs, less combine work).  0 (or <= 0, or more than the
+ * device has) plans for all SMs.  The attention workspace size depends on it:
+ * size and call with the same dims.  Other calls ignore it. */
 typedef struct {
   int B, C, P_max, Hq, Hkv, d_head, W, d_model, V;
+  int sm_share;
 } dg_dims;
 
 /* ---- a1: decoder-mode attention ----------------------------------------

@@ -85,6 +85,11 @@ int num_sms() {
   return g_sms[dev];
 }
 
+int plan_sms(int share) {
+  const int n = num_sms();
+  return (share > 0 && share < n) ? share : n;
+}
+
 bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
   EncodeTiledFn fn = encode_fn();
@@ -229,7 +234,7 @@ size_t dg_workspace_bytes(const dg_dims* d, int which, int rows) {
     case DG_WS_ATTN:
       if (!attn_dims_ok(d)) return 0;
       return dgi::attn_ws_bytes(d->B, d->C, d->P_max, d->Hq, d->Hkv, d->d_head,
-                                d->W > d->C ? d->C : d->W);
+                                d->W > d->C ? d->C : d->W, d->sm_share);
     case DG_WS_LMHEAD:
       if (!dims_lm(d) || rows < 1) return 0;
       return dgi::lmhead_ws_bytes(rows, d->V);
@@ -253,7 +258,7 @@ size_t dg_workspace_bytes(const dg_dims* d, int which, int rows) {
       return dgi::probs_embed8_ws_bytes(rows, d->V, d->d_model);
     case DG_WS_PREFILL:
       if (!prefill_dims_ok(d)) return 0;
-      return dgi::attn_tc_ws_bytes(d->B, d->P_max, 0, d->Hq, d->Hkv, d->P_max);
+      return dgi::attn_tc_ws_bytes(d->B, d->P_max, 0, d->Hq, d->Hkv, d->P_max, d->sm_share);
     default:
       return 0;
   }
@@ -362,6 +367,7 @@ int dg_attn_decode(const dg_dims* d, const uint16_t* q, const uint16_t* kc, cons
   const size_t need = dg_workspace_bytes(d, DG_WS_ATTN, 0);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return DG_ERR_WORKSPACE;
   dgi::AttnArgs a{};
+  a.sms = d->sm_share;
   a.B = d->B;
   a.C = d->C;
   a.Pmax = d->P_max;
@@ -473,6 +479,7 @@ int dg_prefill_attn(const dg_dims* d, const uint16_t* q, const uint16_t* k, cons
   const size_t need = dg_workspace_bytes(d, DG_WS_PREFILL, 0);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return DG_ERR_WORKSPACE;
   dgi::AttnArgs a{};
+  a.sms = d->sm_share;
   a.B = d->B;
   a.C = d->P_max;
   a.Pmax = 0;
@@ -512,6 +519,7 @@ int dg_attn_mixed(const dg_dims* d, const int32_t* mode, const int32_t* rows_len
                      (long long)pages_per_req * page_size < (long long)d->P_max))
     return DG_ERR_SHAPE;
   dgi::AttnArgs a{};
+  a.sms = d->sm_share;
   a.B = d->B;
   a.C = d->C;
   a.Pmax = d->P_max;

@@ -445,14 +445,14 @@ __global__ void attn_combine_kernel(Args a) {
   if (c4 == 0) a.lse[((long long)b * a.Hq + head) * a.C + pos] = (mt + log2f(lt)) * LN2;
 }
 
-int pick_splits(int B, int C, int Hq, int Hkv, int Pmax, int W) {
+int pick_splits(int B, int C, int Hq, int Hkv, int Pmax, int W, int sms) {
   const int G = Hq / Hkv;
   const int npos = BMQ / G;
   const int q_blocks = (C + npos - 1) / npos;
   const int base = q_blocks * Hkv * B;
   const int keys = Pmax + std::min(C, npos + 2 * W);
   const int tiles = std::max(1, (keys + BNK - 1) / BNK);
-  int s = std::max(1, dgi::num_sms() / std::max(1, base));
+  int s = std::max(1, sms / std::max(1, base));
   return std::min(s, tiles);
 }
 
@@ -469,7 +469,7 @@ cudaError_t run(const dgi::AttnArgs& x, void* ws, cudaStream_t st) {
   a.G = x.Hq / x.Hkv;
   a.npos = BMQ / a.G;
   a.q_blocks = (x.C + a.npos - 1) / a.npos;
-  a.splits = pick_splits(x.B, x.C, x.Hq, x.Hkv, x.Pmax, a.W);
+  a.splits = pick_splits(x.B, x.C, x.Hq, x.Hkv, x.Pmax, a.W, dgi::plan_sms(x.sms));
   a.q = reinterpret_cast<const __nv_bfloat16*>(x.q);
   a.kc = reinterpret_cast<const __nv_bfloat16*>(x.kc);
   a.vc = reinterpret_cast<const __nv_bfloat16*>(x.vc);
@@ -505,12 +505,12 @@ cudaError_t run(const dgi::AttnArgs& x, void* ws, cudaStream_t st) {
 
 namespace dgi {
 
-size_t attn_ws_bytes(int B, int C, int Pmax, int Hq, int Hkv, int d, int W) {
-  const int s = pick_splits(B, C, Hq, Hkv, Pmax, std::min(W, C));
+size_t attn_ws_bytes(int B, int C, int Pmax, int Hq, int Hkv, int d, int W, int sms) {
+  const int s = pick_splits(B, C, Hq, Hkv, Pmax, std::min(W, C), plan_sms(sms));
   size_t bytes = 256;
   if (s > 1) bytes = align_up((size_t)s * B * C * Hq * d * 4 + (size_t)s * B * Hq * C * 8, 256);
   // d = 512 runs on the tensor-core kernel unless its page size is unsupported
-  if (d == 512) bytes = std::max(bytes, attn_tc_ws_bytes(B, C, Pmax, Hq, Hkv, W));
+  if (d == 512) bytes = std::max(bytes, attn_tc_ws_bytes(B, C, Pmax, Hq, Hkv, W, sms));
   return bytes;
 }
 

@@ -716,14 +716,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 // Splits of the key range: enough CTAs to fill the SMs; for long key ranges a
 // multiple of the SM count, as long as every split keeps at least 16 tiles.
 // pair: CTA pairs over 256-row tiles (two CTAs per tile).
-int tc_splits(int B, int C, int Hq, int Hkv, int Pmax, int W, bool pair) {
+int tc_splits(int B, int C, int Hq, int Hkv, int Pmax, int W, bool pair, int sms) {
   const int G = Hq / Hkv;
   const int npos = (pair ? 2 : 1) * (BM / G);      // canvas positions of one tile
   const int q_blocks = (C + npos - 1) / npos;
   const int base = B * Hkv * q_blocks * 2 * (pair ? 2 : 1);
   const int keys_c = std::min(C, npos + 2 * W);
   const int nb = std::max(1, (Pmax + BN - 1) / BN + (keys_c + BN - 1) / BN);
-  const int sms = dgi::num_sms();
   int s = std::max(1, sms / base);
   for (int c = s + 1; c <= nb / 16; ++c)
     if ((long long)base * c % sms == 0) {
@@ -752,11 +751,12 @@ bool attn_pair_ok(const AttnArgs& x) {
   return attn_tc_supported(x) && (!x.page_table || (BN / 2) % x.page_size == 0);
 }
 
-size_t attn_tc_ws_bytes(int B, int C, int Pmax, int Hq, int Hkv, int W) {
+size_t attn_tc_ws_bytes(int B, int C, int Pmax, int Hq, int Hkv, int W, int sms) {
   // sized for either kernel (the pair kernel is chosen per call from the page size)
   const int w = std::min(W, C);
-  const int s = std::max(tc_splits(B, C, Hq, Hkv, Pmax, w, false),
-                         tc_splits(B, C, Hq, Hkv, Pmax, w, true));
+  const int n = plan_sms(sms);
+  const int s = std::max(tc_splits(B, C, Hq, Hkv, Pmax, w, false, n),
+                         tc_splits(B, C, Hq, Hkv, Pmax, w, true, n));
   if (s == 1) return 256;
   return align_up((size_t)s * B * C * Hq * HD * 4 + (size_t)s * B * Hq * C * 8, 256);
 }
@@ -773,7 +773,7 @@ cudaError_t attn_decode_tc(const AttnArgs& x, void* ws, cudaStream_t st) {
   const bool pair = attn_pair_ok(x);
   a.npos = (pair ? 2 : 1) * (BM / a.G);   // canvas positions of one tile
   a.q_blocks = (x.C + a.npos - 1) / a.npos;
-  a.splits = tc_splits(x.B, x.C, x.Hq, x.Hkv, x.Pmax, a.W, pair);
+  a.splits = tc_splits(x.B, x.C, x.Hq, x.Hkv, x.Pmax, a.W, pair, plan_sms(x.sms));
   a.causal = x.causal;
   a.seq_len = x.seq_len;
   a.mode = x.mode;

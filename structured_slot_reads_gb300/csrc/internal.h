@@ -10,6 +10,9 @@ namespace dgi {
 // Device address of the library's status word (set-up once per device).
 int* status_ptr();
 int num_sms();
+// SMs a launch plans its grid for: the caller's share when it is in (0, num_sms()),
+// else the whole device.
+int plan_sms(int share);
 // Build a 2-D TMA map over a row-major bf16 matrix [outer, inner] whose rows are
 // row_bytes apart, with a (box_inner x box_outer) box and 128-byte swizzle.
 // Returns false on failure.
@@ -82,8 +85,9 @@ struct AttnArgs {
   const int32_t* seq_len = nullptr;   // causal: rows per request (q/k/v are [B, C, H, d])
   const int32_t* mode = nullptr;      // mixed batch: per request 1 = causal, 0 = decoder
   const int32_t* rows_len = nullptr;  // mixed batch: valid rows per request
+  int sms = 0;                        // SMs to plan the grid for (0: all of the device)
 };
-size_t attn_ws_bytes(int B, int C, int Pmax, int Hq, int Hkv, int d, int W);
+size_t attn_ws_bytes(int B, int C, int Pmax, int Hq, int Hkv, int d, int W, int sms);
 cudaError_t attn_decode(const AttnArgs& a, void* ws, cudaStream_t st);
 // Merge split-KV partials ([splits][B][C][Hq][d] fp32 O, [splits][B][Hq][C] (m, l));
 // with seq_len, rows at or past seq_len[b] are left untouched.
@@ -92,7 +96,7 @@ cudaError_t attn_combine(int B, int C, int Hq, int d, int splits, float* ws_o, f
                          const int32_t* seq_len = nullptr);
 // d = 512 on tcgen05 (attn_tc.cu): 128 query rows x 256 output columns per CTA.
 bool attn_tc_supported(const AttnArgs& a);
-size_t attn_tc_ws_bytes(int B, int C, int Pmax, int Hq, int Hkv, int W);
+size_t attn_tc_ws_bytes(int B, int C, int Pmax, int Hq, int Hkv, int W, int sms);
 cudaError_t attn_decode_tc(const AttnArgs& a, void* ws, cudaStream_t st);
 // Copy the first seq_len[b] rows of k, v [B, P, Hkv, d] into the page pools
 // [n_pages, page_size, Hkv, d] through page_table [B, pages_per_req].

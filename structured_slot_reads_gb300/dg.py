@@ -35,17 +35,17 @@ class DgError(RuntimeError):
 
 class Dims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
-                ("B", "C", "P_max", "Hq", "Hkv", "d_head", "W", "d_model", "V")]
+                ("B", "C", "P_max", "Hq", "Hkv", "d_head", "W", "d_model", "V", "sm_share")]
 
 
-def make_dims(B=1, C=1, P_max=0, Hq=1, Hkv=1, d_head=64, W=0, d_model=8, V=8):
-    return Dims(B, C, P_max, Hq, Hkv, d_head, W, d_model, V)
+def make_dims(B=1, C=1, P_max=0, Hq=1, Hkv=1, d_head=64, W=0, d_model=8, V=8, sm_share=0):
+    return Dims(B, C, P_max, Hq, Hkv, d_head, W, d_model, V, sm_share)
 
 
-def dims_of(shape):
+def dims_of(shape, sm_share=0):
     """Dims from a configs.StepShape."""
     return Dims(shape.B, shape.C, shape.P, shape.Hq, shape.Hkv, shape.d_head, shape.W,
-                shape.D, shape.V)
+                shape.D, shape.V, sm_share)
 
 
 _lib = None

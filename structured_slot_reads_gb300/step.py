@@ -19,8 +19,9 @@ In the fused path (``concurrent=True``, the default) the calls that do not
 feed the self-conditioning GEMM leave the caller's stream once the heads pass
 is done: the slot finish, the commit and the attention run on a side stream
 while dg_selfcond_from_probs streams E (that GEMM is one wave of CTAs on
-7/8 of the SMs, so they run on the SMs it leaves free), and the canvas
-update waits for the commit.  The step is the same work either way;
+7/8 of the SMs, so they run on the SMs it leaves free; the attention plans
+its grid for that eighth, ``dims.sm_share``), and the canvas update waits
+for the commit.  The step is the same work either way;
 ``concurrent=False`` enqueues it in the order above on one stream.
 
 ``fused=False`` runs the unfused calls instead (dg_lmhead_logsoftmax_entropy,
@@ -112,7 +113,13 @@ class DenoiseStep:
         self.committed = torch.zeros((B, C), dtype=u8, device=dev)
         self.tok_state = torch.full((B, C), -1, dtype=i32, device=dev)
         self.e_sc = _empty((self.M, D), f32, dev)
-        self.ws_attn = _empty((max(dg.dg_workspace_bytes(self.dims, dg.DG_WS_ATTN, 0), 256),), u8, dev)
+        # beside the self-conditioning GEMM (which plans for 7/8 of the SMs) the
+        # attention plans its grid for the SMs left over: fewer key splits
+        n_sm = dg.dg_num_sms()
+        self.dims_side = dg.dims_of(shape, sm_share=max(1, n_sm - n_sm * 7 // 8))
+        self.ws_attn = _empty((max(dg.dg_workspace_bytes(self.dims, dg.DG_WS_ATTN, 0),
+                                   dg.dg_workspace_bytes(self.dims_side, dg.DG_WS_ATTN, 0),
+                                   256),), u8, dev)
         # slots (same table for every request)
         self.with_slots = with_slots and len(shape.slots) > 0
         self.seed = seed
@@ -208,10 +215,14 @@ class DenoiseStep:
                                self.M, self.h, stream), "dg_canvas_update")
         return self.kernels_per_step()
 
+    def _attn_dims(self):
+        """The attention's dims: on the side stream it plans for the SMs the GEMM leaves."""
+        return self.dims_side if self.concurrent else self.dims
+
     def _attention(self, stream):
-        dg._check(dg.dg_attn_decode(self.dims, self.q, self.kc, self.vc, self.kenc, self.venc,
-                                    None, 0, 0, 0, self.prompt_len, self.attn_out, self.attn_lse,
-                                    self.ws_attn, stream), "dg_attn_decode")
+        dg._check(dg.dg_attn_decode(self._attn_dims(), self.q, self.kc, self.vc, self.kenc,
+                                    self.venc, None, 0, 0, 0, self.prompt_len, self.attn_out,
+                                    self.attn_lse, self.ws_attn, stream), "dg_attn_decode")
 
     def _selfcond(self, stream):
         dg._check(dg.dg_selfcond_from_probs(self.dims, self.probs, self.probs_ld, self.prob_scale,
@@ -293,7 +304,7 @@ class DenoiseStep:
         return n
 
     def _attn_splits(self):
-        return 1 if dg.dg_workspace_bytes(self.dims, dg.DG_WS_ATTN, 0) <= 256 else 2
+        return 1 if dg.dg_workspace_bytes(self._attn_dims(), dg.DG_WS_ATTN, 0) <= 256 else 2
 
     # ------------------------------------------------------- host round trip
     def host_buffers(self):

@@ -134,6 +134,22 @@ def test_binding_constants_match_header():
         assert getattr(dg, name) == int(val), f"{name}: binding {getattr(dg, name)} != header {val}"
 
 
+def test_binding_dims_match_header():
+    """dg_dims in the header and the binding's ctypes structure: same int fields, same order."""
+    text = open(HEADER).read()
+    body = re.search(r"typedef struct \{(.*?)\} dg_dims;", text, re.S).group(1)
+    fields = []
+    for decl in body.split(";"):
+        decl = decl.strip()
+        if decl:
+            assert decl.startswith("int "), decl
+            fields += [f.strip() for f in decl[4:].split(",")]
+    assert [f for f, _ in dg.Dims._fields_] == fields
+    assert all(t is ctypes.c_int for _, t in dg.Dims._fields_)
+    assert ctypes.sizeof(dg.Dims) == 4 * len(fields)
+    assert dg.make_dims().sm_share == 0 and dg.make_dims(sm_share=19).sm_share == 19
+
+
 @pytest.mark.parametrize("fused", [True, False])
 def test_step_runner_builds_on_host(lib, fused):
     """The step runner's set-up uses only host-side library calls (workspace sizes)."""

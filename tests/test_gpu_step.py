@@ -226,7 +226,10 @@ def test_concurrent_schedule_equals_serial(size):
     """The side-stream schedule (slot finish, commit and attention beside the
     self-conditioning GEMM) computes the same step: three consecutive steps,
     eager and replayed as graphs, equal the one-stream schedule bit for bit,
-    carried state included."""
+    carried state included.  The attention alone may differ in rounding: on
+    the side stream it plans for fewer SMs (fewer key splits, another
+    summation order), so it is compared within the attention tolerance and
+    against the oracle."""
     if size == "tiny":
         shape, x, _ = _tiny_inputs(3)
     else:
@@ -255,8 +258,15 @@ def test_concurrent_schedule_equals_serial(size):
         return out
 
     serial = steps(False, False)
+    ref, ref_lse = oracle.attn_decode(x["q"], x["kc"], x["vc"], x["kenc"], x["venc"],
+                                      x["prompt_len"], shape.W)
     for graphs in (False, True):
         got = steps(True, graphs)
         for t in range(3):
             for k in keys:
+                if k in ("attn_out", "attn_lse"):
+                    continue
                 assert np.array_equal(got[t][k], serial[t][k]), (graphs, t, k)
+            assert_rel(got[t]["attn_out"], ref, what="side-stream attention")
+            assert_abs(got[t]["attn_lse"], ref_lse, what="side-stream attention lse")
+            assert_rel(got[t]["attn_out"], serial[t]["attn_out"], what="attention, two schedules")
