@@ -95,11 +95,12 @@ def test_selfcond_embed(M, V, D):
     assert_rel(host(out), oracle.selfcond_embed(h, w, e, inv_t), what="expected embedding")
 
 
-def _attn_case(B, C, plen, hq, hkv, d, W, seed, paged=False, page_size=16):
+def _attn_case(B, C, plen, hq, hkv, d, W, seed, paged=False, page_size=16, sm_share=0):
     from structured_slot_reads_gb300 import configs
     shp = configs.StepShape("t", B=B, C=C, P=max(plen), Hq=hq, Hkv=hkv, d_head=d, W=W, D=8, V=8)
     x = inputs.attention_inputs(shp, seed, prompt_len=np.array(plen, np.int32))
-    dims = dg.make_dims(B=B, C=C, P_max=max(plen), Hq=hq, Hkv=hkv, d_head=d, W=W)
+    dims = dg.make_dims(B=B, C=C, P_max=max(plen), Hq=hq, Hkv=hkv, d_head=d, W=W,
+                        sm_share=sm_share)
     out = torch.empty((B, C, hq, d), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((B, hq, C), dtype=torch.float32, device="cuda")
     ws = torch.empty(dg.dg_workspace_bytes(dims, dg.DG_WS_ATTN, 0), dtype=torch.uint8,
@@ -137,6 +138,16 @@ def _attn_case(B, C, plen, hq, hkv, d, W, seed, paged=False, page_size=16):
 ])
 def test_attention_contiguous(case):
     _attn_case(**case, seed=11)
+
+
+@pytest.mark.parametrize("sm_share", [1, 19, 40, 100000])
+def test_attention_sm_share(sm_share):
+    """Planning for a share of the SMs changes the key splits (1 SM: one split, no
+    combine; more than the device has: all SMs), never the result beyond rounding:
+    the full-canvas attention shape and a paged ragged batch match the oracle."""
+    _attn_case(B=1, C=256, plen=[4096], hq=8, hkv=2, d=512, W=128, seed=3, sm_share=sm_share)
+    _attn_case(B=3, C=64, plen=[700, 129, 0], hq=8, hkv=2, d=512, W=16, seed=4, paged=True,
+               sm_share=sm_share)
 
 
 def test_attention_rescales_when_late_keys_dominate():
