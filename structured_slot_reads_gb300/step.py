@@ -273,10 +273,9 @@ class DenoiseStep:
         if self.concurrent:
             self.ev_commit.record(side)
             self._attention(side)
+            main.wait_event(self.ev_commit)     # the update reads the commit's state
         else:
             self._selfcond(main)
-        if self.concurrent:
-            main.wait_event(self.ev_commit)
         ck(dg.dg_canvas_update(d, self.h0, self.e_sc, self.e, self.tok_state, self.committed,
                                self.M, self.h, main), "dg_canvas_update")
         if self.concurrent:
