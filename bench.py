@@ -588,7 +588,8 @@ def workload_arm(args, rank, world, local):
     st = build_runner(kind, shape, device, concurrent=args.schedule == "concurrent")
     if kind == "two_stage":
         run = lambda i: st.run()                        # noqa: E731
-        calls = ["dg_attn_decode", "dg_slot_read", "dg_ask_if_select"]
+        calls = ["dg_attn_decode", "dg_slot_noise", "dg_lmhead_logsoftmax_entropy",
+                 "dg_slot_finish", "dg_ask_if_select"]
     elif kind == "prefill":
         run = lambda i: st.run(step_idx=i)              # noqa: E731
         calls = ["dg_prefill_attn"]
@@ -644,13 +645,14 @@ def workload_arm(args, rank, world, local):
         work["dg_slot_read_wide"] = work["dg_slot_read"]
         decisions = st.S
     elif kind == "two_stage":
-        rows = (st.S1 + st.S2) * R / 2                  # mean draw rows of the two passes
-        work["dg_slot_read"] = (Wb + rows * D * 4, 2.0 * rows * V * D)
+        rows = (st.S1 + st.S2) * R                      # draw rows of both stages, one W pass
+        work["dg_lmhead_logsoftmax_entropy"] = (Wb + rows * D * 2 + rows * 16,
+                                                2.0 * rows * V * D)
         decisions = st.decisions()
     else:
         decisions = getattr(st, "S", 0)
     kernels, best = {}, None
-    n_calls = {"dg_slot_read": 2} if kind == "two_stage" else {}
+    n_calls = {"dg_slot_noise": 2, "dg_slot_finish": 2} if kind == "two_stage" else {}
     # e4m3 contractions against their own peak: the measured bf16 figure times the
     # nominal e4m3 / bf16 ratio (4.5 / 2.25 PFLOP/s dense)
     e4m3 = ("dg_lmhead_logsoftmax_entropy_fp8", "dg_selfcond_from_probs8")

@@ -249,7 +249,7 @@ __global__ void slot_epilogue_kernel(const float* lse_rows, const int32_t* n_lab
 // a7: ask_if gating (sotaaz.com, "The server accepts at most 26 alternatives per
 // question": a question carrying ask_if is read only when the earlier answer
 // matches).  Thread per question: fired = chosen1[cond_slot] == cond_value.
-// Thread per stage-2 slot: the first fired question that owns the slot copies
+// Warp per stage-2 slot: the first fired question that owns the slot copies
 // its labels into the stage-2 table; with none, n_labels2 = 0 (not read).
 // ---------------------------------------------------------------------------
 __global__ void ask_if_kernel(const int32_t* chosen1, int S1, const int32_t* cond_slot,
@@ -266,16 +266,29 @@ __global__ void ask_if_kernel(const int32_t* chosen1, int S1, const int32_t* con
     }
     return chosen1[cs] == cond_value[q];
   };
+  // one thread per question: did it fire
   if (i < Q && fired) fired[i] = fires(i) ? 1 : 0;
-  if (i < S2) {
-    int pick = -1;
-    for (int q = 0; q < Q && pick < 0; ++q)
-      if (q_owner[q] == i && fires(q)) pick = q;
+  // one warp per stage-2 slot: the lowest-index fired question it owns (each
+  // lane stops at its first, the warp takes the minimum), labels copied by lane
+  const int slot = i >> 5, lane = threadIdx.x & 31;
+  if (slot < S2) {
+    int first = 0x7fffffff;
+    for (int q = lane; q < Q; q += 32)
+      if (q_owner[q] == slot && fires(q)) {
+        first = q;
+        break;
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) first = min(first, __shfl_xor_sync(0xffffffffu, first, o));
+    const int pick = first == 0x7fffffff ? -1 : first;
     const int n = pick >= 0 ? q_n_labels[pick] : 0;
-    n_labels2[i] = (n >= 0 && n <= MAXL) ? n : 0;
-    if (n < 0 || n > MAXL) atomicOr(status, 4 /* DG_DEV_BAD_LABEL */);
-    for (int k = 0; k < MAXL; ++k)
-      label_ids2[i * MAXL + k] = (pick >= 0 && k < n) ? q_label_ids[pick * MAXL + k] : -1;
+    if (lane == 0) {
+      n_labels2[slot] = (n >= 0 && n <= MAXL) ? n : 0;
+      if (n < 0 || n > MAXL) atomicOr(status, 4 /* DG_DEV_BAD_LABEL */);
+    }
+    if (lane < MAXL)
+      label_ids2[slot * MAXL + lane] = (pick >= 0 && lane < n) ? q_label_ids[pick * MAXL + lane]
+                                                              : -1;
   }
 }
 
@@ -491,9 +504,9 @@ cudaError_t ask_if_select(const int32_t* chosen1, int S1, const int32_t* cond_sl
                           const int32_t* q_label_ids, const int32_t* q_n_labels, int Q, int S2,
                           int32_t* label_ids2, int32_t* n_labels2, uint8_t* fired,
                           cudaStream_t st) {
-  const int n = Q > S2 ? Q : S2;
+  const long long n = std::max<long long>(Q, 32LL * S2);
   if (n == 0) return cudaSuccess;
-  ask_if_kernel<<<(n + 127) / 128, 128, 0, st>>>(chosen1, S1, cond_slot, cond_value, q_owner,
+  ask_if_kernel<<<(int)((n + 127) / 128), 128, 0, st>>>(chosen1, S1, cond_slot, cond_value, q_owner,
                                                   q_label_ids, q_n_labels, Q, S2, label_ids2,
                                                   n_labels2, fired, status_ptr());
   return cudaGetLastError();

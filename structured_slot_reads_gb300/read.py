@@ -7,10 +7,19 @@ stage re-reads a slot four times when its first read's entropy exceeds 0.1.
 One ``TwoStageRead.run`` is, for every request of the batch:
 
   dg_attn_decode      decoder attention of the canvas over its paged prompt KV
-  dg_slot_read        stage 1: group slot + 0-3 other slots (noise draws, one
-                      W pass over all draw rows, gated read)
+  dg_slot_noise       noised draw rows of stage 1 (group slot + 0-3 other
+                      slots) and of stage 2 (the item slot), each stage with
+                      its own step index in the Philox counter
+  dg_lmhead_logsoftmax_entropy
+                      one W pass over the draw rows of both stages: their
+                      full-vocabulary lse does not depend on which labels a
+                      slot is read with, so stage 2 needs no pass of its own
+  dg_slot_finish      stage 1: label logits, renormalise, gate, average
   dg_ask_if_select    stage-2 slot table from the stage-1 answers (on device)
-  dg_slot_read        stage 2: the chosen group's item slot
+  dg_slot_finish      stage 2, with the labels of the question that fired
+
+This is dg_slot_read for each stage (noise, one W pass, finish) with the two
+W passes made one.
 
 Torch allocates every buffer; the library only enqueues work.
 """
@@ -106,22 +115,36 @@ class TwoStageRead:
         d = self.dims
         self.ws_attn = torch.empty(max(dg.dg_workspace_bytes(d, dg.DG_WS_ATTN, 0), 256),
                                    dtype=u8, device=device)
-        self.ws_read = torch.empty(dg.dg_workspace_bytes(d, dg.DG_WS_SLOT_READ,
-                                                         max(self.S1, self.S2) * R),
-                                   dtype=u8, device=device)
+        # the draw rows of both stages (stage 1 first) and their statistics
+        self.r1 = self.S1 * R
+        n = self.r1 + self.S2 * R
+        self.draw_rows = torch.empty((n, D), dtype=bf, device=device)
+        self.inv_t_draw = torch.empty(n, dtype=f32, device=device)
+        self.lse_draw = torch.empty(n, dtype=f32, device=device)
+        self.ent_draw = torch.empty(n, dtype=f32, device=device)
+        self.maxz_draw = torch.empty(n, dtype=f32, device=device)
+        self.arg_draw = torch.empty(n, dtype=i32, device=device)
+        self.ws_lm = torch.empty(dg.dg_workspace_bytes(d, dg.DG_WS_LMHEAD, n), dtype=u8,
+                                 device=device)
 
     def set_kv(self, pool_k, pool_v, page_table):
         self.pool_k, self.pool_v = pool_k, pool_v
         self.page_table = page_table
         self.n_pages = pool_k.shape[0]
 
-    def _read(self, S, slot_row, slot_req, label_ids, n_labels, out, step, stream):
+    def _noise(self, S, slot_row, slot_req, rows, out, step, stream):
         s = self.shape
-        dg._check(dg.dg_slot_read(self.dims, self.h, self.M, self.w, self.e, self.inv_t,
-                                  slot_row, slot_req, label_ids, n_labels, S, self.seed, step,
-                                  s.R, s.gate, out["q_avg"], out["h_slot"], out["chosen"],
-                                  out["lp"], out["resampled"], out["n_reads"], out["tokens"],
-                                  self.ws_read, stream), "dg_slot_read")
+        dg._check(dg.dg_slot_noise(self.dims, self.h, self.M, self.e, self.inv_t, slot_row,
+                                   slot_req, S, s.R, self.seed, step, self.draw_rows[rows],
+                                   self.inv_t_draw[rows], out["tokens"], stream), "dg_slot_noise")
+
+    def _finish(self, S, label_ids, n_labels, rows, out, stream):
+        s = self.shape
+        dg._check(dg.dg_slot_finish(self.dims, self.draw_rows[rows], self.inv_t_draw[rows],
+                                    self.lse_draw[rows], self.w, label_ids, n_labels, S, s.R,
+                                    s.R, s.gate, out["q_avg"], out["h_slot"], out["chosen"],
+                                    out["lp"], out["resampled"], out["n_reads"], stream),
+                  "dg_slot_finish")
 
     def run(self, stream=None):
         """Enqueue attention + both read stages; returns the number of library kernels."""
@@ -130,16 +153,24 @@ class TwoStageRead:
                                     self.n_pages, self.shape.page_size, self.prompt_len,
                                     self.attn_out, self.attn_lse, self.ws_attn, stream),
                   "dg_attn_decode")
-        self._read(self.S1, self.slot_row1, self.slot_req1, self.label_ids1, self.n_labels1,
-                   self.out1, 0, stream)
+        st1, st2 = slice(0, self.r1), slice(self.r1, None)
+        self._noise(self.S1, self.slot_row1, self.slot_req1, st1, self.out1, 0, stream)
+        self._noise(self.S2, self.slot_row2, self.slot_req2, st2, self.out2, 1, stream)
+        dg._check(dg.dg_lmhead_logsoftmax_entropy(self.dims, self.draw_rows,
+                                                  self.draw_rows.shape[0], self.w,
+                                                  self.inv_t_draw, self.lse_draw, self.ent_draw,
+                                                  self.maxz_draw, self.arg_draw, self.ws_lm,
+                                                  stream), "dg_lmhead_logsoftmax_entropy")
+        self._finish(self.S1, self.label_ids1, self.n_labels1, st1, self.out1, stream)
         dg._check(dg.dg_ask_if_select(self.out1["chosen"], self.S1, self.cond_slot,
                                       self.cond_value, self.q_owner, self.q_label_ids,
                                       self.q_n_labels, self.Q, self.S2, self.label_ids2,
                                       self.n_labels2, self.fired, stream), "dg_ask_if_select")
-        self._read(self.S2, self.slot_row2, self.slot_req2, self.label_ids2, self.n_labels2,
-                   self.out2, 1, stream)
+        self._finish(self.S2, self.label_ids2, self.n_labels2, st2, self.out2, stream)
         attn_kernels = 1 if dg.dg_workspace_bytes(self.dims, dg.DG_WS_ATTN, 0) <= 256 else 2
-        return attn_kernels + 5 + 1 + 5   # a slot read: noise, stats, finalize, logits, epilogue
+        # noise x 2, one W pass (stats + finalize), finish (label logits + epilogue) x 2,
+        # ask_if
+        return attn_kernels + 2 + 2 + 4 + 1
 
     def decisions(self):
         """Slot decisions completed by one run (stage-1 slots + asked stage-2 slots)."""

@@ -113,12 +113,14 @@ def test_two_stage_reduced():
         _check_stage(tr.out2, st2, n2, _exact(st2, n2, shape.gate))
 
 
-def test_ask_if_select_matches_oracle():
-    rng = np.random.default_rng(7)
-    S1, S2, Q = 10, 6, 40
+@pytest.mark.parametrize("S1,S2,Q", [(10, 6, 40), (30, 40, 300), (5, 1, 3), (4, 3, 97)])
+def test_ask_if_select_matches_oracle(S1, S2, Q):
+    """Several fired questions per stage-2 slot (the lowest index wins), slots with
+    none, more questions than a warp's lanes, and out-of-range conditions."""
+    rng = np.random.default_rng(7 + Q)
     chosen1 = rng.integers(-1, 5, S1).astype(np.int32)
     cs = rng.integers(0, S1, Q).astype(np.int32)
-    cs[[3, 17]] = [S1, -1]                                   # out of range: flagged, never fire
+    cs[[1, Q - 1]] = [S1, -1]                                # out of range: flagged, never fire
     cv = rng.integers(0, 5, Q).astype(np.int32)
     own = rng.integers(0, S2, Q).astype(np.int32)
     qn = rng.integers(1, 27, Q).astype(np.int32)
