@@ -71,8 +71,9 @@ extern "C" {
  * sm_share: the number of SMs an attention call (dg_attn_decode,
  * dg_prefill_attn, dg_attn_mixed) plans its grid for, when other work on
  * another stream holds the rest of the device: fewer SMs mean fewer key
- * splits (longer CTAs, less combine work).  0 (or <= 0, or more than the
- * device has) plans for all SMs.  The attention workspace size depends on it:
+ * splits (longer CTAs, less combine work), as long as no CTA gets more than
+ * 40 key tiles of 128 keys; longer key ranges are split as for the whole
+ * device.  0 (or <= 0, or more than the device has) plans for all SMs.  The attention workspace size depends on it:
  * size and call with the same dims.  Other calls ignore it. */
 typedef struct {
   int B, C, P_max, Hq, Hkv, d_head, W, d_model, V;

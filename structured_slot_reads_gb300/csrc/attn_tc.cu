@@ -715,7 +715,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
 // Splits of the key range: enough CTAs to fill the SMs; for long key ranges a
 // multiple of the SM count, as long as every split keeps at least 16 tiles.
-// pair: CTA pairs over 256-row tiles (two CTAs per tile).
+// pair: CTA pairs over 256-row tiles (two CTAs per tile).  With a share of the
+// SMs (sms < the device's), the splits fill the share while no CTA gets more
+// than SHARE_MAX_TILES key tiles (about 100 us); beyond that the CTAs that do
+// not fit beside the other work run after it, where shorter ones finish sooner,
+// so the key range is split for the whole device instead.
+constexpr int SHARE_MAX_TILES = 40;
 int tc_splits(int B, int C, int Hq, int Hkv, int Pmax, int W, bool pair, int sms) {
   const int G = Hq / Hkv;
   const int npos = (pair ? 2 : 1) * (BM / G);      // canvas positions of one tile
@@ -723,6 +728,9 @@ int tc_splits(int B, int C, int Hq, int Hkv, int Pmax, int W, bool pair, int sms
   const int base = B * Hkv * q_blocks * 2 * (pair ? 2 : 1);
   const int keys_c = std::min(C, npos + 2 * W);
   const int nb = std::max(1, (Pmax + BN - 1) / BN + (keys_c + BN - 1) / BN);
+  const int all = dgi::num_sms();
+  if (sms < all && (nb + std::max(1, sms / base) - 1) / std::max(1, sms / base) > SHARE_MAX_TILES)
+    sms = all;
   int s = std::max(1, sms / base);
   for (int c = s + 1; c <= nb / 16; ++c)
     if ((long long)base * c % sms == 0) {
