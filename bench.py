@@ -517,7 +517,7 @@ def build_runner(kind, shape, device, concurrent=True):
     w = inputs.device_normal_bf16((shape.V, shape.D), shape.D ** -0.5, 1, device)
     e = inputs.device_normal_bf16((shape.V, shape.D), shape.D ** -0.5, 2, device)
     if kind == "read":
-        st = ReadStep(shape, w, e, device=device, seed=7)
+        st = ReadStep(shape, w, e, device=device, seed=7, concurrent=concurrent)
         fill_common(st, shape, device)
     else:
         plen = inputs.prompt_lengths(shape, 5)
@@ -609,7 +609,7 @@ def workload_arm(args, rank, world, local):
                  "dg_denoise_heads",
                  "dg_slot_finish", "dg_commit", "dg_selfcond_from_probs", "dg_canvas_update"]
     dg.dg_clear_status()
-    sched = st if kind == "step" and getattr(st, "concurrent", False) else None
+    sched = st if kind in ("step", "read") and getattr(st, "concurrent", False) else None
     ms, per_call, launches, clk = timed_steps(args, run, calls, local, world, sched)
     status = dg.dg_get_status()
     steps_per_s = job_rate(ms, args.steps, world)
@@ -709,10 +709,13 @@ def workload_arm(args, rank, world, local):
                    "l2": ("inputs larger than L2: E (1.48 GB bf16, 0.74 GB e4m3) streamed "
                           "every pass" if kind.startswith("selfcond") else
                           "inputs larger than L2: W (1.48 GB) streamed every step"),
-                   "launch": ("eager; slot finish, commit and attention on a side stream beside "
-                              "the self-conditioning GEMM (per-call times from a second, "
-                              "one-stream pass of as many steps)" if sched is not None
-                              else "eager, one stream")},
+                   "launch": ("eager; " + ("slot finish, commit and attention on a side "
+                                           "stream beside the self-conditioning GEMM"
+                                           if kind == "step" else
+                                           "attention on a side stream beside the slot "
+                                           "read's W pass")
+                              + " (per-call times from a second, one-stream pass of as many "
+                                "steps)" if sched is not None else "eager, one stream")},
         "steps_per_s": round(steps_per_s, 3),
         "canvases_per_s": round(steps_per_s * shape.B, 3),
         "slot_decisions_per_s": round(steps_per_s * decisions, 3),

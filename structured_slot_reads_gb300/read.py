@@ -27,6 +27,7 @@ import numpy as np
 import torch
 
 from . import dg, inputs
+from .step import _as_stream
 
 
 def _dev(a, dtype, device):
@@ -184,10 +185,13 @@ class ReadStep:
     the answer slots are left blank and one denoise forward gives the label
     distribution of every slot.  One ``run`` is dg_attn_decode over the
     contiguous prompt KV plus one dg_slot_read over the slot table of every
-    request (the same slots in every request).
+    request (the same slots in every request).  The two do not feed each
+    other: with ``concurrent=True`` (the default) the attention goes first on a
+    side stream, planned for an eighth of the SMs (``dims.sm_share``), and the
+    slot read's W pass takes the SMs it leaves.
     """
 
-    def __init__(self, shape, w, e, device="cuda", seed=0):
+    def __init__(self, shape, w, e, device="cuda", seed=0, concurrent=True):
         """Slots with more than 26 labels are read with dg_slot_read_wide (one table of
         stride L = the largest label count)."""
         self.shape = shape
@@ -216,8 +220,13 @@ class ReadStep:
         self.label_ids = _dev(lab, i32, device)
         self.n_labels = _dev(n, i32, device)
         self.out = slot_outputs(self.S, shape.R, device, self.L)
-        self.ws_attn = torch.empty(max(dg.dg_workspace_bytes(self.dims, dg.DG_WS_ATTN, 0), 256),
-                                   dtype=u8, device=device)
+        self.concurrent = concurrent
+        n_sm = dg.dg_num_sms()
+        self.dims_side = dg.dims_of(shape, sm_share=max(1, n_sm - n_sm * 7 // 8))
+        self._side = None
+        self.ws_attn = torch.empty(max(dg.dg_workspace_bytes(self.dims, dg.DG_WS_ATTN, 0),
+                                       dg.dg_workspace_bytes(self.dims_side, dg.DG_WS_ATTN, 0),
+                                       256), dtype=u8, device=device)
         self.ws_read = torch.empty(dg.dg_workspace_bytes(self.dims, dg.DG_WS_SLOT_READ,
                                                          self.S * shape.R), dtype=u8,
                                    device=device)
@@ -225,9 +234,17 @@ class ReadStep:
     def run(self, step_idx=0, stream=None):
         """Enqueue attention + the slot read; returns the number of library kernels."""
         s, d, o = self.shape, self.dims, self.out
-        dg._check(dg.dg_attn_decode(d, self.q, self.kc, self.vc, self.kenc, self.venc, None, 0,
-                                    0, 0, self.prompt_len, self.attn_out, self.attn_lse,
-                                    self.ws_attn, stream), "dg_attn_decode")
+        main = _as_stream(stream)
+        attn_stream, attn_dims = main, d
+        if self.concurrent:
+            if self._side is None:
+                self._side = torch.cuda.Stream(device=self.h.device)
+            attn_stream, attn_dims = self._side, self.dims_side
+            attn_stream.wait_stream(main)
+        dg._check(dg.dg_attn_decode(attn_dims, self.q, self.kc, self.vc, self.kenc, self.venc,
+                                    None, 0, 0, 0, self.prompt_len, self.attn_out,
+                                    self.attn_lse, self.ws_attn, attn_stream), "dg_attn_decode")
+        stream = main
         if self.L == dg.MAX_LABELS:
             dg._check(dg.dg_slot_read(d, self.h, self.M, self.w, self.e, self.inv_t,
                                       self.slot_row, self.slot_req, self.label_ids,
@@ -242,7 +259,9 @@ class ReadStep:
                                            s.R, s.gate, o["q_avg"], o["h_slot"], o["chosen"],
                                            o["lp"], o["resampled"], o["n_reads"], o["tokens"],
                                            self.ws_read, stream), "dg_slot_read_wide")
-        attn_kernels = 1 if dg.dg_workspace_bytes(d, dg.DG_WS_ATTN, 0) <= 256 else 2
+        if self.concurrent:
+            main.wait_stream(attn_stream)
+        attn_kernels = 1 if dg.dg_workspace_bytes(attn_dims, dg.DG_WS_ATTN, 0) <= 256 else 2
         return attn_kernels + 5
 
 
