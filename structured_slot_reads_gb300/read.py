@@ -27,7 +27,7 @@ import numpy as np
 import torch
 
 from . import dg, inputs
-from .step import _as_stream
+from .step import as_stream
 
 
 def _dev(a, dtype, device):
@@ -234,7 +234,7 @@ class ReadStep:
     def run(self, step_idx=0, stream=None):
         """Enqueue attention + the slot read; returns the number of library kernels."""
         s, d, o = self.shape, self.dims, self.out
-        main = _as_stream(stream)
+        main = as_stream(stream)
         attn_stream, attn_dims = main, d
         if self.concurrent:
             if self._side is None:

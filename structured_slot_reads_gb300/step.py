@@ -35,7 +35,7 @@ import torch
 from . import dg
 
 
-def _as_stream(stream):
+def as_stream(stream):
     """The torch stream of a call: the current one, a raw handle wrapped, or as given."""
     if stream is None:
         return torch.cuda.current_stream()
@@ -240,7 +240,7 @@ class DenoiseStep:
     def _run_fused(self, step_idx, stream):
         s, d = self.shape, self.dims
         ck = dg._check
-        main = _as_stream(stream)
+        main = as_stream(stream)
         if not self.concurrent:
             self._attention(main)
         if self.with_slots and not self.n_draw:
