@@ -8,8 +8,11 @@ same step.  One step = attention, lm-head log-softmax/entropy over all 256
 rows, the slot read (noise + one W pass + gate), the entropy commit,
 self-conditioning and the next-step canvas update.  W and E (1.48 GB each)
 are streamed every step, so every timed step reads inputs far larger than L2.
+The step's slot finish, commit and attention run on a side stream beside the
+self-conditioning GEMM (``--schedule serial``: every call on one stream).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                  [--workload NAME] [--schedule concurrent|serial]
 """
 import argparse
 import hashlib
