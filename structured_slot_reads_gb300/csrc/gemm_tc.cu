@@ -604,10 +604,30 @@ void accum_split(int M, int V, int D, int* k_split, int* kb_per_split, int kb = 
   const int groups = (M + mt * BM - 1) / (mt * BM);
   const int n_tiles = (D + ACC_BN - 1) / ACC_BN;
   const int total_kb = (V + kb - 1) / kb;
-  // The GEMM is bound by the stream of E, which 7/8 of the SMs keep saturated
-  // (256 x 262144 x 2816: 132 CTAs take 280 us against 279 for 143), so the
-  // split leaves the other eighth to work running beside it on another stream.
-  int ks = std::max(1, (dgi::num_sms() * 7 / 8) / (groups * n_tiles));
+  const int tiles = groups * n_tiles, sms = dgi::num_sms();
+  int ks;
+  if (tiles <= sms * 7 / 16) {
+    // Few output tiles: the GEMM is bound by the stream of E, which 7/8 of the
+    // SMs keep saturated (256 x 262144 x 2816: 132 CTAs take 280 us against 279
+    // for 143), so the split leaves the other eighth to work running beside it
+    // on another stream.
+    ks = std::max(1, (sms * 7 / 8) / tiles);
+  } else {
+    // Many output tiles: the CTAs are tensor-bound and come in waves; take the
+    // split with the fewest rounds of whole-tile work, ceil(tiles ks / SMs) / ks
+    // (2048 rows: 88 tiles on 88 SMs, or in 5 splits 440 CTAs in 3 waves of a
+    // fifth of the work each), the smallest split on a tie.
+    ks = 1;
+    long long best_num = (tiles + sms - 1) / sms, best_den = 1;
+    for (int c = 2; c <= 8; ++c) {
+      const long long rounds = ((long long)tiles * c + sms - 1) / sms;
+      if (rounds * best_den < best_num * c) {
+        best_num = rounds;
+        best_den = c;
+        ks = c;
+      }
+    }
+  }
   ks = std::min(ks, total_kb);
   const int kbps = (total_kb + ks - 1) / ks;
   *kb_per_split = kbps;
