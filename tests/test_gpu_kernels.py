@@ -386,6 +386,29 @@ def test_denoise_heads_fused_pass(M, nd, V, D):
     assert_rel(host(out), oracle.selfcond_embed(h, w, e, inv_t), what="expected embedding")
 
 
+@pytest.mark.parametrize("M,V,D", [(2048, 2048, 2816), (4096, 1024, 2816), (256, 4096, 2816)])
+def test_selfcond_from_probs_split_k(M, V, D):
+    """out = prob_scale * (P~ E) against the float64 definition, in the split-K
+    configurations the GEMM picks: 2048 and 4096 rows make 88 and 176 output tiles,
+    split by whole-tile rounds into waves; 256 rows make 11 tiles on 7/8 of the SMs."""
+    rng = np.random.default_rng(M + V)
+    ld = dg.dg_probs_ld(V)
+    p = np.zeros((M, ld), np.float32)
+    p[:, :V] = np.exp(rng.normal(0.0, 2.0, (M, V))).astype(np.float32)
+    p = inputs.to_bf16(p)
+    scale = (1.0 / p[:, :V].astype(np.float64).sum(axis=1)).astype(np.float32)
+    _, e = inputs.weights(V, D, 17)
+    d = dg.make_dims(d_model=D, V=V)
+    out = torch.empty((M, D), dtype=torch.float32, device="cuda")
+    ws = torch.empty(dg.dg_workspace_bytes(d, dg.DG_WS_PROBS_EMBED, M), dtype=torch.uint8,
+                     device="cuda")
+    rc = dg.dg_selfcond_from_probs(d, dev_bf16(p), ld, dev(scale), M, dev_bf16(e), out, ws)
+    assert rc == dg.DG_OK, dg.strerror(rc)
+    torch.cuda.synchronize()
+    want = (p[:, :V].astype(np.float64) @ e.astype(np.float64)) * scale[:, None].astype(np.float64)
+    assert_rel(host(out), want, what="expected embedding")
+
+
 def test_denoise_heads_flags_out_of_range_logits():
     M, V, D = 8, 2048, 128
     h, w, _, inv_t = _lm_inputs(M, V, D, seed=5)
