@@ -10,7 +10,7 @@ import pytest
 
 import oracle
 from structured_slot_reads_gb300 import dg, inputs
-from tests.gpu_util import TOL_LOGPROB, assert_abs, assert_rel, dev, dev_bf16, host, top2_gap
+from tests.gpu_util import assert_abs, assert_rel, dev, dev_bf16, host, top2_gap
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
