@@ -64,6 +64,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-workloads", action="store_true",
+                    help="headline line only (skip the single read, the mixed batch and the "
+                         "long-context read that the default line also reports)")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--schedule", default="concurrent", choices=["concurrent", "serial"],
                     help="step schedule: side stream beside the self-conditioning GEMM, "
@@ -198,11 +201,7 @@ def build_step(shape, device, concurrent=True):
     for i, k in enumerate(("q", "kc", "vc", "kenc", "venc")):
         getattr(st, k).copy_(inputs.device_normal_bf16(getattr(st, k).shape, 1.0, 10 + i, device))
     st.cand.fill_(1)
-    row, req, lab, n = inputs.slot_table(shape, 0)
-    st.slot_row.copy_(torch.from_numpy(row))
-    st.slot_req.copy_(torch.from_numpy(req))
-    st.label_ids.copy_(torch.from_numpy(lab))
-    st.n_labels.copy_(torch.from_numpy(n))
+    st.set_slots(*inputs.slot_table(shape, 0))
     st.reset_state()
     torch.cuda.synchronize()
     return st
@@ -356,12 +355,17 @@ def gpu_arm(args, rank, world, local):
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     src = ("structured_slot_reads_gb300/csrc/heads_tc.cu" if dom == "dg_denoise_heads"
            else "structured_slot_reads_gb300/csrc/gemm_tc.cu")
+    spill = spill_bytes(shape) if dom == "dg_denoise_heads" else 0
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm"], "unit": "GB/s",
             "frac": round(achieved / pk["hbm"], 4),
             "traffic": traffic_from_profile(src, "denoise_heads_full_canvas"
                                             if dom == "dg_denoise_heads"
                                             else "lmhead_stats_full_canvas"),
-            "kernel": dom, "peak_source": pk["source"],
+            "kernel": dom, "peak_source": pk["source"] + " (burst copy)",
+            "algorithmic_bytes": dom_bytes,
+            "bytes_with_probability_spill": dom_bytes + spill,
+            "frac_with_probability_spill": round((dom_bytes + spill) / (dom_ms / 1e3) / 1e9
+                                                 / pk["hbm"], 4),
             "tensor_tflops": round(dom_flops / (dom_ms / 1e3) / 1e12, 1),
             "tensor_frac_sustained": round(dom_flops / (dom_ms / 1e3) / 1e12 / pk["bf16_sus"], 4)}
 
@@ -399,23 +403,51 @@ def gpu_arm(args, rank, world, local):
     return line, st
 
 
+def slot_finish_bytes(shape, n_slots):
+    """Algorithmic bytes of the slot finish: each draw row read once, the W rows of
+    its slot's labels, the draw rows' lse, and the per-slot outputs written."""
+    D, R = shape.D, shape.R
+    labels = sum(k for _, k in shape.slots) * shape.B if n_slots else 0
+    rows = n_slots * R
+    return (rows * D * 2 + R * labels * D * 2 + rows * 4
+            + n_slots * (26 * 4 + 4 + 4 + 1 + 4) + rows * 26 * 4)
+
+
+def commit_bytes(shape):
+    """Algorithmic bytes of the commit: per position entropy, argmax, candidate
+    flag and carried state read; accept flag, token and carried state written."""
+    return shape.B * shape.C * (4 + 4 + 1 + 1 + 4 + 1 + 4 + 1 + 4) + shape.B * 8
+
+
 def call_work(shape, st):
-    """Algorithmic HBM bytes and FLOPs of each library call of one step."""
+    """Algorithmic HBM bytes and FLOPs of each library call of one step.
+
+    The fused heads pass counts what the method must move: W once, the canvas and
+    draw rows, the row statistics.  The bf16 probabilities it also writes for the
+    self-conditioning GEMM (and that GEMM reads back) are this design's hand-off
+    between the two passes, not the method's work; ``spill`` gives them apart."""
     M, V, D = shape.B * shape.C, shape.V, shape.D
     W = V * D * 2
     nd = getattr(st, "n_draw", 0)
-    sr = getattr(st, "S", 0) * shape.R        # draw rows of a dg_slot_read pass
+    S = getattr(st, "S", 0)
+    sr = S * shape.R                          # draw rows of a dg_slot_read pass
     return {
         "dg_attn_decode": (attn_bytes(shape), attn_flops(shape)),
         "dg_lmhead_logsoftmax_entropy": (W + M * D * 2 + M * 16, 2.0 * M * V * D),
         "dg_slot_read": (W + sr * D * 4, 2.0 * sr * V * D),
-        "dg_denoise_heads": (W + (M + nd) * D * 2 + M * V * 2 + M * 20,
-                             2.0 * (M + nd) * V * D),
-        "dg_selfcond_embed": (2 * W + 2 * M * V * 2 + M * D * 4, 4.0 * M * V * D),
-        "dg_selfcond_from_probs": (W + M * V * 2 + M * D * 4, 2.0 * M * V * D),
+        "dg_denoise_heads": (W + (M + nd) * D * 2 + M * 20 + nd * 4, 2.0 * (M + nd) * V * D),
+        "dg_selfcond_embed": (2 * W + M * D * 2 + M * 8 + M * D * 4, 4.0 * M * V * D),
+        "dg_selfcond_from_probs": (W + M * D * 4, 2.0 * M * V * D),
         "dg_slot_noise": (3 * nd * D * 2, 0.0),
+        "dg_slot_finish": (slot_finish_bytes(shape, S) if nd else 0.0, 0.0),
+        "dg_commit": (commit_bytes(shape), 0.0),
         "dg_canvas_update": (M * D * (2 + 4 + 2), 0.0),
     }
+
+
+def spill_bytes(shape):
+    """The heads pass's bf16 probabilities: written once, read once by P.E."""
+    return shape.B * shape.C * shape.V * 2
 
 
 def attn_flops(shape, prompt_len=None):
@@ -750,80 +782,110 @@ def oracle_inputs(shape, st=None):
     return dict(w=w, e=e, h=h, inv_t=inv_t, att=x, slots=slots)
 
 
-def oracle_sample(shape, data, target_rows=16, heads=1, seed=0):
-    """Time the float64 oracle on a bounded sample of one step and scale to a full step.
-
-    Sample: lm-head statistics and self-conditioning for ``target_rows`` canvas
-    rows, attention for ``heads`` query head(s) over the whole canvas, the slot
-    read (three slots x four draws) and the commit in full.  Each part's time
-    is scaled by its share of the full step and the parts are summed.
-    """
+def oracle_step(shape, data, step_idx=0):
+    """One whole denoise step of the workload in the float64 oracle, as it stands:
+    attention of every row and head over the whole prompt, the lm-head statistics
+    of every canvas row, the slot read (noise draws, their full-vocabulary
+    log-normalisers, label logits, gate and average), the commit, the expected
+    embedding of every row and the next canvas input.  Returns (seconds, parts)."""
     import numpy as np
 
     import oracle
-    rng = np.random.default_rng(seed)
     w, e, h, inv_t, x = data["w"], data["e"], data["h"], data["inv_t"], data["att"]
-    M = shape.B * shape.C
-    rows = rng.choice(M, size=target_rows, replace=False)
-    parts = {}
-    t0 = time.perf_counter()
-    lse, ent, maxz, arg = oracle.lmhead_stats(h[rows], w, inv_t[rows])
-    parts["lmhead"] = (time.perf_counter() - t0) * M / target_rows
-    t0 = time.perf_counter()
-    oracle.selfcond_embed(h[rows], w, e, inv_t[rows])
-    parts["selfcond"] = (time.perf_counter() - t0) * M / target_rows
-    t0 = time.perf_counter()
-    oracle.attn_decode(x["q"][:, :, :heads], x["kc"][:, :, :1], x["vc"][:, :, :1],
-                       x["kenc"][:, :, :1], x["venc"][:, :, :1], x["prompt_len"], shape.W)
-    parts["attention"] = (time.perf_counter() - t0) * shape.Hq / heads
     row, req, lab, n = data["slots"]
+    B, C, R = shape.B, shape.C, shape.R
+    parts = {}
+    t_all = time.perf_counter()
     t0 = time.perf_counter()
-    rows_d, _ = oracle.slot_noise_rows(h, e, row, req, 7, 0, shape.R, shape.V)
-    inv_d = np.repeat(inv_t[row], shape.R)
+    oracle.attn_decode(x["q"], x["kc"], x["vc"], x["kenc"], x["venc"], x["prompt_len"], shape.W)
+    parts["attention"] = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    _, ent, _, arg = oracle.lmhead_stats(h, w, inv_t)
+    parts["lmhead"] = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    rows_d, _ = oracle.slot_noise_rows(h, e, row, req, 7, step_idx, R, shape.V)
+    inv_d = np.repeat(inv_t[row], R)
     lse_d, _, _, _ = oracle.lmhead_stats(rows_d, w, inv_d)
-    zl = oracle.label_logits(rows_d, w, inv_d, np.repeat(lab, shape.R, axis=0),
-                             np.repeat(n, shape.R))
-    oracle.slot_read(zl.reshape(len(row), shape.R, -1), lse_d.reshape(len(row), shape.R), n,
-                     shape.R, shape.gate)
+    zl = oracle.label_logits(rows_d, w, inv_d, np.repeat(lab, R, axis=0), np.repeat(n, R))
+    oracle.slot_read(zl.reshape(len(row), R, -1), lse_d.reshape(len(row), R), n, R, shape.gate)
     parts["slot_read"] = time.perf_counter() - t0
     t0 = time.perf_counter()
-    ent_full = np.concatenate([ent, rng.uniform(10, 12, M - target_rows)])
-    oracle.commit(ent_full[None], np.zeros((1, M), int), np.ones((1, M), np.uint8),
-                  np.array([shape.gamma]))
+    cm, tk, _ = oracle.commit(ent.reshape(B, C), arg.reshape(B, C), np.ones((B, C), np.uint8),
+                              np.full(B, shape.gamma))
     parts["commit"] = time.perf_counter() - t0
-    total = sum(parts.values())
-    sample = (f"lm-head + self-conditioning on {target_rows} of {M} canvas rows "
-              f"(x{M // target_rows}), attention for {heads} of {shape.Hq} query heads "
-              f"(x{shape.Hq // heads}), slot read and commit in full; parts summed into one "
-              f"full-step time")
-    return 1.0 / total, sample, {k: round(v, 3) for k, v in parts.items()}
+    t0 = time.perf_counter()
+    e_sc = oracle.selfcond_embed(h, w, e, inv_t)
+    parts["selfcond"] = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.canvas_update(h, e_sc, e, tk.reshape(-1), cm.reshape(-1))
+    parts["canvas_update"] = time.perf_counter() - t0
+    return time.perf_counter() - t_all, parts
 
 
-def reference_arm(args, rank):
-    """The oracle as the reference implementation, timed on the host cores (rank 0 only)."""
+ORACLE_SAMPLE = ("one whole full-canvas step: attention of all 8 heads over the 4096-token "
+                 "prompt and the window, lm-head statistics and self-conditioning of all 256 "
+                 "rows over the 262144-entry vocabulary, the three slot reads (4 draws each), "
+                 "the commit and the canvas update; no part sampled or scaled")
+
+
+def reference_arm(args, rank, budget_s=150.0, shape=None):
+    """The oracle as the reference implementation, timed on the host cores (rank 0 only).
+
+    Each step is one whole float64 step (oracle_step).  Warm-up is at most two
+    steps and the timed steps stop once ``budget_s`` of them have run, so the
+    run ends in a few minutes; the line reports the steps actually timed."""
     from structured_slot_reads_gb300 import configs
     if rank != 0:
         return None
-    shape = configs.FULL_CANVAS
+    shape = shape or configs.FULL_CANVAS
     data = oracle_inputs(shape)
-    times = []
-    sample = ""
-    for i in range(args.warmup + args.steps):
-        v, sample, _ = oracle_sample(shape, data, target_rows=16, heads=1, seed=i)
-        if i >= args.warmup:
-            times.append(1.0 / v)
+    warm = min(args.warmup, 2)
+    for i in range(warm):
+        oracle_step(shape, data, i)
+    times, parts = [], None
+    for i in range(args.steps):
+        dt, parts = oracle_step(shape, data, warm + i)
+        times.append(dt)
+        if sum(times) >= budget_s:
+            break
     t = sum(times)
-    value = args.steps / t
+    value = len(times) / t
     return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
-            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(1e3 * t / args.steps, 3), "higher_is_better": True,
+            "n_gpus": 1, "steps": len(times), "warmup": warm, "steps_requested": args.steps,
+            "warmup_requested": args.warmup,
+            "ms_per_step": round(1e3 * t / len(times), 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "full_canvas_step (float64 CPU oracle, sampled)",
+            "config": {"workload": "full_canvas_step (float64 CPU oracle, whole steps)",
                        "global_batch": 1, "seq_len": shape.C, "parallelism": "host cores"},
-            "cpu_baseline": {"kind": "oracle", "cores": os.cpu_count(), "sample": sample,
-                             "value": round(value, 6), "unit": UNIT},
+            "cpu_baseline": {"kind": "oracle", "cores": os.cpu_count(), "sample": ORACLE_SAMPLE,
+                             "value": round(value, 6), "unit": UNIT,
+                             "parts_s": {k: round(v, 3) for k, v in parts.items()}},
             "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
+
+
+EXTRA_WORKLOADS = ("single_structured_read", "mixed_batched_reads", "long_context_read")
+
+
+def extra_workloads(args, rank, world, local):
+    """The single structured read, the mixed batch of two-stage reads and the
+    long-context read, each timed as ``--workload`` times it (eager, 3 warm-up
+    steps, at most 10 timed steps), summarised into the default line."""
+    import torch
+    out = {}
+    for name in EXTRA_WORKLOADS:
+        wargs = argparse.Namespace(**vars(args))
+        wargs.workload = name
+        wargs.warmup = max(3, min(args.warmup, 5))
+        wargs.steps = min(args.steps, 10)
+        ln = workload_arm(wargs, rank, world, local)
+        out[name] = {k: ln[k] for k in ("value", "unit", "ms_per_step", "steps", "warmup",
+                                        "slot_decisions_per_s", "slot_decisions_per_step",
+                                        "roofline", "kernels", "clocks", "device_status",
+                                        "gpu_launches")}
+        out[name]["workload"] = ln["config"]["workload"]
+        torch.cuda.empty_cache()
+    return out
 
 
 def main():
@@ -850,10 +912,18 @@ def main():
         return 0
     line, st = gpu_arm(args, rank, world, local)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, sample, parts = oracle_sample(st.shape, oracle_inputs(st.shape, st), target_rows=16,
-                                         heads=1)
-        line["cpu_baseline"] = {"value": round(v, 6), "unit": UNIT, "cores": os.cpu_count(),
-                                "kind": "oracle", "sample": sample, "parts_s": parts}
+        data = oracle_inputs(st.shape, st)
+        dt, parts = oracle_step(st.shape, data)
+        line["cpu_baseline"] = {"value": round(1.0 / dt, 6), "unit": UNIT,
+                                "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": ORACLE_SAMPLE, "steps_timed": 1,
+                                "parts_s": {k: round(v, 3) for k, v in parts.items()}}
+    if not args.no_extra_workloads:
+        # the other headline workloads, each timed on its own (the step's buffers freed first)
+        import torch
+        del st
+        torch.cuda.empty_cache()
+        line["workloads"] = extra_workloads(args, rank, world, local)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

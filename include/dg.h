@@ -50,7 +50,7 @@ extern "C" {
 #define DG_DEV_BAD_PAGE 2   /* a page-table entry outside the page pool      */
 #define DG_DEV_BAD_LABEL 4  /* a label id or label count out of range        */
 #define DG_DEV_BAD_INDEX 8  /* a slot row / token id outside its tensor      */
-#define DG_DEV_RANGE 16     /* a logit beyond the fused pass's exponent range */
+#define DG_DEV_RANGE 16     /* reserved: no call of this version raises it    */
 
 #define DG_MAX_LABELS 26 /* sotaaz.com, "The server accepts at most 26 alternatives per question" */
 #define DG_MAX_WIDE_LABELS 256 /* label table stride limit of dg_slot_read_wide */
@@ -95,7 +95,9 @@ typedef struct {
  *     [0, n_pages) set DG_DEV_BAD_PAGE and are read as masked keys.
  *   prompt_len [B] int32, each in [0, P_max]
  *   out [B, C, Hq, d] bf16;  lse [B, Hq, C] fp32 (natural log)
- *   workspace: dg_workspace_bytes(dims, DG_WS_ATTN, 0) bytes. */
+ *   workspace: dg_workspace_bytes(dims, DG_WS_ATTN, 0) bytes.
+ * d_head = 512 runs on the tensor-core kernel, which takes pages of 8, 16, 32,
+ * 64 or 128 keys; another page size returns DG_ERR_SHAPE (nothing launched). */
 int dg_attn_decode(const dg_dims* dims, const uint16_t* q, const uint16_t* kc,
                    const uint16_t* vc, const uint16_t* kenc, const uint16_t* venc,
                    const int32_t* page_table, int pages_per_req, int n_pages,
@@ -355,12 +357,12 @@ int dg_selfcond_embed(const dg_dims* dims, const uint16_t* h, int M,
  *    accepts at most 26 alternatives per question");
  *  - the self-conditioning probabilities of the canvas rows (24-ai.news,
  *    "Token commit mechanism") as unnormalised bf16 values
- *    probs[i][v] = 2^(z_iv log2(e) - r_i), r_i a per-row reference computed from
- *    the first 8 vocabulary entries, and prob_scale[i] = 1 / sum_v probs[i][v],
- *    so p_iv = probs[i][v] * prob_scale[i].
- * If some z_iv lies more than 100 / log2(e) nats above r_i the exponent is
- * clamped and DG_DEV_RANGE is set in the status word; dg_selfcond_embed (which
- * recomputes the logits) is exact for any input.
+ *    probs[i][v] = 2^(z_iv log2(e) - r_i), r_i a per-row reference (from the
+ *    first 8 vocabulary entries, raised by whole powers of two wherever a logit
+ *    lies far above it), and prob_scale[i] = 1 / sum_v probs[i][v], so
+ *    p_iv = probs[i][v] * prob_scale[i].
+ * The statistics and the probabilities are exact for any input whose scaled
+ * logits stay below 2^24 log2 units.
  *   h [M, d_model] bf16;  draw_rows [n_draw, d_model] bf16 (NULL if n_draw = 0)
  *   w [V, d_model] bf16;  inv_t [M], inv_t_draw [n_draw] fp32
  *   lse, entropy, maxz [M] fp32;  argmax [M] int32;  lse_draw [n_draw] fp32
@@ -406,6 +408,13 @@ int dg_philox_fill(uint64_t seed, const uint32_t* ctr4, int n, uint32_t* out4,
 int dg_validate_slots(const dg_dims* dims, const int32_t* slot_row_host,
                       const int32_t* label_ids_host, const int32_t* n_labels_host,
                       int S, int M);
+/* The same check for the label tables of dg_slot_read_wide (row stride L,
+ * 1 <= L <= 256): n_labels in [1, L] (DG_ERR_TOO_MANY_LABELS above L or for
+ * L outside [1, 256]), label ids distinct and in [0, V), slot_row in [0, M).
+ * No GPU work.  dg_validate_slots is this check with L = 26. */
+int dg_validate_slots_wide(const dg_dims* dims, const int32_t* slot_row_host,
+                           const int32_t* label_ids_host, const int32_t* n_labels_host,
+                           int S, int L, int M);
 /* Bytes of device workspace a call needs (rows = M for DG_WS_LMHEAD,
  * DG_WS_SELFCOND, DG_WS_HEADS and DG_WS_PROBS_EMBED, S*samples for
  * DG_WS_SLOT_READ, ignored for DG_WS_ATTN); 0 for an invalid request. */
@@ -445,7 +454,9 @@ int dg_num_sms(void);
  *  - M may be at most DG_NOALLOC_MAX_ROWS; larger M returns DG_ERR_SHAPE.
  *  - The first call on a device looks up the array's device address (a
  *    runtime query, no allocation); make that first call before any stream
- *    capture.  Later calls on that device reuse the address.
+ *    capture.  Later calls on that device reuse the address, unless the
+ *    device's context has been created anew since (after cudaDeviceReset),
+ *    in which case the call looks it up again.
  *  - The array is shared by every call on a device and keeps the last call's
  *    contents (each launch overwrites all of it that it reads, so nothing needs
  *    clearing).  Calls whose work overlaps on the GPU, e.g. on two streams

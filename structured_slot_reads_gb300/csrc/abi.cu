@@ -17,9 +17,12 @@ namespace {
 __device__ int g_status;  // bits DG_DEV_*, sticky until dg_clear_status
 
 constexpr int kMaxDevices = 64;
-int* g_status_addr[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
 std::mutex g_mu;
+// device addresses of this library's __device__ variables, per device, with the
+// context they were looked up in
+void* g_sym_addr[dgi::SYM_COUNT][kMaxDevices] = {};
+uint64_t g_sym_ctx[dgi::SYM_COUNT][kMaxDevices] = {};
 
 int current_device() {
   int dev = 0;
@@ -50,9 +53,10 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-bool dims_lm(const dg_dims* d) {
-  return d && d->d_model >= 8 && d->d_model % 8 == 0 && d->V >= 1;
-}
+bool dims_lm(const dg_dims* d) { return d && dgi::lm_dims_ok(d->d_model, d->V); }
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
 
 int launch_result(cudaError_t e) { return e == cudaSuccess ? DG_OK : DG_ERR_CUDA; }
 
@@ -60,17 +64,47 @@ int launch_result(cudaError_t e) { return e == cudaSuccess ? DG_OK : DG_ERR_CUDA
 
 namespace dgi {
 
-int* status_ptr() {
-  const int dev = current_device();
-  if (dev < 0) return nullptr;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_status_addr[dev]) {
+uint64_t context_id() {
+  static CtxGetCurrentFn get_cur = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
-    g_status_addr[dev] = static_cast<int*>(p);
-  }
-  return g_status_addr[dev];
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (!get_cur || !get_id) return 0;
+  CUcontext c = nullptr;
+  if (get_cur(&c) != CUDA_SUCCESS || !c) return 0;
+  unsigned long long id = 0;
+  if (get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return (uint64_t)id + 1;  // 0 stands for "no context"
 }
+
+void* device_symbol(const void* symbol, int slot) {
+  const int dev = current_device();
+  if (dev < 0 || slot < 0 || slot >= SYM_COUNT) return nullptr;
+  uint64_t ctx = context_id();
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_sym_addr[slot][dev] && ctx != 0 && g_sym_ctx[slot][dev] == ctx)
+    return g_sym_addr[slot][dev];
+  // first use on this device, or a new context (after cudaDeviceReset the old
+  // address belongs to a module that no longer exists): look it up again
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess || !p) return nullptr;
+  if (ctx == 0) ctx = context_id();  // the lookup made the primary context current
+  g_sym_addr[slot][dev] = p;
+  g_sym_ctx[slot][dev] = ctx;
+  return p;
+}
+
+int* status_ptr() { return static_cast<int*>(device_symbol(&g_status, SYM_STATUS)); }
 
 int num_sms() {
   const int dev = current_device();
@@ -303,23 +337,29 @@ int dg_selfcond_from_probs(const dg_dims* d, const uint16_t* probs, size_t probs
                                         out, workspace, static_cast<cudaStream_t>(stream)));
 }
 
-int dg_validate_slots(const dg_dims* d, const int32_t* slot_row, const int32_t* label_ids,
-                      const int32_t* n_labels, int S, int M) {
+int dg_validate_slots_wide(const dg_dims* d, const int32_t* slot_row, const int32_t* label_ids,
+                           const int32_t* n_labels, int S, int L, int M) {
   if (!d || S < 0 || M < 0) return DG_ERR_ARG;
+  if (L < 1 || L > DG_MAX_WIDE_LABELS) return DG_ERR_TOO_MANY_LABELS;
   if (S > 0 && (!slot_row || !label_ids || !n_labels)) return DG_ERR_ARG;
   for (int s = 0; s < S; ++s) {
     const int n = n_labels[s];
-    if (n > DG_MAX_LABELS) return DG_ERR_TOO_MANY_LABELS;
+    if (n > L) return DG_ERR_TOO_MANY_LABELS;
     if (n < 1) return DG_ERR_LABEL;
     if (slot_row[s] < 0 || slot_row[s] >= M) return DG_ERR_SHAPE;
     std::set<int32_t> seen;
     for (int k = 0; k < n; ++k) {
-      const int32_t id = label_ids[s * DG_MAX_LABELS + k];
+      const int32_t id = label_ids[(long long)s * L + k];
       if (id < 0 || id >= d->V) return DG_ERR_LABEL;
       if (!seen.insert(id).second) return DG_ERR_LABEL;
     }
   }
   return DG_OK;
+}
+
+int dg_validate_slots(const dg_dims* d, const int32_t* slot_row, const int32_t* label_ids,
+                      const int32_t* n_labels, int S, int M) {
+  return dg_validate_slots_wide(d, slot_row, label_ids, n_labels, S, DG_MAX_LABELS, M);
 }
 
 int dg_get_status(void* stream, int32_t* status_out) {
@@ -387,6 +427,9 @@ int dg_attn_decode(const dg_dims* d, const uint16_t* q, const uint16_t* kc, cons
   a.prompt_len = prompt_len;
   a.out = out;
   a.lse = lse;
+  // 512-wide heads run only on the tensor-core kernel: page sizes it cannot
+  // take are rejected here rather than run on another kernel
+  if (a.d == 512 && !dgi::attn_tc_supported(a)) return DG_ERR_SHAPE;
   return launch_result(dgi::attn_decode(a, workspace, static_cast<cudaStream_t>(stream)));
 }
 

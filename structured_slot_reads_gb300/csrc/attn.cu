@@ -8,10 +8,12 @@
 // and streams the union of their keys once.  The key range is split across
 // CTAs (split-KV) and the partial (max, sum, O) are merged by a combine kernel.
 //
-// Tensor-core path: warp-level bf16 mma.sync m16n8k16 with fp32 accumulators,
-// operands staged in XOR-swizzled shared memory by cp.async.  For d = 512 the
-// output accumulator is split over two warps per 16-row group (256 columns
-// each) and the score tile over the same two warps (32 keys each).
+// This file serves the 64-wide heads of the tiny correctness shape: warp-level
+// bf16 mma.sync m16n8k16 with fp32 accumulators, operands staged in
+// XOR-swizzled shared memory by cp.async.  A 64 x 64 score tile and the whole
+// 64 x 64 output fit one CTA's registers here, so this small case has none of
+// the tensor-memory pressure that shapes the 512-wide kernel (attn_tc.cu),
+// which every 512-wide call runs on.  The split-KV combine below serves both.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -506,17 +508,16 @@ cudaError_t run(const dgi::AttnArgs& x, void* ws, cudaStream_t st) {
 namespace dgi {
 
 size_t attn_ws_bytes(int B, int C, int Pmax, int Hq, int Hkv, int d, int W, int sms) {
+  // d = 512 runs on the tensor-core kernel (attn_tc.cu)
+  if (d == 512) return attn_tc_ws_bytes(B, C, Pmax, Hq, Hkv, W, sms);
   const int s = pick_splits(B, C, Hq, Hkv, Pmax, std::min(W, C), plan_sms(sms));
-  size_t bytes = 256;
-  if (s > 1) bytes = align_up((size_t)s * B * C * Hq * d * 4 + (size_t)s * B * Hq * C * 8, 256);
-  // d = 512 runs on the tensor-core kernel unless its page size is unsupported
-  if (d == 512) bytes = std::max(bytes, attn_tc_ws_bytes(B, C, Pmax, Hq, Hkv, W, sms));
-  return bytes;
+  if (s == 1) return 256;
+  return align_up((size_t)s * B * C * Hq * d * 4 + (size_t)s * B * Hq * C * 8, 256);
 }
 
 cudaError_t attn_decode(const AttnArgs& a, void* ws, cudaStream_t st) {
   if (a.d == 64) return run<64>(a, ws, st);
-  if (a.d == 512) return attn_tc_supported(a) ? attn_decode_tc(a, ws, st) : run<512>(a, ws, st);
+  if (a.d == 512 && attn_tc_supported(a)) return attn_decode_tc(a, ws, st);
   return cudaErrorInvalidValue;
 }
 

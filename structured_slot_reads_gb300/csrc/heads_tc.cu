@@ -10,6 +10,18 @@
 // rescaling and p_iv = P~_iv / S_i exactly; the P.E GEMM applies 1/S_i in its
 // reduction.
 //
+// The pass is exact for any input whose scaled logits stay below 2^24 log2
+// units (past that a raise no longer counts whole units in a float).  An
+// epilogue thread owns one row of
+// its CTA's vocabulary range; when a chunk's largest exponent passes r + RAISE
+// it raises its own reference by a whole number k of log2 units (so 2^-k is
+// exact), scales its running sums and the probabilities it already wrote by
+// 2^-k, and goes on.  Each CTA reports the reference of its sums and of its
+// probabilities; the finalize takes the largest, merges the sums against it and
+// brings the probabilities of any CTA range with a lower reference to it (again
+// by a power of two).  Without a raise (the usual case) every factor is 1 and
+// nothing is rewritten.
+//
 // For the slot-read draw rows (sotaaz.com "The server accepts at most 26
 // alternatives per question": noise reads of an answer slot) the same W tiles
 // feed a "swapped" MMA: A = the W tile (vocabulary on TMEM lanes), B = the
@@ -39,7 +51,7 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int REF_N = 8;              // vocabulary entries behind the reference
 constexpr float REF_HEADROOM = 24.f;  // log2 units added to the reference maximum
-constexpr float V_CLAMP = 100.f;      // exponent guard (log2 units above the reference)
+constexpr float RAISE = 64.f;         // exponent (log2 units) past which a reference is raised
 constexpr int DRAW_N = 16;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
@@ -73,7 +85,7 @@ struct HeadsParams {
   const float* inv_t;       // [M]
   const float* inv_t_draw;  // [n_draw]
   const float* ref;         // [M] reference r (log2 units)
-  float* part;              // canvas: 4 planes of [M][cpg]: s, t, best, idx
+  float* part;              // canvas: 5 planes of [M][cpg]: s, t, best, idx, reference
   float* part_draw;         // draws: 2 planes of [n_draw][cpg]: m, s
   __nv_bfloat16* probs;     // [M][ldp] or null
   long long ldp;
@@ -156,6 +168,27 @@ struct HCfg {
   static_assert(STAGE_BYTES % 1024 == 0 && W_SLOT % 1024 == 0, "stages stay 1 KB aligned");
   static_assert(NSTAGE >= 2 && SMEM_BYTES <= 232448, "shared memory");
 };
+
+// 2^-k for a whole k >= 0, built from its bit pattern (exact); 0 below the
+// normal range, as the flush-to-zero exponentials of the pass give there.
+__device__ __forceinline__ float pow2_neg(int k) {
+  return k > 126 ? 0.f : __int_as_float((127 - k) << 23);
+}
+
+// Multiply the bf16 probabilities [v0, v1) of one row by f (a power of two, so
+// exact unless a value underflows).  v0, v1 are multiples of 8; rare path.
+__device__ __noinline__ void rescale_probs(__nv_bfloat16* row, int v0, int v1, float f) {
+  for (int v = v0; v < v1; v += 8) {
+    uint4 u = *reinterpret_cast<const uint4*>(row + v);
+    __nv_bfloat162* b = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 x = __bfloat1622float2(b[q]);
+      b[q] = __floats2bfloat162_rn(x.x * f, x.y * f);
+    }
+    *reinterpret_cast<uint4*>(row + v) = u;
+  }
+}
 
 template <int MT, int BN, bool DRAWS>
 __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
@@ -318,8 +351,8 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
     const float scale = row_ok ? __ldg(p.inv_t + row) * LOG2E : 0.f;
     const float r_ref = row_ok ? __ldg(p.ref + row) : 0.f;
     float s_run = 0.f, t_run = 0.f, best = -INFINITY;
+    int kt = 0;  // whole log2 units this thread's reference sits above r_ref
     int best_idx = 0x7fffffff;
-    bool clamped = false;
     // draw-row running statistics: lane = vocabulary row of a half tile
     float dm[DRAW_N], ds[DRAW_N], dscale[DRAW_N];
 #pragma unroll
@@ -345,22 +378,35 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
         if (!row_ok || n0 >= p.V) continue;
         float e[32];
         float cmax = -INFINITY;
-        if (n0 + 32 <= p.V) {
+        const bool full = n0 + 32 <= p.V;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (full || n0 + j < p.V) cmax = fmaxf(cmax, __uint_as_float(r[j]));
+        const float xmax = fmaf(cmax, scale, -r_ref) - (float)kt;
+        if (xmax > RAISE) {
+          // a logit far above this row's reference: raise it by k whole log2
+          // units and scale what was summed and written so far by 2^-k (exact)
+          const int k = (int)fminf(ceilf(xmax), 16777216.f);
+          const float f = pow2_neg(k);
+          s_run *= f;
+          t_run *= f;
+          kt += k;
+          if (p.probs) rescale_probs(p.probs + (long long)row * p.ldp, t_begin * BN, n0, f);
+        }
+        if (kt == 0) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const float a = __uint_as_float(r[j]);
-            cmax = fmaxf(cmax, a);
-            e[j] = ex2(fminf(fmaf(a, scale, -r_ref), V_CLAMP));
+            e[j] = (full || n0 + j < p.V) ? ex2(fmaf(a, scale, -r_ref)) : 0.f;
             s_run += e[j];
             t_run = fmaf(e[j], a, t_run);
           }
         } else {
+          const float ktf = (float)kt;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const float a = __uint_as_float(r[j]);
-            const bool ok = n0 + j < p.V;
-            if (ok) cmax = fmaxf(cmax, a);
-            e[j] = ok ? ex2(fminf(fmaf(a, scale, -r_ref), V_CLAMP)) : 0.f;
+            e[j] = (full || n0 + j < p.V) ? ex2(fmaf(a, scale, -r_ref) - ktf) : 0.f;
             s_run += e[j];
             t_run = fmaf(e[j], a, t_run);
           }
@@ -373,7 +419,6 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
           best = cmax;
           best_idx = first;
         }
-        if (fmaf(cmax, scale, -r_ref) > V_CLAMP) clamped = true;
         if (p.probs) {
           __nv_bfloat16* dst = p.probs + (long long)row * p.ldp + n0;
           if (n0 + 32 <= p.V) {
@@ -441,7 +486,7 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
       p.part[o + plane] = t_run;
       p.part[o + 2 * plane] = best;
       reinterpret_cast<int*>(p.part)[o + 3 * plane] = best_idx;
-      if (clamped) atomicOr(p.status, 16 /* DG_DEV_RANGE */);
+      p.part[o + 4 * plane] = (float)kt;
     }
     if (DRAWS && draws_here) {
       // merge the draw statistics over the lanes, then over the epilogue warps
@@ -487,17 +532,31 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
   if (warp == MMA_WARP) tmem_dealloc(tmem_base, CF::TMEM_COLS);
 }
 
-// Canvas rows: S = sum of the CTA sums (common reference), one warp per row.
+// Canvas rows, one warp per row.  Each CTA's sums and probabilities are
+// relative to ref[row] + k_g (k_g whole log2 units, 0 unless that CTA raised
+// its reference); they are brought to the largest k and added (every factor is
+// exactly 1 without a raise), with the best logit and its lowest index over the
+// CTAs.  The probabilities of a CTA range with a smaller k are scaled to the
+// largest (a power of two, exact), so that p = P~ * prob_scale over the row.
 __device__ void finalize_row(int row, int lane, const float* part, int cpg, int M,
                              const float* inv_t, const float* ref, float* lse, float* entropy,
-                             float* maxz, int32_t* argmax, float* prob_scale) {
+                             float* maxz, int32_t* argmax, float* prob_scale,
+                             __nv_bfloat16* probs, long long ldp, int n_tiles, int bn, int V) {
   const long long plane = (long long)cpg * M;
   const float* pm = part + (long long)row * cpg;
+  int kmax = 0;
+  for (int g = lane; g < cpg; g += 32) kmax = max(kmax, (int)pm[g + 4 * plane]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
   float s = 0.f, t = 0.f, best = -INFINITY;
   int idx = 0x7fffffff;
+  bool lower = false;
   for (int g = lane; g < cpg; g += 32) {
-    s += pm[g];
-    t += pm[g + plane];
+    const int kg = (int)pm[g + 4 * plane];
+    const float f = pow2_neg(kmax - kg);
+    lower |= kg < kmax;
+    s += pm[g] * f;
+    t += pm[g + plane] * f;
     const float bg = pm[g + 2 * plane];
     const int ig = reinterpret_cast<const int*>(pm)[g + 3 * plane];
     if (bg > best || (bg == best && ig < idx)) {
@@ -518,12 +577,32 @@ __device__ void finalize_row(int row, int lane, const float* part, int cpg, int 
   }
   if (lane == 0) {
     const float it = inv_t[row];
-    const float l = (ref[row] + log2f(s)) * LN2;
+    const float l = (ref[row] + (float)kmax + log2f(s)) * LN2;
     lse[row] = l;
     entropy[row] = l - it * (t / s);
     maxz[row] = best * it;
     argmax[row] = idx;
     if (prob_scale) prob_scale[row] = 1.f / s;
+  }
+  // rare: some CTA of this row raised its reference; bring the others to it
+  if (probs && __any_sync(0xffffffffu, lower)) {
+    __nv_bfloat16* pr = probs + (long long)row * ldp;
+    for (int g = 0; g < cpg; ++g) {
+      const int kg = (int)pm[g + 4 * plane];
+      if (kg >= kmax) continue;
+      const float f = pow2_neg(kmax - kg);
+      const int v0 = (int)((long long)g * n_tiles / cpg) * bn;
+      const int v1 = min(V, (int)((long long)(g + 1) * n_tiles / cpg) * bn);
+      for (int v = v0 + 2 * lane; v < v1; v += 64) {
+        if (v + 1 < v1) {
+          __nv_bfloat162* q = reinterpret_cast<__nv_bfloat162*>(pr + v);
+          const float2 x = __bfloat1622float2(*q);
+          *q = __floats2bfloat162_rn(x.x * f, x.y * f);
+        } else {
+          pr[v] = __float2bfloat16_rn(__bfloat162float(pr[v]) * f);
+        }
+      }
+    }
   }
 }
 
@@ -548,14 +627,17 @@ __device__ void finalize_draw(int j, int lane, const float* part_draw, int cpg, 
 // rows, the rest the draw rows (8 rows a block).
 __global__ void heads_finalize_kernel(const float* part, int cpg, int M, const float* inv_t,
                                       const float* ref, float* lse, float* entropy, float* maxz,
-                                      int32_t* argmax, float* prob_scale, const float* part_draw,
+                                      int32_t* argmax, float* prob_scale, __nv_bfloat16* probs,
+                                      long long ldp,
+                                      int n_tiles, int bn, int V, const float* part_draw,
                                       int n_draw, float* lse_draw, int row_blocks) {
   const int lane = threadIdx.x & 31;
   const int w = threadIdx.x >> 5;
   if ((int)blockIdx.x < row_blocks) {
     const int row = blockIdx.x * (blockDim.x >> 5) + w;
     if (row < M)
-      finalize_row(row, lane, part, cpg, M, inv_t, ref, lse, entropy, maxz, argmax, prob_scale);
+      finalize_row(row, lane, part, cpg, M, inv_t, ref, lse, entropy, maxz, argmax, prob_scale,
+                   probs, ldp, n_tiles, bn, V);
   } else {
     const int j = (blockIdx.x - row_blocks) * (blockDim.x >> 5) + w;
     if (j < n_draw) finalize_draw(j, lane, part_draw, cpg, n_draw, lse_draw);
@@ -595,7 +677,7 @@ namespace dgi {
 
 size_t heads_ws_bytes(int M, int V, int n_draw) {
   const int cpg = heads_cpg(M, V, n_draw);
-  return align_up((size_t)4 * cpg * M * 4, 256) + align_up((size_t)2 * cpg * DRAW_N * 4, 256) +
+  return align_up((size_t)5 * cpg * M * 4, 256) + align_up((size_t)2 * cpg * DRAW_N * 4, 256) +
          align_up((size_t)M * 4, 256);
 }
 
@@ -620,7 +702,7 @@ cudaError_t denoise_heads(const uint16_t* h, int M, const uint16_t* draw_rows, i
   p.inv_t_draw = inv_t_draw;
   uint8_t* wp = static_cast<uint8_t*>(ws);
   p.part = reinterpret_cast<float*>(wp);
-  wp += align_up((size_t)4 * p.cpg * M * 4, 256);
+  wp += align_up((size_t)5 * p.cpg * M * 4, 256);
   p.part_draw = reinterpret_cast<float*>(wp);
   wp += align_up((size_t)2 * p.cpg * DRAW_N * 4, 256);
   float* ref = reinterpret_cast<float*>(wp);
@@ -651,8 +733,8 @@ cudaError_t denoise_heads(const uint16_t* h, int M, const uint16_t* draw_rows, i
   if (e != cudaSuccess) return e;
   const int row_blocks = (M + 7) / 8, draw_blocks = (n_draw + 7) / 8;
   heads_finalize_kernel<<<row_blocks + draw_blocks, 256, 0, st>>>(
-      p.part, p.cpg, M, inv_t, ref, out.lse, out.entropy, out.maxz, out.argmax, prob_scale,
-      p.part_draw, n_draw, lse_draw, row_blocks);
+      p.part, p.cpg, M, inv_t, ref, out.lse, out.entropy, out.maxz, out.argmax, prob_scale, p.probs,
+      p.ldp, p.n_tiles, bn, V, p.part_draw, n_draw, lse_draw, row_blocks);
   return cudaGetLastError();
 }
 

@@ -7,8 +7,21 @@
 
 namespace dgi {
 
-// Device address of the library's status word (set-up once per device).
+// Identity of the CUDA context current on this thread (0 if none): a context
+// created again (e.g. after cudaDeviceReset) gets a new identity.
+uint64_t context_id();
+// Device address of one of this library's __device__ variables on the current
+// device.  The address is cached per device together with the context it was
+// looked up in, and looked up again (cudaGetSymbolAddress: no allocation) when
+// the current context differs.  `symbol` is the host-side stand-in of the
+// variable, which must never reach a kernel itself.
+enum SymbolSlot { SYM_STATUS = 0, SYM_NOALLOC_SCRATCH = 1, SYM_COUNT = 2 };
+void* device_symbol(const void* symbol, int slot);
+// Device address of the library's status word on the current device.
 int* status_ptr();
+// Shapes every lm-head entry point accepts: d_model a positive multiple of 8
+// (16-byte rows for TMA), a non-empty vocabulary.
+inline bool lm_dims_ok(int d_model, int V) { return d_model >= 8 && d_model % 8 == 0 && V >= 1; }
 int num_sms();
 // SMs a launch plans its grid for: the caller's share when it is in (0, num_sms()),
 // else the whole device.

@@ -13,7 +13,6 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <mutex>
 
 #include "dg.h"
 #include "internal.h"
@@ -26,22 +25,13 @@ namespace {
 constexpr size_t kScratchBytes = (size_t)5 * 256 * DG_NOALLOC_MAX_ROWS * sizeof(float);
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {};
-std::mutex g_scratch_mu;
-
-// Device address of the scratch array on the current device, looked up once per
-// device (the host-side symbol is only a stand-in and must not reach a kernel).
+// Device address of the scratch array on the current device.  The host-side
+// symbol is only a stand-in and must not reach a kernel; the address is looked
+// up with cudaGetSymbolAddress (no allocation) the first time on a device and
+// again whenever the current context is a different one (after cudaDeviceReset
+// the library's module is loaded anew and the old address is stale).
 void* scratch_on_current_device() {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
-    g_scratch_addr[dev] = p;
-  }
-  return g_scratch_addr[dev];
+  return dgi::device_symbol(g_noalloc_scratch, dgi::SYM_NOALLOC_SCRATCH);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -53,7 +43,8 @@ extern "C" int dg_lmhead_logsoftmax_entropy_noalloc(const dg_dims* d, const uint
                                                     float* lse, float* entropy, float* maxz,
                                                     int32_t* argmax, void* stream) {
   if (!d || M < 1) return DG_ERR_ARG;
-  if (d->d_model < 8 || d->d_model % 8 || d->V < 1) return DG_ERR_SHAPE;
+  // the same shape rule as dg_lmhead_logsoftmax_entropy
+  if (!dgi::lm_dims_ok(d->d_model, d->V)) return DG_ERR_SHAPE;
   if (M > DG_NOALLOC_MAX_ROWS) return DG_ERR_SHAPE;
   if (!h || !w || !inv_t || !lse || !entropy || !maxz || !argmax) return DG_ERR_ARG;
   if (!aligned16(h) || !aligned16(w)) return DG_ERR_ARG;

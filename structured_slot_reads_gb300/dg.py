@@ -78,6 +78,7 @@ _SIGS = {
     "dg_canvas_update": [DP, P, P, P, P, P, I, P, P],
     "dg_philox_fill": [U64, P, I, P, P],
     "dg_validate_slots": [DP, P, P, P, I, I],
+    "dg_validate_slots_wide": [DP, P, P, P, I, I, I],
     "dg_workspace_bytes": [DP, I, I],
     "dg_get_status": [P, P],
     "dg_clear_status": [P],
@@ -296,6 +297,55 @@ def dg_philox_fill(seed, ctr4, n, out4, stream=None):
 def dg_validate_slots(dims, slot_row_host, label_ids_host, n_labels_host, S, M):
     return lib().dg_validate_slots(ctypes.byref(dims), _p(slot_row_host), _p(label_ids_host),
                                    _p(n_labels_host), S, M)
+
+
+def dg_validate_slots_wide(dims, slot_row_host, label_ids_host, n_labels_host, S, L, M):
+    return lib().dg_validate_slots_wide(ctypes.byref(dims), _p(slot_row_host),
+                                        _p(label_ids_host), _p(n_labels_host), S, L, M)
+
+
+def validate_slot_table(dims, slot_row, label_ids, n_labels, M, what="slot table"):
+    """Run the library's synchronous slot-table check on host arrays (int32 copies
+    are made as needed) and raise DgError if it rejects them: more labels than the
+    table allows (the 26-alternative limit for 26-wide tables), a duplicate label,
+    a label id outside the vocabulary or a slot row outside [0, M)."""
+    import numpy as np
+    row = np.ascontiguousarray(np.asarray(slot_row), dtype=np.int32)
+    lab = np.ascontiguousarray(np.asarray(label_ids), dtype=np.int32)
+    n = np.ascontiguousarray(np.asarray(n_labels), dtype=np.int32)
+    S = int(row.shape[0])
+    if S == 0:
+        return
+    L = int(lab.shape[1]) if lab.ndim == 2 else MAX_LABELS
+    if lab.shape != (S, L) or n.shape != (S,):
+        raise DgError(DG_ERR_ARG, what)
+    code = (dg_validate_slots(dims, row, lab, n, S, int(M)) if L == MAX_LABELS else
+            dg_validate_slots_wide(dims, row, lab, n, S, L, int(M)))
+    _check(code, what)
+
+
+class DgDeviceError(RuntimeError):
+    """Bits of the device status word that a step found set (DG_DEV_*)."""
+
+    NAMES = {DG_DEV_TIMEOUT: "a bounded wait timed out", DG_DEV_BAD_PAGE: "bad page index",
+             DG_DEV_BAD_LABEL: "label id or count out of range",
+             DG_DEV_BAD_INDEX: "slot row or token outside its tensor",
+             DG_DEV_RANGE: "reserved status bit"}
+
+    def __init__(self, status, what):
+        names = [v for k, v in self.NAMES.items() if status & k]
+        super().__init__(f"{what}: device status {status:#x} ({'; '.join(names)})")
+        self.status = status
+
+
+def check_status(stream=None, what="libdg"):
+    """dg_get_status on ``stream`` (synchronises it); clears the word and raises
+    DgDeviceError if any bit is set, else returns 0."""
+    status = dg_get_status(stream)
+    if status:
+        dg_clear_status(stream)
+        raise DgDeviceError(status, what)
+    return 0
 
 
 def dg_workspace_bytes(dims, which, rows):

@@ -34,6 +34,16 @@ def _dev(a, dtype, device):
     return torch.as_tensor(np.ascontiguousarray(a)).to(device=device, dtype=dtype)
 
 
+def _pad26(lab):
+    """A label list as one row of a 26-wide table (-1 padded).  A longer list keeps
+    only its first 26 ids here; its count still says how many it had, so the slot
+    table check refuses it."""
+    pad = np.full(dg.MAX_LABELS, -1, np.int32)
+    k = min(len(lab), dg.MAX_LABELS)
+    pad[:k] = np.asarray(lab)[:k]
+    return pad
+
+
 def slot_outputs(S, R, dev, L=dg.MAX_LABELS):
     """Device buffers of one slot read over S slots with R reads each (label stride L)."""
     f32, i32, u8 = torch.float32, torch.int32, torch.uint8
@@ -75,11 +85,11 @@ class TwoStageRead:
             for pos, lab in [(t["group_pos"], t["group_labels"])] + list(t["others"]):
                 rows.append(b * C + pos)
                 reqs.append(b)
-                pad = np.full(dg.MAX_LABELS, -1, np.int32)
-                pad[:len(lab)] = lab
-                labs.append(pad)
+                labs.append(_pad26(lab))
                 ns.append(len(lab))
         self.S1 = len(rows)
+        # the 26-alternative limit and the label checks, before anything reaches the GPU
+        dg.validate_slot_table(self.dims, rows, np.stack(labs), ns, self.M, "stage-1 slot table")
         self.slot_row1 = _dev(rows, i32, device)
         self.slot_req1 = _dev(reqs, i32, device)
         self.label_ids1 = _dev(np.stack(labs), i32, device)
@@ -92,11 +102,13 @@ class TwoStageRead:
                 cs.append(self.group_slot[b])
                 cv.append(g)
                 own.append(b)
-                pad = np.full(dg.MAX_LABELS, -1, np.int32)
-                pad[:len(items)] = items
-                qlab.append(pad)
+                qlab.append(_pad26(items))
                 qn.append(len(items))
         self.Q = len(cs)
+        # every stage-2 question is checked as a slot of its owner's item row
+        item_rows = [b * C + tables[b]["item_pos"] for b in own]
+        dg.validate_slot_table(self.dims, item_rows, np.stack(qlab), qn, self.M,
+                               "stage-2 question table")
         self.cond_slot = _dev(cs, i32, device)
         self.cond_value = _dev(cv, i32, device)
         self.q_owner = _dev(own, i32, device)
@@ -177,6 +189,11 @@ class TwoStageRead:
         """Slot decisions completed by one run (stage-1 slots + asked stage-2 slots)."""
         return self.S1 + int((self.n_labels2 > 0).sum().item())
 
+    def check(self, stream=None):
+        """Raise dg.DgDeviceError if a kernel of the enqueued runs set a status bit
+        (synchronises ``stream``)."""
+        return dg.check_status(stream, "two-stage read")
+
 
 class ReadStep:
     """The read-only step of a structured read (no commit, no self-conditioning).
@@ -214,6 +231,7 @@ class ReadStep:
         self.attn_lse = torch.empty((B, shape.Hq, C), dtype=f32, device=device)
         self.L = max([dg.MAX_LABELS] + [k for _, k in shape.slots])
         row, req, lab, n = inputs.slot_table(shape, seed, self.L)
+        dg.validate_slot_table(self.dims, row, lab, n, self.M)
         self.S = len(row)
         self.slot_row = _dev(row, i32, device)
         self.slot_req = _dev(req, i32, device)
@@ -263,6 +281,11 @@ class ReadStep:
             main.wait_stream(attn_stream)
         attn_kernels = 1 if dg.dg_workspace_bytes(attn_dims, dg.DG_WS_ATTN, 0) <= 256 else 2
         return attn_kernels + 5
+
+    def check(self, stream=None):
+        """Raise dg.DgDeviceError if a kernel of the enqueued reads set a status bit
+        (synchronises ``stream``)."""
+        return dg.check_status(stream, "read step")
 
 
 class Prefill:

@@ -29,6 +29,14 @@ dg_slot_read, dg_selfcond_embed), which stream W three times, on one stream.
 
 The same object serves the end-to-end path: ``upload`` copies a step's inputs
 from pinned host memory, ``download`` reads back the decisions.
+
+Slot tables enter through ``set_slots``, which runs the library's synchronous
+check on the host arrays first (sotaaz.com, "The server accepts at most 26
+alternatives per question": a question with more than 26 alternatives is
+refused before anything runs).  ``check`` reads the device status word after
+the enqueued steps (it synchronises the stream) and raises ``dg.DgDeviceError``
+if any bit is set: a wait that timed out (its kernel stopped early and left
+outputs unwritten) or an index, label or page out of range.
 """
 import torch
 
@@ -167,6 +175,26 @@ class DenoiseStep:
             self.prob_scale = _empty((self.M,), f32, dev)
             self.ws_heads = _empty((dg.dg_workspace_bytes(self.dims, dg.DG_WS_HEADS, self.M),), u8, dev)
             self.ws_pe = _empty((dg.dg_workspace_bytes(self.dims, dg.DG_WS_PROBS_EMBED, self.M),), u8, dev)
+
+    # ------------------------------------------------------------ slots
+    def set_slots(self, slot_row, slot_req, label_ids, n_labels):
+        """Load the slot table from host arrays after the library's synchronous
+        check (raises dg.DgError: more than 26 labels, a duplicate or out-of-vocabulary
+        label, a slot row outside the canvas rows)."""
+        import numpy as np
+        if not self.with_slots:
+            raise ValueError("this step has no slots")
+        dg.validate_slot_table(self.dims, slot_row, label_ids, n_labels, self.M)
+        for name, a in (("slot_row", slot_row), ("slot_req", slot_req),
+                        ("label_ids", label_ids), ("n_labels", n_labels)):
+            t = torch.from_numpy(np.ascontiguousarray(np.asarray(a), dtype=np.int32))
+            getattr(self, name).copy_(t.view(getattr(self, name).shape))
+
+    def check(self, stream=None):
+        """Read the device status word after the enqueued steps (synchronises
+        ``stream``), clear it and raise dg.DgDeviceError if any bit was set.
+        Returns 0 otherwise."""
+        return dg.check_status(stream, "denoise step")
 
     # ------------------------------------------------------------- graphs
     def capture(self, step_idx):

@@ -265,3 +265,86 @@ def test_8bit_self_conditioning_validates(lib):
     assert dg.dg_quantize_cols_e4m3(None, -1, 4, None, None, stream=0) == dg.DG_ERR_ARG
     assert dg.dg_quantize_cols_e4m3(None, 4, 4, None, None, stream=0) == dg.DG_ERR_ARG
     assert dg.dg_quantize_cols_e4m3(None, 0, 4, None, None, stream=0) == dg.DG_OK
+
+
+def test_validate_slots_wide(lib):
+    """Tables of stride L for the wide read: up to L labels per slot, L <= 256."""
+    d = dg.make_dims(V=5000, d_model=8)
+    lab = np.full((2, 77), -1, np.int32)
+    lab[0, :77] = np.arange(77)
+    lab[1, :3] = [7, 8, 9]
+    n = np.array([77, 3], np.int32)
+    rows = np.array([0, 5], np.int32)
+    assert dg.dg_validate_slots_wide(d, rows, lab, n, 2, 77, 10) == dg.DG_OK
+    assert dg.dg_validate_slots_wide(d, rows, lab, np.array([78, 3], np.int32), 2, 77,
+                                     10) == dg.DG_ERR_TOO_MANY_LABELS
+    assert dg.dg_validate_slots_wide(d, rows, lab, n, 2, 257, 10) == dg.DG_ERR_TOO_MANY_LABELS
+    dup = lab.copy()
+    dup[0, 76] = 0
+    assert dg.dg_validate_slots_wide(d, rows, dup, n, 2, 77, 10) == dg.DG_ERR_LABEL
+    # the binding picks the 26-wide or the wide check from the table's width
+    dg.validate_slot_table(d, rows, lab, n, 10)
+    with pytest.raises(dg.DgError) as ei:
+        dg.validate_slot_table(d, rows, dup, n, 10)
+    assert ei.value.code == dg.DG_ERR_LABEL
+
+
+def test_step_set_slots_refuses_bad_tables(lib):
+    """The step's slot tables pass the library's synchronous check before they are
+    copied: 27 alternatives, a repeated label, an id outside the vocabulary and a
+    slot row outside the canvas are refused, and the device tables stay as they were."""
+    import torch
+
+    from structured_slot_reads_gb300 import configs, inputs
+    from structured_slot_reads_gb300.step import DenoiseStep
+    shp = configs.TINY
+    w = torch.zeros((shp.V, shp.D), dtype=torch.bfloat16)
+    st = DenoiseStep(shp, w, w, device="cpu")
+    row, req, lab, n = inputs.slot_table(shp, 0)
+    st.set_slots(row, req, lab, n)
+    assert st.n_labels.tolist() == n.tolist()
+    before = st.label_ids.clone()
+    bad_cases = []
+    n27 = n.copy()
+    n27[0] = 27
+    bad_cases.append(((row, req, lab, n27), dg.DG_ERR_TOO_MANY_LABELS))
+    dup = lab.copy()
+    dup[0, 1] = dup[0, 0]
+    bad_cases.append(((row, req, dup, n), dg.DG_ERR_LABEL))
+    oov = lab.copy()
+    oov[0, 2] = shp.V
+    bad_cases.append(((row, req, oov, n), dg.DG_ERR_LABEL))
+    bad_cases.append(((np.array([shp.B * shp.C], np.int32), req, lab, n), dg.DG_ERR_SHAPE))
+    for args, code in bad_cases:
+        with pytest.raises(dg.DgError) as ei:
+            st.set_slots(*args)
+        assert ei.value.code == code
+    assert torch.equal(st.label_ids, before)
+
+
+def test_two_stage_runner_refuses_27_alternatives(lib):
+    """A stage-2 question with 27 items is refused when the batch is set up."""
+    import torch
+
+    from structured_slot_reads_gb300 import configs, inputs
+    from structured_slot_reads_gb300.read import TwoStageRead
+    shp = configs.scaled(configs.MIXED_BATCH, B=2, C=64, P=200, D=256, V=4096)
+    tables = inputs.two_stage_tables(shp, 3)
+    tables[1]["item_labels"][4] = np.arange(27, dtype=np.int32)
+    plen = inputs.prompt_lengths(shp, 3, lo=100)
+    w = torch.zeros((shp.V, shp.D), dtype=torch.bfloat16)
+    with pytest.raises(dg.DgError) as ei:
+        TwoStageRead(shp, w, w, tables, plen, device="cpu", seed=3)
+    assert ei.value.code == dg.DG_ERR_TOO_MANY_LABELS
+
+
+@pytest.mark.parametrize("page_size", [4, 24, 256])
+def test_attention_refuses_page_sizes_the_512_kernel_cannot_take(lib, page_size):
+    """512-wide heads run only on the tensor-core kernel: a page size it cannot take
+    is refused before launch instead of running on another kernel."""
+    d = dg.make_dims(B=1, C=64, P_max=96, Hq=8, Hkv=2, d_head=512, W=16)
+    ws = dg.dg_workspace_bytes(d, dg.DG_WS_ATTN, 0)
+    pages = (96 + page_size - 1) // page_size
+    rc = dg.lib().dg_attn_decode(ctypes.byref(d), 256, 256, 256, 256, 256, 256, pages, pages,
+                                 page_size, 256, 256, 256, 256, ws, None)
+    assert rc == dg.DG_ERR_SHAPE

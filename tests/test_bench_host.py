@@ -49,3 +49,42 @@ def test_prefill_work_counts_causal_pairs():
     shape = configs.scaled(configs.TINY, B=2, P=9, Hq=4, d_head=64)
     pairs = sum(1 for i in range(9) for j in range(9) if j <= i)
     assert b.prefill_flops(shape) == 4.0 * 2 * 4 * 64 * pairs
+
+
+def test_reference_arm_times_whole_oracle_steps():
+    """The reference arm times whole float64 steps (no sampling) and reports the
+    steps it actually timed; at the tiny shape every part runs in milliseconds."""
+    import argparse
+
+    from structured_slot_reads_gb300 import configs
+    b = _bench()
+    line = b.reference_arm(argparse.Namespace(steps=3, warmup=5), 0, shape=configs.TINY)
+    assert line["impl"] == "reference" and line["steps"] == 3 and line["warmup"] == 2
+    assert line["steps_requested"] == 3 and line["warmup_requested"] == 5
+    assert line["value"] > 0 and line["e2e"]["value"] == line["value"]
+    assert set(line["cpu_baseline"]["parts_s"]) == {"attention", "lmhead", "slot_read", "commit",
+                                                   "selfcond", "canvas_update"}
+    # a tiny time budget stops after the first timed step
+    short = b.reference_arm(argparse.Namespace(steps=50, warmup=0), 0, budget_s=0.0,
+                            shape=configs.TINY)
+    assert short["steps"] == 1 and short["warmup"] == 0
+    assert b.reference_arm(argparse.Namespace(steps=3, warmup=5), 1) is None
+
+
+def test_heads_roofline_counts_algorithmic_bytes():
+    """The heads pass's algorithmic bytes are W plus the rows and statistics; the
+    bf16 probability hand-off to the P.E GEMM is reported apart."""
+    from structured_slot_reads_gb300 import configs
+    b = _bench()
+    shape = configs.FULL_CANVAS
+
+    class St:
+        n_draw, S = 12, 3
+    work = b.call_work(shape, St())
+    W = shape.V * shape.D * 2
+    by, fl = work["dg_denoise_heads"]
+    assert W < by < W * 1.002
+    assert fl == 2.0 * (256 + 12) * shape.V * shape.D
+    assert b.spill_bytes(shape) == 256 * shape.V * 2
+    assert work["dg_selfcond_from_probs"][0] < W * 1.01
+    assert work["dg_commit"][0] > 0 and work["dg_slot_finish"][0] > 0

@@ -409,19 +409,50 @@ def test_selfcond_from_probs_split_k(M, V, D):
     assert_rel(host(out), want, what="expected embedding")
 
 
-def test_denoise_heads_flags_out_of_range_logits():
-    M, V, D = 8, 2048, 128
-    h, w, _, inv_t = _lm_inputs(M, V, D, seed=5)
-    # row 3: one logit far above everything in the first 8 vocabulary entries
-    wl = w[1000].astype(np.float64)
-    x = h[3].astype(np.float64) + (200.0 / float(inv_t[3])) * wl / np.dot(wl, wl)
-    h[3] = inputs.to_bf16(x.astype(np.float32))
+@pytest.mark.parametrize("nd", [0, 4])
+def test_denoise_heads_exact_for_far_logits(nd):
+    """Rows with logits far above their reference (which is read off the first 8
+    vocabulary entries): the CTA that meets one raises its reference by whole powers
+    of two and rescales what it already wrote, the finalize brings the other CTAs'
+    probabilities to it, so the statistics and the self-conditioning probabilities
+    stay exact; no status bit is set.  Row 3 has one logit 200 nats up (CTA-local
+    raise, several hundred log2 units); row 5 has two, 60 and 120 nats up, in two
+    CTA ranges (two raises of different size); row 6 one in the first tile."""
+    M, V, D = 8, 65536, 128
+    h, w, e, inv_t = _lm_inputs(M, V, D, seed=5)
+
+    def plant(row, vid, nats):
+        wl = w[vid].astype(np.float64)
+        x = h[row].astype(np.float64) + (nats / float(inv_t[row])) * wl / np.dot(wl, wl)
+        h[row] = inputs.to_bf16(x.astype(np.float32))
+
+    plant(3, 40000, 200.0)
+    plant(5, 3000, 60.0)
+    plant(5, 61000, 120.0)
+    plant(6, 100, 150.0)
+    draws = inputs.hidden(nd, D, 77) if nd else None
+    inv_d = inputs.inv_temperature(nd, 78) if nd else None
     dg.dg_clear_status()
-    got = _run_heads(h, None, w, inv_t, None)
-    assert dg.dg_get_status() & 16
-    dg.dg_clear_status()
-    # the exact recomputing path is unaffected
-    o_lse, _, _, o_arg = oracle.lmhead_stats(h, w, inv_t)
-    lse, _, _, arg = _run_lmhead(h, w, inv_t)
-    assert_abs(lse, o_lse, what="lse (recomputing path)")
-    assert arg[3] == 1000 and got["arg"][3] == 1000
+    got = _run_heads(h, draws, w, inv_t, inv_d)
+    assert dg.dg_get_status() == 0
+    o_lse, o_ent, o_maxz, o_arg = oracle.lmhead_stats(h, w, inv_t)
+    assert_abs(got["lse"], o_lse, what="lse")
+    assert_abs(got["ent"], o_ent, what="entropy")
+    assert_abs(got["maxz"], o_maxz, what="max logit")
+    assert got["arg"][3] == 40000 and got["arg"][5] == 61000 and got["arg"][6] == 100
+    z = (h.astype(np.float64) @ w.astype(np.float64).T) * inv_t[:, None]
+    clear = top2_gap(z) > 1e-3
+    assert np.array_equal(got["arg"][clear], o_arg[clear])
+    # the probabilities: P.E from them is the expected embedding of every row
+    d = got["dims"]
+    out = torch.empty((M, D), dtype=torch.float32, device="cuda")
+    ws = torch.empty(dg.dg_workspace_bytes(d, dg.DG_WS_PROBS_EMBED, M), dtype=torch.uint8,
+                     device="cuda")
+    rc = dg.dg_selfcond_from_probs(d, got["probs"], got["ld"], got["scale"], M, dev_bf16(e), out,
+                                   ws)
+    assert rc == dg.DG_OK
+    torch.cuda.synchronize()
+    assert_rel(host(out), oracle.selfcond_embed(h, w, e, inv_t), what="expected embedding")
+    if nd:
+        d_lse, _, _, _ = oracle.lmhead_stats(draws, w, inv_d)
+        assert_abs(got["lse_draw"], d_lse, what="draw-row lse")

@@ -33,10 +33,7 @@ def _setup(shape):
     x = inputs.step_inputs(shape, 0)
     st = DenoiseStep(shape, dev_bf16(x["w"]), dev_bf16(x["e"]), seed=3)
     st.prompt_len.copy_(dev(x["prompt_len"]))
-    st.slot_row.copy_(dev(x["slot_row"]))
-    st.slot_req.copy_(dev(x["slot_req"]))
-    st.label_ids.copy_(dev(x["label_ids"]))
-    st.n_labels.copy_(dev(x["n_labels"]))
+    st.set_slots(x["slot_row"], x["slot_req"], x["label_ids"], x["n_labels"])
     return st
 
 

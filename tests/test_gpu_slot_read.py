@@ -110,3 +110,47 @@ def test_slot_read_single_structured_read_full_size(seed, full_weights):
     got = _run_read(h, wd, ed, inv_t, slot_row, slot_req, label_ids, n_labels, seed, 0, 4, 0.1)
     _compare(got, want, n_labels)
     assert np.all(got["resampled"] == (1 if mode == "high" else 0))
+
+
+def test_device_label_count_beyond_26_is_not_read():
+    """A slot whose label count reaches the device out of range (27, or negative: a
+    table that skipped the host check) is not read: chosen -1, no reads, zero
+    distribution, entropy and logprobs, and DG_DEV_BAD_LABEL is set; the other
+    slots of the call are read as usual."""
+    shape = configs.scaled(configs.SINGLE_READ, C=64, D=256, V=4096,
+                           slots=[(5, 2), (30, 26), (50, 5)])
+    h, w, e, inv_t, slot_row, slot_req, label_ids, n_labels = _case(shape, 4)
+    h, want = margins.prepare_slot_inputs(h, w, e, inv_t, slot_row, slot_req, label_ids,
+                                          n_labels, 4, 0, 4, 0.1, [None] * 3)
+    bad_n = n_labels.copy()
+    bad_n[1] = 27
+    bad_n[2] = -1
+    M, D = h.shape
+    S = len(slot_row)
+    d = dg.make_dims(d_model=D, V=shape.V)
+    f32, i32 = torch.float32, torch.int32
+    out = dict(q_avg=torch.full((S, 26), 7.0, dtype=f32, device="cuda"),
+               h_slot=torch.full((S,), 7.0, dtype=f32, device="cuda"),
+               chosen=torch.full((S,), 7, dtype=i32, device="cuda"),
+               lp=torch.full((S, 4, 26), 7.0, dtype=f32, device="cuda"),
+               res=torch.full((S,), 7, dtype=torch.uint8, device="cuda"),
+               nr=torch.full((S,), 7, dtype=i32, device="cuda"),
+               tok=torch.empty((S, 4), dtype=i32, device="cuda"))
+    ws = torch.empty(dg.dg_workspace_bytes(d, dg.DG_WS_SLOT_READ, S * 4), dtype=torch.uint8,
+                     device="cuda")
+    dg.dg_clear_status()
+    rc = dg.dg_slot_read(d, dev_bf16(h), M, dev_bf16(w), dev_bf16(e), dev(inv_t), dev(slot_row),
+                         dev(slot_req), dev(label_ids), dev(bad_n), S, 4, 0, 4, 0.1,
+                         out["q_avg"], out["h_slot"], out["chosen"], out["lp"], out["res"],
+                         out["nr"], out["tok"], ws)
+    assert rc == dg.DG_OK
+    torch.cuda.synchronize()
+    assert dg.dg_get_status() & dg.DG_DEV_BAD_LABEL
+    dg.dg_clear_status()
+    got = {k: host(v) for k, v in out.items()}
+    for s in (1, 2):
+        assert got["chosen"][s] == -1 and got["nr"][s] == 0 and got["res"][s] == 0
+        assert np.all(got["q_avg"][s] == 0) and got["h_slot"][s] == 0
+        assert np.all(got["lp"][s] == 0)
+    assert got["chosen"][0] == want["chosen"][0] and got["nr"][0] == want["n_reads"][0]
+    assert_abs(got["q_avg"][0, :2], want["q_avg"][0, :2], what="slot 0 distribution")

@@ -1,10 +1,10 @@
 """GPU parity of the batched two-stage read (mixed batch, paged prompt KV, ask_if).
 
 Reduced shapes (4 requests, vocabulary 4096, d_model 256, ragged prompts of
-up to 200 tokens in 16-token pages, 512-wide heads) are compared in full; the
-full mixed batch (32 requests, prompts U[512, 8192], vocabulary 262144,
-d_model 2816) is compared on every decision whose margin holds and checked for
-validity elsewhere.
+up to 200 tokens in 16-token pages, 512-wide heads) and the full mixed batch
+(32 requests, prompts U[512, 8192], vocabulary 262144, d_model 2816) are
+compared on every decision of both stages: the slot rows are re-drawn until
+each stage-1 slot and each asked stage-2 slot has its margin.
 """
 import numpy as np
 import pytest
@@ -32,85 +32,66 @@ def _build(shape, seed):
                 plen=plen)
 
 
-def _runner(shape, x, seed):
+def _runner(shape, x, seed, w_or):
+    """The two-stage runner with its slot rows re-drawn until every decision of both
+    stages (each stage-1 slot, each asked stage-2 slot) has its margin; returns the
+    runner and the oracle's result for the final inputs."""
     tr = TwoStageRead(shape, dev_bf16(x["w"]), dev_bf16(x["e"]), x["tables"], x["plen"],
                       seed=seed)
+    rows1, lab1, n1 = tr.host_slots1
+    slots1 = (rows1, host(tr.slot_req1), lab1, n1)
+    slots2 = (host(tr.slot_row2), np.arange(tr.S2))
+    x["h"], want = margins.prepare_two_stage_inputs(x["h"], w_or, x["e"], x["inv_t"], slots1,
+                                                    tr.host_questions, slots2, seed, shape.R,
+                                                    shape.gate)
     tr.h.copy_(dev_bf16(x["h"]))
     tr.inv_t.copy_(dev(x["inv_t"]))
     tr.q.copy_(dev_bf16(x["att"]["q"]))
     tr.kc.copy_(dev_bf16(x["att"]["kc"]))
     tr.vc.copy_(dev_bf16(x["att"]["vc"]))
     tr.set_kv(dev_bf16(x["pk"]), dev_bf16(x["pv"]), dev(x["table"]))
-    return tr
+    return tr, want
 
 
-def _oracle_two_stage(tr, x, w_or, shape, seed):
-    rows1, lab1, n1 = tr.host_slots1
-    req1 = host(tr.slot_req1)
-    st1 = margins.slot_read_oracle(x["h"], w_or, x["e"], x["inv_t"], rows1, req1, lab1, n1,
-                                   seed, 0, shape.R, shape.gate)
-    cs, cv, own, qlab, qn = tr.host_questions
-    lab2, n2, fired = oracle.ask_if_select(st1["chosen"], cs, cv, own, qlab, qn, tr.S2)
-    rows2 = host(tr.slot_row2)
-    st2 = margins.slot_read_oracle(x["h"], w_or, x["e"], x["inv_t"], rows2, np.arange(tr.S2),
-                                   lab2, n2, seed, 1, shape.R, shape.gate)
-    return st1, (lab2, n2, fired), st2
-
-
-def _check_stage(out, want, n_labels, exact_mask):
+def _check_stage(out, want, n_labels):
+    """Every slot of a stage: distributions within 2e-3, decisions bit for bit (the
+    inputs carry margins), not-asked slots (no labels) unread.  Returns the number
+    of decisions compared."""
     got = {k: host(v) for k, v in out.items()}
+    compared = 0
     for s, n in enumerate(n_labels):
         assert_abs(got["q_avg"][s, :n], want["q_avg"][s, :n], what="label distribution")
-        if exact_mask[s]:
-            assert got["chosen"][s] == want["chosen"][s]
-            assert got["resampled"][s] == want["resampled"][s]
-            assert got["n_reads"][s] == want["n_reads"][s]
-        elif n > 0:
-            # no decisive margin: the choice must attain the (oracle) maximum
-            q = want["q_avg"][s, :n]
-            assert q[got["chosen"][s]] >= q.max() - 2e-3
+        assert got["chosen"][s] == want["chosen"][s]
+        assert got["resampled"][s] == want["resampled"][s]
+        assert got["n_reads"][s] == want["n_reads"][s]
+        compared += int(n > 0)
     assert np.array_equal(got["tokens"], want["tokens"])
-
-
-def _exact(want, n_labels, gate):
-    ok = []
-    for s, n in enumerate(n_labels):
-        if n == 0:
-            ok.append(True)
-            continue
-        q = np.sort(want["q_avg"][s, :n])
-        ok.append(abs(want["h_draw"][s, 0] - gate) > margins.GATE_MARGIN
-                  and (n == 1 or q[-1] - q[-2] > margins.CHOICE_MARGIN))
-    return np.array(ok)
+    return compared
 
 
 def test_two_stage_reduced():
     shape = configs.scaled(configs.MIXED_BATCH, B=4, C=64, P=200, D=256, V=4096)
     seed = 3
     x = _build(shape, seed)
-    tr = _runner(shape, x, seed)
+    tr, (st1, (lab2, n2, fired), st2) = _runner(shape, x, seed, x["w"])
     dg.dg_clear_status()
     tr.run()
     torch.cuda.synchronize()
-    assert dg.dg_get_status() == 0
+    tr.check()
     kenc, venc = oracle.paged_to_contiguous(x["pk"], x["pv"], x["table"], x["plen"],
                                             shape.page_size)
     ref, ref_lse = oracle.attn_decode(x["att"]["q"], x["att"]["kc"], x["att"]["vc"], kenc, venc,
                                       x["plen"], shape.W)
     assert_rel(host(tr.attn_out), ref, what="paged attention")
     assert_abs(host(tr.attn_lse), ref_lse, what="paged attention lse")
-    st1, (lab2, n2, fired), st2 = _oracle_two_stage(tr, x, x["w"], shape, seed)
     n1 = tr.host_slots1[2]
-    _check_stage(tr.out1, st1, n1, _exact(st1, n1, shape.gate))
-    # the gate picks exactly the oracle's stage-2 questions where stage 1 agreed
-    exact1 = _exact(st1, n1, shape.gate)
-    for b in range(shape.B):
-        if exact1[tr.group_slot[b]]:
-            assert host(tr.n_labels2)[b] == n2[b]
-            assert np.array_equal(host(tr.label_ids2)[b], lab2[b])
+    assert _check_stage(tr.out1, st1, n1) == tr.S1
+    # the gate picks exactly the oracle's stage-2 questions
+    assert np.array_equal(host(tr.fired), fired)
+    assert np.array_equal(host(tr.n_labels2), n2)
+    assert np.array_equal(host(tr.label_ids2), lab2)
     assert host(tr.fired).sum() == shape.B          # exactly one question fires per request
-    if np.all(exact1):
-        _check_stage(tr.out2, st2, n2, _exact(st2, n2, shape.gate))
+    assert _check_stage(tr.out2, st2, n2) == shape.B
 
 
 @pytest.mark.parametrize("S1,S2,Q", [(10, 6, 40), (30, 40, 300), (5, 1, 3), (4, 3, 97)])
@@ -147,30 +128,21 @@ def test_two_stage_mixed_batch_full_size():
     shape = configs.MIXED_BATCH
     seed = 1
     x = _build(shape, seed)
-    tr = _runner(shape, x, seed)
+    w64 = x["w"].astype(np.float64)
+    tr, (st1, (lab2, n2, fired), st2) = _runner(shape, x, seed, w64)
     tr.run()
     torch.cuda.synchronize()
-    assert dg.dg_get_status() == 0
-    w64 = x["w"].astype(np.float64)
-    st1, (lab2, n2, fired), st2 = _oracle_two_stage(tr, x, w64, shape, seed)
+    tr.check()
     n1 = tr.host_slots1[2]
-    exact1 = _exact(st1, n1, shape.gate)
-    _check_stage(tr.out1, st1, n1, exact1)
+    # every stage-1 and every asked stage-2 decision, bit for bit
+    assert _check_stage(tr.out1, st1, n1) == tr.S1
+    assert np.array_equal(host(tr.fired), fired)
+    assert np.array_equal(host(tr.label_ids2), lab2)
     assert host(tr.fired).sum() == shape.B
-    agree = [b for b in range(shape.B) if exact1[tr.group_slot[b]]]
-    for b in agree:
-        assert np.array_equal(host(tr.label_ids2)[b], lab2[b])
-    got2 = {k: host(v) for k, v in tr.out2.items()}
-    exact2 = _exact(st2, n2, shape.gate)
-    for b in agree:
-        n = n2[b]
-        assert_abs(got2["q_avg"][b, :n], st2["q_avg"][b, :n], what="stage-2 distribution")
-        if exact2[b]:
-            assert got2["chosen"][b] == st2["chosen"][b]
-            assert got2["resampled"][b] == st2["resampled"][b]
+    assert _check_stage(tr.out2, st2, n2) == shape.B
     # a request reads each stage at most four times
     assert np.all(host(tr.out1["n_reads"]) <= shape.R)
-    assert np.all(got2["n_reads"] <= shape.R)
+    assert np.all(host(tr.out2["n_reads"]) <= shape.R)
     # paged attention on sampled requests: the longest prompt and request 0
     got = host(tr.attn_out)
     for b in sorted({0, int(np.argmax(x["plen"]))}):
