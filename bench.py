@@ -43,6 +43,8 @@ WORKLOADS = {
     "lmhead_fp8_m256": ("lmhead_fp8", "FULL_CANVAS", {}),
     "lmhead_bf16_m12": ("lmhead", "FULL_CANVAS", dict(C=12)),
     "lmhead_fp8_m12": ("lmhead_fp8", "FULL_CANVAS", dict(C=12)),
+    "lmhead_nvfp4_m256": ("lmhead_fp4", "FULL_CANVAS", {}),
+    "lmhead_nvfp4_m12": ("lmhead_fp4", "FULL_CANVAS", dict(C=12)),
     "selfcond_bf16_m256": ("selfcond", "FULL_CANVAS", {}),
     "selfcond_fp8_m256": ("selfcond_fp8", "FULL_CANVAS", {}),
     "mixed_decode8_prefill2": ("mixed", "LONG_CONTEXT", dict(B=10, C=2048, P=4096)),
@@ -510,10 +512,11 @@ def build_runner(kind, shape, device, concurrent=True):
     from structured_slot_reads_gb300.read import ReadStep, TwoStageRead
     if kind == "step":
         return build_step(shape, device, concurrent=concurrent)
-    if kind in ("lmhead", "lmhead_fp8"):
+    if kind in ("lmhead", "lmhead_fp8", "lmhead_fp4"):
         from structured_slot_reads_gb300.read import LmHead
         w = inputs.device_normal_bf16((shape.V, shape.D), shape.D ** -0.5, 1, device)
-        st = LmHead(shape, w, shape.B * shape.C, fp8=kind == "lmhead_fp8", device=device)
+        st = LmHead(shape, w, shape.B * shape.C, fp8=kind == "lmhead_fp8", device=device,
+                    fp4=kind == "lmhead_fp4")
         st.h.copy_(inputs.device_normal_bf16(st.h.shape, 1.0, 3, device))
         st.inv_t.copy_(1.0 / inputs.device_uniform(st.inv_t.shape, 0.5, 2.0, 4, device))
         torch.cuda.synchronize()
@@ -631,10 +634,10 @@ def workload_arm(args, rank, world, local):
     elif kind == "mixed":
         run = lambda i: st.run(step_idx=i)              # noqa: E731
         calls = ["dg_attn_mixed"]
-    elif kind in ("lmhead", "lmhead_fp8"):
+    elif kind in ("lmhead", "lmhead_fp8", "lmhead_fp4"):
         run = lambda i: st.run(step_idx=i)              # noqa: E731
         calls = ["dg_lmhead_logsoftmax_entropy", "dg_quantize_rows_e4m3",
-                 "dg_lmhead_logsoftmax_entropy_fp8"]
+                 "dg_lmhead_logsoftmax_entropy_fp8", "dg_lmhead_logsoftmax_entropy_nvfp4"]
     elif kind in ("selfcond", "selfcond_fp8"):
         run = lambda i: st.run(step_idx=i)              # noqa: E731
         calls = ["dg_selfcond_from_probs", "dg_quantize_rows_e4m3", "dg_selfcond_from_probs8"]
@@ -662,12 +665,15 @@ def workload_arm(args, rank, world, local):
         fl = (shape.B - 2) * attn_flops(dec) + 2 * prefill_flops(enc)
         by = (shape.B - 2) * attn_bytes(dec) + 2 * prefill_bytes(enc)
         work["dg_attn_mixed"] = (by, fl)
-    if kind in ("lmhead", "lmhead_fp8"):
+    if kind in ("lmhead", "lmhead_fp8", "lmhead_fp4"):
         Mr = shape.B * shape.C
         esz = 1 if kind == "lmhead_fp8" else 2
         lm = (V * D * esz + Mr * D * esz + V * 4 * (esz == 1) + Mr * 16, 2.0 * Mr * V * D)
         work["dg_lmhead_logsoftmax_entropy"] = lm
         work["dg_lmhead_logsoftmax_entropy_fp8"] = lm
+        # NVFP4 weights: half a byte per element plus one e4m3 scale per 16; bf16 rows
+        work["dg_lmhead_logsoftmax_entropy_nvfp4"] = (V * D // 2 + V * D // 16 + Mr * D * 2
+                                                      + Mr * 16, 2.0 * Mr * V * D)
         work["dg_quantize_rows_e4m3"] = (Mr * D * 3 + Mr * 4, 0.0)
     if kind in ("selfcond", "selfcond_fp8"):
         Mr = shape.B * shape.C
@@ -723,7 +729,7 @@ def workload_arm(args, rank, world, local):
         unit, value = "prompt tokens/s", steps_per_s * shape.B * shape.P
     elif kind == "mixed":
         unit, value = "attention launches/s", steps_per_s
-    elif kind in ("lmhead", "lmhead_fp8"):
+    elif kind in ("lmhead", "lmhead_fp8", "lmhead_fp4"):
         unit, value = "lm-head passes/s", steps_per_s
     elif kind in ("selfcond", "selfcond_fp8"):
         unit, value = "self-conditioning passes/s", steps_per_s
@@ -733,7 +739,8 @@ def workload_arm(args, rank, world, local):
         "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3" if kind.endswith("_fp8") else "bf16",
+        "dtype": ("e4m3" if kind.endswith("_fp8") else
+                  "nvfp4 weights x bf16 rows" if kind.endswith("_fp4") else "bf16"),
         "data": "synthetic",
         "config": {"workload": f"{args.workload}: kind {kind}, B={shape.B}, prompt "
                                f"{'U[512, %d] paged' % shape.P if kind == 'two_stage' else shape.P}"

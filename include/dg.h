@@ -277,6 +277,37 @@ int dg_selfcond_from_probs8(const dg_dims* dims, const uint8_t* p8, const float*
                             const float* e_scale, float* out, void* workspace,
                             size_t workspace_bytes, void* stream);
 
+/* ---- next: the lm-head pass against NVFP4 weights -------------------------
+ * tau-home.com, "DiffusionGemma like Jev" ("Running NVFP4 locally with a
+ * Jev-compatible System One endpoint") and agentlenshq.com, "4x faster via
+ * parallel diffusion" ("Architecture": NVFP4 kernels for Hopper and Blackwell)
+ * run the model on NVFP4 weights: e2m1 elements, one e4m3 scale per 16
+ * elements of a row, one fp32 scale per tensor.  dg_quantize_nvfp4 (a one-time
+ * preparation of W): g = amax|x| / (6 * 448) (1 for an all-zero tensor);
+ * per block of 16 of a row s = e4m3((amax_block / 6) / g) (round to nearest
+ * even, saturating); codes e2m1(x / (s * g)) (round to nearest, ties to the
+ * even mantissa, saturating at 6; 0 for a block whose scale is 0), fp32
+ * arithmetic throughout.  Layout, K-block-major (the layout the pass copies
+ * whole): codes [cols/64][rows][32] bytes (element 64 kb + j of row v is the
+ * low nibble of byte j / 2 for even j, the high nibble for odd j), scales
+ * [cols/64][rows][4] e4m3 bytes (byte q: elements 64 kb + 16 q ..), *g (device).
+ * cols must be a multiple of 64; x and codes 16-byte aligned. */
+int dg_quantize_nvfp4(const uint16_t* x, int rows, int cols, uint8_t* codes, uint8_t* scales,
+                      float* g, void* stream);
+
+/* dg_lmhead_logsoftmax_entropy against NVFP4 weights: the row statistics of
+ * softmax(z_i / T_i) with z_iv = (h_i . (e2m1 * s)_v) * g, the bf16 rows times
+ * the weights widened to bf16 on chip (exact: e2m1 times an e4m3 scale fits
+ * bf16), fp32 accumulation on the tensor cores.  Operands from
+ * dg_quantize_nvfp4(w, V, d_model, ..); outputs, workspace (DG_WS_LMHEAD) and
+ * errors as dg_lmhead_logsoftmax_entropy; d_model a multiple of 64 and V of 4
+ * (else DG_ERR_SHAPE); h, codes and scales 16-byte aligned. */
+int dg_lmhead_logsoftmax_entropy_nvfp4(const dg_dims* dims, const uint16_t* h, int M,
+                                       const uint8_t* codes, const uint8_t* scales,
+                                       const float* g, const float* inv_t, float* lse,
+                                       float* entropy, float* maxz, int32_t* argmax,
+                                       void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---- next: one wide read in place of the two-stage path -----------------
  * sotaaz.com, "The server accepts at most 26 alternatives per question": the
  * example server letters a question's alternatives A-Z, so 77 intents are read

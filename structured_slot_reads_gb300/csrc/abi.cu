@@ -645,6 +645,35 @@ int dg_lmhead_logsoftmax_entropy_fp8(const dg_dims* d, const uint8_t* h8, const 
                                              static_cast<cudaStream_t>(stream)));
 }
 
+int dg_quantize_nvfp4(const uint16_t* x, int rows, int cols, uint8_t* codes, uint8_t* scales,
+                      float* g, void* stream) {
+  if (rows < 0 || cols < 1) return DG_ERR_ARG;
+  if (cols % 64) return DG_ERR_SHAPE;
+  if (rows > 0 && (!x || !codes || !scales || !g)) return DG_ERR_ARG;
+  if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(scales, 4) || !aligned(g, 4))
+    return DG_ERR_ARG;
+  return launch_result(
+      dgi::quantize_nvfp4(x, rows, cols, codes, scales, g, static_cast<cudaStream_t>(stream)));
+}
+
+int dg_lmhead_logsoftmax_entropy_nvfp4(const dg_dims* d, const uint16_t* h, int M,
+                                       const uint8_t* codes, const uint8_t* scales,
+                                       const float* g, const float* inv_t, float* lse,
+                                       float* entropy, float* maxz, int32_t* argmax,
+                                       void* workspace, size_t workspace_bytes, void* stream) {
+  if (!d || M < 1) return DG_ERR_ARG;
+  if (!dims_lm(d) || d->d_model % 64 || d->V % 4) return DG_ERR_SHAPE;
+  if (!h || !codes || !scales || !g || !inv_t || !lse || !entropy || !maxz || !argmax)
+    return DG_ERR_ARG;
+  if (!aligned(h, 16) || !aligned(codes, 16) || !aligned(scales, 16) || !aligned(g, 4))
+    return DG_ERR_ARG;
+  const size_t need = dg_workspace_bytes(d, DG_WS_LMHEAD, M);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DG_ERR_WORKSPACE;
+  return launch_result(dgi::lmhead_stats_nvfp4(h, M, codes, scales, g, d->V, d->d_model, inv_t,
+                                               dgi::RowStats{lse, entropy, maxz, argmax},
+                                               workspace, static_cast<cudaStream_t>(stream)));
+}
+
 int dg_ask_if_select(const int32_t* chosen1, int S1, const int32_t* cond_slot,
                      const int32_t* cond_value, const int32_t* q_owner,
                      const int32_t* q_label_ids, const int32_t* q_n_labels, int Q, int S2,

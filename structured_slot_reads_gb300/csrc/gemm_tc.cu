@@ -22,6 +22,8 @@
 // thread.  B is K-major (W) or MN-major (E read as [V, d_model]).
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -42,6 +44,7 @@ constexpr int EPI_ACCUM = 2;
 constexpr int EPI_ACCUM_MN = 3;  // as EPI_ACCUM with B given N-contiguous ([K, N] row-major)
 constexpr int EPI_STATS8 = 4;    // as EPI_STATS with e4m3 operands and per-row scales
 constexpr int EPI_ACCUM8 = 5;    // as EPI_ACCUM with e4m3 operands (both K-major) and scales
+constexpr int EPI_STATS4 = 6;    // as EPI_STATS with B = NVFP4 weights widened to bf16 on chip
 constexpr int RING_BUDGET = 232448 - 1024 - 512;  // operand rings (227 KB - alignment - barriers)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
@@ -62,18 +65,21 @@ struct GemmParams {
   const float* lse;
   const float* row_scale;  // STATS8 / ACCUM8: scale of each A row
   const float* col_scale;  // STATS8 / ACCUM8: scale of each B row (an output column)
+  const uint8_t* codes4;   // STATS4: e2m1 codes [K/64][N][32 bytes]
+  const uint8_t* scales4;  // STATS4: e4m3 block scales [K/64][N][4]
+  const float* gscale;     // STATS4: the weights' tensor scale
   float* part;            // STATS: 5 x [cpg][M]; ACCUM: [k_split][M][N]
   __nv_bfloat16* probs;   // PROBS: [M][ldp]
   long long ldp;
   int* status;
 };
 
-template <int MT, int BN>
+template <int MT, int BN, int EXTRA = 0>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;   // one 128-row A tile of a K block
   static constexpr int A_STAGE = MT * A_BYTES;
   static constexpr int B_STAGE = BN * BK * 2;
-  static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+  static constexpr int STAGE_BYTES = A_STAGE + B_STAGE + EXTRA;  // EXTRA: packed B staging
   static constexpr int NS_FIT = RING_BUDGET / STAGE_BYTES;
   static constexpr int NSTAGE = NS_FIT > 8 ? 8 : NS_FIT;
   static constexpr int ACC_COLS = MT * BN;
@@ -96,18 +102,25 @@ struct Cfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
+// NVFP4 B staging of one K block: BN rows x (32 code bytes + 4 scale bytes)
+constexpr int f4_extra(int bn) { return bn * 36; }
+constexpr int F4_CONV_WARPS = 4;   // warps widening the packed B tile to bf16
+
 template <int MT, int BN, int EPI>
-__global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
+__global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32 * F4_CONV_WARPS : 0), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, GemmParams p) {
-  using CF = Cfg<MT, BN>;
+  constexpr bool F4 = EPI == EPI_STATS4;
+  using CF = Cfg<MT, BN, F4 ? f4_extra(BN) : 0>;
   constexpr int NSTAGE = CF::NSTAGE;
   constexpr int PRODUCER_WARP = CF::EPI_WARPS;
   constexpr int MMA_WARP = CF::EPI_WARPS + 1;
+  constexpr int CONV0 = CF::EPI_WARPS + 2;   // STATS4: first converter warp
   constexpr bool B_MN = EPI == EPI_ACCUM_MN;
   constexpr bool ACCUM = EPI == EPI_ACCUM || B_MN || EPI == EPI_ACCUM8;
   constexpr bool F8 = EPI == EPI_STATS8 || EPI == EPI_ACCUM8;
-  constexpr bool STATS = EPI == EPI_STATS || EPI == EPI_STATS8;
+  constexpr bool STATS = EPI == EPI_STATS || EPI == EPI_STATS8 || F4;
+  __shared__ uint32_t lut4[F4 ? 256 : 1];     // STATS4: code byte -> two bf16 values
   // a stage holds 128-byte operand rows: 64 bf16 or 128 e4m3 values of K
   constexpr int KB = F8 ? 128 : BK;
   constexpr uint32_t IDESC_F8 = idesc_e4m3_f32(BM, BN);
@@ -121,7 +134,8 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
   uint64_t* tfull_bar = empty_bar + NSTAGE;
   uint64_t* tempty_bar = tfull_bar + CF::ACC_STAGES;
   uint64_t* drain_bar = tempty_bar + CF::ACC_STAGES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  uint64_t* bready_bar = drain_bar + 1;   // STATS4: [NSTAGE] the widened B tile written
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bready_bar + (F4 ? NSTAGE : 0));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -131,6 +145,7 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
     for (int i = 0; i < NSTAGE; ++i) {
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], 1);
+      if (F4) mbar_init(&bready_bar[i], F4_CONV_WARPS);
     }
     for (int a = 0; a < CF::ACC_STAGES; ++a) {
       mbar_init(&tfull_bar[a], 1);
@@ -146,7 +161,20 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
   }
   if (warp == PRODUCER_WARP && lane == 0) {
     prefetch_tmap(&tmA);
-    prefetch_tmap(&tmB);
+    if (!F4) prefetch_tmap(&tmB);
+  }
+  if (F4 && warp >= CONV0) {
+    // e2m1 pairs of a code byte (the even element in the low nibble) as bf16x2
+    const int i = threadIdx.x - CONV0 * 32;
+    for (int b = i; b < 256; b += 32 * F4_CONV_WARPS) {
+      auto e2m1 = [](int c) -> float {
+        const float mag = ((c >> 1) & 3) == 0 ? 0.5f * (c & 1)
+                                              : (1.f + 0.5f * (c & 1)) * (float)(1 << (((c >> 1) & 3) - 1));
+        return (c & 8) ? -mag : mag;
+      };
+      const __nv_bfloat162 v = __floats2bfloat162_rn(e2m1(b & 15), e2m1(b >> 4));
+      lut4[b] = *reinterpret_cast<const uint32_t*>(&v);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -193,14 +221,26 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full_bar[stage], CF::STAGE_BYTES);
           uint8_t* s_a = stages + stage * CF::STAGE_BYTES;
           uint8_t* s_b = s_a + CF::A_STAGE;
+          if (F4) {
+            // the packed codes and scales of rows [t BN, t BN + rows) of K block kb,
+            // contiguous in the K-block-major layout; the converter warps widen them
+            const int rows = min(BN, p.N - t * BN);
+            mbar_arrive_expect_tx(&full_bar[stage], CF::A_STAGE + rows * 36);
+            const long long r0 = (long long)kb * p.N + (long long)t * BN;
+            bulk_load(s_b + CF::B_STAGE, p.codes4 + r0 * 32, rows * 32, &full_bar[stage]);
+            bulk_load(s_b + CF::B_STAGE + BN * 32, p.scales4 + r0 * 4, rows * 4,
+                      &full_bar[stage]);
+          } else {
+            mbar_arrive_expect_tx(&full_bar[stage], CF::STAGE_BYTES);
+          }
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt)
             tma_load_2d_hint(s_a + mt * CF::A_BYTES, &tmA, &full_bar[stage], kb * KB,
                              m_base + mt * BM, pol_a);
-          if (B_MN) {
+          if (F4) {
+          } else if (B_MN) {
             // B [K, N] with N contiguous: BN/64 boxes of 64 N-columns x 64 K-rows
 #pragma unroll
             for (int g = 0; g < BN / 64; ++g)
@@ -232,7 +272,9 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
         tc_fence_after();
         const uint32_t d_base = tmem_base + acc * CF::ACC_COLS;
         for (int kb = kb_begin; kb < kb_end; ++kb) {
-          if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.status)) {
+          // STATS4: the widened B tile (the converters saw the stage full first)
+          if (!mbar_wait(F4 ? &bready_bar[stage] : &full_bar[stage], phase, abort_flag,
+                         p.status)) {
             ok = false;
             break;
           }
@@ -274,6 +316,66 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
       tc_commit(drain_bar);
       mbar_wait_drain(drain_bar, 0);
     }
+  } else if (F4 && warp >= CONV0) {
+    // ---- STATS4 converter warps: each K block's packed B rows -> bf16 tile ----
+    // (128-byte swizzled rows of 64 values, the layout TMA gives the other passes)
+    const int ci = threadIdx.x - CONV0 * 32;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = has_work;
+    for (int t = t_begin; t < t_end && ok; ++t) {
+      const int rows = min(BN, p.N - t * BN);
+      for (int kb = kb_begin; kb < kb_end; ++kb) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&full_bar[stage], phase, abort_flag, p.status));
+        if (!ok) break;
+        uint8_t* s_b = stages + stage * CF::STAGE_BYTES + CF::A_STAGE;
+        const uint8_t* s_c = s_b + CF::B_STAGE;
+        const uint8_t* s_s = s_c + BN * 32;
+        for (int r = ci; r < BN; r += 32 * F4_CONV_WARPS) {
+          uint8_t* dst = s_b + r * 128;
+          if (r >= rows) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(dst + ((c ^ (r & 7)) * 16)) = make_uint4(0, 0, 0, 0);
+            continue;
+          }
+          const uint4 c0 = *reinterpret_cast<const uint4*>(s_c + r * 32);
+          const uint4 c1 = *reinterpret_cast<const uint4*>(s_c + r * 32 + 16);
+          const uint32_t sw = *reinterpret_cast<const uint32_t*>(s_s + r * 4);
+          const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const __half_raw hr =
+                __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)((sw >> (8 * q)) & 0xFF), __NV_E4M3);
+            const float sv = __half2float(__half(hr));
+            const __nv_bfloat162 s2 = __floats2bfloat162_rn(sv, sv);
+            // 16 elements of scale q: code words 2q, 2q+1 -> 16-byte chunks 2q, 2q+1
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t word = cw[2 * q + h];
+              uint32_t o[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint32_t pr2 = lut4[(word >> (8 * k)) & 0xFF];
+                const __nv_bfloat162 v =
+                    __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&pr2), s2);
+                o[k] = *reinterpret_cast<const uint32_t*>(&v);
+              }
+              const int c = 2 * q + h;
+              *reinterpret_cast<uint4*>(dst + ((c ^ (r & 7)) * 16)) =
+                  make_uint4(o[0], o[1], o[2], o[3]);
+            }
+          }
+        }
+        fence_proxy_async_smem();   // generic writes -> the MMA's operand reads
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bready_bar[stage]);
+        if (++stage == NSTAGE) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
   } else {
     // ---- epilogue warps ---------------------------------------------------
     const int mt = warp >> 2;
@@ -283,6 +385,7 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
     float scale = 0.f, lse2 = 0.f, rs = 1.f;
     if (!ACCUM && row_ok) scale = __ldg(p.inv_t + row) * LOG2E;
     if (F8 && row_ok) rs = __ldg(p.row_scale + row);
+    const float gs = F4 ? __ldg(p.gscale) : 1.f;
     if (EPI == EPI_PROBS && row_ok) lse2 = __ldg(p.lse + row) * LOG2E;
     float m_run = -INFINITY, s_run = 0.f, t_run = 0.f, best = -INFINITY;
     int best_idx = 0x7fffffff;
@@ -318,6 +421,10 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS, 1)
             r[j + 2] = __float_as_uint(__uint_as_float(r[j + 2]) * rs * cs.z);
             r[j + 3] = __float_as_uint(__uint_as_float(r[j + 3]) * rs * cs.w);
           }
+        }
+        if (F4) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * gs);
         }
         if (STATS) {
           if (n0 + 32 <= p.N) {
@@ -595,6 +702,52 @@ cudaError_t run_stats_fp8(const uint8_t* h8, const float* h_scale, int M, const 
   return cudaGetLastError();
 }
 
+// The statistics pass against NVFP4 weights: bf16 rows (TMA) times the codes
+// and block scales (bulk copies) widened to bf16 on chip; the tensor scale is
+// applied to the accumulators.
+template <int MT>
+cudaError_t launch_stats4(const CUtensorMap& ta, const GemmParams& p, int grid, cudaStream_t st) {
+  using CF = Cfg<MT, STATS_BN, f4_extra(STATS_BN)>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<MT, STATS_BN, EPI_STATS4>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         CF::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  gemm_tc_kernel<MT, STATS_BN, EPI_STATS4>
+      <<<grid, CF::THREADS + 32 * F4_CONV_WARPS, CF::SMEM_BYTES, st>>>(ta, ta, p);
+  return cudaGetLastError();
+}
+
+cudaError_t run_stats_nvfp4(const uint16_t* h, int M, const uint8_t* codes, const uint8_t* scales,
+                            const float* g, int V, int D, const float* inv_t, dgi::RowStats out,
+                            float* part, cudaStream_t st) {
+  CUtensorMap ta;
+  if (!dgi::make_tmap_bf16_2d(&ta, h, D, M, (uint64_t)D * 2, BK, BM)) return cudaErrorInvalidValue;
+  const int mt = stats_mt(M);
+  const int groups = (M + mt * BM - 1) / (mt * BM);
+  GemmParams p{};
+  p.M = M;
+  p.N = V;
+  p.K = D;
+  p.cpg = stats_cpg(M, V);
+  p.n_tiles = (V + STATS_BN - 1) / STATS_BN;
+  p.inv_t = inv_t;
+  p.codes4 = codes;
+  p.scales4 = scales;
+  p.gscale = g;
+  p.part = part;
+  p.status = dgi::status_ptr();
+  cudaError_t e = (mt == 1) ? launch_stats4<1>(ta, p, groups * p.cpg, st)
+                            : launch_stats4<2>(ta, p, groups * p.cpg, st);
+  if (e != cudaSuccess) return e;
+  stats_finalize_kernel<<<(M + 7) / 8, 256, 0, st>>>(part, p.cpg, M, inv_t, out.lse,
+                                                     out.entropy, out.maxz, out.argmax);
+  return cudaGetLastError();
+}
+
 constexpr int ACC_BN = 256;
 
 // Split of the vocabulary (the K of P . E) over CTAs: every split non-empty.
@@ -651,6 +804,12 @@ cudaError_t lmhead_stats_fp8(const uint8_t* h8, const float* h_scale, int M, con
                              const float* w_scale, int V, int D, const float* inv_t, RowStats out,
                              void* ws, cudaStream_t st) {
   return run_stats_fp8(h8, h_scale, M, w8, w_scale, V, D, inv_t, out, static_cast<float*>(ws), st);
+}
+
+cudaError_t lmhead_stats_nvfp4(const uint16_t* h, int M, const uint8_t* codes,
+                               const uint8_t* scales, const float* g, int V, int D,
+                               const float* inv_t, RowStats out, void* ws, cudaStream_t st) {
+  return run_stats_nvfp4(h, M, codes, scales, g, V, D, inv_t, out, static_cast<float*>(ws), st);
 }
 
 size_t selfcond_ws_bytes(int M, int V, int D) {

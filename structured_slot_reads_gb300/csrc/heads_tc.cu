@@ -10,17 +10,16 @@
 // rescaling and p_iv = P~_iv / S_i exactly; the P.E GEMM applies 1/S_i in its
 // reduction.
 //
-// The pass is exact for any input whose scaled logits stay below 2^24 log2
-// units (past that a raise no longer counts whole units in a float).  An
-// epilogue thread owns one row of
-// its CTA's vocabulary range; when a chunk's largest exponent passes r + RAISE
-// it raises its own reference by a whole number k of log2 units (so 2^-k is
-// exact), scales its running sums and the probabilities it already wrote by
-// 2^-k, and goes on.  Each CTA reports the reference of its sums and of its
-// probabilities; the finalize takes the largest, merges the sums against it and
-// brings the probabilities of any CTA range with a lower reference to it (again
-// by a power of two).  Without a raise (the usual case) every factor is 1 and
-// nothing is rewritten.
+// The pass is exact for any input whose scaled logits stay below 2^13 log2
+// units.  An epilogue thread owns one row of its CTA's vocabulary range and
+// sums each 32-entry chunk against its reference; if the chunk's largest
+// exponent passes RAISE it raises the reference by a whole number k of log2
+// units (2^-k is then exact), scales what it summed and wrote before the chunk
+// by 2^-k and sums the chunk again.  Each CTA reports the reference of its sums
+// and probabilities; the finalize takes the largest, merges the sums against it
+// and brings the probabilities of any CTA range with a lower reference to it
+// (again by a power of two).  Without a raise (the usual case) every factor is
+// 1 and nothing is rewritten.
 //
 // For the slot-read draw rows (sotaaz.com "The server accepts at most 26
 // alternatives per question": noise reads of an answer slot) the same W tiles
@@ -52,6 +51,7 @@ constexpr int BK = 64;
 constexpr int REF_N = 8;              // vocabulary entries behind the reference
 constexpr float REF_HEADROOM = 24.f;  // log2 units added to the reference maximum
 constexpr float RAISE = 64.f;         // exponent (log2 units) past which a reference is raised
+constexpr float V_CLAMP = 100.f;      // exponent guard while a chunk is first summed
 constexpr int DRAW_N = 16;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
@@ -137,7 +137,8 @@ __global__ void __launch_bounds__(REF_N * REF_KSPLIT * 32)
       for (int k = 0; k < REF_KSPLIT; ++k) t += part[k][e];
       m = fmaxf(m, t);
     }
-    ref[row] = m * inv_t[row] * LOG2E + REF_HEADROOM;
+    // on a grid of 1/256 log2 units, so that adding whole raises keeps it exact
+    ref[row] = rintf((m * inv_t[row] * LOG2E + REF_HEADROOM) * 256.f) * (1.f / 256.f);
   }
 }
 
@@ -177,7 +178,7 @@ __device__ __forceinline__ float pow2_neg(int k) {
 
 // Multiply the bf16 probabilities [v0, v1) of one row by f (a power of two, so
 // exact unless a value underflows).  v0, v1 are multiples of 8; rare path.
-__device__ __noinline__ void rescale_probs(__nv_bfloat16* row, int v0, int v1, float f) {
+__device__ __forceinline__ void rescale_probs(__nv_bfloat16* row, int v0, int v1, float f) {
   for (int v = v0; v < v1; v += 8) {
     uint4 u = *reinterpret_cast<const uint4*>(row + v);
     __nv_bfloat162* b = reinterpret_cast<__nv_bfloat162*>(&u);
@@ -351,7 +352,7 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
     const float scale = row_ok ? __ldg(p.inv_t + row) * LOG2E : 0.f;
     const float r_ref = row_ok ? __ldg(p.ref + row) : 0.f;
     float s_run = 0.f, t_run = 0.f, best = -INFINITY;
-    int kt = 0;  // whole log2 units this thread's reference sits above r_ref
+    float r_cur = r_ref;  // reference of the sums and probabilities: r_ref + whole raises
     int best_idx = 0x7fffffff;
     // draw-row running statistics: lane = vocabulary row of a half tile
     float dm[DRAW_N], ds[DRAW_N], dscale[DRAW_N];
@@ -378,38 +379,46 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
         if (!row_ok || n0 >= p.V) continue;
         float e[32];
         float cmax = -INFINITY;
-        const bool full = n0 + 32 <= p.V;
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (full || n0 + j < p.V) cmax = fmaxf(cmax, __uint_as_float(r[j]));
-        const float xmax = fmaf(cmax, scale, -r_ref) - (float)kt;
-        if (xmax > RAISE) {
-          // a logit far above this row's reference: raise it by k whole log2
-          // units and scale what was summed and written so far by 2^-k (exact)
-          const int k = (int)fminf(ceilf(xmax), 16777216.f);
-          const float f = pow2_neg(k);
-          s_run *= f;
-          t_run *= f;
-          kt += k;
-          if (p.probs) rescale_probs(p.probs + (long long)row * p.ldp, t_begin * BN, n0, f);
-        }
-        if (kt == 0) {
+        const float s_prev = s_run, t_prev = t_run;
+        if (n0 + 32 <= p.V) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const float a = __uint_as_float(r[j]);
-            e[j] = (full || n0 + j < p.V) ? ex2(fmaf(a, scale, -r_ref)) : 0.f;
+            cmax = fmaxf(cmax, a);
+            e[j] = ex2(fminf(fmaf(a, scale, -r_cur), V_CLAMP));
             s_run += e[j];
             t_run = fmaf(e[j], a, t_run);
           }
         } else {
-          const float ktf = (float)kt;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const float a = __uint_as_float(r[j]);
-            e[j] = (full || n0 + j < p.V) ? ex2(fmaf(a, scale, -r_ref) - ktf) : 0.f;
+            const bool ok = n0 + j < p.V;
+            if (ok) cmax = fmaxf(cmax, a);
+            e[j] = ok ? ex2(fminf(fmaf(a, scale, -r_cur), V_CLAMP)) : 0.f;
             s_run += e[j];
             t_run = fmaf(e[j], a, t_run);
           }
+        }
+        const float xmax = fmaf(cmax, scale, -r_cur);
+        if (xmax > RAISE) {
+          // rare: a logit far above this row's reference.  Raise the reference by
+          // k whole log2 units, scale what was summed and written before this
+          // chunk by 2^-k (exact) and sum the chunk again against the new one.
+          const int k = (int)fminf(ceilf(xmax), 8192.f);
+          const float f = pow2_neg(k);
+          r_cur += (float)k;
+          float s_c = 0.f, t_c = 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float a = __uint_as_float(r[j]);
+            e[j] = (n0 + j < p.V) ? ex2(fmaf(a, scale, -r_cur)) : 0.f;
+            s_c += e[j];
+            t_c = fmaf(e[j], a, t_c);
+          }
+          s_run = fmaf(s_prev, f, s_c);
+          t_run = fmaf(t_prev, f, t_c);
+          if (p.probs) rescale_probs(p.probs + (long long)row * p.ldp, t_begin * BN, n0, f);
         }
         if (cmax > best) {  // columns ascend, so the first occurrence is the lowest id
           int first = 0x7fffffff;
@@ -486,7 +495,7 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
       p.part[o + plane] = t_run;
       p.part[o + 2 * plane] = best;
       reinterpret_cast<int*>(p.part)[o + 3 * plane] = best_idx;
-      p.part[o + 4 * plane] = (float)kt;
+      p.part[o + 4 * plane] = r_cur;
     }
     if (DRAWS && draws_here) {
       // merge the draw statistics over the lanes, then over the epilogue warps
@@ -533,28 +542,29 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
 }
 
 // Canvas rows, one warp per row.  Each CTA's sums and probabilities are
-// relative to ref[row] + k_g (k_g whole log2 units, 0 unless that CTA raised
-// its reference); they are brought to the largest k and added (every factor is
+// relative to its reference ref[row] + k_g (k_g whole log2 units, 0 unless that
+// CTA raised it; the references lie on a 1/256 grid, so the differences are
+// exact); they are brought to the largest reference and added (every factor is
 // exactly 1 without a raise), with the best logit and its lowest index over the
-// CTAs.  The probabilities of a CTA range with a smaller k are scaled to the
-// largest (a power of two, exact), so that p = P~ * prob_scale over the row.
+// CTAs.  The probabilities of a CTA range with a lower reference are scaled to
+// the largest (a power of two, exact), so that p = P~ * prob_scale over the row.
 __device__ void finalize_row(int row, int lane, const float* part, int cpg, int M,
-                             const float* inv_t, const float* ref, float* lse, float* entropy,
-                             float* maxz, int32_t* argmax, float* prob_scale,
-                             __nv_bfloat16* probs, long long ldp, int n_tiles, int bn, int V) {
+                             const float* inv_t, float* lse, float* entropy, float* maxz,
+                             int32_t* argmax, float* prob_scale, __nv_bfloat16* probs,
+                             long long ldp, int n_tiles, int bn, int V) {
   const long long plane = (long long)cpg * M;
   const float* pm = part + (long long)row * cpg;
-  int kmax = 0;
-  for (int g = lane; g < cpg; g += 32) kmax = max(kmax, (int)pm[g + 4 * plane]);
+  float rmax = -INFINITY;
+  for (int g = lane; g < cpg; g += 32) rmax = fmaxf(rmax, pm[g + 4 * plane]);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  for (int o = 16; o > 0; o >>= 1) rmax = fmaxf(rmax, __shfl_xor_sync(0xffffffffu, rmax, o));
   float s = 0.f, t = 0.f, best = -INFINITY;
   int idx = 0x7fffffff;
   bool lower = false;
   for (int g = lane; g < cpg; g += 32) {
-    const int kg = (int)pm[g + 4 * plane];
-    const float f = pow2_neg(kmax - kg);
-    lower |= kg < kmax;
+    const float rg = pm[g + 4 * plane];
+    const float f = pow2_neg((int)(rmax - rg));
+    lower |= rg < rmax;
     s += pm[g] * f;
     t += pm[g + plane] * f;
     const float bg = pm[g + 2 * plane];
@@ -577,7 +587,7 @@ __device__ void finalize_row(int row, int lane, const float* part, int cpg, int 
   }
   if (lane == 0) {
     const float it = inv_t[row];
-    const float l = (ref[row] + (float)kmax + log2f(s)) * LN2;
+    const float l = (rmax + log2f(s)) * LN2;
     lse[row] = l;
     entropy[row] = l - it * (t / s);
     maxz[row] = best * it;
@@ -588,9 +598,9 @@ __device__ void finalize_row(int row, int lane, const float* part, int cpg, int 
   if (probs && __any_sync(0xffffffffu, lower)) {
     __nv_bfloat16* pr = probs + (long long)row * ldp;
     for (int g = 0; g < cpg; ++g) {
-      const int kg = (int)pm[g + 4 * plane];
-      if (kg >= kmax) continue;
-      const float f = pow2_neg(kmax - kg);
+      const float rg = pm[g + 4 * plane];
+      if (!(rg < rmax)) continue;
+      const float f = pow2_neg((int)(rmax - rg));
       const int v0 = (int)((long long)g * n_tiles / cpg) * bn;
       const int v1 = min(V, (int)((long long)(g + 1) * n_tiles / cpg) * bn);
       for (int v = v0 + 2 * lane; v < v1; v += 64) {
@@ -626,7 +636,7 @@ __device__ void finalize_draw(int j, int lane, const float* part_draw, int cpg, 
 // Both finalisations in one launch: the first row_blocks blocks take the canvas
 // rows, the rest the draw rows (8 rows a block).
 __global__ void heads_finalize_kernel(const float* part, int cpg, int M, const float* inv_t,
-                                      const float* ref, float* lse, float* entropy, float* maxz,
+                                      float* lse, float* entropy, float* maxz,
                                       int32_t* argmax, float* prob_scale, __nv_bfloat16* probs,
                                       long long ldp,
                                       int n_tiles, int bn, int V, const float* part_draw,
@@ -636,7 +646,7 @@ __global__ void heads_finalize_kernel(const float* part, int cpg, int M, const f
   if ((int)blockIdx.x < row_blocks) {
     const int row = blockIdx.x * (blockDim.x >> 5) + w;
     if (row < M)
-      finalize_row(row, lane, part, cpg, M, inv_t, ref, lse, entropy, maxz, argmax, prob_scale,
+      finalize_row(row, lane, part, cpg, M, inv_t, lse, entropy, maxz, argmax, prob_scale,
                    probs, ldp, n_tiles, bn, V);
   } else {
     const int j = (blockIdx.x - row_blocks) * (blockDim.x >> 5) + w;
@@ -733,7 +743,7 @@ cudaError_t denoise_heads(const uint16_t* h, int M, const uint16_t* draw_rows, i
   if (e != cudaSuccess) return e;
   const int row_blocks = (M + 7) / 8, draw_blocks = (n_draw + 7) / 8;
   heads_finalize_kernel<<<row_blocks + draw_blocks, 256, 0, st>>>(
-      p.part, p.cpg, M, inv_t, ref, out.lse, out.entropy, out.maxz, out.argmax, prob_scale, p.probs,
+      p.part, p.cpg, M, inv_t, out.lse, out.entropy, out.maxz, out.argmax, prob_scale, p.probs,
       p.ldp, p.n_tiles, bn, V, p.part_draw, n_draw, lse_draw, row_blocks);
   return cudaGetLastError();
 }

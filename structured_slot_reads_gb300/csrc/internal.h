@@ -60,6 +60,14 @@ cudaError_t quantize_rows_e4m3(const uint16_t* x, int rows, int cols, uint8_t* q
                                cudaStream_t st);
 cudaError_t quantize_cols_e4m3(const uint16_t* x, int rows, int cols, uint8_t* qt, float* scale,
                                cudaStream_t st);
+// NVFP4 weights, K-block-major: codes [cols/64][rows][32] bytes, scales
+// [cols/64][rows][4] e4m3, *g the fp32 tensor scale (cols a multiple of 64).
+cudaError_t quantize_nvfp4(const uint16_t* x, int rows, int cols, uint8_t* codes,
+                           uint8_t* scales, float* g, cudaStream_t st);
+// lm-head statistics of bf16 rows against NVFP4 weights: z = (h . (e2m1 * s)) * g / T.
+cudaError_t lmhead_stats_nvfp4(const uint16_t* h, int M, const uint8_t* codes,
+                               const uint8_t* scales, const float* g, int V, int D,
+                               const float* inv_t, RowStats out, void* ws, cudaStream_t st);
 size_t probs_embed8_ws_bytes(int M, int V, int D);
 cudaError_t probs_embed8(const uint8_t* p8, const float* p_scale, const float* row_scale, int M,
                          const uint8_t* e8t, const float* e_scale, int V, int D, float* out,

@@ -8,8 +8,11 @@
 // vocabulary) and stored transposed, [d_model, V], so that both operands of
 // that GEMM have the vocabulary contiguous.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
+
+#include <algorithm>
 
 #include "internal.h"
 
@@ -177,9 +180,136 @@ __global__ void amax_to_scale_kernel(float* scale_io, int cols) {
     scale_io[c] = col_scale_of(reinterpret_cast<const unsigned int*>(scale_io)[c]);
 }
 
+// ---------------------------------------------------------------------------
+// NVFP4 weights (e2m1 elements, one e4m3 scale per 16 elements of a row, one
+// fp32 scale per tensor).  Tensor scale g = amax|x| / (6 * 448) (1 for an
+// all-zero tensor); block scale s = e4m3((amax_block / 6) / g); element code
+// e2m1(x / (s * g)), rounded to nearest with ties to the even mantissa and
+// saturated at 6.  Stored K-block-major, the layout the 4-bit lm-head pass
+// copies: codes [cols/64][rows][32] bytes (element 64 kb + j of row v in byte
+// j / 2, the even element in the low nibble), scales [cols/64][rows][4] bytes.
+// ---------------------------------------------------------------------------
+__global__ void tensor_amax_kernel(const uint4* x, long long n8, unsigned int* amax_bits) {
+  float m = 0.f;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+       i += (long long)gridDim.x * blockDim.x) {
+    const uint4 u = x[i];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+      m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ float wmax[8];
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float a = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) a = fmaxf(a, wmax[w]);
+    atomicMax(amax_bits, __float_as_uint(a));
+  }
+}
+
+__device__ __forceinline__ float nvfp4_tensor_scale(unsigned int amax_bits) {
+  const float a = __uint_as_float(amax_bits);
+  return a > 0.f ? a / 2688.f : 1.f;
+}
+
+// e2m1 code of y: nearest of 0, 0.5, 1, 1.5, 2, 3, 4, 6 by magnitude, a tie going to
+// the value whose mantissa bit is 0, saturating at 6; the sign bit for a nonzero code
+__device__ __forceinline__ uint32_t e2m1_code(float y) {
+  const float a = fabsf(y);
+  const uint32_t m = a <= 0.25f  ? 0u
+                     : a < 0.75f ? 1u
+                     : a <= 1.25f ? 2u
+                     : a < 1.75f  ? 3u
+                     : a <= 2.5f  ? 4u
+                     : a < 3.5f   ? 5u
+                     : a <= 5.f   ? 6u
+                                  : 7u;
+  return m | ((m != 0u && signbit(y)) ? 8u : 0u);
+}
+
+// One thread per (K block of 64, row): consecutive threads take consecutive rows,
+// so the code and scale writes of a warp are contiguous.
+__global__ void quantize_nvfp4_kernel(const __nv_bfloat16* x, int rows, int cols,
+                                      const unsigned int* amax_bits, uint8_t* codes,
+                                      uint8_t* scales) {
+  const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int nkb = cols / 64;
+  if (t >= (long long)rows * nkb) return;
+  const int kb = (int)(t / rows);
+  const int v = (int)(t % rows);
+  const float g = nvfp4_tensor_scale(*amax_bits);
+  const uint4* src = reinterpret_cast<const uint4*>(x + (long long)v * cols + kb * 64);
+  uint4* cdst = reinterpret_cast<uint4*>(codes + ((long long)kb * rows + v) * 32);
+  uint32_t sc4 = 0;
+  uint32_t cw[8];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float xv[16];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 u = src[2 * q + h];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+        xv[8 * h + 2 * k] = f.x;
+        xv[8 * h + 2 * k + 1] = f.y;
+      }
+    }
+    float bm = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) bm = fmaxf(bm, fabsf(xv[j]));
+    const __nv_fp8_storage_t sb = __nv_cvt_float_to_fp8((bm / 6.f) / g, __NV_SATFINITE, __NV_E4M3);
+    const __half_raw hr = __nv_cvt_fp8_to_halfraw(sb, __NV_E4M3);
+    const float den = __half2float(__half(hr)) * g;
+    sc4 |= (uint32_t)sb << (8 * q);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float y = xv[8 * i + j];
+        const uint32_t c = den > 0.f ? e2m1_code(y / den) : 0u;
+        word |= c << (4 * j);
+      }
+      cw[2 * q + i] = word;
+    }
+  }
+  cdst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+  cdst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+  *reinterpret_cast<uint32_t*>(scales + ((long long)kb * rows + v) * 4) = sc4;
+}
+
+__global__ void nvfp4_scale_kernel(float* g_io) {
+  g_io[0] = nvfp4_tensor_scale(reinterpret_cast<const unsigned int*>(g_io)[0]);
+}
+
 }  // namespace
 
 namespace dgi {
+
+cudaError_t quantize_nvfp4(const uint16_t* x, int rows, int cols, uint8_t* codes,
+                           uint8_t* scales, float* g, cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  // g holds the tensor maximum (as float bits) until the last kernel
+  unsigned int* amax = reinterpret_cast<unsigned int*>(g);
+  cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(unsigned int), st);
+  if (e != cudaSuccess) return e;
+  const long long n8 = (long long)rows * cols / 8;
+  tensor_amax_kernel<<<(int)std::min<long long>((n8 + 255) / 256, 4096), 256, 0, st>>>(
+      reinterpret_cast<const uint4*>(x), n8, amax);
+  const long long items = (long long)rows * (cols / 64);
+  quantize_nvfp4_kernel<<<(int)((items + 127) / 128), 128, 0, st>>>(
+      reinterpret_cast<const __nv_bfloat16*>(x), rows, cols, amax, codes, scales);
+  nvfp4_scale_kernel<<<1, 1, 0, st>>>(g);
+  return cudaGetLastError();
+}
 
 cudaError_t quantize_cols_e4m3(const uint16_t* x, int rows, int cols, uint8_t* qt, float* scale,
                                cudaStream_t st) {

@@ -294,55 +294,121 @@ __global__ void ask_if_kernel(const int32_t* chosen1, int S1, const int32_t* con
 
 // ---------------------------------------------------------------------------
 // a4: one CTA per request, one thread per canvas position (C <= 1024).  The
-// rank of each candidate under (entropy, position) gives its place in the
-// confidence order; an ordered scan of the sorted entropies finds the cut.
+// candidates are put in confidence order by a stable block radix sort of
+// (entropy, position): four passes over 8-bit digits of the entropy's
+// order-preserving bit pattern, closed positions keyed last; within a pass a
+// warp ranks equal digits with __match_any_sync and the per-warp digit counts
+// are scanned digit-major, warp-minor, which keeps equal keys in position
+// order.  A block scan of the sorted entropies then finds the cut.
 // ---------------------------------------------------------------------------
-__global__ void commit_kernel(int C, const float* entropy, const int32_t* argmax,
-                              const uint8_t* cand, const float* gamma, uint8_t* committed_state,
-                              int32_t* token_state, uint8_t* commit_out, int32_t* tokens,
-                              int32_t* n_commit) {
-  extern __shared__ float sh[];
-  float* ent = sh;                                       // [C]
-  int* open = reinterpret_cast<int*>(ent + C);           // [C]
-  float* sorted = reinterpret_cast<float*>(open + C);    // [C]
+__device__ __forceinline__ uint32_t order_bits(float x) {
+  const uint32_t u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__global__ void __launch_bounds__(1024) commit_kernel(int C, const float* entropy,
+                                                     const int32_t* argmax, const uint8_t* cand,
+                                                     const float* gamma,
+                                                     uint8_t* committed_state,
+                                                     int32_t* token_state, uint8_t* commit_out,
+                                                     int32_t* tokens, int32_t* n_commit) {
+  extern __shared__ uint32_t shu[];
+  const int nw = blockDim.x >> 5;
+  uint32_t* key_a = shu;                          // [C] keys in the current order
+  uint16_t* pos_a = reinterpret_cast<uint16_t*>(key_a + C);      // [C] their positions
+  uint32_t* hist = reinterpret_cast<uint32_t*>(pos_a + ((C + 1) & ~1));   // [256][nw]
+  __shared__ uint32_t dig_tot[256];
   __shared__ int n_cand, cut;
   __shared__ float warp_tot[32];
   const int b = blockIdx.x, i = threadIdx.x;
+  const int lane = i & 31, wid = i >> 5;
   const long long base = (long long)b * C;
   float hi = 0.f;
   int oi = 0;
   if (i < C) {
     hi = entropy[base + i];
     oi = cand[base + i] != 0 && !(committed_state && committed_state[base + i]);
-    ent[i] = oi ? hi : INFINITY;
-    open[i] = oi;
   }
   if (i == 0) {
     n_cand = 0;
     cut = 0x7fffffff;
   }
+  // this thread's element in the current order: initially position i
+  // (+0.f turns a -0 entropy into +0, so that the two compare equal as floats do)
+  uint32_t key = (i < C && oi) ? order_bits(hi + 0.f) : 0xffffffffu;
+  int src = i;
   __syncthreads();
-  int rank = 0;
-  if (i < C && oi) {
-    // keys of closed positions are +inf (entropies are finite), so they never count
-    int j = 0;
-    for (; j + 4 <= C; j += 4) {
-      const float4 k4 = *reinterpret_cast<const float4*>(ent + j);
-      rank += (k4.x < hi) || (k4.x == hi && j < i);
-      rank += (k4.y < hi) || (k4.y == hi && j + 1 < i);
-      rank += (k4.z < hi) || (k4.z == hi && j + 2 < i);
-      rank += (k4.w < hi) || (k4.w == hi && j + 3 < i);
+  if (i < C && oi) atomicAdd(&n_cand, 1);
+#pragma unroll 1
+  for (int shift = 0; shift < 32; shift += 8) {
+    const bool live = i < C;
+    const uint32_t d = (key >> shift) & 255u;
+    for (int k = i; k < 256 * nw; k += blockDim.x) hist[k] = 0;
+    __syncthreads();
+    const unsigned act = __ballot_sync(0xffffffffu, live);
+    unsigned peers = 0;
+    if (live) {
+      peers = __match_any_sync(act, d);
+      // the lowest lane of each digit group records the warp's count
+      if ((peers & ((1u << lane) - 1u)) == 0) hist[d * nw + wid] = __popc(peers);
     }
-    for (; j < C; ++j) rank += (ent[j] < hi) || (ent[j] == hi && j < i);
-    sorted[rank] = hi;
-    atomicAdd(&n_cand, 1);
+    __syncthreads();
+    // digit totals, then the exclusive scan over (digit, warp)
+    if (i < 256) {
+      uint32_t t = 0;
+      for (int w = 0; w < nw; ++w) t += hist[i * nw + w];
+      dig_tot[i] = t;
+    }
+    __syncthreads();
+    if (i < 32) {
+      // one warp scans the 256 digit totals, 8 per lane
+      uint32_t v[8], run = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        v[q] = dig_tot[i * 8 + q];
+        run += v[q];
+      }
+      uint32_t inc = run;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (i >= o) inc += y;
+      }
+      uint32_t ex = inc - run;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint32_t t = v[q];
+        dig_tot[i * 8 + q] = ex;
+        ex += t;
+      }
+    }
+    __syncthreads();
+    if (i < 256) {
+      uint32_t run = dig_tot[i];
+      for (int w = 0; w < nw; ++w) {
+        const uint32_t c = hist[i * nw + w];
+        hist[i * nw + w] = run;
+        run += c;
+      }
+    }
+    __syncthreads();
+    if (live) {
+      const int dst = (int)(hist[d * nw + wid] + __popc(peers & ((1u << lane) - 1u)));
+      key_a[dst] = key;
+      pos_a[dst] = (uint16_t)src;
+    }
+    __syncthreads();
+    if (live) {
+      key = key_a[i];
+      src = pos_a[i];
+    }
+    __syncthreads();
   }
-  __syncthreads();
-  // prefix sums of the sorted entropies (block scan: warp scans, then warp totals);
-  // the cut is the first k >= 1 whose prefix passes gamma, else every candidate
-  const int lane = i & 31, wid = i >> 5;
+  // thread i holds the i-th element of the confidence order (position src);
+  // prefix sums of the sorted entropies: the cut is the first k >= 1 whose prefix
+  // passes gamma, else every candidate
   const int nc = n_cand;
-  float run = (i < nc) ? sorted[i] : 0.f;
+  float run = (i < nc) ? entropy[base + src] : 0.f;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const float y = __shfl_up_sync(0xffffffffu, run, o);
@@ -357,12 +423,14 @@ __global__ void commit_kernel(int C, const float* entropy, const int32_t* argmax
   __syncthreads();
   if (i == 0) n_commit[b] = cut;
   if (i < C) {
-    const bool acc = oi && rank < cut;
-    const int tok = argmax[base + i];
-    commit_out[base + i] = acc ? 1 : 0;
-    tokens[base + i] = acc ? tok : -1;
-    if (acc && committed_state) committed_state[base + i] = 1;
-    if (acc && token_state) token_state[base + i] = tok;
+    // every position: accepted iff it is a candidate ranked before the cut
+    const bool acc = i < cut && i < nc;
+    const int p = src;
+    const int tok = argmax[base + p];
+    commit_out[base + p] = acc ? 1 : 0;
+    tokens[base + p] = acc ? tok : -1;
+    if (acc && committed_state) committed_state[base + p] = 1;
+    if (acc && token_state) token_state[base + p] = tok;
   }
 }
 
@@ -518,9 +586,9 @@ cudaError_t commit(int B, int C, const float* entropy, const int32_t* argmax,
                    int32_t* n_commit, cudaStream_t st) {
   if (B == 0) return cudaSuccess;
   const int threads = ((C + 31) / 32) * 32;
-  commit_kernel<<<B, threads, (size_t)C * 12, st>>>(C, entropy, argmax, cand, gamma,
-                                                     committed_state, token_state, commit_out,
-                                                     tokens, n_commit);
+  const size_t shm = (size_t)C * 4 + (size_t)((C + 1) & ~1) * 2 + (size_t)256 * (threads / 32) * 4;
+  commit_kernel<<<B, threads, shm, st>>>(C, entropy, argmax, cand, gamma, committed_state,
+                                         token_state, commit_out, tokens, n_commit);
   return cudaGetLastError();
 }
 

@@ -68,6 +68,8 @@ _SIGS = {
     "dg_quantize_cols_e4m3": [P, I, I, P, P, P],
     "dg_selfcond_from_probs8": [DP, P, P, P, I, P, P, P, P, Z, P],
     "dg_lmhead_logsoftmax_entropy_fp8": [DP, P, P, I, P, P, P, P, P, P, P, P, Z, P],
+    "dg_quantize_nvfp4": [P, I, I, P, P, P, P],
+    "dg_lmhead_logsoftmax_entropy_nvfp4": [DP, P, I, P, P, P, P, P, P, P, P, P, Z, P],
     "dg_commit": [DP, P, P, P, P, P, P, P, P, P, P],
     "dg_selfcond_embed": [DP, P, I, P, P, P, P, P, P, Z, P],
     "dg_denoise_heads": [DP, P, I, P, I, P, P, P, P, P, P, P, P, P, P, Z, P, Z, P],
@@ -233,6 +235,18 @@ def dg_lmhead_logsoftmax_entropy_fp8(dims, h8, h_scale, M, w8, w_scale, inv_t, l
                                                   _p(w8), _p(w_scale), _p(inv_t), _p(lse),
                                                   _p(entropy), _p(maxz), _p(argmax),
                                                   _p(workspace), _nbytes(workspace), _s(stream))
+
+
+def dg_quantize_nvfp4(x, rows, cols, codes, scales, g, stream=None):
+    return lib().dg_quantize_nvfp4(_p(x), rows, cols, _p(codes), _p(scales), _p(g), _s(stream))
+
+
+def dg_lmhead_logsoftmax_entropy_nvfp4(dims, h, M, codes, scales, g, inv_t, lse, entropy, maxz,
+                                       argmax, workspace, stream=None):
+    return lib().dg_lmhead_logsoftmax_entropy_nvfp4(ctypes.byref(dims), _p(h), M, _p(codes),
+                                                    _p(scales), _p(g), _p(inv_t), _p(lse),
+                                                    _p(entropy), _p(maxz), _p(argmax),
+                                                    _p(workspace), _nbytes(workspace), _s(stream))
 
 
 def dg_commit(dims, entropy, argmax, cand, gamma, committed_state, token_state, commit, tokens,

@@ -323,13 +323,14 @@ class Prefill:
 
 class LmHead:
     """One lm-head statistics pass over M rows (lse, entropy, max logit, argmax), on bf16
-    operands (dg_lmhead_logsoftmax_entropy) or on e4m3 operands with per-row scales
-    (dg_quantize_rows_e4m3 of the rows, then dg_lmhead_logsoftmax_entropy_fp8; W is
-    quantised once, when the object is made)."""
+    operands (dg_lmhead_logsoftmax_entropy), on e4m3 operands with per-row scales
+    (dg_quantize_rows_e4m3 of the rows, then dg_lmhead_logsoftmax_entropy_fp8), or on
+    bf16 rows against NVFP4 weights (dg_lmhead_logsoftmax_entropy_nvfp4); W is
+    quantised once, when the object is made."""
 
-    def __init__(self, shape, w, M, fp8=False, device="cuda"):
+    def __init__(self, shape, w, M, fp8=False, device="cuda", fp4=False):
         f32, i32, u8 = torch.float32, torch.int32, torch.uint8
-        self.shape, self.M, self.fp8 = shape, M, fp8
+        self.shape, self.M, self.fp8, self.fp4 = shape, M, fp8, fp4
         self.dims = dg.make_dims(d_model=shape.D, V=shape.V)
         self.h = torch.empty((M, shape.D), dtype=torch.bfloat16, device=device)
         self.inv_t = torch.empty(M, dtype=f32, device=device)
@@ -339,6 +340,13 @@ class LmHead:
         self.ws = torch.empty(dg.dg_workspace_bytes(self.dims, dg.DG_WS_LMHEAD, M), dtype=u8,
                               device=device)
         self.w = w
+        if fp4:
+            D, V = shape.D, shape.V
+            self.codes = torch.empty((D // 64, V, 32), dtype=u8, device=device)
+            self.scales = torch.empty((D // 64, V, 4), dtype=u8, device=device)
+            self.g = torch.empty(1, dtype=f32, device=device)
+            dg._check(dg.dg_quantize_nvfp4(w, V, D, self.codes, self.scales, self.g),
+                      "dg_quantize_nvfp4")
         if fp8:
             self.w8 = torch.empty((shape.V, shape.D), dtype=u8, device=device)
             self.w_scale = torch.empty(shape.V, dtype=f32, device=device)
@@ -350,6 +358,13 @@ class LmHead:
     def run(self, step_idx=0, stream=None):
         """Enqueue one pass; returns the number of library kernels."""
         d = self.dims
+        if self.fp4:
+            dg._check(dg.dg_lmhead_logsoftmax_entropy_nvfp4(d, self.h, self.M, self.codes,
+                                                            self.scales, self.g, self.inv_t,
+                                                            self.lse, self.ent, self.maxz,
+                                                            self.argmax, self.ws, stream),
+                      "dg_lmhead_logsoftmax_entropy_nvfp4")
+            return 2
         if not self.fp8:
             dg._check(dg.dg_lmhead_logsoftmax_entropy(d, self.h, self.M, self.w, self.inv_t,
                                                       self.lse, self.ent, self.maxz, self.argmax,

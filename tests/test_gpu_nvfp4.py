@@ -1,0 +1,97 @@
+"""GPU parity of the 4-bit lm-head pass: the NVFP4 quantiser (bit-exact against the
+oracle's quantisation, in the K-block-major layout) and the statistics pass
+against NVFP4 weights (against the oracle's plain statistics of the dequantised
+weights, 2e-3 absolute; argmax where the top two logits are 1e-3 apart)."""
+import numpy as np
+import pytest
+
+import oracle
+from structured_slot_reads_gb300 import dg, inputs
+from tests.gpu_util import assert_abs, dev, dev_bf16, host, top2_gap
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+def _quantize(wd, V, D):
+    codes = torch.empty((D // 64, V, 32), dtype=torch.uint8, device="cuda")
+    scales = torch.empty((D // 64, V, 4), dtype=torch.uint8, device="cuda")
+    g = torch.empty(1, dtype=torch.float32, device="cuda")
+    assert dg.dg_quantize_nvfp4(wd, V, D, codes, scales, g) == dg.DG_OK
+    return codes, scales, g
+
+
+def _stats(h, codes, scales, g, inv_t, V, D):
+    M = h.shape[0]
+    d = dg.make_dims(d_model=D, V=V)
+    f32 = torch.float32
+    out = [torch.empty(M, dtype=f32, device="cuda") for _ in range(3)]
+    arg = torch.empty(M, dtype=torch.int32, device="cuda")
+    ws = torch.empty(dg.dg_workspace_bytes(d, dg.DG_WS_LMHEAD, M), dtype=torch.uint8,
+                     device="cuda")
+    rc = dg.dg_lmhead_logsoftmax_entropy_nvfp4(d, dev_bf16(h), M, codes, scales, g, dev(inv_t),
+                                               out[0], out[1], out[2], arg, ws)
+    assert rc == dg.DG_OK, dg.strerror(rc)
+    torch.cuda.synchronize()
+    return [host(x) for x in out] + [host(arg)]
+
+
+@pytest.mark.parametrize("V,D", [(1000, 256), (4096, 128), (300, 2816)])
+def test_quantizer_bit_exact(V, D):
+    w = inputs.normal_bf16((V, D), 1.0 / np.sqrt(D), 5 + V, 1)
+    w[3, 64:80] = 0.0                         # a zero block
+    w[7, :16] *= 40.0                          # a block far above the rest
+    codes, scales, g = _quantize(dev_bf16(w), V, D)
+    torch.cuda.synchronize()
+    oc, osc, og = oracle.quantize_nvfp4(w)
+    ckb, skb = oracle.to_kblock_layout(oc, osc)
+    assert host(g)[0] == og
+    assert np.array_equal(host(codes), ckb)
+    assert np.array_equal(host(scales), skb)
+
+
+@pytest.mark.parametrize("M,V,D", [(12, 4096, 256), (256, 8192, 512), (300, 3000, 192),
+                                   (1, 1024, 64)])
+def test_nvfp4_lmhead_stats(M, V, D):
+    h = inputs.hidden(M, D, 11 + M)
+    w, _ = inputs.weights(V, D, 12 + V)
+    inv_t = inputs.inv_temperature(M, 13)
+    codes, scales, g = _quantize(dev_bf16(w), V, D)
+    lse, ent, maxz, arg = _stats(h, codes, scales, g, inv_t, V, D)
+    oc, osc = oracle.from_kblock_layout(host(codes), host(scales))
+    wq = oracle.dequantize_nvfp4(oc, osc, host(g)[0])
+    o_lse, o_ent, o_maxz, o_arg = oracle.lmhead_stats(h, wq, inv_t)
+    assert_abs(lse, o_lse, what="lse")
+    assert_abs(ent, o_ent, what="entropy")
+    assert_abs(maxz, o_maxz, what="max logit")
+    z = (h.astype(np.float64) @ wq.T) * inv_t[:, None]
+    clear = top2_gap(z) > 1e-3
+    assert clear.sum() >= M // 2
+    assert np.array_equal(arg[clear], o_arg[clear])
+
+
+def test_nvfp4_lmhead_full_vocabulary_sampled_rows():
+    """262144 x 2816 weights: the quantiser on a slice of rows (with the whole
+    tensor's scale) and the statistics of sampled canvas rows."""
+    V, D, M = 262144, 2816, 256
+    w, _ = inputs.weights(V, D, 77)
+    wd = dev_bf16(w)
+    codes, scales, g = _quantize(wd, V, D)
+    h = inputs.hidden(M, D, 78)
+    inv_t = inputs.inv_temperature(M, 79)
+    lse, ent, maxz, arg = _stats(h, codes, scales, g, inv_t, V, D)
+    gh = host(g)[0]
+    assert gh == oracle.tensor_scale(np.abs(w).max())
+    # quantiser bit-exact on rows [1000, 1256) of every K block
+    sl = slice(1000, 1256)
+    oc, osc, _ = oracle.quantize_nvfp4(w[sl], g=gh)
+    ckb, skb = oracle.to_kblock_layout(oc, osc)
+    assert np.array_equal(host(codes[:, sl]), ckb)
+    assert np.array_equal(host(scales[:, sl]), skb)
+    oc_all, osc_all = oracle.from_kblock_layout(host(codes), host(scales))
+    wq = oracle.dequantize_nvfp4(oc_all, osc_all, gh)
+    rows = np.array([0, 5, 127, 128, 200, 255])
+    o_lse, o_ent, o_maxz, o_arg = oracle.lmhead_stats(h[rows], wq, inv_t[rows])
+    assert_abs(lse[rows], o_lse, what="lse")
+    assert_abs(ent[rows], o_ent, what="entropy")
+    assert_abs(maxz[rows], o_maxz, what="max logit")
