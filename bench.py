@@ -406,13 +406,11 @@ def gpu_arm(args, rank, world, local):
 
 
 def slot_finish_bytes(shape, n_slots):
-    """Algorithmic bytes of the slot finish: each draw row read once, the W rows of
-    its slot's labels, the draw rows' lse, and the per-slot outputs written."""
-    D, R = shape.D, shape.R
-    labels = sum(k for _, k in shape.slots) * shape.B if n_slots else 0
-    rows = n_slots * R
-    return (rows * D * 2 + R * labels * D * 2 + rows * 4
-            + n_slots * (26 * 4 + 4 + 4 + 1 + 4) + rows * 26 * 4)
+    """Algorithmic bytes of the slot finish from gathered label logits: the label
+    logits of every draw read and rewritten as logprobs, the draw rows' lse, the
+    label counts, and the per-slot outputs written."""
+    rows = n_slots * shape.R
+    return rows * 26 * 4 * 2 + rows * 4 + n_slots * 4 + n_slots * (26 * 4 + 4 + 4 + 1 + 4)
 
 
 def commit_bytes(shape):
@@ -437,7 +435,8 @@ def call_work(shape, st):
         "dg_attn_decode": (attn_bytes(shape), attn_flops(shape)),
         "dg_lmhead_logsoftmax_entropy": (W + M * D * 2 + M * 16, 2.0 * M * V * D),
         "dg_slot_read": (W + sr * D * 4, 2.0 * sr * V * D),
-        "dg_denoise_heads": (W + (M + nd) * D * 2 + M * 20 + nd * 4, 2.0 * (M + nd) * V * D),
+        "dg_denoise_heads": (W + (M + nd) * D * 2 + M * 20 + nd * 4 + nd * 26 * 4,
+                             2.0 * (M + nd) * V * D),
         "dg_selfcond_embed": (2 * W + M * D * 2 + M * 8 + M * D * 4, 4.0 * M * V * D),
         "dg_selfcond_from_probs": (W + M * D * 4, 2.0 * M * V * D),
         "dg_slot_noise": (3 * nd * D * 2, 0.0),

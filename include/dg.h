@@ -105,21 +105,34 @@ int dg_attn_decode(const dg_dims* dims, const uint16_t* q, const uint16_t* kc,
                    float* lse, void* workspace, size_t workspace_bytes,
                    void* stream);
 
-/* ---- a2: lm-head -> log-softmax -> entropy -----------------------------
+/* ---- a2: lm-head -> log-softmax -> entropy -> label gather ---------------
  * tau-home.com, "Refusing JSON token generation": one denoise forward gives
- * the logprobs and entropy that the read uses; 24-ai.news, "Token commit
- * mechanism": per-token confidence for the commit.  For each of the M rows,
+ * the logprobs and entropy that the read uses, and the logprobs of the allowed
+ * label ids at the answer slots; 24-ai.news, "Token commit mechanism":
+ * per-token confidence for the commit.  For each of the M rows,
  * z = (h_i . w_v) * inv_t[i] over the whole vocabulary, and
  *   lse[i] = log sum_v exp z_v, entropy[i] = lse - sum_v p_v z_v (nats),
- *   maxz[i] = max_v z_v, argmax[i] = lowest v attaining it.
- * The [M, V] logits are never written to memory.
+ *   maxz[i] = max_v z_v, argmax[i] = lowest v attaining it;
+ * for each of the S slots (S = 0: none), at row i = slot_row[s],
+ *   label_lp[s][k] = z_i[label_ids[s][k]] - lse[i]   (k < n_labels[s]),
+ * taken from the accumulators in the pass's epilogue.  The [M, V] logits are
+ * never written to memory.
  *   h [M, d_model] bf16;  w [V, d_model] bf16;  inv_t [M] fp32 (> 0)
+ *   slot_row [S] int32 (distinct rows in [0, M));  label_ids [S, 26] int32;
+ *   n_labels [S] int32 (0..26);  label_lp [S, 26] fp32 (entries past
+ *   n_labels[s] untouched)
  *   lse, entropy, maxz [M] fp32;  argmax [M] int32
- *   workspace: dg_workspace_bytes(dims, DG_WS_LMHEAD, M) bytes. */
+ *   workspace: dg_workspace_bytes(dims, DG_WS_LMHEAD, M) bytes.
+ * S > M returns DG_ERR_SHAPE; S > 0 with a NULL slot argument DG_ERR_ARG.  A
+ * label id outside [0, V) sets DG_DEV_BAD_LABEL (its label_lp is -inf); a slot
+ * row outside [0, M) or shared by two slots sets DG_DEV_BAD_INDEX.
+ * dg_validate_slots checks the tables on the host before upload. */
 int dg_lmhead_logsoftmax_entropy(const dg_dims* dims, const uint16_t* h, int M,
-                                 const uint16_t* w, const float* inv_t, float* lse,
+                                 const uint16_t* w, const float* inv_t,
+                                 const int32_t* slot_row, const int32_t* label_ids,
+                                 const int32_t* n_labels, int S, float* lse,
                                  float* entropy, float* maxz, int32_t* argmax,
-                                 void* workspace, size_t workspace_bytes,
+                                 float* label_lp, void* workspace, size_t workspace_bytes,
                                  void* stream);
 
 /* ---- a0: noise draws for the slot reads --------------------------------
@@ -154,7 +167,12 @@ int dg_slot_noise(const dg_dims* dims, const uint16_t* h, int M, const uint16_t*
  *   lp_draws [S, R, 26] fp32;  resampled [S] uint8;  n_reads [S] int32
  * R is the number of draw rows per slot; 1 <= samples <= R <= 8.  A slot with
  * n_labels[s] == 0 is a question that was not asked (see dg_ask_if_select): it
- * is not read; chosen = -1, n_reads = 0 and its outputs are zero. */
+ * is not read; chosen = -1, n_reads = 0 and its outputs are zero.
+ * rows == NULL (w and inv_t_rows then unused): lp_draws already holds every
+ * z_k of every draw, as the label gather of dg_denoise_heads writes them, and
+ * the call turns them into lp in place; otherwise the z_k are computed here as
+ * the dot products above (labels known only after the pass, as in a second
+ * ask_if stage). */
 int dg_slot_finish(const dg_dims* dims, const uint16_t* rows, const float* inv_t_rows,
                    const float* lse_rows, const uint16_t* w, const int32_t* label_ids,
                    const int32_t* n_labels, int S, int R, int samples, float gate,
@@ -163,7 +181,8 @@ int dg_slot_finish(const dg_dims* dims, const uint16_t* rows, const float* inv_t
 
 /* Read-only structured read (the `diffusion_read_only` mode of tau-home.com,
  * "Refusing JSON token generation"): dg_slot_noise, then one lm-head pass over
- * all S*R draw rows (W streamed once), then dg_slot_finish.  Arguments as in
+ * all S*R draw rows (W streamed once) that also gathers every draw's label
+ * logits from its accumulators, then dg_slot_finish on them (rows = NULL).  Arguments as in
  * those calls; R = samples draws are always computed (the gate only selects).
  *   workspace: dg_workspace_bytes(dims, DG_WS_SLOT_READ, S*samples) bytes. */
 int dg_slot_read(const dg_dims* dims, const uint16_t* h, int M, const uint16_t* w,
@@ -239,14 +258,16 @@ int dg_quantize_rows_e4m3(const uint16_t* x, int rows, int cols, uint8_t* q, flo
 
 /* dg_lmhead_logsoftmax_entropy on quantised operands: the row statistics of
  * softmax(z_i / T_i) with z_iv = (sum_k h8[i, k] w8[v, k]) * h_scale[i] * w_scale[v]
- * (e4m3 products accumulated in fp32 by the tensor cores).  Outputs, workspace
- * (DG_WS_LMHEAD) and errors as dg_lmhead_logsoftmax_entropy; d_model must be a
- * multiple of 16; h8, w8 and w_scale 16-byte aligned.
+ * (e4m3 products accumulated in fp32 by the tensor cores).  Label gather,
+ * outputs, workspace (DG_WS_LMHEAD) and errors as dg_lmhead_logsoftmax_entropy;
+ * d_model must be a multiple of 16; h8, w8 and w_scale 16-byte aligned.
  *   h8 [M, d_model], w8 [V, d_model] uint8 (e4m3);  h_scale [M], w_scale [V] fp32 */
 int dg_lmhead_logsoftmax_entropy_fp8(const dg_dims* dims, const uint8_t* h8, const float* h_scale,
                                      int M, const uint8_t* w8, const float* w_scale,
-                                     const float* inv_t, float* lse, float* entropy, float* maxz,
-                                     int32_t* argmax, void* workspace, size_t workspace_bytes,
+                                     const float* inv_t, const int32_t* slot_row,
+                                     const int32_t* label_ids, const int32_t* n_labels, int S,
+                                     float* lse, float* entropy, float* maxz, int32_t* argmax,
+                                     float* label_lp, void* workspace, size_t workspace_bytes,
                                      void* stream);
 
 /* ---- next: the self-conditioning P . E on 8-bit operands -----------------
@@ -299,14 +320,17 @@ int dg_quantize_nvfp4(const uint16_t* x, int rows, int cols, uint8_t* codes, uin
  * softmax(z_i / T_i) with z_iv = (h_i . (e2m1 * s)_v) * g, the bf16 rows times
  * the weights widened to bf16 on chip (exact: e2m1 times an e4m3 scale fits
  * bf16), fp32 accumulation on the tensor cores.  Operands from
- * dg_quantize_nvfp4(w, V, d_model, ..); outputs, workspace (DG_WS_LMHEAD) and
- * errors as dg_lmhead_logsoftmax_entropy; d_model a multiple of 64 and V of 4
- * (else DG_ERR_SHAPE); h, codes and scales 16-byte aligned. */
+ * dg_quantize_nvfp4(w, V, d_model, ..); label gather, outputs, workspace
+ * (DG_WS_LMHEAD) and errors as dg_lmhead_logsoftmax_entropy; d_model a multiple
+ * of 64 and V of 4 (else DG_ERR_SHAPE); h, codes and scales 16-byte aligned. */
 int dg_lmhead_logsoftmax_entropy_nvfp4(const dg_dims* dims, const uint16_t* h, int M,
                                        const uint8_t* codes, const uint8_t* scales,
-                                       const float* g, const float* inv_t, float* lse,
+                                       const float* g, const float* inv_t,
+                                       const int32_t* slot_row, const int32_t* label_ids,
+                                       const int32_t* n_labels, int S, float* lse,
                                        float* entropy, float* maxz, int32_t* argmax,
-                                       void* workspace, size_t workspace_bytes, void* stream);
+                                       float* label_lp, void* workspace, size_t workspace_bytes,
+                                       void* stream);
 
 /* ---- next: one wide read in place of the two-stage path -----------------
  * sotaaz.com, "The server accepts at most 26 alternatives per question": the
@@ -392,11 +416,20 @@ int dg_selfcond_embed(const dg_dims* dims, const uint16_t* h, int M,
  *    first 8 vocabulary entries, raised by whole powers of two wherever a logit
  *    lies far above it), and prob_scale[i] = 1 / sum_v probs[i][v], so
  *    p_iv = probs[i][v] * prob_scale[i].
+ *  - the label gather of the draw rows (tau-home.com, "Refusing JSON token
+ *    generation"): draw j is draw j % draw_R of slot j / draw_R, and
+ *    draw_label_z[j][k] = z_j[draw_label_ids[j / draw_R][k]] (k <
+ *    draw_n_labels[j / draw_R]), the label logits dg_slot_finish takes with
+ *    rows = NULL.
  * The statistics and the probabilities are exact for any input whose scaled
  * logits stay below 2^24 log2 units.
  *   h [M, d_model] bf16;  draw_rows [n_draw, d_model] bf16 (NULL if n_draw = 0)
  *   w [V, d_model] bf16;  inv_t [M], inv_t_draw [n_draw] fp32
  *   lse, entropy, maxz [M] fp32;  argmax [M] int32;  lse_draw [n_draw] fp32
+ *   draw_label_ids [n_draw / draw_R, 26] int32;  draw_n_labels [n_draw / draw_R]
+ *   int32;  draw_label_z [n_draw, 26] fp32 (NULL: no gather; else n_draw a
+ *   multiple of draw_R >= 1, DG_ERR_ARG otherwise; a label id outside [0, V)
+ *   sets DG_DEV_BAD_LABEL and gets -inf)
  *   prob_scale [M] fp32;  probs [M, probs_ld] bf16 (probs_ld >= V, multiple of
  *   64; 32-byte aligned; NULL to skip the probabilities)
  *   workspace: dg_workspace_bytes(dims, DG_WS_HEADS, M) bytes. */
@@ -404,8 +437,10 @@ int dg_denoise_heads(const dg_dims* dims, const uint16_t* h, int M,
                      const uint16_t* draw_rows, int n_draw, const uint16_t* w,
                      const float* inv_t, const float* inv_t_draw, float* lse,
                      float* entropy, float* maxz, int32_t* argmax, float* lse_draw,
-                     float* prob_scale, uint16_t* probs, size_t probs_ld,
-                     void* workspace, size_t workspace_bytes, void* stream);
+                     const int32_t* draw_label_ids, const int32_t* draw_n_labels,
+                     int draw_R, float* draw_label_z, float* prob_scale, uint16_t* probs,
+                     size_t probs_ld, void* workspace, size_t workspace_bytes,
+                     void* stream);
 
 /* Expected embedding from dg_denoise_heads' probabilities:
  * out[i] = prob_scale[i] * sum_v probs[i][v] e[v] (24-ai.news, "Token commit

@@ -176,6 +176,36 @@ size_t slot_read_ws(const dg_dims* d, int rows) {
          dgi::lmhead_ws_bytes(rows, d->V);
 }
 
+// Workspace of the lm-head passes: the per-CTA partial statistics, then the
+// row -> slot map of a label gather ([M] int32).
+size_t lmhead_ws(const dg_dims* d, int M) {
+  return dgi::lmhead_ws_bytes(M, d->V) + dgi::align_up((size_t)M * 4, 256);
+}
+
+// The label gather of an lm-head pass (slot s at row slot_row[s], label table
+// of stride 26, label_lp [S][26] = z - lse): none when S == 0, else every
+// pointer is required.  Call after the workspace has been checked.
+int lm_gather(const dg_dims* d, int M, const int32_t* slot_row, const int32_t* label_ids,
+              const int32_t* n_labels, int S, float* label_lp, void* workspace,
+              dgi::LabelGather* g) {
+  *g = dgi::LabelGather{};
+  if (S < 0) return DG_ERR_ARG;
+  if (S == 0) return DG_OK;
+  if (!slot_row || !label_ids || !n_labels || !label_lp) return DG_ERR_ARG;
+  if (S > M) return DG_ERR_SHAPE;
+  g->label_ids = label_ids;
+  g->n_labels = n_labels;
+  g->slot_row = slot_row;
+  g->row_slot = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) +
+                                           dgi::lmhead_ws_bytes(M, d->V));
+  g->out = label_lp;
+  g->L = DG_MAX_LABELS;
+  g->S = S;
+  g->R = 0;
+  g->sub_lse = 1;
+  return DG_OK;
+}
+
 bool prefill_dims_ok(const dg_dims* d) {
   if (!d || d->B < 1 || d->P_max < 1 || d->Hq < 1 || d->Hkv < 1 || d->Hq % d->Hkv) return false;
   return d->d_head == 512 && 128 % (d->Hq / d->Hkv) == 0;
@@ -226,14 +256,23 @@ int slot_read_impl(const dg_dims* d, const uint16_t* h, int M, const uint16_t* w
   cudaError_t err = dgi::slot_noise(h, M, e, d->V, d->d_model, inv_t, slot_row, slot_req, S, R,
                                     seed, step, draw_rows, inv_rows, noise_tok_out, st);
   if (err != cudaSuccess) return DG_ERR_CUDA;
+  // the pass gathers every draw's label logits z/T into lp_draws from its
+  // accumulators; the finish then works from them alone
+  dgi::LabelGather g{};
+  g.label_ids = label_ids;
+  g.n_labels = n_labels;
+  g.out = lp_draws;
+  g.L = L;
+  g.S = S;
+  g.R = R;
   err = dgi::lmhead_stats(draw_rows, rows, w, d->V, d->d_model, inv_rows,
-                          dgi::RowStats{lse_rows, ent_rows, maxz_rows, arg_rows}, p, st);
+                          dgi::RowStats{lse_rows, ent_rows, maxz_rows, arg_rows}, p, st, &g);
   if (err != cudaSuccess) return DG_ERR_CUDA;
   err = (L == DG_MAX_LABELS)
-            ? dgi::slot_finish(draw_rows, inv_rows, lse_rows, w, d->V, d->d_model, label_ids,
+            ? dgi::slot_finish(nullptr, inv_rows, lse_rows, nullptr, d->V, d->d_model, label_ids,
                                n_labels, S, R, samples, gate, q_avg, h_slot, chosen, lp_draws,
                                resampled, n_reads, st)
-            : dgi::slot_finish_wide(draw_rows, inv_rows, lse_rows, w, d->V, d->d_model,
+            : dgi::slot_finish_wide(nullptr, inv_rows, lse_rows, nullptr, d->V, d->d_model,
                                     label_ids, n_labels, L, S, R, samples, gate, q_avg, h_slot,
                                     chosen, lp_draws, resampled, n_reads, st);
   return launch_result(err);
@@ -271,7 +310,7 @@ size_t dg_workspace_bytes(const dg_dims* d, int which, int rows) {
                                 d->W > d->C ? d->C : d->W, d->sm_share);
     case DG_WS_LMHEAD:
       if (!dims_lm(d) || rows < 1) return 0;
-      return dgi::lmhead_ws_bytes(rows, d->V);
+      return lmhead_ws(d, rows);
     case DG_WS_SLOT_READ:
       if (!dims_lm(d) || rows < 1) return 0;
       return slot_read_ws(d, rows);
@@ -303,8 +342,9 @@ size_t dg_probs_ld(int V) { return V < 1 ? 0 : dgi::heads_probs_ld(V); }
 int dg_denoise_heads(const dg_dims* d, const uint16_t* h, int M, const uint16_t* draw_rows,
                      int n_draw, const uint16_t* w, const float* inv_t, const float* inv_t_draw,
                      float* lse, float* entropy, float* maxz, int32_t* argmax, float* lse_draw,
-                     float* prob_scale, uint16_t* probs, size_t probs_ld, void* workspace,
-                     size_t workspace_bytes, void* stream) {
+                     const int32_t* draw_label_ids, const int32_t* draw_n_labels, int draw_R,
+                     float* draw_label_z, float* prob_scale, uint16_t* probs, size_t probs_ld,
+                     void* workspace, size_t workspace_bytes, void* stream) {
   if (!d || M < 1 || n_draw < 0 || n_draw > 16) return DG_ERR_ARG;
   if (!dims_lm(d)) return DG_ERR_SHAPE;
   if (!h || !w || !inv_t || !lse || !entropy || !maxz || !argmax || !prob_scale)
@@ -314,12 +354,23 @@ int dg_denoise_heads(const dg_dims* d, const uint16_t* h, int M, const uint16_t*
     return DG_ERR_ARG;
   if (probs && (probs_ld < (size_t)d->V || probs_ld % 64 || !aligned(probs, 32)))
     return DG_ERR_ARG;
+  dgi::LabelGather g{};
+  if (draw_label_z && n_draw > 0) {
+    // draw j is draw j % draw_R of slot j / draw_R
+    if (!draw_label_ids || !draw_n_labels || draw_R < 1 || n_draw % draw_R) return DG_ERR_ARG;
+    g.label_ids = draw_label_ids;
+    g.n_labels = draw_n_labels;
+    g.out = draw_label_z;
+    g.L = DG_MAX_LABELS;
+    g.S = n_draw / draw_R;
+    g.R = draw_R;
+  }
   const size_t need = dg_workspace_bytes(d, DG_WS_HEADS, M);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DG_ERR_WORKSPACE;
   return launch_result(dgi::denoise_heads(h, M, draw_rows, n_draw, w, d->V, d->d_model, inv_t,
                                           inv_t_draw, dgi::RowStats{lse, entropy, maxz, argmax},
                                           lse_draw, prob_scale, probs, probs_ld, workspace,
-                                          static_cast<cudaStream_t>(stream)));
+                                          static_cast<cudaStream_t>(stream), &g));
 }
 
 int dg_selfcond_from_probs(const dg_dims* d, const uint16_t* probs, size_t probs_ld,
@@ -434,18 +485,23 @@ int dg_attn_decode(const dg_dims* d, const uint16_t* q, const uint16_t* kc, cons
 }
 
 int dg_lmhead_logsoftmax_entropy(const dg_dims* d, const uint16_t* h, int M, const uint16_t* w,
-                                 const float* inv_t, float* lse, float* entropy, float* maxz,
-                                 int32_t* argmax, void* workspace, size_t workspace_bytes,
+                                 const float* inv_t, const int32_t* slot_row,
+                                 const int32_t* label_ids, const int32_t* n_labels, int S,
+                                 float* lse, float* entropy, float* maxz, int32_t* argmax,
+                                 float* label_lp, void* workspace, size_t workspace_bytes,
                                  void* stream) {
-  if (!d || M < 1) return DG_ERR_ARG;
+  if (!d || M < 1 || S < 0) return DG_ERR_ARG;
   if (!dims_lm(d)) return DG_ERR_SHAPE;
   if (!h || !w || !inv_t || !lse || !entropy || !maxz || !argmax) return DG_ERR_ARG;
   if (!aligned(h, 16) || !aligned(w, 16)) return DG_ERR_ARG;
-  const size_t need = dgi::lmhead_ws_bytes(M, d->V);
+  const size_t need = lmhead_ws(d, M);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return DG_ERR_WORKSPACE;
+  dgi::LabelGather g;
+  if (int rc = lm_gather(d, M, slot_row, label_ids, n_labels, S, label_lp, workspace, &g))
+    return rc;
   return launch_result(dgi::lmhead_stats(h, M, w, d->V, d->d_model, inv_t,
                                          dgi::RowStats{lse, entropy, maxz, argmax}, workspace,
-                                         static_cast<cudaStream_t>(stream)));
+                                         static_cast<cudaStream_t>(stream), &g));
 }
 
 int dg_slot_noise(const dg_dims* d, const uint16_t* h, int M, const uint16_t* e,
@@ -469,9 +525,11 @@ int dg_slot_finish(const dg_dims* d, const uint16_t* rows, const float* inv_t_ro
                    int32_t* n_reads, void* stream) {
   if (!d || S < 0 || R < 1 || R > 8 || samples < 1 || samples > R) return DG_ERR_ARG;
   if (!dims_lm(d)) return DG_ERR_SHAPE;
-  if (S > 0 && (!rows || !inv_t_rows || !lse_rows || !w || !label_ids || !n_labels || !q_avg ||
-                !h_slot || !chosen || !lp_draws || !resampled || !n_reads))
+  if (S > 0 && (!lse_rows || !label_ids || !n_labels || !q_avg || !h_slot || !chosen ||
+                !lp_draws || !resampled || !n_reads))
     return DG_ERR_ARG;
+  // rows == null: lp_draws already holds the gathered label logits
+  if (S > 0 && rows && (!inv_t_rows || !w)) return DG_ERR_ARG;
   if (!aligned(rows, 4) || !aligned(w, 4)) return DG_ERR_ARG;
   return launch_result(dgi::slot_finish(rows, inv_t_rows, lse_rows, w, d->V, d->d_model,
                                         label_ids, n_labels, S, R, samples, gate, q_avg, h_slot,
@@ -630,19 +688,24 @@ int dg_selfcond_from_probs8(const dg_dims* d, const uint8_t* p8, const float* p_
 
 int dg_lmhead_logsoftmax_entropy_fp8(const dg_dims* d, const uint8_t* h8, const float* h_scale,
                                      int M, const uint8_t* w8, const float* w_scale,
-                                     const float* inv_t, float* lse, float* entropy, float* maxz,
-                                     int32_t* argmax, void* workspace, size_t workspace_bytes,
+                                     const float* inv_t, const int32_t* slot_row,
+                                     const int32_t* label_ids, const int32_t* n_labels, int S,
+                                     float* lse, float* entropy, float* maxz, int32_t* argmax,
+                                     float* label_lp, void* workspace, size_t workspace_bytes,
                                      void* stream) {
-  if (!d || M < 1) return DG_ERR_ARG;
+  if (!d || M < 1 || S < 0) return DG_ERR_ARG;
   if (!dims_lm(d) || d->d_model % 16) return DG_ERR_SHAPE;
   if (!h8 || !h_scale || !w8 || !w_scale || !inv_t || !lse || !entropy || !maxz || !argmax)
     return DG_ERR_ARG;
   if (!aligned(h8, 16) || !aligned(w8, 16) || !aligned(w_scale, 16)) return DG_ERR_ARG;
   const size_t need = dg_workspace_bytes(d, DG_WS_LMHEAD, M);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DG_ERR_WORKSPACE;
+  dgi::LabelGather g;
+  if (int rc = lm_gather(d, M, slot_row, label_ids, n_labels, S, label_lp, workspace, &g))
+    return rc;
   return launch_result(dgi::lmhead_stats_fp8(h8, h_scale, M, w8, w_scale, d->V, d->d_model, inv_t,
                                              dgi::RowStats{lse, entropy, maxz, argmax}, workspace,
-                                             static_cast<cudaStream_t>(stream)));
+                                             static_cast<cudaStream_t>(stream), &g));
 }
 
 int dg_quantize_nvfp4(const uint16_t* x, int rows, int cols, uint8_t* codes, uint8_t* scales,
@@ -658,10 +721,13 @@ int dg_quantize_nvfp4(const uint16_t* x, int rows, int cols, uint8_t* codes, uin
 
 int dg_lmhead_logsoftmax_entropy_nvfp4(const dg_dims* d, const uint16_t* h, int M,
                                        const uint8_t* codes, const uint8_t* scales,
-                                       const float* g, const float* inv_t, float* lse,
+                                       const float* g, const float* inv_t,
+                                       const int32_t* slot_row, const int32_t* label_ids,
+                                       const int32_t* n_labels, int S, float* lse,
                                        float* entropy, float* maxz, int32_t* argmax,
-                                       void* workspace, size_t workspace_bytes, void* stream) {
-  if (!d || M < 1) return DG_ERR_ARG;
+                                       float* label_lp, void* workspace, size_t workspace_bytes,
+                                       void* stream) {
+  if (!d || M < 1 || S < 0) return DG_ERR_ARG;
   if (!dims_lm(d) || d->d_model % 64 || d->V % 4) return DG_ERR_SHAPE;
   if (!h || !codes || !scales || !g || !inv_t || !lse || !entropy || !maxz || !argmax)
     return DG_ERR_ARG;
@@ -669,9 +735,13 @@ int dg_lmhead_logsoftmax_entropy_nvfp4(const dg_dims* d, const uint16_t* h, int 
     return DG_ERR_ARG;
   const size_t need = dg_workspace_bytes(d, DG_WS_LMHEAD, M);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DG_ERR_WORKSPACE;
+  dgi::LabelGather lg;
+  if (int rc = lm_gather(d, M, slot_row, label_ids, n_labels, S, label_lp, workspace, &lg))
+    return rc;
   return launch_result(dgi::lmhead_stats_nvfp4(h, M, codes, scales, g, d->V, d->d_model, inv_t,
                                                dgi::RowStats{lse, entropy, maxz, argmax},
-                                               workspace, static_cast<cudaStream_t>(stream)));
+                                               workspace, static_cast<cudaStream_t>(stream),
+                                               &lg));
 }
 
 int dg_ask_if_select(const int32_t* chosen1, int S1, const int32_t* cond_slot,

@@ -68,6 +68,7 @@ struct GemmParams {
   const uint8_t* codes4;   // STATS4: e2m1 codes [K/64][N][32 bytes]
   const uint8_t* scales4;  // STATS4: e4m3 block scales [K/64][N][4]
   const float* gscale;     // STATS4: the weights' tensor scale
+  dgi::LabelGather gl;     // STATS kinds: label gather (gl.out null: none)
   float* part;            // STATS: 5 x [cpg][M]; ACCUM: [k_split][M][N]
   __nv_bfloat16* probs;   // PROBS: [M][ldp]
   long long ldp;
@@ -104,7 +105,17 @@ struct Cfg {
 
 // NVFP4 B staging of one K block: BN rows x (32 code bytes + 4 scale bytes)
 constexpr int f4_extra(int bn) { return bn * 36; }
-constexpr int F4_CONV_WARPS = 4;   // warps widening the packed B tile to bf16
+constexpr int F4_CONV_WARPS = 8;   // warps widening the packed B tile to bf16
+
+// Four bytes of e2m1 code pairs (the even element in the low nibble) as four
+// f16x2 words, by the hardware conversion (exact: every e2m1 value is an f16).
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t word, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(word));
+}
 
 template <int MT, int BN, int EPI>
 __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32 * F4_CONV_WARPS : 0), 1)
@@ -120,7 +131,6 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
   constexpr bool ACCUM = EPI == EPI_ACCUM || B_MN || EPI == EPI_ACCUM8;
   constexpr bool F8 = EPI == EPI_STATS8 || EPI == EPI_ACCUM8;
   constexpr bool STATS = EPI == EPI_STATS || EPI == EPI_STATS8 || F4;
-  __shared__ uint32_t lut4[F4 ? 256 : 1];     // STATS4: code byte -> two bf16 values
   // a stage holds 128-byte operand rows: 64 bf16 or 128 e4m3 values of K
   constexpr int KB = F8 ? 128 : BK;
   constexpr uint32_t IDESC_F8 = idesc_e4m3_f32(BM, BN);
@@ -162,19 +172,6 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
   if (warp == PRODUCER_WARP && lane == 0) {
     prefetch_tmap(&tmA);
     if (!F4) prefetch_tmap(&tmB);
-  }
-  if (F4 && warp >= CONV0) {
-    // e2m1 pairs of a code byte (the even element in the low nibble) as bf16x2
-    const int i = threadIdx.x - CONV0 * 32;
-    for (int b = i; b < 256; b += 32 * F4_CONV_WARPS) {
-      auto e2m1 = [](int c) -> float {
-        const float mag = ((c >> 1) & 3) == 0 ? 0.5f * (c & 1)
-                                              : (1.f + 0.5f * (c & 1)) * (float)(1 << (((c >> 1) & 3) - 1));
-        return (c & 8) ? -mag : mag;
-      };
-      const __nv_bfloat162 v = __floats2bfloat162_rn(e2m1(b & 15), e2m1(b >> 4));
-      lut4[b] = *reinterpret_cast<const uint32_t*>(&v);
-    }
   }
   tc_fence_before();
   __syncthreads();
@@ -347,18 +344,19 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
           for (int q = 0; q < 4; ++q) {
             const __half_raw hr =
                 __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)((sw >> (8 * q)) & 0xFF), __NV_E4M3);
-            const float sv = __half2float(__half(hr));
-            const __nv_bfloat162 s2 = __floats2bfloat162_rn(sv, sv);
-            // 16 elements of scale q: code words 2q, 2q+1 -> 16-byte chunks 2q, 2q+1
+            const __half2 s2 = __halves2half2(__half(hr), __half(hr));
+            // 16 elements of scale q: code words 2q, 2q+1 -> 16-byte chunks 2q, 2q+1.
+            // e2m1 times an e4m3 scale has at most 6 significant bits and lies in
+            // [2^-10, 2688] (or is 0), so the f16 product and the bf16 result are exact.
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-              const uint32_t word = cw[2 * q + h];
-              uint32_t o[4];
+              uint32_t f16[4], o[4];
+              e2m1x8_to_f16x2(cw[2 * q + h], f16);
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
-                const uint32_t pr2 = lut4[(word >> (8 * k)) & 0xFF];
-                const __nv_bfloat162 v =
-                    __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&pr2), s2);
+                const float2 f =
+                    __half22float2(__hmul2(*reinterpret_cast<const __half2*>(&f16[k]), s2));
+                const __nv_bfloat162 v = __floats2bfloat162_rn(f.x, f.y);
                 o[k] = *reinterpret_cast<const uint32_t*>(&v);
               }
               const int c = 2 * q + h;
@@ -389,6 +387,34 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
     if (EPI == EPI_PROBS && row_ok) lse2 = __ldg(p.lse + row) * LOG2E;
     float m_run = -INFINITY, s_run = 0.f, t_run = 0.f, best = -INFINITY;
     int best_idx = 0x7fffffff;
+    // Label gather: this row's slot, its label table, and the smallest of its
+    // label ids at or past the current chunk (INT_MAX: none left in this CTA's
+    // columns), so a chunk without one of the row's labels costs one compare.
+    const int32_t* g_ids = nullptr;
+    int g_n = 0, g_o = 0, g_next = 0x7fffffff;
+    float g_it = 0.f;
+    if (STATS && p.gl.out != nullptr && row_ok && has_work) {
+      int gs = -1;
+      if (p.gl.R > 0) {
+        if (row < p.gl.S * p.gl.R) {
+          gs = row / p.gl.R;
+          g_o = row;
+        }
+      } else {
+        gs = p.gl.row_slot[row];
+        g_o = gs;
+      }
+      if (gs >= 0) {
+        g_n = min(max(__ldg(p.gl.n_labels + gs), 0), p.gl.L);
+        g_ids = p.gl.label_ids + (long long)gs * p.gl.L;
+        g_it = __ldg(p.inv_t + row);
+        const int lo = t_begin * BN;
+        for (int k = 0; k < g_n; ++k) {
+          const int id = __ldg(g_ids + k);
+          if (id >= lo && id < g_next) g_next = id;
+        }
+      }
+    }
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = t_begin; t < t_end && has_work; ++t) {
@@ -425,6 +451,24 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
         if (F4) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * gs);
+        }
+        if (STATS && g_next < n0 + 32) {
+          // one or more of this row's labels fall in the chunk: take their
+          // logits from the registers, and find the next label past the chunk
+          int nn = 0x7fffffff;
+          for (int k = 0; k < g_n; ++k) {
+            const int id = __ldg(g_ids + k);
+            const unsigned dj = (unsigned)(id - n0);
+            if (dj < 32u) {
+              float z = __uint_as_float(r[0]);
+#pragma unroll
+              for (int j = 1; j < 32; ++j) z = dj == (unsigned)j ? __uint_as_float(r[j]) : z;
+              p.gl.out[(long long)g_o * p.gl.L + k] = z * g_it;
+            } else if (id >= n0 + 32 && id < nn) {
+              nn = id;
+            }
+          }
+          g_next = nn;
         }
         if (STATS) {
           if (n0 + 32 <= p.N) {
@@ -547,7 +591,8 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
 // Merge the per-CTA online statistics of every row: one warp per row, lanes over
 // the CTA partials (stored row-major, [M][cpg]), a fixed shuffle-tree order.
 __global__ void stats_finalize_kernel(const float* part, int cpg, int M, const float* inv_t,
-                                      float* lse, float* entropy, float* maxz, int32_t* argmax) {
+                                      float* lse, float* entropy, float* maxz, int32_t* argmax,
+                                      dgi::LabelGather gl, int V, int* status) {
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= M) return;
@@ -584,13 +629,60 @@ __global__ void stats_finalize_kernel(const float* part, int cpg, int M, const f
       idx = io;
     }
   }
+  const float l = (m + log2f(s)) * LN2;
   if (lane == 0) {
-    const float l = (m + log2f(s)) * LN2;
     lse[row] = l;
     entropy[row] = l - (t / s) * LN2;
     maxz[row] = best * inv_t[row];
     argmax[row] = idx;
   }
+  if (gl.out != nullptr) {
+    // the gathered label logits of a slot row: ids checked, lse subtracted
+    int gs = -1, go = 0;
+    if (gl.R > 0) {
+      if (row < gl.S * gl.R) {
+        gs = row / gl.R;
+        go = row;
+      }
+    } else {
+      gs = gl.row_slot[row];
+      go = gs;
+    }
+    if (gs >= 0) {
+      const int n = min(max(gl.n_labels[gs], 0), gl.L);
+      for (int k = lane; k < n; k += 32) {
+        const int id = gl.label_ids[(long long)gs * gl.L + k];
+        float* dst = gl.out + (long long)go * gl.L + k;
+        if (id < 0 || id >= V) {
+          atomicOr(status, 4 /* DG_DEV_BAD_LABEL */);
+          *dst = -INFINITY;
+        } else if (gl.sub_lse) {
+          *dst -= l;
+        }
+      }
+    }
+  }
+}
+
+// Slot of every row for a label gather keyed by slot rows: row_slot was set to
+// -1; a row outside [0, M) or claimed by two slots is flagged.
+__global__ void row_slot_kernel(const int32_t* slot_row, int S, int M, int32_t* row_slot,
+                                int* status) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= S) return;
+  const int r = slot_row[s];
+  if (r < 0 || r >= M || atomicCAS(row_slot + r, -1, s) != -1)
+    atomicOr(status, 8 /* DG_DEV_BAD_INDEX */);
+}
+
+// Prepares a label gather (the row -> slot map when slots are given by row).
+cudaError_t gather_prepare(const dgi::LabelGather* g, int M, cudaStream_t st) {
+  if (!g || !g->out || g->R > 0 || g->S == 0) return cudaSuccess;
+  cudaError_t e = cudaMemsetAsync(g->row_slot, 0xFF, (size_t)M * sizeof(int32_t), st);
+  if (e != cudaSuccess) return e;
+  row_slot_kernel<<<(g->S + 255) / 256, 256, 0, st>>>(g->slot_row, g->S, M, g->row_slot,
+                                                      dgi::status_ptr());
+  return cudaGetLastError();
 }
 
 // out[m][n] = row_scale[m] * sum over splits of part[s][m][n], splits added in
@@ -649,12 +741,14 @@ int stats_cpg(int M, int V) {
 
 // Row statistics over the vocabulary: partials + finalize.
 cudaError_t run_stats(const uint16_t* h, int M, const uint16_t* w, int V, int D,
-                      const float* inv_t, dgi::RowStats out, float* part, cudaStream_t st) {
+                      const float* inv_t, dgi::RowStats out, float* part, cudaStream_t st,
+                      const dgi::LabelGather* gather) {
   CUtensorMap ta, tb;
   if (!dgi::make_tmap_bf16_2d(&ta, h, D, M, (uint64_t)D * 2, BK, BM)) return cudaErrorInvalidValue;
   if (!dgi::make_tmap_bf16_2d(&tb, w, D, V, (uint64_t)D * 2, BK, STATS_BN)) return cudaErrorInvalidValue;
   const int mt = stats_mt(M);
   const int groups = (M + mt * BM - 1) / (mt * BM);
+  if (cudaError_t e0 = gather_prepare(gather, M, st); e0 != cudaSuccess) return e0;
   GemmParams p{};
   p.M = M;
   p.N = V;
@@ -664,24 +758,28 @@ cudaError_t run_stats(const uint16_t* h, int M, const uint16_t* w, int V, int D,
   p.inv_t = inv_t;
   p.part = part;
   p.status = dgi::status_ptr();
+  if (gather) p.gl = *gather;
   cudaError_t e = (mt == 1) ? launch_gemm<1, STATS_BN, EPI_STATS>(ta, tb, p, groups * p.cpg, st)
                             : launch_gemm<2, STATS_BN, EPI_STATS>(ta, tb, p, groups * p.cpg, st);
   if (e != cudaSuccess) return e;
   stats_finalize_kernel<<<(M + 7) / 8, 256, 0, st>>>(part, p.cpg, M, inv_t, out.lse,
-                                                     out.entropy, out.maxz, out.argmax);
+                                                     out.entropy, out.maxz, out.argmax, p.gl, V,
+                                                     p.status);
   return cudaGetLastError();
 }
 
 // The statistics pass on e4m3 operands: K blocks of 128 values (128-byte rows).
 cudaError_t run_stats_fp8(const uint8_t* h8, const float* h_scale, int M, const uint8_t* w8,
                           const float* w_scale, int V, int D, const float* inv_t,
-                          dgi::RowStats out, float* part, cudaStream_t st) {
+                          dgi::RowStats out, float* part, cudaStream_t st,
+                          const dgi::LabelGather* gather) {
   CUtensorMap ta, tb;
   if (!dgi::make_tmap_u8_2d(&ta, h8, D, M, (uint64_t)D, 128, BM)) return cudaErrorInvalidValue;
   if (!dgi::make_tmap_u8_2d(&tb, w8, D, V, (uint64_t)D, 128, STATS_BN))
     return cudaErrorInvalidValue;
   const int mt = stats_mt(M);
   const int groups = (M + mt * BM - 1) / (mt * BM);
+  if (cudaError_t e0 = gather_prepare(gather, M, st); e0 != cudaSuccess) return e0;
   GemmParams p{};
   p.M = M;
   p.N = V;
@@ -693,12 +791,14 @@ cudaError_t run_stats_fp8(const uint8_t* h8, const float* h_scale, int M, const 
   p.col_scale = w_scale;
   p.part = part;
   p.status = dgi::status_ptr();
+  if (gather) p.gl = *gather;
   cudaError_t e =
       (mt == 1) ? launch_gemm<1, STATS_BN, EPI_STATS8>(ta, tb, p, groups * p.cpg, st)
                 : launch_gemm<2, STATS_BN, EPI_STATS8>(ta, tb, p, groups * p.cpg, st);
   if (e != cudaSuccess) return e;
   stats_finalize_kernel<<<(M + 7) / 8, 256, 0, st>>>(part, p.cpg, M, inv_t, out.lse,
-                                                     out.entropy, out.maxz, out.argmax);
+                                                     out.entropy, out.maxz, out.argmax, p.gl, V,
+                                                     p.status);
   return cudaGetLastError();
 }
 
@@ -723,11 +823,12 @@ cudaError_t launch_stats4(const CUtensorMap& ta, const GemmParams& p, int grid, 
 
 cudaError_t run_stats_nvfp4(const uint16_t* h, int M, const uint8_t* codes, const uint8_t* scales,
                             const float* g, int V, int D, const float* inv_t, dgi::RowStats out,
-                            float* part, cudaStream_t st) {
+                            float* part, cudaStream_t st, const dgi::LabelGather* gather) {
   CUtensorMap ta;
   if (!dgi::make_tmap_bf16_2d(&ta, h, D, M, (uint64_t)D * 2, BK, BM)) return cudaErrorInvalidValue;
   const int mt = stats_mt(M);
   const int groups = (M + mt * BM - 1) / (mt * BM);
+  if (cudaError_t e0 = gather_prepare(gather, M, st); e0 != cudaSuccess) return e0;
   GemmParams p{};
   p.M = M;
   p.N = V;
@@ -740,11 +841,13 @@ cudaError_t run_stats_nvfp4(const uint16_t* h, int M, const uint8_t* codes, cons
   p.gscale = g;
   p.part = part;
   p.status = dgi::status_ptr();
+  if (gather) p.gl = *gather;
   cudaError_t e = (mt == 1) ? launch_stats4<1>(ta, p, groups * p.cpg, st)
                             : launch_stats4<2>(ta, p, groups * p.cpg, st);
   if (e != cudaSuccess) return e;
   stats_finalize_kernel<<<(M + 7) / 8, 256, 0, st>>>(part, p.cpg, M, inv_t, out.lse,
-                                                     out.entropy, out.maxz, out.argmax);
+                                                     out.entropy, out.maxz, out.argmax, p.gl, V,
+                                                     p.status);
   return cudaGetLastError();
 }
 
@@ -796,20 +899,24 @@ size_t lmhead_ws_bytes(int M, int V) {
 }
 
 cudaError_t lmhead_stats(const uint16_t* h, int M, const uint16_t* w, int V, int D,
-                         const float* inv_t, RowStats out, void* ws, cudaStream_t st) {
-  return run_stats(h, M, w, V, D, inv_t, out, static_cast<float*>(ws), st);
+                         const float* inv_t, RowStats out, void* ws, cudaStream_t st,
+                         const LabelGather* gather) {
+  return run_stats(h, M, w, V, D, inv_t, out, static_cast<float*>(ws), st, gather);
 }
 
 cudaError_t lmhead_stats_fp8(const uint8_t* h8, const float* h_scale, int M, const uint8_t* w8,
                              const float* w_scale, int V, int D, const float* inv_t, RowStats out,
-                             void* ws, cudaStream_t st) {
-  return run_stats_fp8(h8, h_scale, M, w8, w_scale, V, D, inv_t, out, static_cast<float*>(ws), st);
+                             void* ws, cudaStream_t st, const LabelGather* gather) {
+  return run_stats_fp8(h8, h_scale, M, w8, w_scale, V, D, inv_t, out, static_cast<float*>(ws), st,
+                       gather);
 }
 
 cudaError_t lmhead_stats_nvfp4(const uint16_t* h, int M, const uint8_t* codes,
                                const uint8_t* scales, const float* g, int V, int D,
-                               const float* inv_t, RowStats out, void* ws, cudaStream_t st) {
-  return run_stats_nvfp4(h, M, codes, scales, g, V, D, inv_t, out, static_cast<float*>(ws), st);
+                               const float* inv_t, RowStats out, void* ws, cudaStream_t st,
+                               const LabelGather* gather) {
+  return run_stats_nvfp4(h, M, codes, scales, g, V, D, inv_t, out, static_cast<float*>(ws), st,
+                         gather);
 }
 
 size_t selfcond_ws_bytes(int M, int V, int D) {

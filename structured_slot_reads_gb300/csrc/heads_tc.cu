@@ -89,6 +89,7 @@ struct HeadsParams {
   float* part_draw;         // draws: 2 planes of [n_draw][cpg]: m, s
   __nv_bfloat16* probs;     // [M][ldp] or null
   long long ldp;
+  dgi::LabelGather gl;      // draws' label logits z/T (R > 0 form; gl.out null: none)
   int* status;
 };
 
@@ -155,7 +156,9 @@ struct HCfg {
   static constexpr int TMEM_COLS = 512;
   static constexpr int EPI_WARPS = 4 * MT;
   static constexpr int THREADS = (EPI_WARPS + 2) * 32;    // + producer + MMA issuer
-  static constexpr int BAR_BYTES = 512 + EPI_WARPS * DRAW_N * 8;
+  static constexpr int GBITS_OFF = 512 + EPI_WARPS * DRAW_N * 8;  // label-gather chunk bits
+  static constexpr int GBITS_WORDS = 64;
+  static constexpr int BAR_BYTES = GBITS_OFF + GBITS_WORDS * 4;
   static constexpr int NS_FIT = (232448 - 1024 - BAR_BYTES) / STAGE_BYTES;
   static constexpr int NSTAGE = NS_FIT > 8 ? 8 : NS_FIT;
   static constexpr int SMEM_BYTES = 1024 + NSTAGE * STAGE_BYTES + BAR_BYTES;
@@ -214,6 +217,7 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* draw_red = reinterpret_cast<float*>(bar_base + 512);
+  uint32_t* gbits = reinterpret_cast<uint32_t*>(bar_base + CF::GBITS_OFF);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -363,6 +367,27 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
       dscale[j] = (DRAWS && j < p.n_draw) ? __ldg(p.inv_t_draw + j) * LOG2E : 0.f;
     }
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    // Label gather of the draw rows: one bit per 32 vocabulary rows of this
+    // CTA's range that hold a label of some draw (aliased modulo 2048 chunks,
+    // which can only add chunks to scan), so a warp scans the label table only
+    // for the rare 32-row chunks that hold a label.
+    const bool gat = DRAWS && draws_here && p.gl.out != nullptr;
+    const int g_lo = t_begin * BN;
+    if (gat) {
+      for (int i = threadIdx.x; i < CF::GBITS_WORDS; i += EPI_THREADS) gbits[i] = 0;
+      epi_bar(EPI_THREADS);
+      const int hi = min(t_end * BN, p.V);
+      for (int i = threadIdx.x; i < p.gl.S * p.gl.L; i += EPI_THREADS) {
+        const int sl = i / p.gl.L;
+        if (i % p.gl.L >= min(max(__ldg(p.gl.n_labels + sl), 0), p.gl.L)) continue;
+        const int id = __ldg(p.gl.label_ids + i);
+        if (id >= g_lo && id < hi) {
+          const int c = ((id - g_lo) >> 5) & (CF::GBITS_WORDS * 32 - 1);
+          atomicOr(gbits + (c >> 5), 1u << (c & 31));
+        }
+      }
+      epi_bar(EPI_THREADS);
+    }
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = t_begin; t < t_end; ++t) {
@@ -467,7 +492,8 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
           // lanes below row 128 repeat half 0 and are skipped
           const int vl = (half ? CF::HALF1_ROW : 0) + quarter * 32 + lane;
           const int vocab = t * BN + vl;
-          if ((half == 0 || vl >= 128) && vl < BN && vocab < p.V) {
+          const bool lane_ok = (half == 0 || vl >= 128) && vl < BN && vocab < p.V;
+          if (lane_ok) {
 #pragma unroll
             for (int j = 0; j < DRAW_N; ++j) {
               if (j < p.n_draw) {
@@ -475,6 +501,27 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
                 const float mn = fmaxf(dm[j], v);
                 ds[j] = ds[j] * ex2(dm[j] - mn) + ex2(v - mn);
                 dm[j] = mn;
+              }
+            }
+          }
+          if (gat) {
+            // the warp's 32 vocabulary rows are one chunk (BN and the half-1
+            // offset are multiples of 32): a uniform test, then a scan of the
+            // label table by the lanes whose row is a label
+            const int c = ((t * BN + vl - lane - g_lo) >> 5) & (CF::GBITS_WORDS * 32 - 1);
+            if ((gbits[c >> 5] >> (c & 31)) & 1u) {
+              for (int sl = 0; sl < p.gl.S && lane_ok; ++sl) {
+                const int n = min(max(__ldg(p.gl.n_labels + sl), 0), p.gl.L);
+                for (int k = 0; k < n; ++k) {
+                  if (__ldg(p.gl.label_ids + sl * p.gl.L + k) != vocab) continue;
+                  for (int rr = 0; rr < p.gl.R; ++rr) {
+                    const int j = sl * p.gl.R + rr;
+                    float z = __uint_as_float(r[0]);
+#pragma unroll
+                    for (int q = 1; q < DRAW_N; ++q) z = j == q ? __uint_as_float(r[q]) : z;
+                    p.gl.out[(long long)j * p.gl.L + k] = z * __ldg(p.inv_t_draw + j);
+                  }
+                }
               }
             }
           }
@@ -616,9 +663,21 @@ __device__ void finalize_row(int row, int lane, const float* part, int cpg, int 
   }
 }
 
-// Draw rows: per-CTA (max, sum) pairs merged, one warp per row.
+// Draw rows: per-CTA (max, sum) pairs merged, one warp per row; the row's
+// gathered label logits get their ids checked.
 __device__ void finalize_draw(int j, int lane, const float* part_draw, int cpg, int n_draw,
-                              float* lse_draw) {
+                              float* lse_draw, const dgi::LabelGather& gl, int V, int* status) {
+  if (gl.out != nullptr && j < gl.S * gl.R) {
+    const int sl = j / gl.R;
+    const int n = min(max(gl.n_labels[sl], 0), gl.L);
+    for (int k = lane; k < n; k += 32) {
+      const int id = gl.label_ids[(long long)sl * gl.L + k];
+      if (id < 0 || id >= V) {
+        atomicOr(status, 4 /* DG_DEV_BAD_LABEL */);
+        gl.out[(long long)j * gl.L + k] = -INFINITY;
+      }
+    }
+  }
   const float* pm = part_draw + (long long)j * cpg;
   const float* ps = part_draw + (long long)n_draw * cpg + (long long)j * cpg;
   float m = -INFINITY;
@@ -640,7 +699,8 @@ __global__ void heads_finalize_kernel(const float* part, int cpg, int M, const f
                                       int32_t* argmax, float* prob_scale, __nv_bfloat16* probs,
                                       long long ldp,
                                       int n_tiles, int bn, int V, const float* part_draw,
-                                      int n_draw, float* lse_draw, int row_blocks) {
+                                      int n_draw, float* lse_draw, int row_blocks,
+                                      dgi::LabelGather gl, int* status) {
   const int lane = threadIdx.x & 31;
   const int w = threadIdx.x >> 5;
   if ((int)blockIdx.x < row_blocks) {
@@ -650,7 +710,7 @@ __global__ void heads_finalize_kernel(const float* part, int cpg, int M, const f
                    probs, ldp, n_tiles, bn, V);
   } else {
     const int j = (blockIdx.x - row_blocks) * (blockDim.x >> 5) + w;
-    if (j < n_draw) finalize_draw(j, lane, part_draw, cpg, n_draw, lse_draw);
+    if (j < n_draw) finalize_draw(j, lane, part_draw, cpg, n_draw, lse_draw, gl, V, status);
   }
 }
 
@@ -697,7 +757,7 @@ cudaError_t denoise_heads(const uint16_t* h, int M, const uint16_t* draw_rows, i
                           const uint16_t* w, int V, int D, const float* inv_t,
                           const float* inv_t_draw, RowStats out, float* lse_draw,
                           float* prob_scale, uint16_t* probs, size_t probs_ld, void* ws,
-                          cudaStream_t st) {
+                          cudaStream_t st, const LabelGather* gather) {
   const int mt = heads_mt(M);
   const int groups = (M + mt * BM - 1) / (mt * BM);
   const int bn = heads_bn(n_draw);
@@ -720,6 +780,7 @@ cudaError_t denoise_heads(const uint16_t* h, int M, const uint16_t* draw_rows, i
   p.probs = reinterpret_cast<__nv_bfloat16*>(probs);
   p.ldp = (long long)probs_ld;
   p.status = status_ptr();
+  if (gather && n_draw > 0) p.gl = *gather;
   CUtensorMap ta, tb, td;
   if (!make_tmap_bf16_2d(&ta, h, D, M, (uint64_t)D * 2, BK, BM)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16_2d(&tb, w, D, V, (uint64_t)D * 2, BK, bn)) return cudaErrorInvalidValue;
@@ -744,7 +805,7 @@ cudaError_t denoise_heads(const uint16_t* h, int M, const uint16_t* draw_rows, i
   const int row_blocks = (M + 7) / 8, draw_blocks = (n_draw + 7) / 8;
   heads_finalize_kernel<<<row_blocks + draw_blocks, 256, 0, st>>>(
       p.part, p.cpg, M, inv_t, out.lse, out.entropy, out.maxz, out.argmax, prob_scale, p.probs,
-      p.ldp, p.n_tiles, bn, V, p.part_draw, n_draw, lse_draw, row_blocks);
+      p.ldp, p.n_tiles, bn, V, p.part_draw, n_draw, lse_draw, row_blocks, p.gl, p.status);
   return cudaGetLastError();
 }
 

@@ -47,14 +47,32 @@ struct RowStats {
   float* maxz;
   int32_t* argmax;
 };
+// Label gather of an lm-head pass: for every row g that is a slot row, the
+// logits z/T of its slot's labels (z - lse with sub_lse), taken from the
+// accumulators in the pass's epilogue and written at out[o * L + k].  R > 0:
+// row g < S R is draw g % R of slot g / R and o = g.  R == 0: slot s sits at
+// row slot_row[s] and o = s; row_slot [M] is scratch the call fills (the slot
+// of each row, or -1).  A label id outside [0, V) sets DG_DEV_BAD_LABEL and
+// gets -inf; a slot row outside [0, M) or shared by two slots sets
+// DG_DEV_BAD_INDEX.
+struct LabelGather {
+  const int32_t* label_ids;  // [S][L]
+  const int32_t* n_labels;   // [S] (clamped to [0, L])
+  const int32_t* slot_row;   // R == 0: [S]
+  int32_t* row_slot;         // R == 0: [M] scratch
+  float* out;                // null: no gather
+  int L, S, R;
+  int sub_lse;
+};
 size_t lmhead_ws_bytes(int M, int V);
 cudaError_t lmhead_stats(const uint16_t* h, int M, const uint16_t* w, int V, int D,
-                         const float* inv_t, RowStats out, void* ws, cudaStream_t st);
+                         const float* inv_t, RowStats out, void* ws, cudaStream_t st,
+                         const LabelGather* gather = nullptr);
 // lm-head statistics from e4m3 operands with per-row scales:
 // z[i, v] = (h8_i . w8_v) * h_scale[i] * w_scale[v] / T_i.  Workspace: lmhead_ws_bytes.
 cudaError_t lmhead_stats_fp8(const uint8_t* h8, const float* h_scale, int M, const uint8_t* w8,
                              const float* w_scale, int V, int D, const float* inv_t, RowStats out,
-                             void* ws, cudaStream_t st);
+                             void* ws, cudaStream_t st, const LabelGather* gather = nullptr);
 // Per-row e4m3 quantisation: scale = amax / 448 (1 for a zero row), q = e4m3(x / scale).
 cudaError_t quantize_rows_e4m3(const uint16_t* x, int rows, int cols, uint8_t* q, float* scale,
                                cudaStream_t st);
@@ -67,7 +85,8 @@ cudaError_t quantize_nvfp4(const uint16_t* x, int rows, int cols, uint8_t* codes
 // lm-head statistics of bf16 rows against NVFP4 weights: z = (h . (e2m1 * s)) * g / T.
 cudaError_t lmhead_stats_nvfp4(const uint16_t* h, int M, const uint8_t* codes,
                                const uint8_t* scales, const float* g, int V, int D,
-                               const float* inv_t, RowStats out, void* ws, cudaStream_t st);
+                               const float* inv_t, RowStats out, void* ws, cudaStream_t st,
+                               const LabelGather* gather = nullptr);
 size_t probs_embed8_ws_bytes(int M, int V, int D);
 cudaError_t probs_embed8(const uint8_t* p8, const float* p_scale, const float* row_scale, int M,
                          const uint8_t* e8t, const float* e_scale, int V, int D, float* out,
@@ -91,7 +110,7 @@ cudaError_t denoise_heads(const uint16_t* h, int M, const uint16_t* draw_rows, i
                           const uint16_t* w, int V, int D, const float* inv_t,
                           const float* inv_t_draw, RowStats out, float* lse_draw,
                           float* prob_scale, uint16_t* probs, size_t probs_ld, void* ws,
-                          cudaStream_t st);
+                          cudaStream_t st, const LabelGather* gather = nullptr);
 
 // ---- attention (attn.cu) ---------------------------------------------------
 struct AttnArgs {

@@ -353,11 +353,12 @@ __global__ void __launch_bounds__(1024) commit_kernel(int C, const float* entrop
       if ((peers & ((1u << lane) - 1u)) == 0) hist[d * nw + wid] = __popc(peers);
     }
     __syncthreads();
-    // digit totals, then the exclusive scan over (digit, warp)
-    if (i < 256) {
+    // digit totals, then the exclusive scan over (digit, warp); a block of fewer
+    // than 256 threads takes several digits a thread
+    for (int dg = i; dg < 256; dg += blockDim.x) {
       uint32_t t = 0;
-      for (int w = 0; w < nw; ++w) t += hist[i * nw + w];
-      dig_tot[i] = t;
+      for (int w = 0; w < nw; ++w) t += hist[dg * nw + w];
+      dig_tot[dg] = t;
     }
     __syncthreads();
     if (i < 32) {
@@ -383,11 +384,11 @@ __global__ void __launch_bounds__(1024) commit_kernel(int C, const float* entrop
       }
     }
     __syncthreads();
-    if (i < 256) {
-      uint32_t run = dig_tot[i];
+    for (int dg = i; dg < 256; dg += blockDim.x) {
+      uint32_t run = dig_tot[dg];
       for (int w = 0; w < nw; ++w) {
-        const uint32_t c = hist[i * nw + w];
-        hist[i * nw + w] = run;
+        const uint32_t c = hist[dg * nw + w];
+        hist[dg * nw + w] = run;
         run += c;
       }
     }
@@ -522,6 +523,8 @@ cudaError_t slot_noise(const uint16_t* h, int M, const uint16_t* e, int V, int D
 }
 
 // Label logits then the per-slot read (label tables of stride L <= 32 LPL).
+// rows == null: lp_draws already holds the label logits z/T, gathered by the
+// lm-head pass over the draw rows.
 template <int LPL>
 cudaError_t finish(const uint16_t* rows, const float* inv_t_rows, const float* lse_rows,
                    const uint16_t* w, int V, int D, const int32_t* label_ids,
@@ -529,11 +532,14 @@ cudaError_t finish(const uint16_t* rows, const float* inv_t_rows, const float* l
                    float* q_avg, float* h_slot, int32_t* chosen, float* lp_draws,
                    uint8_t* resampled, int32_t* n_reads, cudaStream_t st) {
   int* stp = status_ptr();
-  slot_dots_kernel<<<dim3(S * R, (L + 7) / 8), 256, 0, st>>>(
-      reinterpret_cast<const __nv_bfloat16*>(rows), inv_t_rows,
-      reinterpret_cast<const __nv_bfloat16*>(w), V, D, label_ids, n_labels, L, R, lp_draws, stp);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (rows != nullptr) {
+    slot_dots_kernel<<<dim3(S * R, (L + 7) / 8), 256, 0, st>>>(
+        reinterpret_cast<const __nv_bfloat16*>(rows), inv_t_rows,
+        reinterpret_cast<const __nv_bfloat16*>(w), V, D, label_ids, n_labels, L, R, lp_draws,
+        stp);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   slot_epilogue_kernel<LPL><<<S, 32, 0, st>>>(lse_rows, n_labels, L, R, samples, gate, q_avg,
                                               h_slot, chosen, lp_draws, resampled, n_reads, stp);
   return cudaGetLastError();

@@ -54,7 +54,7 @@ DP = ctypes.POINTER(Dims)
 
 _SIGS = {
     "dg_attn_decode": [DP, P, P, P, P, P, P, I, I, I, P, P, P, P, Z, P],
-    "dg_lmhead_logsoftmax_entropy": [DP, P, I, P, P, P, P, P, P, P, Z, P],
+    "dg_lmhead_logsoftmax_entropy": [DP, P, I, P, P, P, P, P, I, P, P, P, P, P, P, Z, P],
     "dg_slot_noise": [DP, P, I, P, P, P, P, I, I, U64, I, P, P, P, P],
     "dg_slot_finish": [DP, P, P, P, P, P, P, I, I, I, F, P, P, P, P, P, P, P],
     "dg_slot_read": [DP, P, I, P, P, P, P, P, P, P, I, U64, I, I, F, P, P, P, P, P, P, P, P, Z,
@@ -67,12 +67,14 @@ _SIGS = {
     "dg_quantize_rows_e4m3": [P, I, I, P, P, P],
     "dg_quantize_cols_e4m3": [P, I, I, P, P, P],
     "dg_selfcond_from_probs8": [DP, P, P, P, I, P, P, P, P, Z, P],
-    "dg_lmhead_logsoftmax_entropy_fp8": [DP, P, P, I, P, P, P, P, P, P, P, P, Z, P],
+    "dg_lmhead_logsoftmax_entropy_fp8": [DP, P, P, I, P, P, P, P, P, P, I, P, P, P, P, P, P, Z,
+                                         P],
     "dg_quantize_nvfp4": [P, I, I, P, P, P, P],
-    "dg_lmhead_logsoftmax_entropy_nvfp4": [DP, P, I, P, P, P, P, P, P, P, P, P, Z, P],
+    "dg_lmhead_logsoftmax_entropy_nvfp4": [DP, P, I, P, P, P, P, P, P, P, I, P, P, P, P, P, P,
+                                           Z, P],
     "dg_commit": [DP, P, P, P, P, P, P, P, P, P, P],
     "dg_selfcond_embed": [DP, P, I, P, P, P, P, P, P, Z, P],
-    "dg_denoise_heads": [DP, P, I, P, I, P, P, P, P, P, P, P, P, P, P, Z, P, Z, P],
+    "dg_denoise_heads": [DP, P, I, P, I, P, P, P, P, P, P, P, P, P, P, I, P, P, P, Z, P, Z, P],
     "dg_selfcond_from_probs": [DP, P, Z, P, I, P, P, P, Z, P],
     "dg_probs_ld": [I],
     "dg_ask_if_select": [P, I, P, P, P, P, P, I, I, P, P, P, P],
@@ -152,11 +154,13 @@ def dg_attn_decode(dims, q, kc, vc, kenc, venc, page_table, pages_per_req, n_pag
                                 _nbytes(workspace), _s(stream))
 
 
-def dg_lmhead_logsoftmax_entropy(dims, h, M, w, inv_t, lse, entropy, maxz, argmax, workspace,
-                                 stream=None):
+def dg_lmhead_logsoftmax_entropy(dims, h, M, w, inv_t, slot_row, label_ids, n_labels, S, lse,
+                                 entropy, maxz, argmax, label_lp, workspace, stream=None):
     return lib().dg_lmhead_logsoftmax_entropy(ctypes.byref(dims), _p(h), M, _p(w), _p(inv_t),
+                                              _p(slot_row), _p(label_ids), _p(n_labels), S,
                                               _p(lse), _p(entropy), _p(maxz), _p(argmax),
-                                              _p(workspace), _nbytes(workspace), _s(stream))
+                                              _p(label_lp), _p(workspace), _nbytes(workspace),
+                                              _s(stream))
 
 
 def dg_slot_noise(dims, h, M, e, inv_t, slot_row, slot_req, S, R, seed, step, rows_out,
@@ -229,24 +233,30 @@ def dg_selfcond_from_probs8(dims, p8, p_scale, row_scale, M, e8t, e_scale, out, 
                                          _nbytes(workspace), _s(stream))
 
 
-def dg_lmhead_logsoftmax_entropy_fp8(dims, h8, h_scale, M, w8, w_scale, inv_t, lse, entropy, maxz,
-                                     argmax, workspace, stream=None):
+def dg_lmhead_logsoftmax_entropy_fp8(dims, h8, h_scale, M, w8, w_scale, inv_t, slot_row,
+                                     label_ids, n_labels, S, lse, entropy, maxz, argmax, label_lp,
+                                     workspace, stream=None):
     return lib().dg_lmhead_logsoftmax_entropy_fp8(ctypes.byref(dims), _p(h8), _p(h_scale), M,
-                                                  _p(w8), _p(w_scale), _p(inv_t), _p(lse),
+                                                  _p(w8), _p(w_scale), _p(inv_t), _p(slot_row),
+                                                  _p(label_ids), _p(n_labels), S, _p(lse),
                                                   _p(entropy), _p(maxz), _p(argmax),
-                                                  _p(workspace), _nbytes(workspace), _s(stream))
+                                                  _p(label_lp), _p(workspace), _nbytes(workspace),
+                                                  _s(stream))
 
 
 def dg_quantize_nvfp4(x, rows, cols, codes, scales, g, stream=None):
     return lib().dg_quantize_nvfp4(_p(x), rows, cols, _p(codes), _p(scales), _p(g), _s(stream))
 
 
-def dg_lmhead_logsoftmax_entropy_nvfp4(dims, h, M, codes, scales, g, inv_t, lse, entropy, maxz,
-                                       argmax, workspace, stream=None):
+def dg_lmhead_logsoftmax_entropy_nvfp4(dims, h, M, codes, scales, g, inv_t, slot_row, label_ids,
+                                       n_labels, S, lse, entropy, maxz, argmax, label_lp,
+                                       workspace, stream=None):
     return lib().dg_lmhead_logsoftmax_entropy_nvfp4(ctypes.byref(dims), _p(h), M, _p(codes),
-                                                    _p(scales), _p(g), _p(inv_t), _p(lse),
+                                                    _p(scales), _p(g), _p(inv_t), _p(slot_row),
+                                                    _p(label_ids), _p(n_labels), S, _p(lse),
                                                     _p(entropy), _p(maxz), _p(argmax),
-                                                    _p(workspace), _nbytes(workspace), _s(stream))
+                                                    _p(label_lp), _p(workspace),
+                                                    _nbytes(workspace), _s(stream))
 
 
 def dg_commit(dims, entropy, argmax, cand, gamma, committed_state, token_state, commit, tokens,
@@ -263,11 +273,14 @@ def dg_selfcond_embed(dims, h, M, w, e, inv_t, lse, out, workspace, stream=None)
 
 
 def dg_denoise_heads(dims, h, M, draw_rows, n_draw, w, inv_t, inv_t_draw, lse, entropy, maxz,
-                     argmax, lse_draw, prob_scale, probs, probs_ld, workspace, stream=None):
+                     argmax, lse_draw, draw_label_ids, draw_n_labels, draw_R, draw_label_z,
+                     prob_scale, probs, probs_ld, workspace, stream=None):
     return lib().dg_denoise_heads(ctypes.byref(dims), _p(h), M, _p(draw_rows), n_draw, _p(w),
                                   _p(inv_t), _p(inv_t_draw), _p(lse), _p(entropy), _p(maxz),
-                                  _p(argmax), _p(lse_draw), _p(prob_scale), _p(probs), probs_ld,
-                                  _p(workspace), _nbytes(workspace), _s(stream))
+                                  _p(argmax), _p(lse_draw), _p(draw_label_ids),
+                                  _p(draw_n_labels), draw_R, _p(draw_label_z), _p(prob_scale),
+                                  _p(probs), probs_ld, _p(workspace), _nbytes(workspace),
+                                  _s(stream))
 
 
 def dg_selfcond_from_probs(dims, probs, probs_ld, prob_scale, M, e, out, workspace,

@@ -171,9 +171,10 @@ class TwoStageRead:
         self._noise(self.S2, self.slot_row2, self.slot_req2, st2, self.out2, 1, stream)
         dg._check(dg.dg_lmhead_logsoftmax_entropy(self.dims, self.draw_rows,
                                                   self.draw_rows.shape[0], self.w,
-                                                  self.inv_t_draw, self.lse_draw, self.ent_draw,
-                                                  self.maxz_draw, self.arg_draw, self.ws_lm,
-                                                  stream), "dg_lmhead_logsoftmax_entropy")
+                                                  self.inv_t_draw, None, None, None, 0,
+                                                  self.lse_draw, self.ent_draw, self.maxz_draw,
+                                                  self.arg_draw, None, self.ws_lm, stream),
+                  "dg_lmhead_logsoftmax_entropy")
         self._finish(self.S1, self.label_ids1, self.n_labels1, st1, self.out1, stream)
         dg._check(dg.dg_ask_if_select(self.out1["chosen"], self.S1, self.cond_slot,
                                       self.cond_value, self.q_owner, self.q_label_ids,
@@ -182,7 +183,8 @@ class TwoStageRead:
         self._finish(self.S2, self.label_ids2, self.n_labels2, st2, self.out2, stream)
         attn_kernels = 1 if dg.dg_workspace_bytes(self.dims, dg.DG_WS_ATTN, 0) <= 256 else 2
         # noise x 2, one W pass (stats + finalize), finish (label logits + epilogue) x 2,
-        # ask_if
+        # ask_if.  The finishes compute their label logits from the noised rows: the
+        # stage-2 labels are known only after stage 1 has been read.
         return attn_kernels + 2 + 2 + 4 + 1
 
     def decisions(self):
@@ -280,7 +282,8 @@ class ReadStep:
         if self.concurrent:
             main.wait_stream(attn_stream)
         attn_kernels = 1 if dg.dg_workspace_bytes(attn_dims, dg.DG_WS_ATTN, 0) <= 256 else 2
-        return attn_kernels + 5
+        # noise, the W pass (gathering the label logits) + finalize, slot epilogue
+        return attn_kernels + 4
 
     def check(self, stream=None):
         """Raise dg.DgDeviceError if a kernel of the enqueued reads set a status bit
@@ -361,22 +364,25 @@ class LmHead:
         if self.fp4:
             dg._check(dg.dg_lmhead_logsoftmax_entropy_nvfp4(d, self.h, self.M, self.codes,
                                                             self.scales, self.g, self.inv_t,
-                                                            self.lse, self.ent, self.maxz,
-                                                            self.argmax, self.ws, stream),
+                                                            None, None, None, 0, self.lse,
+                                                            self.ent, self.maxz, self.argmax,
+                                                            None, self.ws, stream),
                       "dg_lmhead_logsoftmax_entropy_nvfp4")
             return 2
         if not self.fp8:
             dg._check(dg.dg_lmhead_logsoftmax_entropy(d, self.h, self.M, self.w, self.inv_t,
-                                                      self.lse, self.ent, self.maxz, self.argmax,
-                                                      self.ws, stream),
+                                                      None, None, None, 0, self.lse, self.ent,
+                                                      self.maxz, self.argmax, None, self.ws,
+                                                      stream),
                       "dg_lmhead_logsoftmax_entropy")
             return 2
         dg._check(dg.dg_quantize_rows_e4m3(self.h, self.M, self.shape.D, self.h8, self.h_scale,
                                            stream), "dg_quantize_rows_e4m3")
         dg._check(dg.dg_lmhead_logsoftmax_entropy_fp8(d, self.h8, self.h_scale, self.M, self.w8,
-                                                      self.w_scale, self.inv_t, self.lse,
-                                                      self.ent, self.maxz, self.argmax, self.ws,
-                                                      stream), "dg_lmhead_logsoftmax_entropy_fp8")
+                                                      self.w_scale, self.inv_t, None, None, None,
+                                                      0, self.lse, self.ent, self.maxz,
+                                                      self.argmax, None, self.ws, stream),
+                  "dg_lmhead_logsoftmax_entropy_fp8")
         return 3
 
 

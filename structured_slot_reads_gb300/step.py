@@ -6,8 +6,9 @@ them; the library never does) and enqueues the library calls of one step:
   dg_attn_decode          decoder-mode attention over prompt KV + window
   dg_slot_noise           noised slot rows of the four reads
   dg_denoise_heads        one W pass: lse / entropy / argmax of every canvas row,
-                          the draw rows' lse, bf16 probabilities for self-cond
-  dg_slot_finish          label gather, renormalise, entropy gate, average
+                          the draw rows' lse and label logits (gathered from
+                          the accumulators), bf16 probabilities for self-cond
+  dg_slot_finish          renormalise over the labels, entropy gate, average
   dg_commit               entropy-ordered commit (state carried forward)
   dg_selfcond_from_probs  expected embedding softmax(z) . E from the probabilities
   dg_canvas_update        next step's canvas input rows
@@ -229,8 +230,9 @@ class DenoiseStep:
         if self.fused:
             return self._run_fused(step_idx, stream)
         self._attention(stream)
-        ck(dg.dg_lmhead_logsoftmax_entropy(d, self.h, self.M, self.w, self.inv_t, self.lse,
-                                           self.ent, self.maxz, self.argmax, self.ws_lm, stream),
+        ck(dg.dg_lmhead_logsoftmax_entropy(d, self.h, self.M, self.w, self.inv_t, None, None,
+                                           None, 0, self.lse, self.ent, self.maxz, self.argmax,
+                                           None, self.ws_lm, stream),
            "dg_lmhead_logsoftmax_entropy")
         if self.with_slots:
             self._slot_read(step_idx, stream)
@@ -277,11 +279,14 @@ class DenoiseStep:
             ck(dg.dg_slot_noise(d, self.h, self.M, self.e, self.inv_t, self.slot_row,
                                 self.slot_req, self.S, s.R, self.seed, step_idx, self.draw_rows,
                                 self.inv_t_draw, self.noise_tok, main), "dg_slot_noise")
-        ck(dg.dg_denoise_heads(d, self.h, self.M, self.draw_rows if self.n_draw else None,
-                               self.n_draw, self.w, self.inv_t, self.inv_t_draw, self.lse,
-                               self.ent, self.maxz, self.argmax, self.lse_draw, self.prob_scale,
-                               self.probs, self.probs_ld, self.ws_heads, main),
-           "dg_denoise_heads")
+        # the draws' label logits are gathered into lp_draws by the pass
+        nd = self.n_draw
+        ck(dg.dg_denoise_heads(d, self.h, self.M, self.draw_rows if nd else None, nd, self.w,
+                               self.inv_t, self.inv_t_draw, self.lse, self.ent, self.maxz,
+                               self.argmax, self.lse_draw, self.label_ids if nd else None,
+                               self.n_labels if nd else None, s.R,
+                               self.lp_draws if nd else None, self.prob_scale, self.probs,
+                               self.probs_ld, self.ws_heads, main), "dg_denoise_heads")
         side = main
         if self.concurrent:
             if self._side is None:
@@ -291,7 +296,8 @@ class DenoiseStep:
             side.wait_stream(main)
             self._selfcond(main)
         if self.n_draw:
-            ck(dg.dg_slot_finish(d, self.draw_rows, self.inv_t_draw, self.lse_draw, self.w,
+            # the label logits came out of the heads pass (rows = None)
+            ck(dg.dg_slot_finish(d, None, None, self.lse_draw, None,
                                  self.label_ids, self.n_labels, self.S, s.R, s.R, s.gate,
                                  self.q_avg, self.h_slot, self.chosen, self.lp_draws,
                                  self.resampled, self.n_reads, side), "dg_slot_finish")
@@ -315,18 +321,19 @@ class DenoiseStep:
         n = 1 + (1 if self._attn_splits() > 1 else 0)
         if self.fused:
             # ref + heads + finalize + commit + accum + reduce + update, and either
-            # noise + finish (label logits, slot epilogue) with the draws in the pass
-            # (their log-normalisers finalised with the canvas rows'), or a slot read
+            # noise + slot epilogue with the draws in the pass (their
+            # log-normalisers finalised with the canvas rows', their label logits
+            # gathered by the pass), or a slot read
             n += 3 + 1 + 2 + 1
             if self.n_draw:
-                n += 3
+                n += 2
             elif self.with_slots:
-                n += 5
+                n += 4
             return n
-        # stats + finalize, [noise + stats + finalize + label logits + slot epilogue],
-        # commit, probs + accum + reduce, update
+        # stats + finalize, [noise + stats + finalize + slot epilogue], commit,
+        # probs + accum + reduce, update
         n += 2
-        n += 5 if self.with_slots else 0
+        n += 4 if self.with_slots else 0
         n += 1 + 3 + 1
         return n
 

@@ -88,8 +88,9 @@ def test_workspace_sizes(lib):
 def test_compute_calls_validate_before_launch(lib):
     d = dg.make_dims(B=1, C=32, P_max=64, Hq=2, Hkv=1, d_head=64, W=8, d_model=128, V=1024)
     # null pointers
-    assert dg.dg_lmhead_logsoftmax_entropy(d, None, 4, None, None, None, None, None, None,
-                                           None, stream=0) == dg.DG_ERR_ARG
+    assert dg.dg_lmhead_logsoftmax_entropy(d, None, 4, None, None, None, None, None, 0, None,
+                                           None, None, None, None, None,
+                                           stream=0) == dg.DG_ERR_ARG
     assert dg.dg_attn_decode(d, None, None, None, None, None, None, 0, 0, 0, None, None, None,
                              None, stream=0) == dg.DG_ERR_ARG
     assert dg.dg_commit(d, None, None, None, None, None, None, None, None, None,
@@ -104,8 +105,8 @@ def test_compute_calls_validate_before_launch(lib):
     assert dg.dg_commit(dg.make_dims(B=1, C=2000), 16, 16, 16, 16, None, None, 16, 16, 16,
                         stream=0) == dg.DG_ERR_SHAPE
     # misaligned TMA operand
-    assert dg.dg_lmhead_logsoftmax_entropy(d, 18, 4, 16, 16, 16, 16, 16, 16, None,
-                                           stream=0) == dg.DG_ERR_ARG
+    assert dg.dg_lmhead_logsoftmax_entropy(d, 18, 4, 16, 16, None, None, None, 0, 16, 16, 16,
+                                           16, None, None, stream=0) == dg.DG_ERR_ARG
     # non power-of-two vocabulary for the noise map
     d1000 = dg.make_dims(d_model=128, V=1000)
     assert dg.dg_slot_noise(d1000, 16, 4, 16, 16, 16, 16, 1, 4, 0, 0, 16, 16, None,
@@ -114,8 +115,11 @@ def test_compute_calls_validate_before_launch(lib):
     assert dg.dg_slot_finish(d, 16, 16, 16, 16, 16, 16, 1, 4, 5, 0.1, 16, 16, 16, 16, 16, 16,
                              stream=0) == dg.DG_ERR_ARG
     # workspace missing
-    assert dg.dg_lmhead_logsoftmax_entropy(d, 16, 4, 16, 16, 16, 16, 16, 16, None,
-                                           stream=0) == dg.DG_ERR_WORKSPACE
+    assert dg.dg_lmhead_logsoftmax_entropy(d, 16, 4, 16, 16, None, None, None, 0, 16, 16, 16,
+                                           16, None, None, stream=0) == dg.DG_ERR_WORKSPACE
+    # a label gather: negative slot count, a missing slot table
+    assert dg.dg_lmhead_logsoftmax_entropy(d, 16, 4, 16, 16, None, None, None, -1, 16, 16, 16,
+                                           16, None, None, stream=0) == dg.DG_ERR_ARG
 
 
 def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
@@ -161,7 +165,7 @@ def test_step_runner_builds_on_host(lib, fused):
     w = torch.zeros((shp.V, shp.D), dtype=torch.bfloat16)
     st = DenoiseStep(shp, w, w, device="cpu", fused=fused)
     assert st.fused == fused
-    assert st.kernels_per_step() == (12 if fused else 14) - (0 if st._attn_splits() > 1 else 1)
+    assert st.kernels_per_step() == (11 if fused else 13) - (0 if st._attn_splits() > 1 else 1)
     if fused:
         assert st.probs.shape == (shp.C, dg.dg_probs_ld(shp.V)) and st.n_draw == 4
 
@@ -176,7 +180,7 @@ def test_batched_step_reads_slots_in_their_own_pass(lib):
     w = torch.zeros((shp.V, shp.D), dtype=torch.bfloat16)
     st = DenoiseStep(shp, w, w, device="cpu", fused=True)
     assert st.S == 8 and st.n_draw == 0 and not hasattr(st, "ws_sc")
-    assert st.kernels_per_step() == 14 - (0 if st._attn_splits() > 1 else 1)
+    assert st.kernels_per_step() == 13 - (0 if st._attn_splits() > 1 else 1)
 
 
 def test_two_stage_runner_builds_on_host(lib):
@@ -244,8 +248,8 @@ def test_heads_pass_wants_32_byte_aligned_probabilities(lib):
     """The probabilities are written with 256-bit stores."""
     d = dg.make_dims(d_model=128, V=1024)
     ld = dg.dg_probs_ld(1024)
-    args = lambda probs: (d, 32, 4, None, 0, 32, 32, None, 32, 32, 32, 32, None, 32,  # noqa: E731
-                          probs, ld, None)
+    args = lambda probs: (d, 32, 4, None, 0, 32, 32, None, 32, 32, 32, 32, None,  # noqa: E731
+                          None, None, 0, None, 32, probs, ld, None)
     assert dg.dg_denoise_heads(*args(48), stream=0) == dg.DG_ERR_ARG        # 16- not 32-aligned
     assert dg.dg_denoise_heads(*args(64), stream=0) == dg.DG_ERR_WORKSPACE  # alignment accepted
 

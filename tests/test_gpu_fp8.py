@@ -29,8 +29,8 @@ def _fp8_stats(q_h, s_h, q_w, s_w, inv_t, D, V):
     am = torch.empty(M, dtype=torch.int32, device="cuda")
     ws = torch.empty(dg.dg_workspace_bytes(d, dg.DG_WS_LMHEAD, M), dtype=torch.uint8,
                      device="cuda")
-    rc = dg.dg_lmhead_logsoftmax_entropy_fp8(d, q_h, s_h, M, q_w, s_w, dev(inv_t), lse, ent, mz,
-                                             am, ws)
+    rc = dg.dg_lmhead_logsoftmax_entropy_fp8(d, q_h, s_h, M, q_w, s_w, dev(inv_t), None, None,
+                                             None, 0, lse, ent, mz, am, None, ws)
     assert rc == dg.DG_OK, dg.strerror(rc)
     torch.cuda.synchronize()
     return host(lse), host(ent), host(mz), host(am)

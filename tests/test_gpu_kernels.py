@@ -31,7 +31,8 @@ def _run_lmhead(h, w, inv_t):
     arg = torch.empty(M, dtype=torch.int32, device="cuda")
     ws = torch.empty(dg.dg_workspace_bytes(d, dg.DG_WS_LMHEAD, M), dtype=torch.uint8, device="cuda")
     hd, wd, it = dev_bf16(h), dev_bf16(w), dev(inv_t)
-    rc = dg.dg_lmhead_logsoftmax_entropy(d, hd, M, wd, it, out[0], out[1], out[2], arg, ws)
+    rc = dg.dg_lmhead_logsoftmax_entropy(d, hd, M, wd, it, None, None, None, 0, out[0], out[1],
+                                         out[2], arg, None, ws)
     assert rc == dg.DG_OK, dg.strerror(rc)
     torch.cuda.synchronize()
     return [host(x) for x in out] + [host(arg)]
@@ -343,7 +344,7 @@ def _run_heads(h, draws, w, inv_t, inv_t_draw, with_probs=True):
     ws = torch.empty(dg.dg_workspace_bytes(d, dg.DG_WS_HEADS, M), dtype=torch.uint8, device="cuda")
     rc = dg.dg_denoise_heads(d, dev_bf16(h), M, dev_bf16(draws) if nd else None, nd, dev_bf16(w),
                              dev(inv_t), dev(inv_t_draw) if nd else None, lse, ent, maxz, arg,
-                             lse_d if nd else None, scale, probs, ld, ws)
+                             lse_d if nd else None, None, None, 0, None, scale, probs, ld, ws)
     assert rc == dg.DG_OK, dg.strerror(rc)
     torch.cuda.synchronize()
     return dict(lse=host(lse), ent=host(ent), maxz=host(maxz), arg=host(arg),

@@ -30,7 +30,8 @@ def _stats(h, codes, scales, g, inv_t, V, D):
     ws = torch.empty(dg.dg_workspace_bytes(d, dg.DG_WS_LMHEAD, M), dtype=torch.uint8,
                      device="cuda")
     rc = dg.dg_lmhead_logsoftmax_entropy_nvfp4(d, dev_bf16(h), M, codes, scales, g, dev(inv_t),
-                                               out[0], out[1], out[2], arg, ws)
+                                               None, None, None, 0, out[0], out[1], out[2], arg,
+                                               None, ws)
     assert rc == dg.DG_OK, dg.strerror(rc)
     torch.cuda.synchronize()
     return [host(x) for x in out] + [host(arg)]
@@ -41,6 +42,7 @@ def test_quantizer_bit_exact(V, D):
     w = inputs.normal_bf16((V, D), 1.0 / np.sqrt(D), 5 + V, 1)
     w[3, 64:80] = 0.0                         # a zero block
     w[7, :16] *= 40.0                          # a block far above the rest
+    w = inputs.to_bf16(w)                      # the operand both sides read
     codes, scales, g = _quantize(dev_bf16(w), V, D)
     torch.cuda.synchronize()
     oc, osc, og = oracle.quantize_nvfp4(w)

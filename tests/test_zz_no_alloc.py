@@ -27,7 +27,8 @@ def _with_workspace(d, h, M, w, it):
     lse, ent, mz, arg = _outs(M)
     ws = torch.empty(dg.dg_workspace_bytes(d, dg.DG_WS_LMHEAD, M), dtype=torch.uint8,
                      device="cuda")
-    assert dg.dg_lmhead_logsoftmax_entropy(d, h, M, w, it, lse, ent, mz, arg, ws) == dg.DG_OK
+    assert dg.dg_lmhead_logsoftmax_entropy(d, h, M, w, it, None, None, None, 0, lse, ent, mz, arg,
+                                           None, ws) == dg.DG_OK
     return lse, ent, mz, arg
 
 
