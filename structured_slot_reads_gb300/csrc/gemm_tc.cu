@@ -75,14 +75,21 @@ struct GemmParams {
   int* status;
 };
 
-template <int MT, int BN, int EXTRA = 0>
+// PK > 0 (NVFP4 B): a second, deeper ring of PK-byte stages holds the packed
+// codes and scales, so that their DRAM latency is hidden while the operand
+// ring holds only the A rows and the widened B tile.
+template <int MT, int BN, int PK = 0>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;   // one 128-row A tile of a K block
   static constexpr int A_STAGE = MT * A_BYTES;
   static constexpr int B_STAGE = BN * BK * 2;
-  static constexpr int STAGE_BYTES = A_STAGE + B_STAGE + EXTRA;  // EXTRA: packed B staging
-  static constexpr int NS_FIT = RING_BUDGET / STAGE_BYTES;
+  static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+  static constexpr int PK_BYTES = PK;
+  static constexpr int NS_FIT = PK == 0 ? RING_BUDGET / STAGE_BYTES
+                                : (3 * STAGE_BYTES + 4 * PK <= RING_BUDGET ? 3 : 2);
   static constexpr int NSTAGE = NS_FIT > 8 ? 8 : NS_FIT;
+  static constexpr int PK_FIT = PK == 0 ? 0 : (RING_BUDGET - NSTAGE * STAGE_BYTES) / PK;
+  static constexpr int PK_STAGES = PK_FIT > 8 ? 8 : PK_FIT;
   static constexpr int ACC_COLS = MT * BN;
   static constexpr int ACC_STAGES = (2 * ACC_COLS <= 512) ? 2 : 1;
   static constexpr int TMEM_NEED = ACC_STAGES * ACC_COLS;
@@ -94,18 +101,20 @@ struct Cfg {
   static constexpr int EPI_WARPS = 4 * MT;
   static constexpr int THREADS = (EPI_WARPS + 2) * 32;  // + producer, MMA issuer
   static constexpr int BAR_BYTES = 512;
-  static constexpr int SMEM_BYTES = 1024 + NSTAGE * STAGE_BYTES + BAR_BYTES;
+  static constexpr int SMEM_BYTES = 1024 + NSTAGE * STAGE_BYTES + PK_STAGES * PK + BAR_BYTES;
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
   static constexpr uint32_t IDESC_BMN = idesc_bf16_f32_bmn(BM, BN);
   static_assert(TMEM_NEED <= 512, "accumulators exceed tensor memory");
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(NSTAGE >= 2, "ring depth");
+  static_assert(PK == 0 || (PK_STAGES >= 2 && PK % 1024 == 0), "packed ring");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
 // NVFP4 B staging of one K block: BN rows x (32 code bytes + 4 scale bytes)
-constexpr int f4_extra(int bn) { return bn * 36; }
+constexpr int f4_pk_bytes(int bn) { return bn * 36; }
 constexpr int F4_CONV_WARPS = 8;   // warps widening the packed B tile to bf16
+constexpr int F4_EXTRA_WARPS = F4_CONV_WARPS + 1;   // + the packed-ring producer
 
 // Four bytes of e2m1 code pairs (the even element in the low nibble) as four
 // f16x2 words, by the hardware conversion (exact: every e2m1 value is an f16).
@@ -118,15 +127,17 @@ __device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t word, uint32_t (&h)[4])
 }
 
 template <int MT, int BN, int EPI>
-__global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32 * F4_CONV_WARPS : 0), 1)
+__global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32 * F4_EXTRA_WARPS : 0), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, GemmParams p) {
   constexpr bool F4 = EPI == EPI_STATS4;
-  using CF = Cfg<MT, BN, F4 ? f4_extra(BN) : 0>;
+  using CF = Cfg<MT, BN, F4 ? f4_pk_bytes(BN) : 0>;
   constexpr int NSTAGE = CF::NSTAGE;
+  constexpr int PK_STAGES = CF::PK_STAGES;
   constexpr int PRODUCER_WARP = CF::EPI_WARPS;
   constexpr int MMA_WARP = CF::EPI_WARPS + 1;
   constexpr int CONV0 = CF::EPI_WARPS + 2;   // STATS4: first converter warp
+  constexpr int PK_WARP = CONV0 + F4_CONV_WARPS;   // STATS4: packed-ring producer
   constexpr bool B_MN = EPI == EPI_ACCUM_MN;
   constexpr bool ACCUM = EPI == EPI_ACCUM || B_MN || EPI == EPI_ACCUM8;
   constexpr bool F8 = EPI == EPI_STATS8 || EPI == EPI_ACCUM8;
@@ -139,13 +150,16 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* stages = smem;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + NSTAGE * CF::STAGE_BYTES);
+  uint8_t* pk_ring = smem + NSTAGE * CF::STAGE_BYTES;   // STATS4: packed codes + scales
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(pk_ring + PK_STAGES * CF::PK_BYTES);
   uint64_t* empty_bar = full_bar + NSTAGE;
   uint64_t* tfull_bar = empty_bar + NSTAGE;
   uint64_t* tempty_bar = tfull_bar + CF::ACC_STAGES;
   uint64_t* drain_bar = tempty_bar + CF::ACC_STAGES;
   uint64_t* bready_bar = drain_bar + 1;   // STATS4: [NSTAGE] the widened B tile written
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bready_bar + (F4 ? NSTAGE : 0));
+  uint64_t* pkfull_bar = bready_bar + (F4 ? NSTAGE : 0);         // STATS4: [PK_STAGES]
+  uint64_t* pkempty_bar = pkfull_bar + PK_STAGES;                 // STATS4: [PK_STAGES]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pkempty_bar + PK_STAGES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -156,6 +170,10 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], 1);
       if (F4) mbar_init(&bready_bar[i], F4_CONV_WARPS);
+    }
+    for (int i = 0; i < PK_STAGES; ++i) {
+      mbar_init(&pkfull_bar[i], 1);
+      mbar_init(&pkempty_bar[i], F4_CONV_WARPS);
     }
     for (int a = 0; a < CF::ACC_STAGES; ++a) {
       mbar_init(&tfull_bar[a], 1);
@@ -220,18 +238,8 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
           }
           uint8_t* s_a = stages + stage * CF::STAGE_BYTES;
           uint8_t* s_b = s_a + CF::A_STAGE;
-          if (F4) {
-            // the packed codes and scales of rows [t BN, t BN + rows) of K block kb,
-            // contiguous in the K-block-major layout; the converter warps widen them
-            const int rows = min(BN, p.N - t * BN);
-            mbar_arrive_expect_tx(&full_bar[stage], CF::A_STAGE + rows * 36);
-            const long long r0 = (long long)kb * p.N + (long long)t * BN;
-            bulk_load(s_b + CF::B_STAGE, p.codes4 + r0 * 32, rows * 32, &full_bar[stage]);
-            bulk_load(s_b + CF::B_STAGE + BN * 32, p.scales4 + r0 * 4, rows * 4,
-                      &full_bar[stage]);
-          } else {
-            mbar_arrive_expect_tx(&full_bar[stage], CF::STAGE_BYTES);
-          }
+          // STATS4: the A rows only; the converter warps write the B tile
+          mbar_arrive_expect_tx(&full_bar[stage], F4 ? CF::A_STAGE : CF::STAGE_BYTES);
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt)
             tma_load_2d_hint(s_a + mt * CF::A_BYTES, &tmA, &full_bar[stage], kb * KB,
@@ -269,9 +277,9 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
         tc_fence_after();
         const uint32_t d_base = tmem_base + acc * CF::ACC_COLS;
         for (int kb = kb_begin; kb < kb_end; ++kb) {
-          // STATS4: the widened B tile (the converters saw the stage full first)
-          if (!mbar_wait(F4 ? &bready_bar[stage] : &full_bar[stage], phase, abort_flag,
-                         p.status)) {
+          // the A rows (and B, by TMA); STATS4: also the B tile the converters widened
+          if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.status) ||
+              (F4 && !mbar_wait(&bready_bar[stage], phase, abort_flag, p.status))) {
             ok = false;
             break;
           }
@@ -313,20 +321,23 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
       tc_commit(drain_bar);
       mbar_wait_drain(drain_bar, 0);
     }
-  } else if (F4 && warp >= CONV0) {
+  } else if (F4 && warp >= CONV0 && warp < PK_WARP) {
     // ---- STATS4 converter warps: each K block's packed B rows -> bf16 tile ----
     // (128-byte swizzled rows of 64 values, the layout TMA gives the other passes)
     const int ci = threadIdx.x - CONV0 * 32;
-    int stage = 0;
-    uint32_t phase = 0;
+    int stage = 0, ps = 0;
+    uint32_t phase = 0, pphase = 0;
     bool ok = has_work;
     for (int t = t_begin; t < t_end && ok; ++t) {
       const int rows = min(BN, p.N - t * BN);
       for (int kb = kb_begin; kb < kb_end; ++kb) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&full_bar[stage], phase, abort_flag, p.status));
+        // the packed rows have landed and the MMAs are done with this B slot
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&pkfull_bar[ps], pphase, abort_flag, p.status) &&
+                            mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.status));
         if (!ok) break;
         uint8_t* s_b = stages + stage * CF::STAGE_BYTES + CF::A_STAGE;
-        const uint8_t* s_c = s_b + CF::B_STAGE;
+        const uint8_t* s_c = pk_ring + ps * CF::PK_BYTES;
         const uint8_t* s_s = s_c + BN * 32;
         for (int r = ci; r < BN; r += 32 * F4_CONV_WARPS) {
           uint8_t* dst = s_b + r * 128;
@@ -367,11 +378,50 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
         }
         fence_proxy_async_smem();   // generic writes -> the MMA's operand reads
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bready_bar[stage]);
+        if (lane == 0) {
+          mbar_arrive(&bready_bar[stage]);
+          mbar_arrive(&pkempty_bar[ps]);
+        }
         if (++stage == NSTAGE) {
           stage = 0;
           phase ^= 1u;
         }
+        if (++ps == PK_STAGES) {
+          ps = 0;
+          pphase ^= 1u;
+        }
+      }
+    }
+  } else if (F4 && warp == PK_WARP) {
+    // ---- STATS4 packed-ring producer: codes and scales of each K block's B rows,
+    // contiguous in the K-block-major layout, up to PK_STAGES blocks ahead ----
+    if (lane == 0 && has_work) {
+      int ps = 0;
+      uint32_t pphase = 0, issued_mask = 0, last_phase = 0;
+      bool ok = true;
+      for (int t = t_begin; t < t_end && ok; ++t) {
+        const int rows = min(BN, p.N - t * BN);
+        for (int kb = kb_begin; kb < kb_end; ++kb) {
+          if (!mbar_wait(&pkempty_bar[ps], pphase ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* dst = pk_ring + ps * CF::PK_BYTES;
+          mbar_arrive_expect_tx(&pkfull_bar[ps], rows * 36);
+          const long long r0 = (long long)kb * p.N + (long long)t * BN;
+          bulk_load(dst, p.codes4 + r0 * 32, rows * 32, &pkfull_bar[ps]);
+          bulk_load(dst + BN * 32, p.scales4 + r0 * 4, rows * 4, &pkfull_bar[ps]);
+          issued_mask |= 1u << ps;
+          last_phase = (last_phase & ~(1u << ps)) | (pphase << ps);
+          if (++ps == PK_STAGES) {
+            ps = 0;
+            pphase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {  // let every copy already issued land before the CTA exits
+        for (int q = 0; q < PK_STAGES; ++q)
+          if (issued_mask & (1u << q)) mbar_wait_drain(&pkfull_bar[q], (last_phase >> q) & 1u);
       }
     }
   } else {
@@ -807,7 +857,7 @@ cudaError_t run_stats_fp8(const uint8_t* h8, const float* h_scale, int M, const 
 // applied to the accumulators.
 template <int MT>
 cudaError_t launch_stats4(const CUtensorMap& ta, const GemmParams& p, int grid, cudaStream_t st) {
-  using CF = Cfg<MT, STATS_BN, f4_extra(STATS_BN)>;
+  using CF = Cfg<MT, STATS_BN, f4_pk_bytes(STATS_BN)>;
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<MT, STATS_BN, EPI_STATS4>,
@@ -817,7 +867,7 @@ cudaError_t launch_stats4(const CUtensorMap& ta, const GemmParams& p, int grid, 
     attr_done = true;
   }
   gemm_tc_kernel<MT, STATS_BN, EPI_STATS4>
-      <<<grid, CF::THREADS + 32 * F4_CONV_WARPS, CF::SMEM_BYTES, st>>>(ta, ta, p);
+      <<<grid, CF::THREADS + 32 * F4_EXTRA_WARPS, CF::SMEM_BYTES, st>>>(ta, ta, p);
   return cudaGetLastError();
 }
 

@@ -143,6 +143,52 @@ __global__ void __launch_bounds__(REF_N * REF_KSPLIT * 32)
   }
 }
 
+// The same reference for many rows (batched canvases): one warp per row reads
+// the row once and takes all REF_N dot products against W's first REF_N rows
+// (which stay in L1), where the kernel above would read each row REF_N times.
+constexpr int REF_ROWS_MIN = 1024;   // rows from which the warp-per-row form is used
+__global__ void __launch_bounds__(256)
+    ref_rows_kernel(const __nv_bfloat16* h, const __nv_bfloat16* w, const float* inv_t, int M,
+                    int V, int D, float* ref) {
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (row >= M) return;
+  const uint4* x = reinterpret_cast<const uint4*>(h + (long long)row * D);
+  const int n16 = D / 8;
+  const int nu = min(REF_N, V);
+  float acc[REF_N];
+#pragma unroll
+  for (int u = 0; u < REF_N; ++u) acc[u] = 0.f;
+#pragma unroll 2
+  for (int i = lane; i < n16; i += 32) {
+    const uint4 a = x[i];
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    float2 fa[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) fa[q] = __bfloat1622float2(a2[q]);
+#pragma unroll
+    for (int u = 0; u < REF_N; ++u) {
+      if (u >= nu) break;
+      const uint4 b = __ldg(reinterpret_cast<const uint4*>(w + (long long)u * D) + i);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 fb = __bfloat1622float2(b2[q]);
+        acc[u] = fmaf(fa[q].x, fb.x, acc[u]);
+        acc[u] = fmaf(fa[q].y, fb.y, acc[u]);
+      }
+    }
+  }
+  float m = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < REF_N; ++u) {
+    float a = acc[u];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+    if (u < nu) m = fmaxf(m, a);
+  }
+  if (lane == 0) ref[row] = rintf((m * inv_t[row] * LOG2E + REF_HEADROOM) * 256.f) * (1.f / 256.f);
+}
+
 template <int MT, int BN, bool DRAWS>
 struct HCfg {
   static constexpr int A_BYTES = BM * BK * 2;             // one 128-row canvas tile
@@ -790,8 +836,13 @@ cudaError_t denoise_heads(const uint16_t* h, int M, const uint16_t* draw_rows, i
   } else {
     td = tb;  // unused
   }
-  ref_kernel<<<M, REF_N * REF_KSPLIT * 32, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(h),
-                                reinterpret_cast<const __nv_bfloat16*>(w), inv_t, M, V, D, ref);
+  if (M >= REF_ROWS_MIN)
+    ref_rows_kernel<<<(M + 7) / 8, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(h),
+                                                reinterpret_cast<const __nv_bfloat16*>(w), inv_t,
+                                                M, V, D, ref);
+  else
+    ref_kernel<<<M, REF_N * REF_KSPLIT * 32, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(h),
+                                  reinterpret_cast<const __nv_bfloat16*>(w), inv_t, M, V, D, ref);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int grid = groups * p.cpg;

@@ -355,7 +355,9 @@ def _run_heads(h, draws, w, inv_t, inv_t_draw, with_probs=True):
                                       (300, 12, 2048, 128), (64, 0, 4096, 256), (1, 16, 1024, 128),
                                       (200, 0, 5000, 256),
                                       # several 256-row groups, ragged vocabularies
-                                      (520, 0, 4000, 128), (384, 16, 2504, 192)])
+                                      (520, 0, 4000, 128), (384, 16, 2504, 192),
+                                      # batched canvases: the warp-per-row reference
+                                      (1100, 8, 2048, 128)])
 def test_denoise_heads_fused_pass(M, nd, V, D):
     h, w, e, inv_t = _lm_inputs(M, V, D, seed=31 + M)
     draws = inputs.hidden(nd, D, 99) if nd else None
