@@ -113,8 +113,10 @@ struct Cfg {
 
 // NVFP4 B staging of one K block: BN rows x (32 code bytes + 4 scale bytes)
 constexpr int f4_pk_bytes(int bn) { return bn * 36; }
-constexpr int F4_CONV_WARPS = 8;   // warps widening the packed B tile to bf16
-constexpr int F4_EXTRA_WARPS = F4_CONV_WARPS + 1;   // + the packed-ring producer
+// Warps widening the packed B tile to bf16 (more where the block has fewer
+// epilogue warps), plus the packed-ring producer.
+constexpr int f4_conv_warps(int mt) { return mt == 1 ? 16 : 8; }
+constexpr int f4_extra_warps(int mt) { return f4_conv_warps(mt) + 1; }
 
 // Four bytes of e2m1 code pairs (the even element in the low nibble) as four
 // f16x2 words, by the hardware conversion (exact: every e2m1 value is an f16).
@@ -127,7 +129,7 @@ __device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t word, uint32_t (&h)[4])
 }
 
 template <int MT, int BN, int EPI>
-__global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32 * F4_EXTRA_WARPS : 0), 1)
+__global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32 * f4_extra_warps(MT) : 0), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, GemmParams p) {
   constexpr bool F4 = EPI == EPI_STATS4;
@@ -137,7 +139,8 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
   constexpr int PRODUCER_WARP = CF::EPI_WARPS;
   constexpr int MMA_WARP = CF::EPI_WARPS + 1;
   constexpr int CONV0 = CF::EPI_WARPS + 2;   // STATS4: first converter warp
-  constexpr int PK_WARP = CONV0 + F4_CONV_WARPS;   // STATS4: packed-ring producer
+  constexpr int CONV_WARPS = f4_conv_warps(MT);
+  constexpr int PK_WARP = CONV0 + CONV_WARPS;   // STATS4: packed-ring producer
   constexpr bool B_MN = EPI == EPI_ACCUM_MN;
   constexpr bool ACCUM = EPI == EPI_ACCUM || B_MN || EPI == EPI_ACCUM8;
   constexpr bool F8 = EPI == EPI_STATS8 || EPI == EPI_ACCUM8;
@@ -169,11 +172,11 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
     for (int i = 0; i < NSTAGE; ++i) {
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], 1);
-      if (F4) mbar_init(&bready_bar[i], F4_CONV_WARPS);
+      if (F4) mbar_init(&bready_bar[i], CONV_WARPS);
     }
     for (int i = 0; i < PK_STAGES; ++i) {
       mbar_init(&pkfull_bar[i], 1);
-      mbar_init(&pkempty_bar[i], F4_CONV_WARPS);
+      mbar_init(&pkempty_bar[i], CONV_WARPS);
     }
     for (int a = 0; a < CF::ACC_STAGES; ++a) {
       mbar_init(&tfull_bar[a], 1);
@@ -339,26 +342,29 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
         uint8_t* s_b = stages + stage * CF::STAGE_BYTES + CF::A_STAGE;
         const uint8_t* s_c = pk_ring + ps * CF::PK_BYTES;
         const uint8_t* s_s = s_c + BN * 32;
-        for (int r = ci; r < BN; r += 32 * F4_CONV_WARPS) {
+        // unit u = half hf of row r: elements [32 hf, 32 hf + 32), i.e. 16 code
+        // bytes, 2 block scales and 16-byte chunks 4 hf .. 4 hf + 3 of the row
+        for (int u = ci; u < 2 * BN; u += 32 * CONV_WARPS) {
+          const int r = u >> 1, hf = u & 1;
           uint8_t* dst = s_b + r * 128;
           if (r >= rows) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-              *reinterpret_cast<uint4*>(dst + ((c ^ (r & 7)) * 16)) = make_uint4(0, 0, 0, 0);
+            for (int j = 0; j < 4; ++j)
+              *reinterpret_cast<uint4*>(dst + (((4 * hf + j) ^ (r & 7)) * 16)) =
+                  make_uint4(0, 0, 0, 0);
             continue;
           }
-          const uint4 c0 = *reinterpret_cast<const uint4*>(s_c + r * 32);
-          const uint4 c1 = *reinterpret_cast<const uint4*>(s_c + r * 32 + 16);
-          const uint32_t sw = *reinterpret_cast<const uint32_t*>(s_s + r * 4);
-          const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          const uint4 cc = *reinterpret_cast<const uint4*>(s_c + r * 32 + hf * 16);
+          const uint32_t sw = *reinterpret_cast<const uint16_t*>(s_s + r * 4 + hf * 2);
+          const uint32_t cw[4] = {cc.x, cc.y, cc.z, cc.w};
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int q = 0; q < 2; ++q) {
             const __half_raw hr =
                 __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)((sw >> (8 * q)) & 0xFF), __NV_E4M3);
             const __half2 s2 = __halves2half2(__half(hr), __half(hr));
-            // 16 elements of scale q: code words 2q, 2q+1 -> 16-byte chunks 2q, 2q+1.
-            // e2m1 times an e4m3 scale has at most 6 significant bits and lies in
-            // [2^-10, 2688] (or is 0), so the f16 product and the bf16 result are exact.
+            // 16 elements of one block scale: code words 2q, 2q+1.  e2m1 times an
+            // e4m3 scale has at most 6 significant bits and lies in [2^-10, 2688]
+            // (or is 0), so the f16 product and the bf16 result are exact.
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               uint32_t f16[4], o[4];
@@ -370,7 +376,7 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
                 const __nv_bfloat162 v = __floats2bfloat162_rn(f.x, f.y);
                 o[k] = *reinterpret_cast<const uint32_t*>(&v);
               }
-              const int c = 2 * q + h;
+              const int c = 4 * hf + 2 * q + h;
               *reinterpret_cast<uint4*>(dst + ((c ^ (r & 7)) * 16)) =
                   make_uint4(o[0], o[1], o[2], o[3]);
             }
@@ -638,6 +644,439 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
   if (warp == MMA_WARP) tmem_dealloc(tmem_base, CF::TMEM_COLS);
 }
 
+// ---------------------------------------------------------------------------
+// Skinny statistics pass (M <= 16 rows: the slot reads' draw rows) with the
+// operands swapped: A = a 128-row slice of the vocabulary tile (streamed), B =
+// the M rows, resident in shared memory for the whole pass (N = 16, rows past M
+// zero).  Per K block only W (or its NVFP4 codes and scales) streams; the MMAs
+// are 16 columns wide instead of 128 rows tall (most of them padding); the
+// accumulator has the vocabulary on the TMEM lanes, so each epilogue thread
+// owns one vocabulary row and keeps the online statistics of all 16 columns,
+// merged over lanes and warps once, at the end.  The partial statistics leave
+// in the planes of the STATS epilogue, so stats_finalize_kernel merges them.
+// ---------------------------------------------------------------------------
+constexpr int SK_N = 16;                    // rows of B (the MMAs' N)
+constexpr int SK_BN = 256;                  // vocabulary rows per tile: two M = 128 MMAs
+constexpr int SK_W_BYTES = SK_BN * BK * 2;  // a W tile of one K block (32 KB)
+constexpr int SK_B_BLOCK = SK_N * BK * 2;   // the rows' 64-column block (2 KB)
+constexpr int SK_MAX_KB = 48;               // resident rows for d_model up to 3072
+constexpr int SK_EPI_WARPS = 4;
+constexpr int SK_CONV_WARPS = 6;     // 12 warps in all: three per SM sub-partition
+constexpr int SK_GBITS = 64;                // label-gather chunk bitmap words
+
+template <bool F4>
+struct SkCfg {
+  static constexpr int B_BYTES = SK_MAX_KB * SK_B_BLOCK;   // 96 KB
+  static constexpr int NW = F4 ? 3 : 4;                    // W tiles in flight
+  static constexpr int NP = F4 ? 3 : 0;                    // packed blocks in flight
+  static constexpr int PK = F4 ? f4_pk_bytes(SK_BN) : 0;
+  static constexpr int BAR_BYTES = 512;
+  static constexpr int SMEM_BYTES = 1024 + B_BYTES + NW * SK_W_BYTES + NP * PK + BAR_BYTES;
+  static constexpr int PRODUCER = SK_EPI_WARPS;            // rows, then W (or the packed ring)
+  static constexpr int MMA = SK_EPI_WARPS + 1;
+  static constexpr int CONV0 = SK_EPI_WARPS + 2;           // F4: converter warps
+  static constexpr int THREADS = (SK_EPI_WARPS + 2 + (F4 ? SK_CONV_WARPS : 0)) * 32;
+  static constexpr int TMEM_COLS = 64;                     // 2 stages x 2 halves x 16 columns
+  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, SK_N);
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+  static_assert(SK_EPI_WARPS == 4, "one epilogue warp per TMEM lane quarter");
+};
+
+__device__ __forceinline__ void sk_epi_bar() {
+  asm volatile("bar.sync 1, %0;" ::"r"(SK_EPI_WARPS * 32) : "memory");
+}
+
+template <bool F4>
+__global__ void __launch_bounds__(SkCfg<F4>::THREADS, 1)
+    skinny_stats_kernel(const __grid_constant__ CUtensorMap tmH,
+                        const __grid_constant__ CUtensorMap tmW, GemmParams p) {
+  using CF = SkCfg<F4>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* bres = smem;                              // [K blocks][16 rows x 128 B]
+  uint8_t* wring = bres + CF::B_BYTES;               // [NW][SK_BN rows x 128 B]
+  uint8_t* pring = wring + CF::NW * SK_W_BYTES;      // F4: [NP][codes, scales]
+  uint64_t* wfull = reinterpret_cast<uint64_t*>(pring + CF::NP * CF::PK);
+  uint64_t* wempty = wfull + CF::NW;
+  uint64_t* pfull = wempty + CF::NW;
+  uint64_t* pempty = pfull + CF::NP;
+  uint64_t* tfull = pempty + CF::NP;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* bres_bar = tempty + 2;
+  uint64_t* drain_bar = bres_bar + 1;
+  uint32_t* gbits = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  uint32_t* tmem_slot = gbits + SK_GBITS;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* sscale = reinterpret_cast<float*>(tmem_slot + 2);   // [16] 1/T of each row, log2 units
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < CF::NW; ++i) {
+      mbar_init(&wfull[i], F4 ? SK_CONV_WARPS : 1);
+      mbar_init(&wempty[i], 1);
+    }
+    for (int i = 0; i < CF::NP; ++i) {
+      mbar_init(&pfull[i], 1);
+      mbar_init(&pempty[i], SK_CONV_WARPS);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], SK_EPI_WARPS);
+    }
+    mbar_init(bres_bar, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == CF::MMA) {
+    tmem_alloc(tmem_slot, CF::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == CF::PRODUCER && lane == 0) {
+    prefetch_tmap(&tmH);
+    if (!F4) prefetch_tmap(&tmW);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int total_kb = (p.K + BK - 1) / BK;
+  const int gn = blockIdx.x;
+  const int t_begin = (int)((long long)gn * p.n_tiles / p.cpg);
+  const int t_end = (int)((long long)(gn + 1) * p.n_tiles / p.cpg);
+  const bool has_work = t_end > t_begin;
+
+  if (warp == CF::PRODUCER) {
+    if (lane == 0 && has_work) {
+      // the rows, once: every 64-column block of rows [0, 16) (rows >= M read as 0)
+      mbar_arrive_expect_tx(bres_bar, total_kb * SK_B_BLOCK);
+      for (int kb = 0; kb < total_kb; ++kb)
+        tma_load_2d(bres + kb * SK_B_BLOCK, &tmH, bres_bar, kb * BK, 0);
+      const uint64_t pol = policy_evict_first();
+      int st = 0;
+      uint32_t ph = 0, issued = 0, last = 0;
+      bool ok = true;
+      constexpr int NR = F4 ? CF::NP : CF::NW;
+      uint64_t* ring_full = F4 ? pfull : wfull;
+      uint64_t* ring_empty = F4 ? pempty : wempty;
+      for (int t = t_begin; t < t_end && ok; ++t) {
+        const int rows = min(SK_BN, p.N - t * SK_BN);
+        for (int kb = 0; kb < total_kb; ++kb) {
+          if (!mbar_wait(&ring_empty[st], ph ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          if (F4) {
+            uint8_t* dst = pring + st * CF::PK;
+            mbar_arrive_expect_tx(&pfull[st], rows * 36);
+            const long long r0 = (long long)kb * p.N + (long long)t * SK_BN;
+            bulk_load(dst, p.codes4 + r0 * 32, rows * 32, &pfull[st]);
+            bulk_load(dst + SK_BN * 32, p.scales4 + r0 * 4, rows * 4, &pfull[st]);
+          } else {
+            mbar_arrive_expect_tx(&wfull[st], SK_W_BYTES);
+            tma_load_2d_hint(wring + st * SK_W_BYTES, &tmW, &wfull[st], kb * BK, t * SK_BN, pol);
+          }
+          issued |= 1u << st;
+          last = (last & ~(1u << st)) | (ph << st);
+          if (++st == NR) {
+            st = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < NR; ++s)
+          if (issued & (1u << s)) mbar_wait_drain(&ring_full[s], (last >> s) & 1u);
+      }
+      mbar_wait_drain(bres_bar, 0);
+    }
+  } else if (warp == CF::MMA) {
+    if (lane == 0 && has_work) {
+      int ws = 0, acc = 0;
+      uint32_t wph = 0, aph = 0;
+      bool ok = mbar_wait(bres_bar, 0, abort_flag, p.status);
+      for (int t = t_begin; t < t_end && ok; ++t) {
+        if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+        for (int kb = 0; kb < total_kb; ++kb) {
+          if (!mbar_wait(&wfull[ws], wph, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t w_addr = smem_u32(wring + ws * SK_W_BYTES);
+          const uint32_t b_addr = smem_u32(bres + kb * SK_B_BLOCK);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t bdesc = sw128_kmajor_desc(b_addr + kk * 32);
+#pragma unroll
+            for (int half = 0; half < 2; ++half)
+              tc_mma_f16(tmem_base + acc * 32 + half * SK_N,
+                         sw128_kmajor_desc(w_addr + half * (BM * 128) + kk * 32), bdesc, CF::IDESC,
+                         (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(&wempty[ws]);
+          if (++ws == CF::NW) {
+            ws = 0;
+            wph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          aph ^= 1u;
+        }
+      }
+      tc_commit(drain_bar);
+      mbar_wait_drain(drain_bar, 0);
+    }
+  } else if (F4 && warp >= CF::CONV0) {
+    // NVFP4: widen each K block's packed rows into the W ring (as in the GEMM)
+    const int ci = threadIdx.x - CF::CONV0 * 32;
+    int ws = 0, ps = 0;
+    uint32_t wph = 0, pph = 0;
+    bool ok = has_work;
+    for (int t = t_begin; t < t_end && ok; ++t) {
+      const int rows = min(SK_BN, p.N - t * SK_BN);
+      for (int kb = 0; kb < total_kb; ++kb) {
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&pfull[ps], pph, abort_flag, p.status) &&
+                            mbar_wait(&wempty[ws], wph ^ 1u, abort_flag, p.status));
+        if (!ok) break;
+        uint8_t* s_b = wring + ws * SK_W_BYTES;
+        const uint8_t* s_c = pring + ps * CF::PK;
+        const uint8_t* s_s = s_c + SK_BN * 32;
+        for (int u = ci; u < 2 * SK_BN; u += 32 * SK_CONV_WARPS) {
+          const int r = u >> 1, hf = u & 1;
+          uint8_t* dst = s_b + r * 128;
+          if (r >= rows) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              *reinterpret_cast<uint4*>(dst + (((4 * hf + j) ^ (r & 7)) * 16)) =
+                  make_uint4(0, 0, 0, 0);
+            continue;
+          }
+          const uint4 cc = *reinterpret_cast<const uint4*>(s_c + r * 32 + hf * 16);
+          const uint32_t sw = *reinterpret_cast<const uint16_t*>(s_s + r * 4 + hf * 2);
+          const uint32_t cw[4] = {cc.x, cc.y, cc.z, cc.w};
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const __half_raw hr =
+                __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)((sw >> (8 * q)) & 0xFF), __NV_E4M3);
+            const __half2 s2 = __halves2half2(__half(hr), __half(hr));
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint32_t f16[4], o[4];
+              e2m1x8_to_f16x2(cw[2 * q + h], f16);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float2 f =
+                    __half22float2(__hmul2(*reinterpret_cast<const __half2*>(&f16[k]), s2));
+                const __nv_bfloat162 v = __floats2bfloat162_rn(f.x, f.y);
+                o[k] = *reinterpret_cast<const uint32_t*>(&v);
+              }
+              const int c = 4 * hf + 2 * q + h;
+              *reinterpret_cast<uint4*>(dst + ((c ^ (r & 7)) * 16)) =
+                  make_uint4(o[0], o[1], o[2], o[3]);
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&wfull[ws]);
+          mbar_arrive(&pempty[ps]);
+        }
+        if (++ws == CF::NW) {
+          ws = 0;
+          wph ^= 1u;
+        }
+        if (++ps == CF::NP) {
+          ps = 0;
+          pph ^= 1u;
+        }
+      }
+    }
+  } else if (warp < SK_EPI_WARPS) {
+    // ---- epilogue: lane = vocabulary row of a 128-row half, 16 columns = rows ----
+    const int q = warp;
+    const int M = p.M;
+    const float gs = F4 ? __ldg(p.gscale) : 1.f;
+    float m[SK_N], s[SK_N], tt[SK_N], best[SK_N];
+    int bidx[SK_N];
+#pragma unroll
+    for (int j = 0; j < SK_N; ++j) {
+      m[j] = -INFINITY;
+      s[j] = 0.f;
+      tt[j] = 0.f;
+      best[j] = -INFINITY;
+      bidx[j] = 0x7fffffff;
+    }
+    if (threadIdx.x < SK_N) sscale[threadIdx.x] = threadIdx.x < M ? __ldg(p.inv_t + threadIdx.x) * LOG2E : 0.f;
+    sk_epi_bar();
+    // label gather: one bit per 32 vocabulary rows of this CTA's range holding a
+    // label of one of the rows (aliased modulo SK_GBITS * 32 chunks)
+    const bool gat = p.gl.out != nullptr && has_work;
+    const int g_lo = t_begin * SK_BN;
+    if (gat) {
+      for (int i = threadIdx.x; i < SK_GBITS; i += SK_EPI_WARPS * 32) gbits[i] = 0;
+      sk_epi_bar();
+      const int hi = min(t_end * SK_BN, p.N);
+      for (int i = threadIdx.x; i < M * p.gl.L; i += SK_EPI_WARPS * 32) {
+        const int j = i / p.gl.L, k = i % p.gl.L;
+        const int sl = p.gl.R > 0 ? (j < p.gl.S * p.gl.R ? j / p.gl.R : -1) : p.gl.row_slot[j];
+        if (sl < 0 || k >= min(max(__ldg(p.gl.n_labels + sl), 0), p.gl.L)) continue;
+        const int id = __ldg(p.gl.label_ids + (long long)sl * p.gl.L + k);
+        if (id >= g_lo && id < hi) {
+          const int c = ((id - g_lo) >> 5) & (SK_GBITS * 32 - 1);
+          atomicOr(gbits + (c >> 5), 1u << (c & 31));
+        }
+      }
+      sk_epi_bar();
+    }
+    int acc = 0;
+    uint32_t aph = 0;
+    for (int t = t_begin; t < t_end; ++t) {
+      if (!mbar_wait(&tfull[acc], aph, abort_flag, p.status)) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        uint32_t r[SK_N];
+        __syncwarp();
+        tmem_ld_32x32b_x16(tmem_base + ((uint32_t)(q * 32) << 16) + acc * 32 + half * SK_N, r);
+        tmem_ld_wait();
+        const int v0 = t * SK_BN + half * BM + q * 32;   // this warp's first vocabulary row
+        const int v = v0 + lane;
+        if (v < p.N) {
+#pragma unroll
+          for (int j = 0; j < SK_N; ++j) {
+            if (j >= M) break;
+            const float a = __uint_as_float(r[j]) * gs;
+            if (a > best[j]) {   // rows ascend, so the first occurrence is the lowest id
+              best[j] = a;
+              bidx[j] = v;
+            }
+            const float x = a * sscale[j];
+            const float mn = fmaxf(m[j], x);
+            const float fo = ex2(m[j] - mn), fx = ex2(x - mn);
+            s[j] = fmaf(s[j], fo, fx);
+            tt[j] = fmaf(tt[j], fo, fx * x);
+            m[j] = mn;
+          }
+        }
+        if (gat) {
+          const int c = ((v0 - g_lo) >> 5) & (SK_GBITS * 32 - 1);
+          if ((gbits[c >> 5] >> (c & 31)) & 1u) {
+            for (int j = 0; j < M && v < p.N; ++j) {
+              int sl, o;
+              if (p.gl.R > 0) {
+                sl = j < p.gl.S * p.gl.R ? j / p.gl.R : -1;
+                o = j;
+              } else {
+                sl = p.gl.row_slot[j];
+                o = sl;
+              }
+              if (sl < 0) continue;
+              const int n = min(max(__ldg(p.gl.n_labels + sl), 0), p.gl.L);
+              for (int k = 0; k < n; ++k) {
+                if (__ldg(p.gl.label_ids + (long long)sl * p.gl.L + k) != v) continue;
+                float z = __uint_as_float(r[0]);
+#pragma unroll
+                for (int jj = 1; jj < SK_N; ++jj) z = j == jj ? __uint_as_float(r[jj]) : z;
+                p.gl.out[(long long)o * p.gl.L + k] = z * gs * __ldg(p.inv_t + j);
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        aph ^= 1u;
+      }
+    }
+    // merge over the lanes, then over the four warps (through the W ring, idle
+    // now that every MMA has completed), and write this CTA's partials
+#pragma unroll
+    for (int j = 0; j < SK_N; ++j) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float mo = __shfl_xor_sync(0xffffffffu, m[j], o);
+        const float so = __shfl_xor_sync(0xffffffffu, s[j], o);
+        const float to = __shfl_xor_sync(0xffffffffu, tt[j], o);
+        const float bo = __shfl_xor_sync(0xffffffffu, best[j], o);
+        const int io = __shfl_xor_sync(0xffffffffu, bidx[j], o);
+        const float mn = fmaxf(m[j], mo);
+        if (mn == -INFINITY) {
+          s[j] = 0.f;
+          tt[j] = 0.f;
+        } else {
+          const float f1 = ex2(m[j] - mn), f2 = ex2(mo - mn);
+          s[j] = s[j] * f1 + so * f2;
+          tt[j] = tt[j] * f1 + to * f2;
+        }
+        m[j] = mn;
+        if (bo > best[j] || (bo == best[j] && io < bidx[j])) {
+          best[j] = bo;
+          bidx[j] = io;
+        }
+      }
+    }
+    float* red = reinterpret_cast<float*>(wring);   // [4 warps][16][5]
+    if (lane == 0 && has_work) {
+#pragma unroll
+      for (int j = 0; j < SK_N; ++j) {
+        float* e = red + (q * SK_N + j) * 5;
+        e[0] = m[j];
+        e[1] = s[j];
+        e[2] = tt[j];
+        e[3] = best[j];
+        reinterpret_cast<int*>(e)[4] = bidx[j];
+      }
+    }
+    sk_epi_bar();
+    if (q == 0 && lane < M && has_work) {
+      const int j = lane;
+      float mm = -INFINITY, ss = 0.f, tv = 0.f, bb = -INFINITY;
+      int ii = 0x7fffffff;
+      for (int w = 0; w < SK_EPI_WARPS; ++w) {
+        const float* e = red + (w * SK_N + j) * 5;
+        const float mo = e[0];
+        const float mn = fmaxf(mm, mo);
+        if (mn != -INFINITY) {
+          const float f1 = ex2(mm - mn), f2 = ex2(mo - mn);
+          ss = ss * f1 + e[1] * f2;
+          tv = tv * f1 + e[2] * f2;
+        }
+        mm = mn;
+        const int io = reinterpret_cast<const int*>(e)[4];
+        if (e[3] > bb || (e[3] == bb && io < ii)) {
+          bb = e[3];
+          ii = io;
+        }
+      }
+      const long long o = (long long)j * p.cpg + gn;
+      const long long plane = (long long)p.cpg * M;
+      p.part[o] = mm;
+      p.part[o + plane] = ss;
+      p.part[o + 2 * plane] = tv;
+      p.part[o + 3 * plane] = bb;
+      reinterpret_cast<int*>(p.part)[o + 4 * plane] = ii;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == CF::MMA) tmem_dealloc(tmem_base, CF::TMEM_COLS);
+}
+
 // Merge the per-CTA online statistics of every row: one warp per row, lanes over
 // the CTA partials (stored row-major, [M][cpg]), a fixed shuffle-tree order.
 __global__ void stats_finalize_kernel(const float* part, int cpg, int M, const float* inv_t,
@@ -777,6 +1216,25 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const Gemm
   return cudaGetLastError();
 }
 
+// The skinny pass of M <= 16 rows (see skinny_stats_kernel).
+bool skinny_ok(int M, int K) { return M <= SK_N && (K + BK - 1) / BK <= SK_MAX_KB; }
+
+template <bool F4>
+cudaError_t launch_skinny(const CUtensorMap& th, const CUtensorMap& tw, const GemmParams& p,
+                          cudaStream_t st) {
+  using CF = SkCfg<F4>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(skinny_stats_kernel<F4>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         CF::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  skinny_stats_kernel<F4><<<p.cpg, CF::THREADS, CF::SMEM_BYTES, st>>>(th, tw, p);
+  return cudaGetLastError();
+}
+
 constexpr int STATS_BN = 256;
 
 int stats_mt(int M) { return M <= BM ? 1 : 2; }
@@ -809,8 +1267,16 @@ cudaError_t run_stats(const uint16_t* h, int M, const uint16_t* w, int V, int D,
   p.part = part;
   p.status = dgi::status_ptr();
   if (gather) p.gl = *gather;
-  cudaError_t e = (mt == 1) ? launch_gemm<1, STATS_BN, EPI_STATS>(ta, tb, p, groups * p.cpg, st)
-                            : launch_gemm<2, STATS_BN, EPI_STATS>(ta, tb, p, groups * p.cpg, st);
+  cudaError_t e;
+  if (skinny_ok(M, D)) {
+    CUtensorMap th;   // the rows as 64 x 16 boxes (rows past M read as 0)
+    if (!dgi::make_tmap_bf16_2d(&th, h, D, M, (uint64_t)D * 2, BK, SK_N))
+      return cudaErrorInvalidValue;
+    e = launch_skinny<false>(th, tb, p, st);
+  } else {
+    e = (mt == 1) ? launch_gemm<1, STATS_BN, EPI_STATS>(ta, tb, p, groups * p.cpg, st)
+                  : launch_gemm<2, STATS_BN, EPI_STATS>(ta, tb, p, groups * p.cpg, st);
+  }
   if (e != cudaSuccess) return e;
   stats_finalize_kernel<<<(M + 7) / 8, 256, 0, st>>>(part, p.cpg, M, inv_t, out.lse,
                                                      out.entropy, out.maxz, out.argmax, p.gl, V,
@@ -867,7 +1333,7 @@ cudaError_t launch_stats4(const CUtensorMap& ta, const GemmParams& p, int grid, 
     attr_done = true;
   }
   gemm_tc_kernel<MT, STATS_BN, EPI_STATS4>
-      <<<grid, CF::THREADS + 32 * F4_EXTRA_WARPS, CF::SMEM_BYTES, st>>>(ta, ta, p);
+      <<<grid, CF::THREADS + 32 * f4_extra_warps(MT), CF::SMEM_BYTES, st>>>(ta, ta, p);
   return cudaGetLastError();
 }
 
@@ -892,8 +1358,16 @@ cudaError_t run_stats_nvfp4(const uint16_t* h, int M, const uint8_t* codes, cons
   p.part = part;
   p.status = dgi::status_ptr();
   if (gather) p.gl = *gather;
-  cudaError_t e = (mt == 1) ? launch_stats4<1>(ta, p, groups * p.cpg, st)
-                            : launch_stats4<2>(ta, p, groups * p.cpg, st);
+  cudaError_t e;
+  if (skinny_ok(M, D)) {
+    CUtensorMap th;
+    if (!dgi::make_tmap_bf16_2d(&th, h, D, M, (uint64_t)D * 2, BK, SK_N))
+      return cudaErrorInvalidValue;
+    e = launch_skinny<true>(th, th, p, st);
+  } else {
+    e = (mt == 1) ? launch_stats4<1>(ta, p, groups * p.cpg, st)
+                  : launch_stats4<2>(ta, p, groups * p.cpg, st);
+  }
   if (e != cudaSuccess) return e;
   stats_finalize_kernel<<<(M + 7) / 8, 256, 0, st>>>(part, p.cpg, M, inv_t, out.lse,
                                                      out.entropy, out.maxz, out.argmax, p.gl, V,

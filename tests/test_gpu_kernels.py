@@ -54,7 +54,10 @@ def test_philox_matches_oracle_bit_exact():
 
 
 @pytest.mark.parametrize("M,V,D", [(1, 1024, 128), (12, 4096, 256), (200, 3000, 200),
-                                   (256, 8192, 512), (300, 2048, 128)])
+                                   (256, 8192, 512), (300, 2048, 128),
+                                   # up to 16 rows: the skinny form (rows resident, vocabulary
+                                   # on the accumulator lanes), ragged vocabulary and K tail
+                                   (16, 3000, 200), (5, 2500, 2816), (17, 1024, 128)])
 def test_lmhead_stats(M, V, D):
     h, w, _, inv_t = _lm_inputs(M, V, D, seed=M + V)
     lse, ent, maxz, arg = _run_lmhead(h, w, inv_t)

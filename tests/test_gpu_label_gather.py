@@ -122,8 +122,8 @@ def test_lmhead_label_gather_fp8():
     _check_lp(lp, _want_lp(hd[slot_row], wd, inv_t[slot_row], ids, n), n, "fp8 label lp")
 
 
-def test_lmhead_label_gather_nvfp4():
-    M, S, V, D = 40, 6, 3000, 192
+@pytest.mark.parametrize("M,S,V,D", [(40, 6, 3000, 192), (12, 5, 4096, 256)])
+def test_lmhead_label_gather_nvfp4(M, S, V, D):
     h = inputs.hidden(M, D, 31)
     w, _ = inputs.weights(V, D, 32)
     inv_t = inputs.inv_temperature(M, 33)
@@ -132,7 +132,7 @@ def test_lmhead_label_gather_nvfp4():
     g = torch.empty(1, dtype=torch.float32, device="cuda")
     assert dg.dg_quantize_nvfp4(dev_bf16(w), V, D, codes, scales, g) == dg.DG_OK
     torch.cuda.synchronize()
-    slot_row = np.array([0, 39, 7, 8, 20, 33], np.int32)
+    slot_row = np.random.default_rng(M).choice(M, S, replace=False).astype(np.int32)
     ids, n = _tables(S, V, 34)
     lp, _ = _lm_call("nvfp4", dg.make_dims(d_model=D, V=V), M, (dev_bf16(h), codes, scales, g),
                      inv_t, slot_row, ids, n, S)

@@ -53,7 +53,7 @@ def test_quantizer_bit_exact(V, D):
 
 
 @pytest.mark.parametrize("M,V,D", [(12, 4096, 256), (256, 8192, 512), (300, 3000, 192),
-                                   (1, 1024, 64)])
+                                   (1, 1024, 64), (16, 3000, 192), (17, 2048, 128)])
 def test_nvfp4_lmhead_stats(M, V, D):
     h = inputs.hidden(M, D, 11 + M)
     w, _ = inputs.weights(V, D, 12 + V)
@@ -72,10 +72,12 @@ def test_nvfp4_lmhead_stats(M, V, D):
     assert np.array_equal(arg[clear], o_arg[clear])
 
 
-def test_nvfp4_lmhead_full_vocabulary_sampled_rows():
+@pytest.mark.parametrize("M", [256, 12])
+def test_nvfp4_lmhead_full_vocabulary_sampled_rows(M):
     """262144 x 2816 weights: the quantiser on a slice of rows (with the whole
-    tensor's scale) and the statistics of sampled canvas rows."""
-    V, D, M = 262144, 2816, 256
+    tensor's scale) and the statistics of sampled rows: 256 canvas rows (the
+    GEMM form) and 12 slot-draw rows (the skinny form, rows resident)."""
+    V, D = 262144, 2816
     w, _ = inputs.weights(V, D, 77)
     wd = dev_bf16(w)
     codes, scales, g = _quantize(wd, V, D)
@@ -92,7 +94,7 @@ def test_nvfp4_lmhead_full_vocabulary_sampled_rows():
     assert np.array_equal(host(scales[:, sl]), skb)
     oc_all, osc_all = oracle.from_kblock_layout(host(codes), host(scales))
     wq = oracle.dequantize_nvfp4(oc_all, osc_all, gh)
-    rows = np.array([0, 5, 127, 128, 200, 255])
+    rows = np.array([0, 5, 127, 128, 200, 255]) if M == 256 else np.arange(M)
     o_lse, o_ent, o_maxz, o_arg = oracle.lmhead_stats(h[rows], wq, inv_t[rows])
     assert_abs(lse[rows], o_lse, what="lse")
     assert_abs(ent[rows], o_ent, what="entropy")
