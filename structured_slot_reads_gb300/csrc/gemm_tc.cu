@@ -661,7 +661,7 @@ constexpr int SK_W_BYTES = SK_BN * BK * 2;  // a W tile of one K block (32 KB)
 constexpr int SK_B_BLOCK = SK_N * BK * 2;   // the rows' 64-column block (2 KB)
 constexpr int SK_MAX_KB = 48;               // resident rows for d_model up to 3072
 constexpr int SK_EPI_WARPS = 4;
-constexpr int SK_CONV_WARPS = 6;     // 12 warps in all: three per SM sub-partition
+constexpr int SK_CONV_WARPS = 10;    // 16 warps in all (128 registers a thread)
 constexpr int SK_GBITS = 64;                // label-gather chunk bitmap words
 
 template <bool F4>
