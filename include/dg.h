@@ -317,9 +317,12 @@ int dg_quantize_nvfp4(const uint16_t* x, int rows, int cols, uint8_t* codes, uin
                       float* g, void* stream);
 
 /* dg_lmhead_logsoftmax_entropy against NVFP4 weights: the row statistics of
- * softmax(z_i / T_i) with z_iv = (h_i . (e2m1 * s)_v) * g, the bf16 rows times
- * the weights widened to bf16 on chip (exact: e2m1 times an e4m3 scale fits
- * bf16), fp32 accumulation on the tensor cores.  Operands from
+ * softmax(z_i / T_i) with z_iv = (h_i . (e2m1 * s)_v) * g, the rows times the
+ * weights widened on chip (exact: e2m1 times an e4m3 scale fits bf16 and f16),
+ * fp32 accumulation on the tensor cores.  Up to 16 rows take f16 operands: each
+ * row is divided by a power of two that keeps it below 2^15 and converted to
+ * f16 (exact for elements of magnitude 2^-14 or more after the division; the
+ * power of two is multiplied back into the logits); more rows stay bf16.  Operands from
  * dg_quantize_nvfp4(w, V, d_model, ..); label gather, outputs, workspace
  * (DG_WS_LMHEAD) and errors as dg_lmhead_logsoftmax_entropy; d_model a multiple
  * of 64 and V of 4 (else DG_ERR_SHAPE); h, codes and scales 16-byte aligned. */

@@ -667,19 +667,27 @@ constexpr int SK_GBITS = 64;                // label-gather chunk bitmap words
 template <bool F4>
 struct SkCfg {
   static constexpr int B_BYTES = SK_MAX_KB * SK_B_BLOCK;   // 96 KB
-  static constexpr int NW = F4 ? 3 : 4;                    // W tiles in flight
-  static constexpr int NP = F4 ? 3 : 0;                    // packed blocks in flight
+  // W tiles in flight; NVFP4: the widened tiles are made on chip, so two
+  // suffice, and the room goes to the packed blocks, whose copies wait on DRAM
+  static constexpr int NW = F4 ? 2 : 4;
+  static constexpr int NP = F4 ? 7 : 0;
   static constexpr int PK = F4 ? f4_pk_bytes(SK_BN) : 0;
-  static constexpr int BAR_BYTES = 512;
+  // barriers (at most 19 x 8 bytes), the gather bitmap (256), the TMEM slot and
+  // abort flag (8), the row scales and powers of two (2 x 64)
+  static constexpr int BAR_BYTES = 1024;
   static constexpr int SMEM_BYTES = 1024 + B_BYTES + NW * SK_W_BYTES + NP * PK + BAR_BYTES;
   static constexpr int PRODUCER = SK_EPI_WARPS;            // rows, then W (or the packed ring)
   static constexpr int MMA = SK_EPI_WARPS + 1;
   static constexpr int CONV0 = SK_EPI_WARPS + 2;           // F4: converter warps
   static constexpr int THREADS = (SK_EPI_WARPS + 2 + (F4 ? SK_CONV_WARPS : 0)) * 32;
   static constexpr int TMEM_COLS = 64;                     // 2 stages x 2 halves x 16 columns
-  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, SK_N);
+  // bf16 W: bf16 operands.  NVFP4 W: f16 operands (the widening is then two
+  // instructions a code pair, and every e2m1 x e4m3 product is an f16)
+  static constexpr uint32_t IDESC = F4 ? idesc_f16_f32(BM, SK_N) : idesc_bf16_f32(BM, SK_N);
   static_assert(SMEM_BYTES <= 232448, "shared memory");
   static_assert(SK_EPI_WARPS == 4, "one epilogue warp per TMEM lane quarter");
+  static_assert((2 * NW + 2 * NP + 7) * 8 + SK_GBITS * 4 + 8 + 2 * SK_N * 4 <= BAR_BYTES,
+                "barrier region");
 };
 
 __device__ __forceinline__ void sk_epi_bar() {
@@ -705,10 +713,12 @@ __global__ void __launch_bounds__(SkCfg<F4>::THREADS, 1)
   uint64_t* tempty = tfull + 2;
   uint64_t* bres_bar = tempty + 2;
   uint64_t* drain_bar = bres_bar + 1;
-  uint32_t* gbits = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  uint64_t* rows16_bar = drain_bar + 1;   // F4: the rows converted to f16
+  uint32_t* gbits = reinterpret_cast<uint32_t*>(rows16_bar + 1);
   uint32_t* tmem_slot = gbits + SK_GBITS;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* sscale = reinterpret_cast<float*>(tmem_slot + 2);   // [16] 1/T of each row, log2 units
+  float* srow = sscale + SK_N;   // F4: [16] 2^k, the power of two row j was divided by
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -726,6 +736,7 @@ __global__ void __launch_bounds__(SkCfg<F4>::THREADS, 1)
       mbar_init(&tempty[a], SK_EPI_WARPS);
     }
     mbar_init(bres_bar, 1);
+    mbar_init(rows16_bar, SK_EPI_WARPS);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -797,7 +808,7 @@ __global__ void __launch_bounds__(SkCfg<F4>::THREADS, 1)
     if (lane == 0 && has_work) {
       int ws = 0, acc = 0;
       uint32_t wph = 0, aph = 0;
-      bool ok = mbar_wait(bres_bar, 0, abort_flag, p.status);
+      bool ok = mbar_wait(F4 ? rows16_bar : bres_bar, 0, abort_flag, p.status);
       for (int t = t_begin; t < t_end && ok; ++t) {
         if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
@@ -870,13 +881,12 @@ __global__ void __launch_bounds__(SkCfg<F4>::THREADS, 1)
             const __half2 s2 = __halves2half2(__half(hr), __half(hr));
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
+              // f16 operands: the exact product stays in f16
               uint32_t f16[4], o[4];
               e2m1x8_to_f16x2(cw[2 * q + h], f16);
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
-                const float2 f =
-                    __half22float2(__hmul2(*reinterpret_cast<const __half2*>(&f16[k]), s2));
-                const __nv_bfloat162 v = __floats2bfloat162_rn(f.x, f.y);
+                const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&f16[k]), s2);
                 o[k] = *reinterpret_cast<const uint32_t*>(&v);
               }
               const int c = 4 * hf + 2 * q + h;
@@ -917,6 +927,49 @@ __global__ void __launch_bounds__(SkCfg<F4>::THREADS, 1)
       bidx[j] = 0x7fffffff;
     }
     if (threadIdx.x < SK_N) sscale[threadIdx.x] = threadIdx.x < M ? __ldg(p.inv_t + threadIdx.x) * LOG2E : 0.f;
+    if (F4 && has_work) {
+      // The resident rows to f16, in place (the same 16-bit slots): row j is
+      // first divided by 2^k_j (exact), k_j >= 0 the least that keeps its
+      // largest element below 2^15, so nothing overflows; the accumulators of
+      // column j are multiplied back by 2^k_j.  An element is exact in f16 unless
+      // it falls below 2^-14 there, where f16's subnormal spacing 2^-24 rounds it.
+      // Thread i takes row i / 8 and the 16-byte chunks i % 8 of every K block.
+      const bool rows_ok = mbar_wait(bres_bar, 0, abort_flag, p.status);
+      const int j = threadIdx.x >> 3, c = threadIdx.x & 7;
+      const int nkb = (p.K + BK - 1) / BK;
+      float amax = 0.f;
+      for (int kb = 0; kb < nkb && rows_ok; ++kb) {
+        const uint4 u = *reinterpret_cast<const uint4*>(bres + kb * SK_B_BLOCK + j * 128 + c * 16);
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[e]));
+          amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+      }
+#pragma unroll
+      for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      // 2^k with k = max(0, e - 15), amax < 2^e (amax's exponent + 1)
+      const int ex = amax > 0.f ? ((__float_as_int(amax) >> 23) & 0xFF) - 126 : 0;
+      const int k = max(0, ex - 15);
+      const float down = __int_as_float((127 - k) << 23);
+      for (int kb = 0; kb < nkb && rows_ok; ++kb) {
+        uint4* ptr = reinterpret_cast<uint4*>(bres + kb * SK_B_BLOCK + j * 128 + c * 16);
+        uint4 u = *ptr;
+        uint32_t* w4 = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[e]));
+          const __half2 hv = __floats2half2_rn(f.x * down, f.y * down);
+          w4[e] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+        *ptr = u;
+      }
+      if (c == 0) srow[j] = __int_as_float((127 + k) << 23);
+      fence_proxy_async_smem();   // generic writes -> the MMAs' operand reads
+      __syncwarp();
+      if (lane == 0) mbar_arrive(rows16_bar);
+    }
     sk_epi_bar();
     // label gather: one bit per 32 vocabulary rows of this CTA's range holding a
     // label of one of the rows (aliased modulo SK_GBITS * 32 chunks)
@@ -955,7 +1008,7 @@ __global__ void __launch_bounds__(SkCfg<F4>::THREADS, 1)
 #pragma unroll
           for (int j = 0; j < SK_N; ++j) {
             if (j >= M) break;
-            const float a = __uint_as_float(r[j]) * gs;
+            const float a = __uint_as_float(r[j]) * (F4 ? gs * srow[j] : gs);
             if (a > best[j]) {   // rows ascend, so the first occurrence is the lowest id
               best[j] = a;
               bidx[j] = v;
@@ -987,7 +1040,8 @@ __global__ void __launch_bounds__(SkCfg<F4>::THREADS, 1)
                 float z = __uint_as_float(r[0]);
 #pragma unroll
                 for (int jj = 1; jj < SK_N; ++jj) z = j == jj ? __uint_as_float(r[jj]) : z;
-                p.gl.out[(long long)o * p.gl.L + k] = z * gs * __ldg(p.inv_t + j);
+                p.gl.out[(long long)o * p.gl.L + k] =
+                    z * (F4 ? gs * srow[j] : gs) * __ldg(p.inv_t + j);
               }
             }
           }

@@ -312,6 +312,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
 
+// Instruction descriptor, kind::f16: f16 A and B (format code 0), both K-major,
+// fp32 D, M x N.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4)                       // D format: f32
+         | ((uint32_t)(N >> 3) << 17)    // N / 8
+         | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
 // Instruction descriptor, kind::f8f6f4: e4m3 A and B (format code 0), both K-major,
 // fp32 D, M x N.
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {

@@ -99,3 +99,31 @@ def test_nvfp4_lmhead_full_vocabulary_sampled_rows(M):
     assert_abs(lse[rows], o_lse, what="lse")
     assert_abs(ent[rows], o_ent, what="entropy")
     assert_abs(maxz[rows], o_maxz, what="max logit")
+
+
+@pytest.mark.parametrize("M", [12, 40])
+def test_nvfp4_lmhead_tiny_block_scales(M):
+    """One block far above the rest makes the tensor scale large, so every other
+    block's e4m3 scale is small and its widened products are tiny (below f16's
+    normal range in the skinny form, which works in f16 times 2^-14).  Rows of
+    magnitude ~400 make the logits depend on those products alone (the large
+    block meets zero row entries): flushing them would move lse by several nats."""
+    V, D = 1024, 256
+    w = inputs.normal_bf16((V, D), 1e-3, 91, 1)
+    w[0, :16] = 1000.0
+    w = inputs.to_bf16(w)
+    h = inputs.normal_bf16((M, D), 400.0, 92, 1)
+    h[:, :16] = 0.0
+    h = inputs.to_bf16(h)
+    inv_t = np.ones(M, np.float32)
+    codes, scales, g = _quantize(dev_bf16(w), V, D)
+    lse, ent, maxz, arg = _stats(h, codes, scales, g, inv_t, V, D)
+    oc, osc = oracle.from_kblock_layout(host(codes), host(scales))
+    wq = oracle.dequantize_nvfp4(oc, osc, host(g)[0])
+    # every other block: e2m1 x scale below 1, i.e. below 2^-14 once times 2^-14
+    assert (np.abs(wq[1:]) / host(g)[0]).max() < 1.0
+    o_lse, o_ent, o_maxz, _ = oracle.lmhead_stats(h, wq, inv_t)
+    assert np.all(o_lse - np.log(V) > 1.0)                         # logits far from flat
+    assert_abs(lse, o_lse, what="lse (tiny block scales)")
+    assert_abs(ent, o_ent, what="entropy (tiny block scales)")
+    assert_abs(maxz, o_maxz, what="max logit (tiny block scales)")
