@@ -8,7 +8,10 @@
 //              24-ai.news "Token commit mechanism"): A = hidden rows, B = W.
 //              Each epilogue thread owns one row and keeps an online
 //              (max, sum 2^(v-max), sum v 2^(v-max), argmax) over the vocabulary
-//              tiles it sees; the [M, V] logits never leave the SM.
+//              tiles it sees, and takes the logits of its row's allowed labels
+//              as they pass (the label gather); the [M, V] logits never leave
+//              the SM.  EPI_STATS8 / EPI_STATS4: the same on e4m3 operands, or
+//              with B = NVFP4 weights widened to bf16 on chip.
 //   EPI_PROBS  first half of self-conditioning (24-ai.news "Token commit
 //              mechanism"): recompute the logits tile and write
 //              p = exp(z - lse) in bf16, the A operand of the second GEMM.
@@ -20,6 +23,10 @@
 // shared-memory ring whose stages hold MT 128x64 A tiles and one BNx64 B tile
 // (128-byte swizzled), warp 4*MT+1 owns TMEM and issues tcgen05.mma from one
 // thread.  B is K-major (W) or MN-major (E read as [V, d_model]).
+//
+// Up to 16 rows, the statistics pass takes skinny_stats_kernel instead: the
+// operands swapped (A = the vocabulary tile, B = the rows, resident in shared
+// memory), so only W streams and the MMAs are 16 columns wide.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
