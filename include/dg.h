@@ -424,8 +424,9 @@ int dg_selfcond_embed(const dg_dims* dims, const uint16_t* h, int M,
  *    draw_label_z[j][k] = z_j[draw_label_ids[j / draw_R][k]] (k <
  *    draw_n_labels[j / draw_R]), the label logits dg_slot_finish takes with
  *    rows = NULL.
- * The statistics and the probabilities are exact for any input whose scaled
- * logits stay below 2^24 log2 units.
+ * The statistics and the probabilities are exact (no clamped or overflowing
+ * exponent) while every scaled logit z_iv log2(e) lies less than 2^13 above the
+ * largest of the row's first eight.
  *   h [M, d_model] bf16;  draw_rows [n_draw, d_model] bf16 (NULL if n_draw = 0)
  *   w [V, d_model] bf16;  inv_t [M], inv_t_draw [n_draw] fp32
  *   lse, entropy, maxz [M] fp32;  argmax [M] int32;  lse_draw [n_draw] fp32

@@ -10,9 +10,10 @@
 // rescaling and p_iv = P~_iv / S_i exactly; the P.E GEMM applies 1/S_i in its
 // reduction.
 //
-// The pass is exact for any input whose scaled logits stay below 2^13 log2
-// units.  An epilogue thread owns one row of its CTA's vocabulary range and
-// sums each 32-entry chunk against its reference; if the chunk's largest
+// The pass is exact while every scaled logit lies less than 2^13 log2 units
+// above the largest of the row's first 8.  An epilogue thread owns one row of
+// its CTA's vocabulary range and sums each 32-entry chunk against its
+// reference; if the chunk's largest
 // exponent passes RAISE it raises the reference by a whole number k of log2
 // units (2^-k is then exact), scales what it summed and wrote before the chunk
 // by 2^-k and sums the chunk again.  Each CTA reports the reference of its sums
