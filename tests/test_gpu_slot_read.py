@@ -79,6 +79,23 @@ def test_slot_read_reduced(seed, samples):
         assert np.all(got["n_reads"] == 1)
 
 
+@pytest.mark.parametrize("seed", [0, 1])
+def test_slot_read_more_than_16_draw_rows(seed):
+    """Six slots x 4 reads = 24 draw rows: past the skinny form, the W pass is the
+    GEMM form with the label gather in its epilogue (two requests' canvases)."""
+    shape = configs.scaled(configs.SINGLE_READ, B=2, C=64, D=256, V=4096,
+                           slots=[(5, 2), (30, 26), (50, 5), (7, 9), (40, 17), (63, 3)])
+    h, w, e, inv_t, slot_row, slot_req, label_ids, n_labels = _case(shape, seed)
+    S = len(slot_row)
+    assert S * 4 > 16
+    mode = "high" if seed % 2 == 0 else "low"
+    h, want = margins.prepare_slot_inputs(h, w, e, inv_t, slot_row, slot_req, label_ids,
+                                          n_labels, seed, 0, 4, 0.1, [mode] * S)
+    got = _run_read(h, w, e, inv_t, slot_row, slot_req, label_ids, n_labels, seed, 0, 4, 0.1)
+    _compare(got, want, n_labels)
+    assert np.all(got["resampled"] == (1 if mode == "high" else 0))
+
+
 def test_slot_read_tiny_config():
     shape = configs.TINY
     h, w, e, inv_t, slot_row, slot_req, label_ids, n_labels = _case(shape, 0)
