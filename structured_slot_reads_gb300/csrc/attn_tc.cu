@@ -242,7 +242,8 @@ __device__ __forceinline__ void softmax_and_store(const TcArgs& a, const Tiles& 
     const uint16_t own = bf16_bits_up(mh == -INFINITY ? -INFINITY : mh * sl2);
     uint16_t* xm = xmax + (j & 1) * 2 * BM;
     xm[half * BM + r] = own;
-    mbar_arrive(&pair_bar[quarter]);
+    __syncwarp();   // the warp's writes, ordered before its one arrival
+    if (lane == 0) mbar_arrive(&pair_bar[quarter]);
     ok = __all_sync(FULL, mbar_wait(&pair_bar[quarter], j & 1u, abort_flag, a.status));
     if (!ok) break;
     const float mb = fmaxf(bf16_bits_to_float(own), bf16_bits_to_float(xm[(half ^ 1) * BM + r]));
@@ -294,10 +295,13 @@ __device__ __forceinline__ void softmax_and_store(const TcArgs& a, const Tiles& 
     l += psum;
     tmem_st_wait();
     tc_fence_before();
-    if constexpr (PAIR)
-      mbar_arrive_cluster((j & 1) ? pready_c1 : pready_c0);
-    else
-      mbar_arrive(&pready_bar[j & 1]);
+    __syncwarp();   // one arrival per warp (a cluster-scope release in the pair)
+    if (lane == 0) {
+      if constexpr (PAIR)
+        mbar_arrive_cluster((j & 1) ? pready_c1 : pready_c0);
+      else
+        mbar_arrive(&pready_bar[j & 1]);
+    }
   }
   // the last two P V products: wait phase n-2 first, so that the parity wait for
   // phase n-1 cannot be satisfied by an older phase
@@ -306,7 +310,8 @@ __device__ __forceinline__ void softmax_and_store(const TcArgs& a, const Tiles& 
   if (!ok) return;
   // row sum over both halves: phase n of the pair's barrier
   xch[half * 128 + r] = l;
-  mbar_arrive(&pair_bar[quarter]);
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&pair_bar[quarter]);
   if (!__all_sync(FULL, mbar_wait(&pair_bar[quarter], n & 1u, abort_flag, a.status))) return;
   l += xch[(half ^ 1) * 128 + r];
   tc_fence_after();
@@ -427,11 +432,11 @@ __device__ __forceinline__ void attn_body(const CUtensorMap& tmQ, const CUtensor
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sfull_bar[i], 1);
       // the softmax threads of both CTAs arrive on the even CTA's barrier
-      mbar_init(&pready_bar[i], (PAIR ? 2 : 1) * SOFT_WARPS * 32);
+      mbar_init(&pready_bar[i], (PAIR ? 2 : 1) * SOFT_WARPS);   // one arrival per softmax warp
     }
     mbar_init(pv_bar, 1);
     mbar_init(drain_bar, 1);
-    for (int i = 0; i < 4; ++i) mbar_init(&pair_bar[i], 64);
+    for (int i = 0; i < 4; ++i) mbar_init(&pair_bar[i], 2);   // the two warps of a lane quarter
     *abort_flag = 0;
     fence_barrier_init();
   }
