@@ -360,7 +360,9 @@ def _run_heads(h, draws, w, inv_t, inv_t_draw, with_probs=True):
                                       # several 256-row groups, ragged vocabularies
                                       (520, 0, 4000, 128), (384, 16, 2504, 192),
                                       # batched canvases: the warp-per-row reference
-                                      (1100, 8, 2048, 128)])
+                                      (1100, 8, 2048, 128),
+                                      # 16 row groups x 19 CTAs: two waves of balanced ranges
+                                      (4096, 0, 4096, 128)])
 def test_denoise_heads_fused_pass(M, nd, V, D):
     h, w, e, inv_t = _lm_inputs(M, V, D, seed=31 + M)
     draws = inputs.hidden(nd, D, 99) if nd else None
