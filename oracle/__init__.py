@@ -30,8 +30,8 @@ Functions with no pin other than their own definition are marked
 "parity unpinned" in their docstring; at present there are none.
 """
 from .nvfp4 import (block_values, decode_e2m1, dequantize_nvfp4, from_kblock_layout,  # noqa: F401
-                    pack_nibbles, quantize_nvfp4, tensor_scale, to_e2m1_codes, to_kblock_layout,
-                    unpack_nibbles)
+                    from_mma_layout, pack_nibbles, quantize_nvfp4, tensor_scale, to_e2m1_codes,
+                    to_kblock_layout, to_mma_layout, unpack_nibbles)
 from .philox import philox4x32_10, noise_tokens, seed_key  # noqa: F401
 from .quant import (dequantize_rows, e4m3_value, quantize_cols_e4m3, quantize_rows_e4m3,  # noqa: F401
                     selfcond_fp8)

@@ -97,3 +97,27 @@ def test_values_on_the_grid_quantise_exactly():
     assert g == 2.0 ** -6
     assert np.array_equal(nvfp4.decode_e2m1(codes), blocks)
     assert np.array_equal(nvfp4.dequantize_nvfp4(codes, scales, g), x.astype(np.float64))
+
+
+def test_mma_layout_places_each_scale_by_its_definition():
+    """The scale atoms of the block-scaled layout: row 32 j + l of a 128-row tile,
+    64-value step k, block q of the step at atom [tile][k], byte 16 l + 4 j + q;
+    codes two a byte, the even element low; rows past R scale 0 (checked byte by
+    byte against that definition, then the inverse)."""
+    R, K = 130, 192
+    rng = np.random.default_rng(3)
+    codes = rng.integers(0, 16, (R, K), dtype=np.uint8)
+    scales = rng.integers(0, 256, (R, K // 16), dtype=np.uint8)
+    packed, atoms = nvfp4.to_mma_layout(codes, scales)
+    assert packed.shape == (R, K // 2) and atoms.shape == (2, 3, 512)
+    assert packed[5, 7] == codes[5, 14] | (codes[5, 15] << 4)
+    for r in range(R):
+        t, rr = divmod(r, 128)
+        j, l = divmod(rr, 32)
+        for b in range(K // 16):
+            k, q = divmod(b, 4)
+            assert atoms[t, k, 16 * l + 4 * j + q] == scales[r, b]
+    assert atoms[1, :, 16 * 2:].sum() == 0            # rows 130..255 of tile 1
+    assert atoms[1, :, 4:16].sum() == 0               # rows 160, 192, 224 (j > 0, l = 0)
+    c2, s2 = nvfp4.from_mma_layout(packed, atoms, R)
+    assert np.array_equal(c2, codes) and np.array_equal(s2, scales)
