@@ -30,6 +30,8 @@ sys.path.insert(0, ROOT)
 METRIC = "denoise steps/s per 256-tok canvas; slot reads/s; % of tensor/HBM roofline"
 UNIT = "denoise steps/s"
 
+LMHEAD_KINDS = ("lmhead", "lmhead_fp8", "lmhead_fp4", "lmhead_fp4mma")
+
 # workload name -> (runner kind, shape name, overrides).  Kinds: "step" = the
 # full denoise step, "read" = the read-only step (attention + one slot read),
 # "two_stage" = the mixed batch of two-stage ask_if reads over paged prompt KV.
@@ -45,6 +47,7 @@ WORKLOADS = {
     "lmhead_fp8_m12": ("lmhead_fp8", "FULL_CANVAS", dict(C=12)),
     "lmhead_nvfp4_m256": ("lmhead_fp4", "FULL_CANVAS", {}),
     "lmhead_nvfp4_m12": ("lmhead_fp4", "FULL_CANVAS", dict(C=12)),
+    "lmhead_nvfp4_mma_m12": ("lmhead_fp4mma", "FULL_CANVAS", dict(C=12)),
     "selfcond_bf16_m256": ("selfcond", "FULL_CANVAS", {}),
     "selfcond_fp8_m256": ("selfcond_fp8", "FULL_CANVAS", {}),
     "mixed_decode8_prefill2": ("mixed", "LONG_CONTEXT", dict(B=10, C=2048, P=4096)),
@@ -511,11 +514,11 @@ def build_runner(kind, shape, device, concurrent=True):
     from structured_slot_reads_gb300.read import ReadStep, TwoStageRead
     if kind == "step":
         return build_step(shape, device, concurrent=concurrent)
-    if kind in ("lmhead", "lmhead_fp8", "lmhead_fp4"):
+    if kind in LMHEAD_KINDS:
         from structured_slot_reads_gb300.read import LmHead
         w = inputs.device_normal_bf16((shape.V, shape.D), shape.D ** -0.5, 1, device)
         st = LmHead(shape, w, shape.B * shape.C, fp8=kind == "lmhead_fp8", device=device,
-                    fp4=kind == "lmhead_fp4")
+                    fp4=kind == "lmhead_fp4", fp4_mma=kind == "lmhead_fp4mma")
         st.h.copy_(inputs.device_normal_bf16(st.h.shape, 1.0, 3, device))
         st.inv_t.copy_(1.0 / inputs.device_uniform(st.inv_t.shape, 0.5, 2.0, 4, device))
         torch.cuda.synchronize()
@@ -633,10 +636,11 @@ def workload_arm(args, rank, world, local):
     elif kind == "mixed":
         run = lambda i: st.run(step_idx=i)              # noqa: E731
         calls = ["dg_attn_mixed"]
-    elif kind in ("lmhead", "lmhead_fp8", "lmhead_fp4"):
+    elif kind in LMHEAD_KINDS:
         run = lambda i: st.run(step_idx=i)              # noqa: E731
         calls = ["dg_lmhead_logsoftmax_entropy", "dg_quantize_rows_e4m3",
-                 "dg_lmhead_logsoftmax_entropy_fp8", "dg_lmhead_logsoftmax_entropy_nvfp4"]
+                 "dg_lmhead_logsoftmax_entropy_fp8", "dg_lmhead_logsoftmax_entropy_nvfp4",
+                 "dg_lmhead_logsoftmax_entropy_nvfp4_mma"]
     elif kind in ("selfcond", "selfcond_fp8"):
         run = lambda i: st.run(step_idx=i)              # noqa: E731
         calls = ["dg_selfcond_from_probs", "dg_quantize_rows_e4m3", "dg_selfcond_from_probs8"]
@@ -664,7 +668,7 @@ def workload_arm(args, rank, world, local):
         fl = (shape.B - 2) * attn_flops(dec) + 2 * prefill_flops(enc)
         by = (shape.B - 2) * attn_bytes(dec) + 2 * prefill_bytes(enc)
         work["dg_attn_mixed"] = (by, fl)
-    if kind in ("lmhead", "lmhead_fp8", "lmhead_fp4"):
+    if kind in LMHEAD_KINDS:
         Mr = shape.B * shape.C
         esz = 1 if kind == "lmhead_fp8" else 2
         lm = (V * D * esz + Mr * D * esz + V * 4 * (esz == 1) + Mr * 16, 2.0 * Mr * V * D)
@@ -673,6 +677,11 @@ def workload_arm(args, rank, world, local):
         # NVFP4 weights: half a byte per element plus one e4m3 scale per 16; bf16 rows
         work["dg_lmhead_logsoftmax_entropy_nvfp4"] = (V * D // 2 + V * D // 16 + Mr * D * 2
                                                       + Mr * 16, 2.0 * Mr * V * D)
+        # both NVFP4: the weights' codes and scales, the rows read once (bf16) and
+        # quantised (their codes and scales written and read back)
+        work["dg_lmhead_logsoftmax_entropy_nvfp4_mma"] = (
+            V * D // 2 + V * D // 16 + Mr * D * 2 + 2 * (Mr * D // 2 + Mr * D // 16) + Mr * 16,
+            2.0 * Mr * V * D)
         work["dg_quantize_rows_e4m3"] = (Mr * D * 3 + Mr * 4, 0.0)
     if kind in ("selfcond", "selfcond_fp8"):
         Mr = shape.B * shape.C
@@ -728,7 +737,7 @@ def workload_arm(args, rank, world, local):
         unit, value = "prompt tokens/s", steps_per_s * shape.B * shape.P
     elif kind == "mixed":
         unit, value = "attention launches/s", steps_per_s
-    elif kind in ("lmhead", "lmhead_fp8", "lmhead_fp4"):
+    elif kind in LMHEAD_KINDS:
         unit, value = "lm-head passes/s", steps_per_s
     elif kind in ("selfcond", "selfcond_fp8"):
         unit, value = "self-conditioning passes/s", steps_per_s
@@ -739,7 +748,8 @@ def workload_arm(args, rank, world, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": ("e4m3" if kind.endswith("_fp8") else
-                  "nvfp4 weights x bf16 rows" if kind.endswith("_fp4") else "bf16"),
+                  "nvfp4 weights x bf16 rows" if kind.endswith("_fp4") else
+                  "nvfp4 weights x nvfp4 rows" if kind.endswith("_fp4mma") else "bf16"),
         "data": "synthetic",
         "config": {"workload": f"{args.workload}: kind {kind}, B={shape.B}, prompt "
                                f"{'U[512, %d] paged' % shape.P if kind == 'two_stage' else shape.P}"

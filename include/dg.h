@@ -64,6 +64,7 @@ extern "C" {
 #define DG_WS_PROBS_EMBED 6
 #define DG_WS_PREFILL 7
 #define DG_WS_PROBS_EMBED8 8
+#define DG_WS_LMHEAD_NVFP4_MMA 9
 
 /* Problem dimensions.  B requests, C canvas tokens each, P_max the longest
  * prompt (encoder KV) length, Hq/Hkv query/KV heads (GQA, Hq % Hkv == 0),
@@ -334,6 +335,38 @@ int dg_lmhead_logsoftmax_entropy_nvfp4(const dg_dims* dims, const uint16_t* h, i
                                        float* entropy, float* maxz, int32_t* argmax,
                                        float* label_lp, void* workspace, size_t workspace_bytes,
                                        void* stream);
+
+/* The same pass with the rows in NVFP4 too (the pages' checkpoint quantises
+ * weights and activations), on the block-scaled tensor-core kind
+ * (kind::mxf4nvf4, one e4m3 scale per 16 values of both operands):
+ * z_iv = (sum_k e2m1(h)_ik s(h)_ik e2m1(w)_vk s(w)_vk) * g_h * g_w, fp32
+ * accumulation; the rows are quantised inside the call by the recipe of
+ * dg_quantize_nvfp4 with their own tensor scale g_h.  At most 16 rows (the slot
+ * reads' draw rows) and d_model a multiple of 64 up to 3072, else DG_ERR_SHAPE.
+ * codes and sf from dg_quantize_nvfp4_mma(w, V, d_model, ..), g its tensor scale;
+ * label gather and outputs as dg_lmhead_logsoftmax_entropy; workspace:
+ * dg_workspace_bytes(dims, DG_WS_LMHEAD_NVFP4_MMA, M) bytes (256-byte aligned).
+ * h, codes and sf 16-byte aligned. */
+int dg_lmhead_logsoftmax_entropy_nvfp4_mma(const dg_dims* dims, const uint16_t* h, int M,
+                                           const uint8_t* codes, const uint8_t* sf,
+                                           const float* g, const float* inv_t,
+                                           const int32_t* slot_row, const int32_t* label_ids,
+                                           const int32_t* n_labels, int S, float* lse,
+                                           float* entropy, float* maxz, int32_t* argmax,
+                                           float* label_lp, void* workspace,
+                                           size_t workspace_bytes, void* stream);
+
+/* NVFP4 quantisation (the recipe of dg_quantize_nvfp4) in the layout the
+ * block-scaled pass reads: codes row-major [rows][cols/2] (element k of row v
+ * in byte k / 2, the low nibble for even k); scales as 512-byte atoms, one per
+ * 128-row tile and 64-value K-step, atoms [ceil(rows/128)][cols/64]: row 32 j + l
+ * of the tile has its four e4m3 scales (values 16 q .. 16 q + 15 of the step in
+ * byte q) at bytes 16 l + 4 j .. 16 l + 4 j + 3 of the atom; rows of the last tile
+ * past `rows` have scale 0.  *g the fp32 tensor scale (device).  sf holds
+ * ceil(rows/128) * (cols/64) * 512 bytes.  cols a multiple of 64 (else
+ * DG_ERR_SHAPE); x and codes 16-byte aligned, sf 4-byte aligned. */
+int dg_quantize_nvfp4_mma(const uint16_t* x, int rows, int cols, uint8_t* codes, uint8_t* sf,
+                          float* g, void* stream);
 
 /* ---- next: one wide read in place of the two-stage path -----------------
  * sotaaz.com, "The server accepts at most 26 alternatives per question": the

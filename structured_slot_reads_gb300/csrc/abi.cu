@@ -329,6 +329,9 @@ size_t dg_workspace_bytes(const dg_dims* d, int which, int rows) {
     case DG_WS_PROBS_EMBED8:
       if (!dims_lm(d) || rows < 1) return 0;
       return dgi::probs_embed8_ws_bytes(rows, d->V, d->d_model);
+    case DG_WS_LMHEAD_NVFP4_MMA:
+      if (!dims_lm(d) || !dgi::lmhead_nvfp4_mma_ok(rows, d->d_model)) return 0;
+      return dgi::lmhead_nvfp4_mma_ws_bytes(rows, d->V, d->d_model);
     case DG_WS_PREFILL:
       if (!prefill_dims_ok(d)) return 0;
       return dgi::attn_tc_ws_bytes(d->B, d->P_max, 0, d->Hq, d->Hkv, d->P_max, d->sm_share);
@@ -742,6 +745,42 @@ int dg_lmhead_logsoftmax_entropy_nvfp4(const dg_dims* d, const uint16_t* h, int 
                                                dgi::RowStats{lse, entropy, maxz, argmax},
                                                workspace, static_cast<cudaStream_t>(stream),
                                                &lg));
+}
+
+int dg_quantize_nvfp4_mma(const uint16_t* x, int rows, int cols, uint8_t* codes, uint8_t* sf,
+                          float* g, void* stream) {
+  if (rows < 0 || cols < 1) return DG_ERR_ARG;
+  if (cols % 64) return DG_ERR_SHAPE;
+  if (rows > 0 && (!x || !codes || !sf || !g)) return DG_ERR_ARG;
+  if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(sf, 4) || !aligned(g, 4))
+    return DG_ERR_ARG;
+  return launch_result(
+      dgi::quantize_nvfp4_mma(x, rows, cols, codes, sf, g, static_cast<cudaStream_t>(stream)));
+}
+
+int dg_lmhead_logsoftmax_entropy_nvfp4_mma(const dg_dims* d, const uint16_t* h, int M,
+                                           const uint8_t* codes, const uint8_t* sf,
+                                           const float* g, const float* inv_t,
+                                           const int32_t* slot_row, const int32_t* label_ids,
+                                           const int32_t* n_labels, int S, float* lse,
+                                           float* entropy, float* maxz, int32_t* argmax,
+                                           float* label_lp, void* workspace,
+                                           size_t workspace_bytes, void* stream) {
+  if (!d || M < 1 || S < 0) return DG_ERR_ARG;
+  if (!dims_lm(d) || !dgi::lmhead_nvfp4_mma_ok(M, d->d_model)) return DG_ERR_SHAPE;
+  if (!h || !codes || !sf || !g || !inv_t || !lse || !entropy || !maxz || !argmax)
+    return DG_ERR_ARG;
+  if (!aligned(h, 16) || !aligned(codes, 16) || !aligned(sf, 16) || !aligned(g, 4))
+    return DG_ERR_ARG;
+  const size_t need = dg_workspace_bytes(d, DG_WS_LMHEAD_NVFP4_MMA, M);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DG_ERR_WORKSPACE;
+  dgi::LabelGather lg;
+  if (int rc = lm_gather(d, M, slot_row, label_ids, n_labels, S, label_lp, workspace, &lg))
+    return rc;
+  return launch_result(dgi::lmhead_stats_nvfp4_mma(h, M, codes, sf, g, d->V, d->d_model, inv_t,
+                                                   dgi::RowStats{lse, entropy, maxz, argmax},
+                                                   workspace, static_cast<cudaStream_t>(stream),
+                                                   &lg));
 }
 
 int dg_ask_if_select(const int32_t* chosen1, int S1, const int32_t* cond_slot,

@@ -75,6 +75,9 @@ struct GemmParams {
   const uint8_t* codes4;   // STATS4: e2m1 codes [K/64][N][32 bytes]
   const uint8_t* scales4;  // STATS4: e4m3 block scales [K/64][N][4]
   const float* gscale;     // STATS4: the weights' tensor scale
+  const uint8_t* sf4;      // skinny block-scaled: the weights' scale atoms [N/128][K/64][512]
+  const uint8_t* sf_rows;  // skinny block-scaled: the rows' scale atoms [K/64][512]
+  const float* gscale_rows;  // skinny block-scaled: the rows' tensor scale
   dgi::LabelGather gl;     // STATS kinds: label gather (gl.out null: none)
   float* part;            // STATS: 5 x [cpg][M]; ACCUM: [k_split][M][N]
   __nv_bfloat16* probs;   // PROBS: [M][ldp]
@@ -661,6 +664,14 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
 // owns one vocabulary row and keeps the online statistics of all 16 columns,
 // merged over lanes and warps once, at the end.  The partial statistics leave
 // in the planes of the STATS epilogue, so stats_finalize_kernel merges them.
+//
+// Three operand modes: bf16 W and rows (MODE 0); NVFP4 W widened on chip to f16
+// against f16 rows (MODE 1); NVFP4 W and NVFP4 rows on the block-scaled tensor-core
+// kind (MODE 2: kind::mxf4nvf4, scale_vec::4X).  MODE 2 streams the packed codes
+// (K blocks of 256 values, 128 bytes a row, by TMA) and each K block's scale atoms
+// (bulk copies); the MMA warp moves the scales into tensor memory with
+// tcgen05.cp (.32x128b.warpx4, one 512-byte atom per 128 rows and 64-value
+// K-step) before the MMAs that read them, alternating two sets of columns.
 // ---------------------------------------------------------------------------
 constexpr int SK_N = 16;                    // rows of B (the MMAs' N)
 constexpr int SK_BN = 256;                  // vocabulary rows per tile: two M = 128 MMAs
@@ -671,9 +682,19 @@ constexpr int SK_EPI_WARPS = 4;
 constexpr int SK_CONV_WARPS = 10;    // 16 warps in all (128 registers a thread)
 constexpr int SK_GBITS = 64;                // label-gather chunk bitmap words
 
-template <bool F4>
+constexpr int SK_X4_KB = 256;               // MODE 2: values of a K block (128 bytes a row)
+constexpr int SK_X4_ROWS = SK_N * 128;      // MODE 2: the rows' codes of a K block (2 KB)
+constexpr int SK_X4_CODES = 12 * SK_X4_ROWS;   // MODE 2: resident row codes, d_model <= 3072
+constexpr int SK_X4_SFA = 2 * 4 * 512;      // MODE 2: W scale atoms of a K block (2 x 4 steps)
+
+template <int MODE>
 struct SkCfg {
-  static constexpr int B_BYTES = SK_MAX_KB * SK_B_BLOCK;   // 96 KB
+  static constexpr bool F4 = MODE == 1;
+  static constexpr bool X4 = MODE == 2;
+  // resident rows: bf16 K blocks; MODE 2: the codes, then the scale atoms
+  static constexpr int B_BYTES = X4 ? 2 * SK_X4_CODES : SK_MAX_KB * SK_B_BLOCK;
+  // one W ring stage: a 256-row tile of a K block (MODE 2: plus its scale atoms)
+  static constexpr int W_STAGE = SK_W_BYTES + (X4 ? SK_X4_SFA : 0);
   // W tiles in flight; NVFP4: the widened tiles are made on chip, so two
   // suffice, and the room goes to the packed blocks, whose copies wait on DRAM
   static constexpr int NW = F4 ? 2 : 4;
@@ -682,15 +703,21 @@ struct SkCfg {
   // barriers (at most 19 x 8 bytes), the gather bitmap (256), the TMEM slot and
   // abort flag (8), the row scales and powers of two (2 x 64)
   static constexpr int BAR_BYTES = 1024;
-  static constexpr int SMEM_BYTES = 1024 + B_BYTES + NW * SK_W_BYTES + NP * PK + BAR_BYTES;
+  static constexpr int SMEM_BYTES = 1024 + B_BYTES + NW * W_STAGE + NP * PK + BAR_BYTES;
   static constexpr int PRODUCER = SK_EPI_WARPS;            // rows, then W (or the packed ring)
   static constexpr int MMA = SK_EPI_WARPS + 1;
   static constexpr int CONV0 = SK_EPI_WARPS + 2;           // F4: converter warps
   static constexpr int THREADS = (SK_EPI_WARPS + 2 + (F4 ? SK_CONV_WARPS : 0)) * 32;
-  static constexpr int TMEM_COLS = 64;                     // 2 stages x 2 halves x 16 columns
+  // 2 stages x 2 halves x 16 columns; MODE 2: then two sets of 48 scale columns
+  // (W: 2 halves x 4 steps x 4, rows: 4 steps x 4)
+  static constexpr int TMEM_COLS = X4 ? 256 : 64;
+  static constexpr int SF_COL = 64;
   // bf16 W: bf16 operands.  NVFP4 W: f16 operands (the widening is then two
   // instructions a code pair, and every e2m1 x e4m3 product is an f16)
-  static constexpr uint32_t IDESC = F4 ? idesc_f16_f32(BM, SK_N) : idesc_bf16_f32(BM, SK_N);
+  static constexpr uint32_t IDESC = X4   ? idesc_nvf4_f32(BM, SK_N)
+                                    : F4 ? idesc_f16_f32(BM, SK_N)
+                                         : idesc_bf16_f32(BM, SK_N);
+  static_assert(W_STAGE % 1024 == 0, "W stages stay 1 KB aligned");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
   static_assert(SK_EPI_WARPS == 4, "one epilogue warp per TMEM lane quarter");
   static_assert((2 * NW + 2 * NP + 7) * 8 + SK_GBITS * 4 + 8 + 2 * SK_N * 4 <= BAR_BYTES,
@@ -701,17 +728,19 @@ __device__ __forceinline__ void sk_epi_bar() {
   asm volatile("bar.sync 1, %0;" ::"r"(SK_EPI_WARPS * 32) : "memory");
 }
 
-template <bool F4>
-__global__ void __launch_bounds__(SkCfg<F4>::THREADS, 1)
+template <int MODE>
+__global__ void __launch_bounds__(SkCfg<MODE>::THREADS, 1)
     skinny_stats_kernel(const __grid_constant__ CUtensorMap tmH,
                         const __grid_constant__ CUtensorMap tmW, GemmParams p) {
-  using CF = SkCfg<F4>;
+  using CF = SkCfg<MODE>;
+  constexpr bool F4 = CF::F4;
+  constexpr bool X4 = CF::X4;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* bres = smem;                              // [K blocks][16 rows x 128 B]
   uint8_t* wring = bres + CF::B_BYTES;               // [NW][SK_BN rows x 128 B]
-  uint8_t* pring = wring + CF::NW * SK_W_BYTES;      // F4: [NP][codes, scales]
+  uint8_t* pring = wring + CF::NW * CF::W_STAGE;     // F4: [NP][codes, scales]
   uint64_t* wfull = reinterpret_cast<uint64_t*>(pring + CF::NP * CF::PK);
   uint64_t* wempty = wfull + CF::NW;
   uint64_t* pfull = wempty + CF::NW;
@@ -761,7 +790,8 @@ __global__ void __launch_bounds__(SkCfg<F4>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int total_kb = (p.K + BK - 1) / BK;
+  const int total_kb = X4 ? (p.K + SK_X4_KB - 1) / SK_X4_KB : (p.K + BK - 1) / BK;
+  const int n_steps = p.K / 64;   // MODE 2: 64-value K-steps (one scale atom each)
   const int gn = blockIdx.x;
   const int t_begin = (int)((long long)gn * p.n_tiles / p.cpg);
   const int t_end = (int)((long long)(gn + 1) * p.n_tiles / p.cpg);
@@ -769,10 +799,18 @@ __global__ void __launch_bounds__(SkCfg<F4>::THREADS, 1)
 
   if (warp == CF::PRODUCER) {
     if (lane == 0 && has_work) {
-      // the rows, once: every 64-column block of rows [0, 16) (rows >= M read as 0)
-      mbar_arrive_expect_tx(bres_bar, total_kb * SK_B_BLOCK);
-      for (int kb = 0; kb < total_kb; ++kb)
-        tma_load_2d(bres + kb * SK_B_BLOCK, &tmH, bres_bar, kb * BK, 0);
+      if (X4) {
+        // the rows' codes (256-value K blocks of 16 rows), then their scale atoms
+        mbar_arrive_expect_tx(bres_bar, total_kb * SK_X4_ROWS + n_steps * 512);
+        for (int kb = 0; kb < total_kb; ++kb)
+          tma_load_2d(bres + kb * SK_X4_ROWS, &tmH, bres_bar, kb * 128, 0);
+        bulk_load(bres + SK_X4_CODES, p.sf_rows, n_steps * 512, bres_bar);
+      } else {
+        // the rows, once: every 64-column block of rows [0, 16) (rows >= M read as 0)
+        mbar_arrive_expect_tx(bres_bar, total_kb * SK_B_BLOCK);
+        for (int kb = 0; kb < total_kb; ++kb)
+          tma_load_2d(bres + kb * SK_B_BLOCK, &tmH, bres_bar, kb * BK, 0);
+      }
       const uint64_t pol = policy_evict_first();
       int st = 0;
       uint32_t ph = 0, issued = 0, last = 0;
@@ -793,9 +831,21 @@ __global__ void __launch_bounds__(SkCfg<F4>::THREADS, 1)
             const long long r0 = (long long)kb * p.N + (long long)t * SK_BN;
             bulk_load(dst, p.codes4 + r0 * 32, rows * 32, &pfull[st]);
             bulk_load(dst + SK_BN * 32, p.scales4 + r0 * 4, rows * 4, &pfull[st]);
+          } else if (X4) {
+            // the codes of 256 vocabulary rows x 256 values (rows past N read as 0) and
+            // the scale atoms of each existing 128-row half for this block's K-steps
+            uint8_t* dst = wring + st * CF::W_STAGE;
+            const int ns = min(4, n_steps - 4 * kb);
+            const bool half1 = (2 * t + 1) * BM < p.N;
+            mbar_arrive_expect_tx(&wfull[st], SK_W_BYTES + (half1 ? 2 : 1) * ns * 512);
+            tma_load_2d_hint(dst, &tmW, &wfull[st], kb * 128, t * SK_BN, pol);
+            for (int h = 0; h < (half1 ? 2 : 1); ++h)
+              bulk_load(dst + SK_W_BYTES + h * 2048,
+                        p.sf4 + ((long long)(2 * t + h) * n_steps + 4 * kb) * 512, ns * 512,
+                        &wfull[st]);
           } else {
             mbar_arrive_expect_tx(&wfull[st], SK_W_BYTES);
-            tma_load_2d_hint(wring + st * SK_W_BYTES, &tmW, &wfull[st], kb * BK, t * SK_BN, pol);
+            tma_load_2d_hint(wring + st * CF::W_STAGE, &tmW, &wfull[st], kb * BK, t * SK_BN, pol);
           }
           issued |= 1u << st;
           last = (last & ~(1u << st)) | (ph << st);
@@ -813,7 +863,7 @@ __global__ void __launch_bounds__(SkCfg<F4>::THREADS, 1)
     }
   } else if (warp == CF::MMA) {
     if (lane == 0 && has_work) {
-      int ws = 0, acc = 0;
+      int ws = 0, acc = 0, sf_set = 0;
       uint32_t wph = 0, aph = 0;
       bool ok = mbar_wait(F4 ? rows16_bar : bres_bar, 0, abort_flag, p.status);
       for (int t = t_begin; t < t_end && ok; ++t) {
@@ -825,16 +875,50 @@ __global__ void __launch_bounds__(SkCfg<F4>::THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t w_addr = smem_u32(wring + ws * SK_W_BYTES);
-          const uint32_t b_addr = smem_u32(bres + kb * SK_B_BLOCK);
+          const uint32_t w_addr = smem_u32(wring + ws * CF::W_STAGE);
+          if constexpr (X4) {
+            // scales of this K block into tensor memory (columns: W half 0 steps,
+            // W half 1 steps, the rows' steps), then its MMAs; the two column sets
+            // alternate by K block, and the tensor pipe runs the copies and MMAs of
+            // this thread in issue order
+            const uint32_t b_addr = smem_u32(bres + kb * SK_X4_ROWS);
+            const uint32_t sfw = w_addr + SK_W_BYTES;
+            const uint32_t sfr = smem_u32(bres + SK_X4_CODES) + 4 * kb * 512;
+            const uint32_t sf_t = tmem_base + CF::SF_COL + sf_set * 48;
+            const int ns = min(4, n_steps - 4 * kb);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t bdesc = sw128_kmajor_desc(b_addr + kk * 32);
+            for (int ks = 0; ks < 4; ++ks) {
+              if (ks < ns) {
+                tc_cp_32x128b_warpx4(sf_t + ks * 4, plain_kmajor_desc(sfw + ks * 512, 128));
+                tc_cp_32x128b_warpx4(sf_t + 16 + ks * 4,
+                                     plain_kmajor_desc(sfw + 2048 + ks * 512, 128));
+                tc_cp_32x128b_warpx4(sf_t + 32 + ks * 4, plain_kmajor_desc(sfr + ks * 512, 128));
+              }
+            }
 #pragma unroll
-            for (int half = 0; half < 2; ++half)
-              tc_mma_f16(tmem_base + acc * 32 + half * SK_N,
-                         sw128_kmajor_desc(w_addr + half * (BM * 128) + kk * 32), bdesc, CF::IDESC,
-                         (kb > 0 || kk > 0) ? 1u : 0u);
+            for (int ks = 0; ks < 4; ++ks) {
+              if (ks < ns) {
+                const uint64_t bdesc = sw128_kmajor_desc(b_addr + ks * 32);
+#pragma unroll
+                for (int half = 0; half < 2; ++half)
+                  tc_mma_nvf4(tmem_base + acc * 32 + half * SK_N,
+                              sw128_kmajor_desc(w_addr + half * (BM * 128) + ks * 32), bdesc,
+                              CF::IDESC, sf_t + half * 16 + ks * 4, sf_t + 32 + ks * 4,
+                              (kb > 0 || ks > 0) ? 1u : 0u);
+              }
+            }
+            sf_set ^= 1;
+          } else {
+            const uint32_t b_addr = smem_u32(bres + kb * SK_B_BLOCK);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint64_t bdesc = sw128_kmajor_desc(b_addr + kk * 32);
+#pragma unroll
+              for (int half = 0; half < 2; ++half)
+                tc_mma_f16(tmem_base + acc * 32 + half * SK_N,
+                           sw128_kmajor_desc(w_addr + half * (BM * 128) + kk * 32), bdesc,
+                           CF::IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+            }
           }
           tc_commit(&wempty[ws]);
           if (++ws == CF::NW) {
@@ -865,7 +949,7 @@ __global__ void __launch_bounds__(SkCfg<F4>::THREADS, 1)
                         mbar_wait(&pfull[ps], pph, abort_flag, p.status) &&
                             mbar_wait(&wempty[ws], wph ^ 1u, abort_flag, p.status));
         if (!ok) break;
-        uint8_t* s_b = wring + ws * SK_W_BYTES;
+        uint8_t* s_b = wring + ws * CF::W_STAGE;
         const uint8_t* s_c = pring + ps * CF::PK;
         const uint8_t* s_s = s_c + SK_BN * 32;
         for (int u = ci; u < 2 * SK_BN; u += 32 * SK_CONV_WARPS) {
@@ -922,7 +1006,9 @@ __global__ void __launch_bounds__(SkCfg<F4>::THREADS, 1)
     // ---- epilogue: lane = vocabulary row of a 128-row half, 16 columns = rows ----
     const int q = warp;
     const int M = p.M;
-    const float gs = F4 ? __ldg(p.gscale) : 1.f;
+    const float gs = F4   ? __ldg(p.gscale)
+                     : X4 ? __ldg(p.gscale) * __ldg(p.gscale_rows)
+                          : 1.f;
     float m[SK_N], s[SK_N], tt[SK_N], best[SK_N];
     int bidx[SK_N];
 #pragma unroll
@@ -1280,19 +1366,19 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const Gemm
 // The skinny pass of M <= 16 rows (see skinny_stats_kernel).
 bool skinny_ok(int M, int K) { return M <= SK_N && (K + BK - 1) / BK <= SK_MAX_KB; }
 
-template <bool F4>
+template <int MODE>
 cudaError_t launch_skinny(const CUtensorMap& th, const CUtensorMap& tw, const GemmParams& p,
                           cudaStream_t st) {
-  using CF = SkCfg<F4>;
+  using CF = SkCfg<MODE>;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(skinny_stats_kernel<F4>,
+    cudaError_t e = cudaFuncSetAttribute(skinny_stats_kernel<MODE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          CF::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  skinny_stats_kernel<F4><<<p.cpg, CF::THREADS, CF::SMEM_BYTES, st>>>(th, tw, p);
+  skinny_stats_kernel<MODE><<<p.cpg, CF::THREADS, CF::SMEM_BYTES, st>>>(th, tw, p);
   return cudaGetLastError();
 }
 
@@ -1333,7 +1419,7 @@ cudaError_t run_stats(const uint16_t* h, int M, const uint16_t* w, int V, int D,
     CUtensorMap th;   // the rows as 64 x 16 boxes (rows past M read as 0)
     if (!dgi::make_tmap_bf16_2d(&th, h, D, M, (uint64_t)D * 2, BK, SK_N))
       return cudaErrorInvalidValue;
-    e = launch_skinny<false>(th, tb, p, st);
+    e = launch_skinny<0>(th, tb, p, st);
   } else {
     e = (mt == 1) ? launch_gemm<1, STATS_BN, EPI_STATS>(ta, tb, p, groups * p.cpg, st)
                   : launch_gemm<2, STATS_BN, EPI_STATS>(ta, tb, p, groups * p.cpg, st);
@@ -1424,13 +1510,57 @@ cudaError_t run_stats_nvfp4(const uint16_t* h, int M, const uint8_t* codes, cons
     CUtensorMap th;
     if (!dgi::make_tmap_bf16_2d(&th, h, D, M, (uint64_t)D * 2, BK, SK_N))
       return cudaErrorInvalidValue;
-    e = launch_skinny<true>(th, th, p, st);
+    e = launch_skinny<1>(th, th, p, st);
   } else {
     e = (mt == 1) ? launch_stats4<1>(ta, p, groups * p.cpg, st)
                   : launch_stats4<2>(ta, p, groups * p.cpg, st);
   }
   if (e != cudaSuccess) return e;
   stats_finalize_kernel<<<(M + 7) / 8, 256, 0, st>>>(part, p.cpg, M, inv_t, out.lse,
+                                                     out.entropy, out.maxz, out.argmax, p.gl, V,
+                                                     p.status);
+  return cudaGetLastError();
+}
+
+// Both operands NVFP4 on the block-scaled kind, at most 16 rows: the rows are
+// quantised into the workspace (codes, scale atoms, tensor scale; after the
+// partials and the label-gather scratch), then the skinny pass in MODE 2.
+size_t x4_rows_offset(int M, int V) {
+  return dgi::lmhead_ws_bytes(M, V) + dgi::align_up((size_t)M * 4, 256);
+}
+
+cudaError_t run_stats_nvfp4_mma(const uint16_t* h, int M, const uint8_t* codes, const uint8_t* sf,
+                                const float* g, int V, int D, const float* inv_t,
+                                dgi::RowStats out, void* ws, cudaStream_t st,
+                                const dgi::LabelGather* gather) {
+  using dgi::align_up;
+  uint8_t* rc = static_cast<uint8_t*>(ws) + x4_rows_offset(M, V);
+  uint8_t* rsf = rc + align_up((size_t)SK_N * (D / 2), 256);
+  float* rg = reinterpret_cast<float*>(rsf + align_up((size_t)(D / 64) * 512, 256));
+  cudaError_t e = dgi::quantize_rows_nvfp4_mma(h, M, D, rc, rsf, rg, st);
+  if (e != cudaSuccess) return e;
+  CUtensorMap th, tw;
+  if (!dgi::make_tmap_u8_2d(&th, rc, D / 2, SK_N, D / 2, 128, SK_N)) return cudaErrorInvalidValue;
+  if (!dgi::make_tmap_u8_2d(&tw, codes, D / 2, V, D / 2, 128, SK_BN)) return cudaErrorInvalidValue;
+  if ((e = gather_prepare(gather, M, st)) != cudaSuccess) return e;
+  GemmParams p{};
+  p.M = M;
+  p.N = V;
+  p.K = D;
+  p.cpg = stats_cpg(M, V);
+  p.n_tiles = (V + SK_BN - 1) / SK_BN;
+  p.inv_t = inv_t;
+  p.codes4 = codes;
+  p.sf4 = sf;
+  p.gscale = g;
+  p.sf_rows = rsf;
+  p.gscale_rows = rg;
+  p.part = static_cast<float*>(ws);
+  p.status = dgi::status_ptr();
+  if (gather) p.gl = *gather;
+  e = launch_skinny<2>(th, tw, p, st);
+  if (e != cudaSuccess) return e;
+  stats_finalize_kernel<<<(M + 7) / 8, 256, 0, st>>>(p.part, p.cpg, M, inv_t, out.lse,
                                                      out.entropy, out.maxz, out.argmax, p.gl, V,
                                                      p.status);
   return cudaGetLastError();
@@ -1502,6 +1632,22 @@ cudaError_t lmhead_stats_nvfp4(const uint16_t* h, int M, const uint8_t* codes,
                                const LabelGather* gather) {
   return run_stats_nvfp4(h, M, codes, scales, g, V, D, inv_t, out, static_cast<float*>(ws), st,
                          gather);
+}
+
+size_t lmhead_nvfp4_mma_ws_bytes(int M, int V, int D) {
+  return x4_rows_offset(M, V) + align_up((size_t)SK_N * (D / 2), 256) +
+         align_up((size_t)(D / 64) * 512, 256) + 256;
+}
+
+bool lmhead_nvfp4_mma_ok(int M, int D) {
+  return M >= 1 && M <= SK_N && D >= 64 && D % 64 == 0 && D <= 12 * SK_X4_KB;
+}
+
+cudaError_t lmhead_stats_nvfp4_mma(const uint16_t* h, int M, const uint8_t* codes,
+                                   const uint8_t* sf, const float* g, int V, int D,
+                                   const float* inv_t, RowStats out, void* ws, cudaStream_t st,
+                                   const LabelGather* gather) {
+  return run_stats_nvfp4_mma(h, M, codes, sf, g, V, D, inv_t, out, ws, st, gather);
 }
 
 size_t selfcond_ws_bytes(int M, int V, int D) {

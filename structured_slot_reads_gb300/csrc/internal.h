@@ -87,6 +87,24 @@ cudaError_t lmhead_stats_nvfp4(const uint16_t* h, int M, const uint8_t* codes,
                                const uint8_t* scales, const float* g, int V, int D,
                                const float* inv_t, RowStats out, void* ws, cudaStream_t st,
                                const LabelGather* gather = nullptr);
+// NVFP4 in the layout of the block-scaled MMA pass: codes row-major [rows][cols/2],
+// scales as 512-byte atoms [ceil(rows/128)][cols/64] (row 32 j + l of a 128-row
+// tile at byte 16 l + 4 j of its atom), *g the fp32 tensor scale.
+cudaError_t quantize_nvfp4_mma(const uint16_t* x, int rows, int cols, uint8_t* codes, uint8_t* sf,
+                               float* g, cudaStream_t st);
+// The same for at most 16 rows in one launch: codes [16][cols/2] (rows >= M zero),
+// scale atoms [cols/64][512] (one tile), *g.
+cudaError_t quantize_rows_nvfp4_mma(const uint16_t* x, int M, int cols, uint8_t* codes,
+                                    uint8_t* sf, float* g, cudaStream_t st);
+// lm-head statistics with both operands in NVFP4 on the block-scaled tensor-core kind:
+// z = (sum_k e2m1_h s_h e2m1_w s_w) * g_h * g_w / T, at most 16 rows (quantised in the
+// call).  Workspace: lmhead_nvfp4_mma_ws_bytes.
+size_t lmhead_nvfp4_mma_ws_bytes(int M, int V, int D);
+bool lmhead_nvfp4_mma_ok(int M, int D);
+cudaError_t lmhead_stats_nvfp4_mma(const uint16_t* h, int M, const uint8_t* codes,
+                                   const uint8_t* sf, const float* g, int V, int D,
+                                   const float* inv_t, RowStats out, void* ws, cudaStream_t st,
+                                   const LabelGather* gather = nullptr);
 size_t probs_embed8_ws_bytes(int M, int V, int D);
 cudaError_t probs_embed8(const uint8_t* p8, const float* p_scale, const float* row_scale, int M,
                          const uint8_t* e8t, const float* e_scale, int V, int D, float* out,

@@ -195,6 +195,39 @@ __device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, 
       : "memory");
 }
 
+// D[tmem] (+)= (A * SFA)[smem desc] * (B * SFB)[smem desc]^T with NVFP4 operands on the
+// block-scaled kind: packed e2m1 A and B (K = 64 per instruction, 32 bytes a row),
+// one e4m3 scale per 16 elements (scale_vec::4X) read from tensor memory at
+// sfa / sfb: four columns per instruction, in the layout tcgen05.cp .32x128b.warpx4
+// writes (both addresses a multiple of 4 columns).
+__device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate));
+}
+
+// Shared memory -> tensor memory: 32 rows of 16 bytes (a no-swizzle K-major tile,
+// desc), written to lanes [0, 32) of four consecutive columns and repeated in the
+// other three lane quarters.
+__device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc));
+}
+
+// Shared-memory matrix descriptor of a K-major tile without swizzling: 8-row x
+// 16-byte core matrices (128 contiguous bytes), `sbo` bytes apart along M/N.
+__device__ __forceinline__ uint64_t plain_kmajor_desc(uint32_t smem_addr, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;                              // leading byte offset (one core matrix)
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
 // D[tmem] (+)= A[smem desc] * B[smem desc]^T with 8-bit float operands (kind::f8f6f4).
 __device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
@@ -308,6 +341,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4)                       // D format: f32
          | (1u << 7)                     // A format: bf16
          | (1u << 10)                    // B format: bf16
+         | ((uint32_t)(N >> 3) << 17)    // N / 8
+         | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+// Instruction descriptor, kind::mxf4nvf4 (block-scaled): e2m1 A and B (format code 1),
+// both K-major, e4m3 scale factors (scale type 0), scale factor ids 0, fp32 D.
+__host__ __device__ constexpr uint32_t idesc_nvf4_f32(int M, int N) {
+  return (1u << 7)                       // A format: e2m1
+         | (1u << 10)                    // B format: e2m1
          | ((uint32_t)(N >> 3) << 17)    // N / 8
          | ((uint32_t)(M >> 4) << 24);   // M / 16
 }

@@ -233,21 +233,13 @@ __device__ __forceinline__ uint32_t e2m1_code(float y) {
   return m | ((m != 0u && signbit(y)) ? 8u : 0u);
 }
 
-// One thread per (K block of 64, row): consecutive threads take consecutive rows,
-// so the code and scale writes of a warp are contiguous.
-__global__ void quantize_nvfp4_kernel(const __nv_bfloat16* x, int rows, int cols,
-                                      const unsigned int* amax_bits, uint8_t* codes,
-                                      uint8_t* scales) {
-  const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const int nkb = cols / 64;
-  if (t >= (long long)rows * nkb) return;
-  const int kb = (int)(t / rows);
-  const int v = (int)(t % rows);
-  const float g = nvfp4_tensor_scale(*amax_bits);
-  const uint4* src = reinterpret_cast<const uint4*>(x + (long long)v * cols + kb * 64);
-  uint4* cdst = reinterpret_cast<uint4*>(codes + ((long long)kb * rows + v) * 32);
+// NVFP4 codes and block scales of 64 consecutive values of a row (four blocks of
+// 16): the 32 code bytes as eight words in cw (element 2i in the low nibble of
+// byte i); returns the four e4m3 scale bytes in one word (block q in byte q).
+__device__ __forceinline__ uint32_t nvfp4_quant64(const __nv_bfloat16* x64, float g,
+                                                  uint32_t (&cw)[8]) {
+  const uint4* src = reinterpret_cast<const uint4*>(x64);
   uint32_t sc4 = 0;
-  uint32_t cw[8];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     float xv[16];
@@ -281,9 +273,98 @@ __global__ void quantize_nvfp4_kernel(const __nv_bfloat16* x, int rows, int cols
       cw[2 * q + i] = word;
     }
   }
+  return sc4;
+}
+
+// One thread per (K block of 64, row): consecutive threads take consecutive rows,
+// so the code and scale writes of a warp are contiguous.
+__global__ void quantize_nvfp4_kernel(const __nv_bfloat16* x, int rows, int cols,
+                                      const unsigned int* amax_bits, uint8_t* codes,
+                                      uint8_t* scales) {
+  const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int nkb = cols / 64;
+  if (t >= (long long)rows * nkb) return;
+  const int kb = (int)(t / rows);
+  const int v = (int)(t % rows);
+  const float g = nvfp4_tensor_scale(*amax_bits);
+  uint32_t cw[8];
+  const uint32_t sc4 = nvfp4_quant64(x + (long long)v * cols + kb * 64, g, cw);
+  uint4* cdst = reinterpret_cast<uint4*>(codes + ((long long)kb * rows + v) * 32);
   cdst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
   cdst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
   *reinterpret_cast<uint32_t*>(scales + ((long long)kb * rows + v) * 4) = sc4;
+}
+
+// The layout of the block-scaled MMA pass (tcgen05 kind::mxf4nvf4): codes row-major
+// [rows][cols/2]; the scales as one 512-byte atom per 128-row tile and 64-column
+// K-step, atoms [ceil(rows/128)][cols/64], row 32 j + l of the tile at byte
+// 16 l + 4 j (its four blocks of 16 in the four bytes), the order in which
+// tcgen05.cp .32x128b.warpx4 places them in tensor memory.  Rows of the last tile
+// past `rows` get scale 0.  One thread per (K-step, padded row).
+__device__ __forceinline__ long long nvfp4_atom_offset(int v, int ks, int nks) {
+  return ((long long)(v >> 7) * nks + ks) * 512 + (v & 31) * 16 + ((v >> 5) & 3) * 4;
+}
+
+__global__ void quantize_nvfp4_mma_kernel(const __nv_bfloat16* x, int rows, int cols,
+                                          const unsigned int* amax_bits, uint8_t* codes,
+                                          uint8_t* sf) {
+  const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int nks = cols / 64;
+  const int rows_pad = (rows + 127) & ~127;
+  if (t >= (long long)rows_pad * nks) return;
+  const int ks = (int)(t / rows_pad);
+  const int v = (int)(t % rows_pad);
+  uint32_t sc4 = 0;
+  if (v < rows) {
+    uint32_t cw[8];
+    sc4 = nvfp4_quant64(x + (long long)v * cols + ks * 64, nvfp4_tensor_scale(*amax_bits), cw);
+    uint4* cdst = reinterpret_cast<uint4*>(codes + (long long)v * (cols / 2) + ks * 32);
+    cdst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+    cdst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+  }
+  *reinterpret_cast<uint32_t*>(sf + nvfp4_atom_offset(v, ks, nks)) = sc4;
+}
+
+// The rows of a block-scaled pass (at most 16), in one CTA: the tensor scale from
+// the rows' largest magnitude, then codes [16][cols/2] (rows >= M all 0) and the
+// scale atoms [cols/64][512] of one 128-row tile (rows >= M scale 0), then g.
+__global__ void __launch_bounds__(256)
+    quantize_rows_nvfp4_mma_kernel(const __nv_bfloat16* x, int M, int cols, uint8_t* codes,
+                                   uint8_t* sf, float* g_out) {
+  __shared__ float wmax[8];
+  float m = 0.f;
+  const long long n8 = (long long)M * cols / 8;
+  for (long long i = threadIdx.x; i < n8; i += blockDim.x) {
+    const uint4 u = reinterpret_cast<const uint4*>(x)[i];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+      m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+  const int nks = cols / 64;
+  for (int i = threadIdx.x; i < nks * 128; i += blockDim.x)
+    reinterpret_cast<uint32_t*>(sf)[i] = 0u;
+  __syncthreads();
+  float a = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) a = fmaxf(a, wmax[w]);
+  const float g = nvfp4_tensor_scale(__float_as_uint(a));
+  for (int i = threadIdx.x; i < 16 * nks; i += blockDim.x) {
+    const int r = i & 15, ks = i >> 4;
+    uint32_t cw[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    if (r < M) {
+      const uint32_t sc4 = nvfp4_quant64(x + (long long)r * cols + ks * 64, g, cw);
+      *reinterpret_cast<uint32_t*>(sf + nvfp4_atom_offset(r, ks, nks)) = sc4;
+    }
+    uint4* cdst = reinterpret_cast<uint4*>(codes + (long long)r * (cols / 2) + ks * 32);
+    cdst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+    cdst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+  }
+  if (threadIdx.x == 0) *g_out = g;
 }
 
 __global__ void nvfp4_scale_kernel(float* g_io) {
@@ -308,6 +389,29 @@ cudaError_t quantize_nvfp4(const uint16_t* x, int rows, int cols, uint8_t* codes
   quantize_nvfp4_kernel<<<(int)((items + 127) / 128), 128, 0, st>>>(
       reinterpret_cast<const __nv_bfloat16*>(x), rows, cols, amax, codes, scales);
   nvfp4_scale_kernel<<<1, 1, 0, st>>>(g);
+  return cudaGetLastError();
+}
+
+cudaError_t quantize_nvfp4_mma(const uint16_t* x, int rows, int cols, uint8_t* codes, uint8_t* sf,
+                               float* g, cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  unsigned int* amax = reinterpret_cast<unsigned int*>(g);
+  cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(unsigned int), st);
+  if (e != cudaSuccess) return e;
+  const long long n8 = (long long)rows * cols / 8;
+  tensor_amax_kernel<<<(int)std::min<long long>((n8 + 255) / 256, 4096), 256, 0, st>>>(
+      reinterpret_cast<const uint4*>(x), n8, amax);
+  const long long items = (long long)((rows + 127) & ~127) * (cols / 64);
+  quantize_nvfp4_mma_kernel<<<(int)((items + 127) / 128), 128, 0, st>>>(
+      reinterpret_cast<const __nv_bfloat16*>(x), rows, cols, amax, codes, sf);
+  nvfp4_scale_kernel<<<1, 1, 0, st>>>(g);
+  return cudaGetLastError();
+}
+
+cudaError_t quantize_rows_nvfp4_mma(const uint16_t* x, int M, int cols, uint8_t* codes,
+                                    uint8_t* sf, float* g, cudaStream_t st) {
+  quantize_rows_nvfp4_mma_kernel<<<1, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(x), M,
+                                                     cols, codes, sf, g);
   return cudaGetLastError();
 }
 

@@ -22,6 +22,7 @@ DG_DEV_TIMEOUT, DG_DEV_BAD_PAGE, DG_DEV_BAD_LABEL, DG_DEV_BAD_INDEX = 1, 2, 4, 8
 DG_DEV_RANGE = 16
 DG_WS_ATTN, DG_WS_LMHEAD, DG_WS_SLOT_READ, DG_WS_SELFCOND = 1, 2, 3, 4
 DG_WS_HEADS, DG_WS_PROBS_EMBED, DG_WS_PREFILL, DG_WS_PROBS_EMBED8 = 5, 6, 7, 8
+DG_WS_LMHEAD_NVFP4_MMA = 9
 DG_MAX_LABELS = MAX_LABELS = 26
 DG_MAX_WIDE_LABELS = 256
 DG_NOALLOC_MAX_ROWS = 512
@@ -72,6 +73,9 @@ _SIGS = {
     "dg_quantize_nvfp4": [P, I, I, P, P, P, P],
     "dg_lmhead_logsoftmax_entropy_nvfp4": [DP, P, I, P, P, P, P, P, P, P, I, P, P, P, P, P, P,
                                            Z, P],
+    "dg_quantize_nvfp4_mma": [P, I, I, P, P, P, P],
+    "dg_lmhead_logsoftmax_entropy_nvfp4_mma": [DP, P, I, P, P, P, P, P, P, P, I, P, P, P, P, P,
+                                               P, Z, P],
     "dg_commit": [DP, P, P, P, P, P, P, P, P, P, P],
     "dg_selfcond_embed": [DP, P, I, P, P, P, P, P, P, Z, P],
     "dg_denoise_heads": [DP, P, I, P, I, P, P, P, P, P, P, P, P, P, P, I, P, P, P, Z, P, Z, P],
@@ -257,6 +261,21 @@ def dg_lmhead_logsoftmax_entropy_nvfp4(dims, h, M, codes, scales, g, inv_t, slot
                                                     _p(entropy), _p(maxz), _p(argmax),
                                                     _p(label_lp), _p(workspace),
                                                     _nbytes(workspace), _s(stream))
+
+
+def dg_quantize_nvfp4_mma(x, rows, cols, codes, sf, g, stream=None):
+    return lib().dg_quantize_nvfp4_mma(_p(x), rows, cols, _p(codes), _p(sf), _p(g), _s(stream))
+
+
+def dg_lmhead_logsoftmax_entropy_nvfp4_mma(dims, h, M, codes, sf, g, inv_t, slot_row, label_ids,
+                                           n_labels, S, lse, entropy, maxz, argmax, label_lp,
+                                           workspace, stream=None):
+    return lib().dg_lmhead_logsoftmax_entropy_nvfp4_mma(ctypes.byref(dims), _p(h), M, _p(codes),
+                                                        _p(sf), _p(g), _p(inv_t), _p(slot_row),
+                                                        _p(label_ids), _p(n_labels), S, _p(lse),
+                                                        _p(entropy), _p(maxz), _p(argmax),
+                                                        _p(label_lp), _p(workspace),
+                                                        _nbytes(workspace), _s(stream))
 
 
 def dg_commit(dims, entropy, argmax, cand, gamma, committed_state, token_state, commit, tokens,

@@ -328,21 +328,30 @@ class LmHead:
     """One lm-head statistics pass over M rows (lse, entropy, max logit, argmax), on bf16
     operands (dg_lmhead_logsoftmax_entropy), on e4m3 operands with per-row scales
     (dg_quantize_rows_e4m3 of the rows, then dg_lmhead_logsoftmax_entropy_fp8), or on
-    bf16 rows against NVFP4 weights (dg_lmhead_logsoftmax_entropy_nvfp4); W is
-    quantised once, when the object is made."""
+    bf16 rows against NVFP4 weights (dg_lmhead_logsoftmax_entropy_nvfp4), or with rows
+    and weights both NVFP4 on the block-scaled kind (fp4_mma: at most 16 rows,
+    dg_lmhead_logsoftmax_entropy_nvfp4_mma); W is quantised once, when the object is
+    made."""
 
-    def __init__(self, shape, w, M, fp8=False, device="cuda", fp4=False):
+    def __init__(self, shape, w, M, fp8=False, device="cuda", fp4=False, fp4_mma=False):
         f32, i32, u8 = torch.float32, torch.int32, torch.uint8
-        self.shape, self.M, self.fp8, self.fp4 = shape, M, fp8, fp4
+        self.shape, self.M, self.fp8, self.fp4, self.fp4_mma = shape, M, fp8, fp4, fp4_mma
         self.dims = dg.make_dims(d_model=shape.D, V=shape.V)
         self.h = torch.empty((M, shape.D), dtype=torch.bfloat16, device=device)
         self.inv_t = torch.empty(M, dtype=f32, device=device)
         self.lse, self.ent, self.maxz = (torch.empty(M, dtype=f32, device=device)
                                          for _ in range(3))
         self.argmax = torch.empty(M, dtype=i32, device=device)
-        self.ws = torch.empty(dg.dg_workspace_bytes(self.dims, dg.DG_WS_LMHEAD, M), dtype=u8,
-                              device=device)
+        kind = dg.DG_WS_LMHEAD_NVFP4_MMA if fp4_mma else dg.DG_WS_LMHEAD
+        self.ws = torch.empty(dg.dg_workspace_bytes(self.dims, kind, M), dtype=u8, device=device)
         self.w = w
+        if fp4_mma:
+            D, V = shape.D, shape.V
+            self.codes = torch.empty((V, D // 2), dtype=u8, device=device)
+            self.sf = torch.empty(((V + 127) // 128, D // 64, 512), dtype=u8, device=device)
+            self.g = torch.empty(1, dtype=f32, device=device)
+            dg._check(dg.dg_quantize_nvfp4_mma(w, V, D, self.codes, self.sf, self.g),
+                      "dg_quantize_nvfp4_mma")
         if fp4:
             D, V = shape.D, shape.V
             self.codes = torch.empty((D // 64, V, 32), dtype=u8, device=device)
@@ -361,6 +370,15 @@ class LmHead:
     def run(self, step_idx=0, stream=None):
         """Enqueue one pass; returns the number of library kernels."""
         d = self.dims
+        if self.fp4_mma:
+            dg._check(dg.dg_lmhead_logsoftmax_entropy_nvfp4_mma(d, self.h, self.M, self.codes,
+                                                                self.sf, self.g, self.inv_t,
+                                                                None, None, None, 0, self.lse,
+                                                                self.ent, self.maxz,
+                                                                self.argmax, None, self.ws,
+                                                                stream),
+                      "dg_lmhead_logsoftmax_entropy_nvfp4_mma")
+            return 3
         if self.fp4:
             dg._check(dg.dg_lmhead_logsoftmax_entropy_nvfp4(d, self.h, self.M, self.codes,
                                                             self.scales, self.g, self.inv_t,
