@@ -671,7 +671,8 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
 // (K blocks of 256 values, 128 bytes a row, by TMA) and each K block's scale atoms
 // (bulk copies); the MMA warp moves the scales into tensor memory with
 // tcgen05.cp (.32x128b.warpx4, one 512-byte atom per 128 rows and 64-value
-// K-step) before the MMAs that read them, alternating two sets of columns.
+// K-step): the rows' scales once, after the rows arrive, and each K block's W
+// scales before the MMAs that read them, alternating two sets of columns.
 // ---------------------------------------------------------------------------
 constexpr int SK_N = 16;                    // rows of B (the MMAs' N)
 constexpr int SK_BN = 256;                  // vocabulary rows per tile: two M = 128 MMAs
@@ -686,6 +687,8 @@ constexpr int SK_X4_KB = 256;               // MODE 2: values of a K block (128 
 constexpr int SK_X4_ROWS = SK_N * 128;      // MODE 2: the rows' codes of a K block (2 KB)
 constexpr int SK_X4_CODES = 12 * SK_X4_ROWS;   // MODE 2: resident row codes, d_model <= 3072
 constexpr int SK_X4_SFA = 2 * 4 * 512;      // MODE 2: W scale atoms of a K block (2 x 4 steps)
+constexpr int SK_X4_SFW_COL = 64;           // MODE 2: tensor-memory columns of the W scales
+constexpr int SK_X4_SFR_COL = 256;          // MODE 2: ... and of the rows' scales
 
 template <int MODE>
 struct SkCfg {
@@ -708,10 +711,9 @@ struct SkCfg {
   static constexpr int MMA = SK_EPI_WARPS + 1;
   static constexpr int CONV0 = SK_EPI_WARPS + 2;           // F4: converter warps
   static constexpr int THREADS = (SK_EPI_WARPS + 2 + (F4 ? SK_CONV_WARPS : 0)) * 32;
-  // 2 stages x 2 halves x 16 columns; MODE 2: then two sets of 48 scale columns
-  // (W: 2 halves x 4 steps x 4, rows: 4 steps x 4)
-  static constexpr int TMEM_COLS = X4 ? 256 : 64;
-  static constexpr int SF_COL = 64;
+  // 2 stages x 2 halves x 16 columns; MODE 2: then two sets of 32 W scale columns
+  // (2 halves x 4 steps x 4) and, from column 256, the rows' scales (4 a step)
+  static constexpr int TMEM_COLS = X4 ? 512 : 64;
   // bf16 W: bf16 operands.  NVFP4 W: f16 operands (the widening is then two
   // instructions a code pair, and every e2m1 x e4m3 product is an f16)
   static constexpr uint32_t IDESC = X4   ? idesc_nvf4_f32(BM, SK_N)
@@ -866,6 +868,13 @@ __global__ void __launch_bounds__(SkCfg<MODE>::THREADS, 1)
       int ws = 0, acc = 0, sf_set = 0;
       uint32_t wph = 0, aph = 0;
       bool ok = mbar_wait(F4 ? rows16_bar : bres_bar, 0, abort_flag, p.status);
+      if (X4 && ok) {
+        // the rows' scales, resident for the whole pass
+        const uint32_t sfr = smem_u32(bres + SK_X4_CODES);
+        for (int s = 0; s < n_steps; ++s)
+          tc_cp_32x128b_warpx4(tmem_base + SK_X4_SFR_COL + 4 * s,
+                               plain_kmajor_desc(sfr + s * 512, 128));
+      }
       for (int t = t_begin; t < t_end && ok; ++t) {
         if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
@@ -877,14 +886,13 @@ __global__ void __launch_bounds__(SkCfg<MODE>::THREADS, 1)
           tc_fence_after();
           const uint32_t w_addr = smem_u32(wring + ws * CF::W_STAGE);
           if constexpr (X4) {
-            // scales of this K block into tensor memory (columns: W half 0 steps,
-            // W half 1 steps, the rows' steps), then its MMAs; the two column sets
-            // alternate by K block, and the tensor pipe runs the copies and MMAs of
-            // this thread in issue order
+            // W scales of this K block into tensor memory (columns: half 0 steps,
+            // half 1 steps), then its MMAs; the two column sets alternate by K
+            // block, and the tensor pipe runs the copies and MMAs of this thread in
+            // issue order
             const uint32_t b_addr = smem_u32(bres + kb * SK_X4_ROWS);
             const uint32_t sfw = w_addr + SK_W_BYTES;
-            const uint32_t sfr = smem_u32(bres + SK_X4_CODES) + 4 * kb * 512;
-            const uint32_t sf_t = tmem_base + CF::SF_COL + sf_set * 48;
+            const uint32_t sf_t = tmem_base + SK_X4_SFW_COL + sf_set * 32;
             const int ns = min(4, n_steps - 4 * kb);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
@@ -892,7 +900,6 @@ __global__ void __launch_bounds__(SkCfg<MODE>::THREADS, 1)
                 tc_cp_32x128b_warpx4(sf_t + ks * 4, plain_kmajor_desc(sfw + ks * 512, 128));
                 tc_cp_32x128b_warpx4(sf_t + 16 + ks * 4,
                                      plain_kmajor_desc(sfw + 2048 + ks * 512, 128));
-                tc_cp_32x128b_warpx4(sf_t + 32 + ks * 4, plain_kmajor_desc(sfr + ks * 512, 128));
               }
             }
 #pragma unroll
@@ -903,7 +910,8 @@ __global__ void __launch_bounds__(SkCfg<MODE>::THREADS, 1)
                 for (int half = 0; half < 2; ++half)
                   tc_mma_nvf4(tmem_base + acc * 32 + half * SK_N,
                               sw128_kmajor_desc(w_addr + half * (BM * 128) + ks * 32), bdesc,
-                              CF::IDESC, sf_t + half * 16 + ks * 4, sf_t + 32 + ks * 4,
+                              CF::IDESC, sf_t + half * 16 + ks * 4,
+                              tmem_base + SK_X4_SFR_COL + 4 * (4 * kb + ks),
                               (kb > 0 || ks > 0) ? 1u : 0u);
               }
             }

@@ -325,9 +325,12 @@ __global__ void quantize_nvfp4_mma_kernel(const __nv_bfloat16* x, int rows, int 
   *reinterpret_cast<uint32_t*>(sf + nvfp4_atom_offset(v, ks, nks)) = sc4;
 }
 
-// The rows of a block-scaled pass (at most 16), in one CTA: the tensor scale from
-// the rows' largest magnitude, then codes [16][cols/2] (rows >= M all 0) and the
-// scale atoms [cols/64][512] of one 128-row tile (rows >= M scale 0), then g.
+// The rows of a block-scaled pass (at most 16): one thread per (row slot, block of
+// 16 values), 16 x cols/16 threads.  Each CTA first takes the tensor scale from the
+// largest magnitude of all M rows (every CTA the same value: the maximum is exact in
+// any order), then writes its blocks' codes (rows >= M all 0) and e4m3 scales into
+// the atoms of one 128-row tile; the atoms' other bytes (rows 16..127) are zeroed by
+// the threads in turn.  CTA 0 writes g.
 __global__ void __launch_bounds__(256)
     quantize_rows_nvfp4_mma_kernel(const __nv_bfloat16* x, int M, int cols, uint8_t* codes,
                                    uint8_t* sf, float* g_out) {
@@ -346,25 +349,51 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
-  const int nks = cols / 64;
-  for (int i = threadIdx.x; i < nks * 128; i += blockDim.x)
-    reinterpret_cast<uint32_t*>(sf)[i] = 0u;
   __syncthreads();
   float a = 0.f;
   for (int w = 0; w < (int)(blockDim.x >> 5); ++w) a = fmaxf(a, wmax[w]);
   const float g = nvfp4_tensor_scale(__float_as_uint(a));
-  for (int i = threadIdx.x; i < 16 * nks; i += blockDim.x) {
-    const int r = i & 15, ks = i >> 4;
-    uint32_t cw[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-    if (r < M) {
-      const uint32_t sc4 = nvfp4_quant64(x + (long long)r * cols + ks * 64, g, cw);
-      *reinterpret_cast<uint32_t*>(sf + nvfp4_atom_offset(r, ks, nks)) = sc4;
-    }
-    uint4* cdst = reinterpret_cast<uint4*>(codes + (long long)r * (cols / 2) + ks * 32);
-    cdst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-    cdst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+  const int nb = cols / 16, nks = cols / 64;
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  // zero the atom words that hold no row < 16 (row l < 16, j = 0 is word 4 l)
+  for (int wi = t; wi < nks * 128; wi += gridDim.x * blockDim.x) {
+    const int wa = wi & 127;
+    if (wa >= 64 || (wa & 3) != 0) reinterpret_cast<uint32_t*>(sf)[wi] = 0u;
   }
-  if (threadIdx.x == 0) *g_out = g;
+  if (t >= 16 * nb) return;
+  const int r = t / nb, blk = t % nb;   // consecutive threads: consecutive blocks of a row
+  uint32_t c0 = 0u, c1 = 0u;
+  uint8_t sb = 0;
+  if (r < M) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (long long)r * cols + blk * 16);
+    float xv[16];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 u = src[h];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+        xv[8 * h + 2 * k] = f.x;
+        xv[8 * h + 2 * k + 1] = f.y;
+      }
+    }
+    float bm = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) bm = fmaxf(bm, fabsf(xv[j]));
+    const __nv_fp8_storage_t s8 = __nv_cvt_float_to_fp8((bm / 6.f) / g, __NV_SATFINITE, __NV_E4M3);
+    const __half_raw hr = __nv_cvt_fp8_to_halfraw(s8, __NV_E4M3);
+    const float den = __half2float(__half(hr)) * g;
+    sb = (uint8_t)s8;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      c0 |= (den > 0.f ? e2m1_code(xv[j] / den) : 0u) << (4 * j);
+      c1 |= (den > 0.f ? e2m1_code(xv[8 + j] / den) : 0u) << (4 * j);
+    }
+  }
+  *reinterpret_cast<uint2*>(codes + (long long)r * (cols / 2) + blk * 8) = make_uint2(c0, c1);
+  sf[(long long)(blk >> 2) * 512 + r * 16 + (blk & 3)] = sb;
+  if (t == 0) *g_out = g;
 }
 
 __global__ void nvfp4_scale_kernel(float* g_io) {
@@ -410,8 +439,9 @@ cudaError_t quantize_nvfp4_mma(const uint16_t* x, int rows, int cols, uint8_t* c
 
 cudaError_t quantize_rows_nvfp4_mma(const uint16_t* x, int M, int cols, uint8_t* codes,
                                     uint8_t* sf, float* g, cudaStream_t st) {
-  quantize_rows_nvfp4_mma_kernel<<<1, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(x), M,
-                                                     cols, codes, sf, g);
+  const int threads = 16 * (cols / 16);
+  quantize_rows_nvfp4_mma_kernel<<<(threads + 255) / 256, 256, 0, st>>>(
+      reinterpret_cast<const __nv_bfloat16*>(x), M, cols, codes, sf, g);
   return cudaGetLastError();
 }
 
