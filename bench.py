@@ -38,6 +38,7 @@ LMHEAD_KINDS = ("lmhead", "lmhead_fp8", "lmhead_fp4", "lmhead_fp4mma")
 WORKLOADS = {
     "full_canvas_step": ("step", "FULL_CANVAS", {}),
     "single_structured_read": ("read", "SINGLE_READ", {}),
+    "single_structured_read_nvfp4": ("read_fp4", "SINGLE_READ", {}),
     "mixed_batched_reads": ("two_stage", "MIXED_BATCH", {}),
     "long_context_read": ("read", "LONG_CONTEXT", {}),
     "wide_read_77": ("read", "SINGLE_READ", dict(slots=[(61, 77)])),
@@ -556,8 +557,9 @@ def build_runner(kind, shape, device, concurrent=True):
         return st
     w = inputs.device_normal_bf16((shape.V, shape.D), shape.D ** -0.5, 1, device)
     e = inputs.device_normal_bf16((shape.V, shape.D), shape.D ** -0.5, 2, device)
-    if kind == "read":
-        st = ReadStep(shape, w, e, device=device, seed=7, concurrent=concurrent)
+    if kind in ("read", "read_fp4"):
+        st = ReadStep(shape, w, e, device=device, seed=7, concurrent=concurrent,
+                      fp4=kind == "read_fp4")
         fill_common(st, shape, device)
     else:
         plen = inputs.prompt_lengths(shape, 5)
@@ -647,10 +649,11 @@ def workload_arm(args, rank, world, local):
     else:
         run = lambda i: st.run(step_idx=i)              # noqa: E731
         calls = ["dg_attn_decode", "dg_slot_read", "dg_slot_read_wide", "dg_slot_noise",
-                 "dg_denoise_heads",
+                 "dg_lmhead_logsoftmax_entropy_nvfp4_mma", "dg_denoise_heads",
                  "dg_slot_finish", "dg_commit", "dg_selfcond_from_probs", "dg_canvas_update"]
     dg.dg_clear_status()
-    sched = st if kind in ("step", "read") and getattr(st, "concurrent", False) else None
+    sched = (st if kind in ("step", "read", "read_fp4") and getattr(st, "concurrent", False)
+             else None)
     ms, per_call, launches, clk = timed_steps(args, run, calls, local, world, sched)
     status = dg.dg_get_status()
     steps_per_s = job_rate(ms, args.steps, world)
@@ -692,6 +695,13 @@ def workload_arm(args, rank, world, local):
     if kind == "read":
         work["dg_slot_read"] = (Wb + st.S * R * D * 4, 2.0 * st.S * R * V * D)
         work["dg_slot_read_wide"] = work["dg_slot_read"]
+        decisions = st.S
+    elif kind == "read_fp4":
+        nd = st.S * R
+        work["dg_lmhead_logsoftmax_entropy_nvfp4_mma"] = (
+            V * D // 2 + V * D // 16 + nd * D * 2 + 2 * (nd * D // 2 + nd * D // 16) + nd * 16,
+            2.0 * nd * V * D)
+        work["dg_slot_noise"] = (3 * nd * D * 2, 0.0)
         decisions = st.S
     elif kind == "two_stage":
         rows = (st.S1 + st.S2) * R                      # draw rows of both stages, one W pass
@@ -749,7 +759,8 @@ def workload_arm(args, rank, world, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": ("e4m3" if kind.endswith("_fp8") else
                   "nvfp4 weights x bf16 rows" if kind.endswith("_fp4") else
-                  "nvfp4 weights x nvfp4 rows" if kind.endswith("_fp4mma") else "bf16"),
+                  "nvfp4 weights x nvfp4 rows" if kind.endswith(("_fp4mma", "read_fp4")) else
+                  "bf16"),
         "data": "synthetic",
         "config": {"workload": f"{args.workload}: kind {kind}, B={shape.B}, prompt "
                                f"{'U[512, %d] paged' % shape.P if kind == 'two_stage' else shape.P}"
@@ -759,6 +770,8 @@ def workload_arm(args, rank, world, local):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": ("inputs larger than L2: E (1.48 GB bf16, 0.74 GB e4m3) streamed "
                           "every pass" if kind.startswith("selfcond") else
+                          "inputs larger than L2: NVFP4 W (0.42 GB) streamed every step"
+                          if kind in ("lmhead_fp4", "lmhead_fp4mma", "read_fp4") else
                           "inputs larger than L2: W (1.48 GB) streamed every step"),
                    "launch": ("eager; " + ("slot finish, commit and attention on a side "
                                            "stream beside the self-conditioning GEMM"

@@ -208,9 +208,17 @@ class ReadStep:
     other: with ``concurrent=True`` (the default) the attention goes first on a
     side stream, planned for an eighth of the SMs (``dims.sm_share``), and the
     slot read's W pass takes the SMs it leaves.
+
+    ``fp4=True`` reads against an NVFP4 checkpoint (tau-home.com, "Running NVFP4
+    locally with a Jev-compatible System One endpoint"): W is quantised once
+    (dg_quantize_nvfp4_mma) and the slot read is dg_slot_noise, then the
+    block-scaled pass over the S*R draw rows (the rows quantised in the call;
+    one gathered label row per draw, which writes z - lse), then dg_slot_finish
+    on those gathered values with zero row lse, so that it keeps them as the
+    draws' label logprobs.  At most 16 draw rows and slots of up to 26 labels.
     """
 
-    def __init__(self, shape, w, e, device="cuda", seed=0, concurrent=True):
+    def __init__(self, shape, w, e, device="cuda", seed=0, concurrent=True, fp4=False):
         """Slots with more than 26 labels are read with dg_slot_read_wide (one table of
         stride L = the largest label count)."""
         self.shape = shape
@@ -250,6 +258,28 @@ class ReadStep:
         self.ws_read = torch.empty(dg.dg_workspace_bytes(self.dims, dg.DG_WS_SLOT_READ,
                                                          self.S * shape.R), dtype=u8,
                                    device=device)
+        self.fp4 = fp4
+        if fp4:
+            nd = self.S * shape.R
+            if nd > 16 or self.L != dg.MAX_LABELS:
+                raise ValueError("the NVFP4 read takes at most 16 draw rows and 26 labels a slot")
+            V = shape.V
+            self.codes = torch.empty((V, D // 2), dtype=u8, device=device)
+            self.sf = torch.empty(((V + 127) // 128, D // 64, 512), dtype=u8, device=device)
+            self.g = torch.empty(1, dtype=f32, device=device)
+            dg._check(dg.dg_quantize_nvfp4_mma(w, V, D, self.codes, self.sf, self.g),
+                      "dg_quantize_nvfp4_mma")
+            self.rows_draw = torch.empty((nd, D), dtype=bf, device=device)
+            self.inv_t_draw = torch.empty(nd, dtype=f32, device=device)
+            self.draw_row = torch.arange(nd, dtype=i32, device=device)
+            self.draw_labels = self.label_ids.repeat_interleave(shape.R, dim=0).contiguous()
+            self.draw_n = self.n_labels.repeat_interleave(shape.R).contiguous()
+            self.lse_draw = torch.empty(nd, dtype=f32, device=device)
+            self.zero_lse = torch.zeros(nd, dtype=f32, device=device)
+            self.lm = [torch.empty(nd, dtype=f32, device=device) for _ in range(2)]
+            self.lm_arg = torch.empty(nd, dtype=i32, device=device)
+            self.ws_lm = torch.empty(dg.dg_workspace_bytes(self.dims, dg.DG_WS_LMHEAD_NVFP4_MMA,
+                                                           nd), dtype=u8, device=device)
 
     def run(self, step_idx=0, stream=None):
         """Enqueue attention + the slot read; returns the number of library kernels."""
@@ -265,7 +295,22 @@ class ReadStep:
                                     None, 0, 0, 0, self.prompt_len, self.attn_out,
                                     self.attn_lse, self.ws_attn, attn_stream), "dg_attn_decode")
         stream = main
-        if self.L == dg.MAX_LABELS:
+        if self.fp4:
+            nd = self.S * s.R
+            dg._check(dg.dg_slot_noise(d, self.h, self.M, self.e, self.inv_t, self.slot_row,
+                                       self.slot_req, self.S, s.R, self.seed, step_idx,
+                                       self.rows_draw, self.inv_t_draw, o["tokens"], stream),
+                      "dg_slot_noise")
+            dg._check(dg.dg_lmhead_logsoftmax_entropy_nvfp4_mma(
+                d, self.rows_draw, nd, self.codes, self.sf, self.g, self.inv_t_draw,
+                self.draw_row, self.draw_labels, self.draw_n, nd, self.lse_draw, self.lm[0],
+                self.lm[1], self.lm_arg, o["lp"], self.ws_lm, stream),
+                "dg_lmhead_logsoftmax_entropy_nvfp4_mma")
+            dg._check(dg.dg_slot_finish(d, None, None, self.zero_lse, None, self.label_ids,
+                                        self.n_labels, self.S, s.R, s.R, s.gate, o["q_avg"],
+                                        o["h_slot"], o["chosen"], o["lp"], o["resampled"],
+                                        o["n_reads"], stream), "dg_slot_finish")
+        elif self.L == dg.MAX_LABELS:
             dg._check(dg.dg_slot_read(d, self.h, self.M, self.w, self.e, self.inv_t,
                                       self.slot_row, self.slot_req, self.label_ids,
                                       self.n_labels, self.S, self.seed, step_idx, s.R, s.gate,
@@ -282,6 +327,9 @@ class ReadStep:
         if self.concurrent:
             main.wait_stream(attn_stream)
         attn_kernels = 1 if dg.dg_workspace_bytes(attn_dims, dg.DG_WS_ATTN, 0) <= 256 else 2
+        if self.fp4:
+            # noise; row quantisation, gather table, W pass, finalize; slot epilogue
+            return attn_kernels + 6
         # noise, the W pass (gathering the label logits) + finalize, slot epilogue
         return attn_kernels + 4
 

@@ -18,7 +18,8 @@ def test_every_workload_resolves_to_a_shape():
     b = _bench()
     for name, (kind, _, kw) in b.WORKLOADS.items():
         k, shape = b.workload_shape(name)
-        assert k == kind in ("step", "read", "two_stage", "prefill", "lmhead", "lmhead_fp8",
+        assert k == kind in ("step", "read", "read_fp4", "two_stage", "prefill", "lmhead",
+                             "lmhead_fp8",
                              "lmhead_fp4", "lmhead_fp4mma", "mixed", "selfcond", "selfcond_fp8")
         for f, v in kw.items():
             assert getattr(shape, f) == v
