@@ -233,11 +233,20 @@ __device__ __forceinline__ void softmax_and_store(const TcArgs& a, const Tiles& 
     const uint32_t vm0 = chunk_mask(2 * half, lo, hi, bad, a.page_size);
     const uint32_t vm1 = chunk_mask(2 * half + 1, lo, hi, bad, a.page_size);
     tmem_ld_wait();
+    // every key of the warp's 64 valid for every row (the prompt tiles but the
+    // last): the maximum and the exponentials without per-key masks
+    const bool fast = __all_sync(FULL, (vm0 & vm1) == 0xffffffffu);
     float mh = -INFINITY;
+    if (fast) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      if ((vm0 >> i) & 1u) mh = fmaxf(mh, __uint_as_float(v0[i]));
-      if ((vm1 >> i) & 1u) mh = fmaxf(mh, __uint_as_float(v1[i]));
+      for (int i = 0; i < 32; ++i)
+        mh = fmaxf(mh, fmaxf(__uint_as_float(v0[i]), __uint_as_float(v1[i])));
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        if ((vm0 >> i) & 1u) mh = fmaxf(mh, __uint_as_float(v0[i]));
+        if ((vm1 >> i) & 1u) mh = fmaxf(mh, __uint_as_float(v1[i]));
+      }
     }
     const uint16_t own = bf16_bits_up(mh == -INFINITY ? -INFINITY : mh * sl2);
     uint16_t* xm = xmax + (j & 1) * 2 * BM;
@@ -279,14 +288,29 @@ __device__ __forceinline__ void softmax_and_store(const TcArgs& a, const Tiles& 
     float psum = 0.f;
     auto probs = [&](const uint32_t (&v)[32], uint32_t vm, int cc) {
       uint32_t pk[16];
+      if (fast) {
+        // packed fp32 pairs: one FMA forms two exponents, one add keeps two partial sums
+        const float2 sc = make_float2(sl2, sl2), off = make_float2(-mr, -mr);
+        float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float x0 = fmaf(__uint_as_float(v[2 * i]), sl2, -mr);
-        const float x1 = fmaf(__uint_as_float(v[2 * i + 1]), sl2, -mr);
-        const float p0 = ((vm >> (2 * i)) & 1u) ? ex2(x0) : 0.f;
-        const float p1 = ((vm >> (2 * i + 1)) & 1u) ? ex2(x1) : 0.f;
-        psum += p0 + p1;
-        pk[i] = pack_bf16(p0, p1);
+        for (int i = 0; i < 16; ++i) {
+          const float2 x = __ffma2_rn(
+              make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), sc, off);
+          const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+          acc = __fadd2_rn(acc, pp);
+          pk[i] = pack_bf16(pp.x, pp.y);
+        }
+        psum += acc.x + acc.y;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float x0 = fmaf(__uint_as_float(v[2 * i]), sl2, -mr);
+          const float x1 = fmaf(__uint_as_float(v[2 * i + 1]), sl2, -mr);
+          const float p0 = ((vm >> (2 * i)) & 1u) ? ex2(x0) : 0.f;
+          const float p1 = ((vm >> (2 * i + 1)) & 1u) ? ex2(x1) : 0.f;
+          psum += p0 + p1;
+          pk[i] = pack_bf16(p0, p1);
+        }
       }
       tmem_st_32x32b_x16(s_addr + half * 64 + cc * 16, pk);
     };
