@@ -49,6 +49,7 @@ WORKLOADS = {
     "lmhead_nvfp4_m256": ("lmhead_fp4", "FULL_CANVAS", {}),
     "lmhead_nvfp4_m12": ("lmhead_fp4", "FULL_CANVAS", dict(C=12)),
     "lmhead_nvfp4_mma_m12": ("lmhead_fp4mma", "FULL_CANVAS", dict(C=12)),
+    "lmhead_nvfp4_mma_m256": ("lmhead_fp4mma", "FULL_CANVAS", {}),
     "selfcond_bf16_m256": ("selfcond", "FULL_CANVAS", {}),
     "selfcond_fp8_m256": ("selfcond_fp8", "FULL_CANVAS", {}),
     "mixed_decode8_prefill2": ("mixed", "LONG_CONTEXT", dict(B=10, C=2048, P=4096)),

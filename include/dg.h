@@ -341,8 +341,10 @@ int dg_lmhead_logsoftmax_entropy_nvfp4(const dg_dims* dims, const uint16_t* h, i
  * (kind::mxf4nvf4, one e4m3 scale per 16 values of both operands):
  * z_iv = (sum_k e2m1(h)_ik s(h)_ik e2m1(w)_vk s(w)_vk) * g_h * g_w, fp32
  * accumulation; the rows are quantised inside the call by the recipe of
- * dg_quantize_nvfp4 with their own tensor scale g_h.  At most 16 rows (the slot
- * reads' draw rows) and d_model a multiple of 64 up to 3072, else DG_ERR_SHAPE.
+ * dg_quantize_nvfp4 with their own tensor scale g_h.  Any M: up to 16 rows (the
+ * slot reads' draw rows) stay resident in one pass with the vocabulary on the
+ * tensor-memory lanes (d_model at most 3072 there), more rows go through the
+ * GEMM form; d_model a multiple of 64, else DG_ERR_SHAPE.
  * codes and sf from dg_quantize_nvfp4_mma(w, V, d_model, ..), g its tensor scale;
  * label gather and outputs as dg_lmhead_logsoftmax_entropy; workspace:
  * dg_workspace_bytes(dims, DG_WS_LMHEAD_NVFP4_MMA, M) bytes (256-byte aligned).

@@ -52,6 +52,7 @@ constexpr int EPI_ACCUM_MN = 3;  // as EPI_ACCUM with B given N-contiguous ([K, 
 constexpr int EPI_STATS8 = 4;    // as EPI_STATS with e4m3 operands and per-row scales
 constexpr int EPI_ACCUM8 = 5;    // as EPI_ACCUM with e4m3 operands (both K-major) and scales
 constexpr int EPI_STATS4 = 6;    // as EPI_STATS with B = NVFP4 weights widened to bf16 on chip
+constexpr int EPI_STATS4X = 7;   // as EPI_STATS with A and B NVFP4 on the block-scaled kind
 constexpr int RING_BUDGET = 232448 - 1024 - 512;  // operand rings (227 KB - alignment - barriers)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
@@ -87,13 +88,15 @@ struct GemmParams {
 
 // PK > 0 (NVFP4 B): a second, deeper ring of PK-byte stages holds the packed
 // codes and scales, so that their DRAM latency is hidden while the operand
-// ring holds only the A rows and the widened B tile.
-template <int MT, int BN, int PK = 0>
+// ring holds only the A rows and the widened B tile.  SF > 0 (block-scaled
+// NVFP4 A and B): each stage also holds SF bytes of scale atoms, and one
+// accumulator stage leaves tensor memory for the scales.
+template <int MT, int BN, int PK = 0, int SF = 0>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;   // one 128-row A tile of a K block
   static constexpr int A_STAGE = MT * A_BYTES;
   static constexpr int B_STAGE = BN * BK * 2;
-  static constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+  static constexpr int STAGE_BYTES = A_STAGE + B_STAGE + SF;
   static constexpr int PK_BYTES = PK;
   static constexpr int NS_FIT = PK == 0 ? RING_BUDGET / STAGE_BYTES
                                 : (3 * STAGE_BYTES + 4 * PK <= RING_BUDGET ? 3 : 2);
@@ -101,8 +104,8 @@ struct Cfg {
   static constexpr int PK_FIT = PK == 0 ? 0 : (RING_BUDGET - NSTAGE * STAGE_BYTES) / PK;
   static constexpr int PK_STAGES = PK_FIT > 8 ? 8 : PK_FIT;
   static constexpr int ACC_COLS = MT * BN;
-  static constexpr int ACC_STAGES = (2 * ACC_COLS <= 512) ? 2 : 1;
-  static constexpr int TMEM_NEED = ACC_STAGES * ACC_COLS;
+  static constexpr int ACC_STAGES = (SF == 0 && 2 * ACC_COLS <= 512) ? 2 : 1;
+  static constexpr int TMEM_NEED = ACC_STAGES * ACC_COLS + (SF > 0 ? 2 * 4 * 4 * (MT + BN / 128) : 0);
   static constexpr int TMEM_COLS = TMEM_NEED <= 32    ? 32
                                    : TMEM_NEED <= 64  ? 64
                                    : TMEM_NEED <= 128 ? 128
@@ -118,11 +121,15 @@ struct Cfg {
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(NSTAGE >= 2, "ring depth");
   static_assert(PK == 0 || (PK_STAGES >= 2 && PK % 1024 == 0), "packed ring");
+  static_assert(SF % 1024 == 0 && (SF == 0 || BN % 128 == 0), "scale atoms");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
 // NVFP4 B staging of one K block: BN rows x (32 code bytes + 4 scale bytes)
 constexpr int f4_pk_bytes(int bn) { return bn * 36; }
+// Block-scaled NVFP4: the scale atoms of one 256-value K block (four 64-value
+// steps, 512 bytes per 128 rows and step) for MT A tiles and BN B rows
+constexpr int x4_sf_bytes(int mt, int bn) { return (mt + bn / 128) * 4 * 512; }
 // Warps widening the packed B tile to bf16 (more where the block has fewer
 // epilogue warps), plus the packed-ring producer.
 constexpr int f4_conv_warps(int mt) { return mt == 1 ? 16 : 8; }
@@ -143,7 +150,8 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, GemmParams p) {
   constexpr bool F4 = EPI == EPI_STATS4;
-  using CF = Cfg<MT, BN, F4 ? f4_pk_bytes(BN) : 0>;
+  constexpr bool X4 = EPI == EPI_STATS4X;
+  using CF = Cfg<MT, BN, F4 ? f4_pk_bytes(BN) : 0, X4 ? x4_sf_bytes(MT, BN) : 0>;
   constexpr int NSTAGE = CF::NSTAGE;
   constexpr int PK_STAGES = CF::PK_STAGES;
   constexpr int PRODUCER_WARP = CF::EPI_WARPS;
@@ -154,10 +162,15 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
   constexpr bool B_MN = EPI == EPI_ACCUM_MN;
   constexpr bool ACCUM = EPI == EPI_ACCUM || B_MN || EPI == EPI_ACCUM8;
   constexpr bool F8 = EPI == EPI_STATS8 || EPI == EPI_ACCUM8;
-  constexpr bool STATS = EPI == EPI_STATS || EPI == EPI_STATS8 || F4;
-  // a stage holds 128-byte operand rows: 64 bf16 or 128 e4m3 values of K
-  constexpr int KB = F8 ? 128 : BK;
+  constexpr bool STATS = EPI == EPI_STATS || EPI == EPI_STATS8 || F4 || X4;
+  // a stage holds 128-byte operand rows: 64 bf16, 128 e4m3 or 256 e2m1 values of K
+  constexpr int KB = X4 ? 256 : F8 ? 128 : BK;
   constexpr uint32_t IDESC_F8 = idesc_e4m3_f32(BM, BN);
+  constexpr uint32_t IDESC_X4 = idesc_nvf4_f32(BM, BN);
+  // X4: tensor-memory columns of the scales, after the accumulator: two sets of
+  // (MT A tiles + one 128-row B tile) x 4 steps x 4 columns
+  constexpr int X4_SF_COL = CF::ACC_STAGES * CF::ACC_COLS;
+  constexpr int X4_SF_SET = 16 * (MT + BN / 128);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -251,13 +264,34 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
           }
           uint8_t* s_a = stages + stage * CF::STAGE_BYTES;
           uint8_t* s_b = s_a + CF::A_STAGE;
-          // STATS4: the A rows only; the converter warps write the B tile
-          mbar_arrive_expect_tx(&full_bar[stage], F4 ? CF::A_STAGE : CF::STAGE_BYTES);
+          // STATS4: the A rows only; the converter warps write the B tile.  STATS4X:
+          // the codes of A and B (128 bytes a row) and the scale atoms of this
+          // K block's steps (the last block may have fewer than four)
+          const int ns = X4 ? min(4, p.K / 64 - 4 * kb) : 0;
+          // X4: the A tiles of this group that hold rows (their scale atoms exist)
+          const int a_tiles = X4 ? min(MT, (p.M - m_base + BM - 1) / BM) : 0;
+          mbar_arrive_expect_tx(&full_bar[stage],
+                                F4   ? CF::A_STAGE
+                                : X4 ? CF::A_STAGE + CF::B_STAGE + (a_tiles + BN / 128) * ns * 512
+                                     : CF::STAGE_BYTES);
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt)
-            tma_load_2d_hint(s_a + mt * CF::A_BYTES, &tmA, &full_bar[stage], kb * KB,
-                             m_base + mt * BM, pol_a);
+            tma_load_2d_hint(s_a + mt * CF::A_BYTES, &tmA, &full_bar[stage],
+                             X4 ? kb * 128 : kb * KB, m_base + mt * BM, pol_a);
           if (F4) {
+          } else if (X4) {
+            const int n_steps = p.K / 64;
+            tma_load_2d_hint(s_b, &tmB, &full_bar[stage], kb * 128, t * BN, pol_b);
+            uint8_t* s_sf = s_b + CF::B_STAGE;
+            for (int mt = 0; mt < a_tiles; ++mt)
+              bulk_load(s_sf + mt * 2048,
+                        p.sf_rows + ((long long)(m_base / BM + mt) * n_steps + 4 * kb) * 512,
+                        ns * 512, &full_bar[stage]);
+#pragma unroll
+            for (int h = 0; h < BN / 128; ++h)
+              bulk_load(s_sf + (MT + h) * 2048,
+                        p.sf4 + ((long long)(t * (BN / 128) + h) * n_steps + 4 * kb) * 512,
+                        ns * 512, &full_bar[stage]);
           } else if (B_MN) {
             // B [K, N] with N contiguous: BN/64 boxes of 64 N-columns x 64 K-rows
 #pragma unroll
@@ -282,7 +316,7 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
     }
   } else if (warp == MMA_WARP) {
     if (lane == 0 && has_work) {
-      int stage = 0, acc = 0;
+      int stage = 0, acc = 0, sf_set = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int t = t_begin; t < t_end && ok; ++t) {
@@ -299,6 +333,41 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
           tc_fence_after();
           const uint32_t a_addr = smem_u32(stages + stage * CF::STAGE_BYTES);
           const uint32_t b_addr = a_addr + CF::A_STAGE;
+          if constexpr (X4) {
+            // the K block's scales into one of two column sets (A tiles, then the
+            // B tile), then its MMAs: the tensor pipe runs both in issue order
+            const uint32_t sfs = b_addr + CF::B_STAGE;
+            const uint32_t sf_t = tmem_base + X4_SF_COL + sf_set * X4_SF_SET;
+            const int ns = min(4, p.K / 64 - 4 * kb);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              if (ks < ns) {
+#pragma unroll
+                for (int u = 0; u < MT + BN / 128; ++u)
+                  tc_cp_32x128b_warpx4(sf_t + u * 16 + ks * 4,
+                                       plain_kmajor_desc(sfs + u * 2048 + ks * 512, 128));
+              }
+            }
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              if (ks < ns) {
+                const uint64_t bdesc = sw128_kmajor_desc(b_addr + ks * 32);
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt)
+                  tc_mma_nvf4(d_base + mt * BN,
+                              sw128_kmajor_desc(a_addr + mt * CF::A_BYTES + ks * 32), bdesc,
+                              IDESC_X4, sf_t + mt * 16 + ks * 4, sf_t + MT * 16 + ks * 4,
+                              (kb > kb_begin || ks > 0) ? 1u : 0u);
+              }
+            }
+            sf_set ^= 1;
+            tc_commit(&empty_bar[stage]);
+            if (++stage == NSTAGE) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             // K-major B: +32 bytes per 16 K inside the 128-byte row; MN-major B:
@@ -449,7 +518,9 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
     float scale = 0.f, lse2 = 0.f, rs = 1.f;
     if (!ACCUM && row_ok) scale = __ldg(p.inv_t + row) * LOG2E;
     if (F8 && row_ok) rs = __ldg(p.row_scale + row);
-    const float gs = F4 ? __ldg(p.gscale) : 1.f;
+    const float gs = F4   ? __ldg(p.gscale)
+                     : X4 ? __ldg(p.gscale) * __ldg(p.gscale_rows)
+                          : 1.f;
     if (EPI == EPI_PROBS && row_ok) lse2 = __ldg(p.lse + row) * LOG2E;
     float m_run = -INFINITY, s_run = 0.f, t_run = 0.f, best = -INFINITY;
     int best_idx = 0x7fffffff;
@@ -514,7 +585,7 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
             r[j + 3] = __float_as_uint(__uint_as_float(r[j + 3]) * rs * cs.w);
           }
         }
-        if (F4) {
+        if (F4 || X4) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * gs);
         }
@@ -1358,7 +1429,7 @@ __global__ void split_reduce_kernel(const float4* part, int k_split, long long n
 template <int MT, int BN, int EPI>
 cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
                         int grid, cudaStream_t st) {
-  using CF = Cfg<MT, BN>;
+  using CF = Cfg<MT, BN, 0, EPI == EPI_STATS4X ? x4_sf_bytes(MT, BN) : 0>;
   static bool attr_done = false;  // per-process; the attribute is per function
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<MT, BN, EPI>,
@@ -1530,33 +1601,44 @@ cudaError_t run_stats_nvfp4(const uint16_t* h, int M, const uint8_t* codes, cons
   return cudaGetLastError();
 }
 
-// Both operands NVFP4 on the block-scaled kind, at most 16 rows: the rows are
-// quantised into the workspace (codes, scale atoms, tensor scale; after the
-// partials and the label-gather scratch), then the skinny pass in MODE 2.
+// Both operands NVFP4 on the block-scaled kind.  The rows are quantised into the
+// workspace (codes, scale atoms, tensor scale; after the partials and the
+// label-gather scratch); up to 16 rows take the skinny pass in MODE 2, more the
+// GEMM form (EPI_STATS4X: rows on the TMEM lanes, 128-row vocabulary tiles).
+constexpr int X4_BN = 128;
+
 size_t x4_rows_offset(int M, int V) {
   return dgi::lmhead_ws_bytes(M, V) + dgi::align_up((size_t)M * 4, 256);
 }
+
+int x4_rows_padded(int M) { return M <= SK_N ? SK_N : M; }
 
 cudaError_t run_stats_nvfp4_mma(const uint16_t* h, int M, const uint8_t* codes, const uint8_t* sf,
                                 const float* g, int V, int D, const float* inv_t,
                                 dgi::RowStats out, void* ws, cudaStream_t st,
                                 const dgi::LabelGather* gather) {
   using dgi::align_up;
+  const bool skinny = M <= SK_N;
+  const int Mp = x4_rows_padded(M);
   uint8_t* rc = static_cast<uint8_t*>(ws) + x4_rows_offset(M, V);
-  uint8_t* rsf = rc + align_up((size_t)SK_N * (D / 2), 256);
-  float* rg = reinterpret_cast<float*>(rsf + align_up((size_t)(D / 64) * 512, 256));
-  cudaError_t e = dgi::quantize_rows_nvfp4_mma(h, M, D, rc, rsf, rg, st);
+  uint8_t* rsf = rc + align_up((size_t)Mp * (D / 2), 256);
+  float* rg = reinterpret_cast<float*>(
+      rsf + align_up((size_t)((Mp + 127) / 128) * (D / 64) * 512, 256));
+  cudaError_t e = skinny ? dgi::quantize_rows_nvfp4_mma(h, M, D, rc, rsf, rg, st)
+                         : dgi::quantize_nvfp4_mma(h, M, D, rc, rsf, rg, st);
   if (e != cudaSuccess) return e;
-  CUtensorMap th, tw;
-  if (!dgi::make_tmap_u8_2d(&th, rc, D / 2, SK_N, D / 2, 128, SK_N)) return cudaErrorInvalidValue;
-  if (!dgi::make_tmap_u8_2d(&tw, codes, D / 2, V, D / 2, 128, SK_BN)) return cudaErrorInvalidValue;
+  CUtensorMap ta, tb;
+  if (!dgi::make_tmap_u8_2d(&ta, rc, D / 2, Mp, D / 2, 128, skinny ? SK_N : BM))
+    return cudaErrorInvalidValue;
+  if (!dgi::make_tmap_u8_2d(&tb, codes, D / 2, V, D / 2, 128, skinny ? SK_BN : X4_BN))
+    return cudaErrorInvalidValue;
   if ((e = gather_prepare(gather, M, st)) != cudaSuccess) return e;
   GemmParams p{};
   p.M = M;
   p.N = V;
   p.K = D;
   p.cpg = stats_cpg(M, V);
-  p.n_tiles = (V + SK_BN - 1) / SK_BN;
+  p.n_tiles = (V + (skinny ? SK_BN : X4_BN) - 1) / (skinny ? SK_BN : X4_BN);
   p.inv_t = inv_t;
   p.codes4 = codes;
   p.sf4 = sf;
@@ -1566,7 +1648,14 @@ cudaError_t run_stats_nvfp4_mma(const uint16_t* h, int M, const uint8_t* codes, 
   p.part = static_cast<float*>(ws);
   p.status = dgi::status_ptr();
   if (gather) p.gl = *gather;
-  e = launch_skinny<2>(th, tw, p, st);
+  if (skinny) {
+    e = launch_skinny<2>(ta, tb, p, st);
+  } else {
+    const int mt = stats_mt(M);
+    const int groups = (M + mt * BM - 1) / (mt * BM);
+    e = (mt == 1) ? launch_gemm<1, X4_BN, EPI_STATS4X>(ta, tb, p, groups * p.cpg, st)
+                  : launch_gemm<2, X4_BN, EPI_STATS4X>(ta, tb, p, groups * p.cpg, st);
+  }
   if (e != cudaSuccess) return e;
   stats_finalize_kernel<<<(M + 7) / 8, 256, 0, st>>>(p.part, p.cpg, M, inv_t, out.lse,
                                                      out.entropy, out.maxz, out.argmax, p.gl, V,
@@ -1643,12 +1732,13 @@ cudaError_t lmhead_stats_nvfp4(const uint16_t* h, int M, const uint8_t* codes,
 }
 
 size_t lmhead_nvfp4_mma_ws_bytes(int M, int V, int D) {
-  return x4_rows_offset(M, V) + align_up((size_t)SK_N * (D / 2), 256) +
-         align_up((size_t)(D / 64) * 512, 256) + 256;
+  const int Mp = x4_rows_padded(M);
+  return x4_rows_offset(M, V) + align_up((size_t)Mp * (D / 2), 256) +
+         align_up((size_t)((Mp + 127) / 128) * (D / 64) * 512, 256) + 256;
 }
 
 bool lmhead_nvfp4_mma_ok(int M, int D) {
-  return M >= 1 && M <= SK_N && D >= 64 && D % 64 == 0 && D <= 12 * SK_X4_KB;
+  return M >= 1 && D >= 64 && D % 64 == 0 && (M > SK_N || D <= 12 * SK_X4_KB);
 }
 
 cudaError_t lmhead_stats_nvfp4_mma(const uint16_t* h, int M, const uint8_t* codes,

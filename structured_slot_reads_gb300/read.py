@@ -215,7 +215,7 @@ class ReadStep:
     block-scaled pass over the S*R draw rows (the rows quantised in the call;
     one gathered label row per draw, which writes z - lse), then dg_slot_finish
     on those gathered values with zero row lse, so that it keeps them as the
-    draws' label logprobs.  At most 16 draw rows and slots of up to 26 labels.
+    draws' label logprobs.  Slots of up to 26 labels.
     """
 
     def __init__(self, shape, w, e, device="cuda", seed=0, concurrent=True, fp4=False):
@@ -261,8 +261,8 @@ class ReadStep:
         self.fp4 = fp4
         if fp4:
             nd = self.S * shape.R
-            if nd > 16 or self.L != dg.MAX_LABELS:
-                raise ValueError("the NVFP4 read takes at most 16 draw rows and 26 labels a slot")
+            if self.L != dg.MAX_LABELS:
+                raise ValueError("the NVFP4 read takes slots of at most 26 labels")
             V = shape.V
             self.codes = torch.empty((V, D // 2), dtype=u8, device=device)
             self.sf = torch.empty(((V + 127) // 128, D // 64, 512), dtype=u8, device=device)

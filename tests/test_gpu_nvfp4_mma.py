@@ -75,7 +75,11 @@ def test_quantizer_mma_layout_bit_exact(V, D):
 
 
 @pytest.mark.parametrize("M,V,D", [(12, 4096, 256), (1, 1024, 64), (16, 3000, 192),
-                                   (5, 2500, 2816), (16, 2048, 3072), (7, 1100, 320)])
+                                   (5, 2500, 2816), (16, 2048, 3072), (7, 1100, 320),
+                                   # the GEMM form: one and two 128-row tiles per group,
+                                   # ragged rows, vocabularies and K blocks
+                                   (17, 2048, 128), (100, 3000, 192), (256, 8192, 512),
+                                   (300, 2500, 320), (40, 1000, 3136)])
 def test_nvfp4_mma_lmhead_stats(M, V, D):
     h = inputs.hidden(M, D, 11 + M)
     w, _ = inputs.weights(V, D, 12 + V)
@@ -119,10 +123,12 @@ def test_nvfp4_mma_label_gather():
         assert np.all(lp[s, n[s]:] == 12345.0)
 
 
-def test_nvfp4_mma_full_vocabulary():
-    """262144 x 2816 weights and 12 slot-draw rows: the quantiser on two 128-row
-    tiles and the statistics of every row over the whole vocabulary."""
-    M, V, D = 12, 262144, 2816
+@pytest.mark.parametrize("M", [12, 256])
+def test_nvfp4_mma_full_vocabulary(M):
+    """262144 x 2816 weights and 12 slot-draw rows (the skinny pass) or 256 canvas
+    rows (the GEMM form): the quantiser on two 128-row tiles and the statistics of
+    every row (12) or of sampled rows (256) over the whole vocabulary."""
+    V, D = 262144, 2816
     w, _ = inputs.weights(V, D, 77)
     codes, sf, g = _quantize(dev_bf16(w), V, D)
     h = inputs.hidden(M, D, 78)
@@ -137,10 +143,11 @@ def test_nvfp4_mma_full_vocabulary():
     assert np.array_equal(host(sf[8:10]), atoms)
     oc_all, osc_all = oracle.from_mma_layout(host(codes), host(sf), V)
     wq = oracle.dequantize_nvfp4(oc_all, osc_all, gh)
-    o_lse, o_ent, o_maxz, o_arg = oracle.lmhead_stats(_dequantized(h), wq, inv_t)
-    assert_abs(lse, o_lse, what="lse")
-    assert_abs(ent, o_ent, what="entropy")
-    assert_abs(maxz, o_maxz, what="max logit")
+    rows = np.arange(M) if M <= 16 else np.array([0, 5, 127, 128, 200, 255])
+    o_lse, o_ent, o_maxz, o_arg = oracle.lmhead_stats(_dequantized(h)[rows], wq, inv_t[rows])
+    assert_abs(lse[rows], o_lse, what="lse")
+    assert_abs(ent[rows], o_ent, what="entropy")
+    assert_abs(maxz[rows], o_maxz, what="max logit")
 
 
 def test_nvfp4_mma_refusals():
@@ -149,12 +156,7 @@ def test_nvfp4_mma_refusals():
     f = torch.empty(64, dtype=torch.float32, device="cuda")
     i = torch.empty(64, dtype=torch.int32, device="cuda")
     h = torch.zeros((17, 256), dtype=torch.bfloat16, device="cuda")
-    # 17 rows: more than the resident 16
-    assert dg.dg_workspace_bytes(d, dg.DG_WS_LMHEAD_NVFP4_MMA, 17) == 0
-    rc = dg.dg_lmhead_logsoftmax_entropy_nvfp4_mma(d, h, 17, buf, buf, f, f, None, None, None, 0,
-                                                   f, f, f, i, None, buf)
-    assert rc == dg.DG_ERR_SHAPE
-    # d_model past 3072, and not a multiple of 64
+    # d_model past 3072 with the rows resident (16 or fewer), and not a multiple of 64
     for dm in (3136, 96):
         dd = dg.make_dims(d_model=dm, V=1024)
         rc = dg.dg_lmhead_logsoftmax_entropy_nvfp4_mma(dd, h, 4, buf, buf, f, f, None, None,
