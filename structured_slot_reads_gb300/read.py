@@ -328,8 +328,9 @@ class ReadStep:
             main.wait_stream(attn_stream)
         attn_kernels = 1 if dg.dg_workspace_bytes(attn_dims, dg.DG_WS_ATTN, 0) <= 256 else 2
         if self.fp4:
-            # noise; row quantisation, gather table, W pass, finalize; slot epilogue
-            return attn_kernels + 6
+            # noise; row quantisation (one kernel up to 16 rows, else three), gather
+            # table, W pass, finalize; slot epilogue
+            return attn_kernels + (6 if self.S * s.R <= 16 else 8)
         # noise, the W pass (gathering the label logits) + finalize, slot epilogue
         return attn_kernels + 4
 
@@ -426,7 +427,9 @@ class LmHead:
                                                                 self.argmax, None, self.ws,
                                                                 stream),
                       "dg_lmhead_logsoftmax_entropy_nvfp4_mma")
-            return 3
+            # the rows' quantisation (one kernel up to 16 rows, else amax, quantise
+            # and scale), the pass, the finalize
+            return (1 if self.M <= 16 else 3) + 2
         if self.fp4:
             dg._check(dg.dg_lmhead_logsoftmax_entropy_nvfp4(d, self.h, self.M, self.codes,
                                                             self.scales, self.g, self.inv_t,
