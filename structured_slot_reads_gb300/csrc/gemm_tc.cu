@@ -104,8 +104,9 @@ struct Cfg {
   static constexpr int PK_FIT = PK == 0 ? 0 : (RING_BUDGET - NSTAGE * STAGE_BYTES) / PK;
   static constexpr int PK_STAGES = PK_FIT > 8 ? 8 : PK_FIT;
   static constexpr int ACC_COLS = MT * BN;
-  static constexpr int ACC_STAGES = (SF == 0 && 2 * ACC_COLS <= 512) ? 2 : 1;
-  static constexpr int TMEM_NEED = ACC_STAGES * ACC_COLS + (SF > 0 ? 2 * 4 * 4 * (MT + BN / 128) : 0);
+  static constexpr int SF_COLS = SF > 0 ? 2 * 4 * 4 * (MT + BN / 128) : 0;   // two sets
+  static constexpr int ACC_STAGES = (2 * ACC_COLS + SF_COLS <= 512) ? 2 : 1;
+  static constexpr int TMEM_NEED = ACC_STAGES * ACC_COLS + SF_COLS;
   static constexpr int TMEM_COLS = TMEM_NEED <= 32    ? 32
                                    : TMEM_NEED <= 64  ? 64
                                    : TMEM_NEED <= 128 ? 128
@@ -1624,8 +1625,10 @@ cudaError_t run_stats_nvfp4_mma(const uint16_t* h, int M, const uint8_t* codes, 
   uint8_t* rsf = rc + align_up((size_t)Mp * (D / 2), 256);
   float* rg = reinterpret_cast<float*>(
       rsf + align_up((size_t)((Mp + 127) / 128) * (D / 64) * 512, 256));
-  cudaError_t e = skinny ? dgi::quantize_rows_nvfp4_mma(h, M, D, rc, rsf, rg, st)
-                         : dgi::quantize_nvfp4_mma(h, M, D, rc, rsf, rg, st);
+  cudaError_t e =
+      skinny ? dgi::quantize_rows_nvfp4_mma(h, M, D, rc, rsf, rg, st)
+             : dgi::quantize_many_rows_nvfp4_mma(h, M, D, rc, rsf, rg,
+                                                 reinterpret_cast<unsigned int*>(rg + 1), st);
   if (e != cudaSuccess) return e;
   CUtensorMap ta, tb;
   if (!dgi::make_tmap_u8_2d(&ta, rc, D / 2, Mp, D / 2, 128, skinny ? SK_N : BM))
@@ -1651,6 +1654,11 @@ cudaError_t run_stats_nvfp4_mma(const uint16_t* h, int M, const uint8_t* codes, 
   if (skinny) {
     e = launch_skinny<2>(ta, tb, p, st);
   } else {
+    // two 128-row tiles a CTA when there are more than 128 rows (one accumulator
+    // stage then, beside the scales): each W tile is copied and its scales moved
+    // into tensor memory once for 256 rows.  One tile a CTA with two accumulator
+    // stages, two groups sharing each W tile through L2, took 20% longer at 256
+    // rows: twice the scale copies and barrier hand-offs per W byte.
     const int mt = stats_mt(M);
     const int groups = (M + mt * BM - 1) / (mt * BM);
     e = (mt == 1) ? launch_gemm<1, X4_BN, EPI_STATS4X>(ta, tb, p, groups * p.cpg, st)
@@ -1737,6 +1745,7 @@ size_t lmhead_nvfp4_mma_ws_bytes(int M, int V, int D) {
          align_up((size_t)((Mp + 127) / 128) * (D / 64) * 512, 256) + 256;
 }
 
+// (the last 256 bytes: g and, above 16 rows, the rows' largest magnitude)
 bool lmhead_nvfp4_mma_ok(int M, int D) {
   return M >= 1 && D >= 64 && D % 64 == 0 && (M > SK_N || D <= 12 * SK_X4_KB);
 }

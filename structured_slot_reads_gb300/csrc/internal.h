@@ -96,6 +96,11 @@ cudaError_t quantize_nvfp4_mma(const uint16_t* x, int rows, int cols, uint8_t* c
 // scale atoms [cols/64][512] (one tile), *g.
 cudaError_t quantize_rows_nvfp4_mma(const uint16_t* x, int M, int cols, uint8_t* codes,
                                     uint8_t* sf, float* g, cudaStream_t st);
+// The same for any number of rows: the largest magnitude into *amax (scratch),
+// then one thread per (padded row, block of 16); *g written.
+cudaError_t quantize_many_rows_nvfp4_mma(const uint16_t* x, int rows, int cols, uint8_t* codes,
+                                         uint8_t* sf, float* g, unsigned int* amax,
+                                         cudaStream_t st);
 // lm-head statistics with both operands in NVFP4 on the block-scaled tensor-core kind:
 // z = (sum_k e2m1_h s_h e2m1_w s_w) * g_h * g_w / T, at most 16 rows (quantised in the
 // call).  Workspace: lmhead_nvfp4_mma_ws_bytes.

@@ -396,6 +396,53 @@ __global__ void __launch_bounds__(256)
   if (t == 0) *g_out = g;
 }
 
+// The rows of a block-scaled pass, more than 16 of them: one thread per (padded row,
+// block of 16 values) after tensor_amax_kernel has left the rows' largest magnitude
+// in *amax_bits; codes [rows][cols/2], scale atoms [ceil(rows/128)][cols/64] (rows
+// past `rows` scale 0); thread 0 writes g.
+__global__ void quantize_blocks_nvfp4_mma_kernel(const __nv_bfloat16* x, int rows, int cols,
+                                                 const unsigned int* amax_bits, uint8_t* codes,
+                                                 uint8_t* sf, float* g_out) {
+  const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int nb = cols / 16, nks = cols / 64;
+  const int rows_pad = (rows + 127) & ~127;
+  if (t >= (long long)rows_pad * nb) return;
+  const int r = (int)(t / nb), blk = (int)(t % nb);
+  const float g = nvfp4_tensor_scale(*amax_bits);
+  if (t == 0) *g_out = g;
+  uint8_t sb = 0;
+  if (r < rows) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (long long)r * cols + blk * 16);
+    float xv[16];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 u = src[h];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+        xv[8 * h + 2 * k] = f.x;
+        xv[8 * h + 2 * k + 1] = f.y;
+      }
+    }
+    float bm = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) bm = fmaxf(bm, fabsf(xv[j]));
+    const __nv_fp8_storage_t s8 = __nv_cvt_float_to_fp8((bm / 6.f) / g, __NV_SATFINITE, __NV_E4M3);
+    const __half_raw hr = __nv_cvt_fp8_to_halfraw(s8, __NV_E4M3);
+    const float den = __half2float(__half(hr)) * g;
+    sb = (uint8_t)s8;
+    uint32_t c0 = 0u, c1 = 0u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      c0 |= (den > 0.f ? e2m1_code(xv[j] / den) : 0u) << (4 * j);
+      c1 |= (den > 0.f ? e2m1_code(xv[8 + j] / den) : 0u) << (4 * j);
+    }
+    *reinterpret_cast<uint2*>(codes + (long long)r * (cols / 2) + blk * 8) = make_uint2(c0, c1);
+  }
+  sf[nvfp4_atom_offset(r, blk >> 2, nks) + (blk & 3)] = sb;
+}
+
 __global__ void nvfp4_scale_kernel(float* g_io) {
   g_io[0] = nvfp4_tensor_scale(reinterpret_cast<const unsigned int*>(g_io)[0]);
 }
@@ -434,6 +481,20 @@ cudaError_t quantize_nvfp4_mma(const uint16_t* x, int rows, int cols, uint8_t* c
   quantize_nvfp4_mma_kernel<<<(int)((items + 127) / 128), 128, 0, st>>>(
       reinterpret_cast<const __nv_bfloat16*>(x), rows, cols, amax, codes, sf);
   nvfp4_scale_kernel<<<1, 1, 0, st>>>(g);
+  return cudaGetLastError();
+}
+
+cudaError_t quantize_many_rows_nvfp4_mma(const uint16_t* x, int rows, int cols, uint8_t* codes,
+                                         uint8_t* sf, float* g, unsigned int* amax,
+                                         cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(unsigned int), st);
+  if (e != cudaSuccess) return e;
+  const long long n8 = (long long)rows * cols / 8;
+  tensor_amax_kernel<<<(int)std::min<long long>((n8 + 255) / 256, 1024), 256, 0, st>>>(
+      reinterpret_cast<const uint4*>(x), n8, amax);
+  const long long items = (long long)((rows + 127) & ~127) * (cols / 16);
+  quantize_blocks_nvfp4_mma_kernel<<<(int)((items + 255) / 256), 256, 0, st>>>(
+      reinterpret_cast<const __nv_bfloat16*>(x), rows, cols, amax, codes, sf, g);
   return cudaGetLastError();
 }
 
