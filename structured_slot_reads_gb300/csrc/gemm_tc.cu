@@ -104,7 +104,9 @@ struct Cfg {
   static constexpr int PK_FIT = PK == 0 ? 0 : (RING_BUDGET - NSTAGE * STAGE_BYTES) / PK;
   static constexpr int PK_STAGES = PK_FIT > 8 ? 8 : PK_FIT;
   static constexpr int ACC_COLS = MT * BN;
-  static constexpr int SF_COLS = SF > 0 ? 2 * 4 * 4 * (MT + BN / 128) : 0;   // two sets
+  // SF > 0: one set of scale columns per ring stage (MT A tiles + the B tile, four
+  // steps of four columns), written by the scale warps while the stage is in flight
+  static constexpr int SF_COLS = SF > 0 ? NSTAGE * 16 * (MT + BN / 128) : 0;
   static constexpr int ACC_STAGES = (2 * ACC_COLS + SF_COLS <= 512) ? 2 : 1;
   static constexpr int TMEM_NEED = ACC_STAGES * ACC_COLS + SF_COLS;
   static constexpr int TMEM_COLS = TMEM_NEED <= 32    ? 32
@@ -147,7 +149,10 @@ __device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t word, uint32_t (&h)[4])
 }
 
 template <int MT, int BN, int EPI>
-__global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32 * f4_extra_warps(MT) : 0), 1)
+__global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4    ? 32 * f4_extra_warps(MT)
+                                                          : EPI == EPI_STATS4X ? 128
+                                                                               : 0),
+                                  1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, GemmParams p) {
   constexpr bool F4 = EPI == EPI_STATS4;
@@ -183,8 +188,9 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
   uint64_t* tfull_bar = empty_bar + NSTAGE;
   uint64_t* tempty_bar = tfull_bar + CF::ACC_STAGES;
   uint64_t* drain_bar = tempty_bar + CF::ACC_STAGES;
-  uint64_t* bready_bar = drain_bar + 1;   // STATS4: [NSTAGE] the widened B tile written
-  uint64_t* pkfull_bar = bready_bar + (F4 ? NSTAGE : 0);         // STATS4: [PK_STAGES]
+  // STATS4: [NSTAGE] the widened B tile written; STATS4X: the stage's scales written
+  uint64_t* bready_bar = drain_bar + 1;
+  uint64_t* pkfull_bar = bready_bar + ((F4 || X4) ? NSTAGE : 0);  // STATS4: [PK_STAGES]
   uint64_t* pkempty_bar = pkfull_bar + PK_STAGES;                 // STATS4: [PK_STAGES]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pkempty_bar + PK_STAGES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -197,6 +203,7 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], 1);
       if (F4) mbar_init(&bready_bar[i], CONV_WARPS);
+      if (X4) mbar_init(&bready_bar[i], 4);
     }
     for (int i = 0; i < PK_STAGES; ++i) {
       mbar_init(&pkfull_bar[i], 1);
@@ -317,7 +324,7 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
     }
   } else if (warp == MMA_WARP) {
     if (lane == 0 && has_work) {
-      int stage = 0, acc = 0, sf_set = 0;
+      int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int t = t_begin; t < t_end && ok; ++t) {
@@ -327,7 +334,7 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
         for (int kb = kb_begin; kb < kb_end; ++kb) {
           // the A rows (and B, by TMA); STATS4: also the B tile the converters widened
           if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.status) ||
-              (F4 && !mbar_wait(&bready_bar[stage], phase, abort_flag, p.status))) {
+              ((F4 || X4) && !mbar_wait(&bready_bar[stage], phase, abort_flag, p.status))) {
             ok = false;
             break;
           }
@@ -335,20 +342,9 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
           const uint32_t a_addr = smem_u32(stages + stage * CF::STAGE_BYTES);
           const uint32_t b_addr = a_addr + CF::A_STAGE;
           if constexpr (X4) {
-            // the K block's scales into one of two column sets (A tiles, then the
-            // B tile), then its MMAs: the tensor pipe runs both in issue order
-            const uint32_t sfs = b_addr + CF::B_STAGE;
-            const uint32_t sf_t = tmem_base + X4_SF_COL + sf_set * X4_SF_SET;
+            // the scale warps have written this stage's scales into its column set
+            const uint32_t sf_t = tmem_base + X4_SF_COL + stage * X4_SF_SET;
             const int ns = min(4, p.K / 64 - 4 * kb);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-              if (ks < ns) {
-#pragma unroll
-                for (int u = 0; u < MT + BN / 128; ++u)
-                  tc_cp_32x128b_warpx4(sf_t + u * 16 + ks * 4,
-                                       plain_kmajor_desc(sfs + u * 2048 + ks * 512, 128));
-              }
-            }
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
               if (ks < ns) {
@@ -361,7 +357,6 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
                               (kb > kb_begin || ks > 0) ? 1u : 0u);
               }
             }
-            sf_set ^= 1;
             tc_commit(&empty_bar[stage]);
             if (++stage == NSTAGE) {
               stage = 0;
@@ -403,6 +398,42 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4 ? 32
       // every MMA issued by this thread has completed once drain_bar flips
       tc_commit(drain_bar);
       mbar_wait_drain(drain_bar, 0);
+    }
+  } else if (X4 && warp >= CONV0 && warp < CONV0 + 4) {
+    // ---- STATS4X scale warps, one per TMEM lane quarter: each stage's scale atoms
+    // (32 rows of 16 bytes) into the stage's column set, every quarter the same
+    // rows (the layout the block-scaled MMA reads), off the tensor pipe's queue ----
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = has_work;
+    for (int t = t_begin; t < t_end && ok; ++t) {
+      for (int kb = kb_begin; kb < kb_end; ++kb) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&full_bar[stage], phase, abort_flag, p.status));
+        if (!ok) break;
+        const uint8_t* sfs = stages + stage * CF::STAGE_BYTES + CF::A_STAGE + CF::B_STAGE;
+        const uint32_t col = tmem_base + lane_base + X4_SF_COL + stage * X4_SF_SET;
+        const int ns = min(4, p.K / 64 - 4 * kb);
+#pragma unroll
+        for (int u = 0; u < MT + BN / 128; ++u) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            if (ks < ns) {
+              const uint4 v =
+                  *reinterpret_cast<const uint4*>(sfs + u * 2048 + ks * 512 + lane * 16);
+              tmem_st_32x32b_x4(col + u * 16 + ks * 4, v);
+            }
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bready_bar[stage]);
+        if (++stage == NSTAGE) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
     }
   } else if (F4 && warp >= CONV0 && warp < PK_WARP) {
     // ---- STATS4 converter warps: each K block's packed B rows -> bf16 tile ----
@@ -781,10 +812,11 @@ struct SkCfg {
   static constexpr int SMEM_BYTES = 1024 + B_BYTES + NW * W_STAGE + NP * PK + BAR_BYTES;
   static constexpr int PRODUCER = SK_EPI_WARPS;            // rows, then W (or the packed ring)
   static constexpr int MMA = SK_EPI_WARPS + 1;
-  static constexpr int CONV0 = SK_EPI_WARPS + 2;           // F4: converter warps
-  static constexpr int THREADS = (SK_EPI_WARPS + 2 + (F4 ? SK_CONV_WARPS : 0)) * 32;
-  // 2 stages x 2 halves x 16 columns; MODE 2: then two sets of 32 W scale columns
-  // (2 halves x 4 steps x 4) and, from column 256, the rows' scales (4 a step)
+  static constexpr int CONV0 = SK_EPI_WARPS + 2;           // F4: converter warps; X4: scale warps
+  static constexpr int THREADS = (SK_EPI_WARPS + 2 + (F4 ? SK_CONV_WARPS : X4 ? 4 : 0)) * 32;
+  static constexpr int NSF = X4 ? NW : 0;                  // X4: "scales written" barriers
+  // 2 stages x 2 halves x 16 columns; MODE 2: then one set of 32 W scale columns
+  // per W stage (2 halves x 4 steps x 4) and, from column 256, the rows' scales
   static constexpr int TMEM_COLS = X4 ? 512 : 64;
   // bf16 W: bf16 operands.  NVFP4 W: f16 operands (the widening is then two
   // instructions a code pair, and every e2m1 x e4m3 product is an f16)
@@ -794,7 +826,7 @@ struct SkCfg {
   static_assert(W_STAGE % 1024 == 0, "W stages stay 1 KB aligned");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
   static_assert(SK_EPI_WARPS == 4, "one epilogue warp per TMEM lane quarter");
-  static_assert((2 * NW + 2 * NP + 7) * 8 + SK_GBITS * 4 + 8 + 2 * SK_N * 4 <= BAR_BYTES,
+  static_assert((2 * NW + 2 * NP + NSF + 7) * 8 + SK_GBITS * 4 + 8 + 2 * SK_N * 4 <= BAR_BYTES,
                 "barrier region");
 };
 
@@ -819,7 +851,8 @@ __global__ void __launch_bounds__(SkCfg<MODE>::THREADS, 1)
   uint64_t* wempty = wfull + CF::NW;
   uint64_t* pfull = wempty + CF::NW;
   uint64_t* pempty = pfull + CF::NP;
-  uint64_t* tfull = pempty + CF::NP;
+  uint64_t* sfready = pempty + CF::NP;   // X4: [NW] a stage's W scales written
+  uint64_t* tfull = sfready + CF::NSF;
   uint64_t* tempty = tfull + 2;
   uint64_t* bres_bar = tempty + 2;
   uint64_t* drain_bar = bres_bar + 1;
@@ -841,6 +874,7 @@ __global__ void __launch_bounds__(SkCfg<MODE>::THREADS, 1)
       mbar_init(&pfull[i], 1);
       mbar_init(&pempty[i], SK_CONV_WARPS);
     }
+    for (int i = 0; i < CF::NSF; ++i) mbar_init(&sfready[i], 4);
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], SK_EPI_WARPS);
@@ -937,7 +971,7 @@ __global__ void __launch_bounds__(SkCfg<MODE>::THREADS, 1)
     }
   } else if (warp == CF::MMA) {
     if (lane == 0 && has_work) {
-      int ws = 0, acc = 0, sf_set = 0;
+      int ws = 0, acc = 0;
       uint32_t wph = 0, aph = 0;
       bool ok = mbar_wait(F4 ? rows16_bar : bres_bar, 0, abort_flag, p.status);
       if (X4 && ok) {
@@ -951,29 +985,19 @@ __global__ void __launch_bounds__(SkCfg<MODE>::THREADS, 1)
         if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, p.status)) break;
         tc_fence_after();
         for (int kb = 0; kb < total_kb; ++kb) {
-          if (!mbar_wait(&wfull[ws], wph, abort_flag, p.status)) {
+          if (!mbar_wait(&wfull[ws], wph, abort_flag, p.status) ||
+              (X4 && !mbar_wait(&sfready[ws], wph, abort_flag, p.status))) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t w_addr = smem_u32(wring + ws * CF::W_STAGE);
           if constexpr (X4) {
-            // W scales of this K block into tensor memory (columns: half 0 steps,
-            // half 1 steps), then its MMAs; the two column sets alternate by K
-            // block, and the tensor pipe runs the copies and MMAs of this thread in
-            // issue order
+            // the scale warps have written this stage's W scales into its column
+            // set (half 0 steps, half 1 steps)
             const uint32_t b_addr = smem_u32(bres + kb * SK_X4_ROWS);
-            const uint32_t sfw = w_addr + SK_W_BYTES;
-            const uint32_t sf_t = tmem_base + SK_X4_SFW_COL + sf_set * 32;
+            const uint32_t sf_t = tmem_base + SK_X4_SFW_COL + ws * 32;
             const int ns = min(4, n_steps - 4 * kb);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-              if (ks < ns) {
-                tc_cp_32x128b_warpx4(sf_t + ks * 4, plain_kmajor_desc(sfw + ks * 512, 128));
-                tc_cp_32x128b_warpx4(sf_t + 16 + ks * 4,
-                                     plain_kmajor_desc(sfw + 2048 + ks * 512, 128));
-              }
-            }
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
               if (ks < ns) {
@@ -987,7 +1011,6 @@ __global__ void __launch_bounds__(SkCfg<MODE>::THREADS, 1)
                               (kb > 0 || ks > 0) ? 1u : 0u);
               }
             }
-            sf_set ^= 1;
           } else {
             const uint32_t b_addr = smem_u32(bres + kb * SK_B_BLOCK);
 #pragma unroll
@@ -1015,6 +1038,42 @@ __global__ void __launch_bounds__(SkCfg<MODE>::THREADS, 1)
       }
       tc_commit(drain_bar);
       mbar_wait_drain(drain_bar, 0);
+    }
+  } else if (X4 && warp >= CF::CONV0) {
+    // ---- MODE 2 scale warps, one per TMEM lane quarter: each W stage's scale
+    // atoms into the stage's column set, every quarter the same 32 rows of 16
+    // bytes (the layout the block-scaled MMA reads), off the tensor pipe's queue ----
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    int ws = 0;
+    uint32_t wph = 0;
+    bool ok = has_work;
+    for (int t = t_begin; t < t_end && ok; ++t) {
+      for (int kb = 0; kb < total_kb; ++kb) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&wfull[ws], wph, abort_flag, p.status));
+        if (!ok) break;
+        const uint8_t* sfw = wring + ws * CF::W_STAGE + SK_W_BYTES;
+        const uint32_t col = tmem_base + lane_base + SK_X4_SFW_COL + ws * 32;
+        const int ns = min(4, n_steps - 4 * kb);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            if (ks < ns) {
+              const uint4 v =
+                  *reinterpret_cast<const uint4*>(sfw + h * 2048 + ks * 512 + lane * 16);
+              tmem_st_32x32b_x4(col + h * 16 + ks * 4, v);
+            }
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfready[ws]);
+        if (++ws == CF::NW) {
+          ws = 0;
+          wph ^= 1u;
+        }
+      }
     }
   } else if (F4 && warp >= CF::CONV0) {
     // NVFP4: widen each K block's packed rows into the W ring (as in the GEMM)
@@ -1439,7 +1498,9 @@ cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const Gemm
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  gemm_tc_kernel<MT, BN, EPI><<<grid, CF::THREADS, CF::SMEM_BYTES, st>>>(ta, tb, p);
+  // STATS4X: four scale warps besides the epilogue, producer and MMA warps
+  const int threads = CF::THREADS + (EPI == EPI_STATS4X ? 128 : 0);
+  gemm_tc_kernel<MT, BN, EPI><<<grid, threads, CF::SMEM_BYTES, st>>>(ta, tb, p);
   return cudaGetLastError();
 }
 
