@@ -309,17 +309,29 @@ def test_commit(B, C, gamma, frac, state):
     _commit_case(B, C, gamma, seed=B * C, frac_open=frac, state=state)
 
 
-def test_canvas_update_bit_exact():
-    M, V, D = 40, 512, 128
+@pytest.mark.parametrize("shift", [0, 1])
+def test_canvas_update_bit_exact(shift):
+    """16-byte aligned buffers (one thread per 8 values) and buffers 4 or 8 bytes
+    past a 16-byte boundary (the row-per-CTA form): the same bits as the oracle."""
+    M, V, D = 40, 512, 136
     h0 = inputs.hidden(M, D, 1)
     emb, _ = inputs.weights(V, D, 1)
     e_sc = (np.random.default_rng(2).standard_normal((M, D)) * 0.05).astype(np.float32)
     committed = (np.arange(M) % 3 == 0).astype(np.uint8)
     tokens = np.where(committed == 1, np.arange(M) * 7 % V, -1).astype(np.int32)
     d = dg.make_dims(d_model=D, V=V)
-    out = torch.empty((M, D), dtype=torch.bfloat16, device="cuda")
-    rc = dg.dg_canvas_update(d, dev_bf16(h0), dev(e_sc), dev_bf16(emb), dev(tokens),
-                             dev(committed), M, out)
+
+    def shifted(x, k):
+        # a view k elements into a larger buffer: 2 bf16 or 2 floats past 16-byte alignment
+        buf = torch.empty(x.numel() + 8, dtype=x.dtype, device="cuda")
+        v = buf[k:k + x.numel()].view(x.shape)
+        v.copy_(x)
+        return v
+
+    k = 2 * shift
+    h0_d, es_d = shifted(dev_bf16(h0), k), shifted(dev(e_sc), k)
+    out = shifted(torch.zeros((M, D), dtype=torch.bfloat16, device="cuda"), k)
+    rc = dg.dg_canvas_update(d, h0_d, es_d, dev_bf16(emb), dev(tokens), dev(committed), M, out)
     assert rc == dg.DG_OK
     torch.cuda.synchronize()
     want = oracle.canvas_update(h0, e_sc, emb, tokens, committed)
