@@ -464,6 +464,10 @@ int dg_selfcond_embed(const dg_dims* dims, const uint16_t* h, int M,
  * largest of the row's first eight.
  *   h [M, d_model] bf16;  draw_rows [n_draw, d_model] bf16 (NULL if n_draw = 0)
  *   w [V, d_model] bf16;  inv_t [M], inv_t_draw [n_draw] fp32
+ *   w_tiled: NULL, or dg_heads_weights_tile's copy of the same w (16-byte
+ *   aligned; DG_ERR_ARG when d_model is not a multiple of 64).  With draw rows
+ *   the pass streams W from it (the same values, read in contiguous blocks);
+ *   without draw rows it reads w.  The caller keeps it in step with w.
  *   lse, entropy, maxz [M] fp32;  argmax [M] int32;  lse_draw [n_draw] fp32
  *   draw_label_ids [n_draw / draw_R, 26] int32;  draw_n_labels [n_draw / draw_R]
  *   int32;  draw_label_z [n_draw, 26] fp32 (NULL: no gather; else n_draw a
@@ -474,12 +478,27 @@ int dg_selfcond_embed(const dg_dims* dims, const uint16_t* h, int M,
  *   workspace: dg_workspace_bytes(dims, DG_WS_HEADS, M) bytes. */
 int dg_denoise_heads(const dg_dims* dims, const uint16_t* h, int M,
                      const uint16_t* draw_rows, int n_draw, const uint16_t* w,
-                     const float* inv_t, const float* inv_t_draw, float* lse,
+                     const uint16_t* w_tiled, const float* inv_t, const float* inv_t_draw, float* lse,
                      float* entropy, float* maxz, int32_t* argmax, float* lse_draw,
                      const int32_t* draw_label_ids, const int32_t* draw_n_labels,
                      int draw_R, float* draw_label_z, float* prob_scale, uint16_t* probs,
                      size_t probs_ld, void* workspace, size_t workspace_bytes,
                      void* stream);
+
+/* W in the tiled layout dg_denoise_heads streams (a layout of the lm-head
+ * weights of tau-home.com, "Refusing JSON token generation", no arithmetic):
+ * tiles of 224 vocabulary rows, each cut into blocks of 64 columns, block
+ * (t, kb) one contiguous run of 224 x 64 bf16:
+ *   w_tiled[((t * (d_model / 64) + kb) * 224 + r) * 64 + c] = w[224 t + r][64 kb + c]
+ * and zero for rows 224 t + r >= V.  dg_heads_weights_bytes gives its size,
+ * ceil(V / 224) * 224 * d_model * 2 bytes (0 when d_model is not a multiple of
+ * 64 or the dims are invalid); dg_heads_weights_tile writes it on the stream
+ * (DG_ERR_SHAPE for such dims; w and w_tiled 16-byte aligned, DG_ERR_ARG
+ * otherwise).  Written once per weight matrix, beside the row-major w that
+ * the other calls read. */
+size_t dg_heads_weights_bytes(const dg_dims* dims);
+int dg_heads_weights_tile(const dg_dims* dims, const uint16_t* w, uint16_t* w_tiled,
+                          void* stream);
 
 /* Expected embedding from dg_denoise_heads' probabilities:
  * out[i] = prob_scale[i] * sum_v probs[i][v] e[v] (24-ai.news, "Token commit

@@ -342,8 +342,22 @@ size_t dg_workspace_bytes(const dg_dims* d, int which, int rows) {
 
 size_t dg_probs_ld(int V) { return V < 1 ? 0 : dgi::heads_probs_ld(V); }
 
+size_t dg_heads_weights_bytes(const dg_dims* d) {
+  if (!d || !dims_lm(d)) return 0;
+  return dgi::heads_tiled_bytes(d->V, d->d_model);
+}
+
+int dg_heads_weights_tile(const dg_dims* d, const uint16_t* w, uint16_t* w_tiled, void* stream) {
+  if (!d) return DG_ERR_ARG;
+  if (!dims_lm(d) || !dgi::heads_tiled_bytes(d->V, d->d_model)) return DG_ERR_SHAPE;
+  if (!w || !w_tiled || !aligned(w, 16) || !aligned(w_tiled, 16)) return DG_ERR_ARG;
+  return launch_result(dgi::heads_tile_weights(w, d->V, d->d_model, w_tiled,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
 int dg_denoise_heads(const dg_dims* d, const uint16_t* h, int M, const uint16_t* draw_rows,
-                     int n_draw, const uint16_t* w, const float* inv_t, const float* inv_t_draw,
+                     int n_draw, const uint16_t* w, const uint16_t* w_tiled,
+                     const float* inv_t, const float* inv_t_draw,
                      float* lse, float* entropy, float* maxz, int32_t* argmax, float* lse_draw,
                      const int32_t* draw_label_ids, const int32_t* draw_n_labels, int draw_R,
                      float* draw_label_z, float* prob_scale, uint16_t* probs, size_t probs_ld,
@@ -354,6 +368,8 @@ int dg_denoise_heads(const dg_dims* d, const uint16_t* h, int M, const uint16_t*
     return DG_ERR_ARG;
   if (n_draw > 0 && (!draw_rows || !inv_t_draw || !lse_draw)) return DG_ERR_ARG;
   if (!aligned(h, 16) || !aligned(w, 16) || (n_draw > 0 && !aligned(draw_rows, 16)))
+    return DG_ERR_ARG;
+  if (w_tiled && (!aligned(w_tiled, 16) || !dgi::heads_tiled_bytes(d->V, d->d_model)))
     return DG_ERR_ARG;
   if (probs && (probs_ld < (size_t)d->V || probs_ld % 64 || !aligned(probs, 32)))
     return DG_ERR_ARG;
@@ -370,8 +386,9 @@ int dg_denoise_heads(const dg_dims* d, const uint16_t* h, int M, const uint16_t*
   }
   const size_t need = dg_workspace_bytes(d, DG_WS_HEADS, M);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DG_ERR_WORKSPACE;
-  return launch_result(dgi::denoise_heads(h, M, draw_rows, n_draw, w, d->V, d->d_model, inv_t,
-                                          inv_t_draw, dgi::RowStats{lse, entropy, maxz, argmax},
+  return launch_result(dgi::denoise_heads(h, M, draw_rows, n_draw, w, w_tiled, d->V, d->d_model,
+                                          inv_t, inv_t_draw,
+                                          dgi::RowStats{lse, entropy, maxz, argmax},
                                           lse_draw, prob_scale, probs, probs_ld, workspace,
                                           static_cast<cudaStream_t>(stream), &g));
 }

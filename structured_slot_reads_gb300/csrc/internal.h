@@ -129,8 +129,14 @@ cudaError_t probs_embed(const uint16_t* probs, size_t ldp, const float* row_scal
 // ---- fused lm-head pass of a step (heads_tc.cu) ------------------------------
 size_t heads_ws_bytes(int M, int V, int n_draw);
 size_t heads_probs_ld(int V);
+// W's tiled copy for the pass with draw rows (224-row tiles x 64-column blocks,
+// each block contiguous); 0 bytes when d_model is not a multiple of 64.
+size_t heads_tiled_bytes(int V, int D);
+cudaError_t heads_tile_weights(const uint16_t* w, int V, int D, uint16_t* out, cudaStream_t st);
+// w_tiled (or null): the tiled copy of w, streamed instead of w when there are draw rows
 cudaError_t denoise_heads(const uint16_t* h, int M, const uint16_t* draw_rows, int n_draw,
-                          const uint16_t* w, int V, int D, const float* inv_t,
+                          const uint16_t* w, const uint16_t* w_tiled, int V, int D,
+                          const float* inv_t,
                           const float* inv_t_draw, RowStats out, float* lse_draw,
                           float* prob_scale, uint16_t* probs, size_t probs_ld, void* ws,
                           cudaStream_t st, const LabelGather* gather = nullptr);

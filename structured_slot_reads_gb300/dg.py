@@ -78,7 +78,9 @@ _SIGS = {
                                                P, Z, P],
     "dg_commit": [DP, P, P, P, P, P, P, P, P, P, P],
     "dg_selfcond_embed": [DP, P, I, P, P, P, P, P, P, Z, P],
-    "dg_denoise_heads": [DP, P, I, P, I, P, P, P, P, P, P, P, P, P, P, I, P, P, P, Z, P, Z, P],
+    "dg_denoise_heads": [DP, P, I, P, I, P, P, P, P, P, P, P, P, P, P, P, I, P, P, P, Z, P, Z, P],
+    "dg_heads_weights_bytes": [DP],
+    "dg_heads_weights_tile": [DP, P, P, P],
     "dg_selfcond_from_probs": [DP, P, Z, P, I, P, P, P, Z, P],
     "dg_probs_ld": [I],
     "dg_ask_if_select": [P, I, P, P, P, P, P, I, I, P, P, P, P],
@@ -93,7 +95,8 @@ _SIGS = {
     "dg_strerror": [I],
     "dg_num_sms": [],
 }
-_RES = {"dg_workspace_bytes": Z, "dg_strerror": ctypes.c_char_p, "dg_probs_ld": Z}
+_RES = {"dg_workspace_bytes": Z, "dg_strerror": ctypes.c_char_p, "dg_probs_ld": Z,
+        "dg_heads_weights_bytes": Z}
 
 
 def lib():
@@ -293,13 +296,21 @@ def dg_selfcond_embed(dims, h, M, w, e, inv_t, lse, out, workspace, stream=None)
 
 def dg_denoise_heads(dims, h, M, draw_rows, n_draw, w, inv_t, inv_t_draw, lse, entropy, maxz,
                      argmax, lse_draw, draw_label_ids, draw_n_labels, draw_R, draw_label_z,
-                     prob_scale, probs, probs_ld, workspace, stream=None):
+                     prob_scale, probs, probs_ld, workspace, stream=None, w_tiled=None):
     return lib().dg_denoise_heads(ctypes.byref(dims), _p(h), M, _p(draw_rows), n_draw, _p(w),
-                                  _p(inv_t), _p(inv_t_draw), _p(lse), _p(entropy), _p(maxz),
+                                  _p(w_tiled), _p(inv_t), _p(inv_t_draw), _p(lse), _p(entropy), _p(maxz),
                                   _p(argmax), _p(lse_draw), _p(draw_label_ids),
                                   _p(draw_n_labels), draw_R, _p(draw_label_z), _p(prob_scale),
                                   _p(probs), probs_ld, _p(workspace), _nbytes(workspace),
                                   _s(stream))
+
+
+def dg_heads_weights_bytes(dims):
+    return lib().dg_heads_weights_bytes(ctypes.byref(dims))
+
+
+def dg_heads_weights_tile(dims, w, w_tiled, stream=None):
+    return lib().dg_heads_weights_tile(ctypes.byref(dims), _p(w), _p(w_tiled), _s(stream))
 
 
 def dg_selfcond_from_probs(dims, probs, probs_ld, prob_scale, M, e, out, workspace,

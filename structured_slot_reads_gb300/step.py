@@ -161,6 +161,7 @@ class DenoiseStep:
         self.concurrent = fused and concurrent
         self._side = None                   # side stream and its event, made on first use
         self.n_draw = self.S * shape.R if (self.with_slots and self.S * shape.R <= 16) else 0
+        self.w_tiled = None
         if not self.fused:
             self.ws_lm = _empty((dg.dg_workspace_bytes(self.dims, dg.DG_WS_LMHEAD, self.M),), u8,
                                 dev)
@@ -176,6 +177,18 @@ class DenoiseStep:
             self.prob_scale = _empty((self.M,), f32, dev)
             self.ws_heads = _empty((dg.dg_workspace_bytes(self.dims, dg.DG_WS_HEADS, self.M),), u8, dev)
             self.ws_pe = _empty((dg.dg_workspace_bytes(self.dims, dg.DG_WS_PROBS_EMBED, self.M),), u8, dev)
+            # W's tiled copy, which the pass streams when the draw rows ride in it
+            # (written here once; call tile_weights() again after changing w)
+            if self.n_draw and dg.dg_heads_weights_bytes(self.dims):
+                self.w_tiled = _empty((dg.dg_heads_weights_bytes(self.dims) // 2,), bf, dev)
+                if self.w_tiled.is_cuda:
+                    self.tile_weights()
+
+    def tile_weights(self, stream=None):
+        """Rewrite the tiled copy of ``w`` the heads pass streams (dg_heads_weights_tile)."""
+        if self.w_tiled is not None:
+            dg._check(dg.dg_heads_weights_tile(self.dims, self.w, self.w_tiled, stream),
+                      "dg_heads_weights_tile")
 
     # ------------------------------------------------------------ slots
     def set_slots(self, slot_row, slot_req, label_ids, n_labels):
@@ -286,7 +299,8 @@ class DenoiseStep:
                                self.argmax, self.lse_draw, self.label_ids if nd else None,
                                self.n_labels if nd else None, s.R,
                                self.lp_draws if nd else None, self.prob_scale, self.probs,
-                               self.probs_ld, self.ws_heads, main), "dg_denoise_heads")
+                               self.probs_ld, self.ws_heads, main, w_tiled=self.w_tiled),
+           "dg_denoise_heads")
         side = main
         if self.concurrent:
             if self._side is None:

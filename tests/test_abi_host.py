@@ -168,6 +168,9 @@ def test_step_runner_builds_on_host(lib, fused):
     assert st.kernels_per_step() == (11 if fused else 13) - (0 if st._attn_splits() > 1 else 1)
     if fused:
         assert st.probs.shape == (shp.C, dg.dg_probs_ld(shp.V)) and st.n_draw == 4
+        # the pass streams W from its tiled copy (whole 224-row tiles)
+        assert st.w_tiled.numel() * 2 == dg.dg_heads_weights_bytes(st.dims)
+        assert st.w_tiled.numel() == -(-shp.V // 224) * 224 * shp.D
 
 
 def test_batched_step_reads_slots_in_their_own_pass(lib):
@@ -179,7 +182,7 @@ def test_batched_step_reads_slots_in_their_own_pass(lib):
     shp = configs.scaled(configs.TINY, B=8)
     w = torch.zeros((shp.V, shp.D), dtype=torch.bfloat16)
     st = DenoiseStep(shp, w, w, device="cpu", fused=True)
-    assert st.S == 8 and st.n_draw == 0 and not hasattr(st, "ws_sc")
+    assert st.S == 8 and st.n_draw == 0 and not hasattr(st, "ws_sc") and st.w_tiled is None
     assert st.kernels_per_step() == 13 - (0 if st._attn_splits() > 1 else 1)
 
 
@@ -252,6 +255,27 @@ def test_heads_pass_wants_32_byte_aligned_probabilities(lib):
                           None, None, 0, None, 32, probs, ld, None)
     assert dg.dg_denoise_heads(*args(48), stream=0) == dg.DG_ERR_ARG        # 16- not 32-aligned
     assert dg.dg_denoise_heads(*args(64), stream=0) == dg.DG_ERR_WORKSPACE  # alignment accepted
+
+
+def test_heads_weights_tiled_copy_validates(lib):
+    """The tiled copy of W: ceil(V / 224) whole tiles of d_model columns, only for
+    d_model a multiple of 64; refusals come before any launch."""
+    d = dg.make_dims(d_model=2816, V=262144)
+    assert dg.dg_heads_weights_bytes(d) == 1171 * 224 * 2816 * 2
+    assert dg.dg_heads_weights_bytes(dg.make_dims(d_model=128, V=224)) == 224 * 128 * 2
+    assert dg.dg_heads_weights_bytes(dg.make_dims(d_model=128, V=225)) == 2 * 224 * 128 * 2
+    d96 = dg.make_dims(d_model=96, V=1024)
+    assert dg.dg_heads_weights_bytes(d96) == 0
+    assert dg.dg_heads_weights_tile(d96, 32, 32, stream=0) == dg.DG_ERR_SHAPE
+    d128 = dg.make_dims(d_model=128, V=1024)
+    assert dg.dg_heads_weights_tile(d128, None, 32, stream=0) == dg.DG_ERR_ARG
+    assert dg.dg_heads_weights_tile(d128, 32, 40, stream=0) == dg.DG_ERR_ARG   # 8-byte aligned
+    # the pass refuses a tiled copy it cannot use (d_model not a multiple of 64)
+    ld = dg.dg_probs_ld(1024)
+    args = (d96, 32, 4, None, 0, 32, 32, None, 32, 32, 32, 32, None, None, None, 0, None, 32,
+            64, ld, None)
+    assert dg.dg_denoise_heads(*args, stream=0, w_tiled=32) == dg.DG_ERR_ARG
+    assert dg.dg_denoise_heads(*args, stream=0) == dg.DG_ERR_WORKSPACE
 
 
 def test_8bit_self_conditioning_validates(lib):

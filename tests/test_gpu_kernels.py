@@ -344,7 +344,14 @@ def test_status_word_clean_after_valid_calls():
     assert dg.dg_get_status() == 0
 
 
-def _run_heads(h, draws, w, inv_t, inv_t_draw, with_probs=True):
+def _tiled(wd, V, D):
+    d = dg.make_dims(d_model=D, V=V)
+    out = torch.empty(dg.dg_heads_weights_bytes(d) // 2, dtype=torch.bfloat16, device="cuda")
+    assert dg.dg_heads_weights_tile(d, wd, out) == dg.DG_OK
+    return out
+
+
+def _run_heads(h, draws, w, inv_t, inv_t_draw, with_probs=True, tiled=False):
     M, D = h.shape
     V = w.shape[0]
     nd = 0 if draws is None else draws.shape[0]
@@ -357,9 +364,12 @@ def _run_heads(h, draws, w, inv_t, inv_t_draw, with_probs=True):
     ld = dg.dg_probs_ld(V)
     probs = torch.empty((M, ld), dtype=torch.bfloat16, device="cuda") if with_probs else None
     ws = torch.empty(dg.dg_workspace_bytes(d, dg.DG_WS_HEADS, M), dtype=torch.uint8, device="cuda")
-    rc = dg.dg_denoise_heads(d, dev_bf16(h), M, dev_bf16(draws) if nd else None, nd, dev_bf16(w),
+    wd = w if isinstance(w, torch.Tensor) else dev_bf16(w)
+    wt = _tiled(wd, V, D) if tiled else None
+    rc = dg.dg_denoise_heads(d, dev_bf16(h), M, dev_bf16(draws) if nd else None, nd, wd,
                              dev(inv_t), dev(inv_t_draw) if nd else None, lse, ent, maxz, arg,
-                             lse_d if nd else None, None, None, 0, None, scale, probs, ld, ws)
+                             lse_d if nd else None, None, None, 0, None, scale, probs, ld, ws,
+                             w_tiled=wt)
     assert rc == dg.DG_OK, dg.strerror(rc)
     torch.cuda.synchronize()
     return dict(lse=host(lse), ent=host(ent), maxz=host(maxz), arg=host(arg),
@@ -405,6 +415,40 @@ def test_denoise_heads_fused_pass(M, nd, V, D):
     assert rc == dg.DG_OK
     torch.cuda.synchronize()
     assert_rel(host(out), oracle.selfcond_embed(h, w, e, inv_t), what="expected embedding")
+
+
+@pytest.mark.parametrize("V,D", [(1000, 128), (224, 64), (4096, 2816), (2504, 192)])
+def test_heads_weights_tiled_layout(V, D):
+    """dg_heads_weights_tile against the layout written out with numpy: 224-row
+    tiles of 64-column blocks, block (t, kb) contiguous, zero rows past V."""
+    w = inputs.normal_bf16((V, D), 1.0, 7 + V, 1)
+    got = host(_tiled(dev_bf16(w), V, D))
+    tiles = -(-V // 224)
+    pad = np.zeros((tiles * 224, D), np.float32)
+    pad[:V] = w
+    want = pad.reshape(tiles, 224, D // 64, 64).transpose(0, 2, 1, 3).reshape(-1)
+    assert got.shape == want.shape and np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("M,nd,V,D", [(256, 12, 8192, 512), (100, 5, 3000, 192),
+                                      (384, 16, 2504, 192), (1, 16, 1024, 128),
+                                      (1100, 8, 2048, 128), (64, 0, 4096, 256),
+                                      (256, 12, 262144, 2816)])
+def test_denoise_heads_tiled_weights_bit_identical(M, nd, V, D):
+    """The pass on W's tiled copy reads the same values in the same order: every
+    output bit-identical to the pass on the row-major W (without draw rows the
+    copy is not used), including the 262144 x 2816 lm-head of the full canvas."""
+    h, w, _, inv_t = _lm_inputs(M, V, D, seed=5 + M)
+    wd = dev_bf16(w)
+    del w
+    draws = inputs.hidden(nd, D, 99) if nd else None
+    inv_d = inputs.inv_temperature(nd, 98) if nd else None
+    a = _run_heads(h, draws, wd, inv_t, inv_d)
+    b = _run_heads(h, draws, wd, inv_t, inv_d, tiled=True)
+    for k in ("lse", "ent", "maxz", "arg", "lse_draw"):
+        assert np.array_equal(a[k], b[k]), k
+    assert torch.equal(a["scale"], b["scale"])
+    assert torch.equal(a["probs"][:, :V], b["probs"][:, :V])
 
 
 @pytest.mark.parametrize("M,V,D", [(2048, 2048, 2816), (4096, 1024, 2816), (256, 4096, 2816)])
