@@ -61,6 +61,9 @@ WORKLOADS = {
     "sweep_step_b1": ("step", "FULL_CANVAS", dict(B=1, P=8192)),
     "sweep_step_b8": ("step", "FULL_CANVAS", dict(B=8, P=8192)),
     "sweep_step_b64": ("step", "FULL_CANVAS", dict(B=64, P=8192)),
+    # the full-canvas step with a 65536-entry vocabulary (W 369 MB, still past
+    # L2): the small case for whole-kernel profiler captures of the step
+    "step_v65536": ("step", "FULL_CANVAS", dict(V=65536)),
 }
 
 
