@@ -359,8 +359,15 @@ int dg_lmhead_logsoftmax_entropy_nvfp4_mma(const dg_dims* dims, const uint16_t* 
                                            size_t workspace_bytes, void* stream);
 
 /* NVFP4 quantisation (the recipe of dg_quantize_nvfp4) in the layout the
- * block-scaled pass reads: codes row-major [rows][cols/2] (element k of row v
- * in byte k / 2, the low nibble for even k); scales as 512-byte atoms, one per
+ * block-scaled pass reads.  Codes in 16 KB blocks, one per (128-row tile,
+ * 256-value K block), [ceil(rows/128)][ceil(cols/256)][128][128] bytes: element
+ * k of row v sits in byte (k % 256) / 2 of row v % 128 of block
+ * (v / 128, k / 256), the low nibble for even k; rows past `rows` and values
+ * past cols in the last block are zero codes.  dg_nvfp4_mma_codes_bytes(rows,
+ * cols) gives the size (0 for rows < 1 or cols not a positive multiple of 64).
+ * Every TMA box of the pass is one block or two consecutive tiles' blocks, a
+ * contiguous run, where row-major codes made it 128 rows of 128 bytes cols/2
+ * bytes apart.  Scales as 512-byte atoms, one per
  * 128-row tile and 64-value K-step, atoms [ceil(rows/128)][cols/64]: row 32 j + l
  * of the tile has its four e4m3 scales (values 16 q .. 16 q + 15 of the step in
  * byte q) at bytes 16 l + 4 j .. 16 l + 4 j + 3 of the atom; rows of the last tile
@@ -369,6 +376,7 @@ int dg_lmhead_logsoftmax_entropy_nvfp4_mma(const dg_dims* dims, const uint16_t* 
  * DG_ERR_SHAPE); x and codes 16-byte aligned, sf 4-byte aligned. */
 int dg_quantize_nvfp4_mma(const uint16_t* x, int rows, int cols, uint8_t* codes, uint8_t* sf,
                           float* g, void* stream);
+size_t dg_nvfp4_mma_codes_bytes(int rows, int cols);
 
 /* ---- next: one wide read in place of the two-stage path -----------------
  * sotaaz.com, "The server accepts at most 26 alternatives per question": the

@@ -142,24 +142,33 @@ def from_kblock_layout(codes_kb, scales_kb):
 
 
 def to_mma_layout(codes, scales):
-    """The layout of the block-scaled pass (dg_quantize_nvfp4_mma): codes row-major
-    [R][K/2] (two a byte, the even element low) and scales as 512-byte atoms
-    [ceil(R/128)][K/64][512]: row 32 j + l of a 128-row tile has the four scales of
-    a 64-value step (its blocks of 16 in order) at bytes 16 l + 4 j .. 16 l + 4 j + 3;
-    rows past R have scale 0."""
+    """The layout of the block-scaled pass (dg_quantize_nvfp4_mma).  Codes two a
+    byte (the even element low) in 128 x 128-byte blocks, one per (128-row tile,
+    256-value K block): [ceil(R/128)][ceil(K/256)][128][128], element k of row v in
+    byte (k % 256) / 2 of row v % 128 of block (v // 128, k // 256), zero past R
+    rows and past K.  Scales as 512-byte atoms [ceil(R/128)][K/64][512]: row
+    32 j + l of a 128-row tile has the four scales of a 64-value step (its blocks of
+    16 in order) at bytes 16 l + 4 j .. 16 l + 4 j + 3; rows past R have scale 0."""
     R, K = codes.shape
     nks = K // 64
+    nkb = (nks + 3) // 4
     tiles = (R + 127) // 128
     sc = np.zeros((tiles * 128, nks, 4), np.uint8)
     sc[:R] = np.asarray(scales, np.uint8).reshape(R, nks, 4)
     sc = sc.reshape(tiles, 4, 32, nks, 4)                 # [tile][j][l][step][block]
     atoms = sc.transpose(0, 3, 2, 1, 4)                   # [tile][step][l][j][block]
-    return pack_nibbles(codes), np.ascontiguousarray(atoms).reshape(tiles, nks, 512)
+    flat = np.zeros((tiles * 128, nkb * 128), np.uint8)
+    flat[:R, :K // 2] = pack_nibbles(codes)
+    blocks = flat.reshape(tiles, 128, nkb, 128).transpose(0, 2, 1, 3)
+    return np.ascontiguousarray(blocks), np.ascontiguousarray(atoms).reshape(tiles, nks, 512)
 
 
 def from_mma_layout(packed, atoms, R):
     """Inverse of to_mma_layout: codes [R, K], scales [R, K / 16]."""
     tiles, nks, _ = atoms.shape
+    nkb = (nks + 3) // 4
     a = np.asarray(atoms, np.uint8).reshape(tiles, nks, 32, 4, 4)
     sc = a.transpose(0, 3, 2, 1, 4).reshape(tiles * 128, nks * 4)
-    return unpack_nibbles(np.asarray(packed, np.uint8)[:R]), np.ascontiguousarray(sc[:R])
+    blocks = np.asarray(packed, np.uint8).reshape(tiles, nkb, 128, 128)
+    flat = blocks.transpose(0, 2, 1, 3).reshape(tiles * 128, nkb * 128)
+    return unpack_nibbles(flat[:R, :nks * 32]), np.ascontiguousarray(sc[:R])

@@ -152,6 +152,19 @@ bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_tmap_u8_4d(CUtensorMap* map, const void* base, const uint64_t (&dims)[4],
+                     const uint64_t (&stride_bytes)[3], const uint32_t (&box)[4]) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t d[4] = {dims[0], dims[1], dims[2], dims[3]};
+  const cuuint64_t st[3] = {stride_bytes[0], stride_bytes[1], stride_bytes[2]};
+  const cuuint32_t bx[4] = {box[0], box[1], box[2], box[3]};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), d, st, bx, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, const uint64_t (&dims)[3],
                        const uint64_t (&stride_bytes)[2], const uint32_t (&box)[3]) {
   EncodeTiledFn fn = encode_fn();
@@ -762,6 +775,11 @@ int dg_lmhead_logsoftmax_entropy_nvfp4(const dg_dims* d, const uint16_t* h, int 
                                                dgi::RowStats{lse, entropy, maxz, argmax},
                                                workspace, static_cast<cudaStream_t>(stream),
                                                &lg));
+}
+
+size_t dg_nvfp4_mma_codes_bytes(int rows, int cols) {
+  if (rows < 1 || cols < 64 || cols % 64) return 0;
+  return (size_t)((rows + 127) / 128) * ((cols / 64 + 3) / 4) * 128 * 128;
 }
 
 int dg_quantize_nvfp4_mma(const uint16_t* x, int rows, int cols, uint8_t* codes, uint8_t* sf,

@@ -289,7 +289,8 @@ __global__ void __launch_bounds__(Cfg<MT, BN>::THREADS + (EPI == EPI_STATS4    ?
           if (F4) {
           } else if (X4) {
             const int n_steps = p.K / 64;
-            tma_load_2d_hint(s_b, &tmB, &full_bar[stage], kb * 128, t * BN, pol_b);
+            // the tiled codes: block (128-row tile t, K block kb) is one 16 KB run
+            tma_load_4d_hint(s_b, &tmB, &full_bar[stage], 0, 0, kb, t, pol_b);
             uint8_t* s_sf = s_b + CF::B_STAGE;
             for (int mt = 0; mt < a_tiles; ++mt)
               bulk_load(s_sf + mt * 2048,
@@ -946,7 +947,8 @@ __global__ void __launch_bounds__(SkCfg<MODE>::THREADS, 1)
             const int ns = min(4, n_steps - 4 * kb);
             const bool half1 = (2 * t + 1) * BM < p.N;
             mbar_arrive_expect_tx(&wfull[st], SK_W_BYTES + (half1 ? 2 : 1) * ns * 512);
-            tma_load_2d_hint(dst, &tmW, &wfull[st], kb * 128, t * SK_BN, pol);
+            // the tiled codes: the 16 KB blocks of 128-row tiles 2t and 2t + 1
+            tma_load_4d_hint(dst, &tmW, &wfull[st], 0, 0, kb, 2 * t, pol);
             for (int h = 0; h < (half1 ? 2 : 1); ++h)
               bulk_load(dst + SK_W_BYTES + h * 2048,
                         p.sf4 + ((long long)(2 * t + h) * n_steps + 4 * kb) * 512, ns * 512,
@@ -1694,8 +1696,16 @@ cudaError_t run_stats_nvfp4_mma(const uint16_t* h, int M, const uint8_t* codes, 
   CUtensorMap ta, tb;
   if (!dgi::make_tmap_u8_2d(&ta, rc, D / 2, Mp, D / 2, 128, skinny ? SK_N : BM))
     return cudaErrorInvalidValue;
-  if (!dgi::make_tmap_u8_2d(&tb, codes, D / 2, V, D / 2, 128, skinny ? SK_BN : X4_BN))
-    return cudaErrorInvalidValue;
+  {
+    // tiled codes [ceil(V/128)][ceil(D/256)][128 rows][128 bytes]; a box is one
+    // 128-row block (the GEMM form) or two consecutive tiles' blocks (skinny)
+    const int nkb = (D / 64 + 3) / 4;
+    const uint64_t tiles = (uint64_t)(V + 127) / 128;
+    const uint64_t dims[4] = {128, 128, (uint64_t)nkb, tiles};
+    const uint64_t str[3] = {128, 128 * 128, (uint64_t)nkb * 128 * 128};
+    const uint32_t box[4] = {128, 128, 1, skinny ? SK_BN / 128u : X4_BN / 128u};
+    if (!dgi::make_tmap_u8_4d(&tb, codes, dims, str, box)) return cudaErrorInvalidValue;
+  }
   if ((e = gather_prepare(gather, M, st)) != cudaSuccess) return e;
   GemmParams p{};
   p.M = M;

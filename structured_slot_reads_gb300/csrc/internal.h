@@ -34,6 +34,10 @@ bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint6
 // 2-D tensor map of 8-bit elements (e4m3 operands), 128-byte swizzle.
 bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                      uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+// 4-D tensor map of 8-bit elements (dims innermost first; strides of dims 1..3 in
+// bytes), 128-byte swizzle.
+bool make_tmap_u8_4d(CUtensorMap* map, const void* base, const uint64_t (&dims)[4],
+                     const uint64_t (&stride_bytes)[3], const uint32_t (&box)[4]);
 // 3-D tensor map (dims innermost first; strides of dims 1 and 2 in bytes), 128-byte swizzle.
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, const uint64_t (&dims)[3],
                        const uint64_t (&stride_bytes)[2], const uint32_t (&box)[3]);

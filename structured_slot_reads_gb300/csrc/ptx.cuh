@@ -130,6 +130,17 @@ __device__ __forceinline__ void tma_load_3d_hint(void* smem_dst, const void* tma
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d_hint(void* smem_dst, const void* tmap, uint64_t* bar,
+                                                 int32_t x, int32_t y, int32_t z, int32_t w,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(w),
+      "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 // Plain (non-tensor) bulk copy of `bytes` contiguous bytes global -> shared,
 // completing on `bar`; both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,

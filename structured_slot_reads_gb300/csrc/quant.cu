@@ -305,24 +305,32 @@ __device__ __forceinline__ long long nvfp4_atom_offset(int v, int ks, int nks) {
   return ((long long)(v >> 7) * nks + ks) * 512 + (v & 31) * 16 + ((v >> 5) & 3) * 4;
 }
 
+// Byte offset of the 32 code bytes of row v, 64-value step ks in the tiled codes:
+// 16 KB blocks [ceil(rows/128)][nkb][128 rows][128 bytes], nkb = ceil(cols/256).
+__device__ __forceinline__ long long nvfp4_code_offset(int v, int ks, int nkb) {
+  return (((long long)(v >> 7) * nkb + (ks >> 2)) * 128 + (v & 127)) * 128 + (ks & 3) * 32;
+}
+
+// One thread per (row, 64-value step) of the padded rows x steps, so that the
+// padding rows and the steps past cols in the last 256-value block get zero codes.
 __global__ void quantize_nvfp4_mma_kernel(const __nv_bfloat16* x, int rows, int cols,
                                           const unsigned int* amax_bits, uint8_t* codes,
                                           uint8_t* sf) {
   const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const int nks = cols / 64;
+  const int nkb = (nks + 3) / 4;
   const int rows_pad = (rows + 127) & ~127;
-  if (t >= (long long)rows_pad * nks) return;
+  if (t >= (long long)rows_pad * nkb * 4) return;
   const int ks = (int)(t / rows_pad);
   const int v = (int)(t % rows_pad);
   uint32_t sc4 = 0;
-  if (v < rows) {
-    uint32_t cw[8];
+  uint32_t cw[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if (v < rows && ks < nks)
     sc4 = nvfp4_quant64(x + (long long)v * cols + ks * 64, nvfp4_tensor_scale(*amax_bits), cw);
-    uint4* cdst = reinterpret_cast<uint4*>(codes + (long long)v * (cols / 2) + ks * 32);
-    cdst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-    cdst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-  }
-  *reinterpret_cast<uint32_t*>(sf + nvfp4_atom_offset(v, ks, nks)) = sc4;
+  uint4* cdst = reinterpret_cast<uint4*>(codes + nvfp4_code_offset(v, ks, nkb));
+  cdst[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+  cdst[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+  if (ks < nks) *reinterpret_cast<uint32_t*>(sf + nvfp4_atom_offset(v, ks, nks)) = sc4;
 }
 
 // The rows of a block-scaled pass (at most 16): one thread per (row slot, block of
@@ -477,7 +485,7 @@ cudaError_t quantize_nvfp4_mma(const uint16_t* x, int rows, int cols, uint8_t* c
   const long long n8 = (long long)rows * cols / 8;
   tensor_amax_kernel<<<(int)std::min<long long>((n8 + 255) / 256, 4096), 256, 0, st>>>(
       reinterpret_cast<const uint4*>(x), n8, amax);
-  const long long items = (long long)((rows + 127) & ~127) * (cols / 64);
+  const long long items = (long long)((rows + 127) & ~127) * ((cols / 64 + 3) / 4 * 4);
   quantize_nvfp4_mma_kernel<<<(int)((items + 127) / 128), 128, 0, st>>>(
       reinterpret_cast<const __nv_bfloat16*>(x), rows, cols, amax, codes, sf);
   nvfp4_scale_kernel<<<1, 1, 0, st>>>(g);

@@ -74,6 +74,7 @@ _SIGS = {
     "dg_lmhead_logsoftmax_entropy_nvfp4": [DP, P, I, P, P, P, P, P, P, P, I, P, P, P, P, P, P,
                                            Z, P],
     "dg_quantize_nvfp4_mma": [P, I, I, P, P, P, P],
+    "dg_nvfp4_mma_codes_bytes": [I, I],
     "dg_lmhead_logsoftmax_entropy_nvfp4_mma": [DP, P, I, P, P, P, P, P, P, P, I, P, P, P, P, P,
                                                P, Z, P],
     "dg_commit": [DP, P, P, P, P, P, P, P, P, P, P],
@@ -96,7 +97,7 @@ _SIGS = {
     "dg_num_sms": [],
 }
 _RES = {"dg_workspace_bytes": Z, "dg_strerror": ctypes.c_char_p, "dg_probs_ld": Z,
-        "dg_heads_weights_bytes": Z}
+        "dg_heads_weights_bytes": Z, "dg_nvfp4_mma_codes_bytes": Z}
 
 
 def lib():
@@ -264,6 +265,10 @@ def dg_lmhead_logsoftmax_entropy_nvfp4(dims, h, M, codes, scales, g, inv_t, slot
                                                     _p(entropy), _p(maxz), _p(argmax),
                                                     _p(label_lp), _p(workspace),
                                                     _nbytes(workspace), _s(stream))
+
+
+def dg_nvfp4_mma_codes_bytes(rows, cols):
+    return lib().dg_nvfp4_mma_codes_bytes(rows, cols)
 
 
 def dg_quantize_nvfp4_mma(x, rows, cols, codes, sf, g, stream=None):

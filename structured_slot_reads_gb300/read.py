@@ -264,7 +264,8 @@ class ReadStep:
             if self.L != dg.MAX_LABELS:
                 raise ValueError("the NVFP4 read takes slots of at most 26 labels")
             V = shape.V
-            self.codes = torch.empty((V, D // 2), dtype=u8, device=device)
+            self.codes = torch.empty((dg.dg_nvfp4_mma_codes_bytes(V, D),), dtype=u8,
+                                     device=device)
             self.sf = torch.empty(((V + 127) // 128, D // 64, 512), dtype=u8, device=device)
             self.g = torch.empty(1, dtype=f32, device=device)
             dg._check(dg.dg_quantize_nvfp4_mma(w, V, D, self.codes, self.sf, self.g),
@@ -396,7 +397,8 @@ class LmHead:
         self.w = w
         if fp4_mma:
             D, V = shape.D, shape.V
-            self.codes = torch.empty((V, D // 2), dtype=u8, device=device)
+            self.codes = torch.empty((dg.dg_nvfp4_mma_codes_bytes(V, D),), dtype=u8,
+                                     device=device)
             self.sf = torch.empty(((V + 127) // 128, D // 64, 512), dtype=u8, device=device)
             self.g = torch.empty(1, dtype=f32, device=device)
             dg._check(dg.dg_quantize_nvfp4_mma(w, V, D, self.codes, self.sf, self.g),

@@ -22,7 +22,7 @@ L = 26
 
 
 def _quantize(wd, V, D):
-    codes = torch.empty((V, D // 2), dtype=torch.uint8, device="cuda")
+    codes = torch.empty(dg.dg_nvfp4_mma_codes_bytes(V, D), dtype=torch.uint8, device="cuda")
     sf = torch.empty(((V + 127) // 128, D // 64, 512), dtype=torch.uint8, device="cuda")
     g = torch.empty(1, dtype=torch.float32, device="cuda")
     assert dg.dg_quantize_nvfp4_mma(wd, V, D, codes, sf, g) == dg.DG_OK
@@ -59,7 +59,7 @@ def _dequantized(x):
     return oracle.dequantize_nvfp4(c, s, g)
 
 
-@pytest.mark.parametrize("V,D", [(1000, 256), (4096, 128), (300, 2816), (130, 192)])
+@pytest.mark.parametrize("V,D", [(1000, 256), (4096, 128), (300, 2816), (130, 192), (257, 320)])
 def test_quantizer_mma_layout_bit_exact(V, D):
     w = inputs.normal_bf16((V, D), 1.0 / np.sqrt(D), 5 + V, 1)
     w[3, 64:80] = 0.0                         # a zero block
@@ -70,7 +70,7 @@ def test_quantizer_mma_layout_bit_exact(V, D):
     oc, osc, og = oracle.quantize_nvfp4(w)
     packed, atoms = oracle.to_mma_layout(oc, osc)
     assert host(g)[0] == og
-    assert np.array_equal(host(codes), packed)
+    assert np.array_equal(host(codes), packed.reshape(-1))
     assert np.array_equal(host(sf), atoms)
 
 
@@ -139,7 +139,8 @@ def test_nvfp4_mma_full_vocabulary(M):
     sl = slice(1024, 1280)
     oc, osc, _ = oracle.quantize_nvfp4(w[sl], g=gh)
     packed, atoms = oracle.to_mma_layout(oc, osc)
-    assert np.array_equal(host(codes[sl]), packed)
+    blocks = codes.view(V // 128, -1)    # one row of blocks per 128-row tile
+    assert np.array_equal(host(blocks[8:10]), packed.reshape(2, -1))
     assert np.array_equal(host(sf[8:10]), atoms)
     oc_all, osc_all = oracle.from_mma_layout(host(codes), host(sf), V)
     wq = oracle.dequantize_nvfp4(oc_all, osc_all, gh)

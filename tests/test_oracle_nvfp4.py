@@ -100,17 +100,25 @@ def test_values_on_the_grid_quantise_exactly():
 
 
 def test_mma_layout_places_each_scale_by_its_definition():
-    """The scale atoms of the block-scaled layout: row 32 j + l of a 128-row tile,
-    64-value step k, block q of the step at atom [tile][k], byte 16 l + 4 j + q;
-    codes two a byte, the even element low; rows past R scale 0 (checked byte by
-    byte against that definition, then the inverse)."""
-    R, K = 130, 192
+    """The block-scaled layout.  Scale atoms: row 32 j + l of a 128-row tile, 64-value
+    step k, block q of the step at atom [tile][k], byte 16 l + 4 j + q; rows past R
+    scale 0.  Codes two a byte, the even element low, in 128 x 128-byte blocks per
+    (128-row tile, 256-value K block): element k of row r in byte (k % 256) // 2 of
+    row r % 128 of block (r // 128, k // 256), zero past R and past K.  Checked
+    byte by byte against that definition (a ragged last K block: K = 320), then
+    the inverse."""
+    R, K = 130, 320
     rng = np.random.default_rng(3)
     codes = rng.integers(0, 16, (R, K), dtype=np.uint8)
     scales = rng.integers(0, 256, (R, K // 16), dtype=np.uint8)
     packed, atoms = nvfp4.to_mma_layout(codes, scales)
-    assert packed.shape == (R, K // 2) and atoms.shape == (2, 3, 512)
-    assert packed[5, 7] == codes[5, 14] | (codes[5, 15] << 4)
+    assert packed.shape == (2, 2, 128, 128) and atoms.shape == (2, 5, 512)
+    for r in range(R):
+        for k in range(0, K, 2):
+            byte = packed[r // 128, k // 256, r % 128, (k % 256) // 2]
+            assert byte == codes[r, k] | (codes[r, k + 1] << 4)
+    assert packed[1, :, 2:, :].sum() == 0              # rows 130..255
+    assert packed[:, 1, :, 32:].sum() == 0             # values 320..511 of block 1
     for r in range(R):
         t, rr = divmod(r, 128)
         j, l = divmod(rr, 32)
