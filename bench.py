@@ -61,9 +61,10 @@ WORKLOADS = {
     "sweep_step_b1": ("step", "FULL_CANVAS", dict(B=1, P=8192)),
     "sweep_step_b8": ("step", "FULL_CANVAS", dict(B=8, P=8192)),
     "sweep_step_b64": ("step", "FULL_CANVAS", dict(B=64, P=8192)),
-    # the full-canvas step with a 65536-entry vocabulary (W 369 MB, still past
-    # L2): the small case for whole-kernel profiler captures of the step
+    # the full-canvas step and the single read with a 65536-entry vocabulary (W
+    # 369 MB, still past L2): the small cases for whole-kernel profiler captures
     "step_v65536": ("step", "FULL_CANVAS", dict(V=65536)),
+    "single_read_v65536": ("read", "SINGLE_READ", dict(V=65536)),
 }
 
 
