@@ -717,10 +717,13 @@ def workload_arm(args, rank, world, local):
         decisions = getattr(st, "S", 0)
     kernels, best = {}, None
     n_calls = {"dg_slot_noise": 2, "dg_slot_finish": 2} if kind == "two_stage" else {}
-    # e4m3 contractions against their own peak: the measured bf16 figure times the
-    # nominal e4m3 / bf16 ratio (4.5 / 2.25 PFLOP/s dense)
+    # 8- and 4-bit contractions against their own peak: the measured bf16 figure
+    # times the nominal ratio (dense: e4m3 4.5, NVFP4 13.5 against bf16 2.25
+    # PFLOP/s); the widened NVFP4 pass multiplies in bf16 / f16 and keeps bf16's
     e4m3 = ("dg_lmhead_logsoftmax_entropy_fp8", "dg_selfcond_from_probs8")
-    tpeak = lambda n: pk["bf16_sus"] * (2.0 if n in e4m3 else 1.0)   # noqa: E731
+    nvf4 = ("dg_lmhead_logsoftmax_entropy_nvfp4_mma",)
+    ratio = lambda n: 2.0 if n in e4m3 else 6.0 if n in nvf4 else 1.0   # noqa: E731
+    tpeak = lambda n: pk["bf16_sus"] * ratio(n)   # noqa: E731
     for n, t in per_call.items():
         b, f = work.get(n, (0.0, 0.0))
         kernels[n] = {"ms": round(t, 4), "bytes": b, "flops": f}
@@ -745,7 +748,9 @@ def workload_arm(args, rank, world, local):
                 "peak": peak, "unit": unit, "frac": round(ach / peak, 4), "traffic": None,
                 "kernel": n, "peak_source": pk["source"] + (
                     " (bf16 sustained x 2, the nominal e4m3 ratio)"
-                    if tensor_bound and n in e4m3 else "")}
+                    if tensor_bound and n in e4m3 else
+                    " (bf16 sustained x 6, the nominal NVFP4 ratio)"
+                    if tensor_bound and n in nvf4 else "")}
     if kind == "step":
         unit, value = UNIT, steps_per_s * shape.B
     elif kind == "prefill":
