@@ -483,8 +483,12 @@ class HostPipeline:
         s.wait_stream(self.down)
 
     def sync(self):
+        """Wait for every enqueued step and transfer, then read the device status
+        word (DenoiseStep.check): raises dg.DgDeviceError if a kernel of these
+        steps recorded an error (a wait that timed out, a bad label or page)."""
         self.join()
         torch.cuda.current_stream().synchronize()
+        return self.step.check(torch.cuda.current_stream())
 
 
 def _copy_set(dst, src):

@@ -62,7 +62,7 @@ def test_pipeline_matches_serial_steps(use_graphs):
     for i, (ins, outs) in enumerate(bufs):
         h2d, d2h = pipe.submit(i, ins, outs)
         total += h2d
-    pipe.sync()
+    assert pipe.sync() == 0     # the device status word read after the steps is clean
     # one arena copy per step: every input tensor plus the alignment gaps
     assert total == 3 * bufs[0][0].arena.numel()
     assert bufs[0][0].arena.numel() >= sum(t.numel() * t.element_size() for t in bufs[0][0].values())
