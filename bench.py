@@ -50,6 +50,8 @@ WORKLOADS = {
     "lmhead_nvfp4_m12": ("lmhead_fp4", "FULL_CANVAS", dict(C=12)),
     "lmhead_nvfp4_mma_m12": ("lmhead_fp4mma", "FULL_CANVAS", dict(C=12)),
     "lmhead_nvfp4_mma_m256": ("lmhead_fp4mma", "FULL_CANVAS", {}),
+    "heads_bf16_m256": ("heads", "FULL_CANVAS", {}),
+    "heads_fp8_m256": ("heads_fp8", "FULL_CANVAS", {}),
     "selfcond_bf16_m256": ("selfcond", "FULL_CANVAS", {}),
     "selfcond_fp8_m256": ("selfcond_fp8", "FULL_CANVAS", {}),
     "mixed_decode8_prefill2": ("mixed", "LONG_CONTEXT", dict(B=10, C=2048, P=4096)),
@@ -529,6 +531,18 @@ def build_runner(kind, shape, device, concurrent=True):
         st.inv_t.copy_(1.0 / inputs.device_uniform(st.inv_t.shape, 0.5, 2.0, 4, device))
         torch.cuda.synchronize()
         return st
+    if kind in ("heads", "heads_fp8"):
+        # the fused pass alone: 256 canvas rows and the 12 draw rows of three slots
+        from structured_slot_reads_gb300.read import Heads
+        w = inputs.device_normal_bf16((shape.V, shape.D), shape.D ** -0.5, 1, device)
+        nd = len(shape.slots) * shape.R
+        st = Heads(shape, w, shape.B * shape.C, nd, fp8=kind == "heads_fp8", device=device)
+        st.h.copy_(inputs.device_normal_bf16(st.h.shape, 1.0, 3, device))
+        st.draw_rows.copy_(inputs.device_normal_bf16(st.draw_rows.shape, 1.0, 5, device))
+        st.inv_t.copy_(1.0 / inputs.device_uniform(st.inv_t.shape, 0.5, 2.0, 4, device))
+        st.inv_t_draw.copy_(1.0 / inputs.device_uniform(st.inv_t_draw.shape, 0.5, 2.0, 6, device))
+        torch.cuda.synchronize()
+        return st
     if kind in ("selfcond", "selfcond_fp8"):
         from structured_slot_reads_gb300.read import SelfCond
         e = inputs.device_normal_bf16((shape.V, shape.D), shape.D ** -0.5, 2, device)
@@ -651,6 +665,9 @@ def workload_arm(args, rank, world, local):
     elif kind in ("selfcond", "selfcond_fp8"):
         run = lambda i: st.run(step_idx=i)              # noqa: E731
         calls = ["dg_selfcond_from_probs", "dg_quantize_rows_e4m3", "dg_selfcond_from_probs8"]
+    elif kind in ("heads", "heads_fp8"):
+        run = lambda i: st.run(step_idx=i)              # noqa: E731
+        calls = ["dg_denoise_heads", "dg_quantize_rows_e4m3", "dg_denoise_heads_fp8"]
     else:
         run = lambda i: st.run(step_idx=i)              # noqa: E731
         calls = ["dg_attn_decode", "dg_slot_read", "dg_slot_read_wide", "dg_slot_noise",
@@ -697,6 +714,14 @@ def workload_arm(args, rank, world, local):
         work["dg_selfcond_from_probs"] = (V * D * 2 + Mr * V * 2 + Mr * D * 4, pe)
         work["dg_quantize_rows_e4m3"] = (Mr * V * 3 + Mr * 4, 0.0)
         work["dg_selfcond_from_probs8"] = (V * D + D * 4 + Mr * V + Mr * D * 4, pe)
+    if kind in ("heads", "heads_fp8"):
+        # algorithmic bytes: W (bf16, or e4m3 and its row scales) and the rows;
+        # the probabilities this design writes are not counted
+        Mr, nd = st.M, st.n_draw
+        fl = 2.0 * (Mr + nd) * V * D
+        work["dg_denoise_heads"] = (Wb + (Mr + nd) * D * 2 + Mr * 16, fl)
+        work["dg_denoise_heads_fp8"] = (V * D + V * 4 + (Mr + nd) * (D + 4) + Mr * 16, fl)
+        work["dg_quantize_rows_e4m3"] = ((Mr + nd) * D * 3 + (Mr + nd) * 4, 0.0)
     if kind == "read":
         work["dg_slot_read"] = (Wb + st.S * R * D * 4, 2.0 * st.S * R * V * D)
         work["dg_slot_read_wide"] = work["dg_slot_read"]
@@ -720,7 +745,7 @@ def workload_arm(args, rank, world, local):
     # 8- and 4-bit contractions against their own peak: the measured bf16 figure
     # times the nominal ratio (dense: e4m3 4.5, NVFP4 13.5 against bf16 2.25
     # PFLOP/s); the widened NVFP4 pass multiplies in bf16 / f16 and keeps bf16's
-    e4m3 = ("dg_lmhead_logsoftmax_entropy_fp8", "dg_selfcond_from_probs8")
+    e4m3 = ("dg_lmhead_logsoftmax_entropy_fp8", "dg_selfcond_from_probs8", "dg_denoise_heads_fp8")
     nvf4 = ("dg_lmhead_logsoftmax_entropy_nvfp4_mma",)
     ratio = lambda n: 2.0 if n in e4m3 else 6.0 if n in nvf4 else 1.0   # noqa: E731
     tpeak = lambda n: pk["bf16_sus"] * ratio(n)   # noqa: E731
@@ -761,6 +786,8 @@ def workload_arm(args, rank, world, local):
         unit, value = "lm-head passes/s", steps_per_s
     elif kind in ("selfcond", "selfcond_fp8"):
         unit, value = "self-conditioning passes/s", steps_per_s
+    elif kind in ("heads", "heads_fp8"):
+        unit, value = "fused heads passes/s", steps_per_s
     else:
         unit, value = "slot decisions/s", steps_per_s * decisions
     return {
@@ -782,6 +809,8 @@ def workload_arm(args, rank, world, local):
                           "every pass" if kind.startswith("selfcond") else
                           "inputs larger than L2: NVFP4 W (0.42 GB) streamed every step"
                           if kind in ("lmhead_fp4", "lmhead_fp4mma", "read_fp4") else
+                          "inputs larger than L2: e4m3 W (0.74 GB) streamed every pass"
+                          if kind == "heads_fp8" else
                           "inputs larger than L2: W (1.48 GB) streamed every step"),
                    "launch": ("eager; " + ("slot finish, commit and attention on a side "
                                            "stream beside the self-conditioning GEMM"

@@ -493,6 +493,28 @@ int dg_denoise_heads(const dg_dims* dims, const uint16_t* h, int M,
                      size_t probs_ld, void* workspace, size_t workspace_bytes,
                      void* stream);
 
+/* The fused pass on e4m3 operands (tau-home.com, "Running NVFP4 locally with a
+ * Jev-compatible System One endpoint"; 24-ai.news, "Measured performance": the
+ * FP8 checkpoint): the canvas rows, the draw rows and W each quantised to e4m3
+ * with one fp32 scale per row (dg_quantize_rows_e4m3), and
+ * z_iv = (sum_k h8_ik w8_vk) h_scale_i w_scale_v, likewise for the draw rows
+ * with draw_scale.  Everything else (statistics, draw-row normalisers, label
+ * gather, probabilities, the exactness range, workspace DG_WS_HEADS) as
+ * dg_denoise_heads, on those logits: the statistics of the dequantised
+ * operands.  The per-row reference comes from the dequantised first eight W
+ * rows.  d_model a multiple of 16 (else DG_ERR_SHAPE).
+ *   h8 [M, d_model], draw8 [n_draw, d_model], w8 [V, d_model] e4m3 bytes
+ *   (16-byte aligned); h_scale [M], draw_scale [n_draw], w_scale [V] fp32
+ *   (w_scale 16-byte aligned); the rest as dg_denoise_heads. */
+int dg_denoise_heads_fp8(const dg_dims* dims, const uint8_t* h8, const float* h_scale,
+                         int M, const uint8_t* draw8, const float* draw_scale, int n_draw,
+                         const uint8_t* w8, const float* w_scale, const float* inv_t,
+                         const float* inv_t_draw, float* lse, float* entropy, float* maxz,
+                         int32_t* argmax, float* lse_draw, const int32_t* draw_label_ids,
+                         const int32_t* draw_n_labels, int draw_R, float* draw_label_z,
+                         float* prob_scale, uint16_t* probs, size_t probs_ld, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
 /* W in the tiled layout dg_denoise_heads streams (a layout of the lm-head
  * weights of tau-home.com, "Refusing JSON token generation", no arithmetic):
  * tiles of 224 vocabulary rows, each cut into blocks of 64 columns, block

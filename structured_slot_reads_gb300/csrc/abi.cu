@@ -406,6 +406,43 @@ int dg_denoise_heads(const dg_dims* d, const uint16_t* h, int M, const uint16_t*
                                           static_cast<cudaStream_t>(stream), &g));
 }
 
+int dg_denoise_heads_fp8(const dg_dims* d, const uint8_t* h8, const float* h_scale, int M,
+                         const uint8_t* draw8, const float* draw_scale, int n_draw,
+                         const uint8_t* w8, const float* w_scale, const float* inv_t,
+                         const float* inv_t_draw, float* lse, float* entropy, float* maxz,
+                         int32_t* argmax, float* lse_draw, const int32_t* draw_label_ids,
+                         const int32_t* draw_n_labels, int draw_R, float* draw_label_z,
+                         float* prob_scale, uint16_t* probs, size_t probs_ld, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  if (!d || M < 1 || n_draw < 0 || n_draw > 16) return DG_ERR_ARG;
+  if (!dims_lm(d) || d->d_model % 16) return DG_ERR_SHAPE;
+  if (!h8 || !h_scale || !w8 || !w_scale || !inv_t || !lse || !entropy || !maxz || !argmax ||
+      !prob_scale)
+    return DG_ERR_ARG;
+  if (n_draw > 0 && (!draw8 || !draw_scale || !inv_t_draw || !lse_draw)) return DG_ERR_ARG;
+  if (!aligned(h8, 16) || !aligned(w8, 16) || !aligned(w_scale, 16) ||
+      (n_draw > 0 && !aligned(draw8, 16)))
+    return DG_ERR_ARG;
+  if (probs && (probs_ld < (size_t)d->V || probs_ld % 64 || !aligned(probs, 32)))
+    return DG_ERR_ARG;
+  dgi::LabelGather g{};
+  if (draw_label_z && n_draw > 0) {
+    if (!draw_label_ids || !draw_n_labels || draw_R < 1 || n_draw % draw_R) return DG_ERR_ARG;
+    g.label_ids = draw_label_ids;
+    g.n_labels = draw_n_labels;
+    g.out = draw_label_z;
+    g.L = DG_MAX_LABELS;
+    g.S = n_draw / draw_R;
+    g.R = draw_R;
+  }
+  const size_t need = dg_workspace_bytes(d, DG_WS_HEADS, M);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return DG_ERR_WORKSPACE;
+  return launch_result(dgi::denoise_heads_fp8(
+      h8, h_scale, M, draw8, draw_scale, n_draw, w8, w_scale, d->V, d->d_model, inv_t, inv_t_draw,
+      dgi::RowStats{lse, entropy, maxz, argmax}, lse_draw, prob_scale, probs, probs_ld, workspace,
+      static_cast<cudaStream_t>(stream), &g));
+}
+
 int dg_selfcond_from_probs(const dg_dims* d, const uint16_t* probs, size_t probs_ld,
                            const float* prob_scale, int M, const uint16_t* e, float* out,
                            void* workspace, size_t workspace_bytes, void* stream) {

@@ -40,6 +40,7 @@
 // the two layouts on GB300 measured 6.63 TB/s tiled against 6.12 TB/s row-major.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -88,6 +89,10 @@ struct HeadsParams {
   dgi::LabelGather gl;      // draws' label logits z/T (R > 0 form; gl.out null: none)
   int* status;
   int w_nkb;                // W from its tiled copy (K blocks per tile), 0: row-major W
+  // e4m3 operands (the 8-bit pass): the scale of each canvas row, W row and draw row
+  const float* h_scale;
+  const float* w_scale;
+  const float* d_scale;
 };
 
 // Reference of each canvas row: max over the first REF_N vocabulary entries of
@@ -140,6 +145,46 @@ __global__ void __launch_bounds__(REF_N * REF_KSPLIT * 32)
   }
 }
 
+// The reference of the e4m3 pass: the same definition on the dequantised
+// operands, max over the first REF_N entries of (h8 . w8_v) h_scale w_scale_v / T.
+// One CTA per row, warp e takes entry e; each lane reads 16 codes at a time.
+__device__ __forceinline__ float e4m3_to_float(uint32_t byte) {
+  return __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)byte, __NV_E4M3)));
+}
+
+__global__ void __launch_bounds__(REF_N * 32)
+    ref8_kernel(const uint8_t* h8, const float* h_scale, const uint8_t* w8, const float* w_scale,
+                const float* inv_t, int V, int D, float* ref) {
+  const int e = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x;
+  __shared__ float part[REF_N];
+  float acc = 0.f;
+  if (e < V) {
+    const uint4* x = reinterpret_cast<const uint4*>(h8 + (long long)row * D);
+    const uint4* y = reinterpret_cast<const uint4*>(w8 + (long long)e * D);
+    for (int i = lane; i < D / 16; i += 32) {
+      const uint4 a = __ldg(x + i), b = __ldg(y + i);
+      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          acc = fmaf(e4m3_to_float((av[q] >> (8 * k)) & 0xFFu),
+                     e4m3_to_float((bv[q] >> (8 * k)) & 0xFFu), acc);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    acc *= __ldg(h_scale + row) * __ldg(w_scale + e);
+  }
+  if (lane == 0) part[e] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m = -INFINITY;
+    for (int k = 0; k < REF_N && k < V; ++k) m = fmaxf(m, part[k]);
+    ref[row] = rintf((m * inv_t[row] * LOG2E + REF_HEADROOM) * 256.f) * (1.f / 256.f);
+  }
+}
+
 // The same reference for many rows (batched canvases): one warp per row reads
 // the row once and takes all REF_N dot products against W's first REF_N rows
 // (which stay in L1), where the kernel above would read each row REF_N times.
@@ -186,8 +231,11 @@ __global__ void __launch_bounds__(256)
   if (lane == 0) ref[row] = rintf((m * inv_t[row] * LOG2E + REF_HEADROOM) * 256.f) * (1.f / 256.f);
 }
 
-template <int MT, int BN, bool DRAWS>
+// F8: e4m3 operands, K blocks of 128 values, so every row of a block is 128
+// bytes as in the bf16 pass and the stage geometry is the same.
+template <int MT, int BN, bool DRAWS, bool F8 = false>
 struct HCfg {
+  static constexpr int KBE = F8 ? 2 * BK : BK;            // values of a K block
   static constexpr int A_BYTES = BM * BK * 2;             // one 128-row canvas tile
   static constexpr int A_STAGE = MT * A_BYTES;
   static constexpr int W_SLOT = BN * BK * 2;
@@ -205,8 +253,9 @@ struct HCfg {
   static constexpr int NS_FIT = (232448 - 1024 - BAR_BYTES) / STAGE_BYTES;
   static constexpr int NSTAGE = NS_FIT > 8 ? 8 : NS_FIT;
   static constexpr int SMEM_BYTES = 1024 + NSTAGE * STAGE_BYTES + BAR_BYTES;
-  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
-  static constexpr uint32_t IDESC_DRAW = idesc_bf16_f32(BM, DRAW_N);
+  static constexpr uint32_t IDESC = F8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN);
+  static constexpr uint32_t IDESC_DRAW =
+      F8 ? idesc_e4m3_f32(BM, DRAW_N) : idesc_bf16_f32(BM, DRAW_N);
   static constexpr int HALF1_ROW = BN - 128;  // the second swapped MMA reads W rows [BN-128, BN)
   static constexpr uint32_t TX = A_STAGE + W_SLOT;
   static_assert(ACC_COLS <= 512, "accumulators exceed tensor memory");
@@ -237,11 +286,11 @@ __device__ __forceinline__ void rescale_probs(__nv_bfloat16* row, int v0, int v1
   }
 }
 
-template <int MT, int BN, bool DRAWS>
-__global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
+template <int MT, int BN, bool DRAWS, bool F8>
+__global__ void __launch_bounds__(HCfg<MT, BN, DRAWS, F8>::THREADS, 1)
     heads_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmD, HeadsParams p) {
-  using CF = HCfg<MT, BN, DRAWS>;
+  using CF = HCfg<MT, BN, DRAWS, F8>;
   constexpr int NSTAGE = CF::NSTAGE;
   constexpr int PRODUCER_WARP = CF::EPI_WARPS;
   constexpr int MMA_WARP = CF::EPI_WARPS + 1;
@@ -292,7 +341,7 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int total_kb = (p.K + BK - 1) / BK;
+  const int total_kb = (p.K + CF::KBE - 1) / CF::KBE;
   const int gm = blockIdx.x / p.cpg;
   const int gn = blockIdx.x % p.cpg;
   const int t_begin = (int)((long long)gn * p.n_tiles / p.cpg);
@@ -318,14 +367,14 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
           mbar_arrive_expect_tx(&full_bar[stage], CF::TX + (draws_here ? CF::D_BYTES : 0));
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt)
-            tma_load_2d_hint(s_a + mt * CF::A_BYTES, &tmA, &full_bar[stage], kb * BK,
+            tma_load_2d_hint(s_a + mt * CF::A_BYTES, &tmA, &full_bar[stage], kb * CF::KBE,
                              m_base + mt * BM, pol_keep);
           if (p.w_nkb)  // tiled copy: block (t, kb) is one contiguous box
             tma_load_3d_hint(s_w, &tmB, &full_bar[stage], 0, 0, t * p.w_nkb + kb, pol_stream);
           else
-            tma_load_2d_hint(s_w, &tmB, &full_bar[stage], kb * BK, t * BN, pol_stream);
+            tma_load_2d_hint(s_w, &tmB, &full_bar[stage], kb * CF::KBE, t * BN, pol_stream);
           if (draws_here)
-            tma_load_2d_hint(s_w + CF::W_SLOT, &tmD, &full_bar[stage], kb * BK, 0, pol_keep);
+            tma_load_2d_hint(s_w + CF::W_SLOT, &tmD, &full_bar[stage], kb * CF::KBE, 0, pol_keep);
           issued_mask |= 1u << stage;
           last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == NSTAGE) {
@@ -364,7 +413,10 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
               const uint64_t adesc = sw128_kmajor_desc(a_addr + mt * CF::A_BYTES + kk * 32);
-              tc_mma_f16(d_base + mt * BN, adesc, bdesc, CF::IDESC, acc_flag);
+              if constexpr (F8)
+                tc_mma_f8(d_base + mt * BN, adesc, bdesc, CF::IDESC, acc_flag);
+              else
+                tc_mma_f16(d_base + mt * BN, adesc, bdesc, CF::IDESC, acc_flag);
             }
             if (DRAWS && draws_here) {
               const uint64_t ddesc = sw128_kmajor_desc(d_addr + kk * 32);
@@ -372,8 +424,12 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
               for (int half = 0; half < 2; ++half) {
                 const uint32_t row0 = half ? CF::HALF1_ROW : 0;
                 const uint64_t wdesc = sw128_kmajor_desc(w_addr + row0 * 128 + kk * 32);
-                tc_mma_f16(d_base + MT * BN + half * DRAW_N, wdesc, ddesc, CF::IDESC_DRAW,
-                           acc_flag);
+                if constexpr (F8)
+                  tc_mma_f8(d_base + MT * BN + half * DRAW_N, wdesc, ddesc, CF::IDESC_DRAW,
+                            acc_flag);
+                else
+                  tc_mma_f16(d_base + MT * BN + half * DRAW_N, wdesc, ddesc, CF::IDESC_DRAW,
+                             acc_flag);
               }
             }
           }
@@ -401,6 +457,7 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
     const bool row_ok = row < p.M;
     const float scale = row_ok ? __ldg(p.inv_t + row) * LOG2E : 0.f;
     const float r_ref = row_ok ? __ldg(p.ref + row) : 0.f;
+    const float rs8 = (F8 && row_ok) ? __ldg(p.h_scale + row) : 1.f;   // e4m3: the row's scale
     float s_run = 0.f, t_run = 0.f, best = -INFINITY;
     float r_cur = r_ref;  // reference of the sums and probabilities: r_ref + whole raises
     int best_idx = 0x7fffffff;
@@ -411,6 +468,7 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
       dm[j] = -INFINITY;
       ds[j] = 0.f;
       dscale[j] = (DRAWS && j < p.n_draw) ? __ldg(p.inv_t_draw + j) * LOG2E : 0.f;
+      if (F8 && DRAWS && j < p.n_draw) dscale[j] *= __ldg(p.d_scale + j);
     }
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     // Label gather of the draw rows: one bit per 32 vocabulary rows of this
@@ -448,6 +506,25 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
         tmem_ld_wait();
         const int n0 = t * BN + c * 32;
         if (!row_ok || n0 >= p.V) continue;
+        if constexpr (F8) {
+          // the logits of e4m3 operands: the sums times the row's and the W rows' scales
+          if (n0 + 32 <= p.V) {
+            const float4* cs4 = reinterpret_cast<const float4*>(p.w_scale + n0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float4 c4 = __ldg(cs4 + q);
+              r[4 * q] = __float_as_uint(__uint_as_float(r[4 * q]) * rs8 * c4.x);
+              r[4 * q + 1] = __float_as_uint(__uint_as_float(r[4 * q + 1]) * rs8 * c4.y);
+              r[4 * q + 2] = __float_as_uint(__uint_as_float(r[4 * q + 2]) * rs8 * c4.z);
+              r[4 * q + 3] = __float_as_uint(__uint_as_float(r[4 * q + 3]) * rs8 * c4.w);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (n0 + j < p.V)
+                r[j] = __float_as_uint(__uint_as_float(r[j]) * rs8 * __ldg(p.w_scale + n0 + j));
+          }
+        }
         float e[32];
         float cmax = -INFINITY;
         const float s_prev = s_run, t_prev = t_run;
@@ -539,11 +616,13 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
           const int vl = (half ? CF::HALF1_ROW : 0) + quarter * 32 + lane;
           const int vocab = t * BN + vl;
           const bool lane_ok = (half == 0 || vl >= 128) && vl < BN && vocab < p.V;
+          // e4m3: this lane's W row scale (the draw rows' scales are in dscale)
+          const float wsv = (F8 && lane_ok) ? __ldg(p.w_scale + vocab) : 1.f;
           if (lane_ok) {
 #pragma unroll
             for (int j = 0; j < DRAW_N; ++j) {
               if (j < p.n_draw) {
-                const float v = __uint_as_float(r[j]) * dscale[j];
+                const float v = __uint_as_float(r[j]) * wsv * dscale[j];
                 const float mn = fmaxf(dm[j], v);
                 ds[j] = ds[j] * ex2(dm[j] - mn) + ex2(v - mn);
                 dm[j] = mn;
@@ -565,6 +644,7 @@ __global__ void __launch_bounds__(HCfg<MT, BN, DRAWS>::THREADS, 1)
                     float z = __uint_as_float(r[0]);
 #pragma unroll
                     for (int q = 1; q < DRAW_N; ++q) z = j == q ? __uint_as_float(r[q]) : z;
+                    if (F8) z *= wsv * __ldg(p.d_scale + j);
                     p.gl.out[(long long)j * p.gl.L + k] = z * __ldg(p.inv_t_draw + j);
                   }
                 }
@@ -760,19 +840,19 @@ __global__ void heads_finalize_kernel(const float* part, int cpg, int M, const f
   }
 }
 
-template <int MT, int BN, bool DRAWS>
+template <int MT, int BN, bool DRAWS, bool F8 = false>
 cudaError_t launch_heads(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
                          const HeadsParams& p, int grid, cudaStream_t st) {
-  using CF = HCfg<MT, BN, DRAWS>;
+  using CF = HCfg<MT, BN, DRAWS, F8>;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(heads_kernel<MT, BN, DRAWS>,
+    cudaError_t e = cudaFuncSetAttribute(heads_kernel<MT, BN, DRAWS, F8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          CF::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  heads_kernel<MT, BN, DRAWS><<<grid, CF::THREADS, CF::SMEM_BYTES, st>>>(ta, tb, td, p);
+  heads_kernel<MT, BN, DRAWS, F8><<<grid, CF::THREADS, CF::SMEM_BYTES, st>>>(ta, tb, td, p);
   return cudaGetLastError();
 }
 
@@ -893,6 +973,70 @@ cudaError_t denoise_heads(const uint16_t* h, int M, const uint16_t* draw_rows, i
   else
     e = (mt == 1) ? launch_heads<1, 256, false>(ta, tb, td, p, grid, st)
                   : launch_heads<2, 256, false>(ta, tb, td, p, grid, st);
+  if (e != cudaSuccess) return e;
+  const int row_blocks = (M + 7) / 8, draw_blocks = (n_draw + 7) / 8;
+  heads_finalize_kernel<<<row_blocks + draw_blocks, 256, 0, st>>>(
+      p.part, p.cpg, M, inv_t, out.lse, out.entropy, out.maxz, out.argmax, prob_scale, p.probs,
+      p.ldp, p.n_tiles, bn, V, p.part_draw, n_draw, lse_draw, row_blocks, p.gl, p.status);
+  return cudaGetLastError();
+}
+
+// The same pass on e4m3 operands (rows, draw rows and W each with one fp32 scale
+// per row): 128-value K blocks through 8-bit tensor maps, kind::f8f6f4 MMAs,
+// the scales applied to the accumulators in the epilogue.
+cudaError_t denoise_heads_fp8(const uint8_t* h8, const float* h_scale, int M,
+                              const uint8_t* d8, const float* d_scale, int n_draw,
+                              const uint8_t* w8, const float* w_scale, int V, int D,
+                              const float* inv_t, const float* inv_t_draw, RowStats out,
+                              float* lse_draw, float* prob_scale, uint16_t* probs,
+                              size_t probs_ld, void* ws, cudaStream_t st,
+                              const LabelGather* gather) {
+  const int mt = heads_mt(M);
+  const int groups = (M + mt * BM - 1) / (mt * BM);
+  const int bn = heads_bn(n_draw);
+  HeadsParams p{};
+  p.M = M;
+  p.n_draw = n_draw;
+  p.V = V;
+  p.K = D;
+  p.cpg = heads_cpg(M, V, n_draw);
+  p.n_tiles = (V + bn - 1) / bn;
+  p.inv_t = inv_t;
+  p.inv_t_draw = inv_t_draw;
+  p.h_scale = h_scale;
+  p.w_scale = w_scale;
+  p.d_scale = d_scale;
+  uint8_t* wp = static_cast<uint8_t*>(ws);
+  p.part = reinterpret_cast<float*>(wp);
+  wp += align_up((size_t)5 * p.cpg * M * 4, 256);
+  p.part_draw = reinterpret_cast<float*>(wp);
+  wp += align_up((size_t)2 * p.cpg * DRAW_N * 4, 256);
+  float* ref = reinterpret_cast<float*>(wp);
+  p.ref = ref;
+  p.probs = reinterpret_cast<__nv_bfloat16*>(probs);
+  p.ldp = (long long)probs_ld;
+  p.status = status_ptr();
+  if (gather && n_draw > 0) p.gl = *gather;
+  CUtensorMap ta, tb, td;
+  // one 128-byte row of a box is one 128-value K block of e4m3
+  if (!make_tmap_u8_2d(&ta, h8, D, M, (uint64_t)D, 128, BM)) return cudaErrorInvalidValue;
+  if (!make_tmap_u8_2d(&tb, w8, D, V, (uint64_t)D, 128, bn)) return cudaErrorInvalidValue;
+  if (n_draw > 0) {
+    if (!make_tmap_u8_2d(&td, d8, D, n_draw, (uint64_t)D, 128, DRAW_N))
+      return cudaErrorInvalidValue;
+  } else {
+    td = tb;  // unused
+  }
+  ref8_kernel<<<M, REF_N * 32, 0, st>>>(h8, h_scale, w8, w_scale, inv_t, V, D, ref);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int grid = groups * p.cpg;
+  if (n_draw > 0)
+    e = (mt == 1) ? launch_heads<1, TILED_ROWS, true, true>(ta, tb, td, p, grid, st)
+                  : launch_heads<2, TILED_ROWS, true, true>(ta, tb, td, p, grid, st);
+  else
+    e = (mt == 1) ? launch_heads<1, 256, false, true>(ta, tb, td, p, grid, st)
+                  : launch_heads<2, 256, false, true>(ta, tb, td, p, grid, st);
   if (e != cudaSuccess) return e;
   const int row_blocks = (M + 7) / 8, draw_blocks = (n_draw + 7) / 8;
   heads_finalize_kernel<<<row_blocks + draw_blocks, 256, 0, st>>>(

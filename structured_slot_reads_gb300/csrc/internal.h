@@ -145,6 +145,16 @@ cudaError_t denoise_heads(const uint16_t* h, int M, const uint16_t* draw_rows, i
                           float* prob_scale, uint16_t* probs, size_t probs_ld, void* ws,
                           cudaStream_t st, const LabelGather* gather = nullptr);
 
+// The fused pass on e4m3 operands (per-row scales h_scale [M], d_scale [n_draw],
+// w_scale [V]); d_model a multiple of 16.
+cudaError_t denoise_heads_fp8(const uint8_t* h8, const float* h_scale, int M,
+                              const uint8_t* d8, const float* d_scale, int n_draw,
+                              const uint8_t* w8, const float* w_scale, int V, int D,
+                              const float* inv_t, const float* inv_t_draw, RowStats out,
+                              float* lse_draw, float* prob_scale, uint16_t* probs,
+                              size_t probs_ld, void* ws, cudaStream_t st,
+                              const LabelGather* gather = nullptr);
+
 // ---- attention (attn.cu) ---------------------------------------------------
 struct AttnArgs {
   int B, C, Pmax, Hq, Hkv, d, W;

@@ -80,6 +80,8 @@ _SIGS = {
     "dg_commit": [DP, P, P, P, P, P, P, P, P, P, P],
     "dg_selfcond_embed": [DP, P, I, P, P, P, P, P, P, Z, P],
     "dg_denoise_heads": [DP, P, I, P, I, P, P, P, P, P, P, P, P, P, P, P, I, P, P, P, Z, P, Z, P],
+    "dg_denoise_heads_fp8": [DP, P, P, I, P, P, I, P, P, P, P, P, P, P, P, P, P, P, I, P, P, P,
+                             Z, P, Z, P],
     "dg_heads_weights_bytes": [DP],
     "dg_heads_weights_tile": [DP, P, P, P],
     "dg_selfcond_from_probs": [DP, P, Z, P, I, P, P, P, Z, P],
@@ -308,6 +310,19 @@ def dg_denoise_heads(dims, h, M, draw_rows, n_draw, w, inv_t, inv_t_draw, lse, e
                                   _p(draw_n_labels), draw_R, _p(draw_label_z), _p(prob_scale),
                                   _p(probs), probs_ld, _p(workspace), _nbytes(workspace),
                                   _s(stream))
+
+
+def dg_denoise_heads_fp8(dims, h8, h_scale, M, draw8, draw_scale, n_draw, w8, w_scale, inv_t,
+                         inv_t_draw, lse, entropy, maxz, argmax, lse_draw, draw_label_ids,
+                         draw_n_labels, draw_R, draw_label_z, prob_scale, probs, probs_ld,
+                         workspace, stream=None):
+    return lib().dg_denoise_heads_fp8(ctypes.byref(dims), _p(h8), _p(h_scale), M, _p(draw8),
+                                      _p(draw_scale), n_draw, _p(w8), _p(w_scale), _p(inv_t),
+                                      _p(inv_t_draw), _p(lse), _p(entropy), _p(maxz),
+                                      _p(argmax), _p(lse_draw), _p(draw_label_ids),
+                                      _p(draw_n_labels), draw_R, _p(draw_label_z),
+                                      _p(prob_scale), _p(probs), probs_ld, _p(workspace),
+                                      _nbytes(workspace), _s(stream))
 
 
 def dg_heads_weights_bytes(dims):

@@ -457,6 +457,75 @@ class LmHead:
         return 3
 
 
+class Heads:
+    """The fused pass of a step alone (statistics of M canvas rows, the normalisers
+    of n_draw draw rows, the bf16 self-conditioning probabilities) on bf16
+    operands (dg_denoise_heads, W streamed from its tiled copy) or on e4m3
+    operands with per-row scales (dg_quantize_rows_e4m3 of the canvas and draw
+    rows, then dg_denoise_heads_fp8); W is tiled or quantised once, when the
+    object is made."""
+
+    def __init__(self, shape, w, M, n_draw, fp8=False, device="cuda"):
+        f32, i32, u8, bf = torch.float32, torch.int32, torch.uint8, torch.bfloat16
+        V, D = shape.V, shape.D
+        self.shape, self.M, self.n_draw, self.fp8 = shape, M, n_draw, fp8
+        self.dims = dg.make_dims(d_model=D, V=V)
+        nd = max(n_draw, 1)
+        self.h = torch.empty((M, D), dtype=bf, device=device)
+        self.draw_rows = torch.empty((nd, D), dtype=bf, device=device)
+        self.inv_t = torch.empty(M, dtype=f32, device=device)
+        self.inv_t_draw = torch.empty(nd, dtype=f32, device=device)
+        self.lse, self.ent, self.maxz, self.prob_scale = (torch.empty(M, dtype=f32, device=device)
+                                                          for _ in range(4))
+        self.argmax = torch.empty(M, dtype=i32, device=device)
+        self.lse_draw = torch.empty(nd, dtype=f32, device=device)
+        self.probs_ld = dg.dg_probs_ld(V)
+        self.probs = torch.empty((M, self.probs_ld), dtype=bf, device=device)
+        self.ws = torch.empty(dg.dg_workspace_bytes(self.dims, dg.DG_WS_HEADS, M), dtype=u8,
+                              device=device)
+        self.w, self.w_tiled = w, None
+        if fp8:
+            self.w8 = torch.empty((V, D), dtype=u8, device=device)
+            self.w_scale = torch.empty(V, dtype=f32, device=device)
+            dg._check(dg.dg_quantize_rows_e4m3(w, V, D, self.w8, self.w_scale),
+                      "dg_quantize_rows_e4m3")
+            self.h8 = torch.empty((M, D), dtype=u8, device=device)
+            self.h_scale = torch.empty(M, dtype=f32, device=device)
+            self.d8 = torch.empty((nd, D), dtype=u8, device=device)
+            self.d_scale = torch.empty(nd, dtype=f32, device=device)
+        elif n_draw and dg.dg_heads_weights_bytes(self.dims):
+            self.w_tiled = torch.empty(dg.dg_heads_weights_bytes(self.dims) // 2, dtype=bf,
+                                       device=device)
+            dg._check(dg.dg_heads_weights_tile(self.dims, w, self.w_tiled),
+                      "dg_heads_weights_tile")
+
+    def run(self, step_idx=0, stream=None):
+        """Enqueue one pass; returns the number of library kernels."""
+        d, nd = self.dims, self.n_draw
+        if not self.fp8:
+            dg._check(dg.dg_denoise_heads(d, self.h, self.M, self.draw_rows if nd else None, nd,
+                                          self.w, self.inv_t, self.inv_t_draw, self.lse,
+                                          self.ent, self.maxz, self.argmax, self.lse_draw,
+                                          None, None, 0, None, self.prob_scale, self.probs,
+                                          self.probs_ld, self.ws, stream, w_tiled=self.w_tiled),
+                      "dg_denoise_heads")
+            return 3
+        D = self.shape.D
+        dg._check(dg.dg_quantize_rows_e4m3(self.h, self.M, D, self.h8, self.h_scale, stream),
+                  "dg_quantize_rows_e4m3")
+        if nd:
+            dg._check(dg.dg_quantize_rows_e4m3(self.draw_rows, nd, D, self.d8, self.d_scale,
+                                               stream), "dg_quantize_rows_e4m3")
+        dg._check(dg.dg_denoise_heads_fp8(d, self.h8, self.h_scale, self.M,
+                                          self.d8 if nd else None, self.d_scale if nd else None,
+                                          nd, self.w8, self.w_scale, self.inv_t, self.inv_t_draw,
+                                          self.lse, self.ent, self.maxz, self.argmax,
+                                          self.lse_draw, None, None, 0, None, self.prob_scale,
+                                          self.probs, self.probs_ld, self.ws, stream),
+                  "dg_denoise_heads_fp8")
+        return 3 + (2 if nd else 1)
+
+
 class SelfCond:
     """The expected-embedding GEMM of self-conditioning from given probabilities
     (dg_denoise_heads' output layout: P~ [M, probs_ld] bf16 and prob_scale = 1/S),

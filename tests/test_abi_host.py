@@ -278,6 +278,25 @@ def test_heads_weights_tiled_copy_validates(lib):
     assert dg.dg_denoise_heads(*args, stream=0) == dg.DG_ERR_WORKSPACE
 
 
+def test_fp8_heads_pass_validates(lib):
+    """dg_denoise_heads_fp8 refuses before any launch: d_model not a multiple of 16,
+    more than 16 draw rows, a W-scale vector not 16-byte aligned, a missing
+    workspace."""
+    d = dg.make_dims(d_model=128, V=1024)
+    ld = dg.dg_probs_ld(1024)
+
+    def call(dims=d, n_draw=0, w_scale=64, ws=None):
+        return dg.dg_denoise_heads_fp8(dims, 64, 64, 4, 64 if n_draw else None,
+                                       64 if n_draw else None, n_draw, 64, w_scale, 64,
+                                       64 if n_draw else None, 64, 64, 64, 64,
+                                       64 if n_draw else None, None, None, 0, None, 64, 64, ld,
+                                       ws, stream=0)
+    assert call(dims=dg.make_dims(d_model=120, V=1024)) == dg.DG_ERR_SHAPE
+    assert call(n_draw=17) == dg.DG_ERR_ARG
+    assert call(w_scale=72) == dg.DG_ERR_ARG          # 8-byte aligned
+    assert call() == dg.DG_ERR_WORKSPACE              # everything else accepted
+
+
 def test_8bit_self_conditioning_validates(lib):
     d = dg.make_dims(d_model=128, V=1024)
     ok = (d, 32, 32, None, 4, 32, 32, 32, None)

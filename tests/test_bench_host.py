@@ -20,7 +20,8 @@ def test_every_workload_resolves_to_a_shape():
         k, shape = b.workload_shape(name)
         assert k == kind in ("step", "read", "read_fp4", "two_stage", "prefill", "lmhead",
                              "lmhead_fp8",
-                             "lmhead_fp4", "lmhead_fp4mma", "mixed", "selfcond", "selfcond_fp8")
+                             "lmhead_fp4", "lmhead_fp4mma", "mixed", "selfcond", "selfcond_fp8",
+                             "heads", "heads_fp8")
         for f, v in kw.items():
             assert getattr(shape, f) == v
     assert b.workload_shape("sweep_read_b64")[1].B == 64
