@@ -932,7 +932,8 @@ def reference_arm(args, rank, budget_s=150.0, shape=None):
                     "d2h_bytes_per_step": 0}}
 
 
-EXTRA_WORKLOADS = ("single_structured_read", "mixed_batched_reads", "long_context_read")
+EXTRA_WORKLOADS = ("single_structured_read", "mixed_batched_reads", "long_context_read",
+                   "single_structured_read_nvfp4")
 
 
 def extra_workloads(args, rank, world, local):
